@@ -1,0 +1,207 @@
+/*
+ * moe.h -- C ABI of a single-GPU mixture-of-experts layer for NVIDIA GB300
+ * (sm_103a): router top-k, device-side schedule, dispatch gather, grouped
+ * expert GEMMs (BF16 or OCP MXFP8) with fused SwiGLU and quantisation,
+ * deterministic combine, an optional BF16 shared expert, and the backward
+ * pass.
+ *
+ * The method is the one described by the "Mixture-of-Kittens" pages (Cursor's
+ * MoE training megakernel): token routing, a device-side schedule kernel with
+ * no CPU synchronisation, dispatch, expert grouped GEMMs with SwiGLU and
+ * activation quantisation fused in, and a bitwise-deterministic combine
+ * ("Mixture-of-Kittens" wiki page, TL;DR, flowchart and Key claims).  The
+ * pages' inter-GPU dispatch/combine become intra-GPU gathers here.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - All pointers are DEVICE pointers unless stated otherwise; the caller owns
+ *   every buffer.  The library allocates nothing and keeps no per-call state.
+ * - Every tensor is row-major and contiguous.  bf16 = IEEE bfloat16 bits.
+ *   Pointers must be 16-byte aligned (MOE_ERR_ALIGN otherwise).
+ * - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *   default stream): no host synchronisation, no device-to-host copy.  Only
+ *   moe_get_status synchronises.
+ * - Return value: MOE_OK (0), or a negative moe_status for errors detected on
+ *   the host before anything is launched.  Errors detected on the device
+ *   (a bounded wait that ran out) are recorded in the status word inside the
+ *   workspace and read with moe_get_status.
+ * - Results are bitwise reproducible: the same inputs give the same bits on
+ *   every call (fixed floating-point operation order, no atomics on floats).
+ *
+ * MXFP8 format (OCP Microscaling v1.0, as the layer's MXFP8 configurations
+ * state): codes are E4M3 bytes; every 32 consecutive elements along the
+ * reduction axis K share one E8M0 scale byte (2**(byte-127)); the shared
+ * exponent is floor(log2(amax)) - 8, clamped to [-127, 127] (an all-zero
+ * block gets byte 0); codes are round-to-nearest-even and saturate to +-448.
+ *
+ * MXFP8 scale layout ("tiled"): a matrix with `rows` rows and reduction
+ * length K (rows and K multiples of 128) has rows*K/32 scale bytes; the
+ * scale of (row r, block b = column/32) is at byte
+ *     ((r / 128) * (K / 128) + b / 4) * 512
+ *       + (r % 32) * 16 + ((r % 128) / 32) * 4 + (b % 4)
+ * i.e. 512-byte atoms covering 128 rows x 4 blocks, in the order the tensor
+ * cores' scale-factor copy reads them.  Batched matrices stack along rows.
+ */
+#ifndef MOE_H
+#define MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *moe_stream_t; /* same type as cudaStream_t */
+
+typedef enum { MOE_BF16 = 0, MOE_MXFP8 = 1 } moe_dtype;
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_ARG = -1,     /* NULL pointer, non-positive size, k > E, unknown name */
+  MOE_ERR_SHAPE = -2,   /* shape outside what the kernels tile (see moe_config) */
+  MOE_ERR_ALIGN = -3,   /* a pointer is not 16-byte aligned */
+  MOE_ERR_CUDA = -4,    /* a CUDA runtime / driver call or a launch failed */
+  MOE_ERR_DEVICE = -5,  /* current device is not sm_103 / sm_100 family */
+  MOE_ERR_TIMEOUT = -6  /* device side: a bounded wait inside a kernel ran out */
+} moe_status;
+
+/* moe_config.flags bits */
+#define MOE_FLAG_BACKWARD 1 /* size the workspace for moe_backward as well */
+
+/*
+ * Layer shape.  T tokens, hidden d, expert intermediate m, E experts, top-k k.
+ * Supported: 1 <= k <= min(E, 16), E <= 1024, d % 256 == 0, m % 128 == 0,
+ * m_shared % 128 == 0 (0 = no shared expert), T*k < 2^31 - 127*E.  dtype is
+ * the routed experts' arithmetic; the shared expert is always BF16.  flags:
+ * MOE_FLAG_BACKWARD or 0 (moe_backward needs a workspace sized with it).
+ */
+typedef struct {
+  int32_t T, d, m, E, k;
+  int32_t m_shared;
+  int32_t dtype; /* moe_dtype */
+  int32_t flags;
+} moe_config;
+
+/*
+ * Expert weights.  BF16 path: `gu` [E, 2m, d] bf16 (rows 0..m-1 of each
+ * expert are the gate projection, m..2m-1 the up projection), `dn` [E, d, m]
+ * bf16; the *_scale pointers are unused.
+ * MXFP8 path: `gu` = E4M3 codes [E*2m, d] with tiled scales `gu_scale`
+ * (rows E*2m, K d); `dn` = codes [E*d, m], `dn_scale` (rows E*d, K m) --
+ * both from moe_quantize_mx(transpose=0) of the bf16 masters.
+ * Backward operands (NULL for a forward-only layer):
+ *   BF16:  gu_t = [E, d, 2m] bf16 = per-expert transpose of gu,
+ *          dn_t = [E, m, d] bf16 = per-expert transpose of dn
+ *          (moe_transpose_bf16);
+ *   MXFP8: gu_t = codes [E*d, 2m] + gu_t_scale, dn_t = codes [E*m, d] +
+ *          dn_t_scale (moe_quantize_mx(transpose=1) of the masters).
+ * Shared expert (BF16 always; NULL when m_shared == 0): s_gu [2m_s, d],
+ * s_dn [d, m_s]; for backward also s_gu_t [d, 2m_s], s_dn_t [m_s, d].
+ */
+typedef struct {
+  const void *gu, *gu_scale;
+  const void *dn, *dn_scale;
+  const void *gu_t, *gu_t_scale;
+  const void *dn_t, *dn_t_scale;
+  const void *s_gu, *s_dn;
+  const void *s_gu_t, *s_dn_t;
+} moe_weights;
+
+/* Bytes of scratch (`ws`) that moe_route / moe_forward / moe_backward need
+ * for this config (one buffer serves all three; 0 on invalid config). */
+size_t moe_workspace_bytes(const moe_config *cfg);
+
+/* Bytes of the activations a training forward saves for the backward
+ * (`saved`; 0 on invalid config). */
+size_t moe_saved_bytes(const moe_config *cfg);
+
+/* Byte offset and size of a named sub-buffer of `saved` (which = 0) or of the
+ * workspace (which = 1), for inspection by tests and tools.  Names: "idx",
+ * "w", "counts", "offsets", "perm", "inv", "poff", "o", "GU", "h", "xs",
+ * "xs_sf", "hq", "hq_sf", "s_out", "s_GU", "s_h", "dO", "dX", "dGU", "g".
+ * Row-indexed buffers use padded rows (see moe_forward).  Returns MOE_OK or
+ * MOE_ERR_ARG (unknown name / buffer absent for this config). */
+int moe_buffer_info(const moe_config *cfg, int which, const char *name, size_t *offset,
+                    size_t *bytes);
+
+/* Number of padded expert-sorted rows the buffers are sized for:
+ * roundup(T*k + 127*E, 128). */
+int64_t moe_padded_rows(const moe_config *cfg);
+
+/*
+ * S0: MXFP8 weight quantisation ("Mixture-of-Kittens" wiki page, Key claims,
+ * MXFP8 bullet: MXFP8 is the default expert format).
+ * src: [batch, rows, cols] bf16.
+ *   transpose = 0: codes [batch*rows, cols], blocks of 32 along cols;
+ *                  scales tiled with rows' = batch*rows, K = cols.
+ *   transpose = 1: codes [batch*cols, rows] = per-batch transpose, blocks of
+ *                  32 along the original rows; scales tiled with
+ *                  rows' = batch*cols, K = rows.
+ * rows and cols must be multiples of 128.  Inputs must be finite.
+ */
+int moe_quantize_mx(const void *src, int batch, int rows, int cols, int transpose, void *codes,
+                    void *scales, moe_stream_t stream);
+
+/* Per-batch transpose of bf16 matrices: src [batch, rows, cols] ->
+ * dst [batch, cols, rows] (rows, cols multiples of 32). */
+int moe_transpose_bf16(const void *src, int batch, int rows, int cols, void *dst,
+                       moe_stream_t stream);
+
+/*
+ * S1 + S2: router top-k and the device-side schedule (daily-ai-frontier
+ * summary, TL;DR: routing fused into the layer; wiki page, flowchart and Key
+ * claims: the device-side schedule kernel never talks to the host).
+ * logits [T, E] fp32 (finite).  Outputs (device, caller-owned):
+ *   idx [T, k] int32: experts ordered by (logit desc, index asc), first k;
+ *   w [T, k] fp32: softmax over the k chosen logits (= softmax over E
+ *                  renormalised to the chosen k);
+ *   counts [E] int32; offsets [E+1] int32 (exclusive prefix sum);
+ *   perm [T*k] int32: perm[t*k+j] = expert-sorted row of slot (t, j); rows of
+ *                  one expert keep ascending slot order (stable).
+ * Any output pointer may be NULL, in which case that output stays in `ws`.
+ */
+int moe_route(const moe_config *cfg, const float *logits, int32_t *idx, float *w, int32_t *counts,
+              int32_t *offsets, int32_t *perm, void *ws, moe_stream_t stream);
+
+/*
+ * Forward pass: route -> schedule -> dispatch gather (MXFP8: x quantised in
+ * the gather) -> gate/up grouped GEMM with SwiGLU (MXFP8: h quantised in the
+ * epilogue) -> down grouped GEMM -> shared expert -> combine
+ *     y[t] = bf16( sum_{j<k} w[t,j] * o[row(t,j)] + s[t] )   (fixed j order)
+ * x [T, d] bf16; logits [T, E] fp32; y [T, d] bf16 output.
+ * saved: NULL for inference, else moe_saved_bytes() bytes that the backward
+ * reads.  ws: moe_workspace_bytes() bytes.
+ * Expert-sorted rows are padded per expert to multiples of 128: the rows of
+ * expert e occupy [poff[e], poff[e] + counts[e]) with
+ * poff[e] = sum_{e'<e} roundup(counts[e'], 128).
+ */
+int moe_forward(const moe_config *cfg, const void *x, const float *logits, const moe_weights *W,
+                void *y, void *saved, void *ws, moe_stream_t stream);
+
+/*
+ * Backward pass (wiki page, Key claims: reverse-combine, then the expert
+ * GEMMs' dgrad/wgrad, then reverse-dispatch).  Inputs: dy [T, d] bf16, the
+ * forward's x, weights (including the backward operands) and `saved`.
+ * Outputs: dx [T, d] bf16; dlogits [T, E] fp32 (w_j (g_j - sum_i w_i g_i) at
+ * the chosen experts, g_j = <dy_t, o_j>, 0 elsewhere); dW_gu [E, 2m, d] bf16;
+ * dW_dn [E, d, m] bf16 (zero for experts with no rows); dWs_gu [2m_s, d],
+ * dWs_dn [d, m_s] bf16 (shared expert; NULL when absent).
+ */
+int moe_backward(const moe_config *cfg, const void *dy, const void *x, const moe_weights *W,
+                 const void *saved, void *dx, float *dlogits, void *dW_gu, void *dW_dn,
+                 void *dWs_gu, void *dWs_dn, void *ws, moe_stream_t stream);
+
+/* Synchronises `stream`, returns the device status word recorded in `ws`
+ * (MOE_OK or MOE_ERR_TIMEOUT) and clears it.  Returns MOE_ERR_CUDA if the
+ * stream reports a CUDA error. */
+int moe_get_status(void *ws, moe_stream_t stream);
+
+/* Static description of a status code (never NULL). */
+const char *moe_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H */

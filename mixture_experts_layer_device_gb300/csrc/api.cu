@@ -1,0 +1,783 @@
+// Host side of the C ABI declared in include/moe.h: argument checks, the
+// layout of the caller-owned workspace / saved buffers, TMA tensor maps, and
+// the launch sequence of the forward and backward passes.  Nothing here
+// allocates memory or synchronises the host with the device (except
+// moe_get_status, which exists to do exactly that).
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "../../include/moe.h"
+#include "kernels.h"
+
+namespace {
+
+using moe::GemmArgs;
+using moe::RouteBufs;
+
+// ---------------------------------------------------------------- shapes
+struct Dims {
+  int T, d, m, E, k, ms;
+  bool mx, bwd;
+  long R, Rp, Tp;
+  int nchunks;
+};
+
+int check_config(const moe_config *c, Dims *D) {
+  if (!c) return MOE_ERR_ARG;
+  if (c->T <= 0 || c->d <= 0 || c->m <= 0 || c->E <= 0 || c->k <= 0 || c->m_shared < 0)
+    return MOE_ERR_ARG;
+  if (c->k > c->E || c->k > 16 || c->E > 1024) return MOE_ERR_SHAPE;
+  if (c->dtype != MOE_BF16 && c->dtype != MOE_MXFP8) return MOE_ERR_ARG;
+  if ((c->flags & ~MOE_FLAG_BACKWARD) != 0) return MOE_ERR_ARG;
+  if (c->d % 256 || c->m % 128 || c->m_shared % 128) return MOE_ERR_SHAPE;
+  const long R = static_cast<long>(c->T) * c->k;
+  const long Rp = (R + 127L * c->E + 127) / 128 * 128;
+  if (Rp >= (1L << 31)) return MOE_ERR_SHAPE;
+  D->T = c->T;
+  D->d = c->d;
+  D->m = c->m;
+  D->E = c->E;
+  D->k = c->k;
+  D->ms = c->m_shared;
+  D->mx = c->dtype == MOE_MXFP8;
+  D->bwd = (c->flags & MOE_FLAG_BACKWARD) != 0;
+  D->R = R;
+  D->Rp = Rp;
+  D->Tp = (c->T + 127L) / 128 * 128;
+  D->nchunks = static_cast<int>((R + moe::kSchedChunk - 1) / moe::kSchedChunk);
+  return MOE_OK;
+}
+
+// ---------------------------------------------------------------- layouts
+struct Entry {
+  const char *name;
+  size_t off, bytes;
+};
+struct Layout {
+  Entry e[80];
+  int n = 0;
+  size_t total = 0;
+  void add(const char *name, size_t bytes) {
+    if (bytes == 0) return;
+    const size_t off = (total + 255) & ~static_cast<size_t>(255);
+    e[n++] = {name, off, bytes};
+    total = off + bytes;
+  }
+  const Entry *find(const char *name) const {
+    for (int i = 0; i < n; ++i)
+      if (strcmp(e[i].name, name) == 0) return &e[i];
+    return nullptr;
+  }
+  char *ptr(void *base, const char *name) const {
+    const Entry *x = find(name);
+    return x ? static_cast<char *>(base) + x->off : nullptr;
+  }
+};
+
+void add_route(const Dims &D, Layout &L) {
+  L.add("idx", D.R * 4);
+  L.add("w", D.R * 4);
+  L.add("counts", D.E * 4);
+  L.add("offsets", (D.E + 1) * 4);
+  L.add("perm", D.R * 4);
+  L.add("inv", D.R * 4);
+  L.add("poff", (D.E + 1) * 4);
+}
+
+// Activations a training forward keeps for the backward.
+void saved_layout(const Dims &D, Layout &L) {
+  add_route(D, L);
+  L.add("o", D.Rp * D.d * 2);
+  L.add("GU", D.Rp * 2 * D.m * 2);
+  L.add("h", D.Rp * D.m * 2);
+  if (D.ms) {
+    L.add("s_GU", D.Tp * 2 * D.ms * 2);
+    L.add("s_h", D.Tp * D.ms * 2);
+  }
+}
+
+void ws_layout(const Dims &D, Layout &L) {
+  L.add("status", 16);
+  L.add("hist", static_cast<size_t>(D.nchunks) * D.E * 4);
+  add_route(D, L);  // used when the forward saves nothing
+  const size_t eb = D.mx ? 1 : 2;
+  L.add("xs", D.Rp * D.d * eb);
+  if (D.mx) {
+    L.add("xs_sf", D.Rp * D.d / 32);
+    L.add("hq", D.Rp * D.m);
+    L.add("hq_sf", D.Rp * D.m / 32);
+  } else {
+    L.add("h", D.Rp * D.m * 2);
+  }
+  L.add("o", D.Rp * D.d * 2);
+  if (D.ms) {
+    L.add("s_h", D.Tp * D.ms * 2);
+    L.add("s_out", D.Tp * D.d * 2);
+  }
+  if (!D.bwd) return;
+  L.add("g", D.R * 4);
+  L.add("dO", D.Rp * D.d * 2);
+  L.add("dGU", D.Rp * 2 * D.m * 2);
+  L.add("dX", D.Rp * D.d * 2);
+  L.add("dOT", D.d * D.Rp * eb);
+  L.add("hT", D.m * D.Rp * eb);
+  L.add("dGUT", 2 * D.m * D.Rp * eb);
+  L.add("xT", D.d * D.Rp * eb);
+  if (D.mx) {
+    L.add("dOq", D.Rp * D.d);
+    L.add("dOq_sf", D.Rp * D.d / 32);
+    L.add("dGUq", D.Rp * 2 * D.m);
+    L.add("dGUq_sf", D.Rp * 2 * D.m / 32);
+    L.add("dOT_sf", D.d * D.Rp / 32);
+    L.add("hT_sf", D.m * D.Rp / 32);
+    L.add("dGUT_sf", 2 * D.m * D.Rp / 32);
+    L.add("xT_sf", D.d * D.Rp / 32);
+  }
+  if (D.ms) {
+    L.add("s_dGU", D.Tp * 2 * D.ms * 2);
+    L.add("s_dx", D.Tp * D.d * 2);
+    L.add("s_dyT", D.d * D.Tp * 2);
+    L.add("s_hT", D.ms * D.Tp * 2);
+    L.add("s_dGUT", 2 * D.ms * D.Tp * 2);
+    L.add("s_xT", D.d * D.Tp * 2);
+  }
+}
+
+// ---------------------------------------------------------------- device info
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+struct DeviceInfo {
+  bool ok = false;
+  int num_sms = 0;
+};
+std::mutex g_mu;
+EncodeTiledFn g_encode = nullptr;
+DeviceInfo g_dev[64];
+
+int device_info(DeviceInfo *out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_encode) {
+    cudaDriverEntryPointQueryResult q;
+    void *fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+      return MOE_ERR_CUDA;
+    g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  }
+  if (!g_dev[dev].ok) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    if (major != 10 || minor != 3) return MOE_ERR_DEVICE;
+    g_dev[dev].num_sms = sms;
+    g_dev[dev].ok = true;
+  }
+  *out = g_dev[dev];
+  return MOE_OK;
+}
+
+// 2-D K-major tensor map: `rows` rows of `inner` elements (bf16 or 1-byte codes),
+// box 128 rows x 128 bytes, 128-byte swizzle, zero fill out of bounds.
+bool make_map(CUtensorMap *m, const void *base, bool bytes1, uint64_t inner, uint64_t rows) {
+  const uint64_t esz = bytes1 ? 1 : 2;
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {inner * esz};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / esz), 128};
+  cuuint32_t estr[2] = {1, 1};
+  const CUresult r = g_encode(m, bytes1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                              2, const_cast<void *>(base), dims, strides, box, estr,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+// One GEMM launch: A [a_rows, K] and B [b_rows, K] (K-major) plus arguments.
+struct Gemm {
+  bool mx;
+  int bn, epi;
+  const void *a;
+  long a_rows;
+  const void *b;
+  long b_rows;
+  long K;
+  GemmArgs g;
+  long max_tiles;
+};
+
+int run_gemm(const Gemm &q, const DeviceInfo &dev, cudaStream_t s) {
+  CUtensorMap ta, tb;
+  if (!make_map(&ta, q.a, q.mx, q.K, q.a_rows) || !make_map(&tb, q.b, q.mx, q.K, q.b_rows))
+    return MOE_ERR_CUDA;
+  const long grid = q.max_tiles < dev.num_sms ? q.max_tiles : dev.num_sms;
+  return cuda_status(moe::launch_gemm(q.mx, q.bn, q.epi, ta, tb, q.g, static_cast<int>(grid), s));
+}
+
+int bn_for(long n) { return n % 256 == 0 ? 256 : 128; }
+
+struct Ptrs {
+  RouteBufs rb;
+  int *status;
+};
+
+Ptrs route_ptrs(const Layout &L, void *base, void *ws, const Layout &W) {
+  Ptrs p;
+  p.rb.idx = reinterpret_cast<int *>(L.ptr(base, "idx"));
+  p.rb.w = reinterpret_cast<float *>(L.ptr(base, "w"));
+  p.rb.counts = reinterpret_cast<int *>(L.ptr(base, "counts"));
+  p.rb.offsets = reinterpret_cast<int *>(L.ptr(base, "offsets"));
+  p.rb.perm = reinterpret_cast<int *>(L.ptr(base, "perm"));
+  p.rb.inv = reinterpret_cast<int *>(L.ptr(base, "inv"));
+  p.rb.poff = reinterpret_cast<int *>(L.ptr(base, "poff"));
+  p.rb.hist = reinterpret_cast<int *>(W.ptr(ws, "hist"));
+  p.status = reinterpret_cast<int *>(W.ptr(ws, "status"));
+  return p;
+}
+
+GemmArgs base_args(int sched, int E, const int *poff, int *status) {
+  GemmArgs g;
+  memset(&g, 0, sizeof(g));
+  g.sched = sched;
+  g.E = E;
+  g.poff = poff;
+  g.status = status;
+  return g;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t moe_workspace_bytes(const moe_config *cfg) {
+  Dims D;
+  if (check_config(cfg, &D) != MOE_OK) return 0;
+  Layout L;
+  ws_layout(D, L);
+  return L.total;
+}
+
+size_t moe_saved_bytes(const moe_config *cfg) {
+  Dims D;
+  if (check_config(cfg, &D) != MOE_OK) return 0;
+  Layout L;
+  saved_layout(D, L);
+  return L.total;
+}
+
+int moe_buffer_info(const moe_config *cfg, int which, const char *name, size_t *offset,
+                    size_t *bytes) {
+  Dims D;
+  const int rc = check_config(cfg, &D);
+  if (rc != MOE_OK) return rc;
+  if (!name || !offset || !bytes || (which != 0 && which != 1)) return MOE_ERR_ARG;
+  Layout L;
+  if (which == 0) saved_layout(D, L);
+  else ws_layout(D, L);
+  const Entry *e = L.find(name);
+  if (!e) return MOE_ERR_ARG;
+  *offset = e->off;
+  *bytes = e->bytes;
+  return MOE_OK;
+}
+
+int64_t moe_padded_rows(const moe_config *cfg) {
+  Dims D;
+  if (check_config(cfg, &D) != MOE_OK) return 0;
+  return D.Rp;
+}
+
+int moe_quantize_mx(const void *src, int batch, int rows, int cols, int transpose, void *codes,
+                    void *scales, moe_stream_t stream) {
+  if (!src || !codes || !scales || batch <= 0 || rows <= 0 || cols <= 0) return MOE_ERR_ARG;
+  if (rows % 128 || cols % 128) return MOE_ERR_SHAPE;
+  if (!aligned16(src) || !aligned16(codes) || !aligned16(scales)) return MOE_ERR_ALIGN;
+  DeviceInfo dev;
+  const int rc = device_info(&dev);
+  if (rc != MOE_OK) return rc;
+  return cuda_status(moe::launch_quantize_mx(src, batch, rows, cols, transpose != 0,
+                                             static_cast<uint8_t *>(codes),
+                                             static_cast<uint8_t *>(scales), stream));
+}
+
+int moe_transpose_bf16(const void *src, int batch, int rows, int cols, void *dst,
+                       moe_stream_t stream) {
+  if (!src || !dst || batch <= 0 || rows <= 0 || cols <= 0) return MOE_ERR_ARG;
+  if (rows % 32 || cols % 64) return MOE_ERR_SHAPE;
+  if (!aligned16(src) || !aligned16(dst)) return MOE_ERR_ALIGN;
+  DeviceInfo dev;
+  const int rc = device_info(&dev);
+  if (rc != MOE_OK) return rc;
+  return cuda_status(moe::launch_transpose_bf16(src, batch, rows, cols, dst, stream));
+}
+
+static int route_impl(const Dims &D, const float *logits, const RouteBufs &rb, cudaStream_t s) {
+  return cuda_status(moe::launch_route(logits, D.T, D.E, D.k, rb, s));
+}
+
+int moe_route(const moe_config *cfg, const float *logits, int32_t *idx, float *w, int32_t *counts,
+              int32_t *offsets, int32_t *perm, void *ws, moe_stream_t stream) {
+  Dims D;
+  int rc = check_config(cfg, &D);
+  if (rc != MOE_OK) return rc;
+  if (!logits || !ws) return MOE_ERR_ARG;
+  if (!aligned16(logits) || !aligned16(ws)) return MOE_ERR_ALIGN;
+  DeviceInfo dev;
+  if ((rc = device_info(&dev)) != MOE_OK) return rc;
+  Layout W;
+  ws_layout(D, W);
+  Ptrs p = route_ptrs(W, ws, ws, W);
+  if (idx) p.rb.idx = idx;
+  if (w) p.rb.w = w;
+  if (counts) p.rb.counts = counts;
+  if (offsets) p.rb.offsets = offsets;
+  if (perm) p.rb.perm = perm;
+  if (cudaMemsetAsync(p.status, 0, 4, stream) != cudaSuccess) return MOE_ERR_CUDA;
+  return route_impl(D, logits, p.rb, stream);
+}
+
+int moe_forward(const moe_config *cfg, const void *x, const float *logits, const moe_weights *Wt,
+                void *y, void *saved, void *ws, moe_stream_t stream) {
+  Dims D;
+  int rc = check_config(cfg, &D);
+  if (rc != MOE_OK) return rc;
+  if (!x || !logits || !Wt || !y || !ws || !Wt->gu || !Wt->dn) return MOE_ERR_ARG;
+  if (D.mx && (!Wt->gu_scale || !Wt->dn_scale)) return MOE_ERR_ARG;
+  if (D.ms && (!Wt->s_gu || !Wt->s_dn)) return MOE_ERR_ARG;
+  if (!aligned16(x) || !aligned16(logits) || !aligned16(y) || !aligned16(ws) ||
+      !aligned16(Wt->gu) || !aligned16(Wt->dn) || (saved && !aligned16(saved)) ||
+      (D.mx && (!aligned16(Wt->gu_scale) || !aligned16(Wt->dn_scale))) ||
+      (D.ms && (!aligned16(Wt->s_gu) || !aligned16(Wt->s_dn))))
+    return MOE_ERR_ALIGN;
+  DeviceInfo dev;
+  if ((rc = device_info(&dev)) != MOE_OK) return rc;
+  cudaStream_t s = stream;
+  Layout W, S;
+  ws_layout(D, W);
+  saved_layout(D, S);
+  const bool train = saved != nullptr;
+  const Layout &RL = train ? S : W;
+  void *rbase = train ? saved : ws;
+  Ptrs p = route_ptrs(RL, rbase, ws, W);
+  const RouteBufs &rb = p.rb;
+  if (cudaMemsetAsync(p.status, 0, 4, s) != cudaSuccess) return MOE_ERR_CUDA;
+
+  // S1 + S2
+  if ((rc = route_impl(D, logits, rb, s)) != MOE_OK) return rc;
+  // S3 dispatch gather (+ MX quantisation of x)
+  char *xs = W.ptr(ws, "xs");
+  uint8_t *xs_sf = reinterpret_cast<uint8_t *>(W.ptr(ws, "xs_sf"));
+  if ((rc = cuda_status(moe::launch_gather(x, D.T, D.d, D.k, D.E, rb, D.Rp, D.mx, xs, xs_sf, s))) != MOE_OK)
+    return rc;
+  // S4 gate/up GEMM + SwiGLU (+ MX quantisation of h)
+  char *h_bf16 = train ? S.ptr(saved, "h") : (D.mx ? nullptr : W.ptr(ws, "h"));
+  char *GU = train ? S.ptr(saved, "GU") : nullptr;
+  uint8_t *hq = reinterpret_cast<uint8_t *>(W.ptr(ws, "hq"));
+  uint8_t *hq_sf = reinterpret_cast<uint8_t *>(W.ptr(ws, "hq_sf"));
+  char *o = RL.ptr(rbase, "o");
+  {
+    Gemm q;
+    q.mx = D.mx;
+    q.bn = 256;
+    q.epi = moe::EPI_SWIGLU;
+    q.a = xs;
+    q.a_rows = D.Rp;
+    q.b = Wt->gu;
+    q.b_rows = static_cast<long>(D.E) * 2 * D.m;
+    q.K = D.d;
+    q.g = base_args(moe::SCHED_GROUP_M, D.E, rb.poff, p.status);
+    q.g.K = D.d;
+    q.g.n_tiles = D.m / 128;
+    q.g.b_rows_per_group = 2 * D.m;
+    q.g.b_split = D.m;
+    q.g.sfa = xs_sf;
+    q.g.sfa_kg = D.d / 128;
+    q.g.sfb = static_cast<const uint8_t *>(Wt->gu_scale);
+    q.g.sfb_kg = D.d / 128;
+    q.g.out = h_bf16;
+    q.g.ldo = D.m;
+    q.g.out2 = GU;
+    q.g.ldo2 = 2 * D.m;
+    q.g.outq = D.mx ? hq : nullptr;
+    q.g.outq_sf = hq_sf;
+    q.g.ldq = D.m;
+    q.g.m_half = D.m;
+    q.max_tiles = (D.Rp / 128) * q.g.n_tiles;
+    if ((rc = run_gemm(q, dev, s)) != MOE_OK) return rc;
+  }
+  // S5 down GEMM
+  {
+    Gemm q;
+    q.mx = D.mx;
+    q.bn = bn_for(D.d);
+    q.epi = moe::EPI_STORE;
+    q.a = D.mx ? static_cast<const void *>(hq) : h_bf16;
+    q.a_rows = D.Rp;
+    q.b = Wt->dn;
+    q.b_rows = static_cast<long>(D.E) * D.d;
+    q.K = D.m;
+    q.g = base_args(moe::SCHED_GROUP_M, D.E, rb.poff, p.status);
+    q.g.K = D.m;
+    q.g.n_tiles = D.d / q.bn;
+    q.g.b_rows_per_group = D.d;
+    q.g.sfa = hq_sf;
+    q.g.sfa_kg = D.m / 128;
+    q.g.sfb = static_cast<const uint8_t *>(Wt->dn_scale);
+    q.g.sfb_kg = D.m / 128;
+    q.g.out = o;
+    q.g.ldo = D.d;
+    q.max_tiles = (D.Rp / 128) * q.g.n_tiles;
+    if ((rc = run_gemm(q, dev, s)) != MOE_OK) return rc;
+  }
+  // S7 shared expert (BF16, dense over all tokens)
+  char *s_out = nullptr;
+  if (D.ms) {
+    char *s_h = train ? S.ptr(saved, "s_h") : W.ptr(ws, "s_h");
+    char *s_GU = train ? S.ptr(saved, "s_GU") : nullptr;
+    s_out = W.ptr(ws, "s_out");
+    Gemm q;
+    q.mx = false;
+    q.bn = 256;
+    q.epi = moe::EPI_SWIGLU;
+    q.a = x;
+    q.a_rows = D.T;
+    q.b = Wt->s_gu;
+    q.b_rows = 2L * D.ms;
+    q.K = D.d;
+    q.g = base_args(moe::SCHED_DENSE, 1, nullptr, p.status);
+    q.g.M = D.T;
+    q.g.K = D.d;
+    q.g.n_tiles = D.ms / 128;
+    q.g.b_rows_per_group = 2 * D.ms;
+    q.g.b_split = D.ms;
+    q.g.out = s_h;
+    q.g.ldo = D.ms;
+    q.g.out2 = s_GU;
+    q.g.ldo2 = 2 * D.ms;
+    q.g.m_half = D.ms;
+    q.max_tiles = (D.Tp / 128) * q.g.n_tiles;
+    if ((rc = run_gemm(q, dev, s)) != MOE_OK) return rc;
+    Gemm q2;
+    q2.mx = false;
+    q2.bn = bn_for(D.d);
+    q2.epi = moe::EPI_STORE;
+    q2.a = s_h;
+    q2.a_rows = D.Tp;
+    q2.b = Wt->s_dn;
+    q2.b_rows = D.d;
+    q2.K = D.ms;
+    q2.g = base_args(moe::SCHED_DENSE, 1, nullptr, p.status);
+    q2.g.M = D.T;
+    q2.g.K = D.ms;
+    q2.g.n_tiles = D.d / q2.bn;
+    q2.g.b_rows_per_group = D.d;
+    q2.g.out = s_out;
+    q2.g.ldo = D.d;
+    q2.max_tiles = (D.Tp / 128) * q2.g.n_tiles;
+    if ((rc = run_gemm(q2, dev, s)) != MOE_OK) return rc;
+  }
+  // S6 combine
+  return cuda_status(moe::launch_combine(o, s_out, D.T, D.d, D.k, D.E, rb, y, s));
+}
+
+int moe_backward(const moe_config *cfg, const void *dy, const void *x, const moe_weights *Wt,
+                 const void *saved_c, void *dx, float *dlogits, void *dW_gu, void *dW_dn,
+                 void *dWs_gu, void *dWs_dn, void *ws, moe_stream_t stream) {
+  Dims D;
+  int rc = check_config(cfg, &D);
+  if (rc != MOE_OK) return rc;
+  if (!D.bwd) return MOE_ERR_ARG;
+  if (!dy || !x || !Wt || !saved_c || !dx || !dlogits || !dW_gu || !dW_dn || !ws) return MOE_ERR_ARG;
+  if (!Wt->gu_t || !Wt->dn_t) return MOE_ERR_ARG;
+  if (D.mx && (!Wt->gu_t_scale || !Wt->dn_t_scale)) return MOE_ERR_ARG;
+  if (D.ms && (!Wt->s_gu_t || !Wt->s_dn_t || !dWs_gu || !dWs_dn)) return MOE_ERR_ARG;
+  const void *ptrs[] = {dy, x, saved_c, dx, dlogits, dW_gu, dW_dn, ws, Wt->gu_t, Wt->dn_t};
+  for (const void *q : ptrs)
+    if (!aligned16(q)) return MOE_ERR_ALIGN;
+  if (D.mx && (!aligned16(Wt->gu_t_scale) || !aligned16(Wt->dn_t_scale))) return MOE_ERR_ALIGN;
+  if (D.ms && (!aligned16(Wt->s_gu_t) || !aligned16(Wt->s_dn_t) || !aligned16(dWs_gu) ||
+               !aligned16(dWs_dn)))
+    return MOE_ERR_ALIGN;
+  DeviceInfo dev;
+  if ((rc = device_info(&dev)) != MOE_OK) return rc;
+  cudaStream_t s = stream;
+  void *saved = const_cast<void *>(saved_c);
+  Layout W, S;
+  ws_layout(D, W);
+  saved_layout(D, S);
+  Ptrs p = route_ptrs(S, saved, ws, W);
+  const RouteBufs &rb = p.rb;
+  const int *nrows_dev = rb.poff + D.E;
+  const bool mx = D.mx;
+  auto u8 = [&](const char *n) { return reinterpret_cast<uint8_t *>(W.ptr(ws, n)); };
+
+  char *o = S.ptr(saved, "o");
+  char *GU = S.ptr(saved, "GU");
+  char *h = S.ptr(saved, "h");
+  float *g = reinterpret_cast<float *>(W.ptr(ws, "g"));
+  char *dO = W.ptr(ws, "dO");
+  char *dGU = W.ptr(ws, "dGU");
+  char *dX = W.ptr(ws, "dX");
+
+  // B1 reverse combine: dO = w * dy (bf16; MX row-quantised along d), g = <dy, o>
+  if ((rc = cuda_status(moe::launch_reverse_combine(dy, o, D.T, D.d, D.k, D.E, rb, D.Rp, dO, g, mx,
+                                                    u8("dOq"), u8("dOq_sf"), s))) != MOE_OK)
+    return rc;
+  // B2 dgrad of the down projection with the SwiGLU backward in the epilogue
+  {
+    Gemm q;
+    q.mx = mx;
+    q.bn = bn_for(D.m);
+    q.epi = moe::EPI_SWIGLU_BWD;
+    q.a = mx ? static_cast<const void *>(u8("dOq")) : dO;
+    q.a_rows = D.Rp;
+    q.b = Wt->dn_t;
+    q.b_rows = static_cast<long>(D.E) * D.m;
+    q.K = D.d;
+    q.g = base_args(moe::SCHED_GROUP_M, D.E, rb.poff, p.status);
+    q.g.K = D.d;
+    q.g.n_tiles = D.m / q.bn;
+    q.g.b_rows_per_group = D.m;
+    q.g.sfa = u8("dOq_sf");
+    q.g.sfa_kg = D.d / 128;
+    q.g.sfb = static_cast<const uint8_t *>(Wt->dn_t_scale);
+    q.g.sfb_kg = D.d / 128;
+    q.g.out = dGU;
+    q.g.ldo = 2 * D.m;
+    q.g.outq = mx ? u8("dGUq") : nullptr;
+    q.g.outq_sf = u8("dGUq_sf");
+    q.g.ldq = 2 * D.m;
+    q.g.aux = GU;
+    q.g.ld_aux = 2 * D.m;
+    q.g.m_half = D.m;
+    q.max_tiles = (D.Rp / 128) * q.g.n_tiles;
+    if ((rc = run_gemm(q, dev, s)) != MOE_OK) return rc;
+  }
+  // B4 dgrad of the gate/up projection
+  {
+    Gemm q;
+    q.mx = mx;
+    q.bn = bn_for(D.d);
+    q.epi = moe::EPI_STORE;
+    q.a = mx ? static_cast<const void *>(u8("dGUq")) : dGU;
+    q.a_rows = D.Rp;
+    q.b = Wt->gu_t;
+    q.b_rows = static_cast<long>(D.E) * D.d;
+    q.K = 2L * D.m;
+    q.g = base_args(moe::SCHED_GROUP_M, D.E, rb.poff, p.status);
+    q.g.K = 2 * D.m;
+    q.g.n_tiles = D.d / q.bn;
+    q.g.b_rows_per_group = D.d;
+    q.g.sfa = u8("dGUq_sf");
+    q.g.sfa_kg = 2 * D.m / 128;
+    q.g.sfb = static_cast<const uint8_t *>(Wt->gu_t_scale);
+    q.g.sfb_kg = 2 * D.m / 128;
+    q.g.out = dX;
+    q.g.ldo = D.d;
+    q.max_tiles = (D.Rp / 128) * q.g.n_tiles;
+    if ((rc = run_gemm(q, dev, s)) != MOE_OK) return rc;
+  }
+  // Transposed (column-blocked for MX) wgrad operands, K = padded rows.
+  struct Tr {
+    const void *src;
+    int C;
+    bool gather;
+    const char *dst, *sf;
+  } trs[] = {{dO, D.d, false, "dOT", "dOT_sf"},
+             {h, D.m, false, "hT", "hT_sf"},
+             {dGU, 2 * D.m, false, "dGUT", "dGUT_sf"},
+             {x, D.d, true, "xT", "xT_sf"}};
+  for (const Tr &t : trs)
+    if ((rc = cuda_status(moe::launch_transpose_rows(t.src, t.C, 0, nrows_dev, D.Rp, t.gather, D.k,
+                                                     D.E, &rb, D.Rp, mx, W.ptr(ws, t.dst),
+                                                     u8(t.sf), D.Rp, s))) != MOE_OK)
+      return rc;
+  // B3 wgrad of the down projection: dW_dn[e] = dO_e^T h_e
+  {
+    Gemm q;
+    q.mx = mx;
+    q.bn = bn_for(D.m);
+    q.epi = moe::EPI_STORE;
+    q.a = W.ptr(ws, "dOT");
+    q.a_rows = D.d;
+    q.b = W.ptr(ws, "hT");
+    q.b_rows = D.m;
+    q.K = D.Rp;
+    q.g = base_args(moe::SCHED_GROUP_K, D.E, rb.poff, p.status);
+    q.g.M = D.d;
+    q.g.n_tiles = D.m / q.bn;
+    q.g.sfa = u8("dOT_sf");
+    q.g.sfa_kg = static_cast<int>(D.Rp / 128);
+    q.g.sfb = u8("hT_sf");
+    q.g.sfb_kg = static_cast<int>(D.Rp / 128);
+    q.g.out = dW_dn;
+    q.g.ldo = D.m;
+    q.max_tiles = static_cast<long>(D.E) * (D.d / 128) * q.g.n_tiles;
+    if ((rc = run_gemm(q, dev, s)) != MOE_OK) return rc;
+  }
+  // B5 wgrad of the gate/up projection: dW_gu[e] = dGU_e^T X_e
+  {
+    Gemm q;
+    q.mx = mx;
+    q.bn = bn_for(D.d);
+    q.epi = moe::EPI_STORE;
+    q.a = W.ptr(ws, "dGUT");
+    q.a_rows = 2L * D.m;
+    q.b = W.ptr(ws, "xT");
+    q.b_rows = D.d;
+    q.K = D.Rp;
+    q.g = base_args(moe::SCHED_GROUP_K, D.E, rb.poff, p.status);
+    q.g.M = 2 * D.m;
+    q.g.n_tiles = D.d / q.bn;
+    q.g.sfa = u8("dGUT_sf");
+    q.g.sfa_kg = static_cast<int>(D.Rp / 128);
+    q.g.sfb = u8("xT_sf");
+    q.g.sfb_kg = static_cast<int>(D.Rp / 128);
+    q.g.out = dW_gu;
+    q.g.ldo = D.d;
+    q.max_tiles = static_cast<long>(D.E) * (2 * D.m / 128) * q.g.n_tiles;
+    if ((rc = run_gemm(q, dev, s)) != MOE_OK) return rc;
+  }
+  // B7 shared expert backward (BF16, dense)
+  char *s_dx = nullptr;
+  if (D.ms) {
+    char *s_GU = S.ptr(saved, "s_GU");
+    char *s_h = S.ptr(saved, "s_h");
+    char *s_dGU = W.ptr(ws, "s_dGU");
+    s_dx = W.ptr(ws, "s_dx");
+    {
+      Gemm q;
+      q.mx = false;
+      q.bn = bn_for(D.ms);
+      q.epi = moe::EPI_SWIGLU_BWD;
+      q.a = dy;
+      q.a_rows = D.T;
+      q.b = Wt->s_dn_t;
+      q.b_rows = D.ms;
+      q.K = D.d;
+      q.g = base_args(moe::SCHED_DENSE, 1, nullptr, p.status);
+      q.g.M = D.T;
+      q.g.K = D.d;
+      q.g.n_tiles = D.ms / q.bn;
+      q.g.b_rows_per_group = D.ms;
+      q.g.out = s_dGU;
+      q.g.ldo = 2 * D.ms;
+      q.g.aux = s_GU;
+      q.g.ld_aux = 2 * D.ms;
+      q.g.m_half = D.ms;
+      q.max_tiles = (D.Tp / 128) * q.g.n_tiles;
+      if ((rc = run_gemm(q, dev, s)) != MOE_OK) return rc;
+    }
+    {
+      Gemm q;
+      q.mx = false;
+      q.bn = bn_for(D.d);
+      q.epi = moe::EPI_STORE;
+      q.a = s_dGU;
+      q.a_rows = D.Tp;
+      q.b = Wt->s_gu_t;
+      q.b_rows = D.d;
+      q.K = 2L * D.ms;
+      q.g = base_args(moe::SCHED_DENSE, 1, nullptr, p.status);
+      q.g.M = D.T;
+      q.g.K = 2 * D.ms;
+      q.g.n_tiles = D.d / q.bn;
+      q.g.b_rows_per_group = D.d;
+      q.g.out = s_dx;
+      q.g.ldo = D.d;
+      q.max_tiles = (D.Tp / 128) * q.g.n_tiles;
+      if ((rc = run_gemm(q, dev, s)) != MOE_OK) return rc;
+    }
+    struct TrS {
+      const void *src;
+      int C;
+      long nsrc;
+      const char *dst;
+    } ts[] = {{dy, D.d, D.T, "s_dyT"},
+              {s_h, D.ms, D.Tp, "s_hT"},
+              {s_dGU, 2 * D.ms, D.Tp, "s_dGUT"},
+              {x, D.d, D.T, "s_xT"}};
+    for (const TrS &t : ts)
+      if ((rc = cuda_status(moe::launch_transpose_rows(t.src, t.C, static_cast<int>(D.Tp), nullptr,
+                                                       t.nsrc, false, D.k, D.E, nullptr, D.Tp, false,
+                                                       W.ptr(ws, t.dst), nullptr, D.Tp, s))) != MOE_OK)
+        return rc;
+    {
+      Gemm q;
+      q.mx = false;
+      q.bn = bn_for(D.ms);
+      q.epi = moe::EPI_STORE;
+      q.a = W.ptr(ws, "s_dyT");
+      q.a_rows = D.d;
+      q.b = W.ptr(ws, "s_hT");
+      q.b_rows = D.ms;
+      q.K = D.Tp;
+      q.g = base_args(moe::SCHED_GROUP_K, 1, nullptr, p.status);
+      q.g.M = D.d;
+      q.g.K = static_cast<int>(D.Tp);
+      q.g.n_tiles = D.ms / q.bn;
+      q.g.out = dWs_dn;
+      q.g.ldo = D.ms;
+      q.max_tiles = (D.d / 128) * q.g.n_tiles;
+      if ((rc = run_gemm(q, dev, s)) != MOE_OK) return rc;
+    }
+    {
+      Gemm q;
+      q.mx = false;
+      q.bn = bn_for(D.d);
+      q.epi = moe::EPI_STORE;
+      q.a = W.ptr(ws, "s_dGUT");
+      q.a_rows = 2L * D.ms;
+      q.b = W.ptr(ws, "s_xT");
+      q.b_rows = D.d;
+      q.K = D.Tp;
+      q.g = base_args(moe::SCHED_GROUP_K, 1, nullptr, p.status);
+      q.g.M = 2 * D.ms;
+      q.g.K = static_cast<int>(D.Tp);
+      q.g.n_tiles = D.d / q.bn;
+      q.g.out = dWs_gu;
+      q.g.ldo = D.d;
+      q.max_tiles = (2L * D.ms / 128) * q.g.n_tiles;
+      if ((rc = run_gemm(q, dev, s)) != MOE_OK) return rc;
+    }
+  }
+  // B6 reverse dispatch + dlogits
+  return cuda_status(moe::launch_reverse_dispatch(dX, s_dx, g, D.T, D.d, D.k, D.E, rb, dx, dlogits, s));
+}
+
+int moe_get_status(void *ws, moe_stream_t stream) {
+  if (!ws) return MOE_ERR_ARG;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return MOE_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, ws, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemset(ws, 0, 4) != cudaSuccess) return MOE_ERR_CUDA;
+  return (v & moe::kStatusTimeout) ? MOE_ERR_TIMEOUT : MOE_OK;
+}
+
+const char *moe_status_string(int status) {
+  switch (status) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_ARG: return "invalid argument";
+    case MOE_ERR_SHAPE: return "unsupported shape";
+    case MOE_ERR_ALIGN: return "pointer not 16-byte aligned";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_DEVICE: return "device is not sm_103";
+    case MOE_ERR_TIMEOUT: return "a device-side wait timed out";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,281 @@
+// Device helpers shared by the layer's kernels (sm_103a): PTX wrappers for
+// mbarrier, TMA and tcgen05 (5th-generation tensor cores with TMEM), bounded
+// waits, bf16 / MXFP8 conversions.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+#include "kernels.h"
+
+#define MOE_DEV __device__ __forceinline__
+
+namespace moe {
+
+// Every spin-wait in a kernel gives up after this much wall-clock time,
+// records kStatusTimeout and lets the kernel drain and return.
+constexpr unsigned long long kWaitTimeoutNs = 4000000000ull;
+
+MOE_DEV uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+MOE_DEV unsigned long long globaltimer() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+MOE_DEV uint32_t lane_id() { return threadIdx.x & 31u; }
+
+MOE_DEV uint32_t elect_one_sync() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n .reg .b32 rx;\n .reg .pred px;\n"
+      " elect.sync rx|px, %1;\n selp.b32 %0, 1, 0, px;\n}\n"
+      : "=r"(pred)
+      : "r"(0xffffffffu));
+  return pred;
+}
+
+// ---------------------------------------------------------------- mbarrier
+MOE_DEV void mbar_init(uint64_t *bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+MOE_DEV void fence_mbar_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
+MOE_DEV void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+MOE_DEV void mbar_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+MOE_DEV bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n"
+      " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Waits for the phase with the given parity to complete.  Gives up (returns
+// false) when *abort becomes non-zero or after kWaitTimeoutNs; in the latter
+// case it records the timeout in the global status word and raises *abort so
+// the other roles of the CTA stop too.
+MOE_DEV bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort, int *status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
+    if (globaltimer() - t0 > kWaitTimeoutNs) {
+      if (status) atomicOr(status, kStatusTimeout);
+      *abort = 1;
+      return false;
+    }
+  }
+}
+
+// ---------------------------------------------------------------- TMA
+MOE_DEV void tma_load_2d(const CUtensorMap *map, uint64_t *bar, void *dst, int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
+      : "memory");
+}
+MOE_DEV void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+MOE_DEV void prefetch_tensormap(const CUtensorMap *map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
+}
+
+// ---------------------------------------------------------------- tcgen05
+MOE_DEV void tmem_alloc(uint32_t *dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_u32(dst_smem)),
+               "r"(ncols)
+               : "memory");
+}
+MOE_DEV void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+MOE_DEV void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+MOE_DEV void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+MOE_DEV void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// D[tmem] (+)= A[smem] * B[smem]^T, bf16 inputs, fp32 accumulation.
+MOE_DEV void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                      uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Block-scaled MXFP8 (E4M3 x E4M3, E8M0 scales per 32 along K) variant.
+MOE_DEV void mma_mxf8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                      uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale [%0], %1, %2, %3, [%4], [%5], p;\n}\n" ::
+          "r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+// Arrive on an mbarrier once all previously issued tcgen05 ops of this thread finish.
+MOE_DEV void mma_commit(uint64_t *bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+// Copy 32 rows x 16 bytes of shared memory into TMEM, replicated into all four
+// 32-lane quarters (the scale-factor copy shape).
+MOE_DEV void tmem_cp_32x128b_warpx4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+               : "memory");
+}
+
+// Load 32 consecutive fp32 columns of this warp's 32 TMEM lanes.
+MOE_DEV void tmem_ld32(uint32_t taddr, float *v) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+MOE_DEV void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Shared-memory matrix descriptor for a K-major operand tile stored with the
+// 128-byte swizzle: rows of 128 bytes, 8-row (1024-byte) swizzle atoms
+// stacked along M/N.  Fields: start address >> 4 [0,14), leading byte offset
+// >> 4 [16,30) (unused for this layout), stride byte offset >> 4 [32,46)
+// = 1024 B between 8-row groups, descriptor version 1 at bit 46, swizzle mode
+// 2 (128-byte) at [61,64).  The tile base must be 1024-byte aligned; stepping
+// along K inside the 128-byte row adds the byte offset to the start address.
+MOE_DEV uint64_t sw128_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(1u) << 16;
+  d |= static_cast<uint64_t>(1024u >> 4) << 32;
+  d |= static_cast<uint64_t>(1u) << 46;
+  d |= static_cast<uint64_t>(2u) << 61;
+  return d;
+}
+// Descriptor of a non-swizzled K-major source: 8-row x 16-byte core matrices,
+// 128 bytes apart along M (used for the 32 x 16-byte scale-factor atoms).
+MOE_DEV uint64_t plain_desc_sbo128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(128u >> 4) << 32;
+  d |= static_cast<uint64_t>(1u) << 46;
+  return d;
+}
+
+// Instruction descriptors (32-bit), M = 128, K-major A and B.
+//   kind::f16:   D fmt F32 (1) at [4,6), A fmt BF16 (1) at [7,10), B fmt BF16
+//                (1) at [10,13), N>>3 at [17,23), M>>4 at [24,29).
+//   kind::mxf8f6f4.block_scale: B scale id at [4,6), A/B fmt E4M3 (0),
+//                N>>3 at [17,23), scale fmt UE8M0 (1) at bit 23, M>>4 at
+//                [24,29), A scale id at [29,31).
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+__host__ __device__ constexpr uint32_t idesc_mxf8(int M, int N) {
+  return (static_cast<uint32_t>(N >> 3) << 17) | (1u << 23) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+MOE_DEV uint32_t idesc_sf_ids(uint32_t idesc, uint32_t a_id, uint32_t b_id) {
+  return idesc | (b_id << 4) | (a_id << 29);
+}
+
+// ---------------------------------------------------------------- numerics
+MOE_DEV float silu(float g) { return g / (1.0f + expf(-g)); }
+MOE_DEV float sigmoidf(float g) { return 1.0f / (1.0f + expf(-g)); }
+
+MOE_DEV uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);  // .x = lo (low half)
+  return *reinterpret_cast<uint32_t *>(&v);
+}
+MOE_DEV float bf16lo(uint32_t v) { return __uint_as_float(v << 16); }
+MOE_DEV float bf16hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+MOE_DEV float round_bf16(float v) { return __bfloat162float(__float2bfloat16_rn(v)); }
+
+// E8M0 scale byte of an MX block from its absolute maximum:
+// floor(log2(amax)) - 8 + 127, clamped at 0 (= 2^-127).  A zero or subnormal
+// amax has floor(log2) <= -127 and therefore clamps to 0.
+MOE_DEV uint32_t mx_scale_byte(float amax) {
+  const int e = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu);
+  if (e == 0) return 0u;
+  const int b = e - 8;  // (e - 127 - 8) + 127
+  return b < 0 ? 0u : static_cast<uint32_t>(b);
+}
+// 2^-(byte-127) as a float: multiplies a block's values into E4M3 range
+// exactly (a power of two; byte <= 246 keeps it a normal float).
+MOE_DEV float mx_inv_scale(uint32_t byte) {
+  return __uint_as_float(static_cast<uint32_t>(254 - static_cast<int>(byte)) << 23);
+}
+// Two floats -> two E4M3 codes (round to nearest even, saturating); x -> low byte.
+MOE_DEV uint32_t e4m3x2(float x, float y) {
+  return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(x, y), __NV_SATFINITE, __NV_E4M3));
+}
+// 32 values -> 32 codes packed into 8 words (little-endian byte order).
+MOE_DEV void mx_encode32(const float *v, uint32_t byte, uint32_t *out8) {
+  const float s = mx_inv_scale(byte);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t lo = e4m3x2(v[4 * i] * s, v[4 * i + 1] * s);
+    const uint32_t hi = e4m3x2(v[4 * i + 2] * s, v[4 * i + 3] * s);
+    out8[i] = lo | (hi << 16);
+  }
+}
+
+// Byte offset of the scale of (row r, 32-block b) in the tiled scale layout
+// of a matrix with reduction length K (both multiples of 128).
+__host__ __device__ __forceinline__ size_t sf_tiled_offset(long r, long b, long K) {
+  return (static_cast<size_t>(r / 128) * static_cast<size_t>(K / 128) + static_cast<size_t>(b / 4)) *
+             512u +
+         static_cast<size_t>((r % 32) * 16 + ((r % 128) / 32) * 4 + (b % 4));
+}
+
+// Expert of padded row pr: the largest e with poff[e] <= pr (poff has E+1 entries).
+MOE_DEV int expert_of_row(const int *poff, int E, int pr) {
+  int lo = 0, hi = E - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(poff + mid) <= pr) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
+}  // namespace moe

@@ -1,0 +1,431 @@
+// Grouped expert GEMMs on the 5th-generation tensor cores (tcgen05 + TMEM).
+//
+// D[128 x BN] = A[128 x K] * B[BN x K]^T per tile, both operands K-major,
+// moved by TMA into 128-byte-swizzled shared memory, multiplied by one thread
+// issuing tcgen05.mma into a TMEM accumulator, and drained by four epilogue
+// warps with tcgen05.ld.  BF16 (kind::f16) or OCP MXFP8 (kind::mxf8f6f4 with
+// E8M0 block scales copied into TMEM by tcgen05.cp).
+//
+// Method references ("Mixture-of-Kittens" wiki page): expert grouped GEMMs in
+// MXFP8 with SwiGLU and quantisation fused (flowchart, Key claims MXFP8
+// bullet); a persistent kernel whose roles hand off through counters rather
+// than a global barrier (TL;DR) -- here the roles are warps of one CTA and the
+// counters are shared-memory mbarriers.
+//
+// Tile schedules:
+//   GROUP_M  rows of A are expert-sorted and padded per expert to 128, so every
+//            128-row tile belongs to one expert; B is that expert's weights.
+//            Tiles of one expert are consecutive (m-tile major), which keeps
+//            the expert's weight panel hot in L2 while its rows stream.
+//   DENSE    one group (shared expert).
+//   GROUP_K  weight gradients: the reduction runs over one expert's padded
+//            rows [poff[e], poff[e+1]) of two transposed operands.
+// Every output element is produced by one CTA with a fixed K order, so results
+// are bitwise reproducible.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+namespace {
+
+template <bool MX, int BN>
+struct Cfg {
+  static constexpr int BM = 128;
+  static constexpr int BK = MX ? 128 : 64;  // elements per 128-byte smem row
+  static constexpr int UK = MX ? 32 : 16;   // K per tcgen05.mma
+  static constexpr int KSTEPS = BK / UK;
+  static constexpr int A_BYTES = BM * 128;
+  static constexpr int B_BYTES = BN * 128;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES = BN == 256 ? 4 : 6;
+  static constexpr int SFA_BYTES = MX ? 512 : 0;
+  static constexpr int SFB_BYTES = MX ? (BN / 128) * 512 : 0;
+  static constexpr int SF_STAGE = SFA_BYTES + SFB_BYTES;
+  static constexpr int NUM_ACC = (MX && BN == 256) ? 1 : 2;
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr int SFA_COL = NUM_ACC * BN;
+  static constexpr int SFB_COL = SFA_COL + 4;
+  static constexpr uint32_t TX_BYTES = STAGE_BYTES + SF_STAGE;
+  static constexpr uint32_t IDESC = MX ? idesc_mxf8(128, BN) : idesc_bf16(128, BN);
+  // barriers: full[S], empty[S], tfull[NA], tempty[NA], done
+  static constexpr int NBAR = 2 * STAGES + 2 * NUM_ACC + 1;
+  static constexpr size_t SMEM =
+      1024 + static_cast<size_t>(STAGES) * (STAGE_BYTES + SF_STAGE) + NBAR * 8 + 16;
+  static_assert(!MX || SFB_COL + BN / 32 <= 512, "TMEM columns");
+  static_assert(NUM_ACC * BN <= 512, "TMEM columns");
+  static_assert(SMEM <= 232448, "shared memory");
+};
+
+struct Tile {
+  int a_row, k0, nk, b_row0, b_row1, out_row, out_col;
+};
+
+template <int BK, int BN, int EPI>
+MOE_DEV int total_tiles(const GemmArgs &g) {
+  if (g.sched == SCHED_GROUP_M) return g.n_tiles * (__ldg(g.poff + g.E) >> 7);
+  if (g.sched == SCHED_DENSE) return g.n_tiles * ((g.M + 127) >> 7);
+  return g.E * (g.M >> 7) * g.n_tiles;
+}
+
+template <int BK, int BN, int EPI>
+MOE_DEV Tile decode_tile(const GemmArgs &g, int t) {
+  Tile ti;
+  const int nt = g.n_tiles;
+  int e = 0, mt, ntile;
+  if (g.sched == SCHED_GROUP_M) {
+    int lo = 0, hi = g.E - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (nt * (__ldg(g.poff + mid) >> 7) <= t) lo = mid;
+      else hi = mid - 1;
+    }
+    e = lo;
+    const int ms = __ldg(g.poff + e) >> 7;
+    const int local = t - nt * ms;
+    mt = local / nt;
+    ntile = local % nt;
+    ti.a_row = (ms + mt) * 128;
+    ti.k0 = 0;
+    ti.nk = g.K / BK;
+    ti.out_row = ti.a_row;
+  } else if (g.sched == SCHED_DENSE) {
+    mt = t / nt;
+    ntile = t % nt;
+    ti.a_row = mt * 128;
+    ti.k0 = 0;
+    ti.nk = g.K / BK;
+    ti.out_row = ti.a_row;
+  } else {
+    const int mtn = (g.M >> 7) * nt;
+    e = t / mtn;
+    const int r = t % mtn;
+    mt = r / nt;
+    ntile = r % nt;
+    ti.a_row = mt * 128;
+    if (g.poff) {
+      ti.k0 = __ldg(g.poff + e);
+      ti.nk = (__ldg(g.poff + e + 1) - ti.k0) / BK;
+    } else {
+      ti.k0 = 0;
+      ti.nk = g.K / BK;
+    }
+    ti.out_row = e * g.M + mt * 128;
+  }
+  if (EPI == EPI_SWIGLU) {
+    ti.b_row0 = e * g.b_rows_per_group + ntile * 128;
+    ti.b_row1 = ti.b_row0 + g.b_split;
+    ti.out_col = ntile * 128;
+  } else {
+    ti.b_row0 = (g.sched == SCHED_GROUP_K ? 0 : e * g.b_rows_per_group) + ntile * BN;
+    ti.b_row1 = ti.b_row0 + 128;
+    ti.out_col = ntile * BN;
+  }
+  return ti;
+}
+
+MOE_DEV void store_bf16x32(void *base, long row, long ld, long col, const float *v) {
+  uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(base) + row * ld + col);
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    dst[i] = make_uint4(pack_bf16x2(v[8 * i], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
+                        pack_bf16x2(v[8 * i + 4], v[8 * i + 5]),
+                        pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
+}
+MOE_DEV void load_bf16x32(const void *base, long row, long ld, long col, float *v) {
+  const uint4 *src =
+      reinterpret_cast<const uint4 *>(reinterpret_cast<const __nv_bfloat16 *>(base) + row * ld + col);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint4 q = src[i];
+    v[8 * i + 0] = bf16lo(q.x); v[8 * i + 1] = bf16hi(q.x);
+    v[8 * i + 2] = bf16lo(q.y); v[8 * i + 3] = bf16hi(q.y);
+    v[8 * i + 4] = bf16lo(q.z); v[8 * i + 5] = bf16hi(q.z);
+    v[8 * i + 6] = bf16lo(q.w); v[8 * i + 7] = bf16hi(q.w);
+  }
+}
+// MX-quantise 32 values held by one thread (one block) and store codes + scale.
+MOE_DEV void store_mx32(uint8_t *codes, uint8_t *sf, long row, long ld, long col, const float *v) {
+  float am = 0.f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) am = fmaxf(am, fabsf(v[i]));
+  const uint32_t byte = mx_scale_byte(am);
+  uint32_t w[8];
+  mx_encode32(v, byte, w);
+  uint4 *dst = reinterpret_cast<uint4 *>(codes + row * ld + col);
+  dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+  dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  sf[sf_tiled_offset(row, col / 32, ld)] = static_cast<uint8_t>(byte);
+}
+
+template <bool MX, int BN, int EPI>
+__global__ void __launch_bounds__(192, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const GemmArgs g) {
+  using C = Cfg<MX, BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~static_cast<uintptr_t>(1023));
+  uint8_t *sf_base = smem + C::STAGES * C::STAGE_BYTES;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sf_base + C::STAGES * C::SF_STAGE);
+  uint64_t *full = bars;
+  uint64_t *empty = bars + C::STAGES;
+  uint64_t *tfull = bars + 2 * C::STAGES;
+  uint64_t *tempty = tfull + C::NUM_ACC;
+  uint64_t *done = tempty + C::NUM_ACC;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(done + 1);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < C::NUM_ACC; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 128);
+    }
+    mbar_init(done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int total = total_tiles<C::BK, BN, EPI>(g);
+
+  if (warp == 0) {
+    // ------------------------------------------------ TMA producer
+    if (lane == 0) {
+      prefetch_tensormap(&tmA);
+      prefetch_tensormap(&tmB);
+      int stage = 0;
+      uint32_t ph = 0;
+      int armed[C::STAGES];
+      for (int s = 0; s < C::STAGES; ++s) armed[s] = -1;
+      for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x) {
+        const Tile ti = decode_tile<C::BK, BN, EPI>(g, t);
+        for (int kb = 0; kb < ti.nk; ++kb) {
+          if (!mbar_wait(&empty[stage], ph ^ 1u, abort_flag, g.status)) break;
+          uint8_t *sa = smem + stage * C::STAGE_BYTES;
+          uint8_t *sb = sa + C::A_BYTES;
+          mbar_arrive_expect_tx(&full[stage], C::TX_BYTES);
+          armed[stage] = static_cast<int>(ph);
+          const int kc = ti.k0 + kb * C::BK;
+          tma_load_2d(&tmA, &full[stage], sa, kc, ti.a_row);
+          tma_load_2d(&tmB, &full[stage], sb, kc, ti.b_row0);
+          if (BN == 256) tma_load_2d(&tmB, &full[stage], sb + 128 * 128, kc, ti.b_row1);
+          if constexpr (MX) {
+            uint8_t *sfs = sf_base + stage * C::SF_STAGE;
+            const int kg = kc >> 7;
+            bulk_load(sfs, g.sfa + (static_cast<size_t>(ti.a_row >> 7) * g.sfa_kg + kg) * 512, 512,
+                      &full[stage]);
+            bulk_load(sfs + 512, g.sfb + (static_cast<size_t>(ti.b_row0 >> 7) * g.sfb_kg + kg) * 512,
+                      512, &full[stage]);
+            if (BN == 256)
+              bulk_load(sfs + 1024,
+                        g.sfb + (static_cast<size_t>(ti.b_row1 >> 7) * g.sfb_kg + kg) * 512, 512,
+                        &full[stage]);
+          }
+          if (++stage == C::STAGES) {
+            stage = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+      // Let every copy this thread started land before the CTA exits.
+      for (int s = 0; s < C::STAGES; ++s)
+        if (armed[s] >= 0) {
+          volatile int no_abort = 0;
+          mbar_wait(&full[s], static_cast<uint32_t>(armed[s]), &no_abort, g.status);
+        }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t ph = 0;
+      int acc = 0;
+      uint32_t aph = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        const Tile ti = decode_tile<C::BK, BN, EPI>(g, t);
+        if (!mbar_wait(&tempty[acc], aph ^ 1u, abort_flag, g.status)) break;
+        tc_fence_after();
+        const uint32_t dt = tmem_base + static_cast<uint32_t>(acc * BN);
+        for (int kb = 0; kb < ti.nk; ++kb) {
+          if (!mbar_wait(&full[stage], ph, abort_flag, g.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + stage * C::STAGE_BYTES);
+          const uint32_t sb = sa + C::A_BYTES;
+          if constexpr (MX) {
+            const uint32_t sfs = smem_u32(sf_base + stage * C::SF_STAGE);
+            tmem_cp_32x128b_warpx4(tmem_base + C::SFA_COL, plain_desc_sbo128(sfs));
+#pragma unroll
+            for (int c = 0; c < BN / 128; ++c)
+              tmem_cp_32x128b_warpx4(tmem_base + C::SFB_COL + 4 * c,
+                                     plain_desc_sbo128(sfs + 512 + 512 * c));
+          }
+#pragma unroll
+          for (int k = 0; k < C::KSTEPS; ++k) {
+            const uint64_t ad = sw128_desc(sa + 32 * k);
+            const uint64_t bd = sw128_desc(sb + 32 * k);
+            const uint32_t accum = (kb | k) ? 1u : 0u;
+            if constexpr (MX)
+              mma_mxf8(dt, ad, bd, idesc_sf_ids(C::IDESC, k, k), tmem_base + C::SFA_COL,
+                       tmem_base + C::SFB_COL, accum);
+            else
+              mma_bf16(dt, ad, bd, C::IDESC, accum);
+          }
+          mma_commit(&empty[stage]);
+          if (++stage == C::STAGES) {
+            stage = 0;
+            ph ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit(&tfull[acc]);
+        if (++acc == C::NUM_ACC) {
+          acc = 0;
+          aph ^= 1u;
+        }
+      }
+      // All MMAs this thread issued must finish before TMEM is released.
+      mma_commit(done);
+      volatile int no_abort = 0;
+      mbar_wait(done, 0, &no_abort, g.status);
+    }
+  } else {
+    // ------------------------------------------------ epilogue (warps 2..5)
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int r = q * 32 + lane;
+    int acc = 0;
+    uint32_t aph = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+      const Tile ti = decode_tile<C::BK, BN, EPI>(g, t);
+      if (!mbar_wait(&tfull[acc], aph, abort_flag, g.status)) break;
+      tc_fence_after();
+      const uint32_t tb =
+          tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
+      const long grow = ti.out_row + r;
+      if constexpr (EPI == EPI_STORE) {
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          float v[32];
+          if (ti.nk > 0) {
+            tmem_ld32(tb + 32 * c, v);
+            tmem_ld_wait();
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = 0.f;
+          }
+          store_bf16x32(g.out, grow, g.ldo, ti.out_col + 32 * c, v);
+        }
+      } else if constexpr (EPI == EPI_SWIGLU) {
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          float gv[32], uv[32];
+          tmem_ld32(tb + 32 * c, gv);
+          tmem_ld32(tb + 128 + 32 * c, uv);
+          tmem_ld_wait();
+          const long col = ti.out_col + 32 * c;
+          if (g.out2) {
+            store_bf16x32(g.out2, grow, g.ldo2, col, gv);
+            store_bf16x32(g.out2, grow, g.ldo2, g.m_half + col, uv);
+          }
+          float h[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) h[i] = silu(gv[i]) * uv[i];
+          if (g.out) store_bf16x32(g.out, grow, g.ldo, col, h);
+          if (g.outq) store_mx32(g.outq, g.outq_sf, grow, g.ldq, col, h);
+        }
+      } else {  // EPI_SWIGLU_BWD
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          float dh[32], G[32], U[32];
+          tmem_ld32(tb + 32 * c, dh);
+          tmem_ld_wait();
+          const long col = ti.out_col + 32 * c;
+          load_bf16x32(g.aux, grow, g.ld_aux, col, G);
+          load_bf16x32(g.aux, grow, g.ld_aux, g.m_half + col, U);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float s = sigmoidf(G[i]);
+            const float dg = round_bf16(dh[i] * U[i] * s * (1.0f + G[i] * (1.0f - s)));
+            const float du = round_bf16(dh[i] * G[i] * s);
+            G[i] = dg;
+            U[i] = du;
+          }
+          store_bf16x32(g.out, grow, g.ldo, col, G);
+          store_bf16x32(g.out, grow, g.ldo, g.m_half + col, U);
+          if (g.outq) {
+            store_mx32(g.outq, g.outq_sf, grow, g.ldq, col, G);
+            store_mx32(g.outq, g.outq_sf, grow, g.ldq, g.m_half + col, U);
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&tempty[acc]);
+      if (++acc == C::NUM_ACC) {
+        acc = 0;
+        aph ^= 1u;
+      }
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+}
+
+template <bool MX, int BN, int EPI>
+cudaError_t launch_one(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs &g, int grid,
+                       cudaStream_t s) {
+  using C = Cfg<MX, BN>;
+  static bool attr_set = false;  // per instantiation; idempotent, benign if repeated
+  if (!attr_set) {
+    const cudaError_t e = cudaFuncSetAttribute(gemm_kernel<MX, BN, EPI>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               static_cast<int>(C::SMEM));
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  gemm_kernel<MX, BN, EPI><<<grid, 192, C::SMEM, s>>>(ta, tb, g);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(bool mx, int bn, int epi, const CUtensorMap &ta, const CUtensorMap &tb,
+                        const GemmArgs &g, int grid, cudaStream_t s) {
+  if (grid <= 0) return cudaSuccess;
+#define MOE_GEMM_CASE(MXV, BNV, EPIV) \
+  if (mx == MXV && bn == BNV && epi == EPIV) return launch_one<MXV, BNV, EPIV>(ta, tb, g, grid, s);
+  MOE_GEMM_CASE(false, 256, EPI_STORE)
+  MOE_GEMM_CASE(false, 128, EPI_STORE)
+  MOE_GEMM_CASE(false, 256, EPI_SWIGLU)
+  MOE_GEMM_CASE(false, 256, EPI_SWIGLU_BWD)
+  MOE_GEMM_CASE(false, 128, EPI_SWIGLU_BWD)
+  MOE_GEMM_CASE(true, 256, EPI_STORE)
+  MOE_GEMM_CASE(true, 128, EPI_STORE)
+  MOE_GEMM_CASE(true, 256, EPI_SWIGLU)
+  MOE_GEMM_CASE(true, 256, EPI_SWIGLU_BWD)
+  MOE_GEMM_CASE(true, 128, EPI_SWIGLU_BWD)
+#undef MOE_GEMM_CASE
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace moe

@@ -1,0 +1,574 @@
+// Memory-bound kernels of the layer: router top-k, the device-side schedule
+// (histogram, scan, stable permutation), dispatch gather with fused MXFP8
+// quantisation, deterministic combine, reverse combine / reverse dispatch of
+// the backward pass, transposes and weight quantisation.
+//
+// Method references ("Mixture-of-Kittens" pages):
+//   routing fused into the layer            -- daily-ai-frontier summary, TL;DR
+//   device-side schedule, no CPU sync        -- wiki page, flowchart + Key claims
+//   quantisation fused into dispatch          -- wiki page, Key claims (MXFP8)
+//   fixed-order (bitwise deterministic) sum  -- wiki page, TL;DR + Key claims
+//   reverse-combine / reverse-dispatch       -- wiki page, Key claims (directions)
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+namespace {
+
+MOE_DEV void unpack8(const uint4 &q, float *f) {
+  f[0] = bf16lo(q.x); f[1] = bf16hi(q.x);
+  f[2] = bf16lo(q.y); f[3] = bf16hi(q.y);
+  f[4] = bf16lo(q.z); f[5] = bf16hi(q.z);
+  f[6] = bf16lo(q.w); f[7] = bf16hi(q.w);
+}
+MOE_DEV uint4 pack8(const float *f) {
+  return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                    pack_bf16x2(f[6], f[7]));
+}
+// MX-encode 8 values owned by this lane; the 4 lanes (lane & ~3 .. +3) hold one
+// 32-element block.  Returns the 8 codes; *byte gets the block's scale byte.
+MOE_DEV uint2 mx_encode8_quad(const float *f, uint32_t *byte) {
+  float am = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) am = fmaxf(am, fabsf(f[i]));
+  am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
+  am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 2));
+  const uint32_t b = mx_scale_byte(am);
+  const float s = mx_inv_scale(b);
+  uint2 c;
+  c.x = e4m3x2(f[0] * s, f[1] * s) | (e4m3x2(f[2] * s, f[3] * s) << 16);
+  c.y = e4m3x2(f[4] * s, f[5] * s) | (e4m3x2(f[6] * s, f[7] * s) << 16);
+  *byte = b;
+  return c;
+}
+
+// Token of padded expert-sorted row pr, or -1 for a padding row.
+MOE_DEV int token_of_row(const RouteBufs &b, int E, int k, int pr, int *slot_out) {
+  const int e = expert_of_row(b.poff, E, pr);
+  const int local = pr - __ldg(b.poff + e);
+  if (local >= __ldg(b.counts + e)) return -1;
+  const int slot = __ldg(b.inv + __ldg(b.offsets + e) + local);
+  if (slot_out) *slot_out = slot;
+  return slot / k;
+}
+
+// ------------------------------------------------------------ S1: route
+// One warp per token.  Top-k by repeated warp argmax under the total order
+// (logit descending, index ascending); weights = softmax over the k chosen
+// logits, summed in slot order.
+template <int VPL>
+__global__ void __launch_bounds__(256) route_topk_kernel(const float *__restrict__ logits, int T,
+                                                         int E, int k, int *__restrict__ idx,
+                                                         float *__restrict__ w) {
+  const int t = static_cast<int>((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  if (t >= T) return;
+  const float *row = logits + static_cast<size_t>(t) * E;
+  float v[VPL];
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    const int e = lane + 32 * i;
+    v[i] = e < E ? __ldg(row + e) : -INFINITY;
+  }
+  uint32_t taken = 0;
+  int my_e = 0;
+  float my_l = 0.f;
+  for (int j = 0; j < k; ++j) {
+    float bv = -INFINITY;
+    int be = 0x7fffffff;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+      const int e = lane + 32 * i;
+      const bool ok = e < E && !((taken >> i) & 1u);
+      if (ok && (v[i] > bv || (v[i] == bv && e < be))) {
+        bv = v[i];
+        be = e;
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+      const int oe = __shfl_xor_sync(0xffffffffu, be, off);
+      if (ov > bv || (ov == bv && oe < be)) {
+        bv = ov;
+        be = oe;
+      }
+    }
+    if ((be & 31) == lane) taken |= 1u << (be >> 5);
+    if (lane == j) {
+      my_e = be;
+      my_l = bv;
+    }
+  }
+  const float l0 = __shfl_sync(0xffffffffu, my_l, 0);
+  const float ex = lane < k ? expf(my_l - l0) : 0.f;
+  float sum = 0.f;
+  for (int j = 0; j < k; ++j) sum += __shfl_sync(0xffffffffu, ex, j);
+  if (lane < k) {
+    idx[static_cast<size_t>(t) * k + lane] = my_e;
+    w[static_cast<size_t>(t) * k + lane] = ex / sum;
+  }
+}
+
+// ------------------------------------------------------------ S2: schedule
+// (a) per-chunk expert histograms (integer counts: order-independent).
+__global__ void __launch_bounds__(128) sched_hist_kernel(const int *__restrict__ idx, int R, int E,
+                                                         int nchunks, int *__restrict__ hist) {
+  extern __shared__ int cnt[];
+  const int wib = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int c = blockIdx.x * (blockDim.x >> 5) + wib;
+  int *my = cnt + wib * E;
+  if (c >= nchunks) return;
+  for (int e = lane; e < E; e += 32) my[e] = 0;
+  __syncwarp();
+  const int base = c * kSchedChunk;
+  for (int i = lane; i < kSchedChunk; i += 32) {
+    const int s = base + i;
+    if (s < R) atomicAdd(&my[__ldg(idx + s)], 1);
+  }
+  __syncwarp();
+  for (int e = lane; e < E; e += 32) hist[static_cast<size_t>(c) * E + e] = my[e];
+}
+
+MOE_DEV int block_exclusive_scan(int v, int *warp_tot, int *total) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  int inc = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int o = __shfl_up_sync(0xffffffffu, inc, off);
+    if (lane >= off) inc += o;
+  }
+  if (lane == 31) warp_tot[wid] = inc;
+  __syncthreads();
+  if (wid == 0) {
+    const int nw = blockDim.x >> 5;
+    int x = lane < nw ? warp_tot[lane] : 0;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, x, off);
+      if (lane >= off) x += o;
+    }
+    if (lane < nw) warp_tot[lane] = x - (lane < nw ? warp_tot[lane] : 0);  // exclusive
+    if (lane == nw - 1) *total = x;
+  }
+  __syncthreads();
+  return inc - v + warp_tot[wid];
+}
+
+// (b) one block: per-expert exclusive prefix over chunks (in place), counts,
+// offsets (exclusive scan) and 128-padded offsets.
+__global__ void __launch_bounds__(1024) sched_scan_kernel(int *__restrict__ hist, int nchunks, int E,
+                                                          int *__restrict__ counts,
+                                                          int *__restrict__ offsets,
+                                                          int *__restrict__ poff) {
+  __shared__ int wt[32];
+  __shared__ int tot;
+  const int e = threadIdx.x;
+  int total = 0;
+  if (e < E) {
+    for (int c = 0; c < nchunks; ++c) {
+      const size_t p = static_cast<size_t>(c) * E + e;
+      const int v = hist[p];
+      hist[p] = total;
+      total += v;
+    }
+    counts[e] = total;
+  }
+  const int a = e < E ? total : 0;
+  const int pc = e < E ? ((total + 127) & ~127) : 0;
+  const int ea = block_exclusive_scan(a, wt, &tot);
+  const int ta = tot;
+  __syncthreads();
+  const int ep = block_exclusive_scan(pc, wt, &tot);
+  if (e < E) {
+    offsets[e] = ea;
+    poff[e] = ep;
+  }
+  if (e == 0) {
+    offsets[E] = ta;
+    poff[E] = tot;
+  }
+}
+
+// (c) one warp per chunk: stable ranks.  Slots are visited in flat order 32 at
+// a time; lanes with equal experts are ranked by lane (match_any), so rows of
+// an expert keep ascending slot order.
+__global__ void __launch_bounds__(128) sched_scatter_kernel(const int *__restrict__ idx, int R, int E,
+                                                            int nchunks,
+                                                            const int *__restrict__ hist_excl,
+                                                            const int *__restrict__ offsets,
+                                                            int *__restrict__ perm,
+                                                            int *__restrict__ inv) {
+  extern __shared__ int cnt[];
+  const int wib = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int c = blockIdx.x * (blockDim.x >> 5) + wib;
+  if (c >= nchunks) return;
+  int *my = cnt + wib * E;
+  for (int e = lane; e < E; e += 32) my[e] = offsets[e] + hist_excl[static_cast<size_t>(c) * E + e];
+  __syncwarp();
+  const int base = c * kSchedChunk;
+  for (int it = 0; it < kSchedChunk; it += 32) {
+    const int s = base + it + lane;
+    const int e = s < R ? __ldg(idx + s) : -1;
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    const int rank = __popc(peers & ((1u << lane) - 1u));
+    const int row = e >= 0 ? my[e] + rank : 0;
+    __syncwarp();
+    if (e >= 0 && rank == 0) my[e] += __popc(peers);
+    __syncwarp();
+    if (e >= 0) {
+      perm[s] = row;
+      inv[row] = s;
+    }
+  }
+}
+
+// ------------------------------------------------------------ S3: dispatch
+// One warp per padded row; rows of x are copied (bf16) or quantised (MXFP8).
+template <bool MX>
+__global__ void __launch_bounds__(256) gather_kernel(const uint4 *__restrict__ x, int d, int k, int E,
+                                                     RouteBufs b, int64_t rp_max, void *xs,
+                                                     uint8_t *__restrict__ xs_sf) {
+  const int64_t pr = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (pr >= rp_max || pr >= __ldg(b.poff + E)) return;
+  const int tok = token_of_row(b, E, k, static_cast<int>(pr), nullptr);
+  const int vec = d >> 3;
+  const uint4 *src = x + static_cast<size_t>(tok < 0 ? 0 : tok) * vec;
+  for (int i = lane; i < vec; i += 32) {
+    const uint4 q = tok >= 0 ? __ldg(src + i) : make_uint4(0, 0, 0, 0);
+    if constexpr (!MX) {
+      reinterpret_cast<uint4 *>(xs)[static_cast<size_t>(pr) * vec + i] = q;
+    } else {
+      float f[8];
+      unpack8(q, f);
+      uint32_t byte;
+      const uint2 c = mx_encode8_quad(f, &byte);
+      reinterpret_cast<uint2 *>(xs)[static_cast<size_t>(pr) * vec + i] = c;
+      if ((lane & 3) == 0) xs_sf[sf_tiled_offset(pr, i >> 2, d)] = static_cast<uint8_t>(byte);
+    }
+  }
+}
+
+// ------------------------------------------------------------ S6: combine
+__global__ void __launch_bounds__(256) combine_kernel(const uint4 *__restrict__ o,
+                                                      const uint4 *__restrict__ s_out, int T, int d,
+                                                      int k, int E, RouteBufs b,
+                                                      uint4 *__restrict__ y) {
+  const int t = static_cast<int>((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  if (t >= T) return;
+  int my_row = 0;
+  float my_w = 0.f;
+  if (lane < k) {
+    const int slot = t * k + lane;
+    const int e = __ldg(b.idx + slot);
+    my_row = __ldg(b.poff + e) + __ldg(b.perm + slot) - __ldg(b.offsets + e);
+    my_w = __ldg(b.w + slot);
+  }
+  const int vec = d >> 3;
+  for (int i = lane; i < vec; i += 32) {
+    float acc[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) acc[q] = 0.f;
+    for (int j = 0; j < k; ++j) {
+      const int row = __shfl_sync(0xffffffffu, my_row, j);
+      const float wj = __shfl_sync(0xffffffffu, my_w, j);
+      float f[8];
+      unpack8(__ldg(o + static_cast<size_t>(row) * vec + i), f);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) acc[q] = fmaf(wj, f[q], acc[q]);
+    }
+    if (s_out) {
+      float f[8];
+      unpack8(__ldg(s_out + static_cast<size_t>(t) * vec + i), f);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) acc[q] += f[q];
+    }
+    y[static_cast<size_t>(t) * vec + i] = pack8(acc);
+  }
+}
+
+// ------------------------------------------------------------ B1: reverse combine
+template <bool MX>
+__global__ void __launch_bounds__(256) reverse_combine_kernel(
+    const uint4 *__restrict__ dy, const uint4 *__restrict__ o, int d, int k, int E, RouteBufs b,
+    int64_t rp_max, uint4 *__restrict__ dO, float *__restrict__ g, uint8_t *__restrict__ dOq,
+    uint8_t *__restrict__ dOq_sf) {
+  const int64_t pr = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (pr >= rp_max || pr >= __ldg(b.poff + E)) return;
+  int slot = 0;
+  const int tok = token_of_row(b, E, k, static_cast<int>(pr), &slot);
+  const float wv = tok >= 0 ? __ldg(b.w + slot) : 0.f;
+  const int vec = d >> 3;
+  float dot = 0.f;
+  for (int i = lane; i < vec; i += 32) {
+    float f[8];
+    if (tok >= 0) {
+      float fy[8], fo[8];
+      unpack8(__ldg(dy + static_cast<size_t>(tok) * vec + i), fy);
+      unpack8(__ldg(o + static_cast<size_t>(pr) * vec + i), fo);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        dot = fmaf(fy[q], fo[q], dot);
+        f[q] = round_bf16(wv * fy[q]);
+      }
+    } else {
+#pragma unroll
+      for (int q = 0; q < 8; ++q) f[q] = 0.f;
+    }
+    dO[static_cast<size_t>(pr) * vec + i] = pack8(f);
+    if constexpr (MX) {
+      uint32_t byte;
+      const uint2 c = mx_encode8_quad(f, &byte);
+      reinterpret_cast<uint2 *>(dOq)[static_cast<size_t>(pr) * vec + i] = c;
+      if ((lane & 3) == 0) dOq_sf[sf_tiled_offset(pr, i >> 2, d)] = static_cast<uint8_t>(byte);
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
+  if (tok >= 0 && lane == 0) g[slot] = dot;
+}
+
+// ------------------------------------------------------------ B6: reverse dispatch
+__global__ void __launch_bounds__(256) reverse_dispatch_kernel(
+    const uint4 *__restrict__ dX, const uint4 *__restrict__ dxs, const float *__restrict__ g, int T,
+    int d, int k, int E, RouteBufs b, uint4 *__restrict__ dx, float *__restrict__ dlogits) {
+  const int t = static_cast<int>((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  if (t >= T) return;
+  int my_row = 0, my_e = -1;
+  float my_w = 0.f, my_g = 0.f;
+  if (lane < k) {
+    const int slot = t * k + lane;
+    my_e = __ldg(b.idx + slot);
+    my_row = __ldg(b.poff + my_e) + __ldg(b.perm + slot) - __ldg(b.offsets + my_e);
+    my_w = __ldg(b.w + slot);
+    my_g = __ldg(g + slot);
+  }
+  // dlogits: softmax-over-k gradient w_j (g_j - sum_i w_i g_i), slot order sum.
+  float S = 0.f;
+  for (int j = 0; j < k; ++j)
+    S = fmaf(__shfl_sync(0xffffffffu, my_w, j), __shfl_sync(0xffffffffu, my_g, j), S);
+  const float dl = my_w * (my_g - S);
+  float *drow = dlogits + static_cast<size_t>(t) * E;
+  for (int e = lane; e < E; e += 32) drow[e] = 0.f;
+  __syncwarp();
+  if (lane < k) drow[my_e] = dl;
+  const int vec = d >> 3;
+  for (int i = lane; i < vec; i += 32) {
+    float acc[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) acc[q] = 0.f;
+    for (int j = 0; j < k; ++j) {
+      const int row = __shfl_sync(0xffffffffu, my_row, j);
+      float f[8];
+      unpack8(__ldg(dX + static_cast<size_t>(row) * vec + i), f);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) acc[q] += f[q];
+    }
+    if (dxs) {
+      float f[8];
+      unpack8(__ldg(dxs + static_cast<size_t>(t) * vec + i), f);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) acc[q] += f[q];
+    }
+    dx[static_cast<size_t>(t) * vec + i] = pack8(acc);
+  }
+}
+
+// ------------------------------------------------------------ transposes
+// Tile: 32 source rows x 64 columns.  Output rows are source columns; MX
+// output quantises each 32-long output run (one tile's rows) as one block.
+template <bool MX, bool GATHER>
+__global__ void __launch_bounds__(256) transpose_rows_kernel(
+    const uint16_t *__restrict__ src, long src_batch_stride, int C, int nrows_host,
+    const int *__restrict__ nrows_dev, long nsrc, int k, int E, RouteBufs b, void *dst,
+    long dst_batch_stride, uint8_t *__restrict__ dst_sf, long sf_batch_rows, long ld_dst) {
+  __shared__ float tile[32][65];
+  const int r0 = blockIdx.x * 32;
+  const int c0 = blockIdx.y * 64;
+  const int bz = blockIdx.z;
+  const int nrows = nrows_dev ? __ldg(nrows_dev) : nrows_host;
+  if (r0 >= nrows) return;
+  src += static_cast<size_t>(bz) * src_batch_stride;
+  {
+    const int rr = threadIdx.x >> 3;          // 0..31
+    const int cc = (threadIdx.x & 7) * 8;     // 0..56
+    const int r = r0 + rr;
+    long srow = r;
+    if constexpr (GATHER) srow = token_of_row(b, E, k, r, nullptr);
+    float f[8];
+    if (srow >= 0 && srow < nsrc) {
+      unpack8(__ldg(reinterpret_cast<const uint4 *>(src + static_cast<size_t>(srow) * C + c0 + cc)), f);
+    } else {
+#pragma unroll
+      for (int q = 0; q < 8; ++q) f[q] = 0.f;
+    }
+#pragma unroll
+    for (int q = 0; q < 8; ++q) tile[rr][cc + q] = f[q];
+  }
+  __syncthreads();
+  const int c = threadIdx.x >> 2;   // output row within tile (0..63)
+  const int part = threadIdx.x & 3; // 8 source rows each
+  float f[8];
+#pragma unroll
+  for (int q = 0; q < 8; ++q) f[q] = tile[part * 8 + q][c];
+  const size_t orow = static_cast<size_t>(c0 + c);
+  if constexpr (!MX) {
+    uint16_t *o = reinterpret_cast<uint16_t *>(dst) + static_cast<size_t>(bz) * dst_batch_stride;
+    *reinterpret_cast<uint4 *>(o + orow * ld_dst + r0 + part * 8) = pack8(f);
+  } else {
+    uint8_t *o = reinterpret_cast<uint8_t *>(dst) + static_cast<size_t>(bz) * dst_batch_stride;
+    uint32_t byte;
+    const uint2 code = mx_encode8_quad(f, &byte);
+    *reinterpret_cast<uint2 *>(o + orow * ld_dst + r0 + part * 8) = code;
+    if (part == 0)
+      dst_sf[sf_tiled_offset(static_cast<long>(bz) * sf_batch_rows + static_cast<long>(orow), r0 / 32,
+                             ld_dst)] = static_cast<uint8_t>(byte);
+  }
+}
+
+// Row-blocked weight quantisation: src [rows, cols] bf16 -> codes + tiled scales.
+__global__ void __launch_bounds__(256) quantize_rows_kernel(const uint4 *__restrict__ src, long rows,
+                                                            int cols, uint2 *__restrict__ codes,
+                                                            uint8_t *__restrict__ sf) {
+  const long r = static_cast<long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (r >= rows) return;
+  const int vec = cols >> 3;
+  for (int i = lane; i < vec; i += 32) {
+    float f[8];
+    unpack8(__ldg(src + static_cast<size_t>(r) * vec + i), f);
+    uint32_t byte;
+    codes[static_cast<size_t>(r) * vec + i] = mx_encode8_quad(f, &byte);
+    if ((lane & 3) == 0) sf[sf_tiled_offset(r, i >> 2, cols)] = static_cast<uint8_t>(byte);
+  }
+}
+
+inline unsigned blocks_for(long n, int per_block) {
+  return static_cast<unsigned>((n + per_block - 1) / per_block);
+}
+
+}  // namespace
+
+cudaError_t launch_route(const float *logits, int T, int E, int k, const RouteBufs &b,
+                         cudaStream_t s) {
+  const unsigned grid = blocks_for(T, 8);
+  const int vpl = (E + 31) / 32;
+  if (vpl <= 1) route_topk_kernel<1><<<grid, 256, 0, s>>>(logits, T, E, k, b.idx, b.w);
+  else if (vpl <= 2) route_topk_kernel<2><<<grid, 256, 0, s>>>(logits, T, E, k, b.idx, b.w);
+  else if (vpl <= 4) route_topk_kernel<4><<<grid, 256, 0, s>>>(logits, T, E, k, b.idx, b.w);
+  else if (vpl <= 8) route_topk_kernel<8><<<grid, 256, 0, s>>>(logits, T, E, k, b.idx, b.w);
+  else if (vpl <= 16) route_topk_kernel<16><<<grid, 256, 0, s>>>(logits, T, E, k, b.idx, b.w);
+  else route_topk_kernel<32><<<grid, 256, 0, s>>>(logits, T, E, k, b.idx, b.w);
+  const int R = T * k;
+  const int nchunks = (R + kSchedChunk - 1) / kSchedChunk;
+  const size_t smem = 4 * static_cast<size_t>(E) * sizeof(int);
+  sched_hist_kernel<<<blocks_for(nchunks, 4), 128, smem, s>>>(b.idx, R, E, nchunks, b.hist);
+  sched_scan_kernel<<<1, 1024, 0, s>>>(b.hist, nchunks, E, b.counts, b.offsets, b.poff);
+  sched_scatter_kernel<<<blocks_for(nchunks, 4), 128, smem, s>>>(b.idx, R, E, nchunks, b.hist,
+                                                                  b.offsets, b.perm, b.inv);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather(const void *x, int T, int d, int k, int E, const RouteBufs &b,
+                          int64_t rp_max, bool mx, void *xs, uint8_t *xs_sf, cudaStream_t s) {
+  (void)T;
+  const unsigned grid = blocks_for(rp_max, 8);
+  if (mx)
+    gather_kernel<true><<<grid, 256, 0, s>>>(static_cast<const uint4 *>(x), d, k, E, b, rp_max, xs, xs_sf);
+  else
+    gather_kernel<false><<<grid, 256, 0, s>>>(static_cast<const uint4 *>(x), d, k, E, b, rp_max, xs, xs_sf);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const void *o, const void *s_out, int T, int d, int k, int E,
+                           const RouteBufs &b, void *y, cudaStream_t s) {
+  combine_kernel<<<blocks_for(T, 8), 256, 0, s>>>(static_cast<const uint4 *>(o),
+                                                  static_cast<const uint4 *>(s_out), T, d, k, E, b,
+                                                  static_cast<uint4 *>(y));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_reverse_combine(const void *dy, const void *o, int T, int d, int k, int E,
+                                   const RouteBufs &b, int64_t rp_max, void *dO, float *g,
+                                   bool mx, uint8_t *dOq, uint8_t *dOq_sf, cudaStream_t s) {
+  (void)T;
+  const unsigned grid = blocks_for(rp_max, 8);
+  if (mx)
+    reverse_combine_kernel<true><<<grid, 256, 0, s>>>(
+        static_cast<const uint4 *>(dy), static_cast<const uint4 *>(o), d, k, E, b, rp_max,
+        static_cast<uint4 *>(dO), g, dOq, dOq_sf);
+  else
+    reverse_combine_kernel<false><<<grid, 256, 0, s>>>(
+        static_cast<const uint4 *>(dy), static_cast<const uint4 *>(o), d, k, E, b, rp_max,
+        static_cast<uint4 *>(dO), g, dOq, dOq_sf);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_reverse_dispatch(const void *dX, const void *dxs, const float *g, int T,
+                                    int d, int k, int E, const RouteBufs &b, void *dx,
+                                    float *dlogits, cudaStream_t s) {
+  reverse_dispatch_kernel<<<blocks_for(T, 8), 256, 0, s>>>(
+      static_cast<const uint4 *>(dX), static_cast<const uint4 *>(dxs), g, T, d, k, E, b,
+      static_cast<uint4 *>(dx), dlogits);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_transpose_rows(const void *src, int C, int nrows_out, const int *nrows_dev,
+                                  long nsrc, bool gather, int k, int E, const RouteBufs *b,
+                                  int64_t rows_alloc, bool mx, void *dst, uint8_t *dst_sf,
+                                  int64_t ld_dst, cudaStream_t s) {
+  const dim3 grid(blocks_for(rows_alloc, 32), C / 64, 1);
+  const RouteBufs bb = b ? *b : RouteBufs{};
+  const uint16_t *sp = static_cast<const uint16_t *>(src);
+  const long ns = gather ? (1L << 40) : nsrc;
+  if (mx) {
+    if (gather)
+      transpose_rows_kernel<true, true><<<grid, 256, 0, s>>>(sp, 0, C, nrows_out, nrows_dev, ns, k, E,
+                                                             bb, dst, 0, dst_sf, 0, ld_dst);
+    else
+      transpose_rows_kernel<true, false><<<grid, 256, 0, s>>>(sp, 0, C, nrows_out, nrows_dev, ns, k, E,
+                                                              bb, dst, 0, dst_sf, 0, ld_dst);
+  } else {
+    if (gather)
+      transpose_rows_kernel<false, true><<<grid, 256, 0, s>>>(sp, 0, C, nrows_out, nrows_dev, ns, k, E,
+                                                              bb, dst, 0, dst_sf, 0, ld_dst);
+    else
+      transpose_rows_kernel<false, false><<<grid, 256, 0, s>>>(sp, 0, C, nrows_out, nrows_dev, ns, k,
+                                                               E, bb, dst, 0, dst_sf, 0, ld_dst);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_mx(const void *src, int batch, int rows, int cols, bool transpose,
+                               uint8_t *codes, uint8_t *scales, cudaStream_t s) {
+  if (!transpose) {
+    const long total = static_cast<long>(batch) * rows;
+    quantize_rows_kernel<<<blocks_for(total, 8), 256, 0, s>>>(
+        static_cast<const uint4 *>(src), total, cols, reinterpret_cast<uint2 *>(codes), scales);
+  } else {
+    const dim3 grid(blocks_for(rows, 32), cols / 64, batch);
+    transpose_rows_kernel<true, false><<<grid, 256, 0, s>>>(
+        static_cast<const uint16_t *>(src), static_cast<long>(rows) * cols, cols, rows, nullptr, rows,
+        1, 1, RouteBufs{}, codes, static_cast<long>(rows) * cols, scales, cols, rows);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_transpose_bf16(const void *src, int batch, int rows, int cols, void *dst,
+                                  cudaStream_t s) {
+  const dim3 grid(blocks_for(rows, 32), cols / 64, batch);
+  transpose_rows_kernel<false, false><<<grid, 256, 0, s>>>(
+      static_cast<const uint16_t *>(src), static_cast<long>(rows) * cols, cols, rows, nullptr, rows, 1,
+      1, RouteBufs{}, dst, static_cast<long>(rows) * cols, nullptr, 0, rows);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

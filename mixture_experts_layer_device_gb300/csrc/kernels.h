@@ -1,0 +1,107 @@
+// Internal launchers of the layer's kernels (host side).  All launches are
+// asynchronous on the given stream; each returns cudaGetLastError().
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moe {
+
+// Device status word bits (kept in the workspace, read by moe_get_status).
+constexpr int kStatusTimeout = 1;
+
+// Chunk of flat slots handled by one warp in the schedule kernels.
+constexpr int kSchedChunk = 1024;
+
+struct RouteBufs {
+  int *idx;       // [T*k]
+  float *w;       // [T*k]
+  int *counts;    // [E]
+  int *offsets;   // [E+1]
+  int *perm;      // [R]  slot -> row
+  int *inv;       // [R]  row -> slot
+  int *poff;      // [E+1] padded offsets (multiples of 128)
+  int *hist;      // [nchunks * E] scratch
+};
+
+cudaError_t launch_route(const float *logits, int T, int E, int k, const RouteBufs &b,
+                         cudaStream_t s);
+
+// Gather routed rows of x into padded expert-sorted order (zero padding rows).
+// MX: writes E4M3 codes [Rp, d] and tiled scales (K = d) instead of bf16 rows.
+cudaError_t launch_gather(const void *x, int T, int d, int k, int E, const RouteBufs &b,
+                          int64_t rp_max, bool mx, void *xs, uint8_t *xs_sf, cudaStream_t s);
+
+// y[t] = bf16( sum_j w[t,j] * o[row(t,j)] + s[t] ), fixed j order.
+cudaError_t launch_combine(const void *o, const void *s_out, int T, int d, int k, int E,
+                           const RouteBufs &b, void *y, cudaStream_t s);
+
+// Reverse combine: dO[row] = bf16(w * dy[t]) (zero on padding rows), g[slot] =
+// <dy[t], o[row]>; MX: dO also row-quantised along d into codes + tiled scales.
+cudaError_t launch_reverse_combine(const void *dy, const void *o, int T, int d, int k, int E,
+                                   const RouteBufs &b, int64_t rp_max, void *dO, float *g,
+                                   bool mx, uint8_t *dOq, uint8_t *dOq_sf, cudaStream_t s);
+
+// Reverse dispatch: dx[t] = bf16( sum_j dX[row(t,j)] + dxs[t] ); dlogits row.
+cudaError_t launch_reverse_dispatch(const void *dX, const void *dxs, const float *g, int T,
+                                    int d, int k, int E, const RouteBufs &b, void *dx,
+                                    float *dlogits, cudaStream_t s);
+
+// Transpose of a row block: src [*, C] (row stride C) -> dst [C, ld_dst],
+// dst[c][r] = src[row(r)][c] for r < nrows (device count *nrows_dev when not
+// NULL, else nrows_out, a multiple of 32).  With `gather`, row(r) is the token
+// of padded expert row r (x re-gathered; -1 on padding rows), else row(r) = r;
+// rows with row(r) < 0 or row(r) >= nsrc read as zero.  bf16 output, or (mx)
+// E4M3 codes quantised in blocks of 32 along r with tiled scales
+// (K = ld_dst).  Rows beyond nrows are not written.
+cudaError_t launch_transpose_rows(const void *src, int C, int nrows_out, const int *nrows_dev,
+                                  long nsrc, bool gather, int k, int E, const RouteBufs *b,
+                                  int64_t rows_alloc, bool mx, void *dst, uint8_t *dst_sf,
+                                  int64_t ld_dst, cudaStream_t s);
+
+// Weight preparation.
+cudaError_t launch_quantize_mx(const void *src, int batch, int rows, int cols, bool transpose,
+                               uint8_t *codes, uint8_t *scales, cudaStream_t s);
+cudaError_t launch_transpose_bf16(const void *src, int batch, int rows, int cols, void *dst,
+                                  cudaStream_t s);
+
+// ---------------------------------------------------------------- GEMM
+enum GemmSched { SCHED_GROUP_M = 0, SCHED_DENSE = 1, SCHED_GROUP_K = 2 };
+enum GemmEpi { EPI_STORE = 0, EPI_SWIGLU = 1, EPI_SWIGLU_BWD = 2 };
+
+struct GemmArgs {
+  int sched;
+  int E;              // groups (experts); 1 for dense
+  const int *poff;    // [E+1] padded offsets (GROUP_M: A rows; GROUP_K: K ranges)
+  int M;              // DENSE: rows of A; GROUP_K: rows of A (= output rows per group)
+  int K;              // GROUP_M / DENSE: reduction length; GROUP_K with poff == NULL: K
+  int n_tiles;        // output column tiles
+  int b_rows_per_group;  // GROUP_M: rows of B per expert
+  int b_split;        // SWIGLU: row offset of the up half inside an expert's B (m); else 0
+  // MX scales (tiled layout), K groups of 128 per 128-row group
+  const uint8_t *sfa;
+  int sfa_kg;
+  const uint8_t *sfb;
+  int sfb_kg;
+  // epilogue
+  void *out;          // bf16 output (STORE: D; SWIGLU: h; SWIGLU_BWD: dGU)
+  long ldo;
+  void *out2;         // SWIGLU: G|U save [rows, 2m] bf16 (may be NULL)
+  long ldo2;
+  uint8_t *outq;      // SWIGLU / SWIGLU_BWD MX codes (may be NULL)
+  uint8_t *outq_sf;   // tiled scales of outq
+  long ldq;           // row stride of outq (= its K)
+  const void *aux;    // SWIGLU_BWD: saved G|U bf16
+  long ld_aux;
+  int m_half;         // SWIGLU / SWIGLU_BWD: m
+  int *status;
+};
+
+// D = A * B^T with A [rows, K] and B [rows, K] K-major (TMA maps built by the
+// caller, box = 128 rows x 128 bytes, 128-byte swizzle); bn = 128 or 256
+// output columns per tile; `grid` persistent CTAs (<= number of SMs).
+cudaError_t launch_gemm(bool mx, int bn, int epi, const CUtensorMap &ta, const CUtensorMap &tb,
+                        const GemmArgs &args, int grid, cudaStream_t s);
+
+}  // namespace moe

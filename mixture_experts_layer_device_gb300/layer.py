@@ -1,0 +1,136 @@
+"""Device-memory plumbing around the C ABI: owns the workspace / saved buffers
+and the prepared expert weights (torch tensors), and calls the library.
+
+All arithmetic (weight quantisation and transposes included) runs in the
+library's CUDA kernels; torch only allocates memory and provides the stream.
+"""
+import torch
+
+from . import (MOE_BF16, MOE_FLAG_BACKWARD, MOE_MXFP8, check, config, moe_backward, moe_buffer_info,
+               moe_forward, moe_get_status, moe_padded_rows, moe_quantize_mx, moe_saved_bytes,
+               moe_transpose_bf16, moe_workspace_bytes, weights)
+
+_DT = {"i32": torch.int32, "f32": torch.float32, "bf16": torch.bfloat16, "u8": torch.uint8}
+
+
+def _u8(nbytes, device):
+    return torch.empty(max(int(nbytes), 16), dtype=torch.uint8, device=device)
+
+
+class MoELayer:
+    """One MoE layer's prepared weights and buffers on one GPU.
+
+    ``expert(e)`` returns the bf16 masters (W_gu [2m, d], W_dn [d, m]) of
+    expert e as device tensors; they are converted expert by expert into the
+    layout the kernels read (MXFP8 codes + tiled scales, and for the backward
+    the per-expert transposed copies), so the masters never need to be
+    resident all at once.
+    """
+
+    def __init__(self, T, d, m, E, k, fmt, expert, shared=None, backward=False, device="cuda"):
+        self.T, self.d, self.m, self.E, self.k = T, d, m, E, k
+        self.fmt = fmt
+        self.mx = fmt == "mxfp8"
+        self.ms = 0 if shared is None else shared[1].shape[1]
+        self.backward_enabled = backward
+        self.device = device
+        self.cfg = config(T, d, m, E, k, self.ms, MOE_MXFP8 if self.mx else MOE_BF16,
+                          MOE_FLAG_BACKWARD if backward else 0)
+        self.Rp = moe_padded_rows(self.cfg)
+        self.ws = _u8(moe_workspace_bytes(self.cfg), device)
+        self.saved = _u8(moe_saved_bytes(self.cfg), device) if backward else None
+        self._prepare(expert, shared)
+
+    # ------------------------------------------------------------ weights
+    def _prepare(self, expert, shared):
+        d, m, E, dev = self.d, self.m, self.E, self.device
+        t = {}
+        if self.mx:
+            t["gu"] = torch.empty((E * 2 * m, d), dtype=torch.uint8, device=dev)
+            t["gu_scale"] = torch.empty((E * 2 * m * d // 32,), dtype=torch.uint8, device=dev)
+            t["dn"] = torch.empty((E * d, m), dtype=torch.uint8, device=dev)
+            t["dn_scale"] = torch.empty((E * d * m // 32,), dtype=torch.uint8, device=dev)
+            if self.backward_enabled:
+                t["gu_t"] = torch.empty((E * d, 2 * m), dtype=torch.uint8, device=dev)
+                t["gu_t_scale"] = torch.empty((E * d * 2 * m // 32,), dtype=torch.uint8, device=dev)
+                t["dn_t"] = torch.empty((E * m, d), dtype=torch.uint8, device=dev)
+                t["dn_t_scale"] = torch.empty((E * m * d // 32,), dtype=torch.uint8, device=dev)
+        else:
+            t["gu"] = torch.empty((E, 2 * m, d), dtype=torch.bfloat16, device=dev)
+            t["dn"] = torch.empty((E, d, m), dtype=torch.bfloat16, device=dev)
+            if self.backward_enabled:
+                t["gu_t"] = torch.empty((E, d, 2 * m), dtype=torch.bfloat16, device=dev)
+                t["dn_t"] = torch.empty((E, m, d), dtype=torch.bfloat16, device=dev)
+        gsz, dsz = 2 * m * d, d * m
+        for e in range(E):
+            gu, dn = expert(e)
+            assert gu.is_cuda and gu.dtype == torch.bfloat16 and gu.shape == (2 * m, d)
+            assert dn.is_cuda and dn.dtype == torch.bfloat16 and dn.shape == (d, m)
+            gu, dn = gu.contiguous(), dn.contiguous()
+            if self.mx:
+                check(moe_quantize_mx(gu, 1, 2 * m, d, 0, t["gu"].view(-1)[e * gsz:],
+                                      t["gu_scale"][e * gsz // 32:]))
+                check(moe_quantize_mx(dn, 1, d, m, 0, t["dn"].view(-1)[e * dsz:], t["dn_scale"][e * dsz // 32:]))
+                if self.backward_enabled:
+                    check(moe_quantize_mx(gu, 1, 2 * m, d, 1, t["gu_t"].view(-1)[e * gsz:],
+                                          t["gu_t_scale"][e * gsz // 32:]))
+                    check(moe_quantize_mx(dn, 1, d, m, 1, t["dn_t"].view(-1)[e * dsz:],
+                                          t["dn_t_scale"][e * dsz // 32:]))
+            else:
+                t["gu"][e].copy_(gu)
+                t["dn"][e].copy_(dn)
+                if self.backward_enabled:
+                    check(moe_transpose_bf16(gu, 1, 2 * m, d, t["gu_t"][e]))
+                    check(moe_transpose_bf16(dn, 1, d, m, t["dn_t"][e]))
+        if shared is not None:
+            s_gu, s_dn = (w.contiguous() for w in shared)
+            t["s_gu"], t["s_dn"] = s_gu, s_dn
+            if self.backward_enabled:
+                ms = self.ms
+                t["s_gu_t"] = torch.empty((d, 2 * ms), dtype=torch.bfloat16, device=self.device)
+                t["s_dn_t"] = torch.empty((ms, d), dtype=torch.bfloat16, device=self.device)
+                check(moe_transpose_bf16(s_gu, 1, 2 * ms, d, t["s_gu_t"]))
+                check(moe_transpose_bf16(s_dn, 1, d, ms, t["s_dn_t"]))
+        self.tensors = t
+        self.W = weights(**t)
+
+    # ------------------------------------------------------------ passes
+    def forward(self, x, logits, y=None, train=False, stream=None):
+        if y is None:
+            y = torch.empty((self.T, self.d), dtype=torch.bfloat16, device=self.device)
+        if train and self.saved is None:
+            raise ValueError("layer was built without backward support")
+        check(moe_forward(self.cfg, x, logits, self.W, y, self.saved if train else None, self.ws, stream))
+        return y
+
+    def alloc_grads(self):
+        d, m, E, ms, dev = self.d, self.m, self.E, self.ms, self.device
+        g = dict(dx=torch.empty((self.T, d), dtype=torch.bfloat16, device=dev),
+                 dlogits=torch.empty((self.T, E), dtype=torch.float32, device=dev),
+                 dW_gu=torch.empty((E, 2 * m, d), dtype=torch.bfloat16, device=dev),
+                 dW_dn=torch.empty((E, d, m), dtype=torch.bfloat16, device=dev),
+                 dWs_gu=None, dWs_dn=None)
+        if ms:
+            g["dWs_gu"] = torch.empty((2 * ms, d), dtype=torch.bfloat16, device=dev)
+            g["dWs_dn"] = torch.empty((d, ms), dtype=torch.bfloat16, device=dev)
+        return g
+
+    def backward(self, dy, x, grads=None, stream=None):
+        g = grads or self.alloc_grads()
+        check(moe_backward(self.cfg, dy, x, self.W, self.saved, g["dx"], g["dlogits"], g["dW_gu"], g["dW_dn"],
+                           g["dWs_gu"], g["dWs_dn"], self.ws, stream))
+        return g
+
+    def status(self, stream=None):
+        return moe_get_status(self.ws, stream)
+
+    # ------------------------------------------------------------ inspection
+    def view(self, which, name, dtype, shape):
+        """Tensor view of a named sub-buffer of `saved` (which=0) or the workspace (1)."""
+        off, nb = moe_buffer_info(self.cfg, which, name)
+        base = self.saved if which == 0 else self.ws
+        t = base[off:off + nb].view(_DT[dtype])
+        n = 1
+        for s in shape:
+            n *= s
+        return t[:n].view(*shape)

@@ -1,0 +1,84 @@
+"""Helpers shared by the GPU parity tests: build a layer from a workload
+description, run the oracle on the same inputs, map padded GPU rows to the
+oracle's expert-sorted rows."""
+import numpy as np
+import torch
+
+import moe_inputs as mi
+from oracle import moe as om
+from oracle import numerics as nx
+
+
+def rel(a, b):
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    nb = np.linalg.norm(b)
+    return np.linalg.norm(a - b) / (nb if nb > 0 else 1.0)
+
+
+TOL = {"bf16": 5e-3, "mxfp8": 3e-2}
+
+
+class Case:
+    """Inputs drawn on the CPU (small workloads), a GPU layer, and oracle views."""
+
+    def __init__(self, cfg, backward=False, device="cuda"):
+        from mixture_experts_layer_device_gb300.layer import MoELayer
+        self.cfg = cfg
+        self.logits = mi.logits(cfg)
+        self.x = mi.tokens(cfg)
+        self.gu, self.dn = mi.experts(cfg)
+        self.shared = mi.shared(cfg)
+        self.dy = mi.out_grad(cfg)
+        self.layer = MoELayer(cfg["T"], cfg["d"], cfg["m"], cfg["E"], cfg["k"], cfg["fmt"],
+                              lambda e: (self.gu[e].to(device), self.dn[e].to(device)),
+                              shared=None if self.shared is None else tuple(w.to(device) for w in self.shared),
+                              backward=backward, device=device)
+        self.xg = self.x.to(device)
+        self.lg = self.logits.to(device)
+        self.dyg = self.dy.to(device)
+
+    def oracle_experts(self):
+        gu = mi.to_f64(self.gu)
+        dn = mi.to_f64(self.dn)
+        return [(gu[e], dn[e]) for e in range(self.cfg["E"])]
+
+    def oracle_shared(self):
+        return None if self.shared is None else tuple(mi.to_f64(w) for w in self.shared)
+
+    def route_views(self, which):
+        """(counts, offsets, poff, inv) the GPU schedule wrote (numpy)."""
+        E, R = self.cfg["E"], self.cfg["T"] * self.cfg["k"]
+        L = self.layer
+        return tuple(L.view(which, n, "i32", (s,)).cpu().numpy()
+                     for n, s in (("counts", E), ("offsets", E + 1), ("poff", E + 1), ("inv", R)))
+
+    def buffer(self, which, name):
+        """Raw bytes (numpy uint8) of a named buffer."""
+        import mixture_experts_layer_device_gb300 as pkg
+        off, nb = pkg.moe_buffer_info(self.layer.cfg, which, name)
+        base = self.layer.saved if which == 0 else self.layer.ws
+        return base[off:off + nb].cpu().numpy()
+
+    def oracle_forward(self):
+        return om.forward(mi.to_f64(self.x), self.logits.numpy(), self.oracle_experts(), self.cfg["k"],
+                          self.cfg["fmt"], shared=self.oracle_shared())
+
+
+def padded_rows(counts, offsets, poff):
+    """GPU padded row of each oracle (unpadded) expert-sorted row."""
+    counts = np.asarray(counts)
+    offsets = np.asarray(offsets)
+    poff = np.asarray(poff)
+    R = int(offsets[-1])
+    e_of = np.repeat(np.arange(counts.size), counts)
+    return poff[e_of] + np.arange(R) - offsets[e_of]
+
+
+def unpack_tiled_scales(sf, rows, K):
+    """Canonical [rows, K/32] scale bytes from the tiled layout (index permutation only)."""
+    sf = np.asarray(sf, dtype=np.uint8)
+    r = np.arange(rows)[:, None]
+    b = np.arange(K // 32)[None, :]
+    off = ((r // 128) * (K // 128) + b // 4) * 512 + (r % 32) * 16 + ((r % 128) // 32) * 4 + (b % 4)
+    return sf[off]

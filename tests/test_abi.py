@@ -1,0 +1,88 @@
+"""CPU-only checks of the C ABI: the library loads, exports every function that
+include/moe.h declares, and its host-side logic (sizes, layouts, argument
+checks) behaves as documented.  No compute call is made."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe.h")
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^[A-Za-z_][\w \*]*?\b(moe_\w+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def pkg():
+    from mixture_experts_layer_device_gb300 import build
+    build.build()
+    import mixture_experts_layer_device_gb300 as m
+    return m
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ["moe_route", "moe_forward", "moe_backward", "moe_quantize_mx", "moe_get_status"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(pkg):
+    L = ctypes.CDLL(pkg.LIB_PATH)
+    for n in declared_functions():
+        assert hasattr(L, n), n
+    assert sorted(pkg.EXPORTS) == declared_functions()
+
+
+def test_sizes_and_layout(pkg):
+    cfg = pkg.config(256, 256, 128, 8, 2, 0, "bf16", pkg.MOE_FLAG_BACKWARD)
+    assert pkg.moe_padded_rows(cfg) == ((256 * 2 + 127 * 8 + 127) // 128) * 128
+    ws = pkg.moe_workspace_bytes(cfg)
+    sv = pkg.moe_saved_bytes(cfg)
+    assert ws > 0 and sv > 0
+    off, nb = pkg.moe_buffer_info(cfg, 0, "o")
+    assert off % 256 == 0 and nb == pkg.moe_padded_rows(cfg) * 256 * 2 and off + nb <= sv
+    off, nb = pkg.moe_buffer_info(cfg, 1, "status")
+    assert off == 0
+    cfg_f = pkg.config(256, 256, 128, 8, 2, 0, "bf16", 0)
+    assert pkg.moe_workspace_bytes(cfg_f) < ws          # backward buffers only with the flag
+    with pytest.raises(RuntimeError):
+        pkg.moe_buffer_info(cfg_f, 1, "dO")
+    cmx = pkg.config(256, 256, 128, 8, 2, 0, "mxfp8", 0)
+    off, nb = pkg.moe_buffer_info(cmx, 1, "xs_sf")
+    assert nb == pkg.moe_padded_rows(cmx) * 256 // 32
+
+
+@pytest.mark.parametrize("bad,code", [
+    (dict(d=100), -2), (dict(m=64), -2), (dict(k=9), -2), (dict(k=0), -1), (dict(E=2000), -2),
+    (dict(T=0), -1), (dict(flags=4), -1), (dict(dtype=7), -1), (dict(m_shared=100), -2),
+])
+def test_invalid_configs_rejected_on_host(pkg, bad, code):
+    args = dict(T=64, d=256, m=128, E=8, k=2, m_shared=0, dtype=0, flags=0)
+    args.update(bad)
+    cfg = pkg.MoeConfig(*[args[n] for n in ("T", "d", "m", "E", "k", "m_shared", "dtype", "flags")])
+    assert pkg.moe_workspace_bytes(cfg) == 0
+    W = pkg.weights()
+    assert pkg.moe_forward(cfg, 16, 16, W, 16, None, 16, 0) == code
+
+
+def test_null_and_misaligned_pointers_rejected_on_host(pkg):
+    cfg = pkg.config(64, 256, 128, 8, 2)
+    W = pkg.weights(gu=1 << 20, dn=1 << 21)
+    assert pkg.moe_forward(cfg, None, 16, W, 16, None, 16, 0) == -1
+    assert pkg.moe_forward(cfg, 1 << 12, 1 << 12, W, 1 << 12, None, (1 << 12) + 4, 0) == -3
+    assert pkg.moe_quantize_mx(16, 1, 100, 128, 0, 16, 16, 0) == -2
+    assert pkg.moe_quantize_mx(8, 1, 128, 128, 0, 16, 16, 0) == -3
+    # backward without a backward-sized workspace
+    assert pkg.moe_backward(cfg, 16, 16, W, 16, 16, 16, 16, 16, None, None, 16, 0) == -1
+
+
+def test_status_strings(pkg):
+    L = pkg.lib()
+    for c in range(-6, 1):
+        assert L.moe_status_string(c).decode() == pkg.STATUS[c]

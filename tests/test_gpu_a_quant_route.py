@@ -1,0 +1,120 @@
+"""GPU parity of the integer / byte parts of the path: MXFP8 quantisation
+(codes and scales bit-exact), router top-k and the schedule (bit-exact), the
+softmax weights (fp32 vs fp64 within a derived bound)."""
+import numpy as np
+import pytest
+import torch
+
+import moe_inputs as mi
+from gpu_util import unpack_tiled_scales
+from oracle import moe as om
+from oracle import numerics as nx
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def pkg():
+    import mixture_experts_layer_device_gb300 as m
+    return m
+
+
+def _quant(pkg, w, transpose):
+    B, rows, cols = w.shape
+    n = B * rows * cols
+    codes = torch.empty(n, dtype=torch.uint8, device="cuda")
+    sf = torch.empty(n // 32, dtype=torch.uint8, device="cuda")
+    pkg.check(pkg.moe_quantize_mx(w, B, rows, cols, transpose, codes, sf))
+    torch.cuda.synchronize()
+    return codes.cpu().numpy(), sf.cpu().numpy()
+
+
+def edge_values(rng, shape):
+    v = rng.standard_normal(shape).astype(np.float32)
+    v[0, 0, :64] = 0.0                                   # all-zero blocks
+    v[0, 1, :32] = rng.standard_normal(32) * 1e-39       # subnormal-only block
+    v[0, 2, :32] = rng.uniform(-1.0, 1.0, 32) * 3e38     # near the top of the range
+    v[0, 3, :32] = np.float32(448.0) * 2.0 ** rng.integers(-20, 20)
+    v[0, 3, 5] = -v[0, 3, 5]
+    v[0, 4, :] = -0.0
+    v[0, 5, :32] = np.ldexp(1.0, rng.integers(-140, 120, 32))   # wide per-element exponent spread
+    return v
+
+
+@pytest.mark.parametrize("transpose", [0, 1])
+def test_quantize_mx_bit_exact(pkg, transpose):
+    rng = np.random.default_rng(0)
+    v = edge_values(rng, (2, 256, 384))
+    w = torch.from_numpy(v).to(torch.bfloat16)
+    codes, sf = _quant(pkg, w.cuda(), transpose)
+    ref = mi.to_f64(w)
+    c_ref, s_ref = om.quantize_weights(ref, transpose=bool(transpose))
+    B, rows, cols = c_ref.shape
+    assert np.array_equal(codes.reshape(B * rows, cols), c_ref.reshape(B * rows, cols))
+    assert np.array_equal(unpack_tiled_scales(sf, B * rows, cols), s_ref.reshape(B * rows, cols // 32))
+
+
+def test_quantize_mx_exhaustive_bf16_patterns(pkg):
+    # every finite bf16 bit pattern, in blocks that also carry a large element
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    vals = nx.bf16_from_bits(bits)
+    vals = vals[np.isfinite(vals)]
+    n = (vals.size + 127) // 128 * 128 * 128
+    arr = np.zeros(n)
+    arr[:vals.size] = vals
+    w = torch.from_numpy(arr.reshape(1, -1, 128).astype(np.float32)).to(torch.bfloat16)
+    codes, sf = _quant(pkg, w.cuda(), 0)
+    c_ref, s_ref = nx.mx_quantize(mi.to_f64(w)[0], axis=1)
+    assert np.array_equal(codes.reshape(c_ref.shape), c_ref)
+    assert np.array_equal(unpack_tiled_scales(sf, c_ref.shape[0], 128), s_ref)
+
+
+def _route(pkg, logits, k):
+    T, E = logits.shape
+    cfg = pkg.config(T, 256, 128, E, k)
+    ws = torch.empty(pkg.moe_workspace_bytes(cfg), dtype=torch.uint8, device="cuda")
+    idx = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    counts = torch.empty(E, dtype=torch.int32, device="cuda")
+    offsets = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    perm = torch.empty(T * k, dtype=torch.int32, device="cuda")
+    pkg.check(pkg.moe_route(cfg, logits.cuda(), idx, w, counts, offsets, perm, ws))
+    assert pkg.moe_get_status(ws) == 0
+    return [t.cpu().numpy() for t in (idx, w, counts, offsets, perm)]
+
+
+def _check_route(pkg, logits, k):
+    idx, w, counts, offsets, perm = _route(pkg, logits, k)
+    l = logits.numpy()
+    ridx, rw = om.route(l, k)
+    rc, ro, rp, _ = om.schedule(ridx, l.shape[1])
+    assert np.array_equal(idx, ridx)
+    assert np.array_equal(counts, rc) and np.array_equal(offsets, ro) and np.array_equal(perm, rp)
+    # fp32 softmax over k values vs fp64: expf error (a few ulp), k-term sum and a
+    # division -> |err| <= (4 + k) * 2**-24 relative to the largest weight (<= 1).
+    assert np.abs(w - rw).max() <= (4 + k) * 2.0 ** -24 * 2
+    assert np.allclose(w.sum(1), 1.0, atol=(k + 2) * 2.0 ** -23)
+
+
+@pytest.mark.parametrize("name", mi.ORDER)
+def test_route_full_size_bit_exact(pkg, name):
+    cfg = mi.WORKLOADS[name]
+    _check_route(pkg, mi.logits(cfg), cfg["k"])
+
+
+@pytest.mark.parametrize("T,E,k", [(1, 8, 2), (37, 5, 5), (300, 33, 7), (1000, 512, 16), (129, 1024, 3)])
+def test_route_ragged_shapes(pkg, T, E, k):
+    g = torch.Generator().manual_seed(T * 7 + E)
+    _check_route(pkg, torch.randn((T, E), generator=g), k)
+
+
+def test_route_ties_and_degenerate_loads(pkg):
+    T, E, k = 700, 40, 6
+    g = torch.Generator().manual_seed(5)
+    l = torch.round(torch.randn((T, E), generator=g) * 2) / 2     # many exact ties
+    l[10] = 0.0                                                   # an all-equal row
+    l[:, 7] += 100.0                                              # an expert with every token
+    l[:, 30:] -= 100.0                                            # experts that no token picks
+    l[20, :] = -0.0
+    l[21, ::2] = 0.0
+    _check_route(pkg, l.contiguous(), k)

@@ -1,0 +1,102 @@
+"""GPU parity of the forward pass against the oracle, element by element, on
+reduced-size workloads with the structure of each named workload (several GEMM
+tiles, ragged tails, skewed loads, empty experts), plus the dispatch
+quantisation bit-exact and run-to-run bitwise determinism."""
+import numpy as np
+import pytest
+import torch
+
+import moe_inputs as mi
+from gpu_util import TOL, Case, padded_rows, rel, unpack_tiled_scales
+from oracle import numerics as nx
+
+pytestmark = pytest.mark.gpu
+
+
+def small(name, **over):
+    c = dict(mi.SMALL[name])
+    c.update(over)
+    return c
+
+
+def run_forward(case, train=True):
+    y = case.layer.forward(case.xg, case.lg, train=train)
+    assert case.layer.status() == 0
+    return y
+
+
+def saved_rows(case, name, width, dtype="bf16"):
+    L = case.layer
+    t = L.view(0, name, dtype, (L.Rp, width))
+    return t.float().cpu().numpy().astype(np.float64)
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "mxfp8"])
+def test_single_expert_ffn(fmt):
+    """E = 1, k = 1: the layer is one SwiGLU FFN; checks GEMM1, SwiGLU and GEMM2 alone."""
+    cfg = dict(T=200, d=256, m=128, E=1, k=1, m_shared=0, fmt=fmt, bias="none", seed=21, backward=False)
+    c = Case(cfg, backward=True)
+    y = run_forward(c).float().cpu().numpy()
+    y_ref, s = c.oracle_forward()
+    counts, offsets, poff, _ = c.route_views(0)
+    assert list(poff) == [0, 256]
+    pr = padded_rows(counts, offsets, poff)
+    assert rel(saved_rows(c, "GU", 2 * cfg["m"])[pr], s["GU"]) < TOL[fmt] / 5, "gate/up GEMM"
+    assert rel(saved_rows(c, "o", cfg["d"])[pr], s["o"]) < TOL[fmt], "down GEMM"
+    assert rel(y, y_ref) < TOL[fmt]
+
+
+@pytest.mark.parametrize("name", mi.ORDER)
+def test_forward_matches_oracle(name):
+    cfg = small(name)
+    c = Case(cfg, backward=True)
+    y = run_forward(c).float().cpu().numpy()
+    y_ref, s = c.oracle_forward()
+    counts, offsets, poff, _ = c.route_views(0)
+    assert np.array_equal(counts, s["counts"]) and np.array_equal(offsets, s["offsets"])
+    assert np.array_equal(poff[1:] - poff[:-1], (counts + 127) // 128 * 128)
+    pr = padded_rows(counts, offsets, poff)
+    tol = TOL[cfg["fmt"]]
+    assert rel(saved_rows(c, "GU", 2 * cfg["m"])[pr], s["GU"]) < tol
+    assert rel(saved_rows(c, "h", cfg["m"])[pr], s["h"]) < tol
+    assert rel(saved_rows(c, "o", cfg["d"])[pr], s["o"]) < tol
+    assert rel(y, y_ref) < tol
+    # elementwise: no single output is far off (catches a wrong row or block)
+    err = np.abs(y - y_ref)
+    assert err.max() <= 0.05 * np.abs(y_ref).max() + 1e-2
+
+
+@pytest.mark.parametrize("name", ["glm-5.2", "deepseek-v4-pro"])
+def test_dispatch_quantisation_bit_exact(name):
+    cfg = small(name)
+    c = Case(cfg, backward=False)
+    run_forward(c, train=False)
+    L = c.layer
+    counts, offsets, poff, inv = c.route_views(1)
+    pr = padded_rows(counts, offsets, poff)
+    d = cfg["d"]
+    codes = L.view(1, "xs", "u8", (L.Rp, d)).cpu().numpy()
+    sf = c.buffer(1, "xs_sf")
+    x = mi.to_f64(c.x)
+    c_ref, s_ref = nx.mx_quantize(x[inv // cfg["k"]], axis=1)
+    assert np.array_equal(codes[pr], c_ref)
+    assert np.array_equal(unpack_tiled_scales(sf, L.Rp, d)[pr], s_ref)
+    # padding rows are zero codes with scale byte 0
+    pad = np.setdiff1d(np.arange(int(poff[-1])), pr)
+    assert np.all(codes[pad] == 0) and np.all(unpack_tiled_scales(sf, L.Rp, d)[pad] == 0)
+
+
+@pytest.mark.parametrize("name", ["qwen3.5-397b", "kimi-k2.7"])
+def test_forward_bitwise_deterministic(name):
+    cfg = small(name)
+    c = Case(cfg, backward=True)
+    y1 = run_forward(c).clone()
+    o1 = c.layer.view(0, "o", "bf16", (c.layer.Rp, cfg["d"])).clone()
+    y2 = run_forward(c, train=False)
+    y3 = run_forward(c)
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+    assert torch.equal(y1.view(torch.int16), y3.view(torch.int16))
+    counts, offsets, poff, _ = c.route_views(0)
+    pr = torch.as_tensor(padded_rows(counts, offsets, poff), device="cuda")
+    o3 = c.layer.view(0, "o", "bf16", (c.layer.Rp, cfg["d"]))
+    assert torch.equal(o1[pr].view(torch.int16), o3[pr].view(torch.int16))
