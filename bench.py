@@ -1,0 +1,544 @@
+#!/usr/bin/env python
+"""Throughput of the GB300 mixture-of-experts layer (one JSON line on stdout).
+
+A step is one pass of the layer's hot path over one batch of synthetic input:
+route + schedule, dispatch, expert GEMMs with SwiGLU and MXFP8 quantisation,
+shared expert, combine, and (for a fwd+bwd pass) the whole backward.  Expert
+weight preparation (MXFP8 quantisation of the bf16 masters and the backward
+copies) happens once per weight update, so it is timed separately ("s0_ms").
+
+  python bench.py [--gpus N --steps K --warmup W] [--workload NAME] [--pass fwd|fwdbwd]
+  python bench.py --impl reference ...     # the CPU oracle on a bounded sample
+
+Default workload: the Kimi-K2.7-shaped layer (E=384, d=7168, m=2048, top-8,
+T=16384, MXFP8 experts + BF16 shared expert of intermediate 2048), forward +
+backward -- the one workload that runs every step of the path.  N > 1 runs
+independent replicas (one per GPU, weak scaling): the layer has no exchange
+step on a single GPU.
+"""
+import argparse
+import json
+import math
+import multiprocessing as mp
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer tokens/s fwd & fwd+bwd on 1 GB300; % of GEMM/HBM roofline"
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+MX_OVER_BF16 = 2.0   # nominal dense MXFP8 : BF16 tensor-core ratio (4.5 : 2.25 PFLOP/s)
+
+# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from the
+# ncu capture summarised in profiles/, keyed by (workload, kernel).  An entry is
+# removed whenever the kernel changes after the capture.
+NCU_TRAFFIC = {}
+
+
+# ----------------------------------------------------------------------------- helpers
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return PEAKS_FALLBACK, "fallback"
+
+
+def workload(name):
+    import moe_inputs as mi
+    cfg = dict(mi.WORKLOADS[name])
+    cfg["name"] = name
+    return cfg
+
+
+def layer_work(cfg, passes):
+    """Algorithmic FLOPs (split by arithmetic) and bytes of one step."""
+    T, d, m, E, k, ms = (cfg[n] for n in ("T", "d", "m", "E", "k", "m_shared"))
+    R = T * k
+    mx = cfg["fmt"] == "mxfp8"
+    mult = 3 if passes == "fwdbwd" else 1
+    fl_exp = 6.0 * d * m * R * mult
+    fl_sh = 6.0 * d * ms * T * mult
+    wb = 1 + 1 / 32 if mx else 2                     # stored bytes per weight element
+    wts = E * 3 * d * m * wb
+    byt = wts + T * d * 2 + T * E * 4 + T * d * 2 + (3 * d * ms * 2 if ms else 0)
+    if passes == "fwdbwd":
+        byt += wts if mx else 0                      # backward operand copies
+        byt += T * d * 2 * 2 + T * E * 4             # dy, dx, dlogits
+        byt += E * 3 * d * m * 2 + 3 * d * ms * 2    # weight gradients (bf16)
+        byt += 3 * d * ms * 2                        # shared weights re-read
+    return fl_exp, fl_sh, byt
+
+
+def kernel_work(cfg, name):
+    """(bound, algorithmic work per launch, is_mx) for a traced kernel name."""
+    T, d, m, E, k, ms = (cfg[n] for n in ("T", "d", "m", "E", "k", "m_shared"))
+    R = T * k
+    mx = cfg["fmt"] == "mxfp8"
+    act = (1 + 1 / 32) if mx else 2
+    tbl = {
+        "gemm1_gate_up_swiglu": ("tensor", 2.0 * R * 2 * m * d, mx),
+        "gemm2_down": ("tensor", 2.0 * R * d * m, mx),
+        "dgrad_down_swiglu_bwd": ("tensor", 2.0 * R * m * d, mx),
+        "dgrad_gate_up": ("tensor", 2.0 * R * d * 2 * m, mx),
+        "wgrad_down": ("tensor", 2.0 * R * d * m, mx),
+        "wgrad_gate_up": ("tensor", 2.0 * R * 2 * m * d, mx),
+        "shared_gemm1_gate_up_swiglu": ("tensor", 2.0 * T * 2 * ms * d, False),
+        "shared_gemm2_down": ("tensor", 2.0 * T * d * ms, False),
+        "shared_dgrad_down_swiglu_bwd": ("tensor", 2.0 * T * ms * d, False),
+        "shared_dgrad_gate_up": ("tensor", 2.0 * T * d * 2 * ms, False),
+        "shared_wgrad_down": ("tensor", 2.0 * T * d * ms, False),
+        "shared_wgrad_gate_up": ("tensor", 2.0 * T * 2 * ms * d, False),
+        "dispatch_gather": ("hbm", R * d * (2 + act), mx),
+        "combine": ("hbm", R * d * 2 + T * d * 2 * (2 if ms else 1) + R * 8, mx),
+        "reverse_combine": ("hbm", R * d * (6 + (act if mx else 0)), mx),
+        "reverse_dispatch": ("hbm", R * d * 2 + T * d * 2 * (2 if ms else 1) + T * E * 4, mx),
+        "route_schedule": ("hbm", T * E * 4 + R * 4 * 6, mx),
+    }
+    return tbl.get(name)
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons while running."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", "-i", str(gpu_index), "--query-gpu=" + self.Q,
+                                       "--format=csv,noheader,nounits", "-lms", "200"],
+                                      stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.p.terminate()
+        self.p.wait()
+        self.f.seek(0)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.f:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        self.f.close()
+        os.unlink(self.f.name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def gpu_index(local_rank):
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        ids = [v.strip() for v in vis.split(",") if v.strip()]
+        if local_rank < len(ids) and ids[local_rank].isdigit():
+            return int(ids[local_rank])
+    return local_rank
+
+
+# ----------------------------------------------------------------------------- oracle (CPU)
+def _prep_worker(args):
+    from oracle import moe as om
+    e, gu, dn, fmt, backward = args
+    return e, om.prepare_expert(gu.astype("float64"), dn.astype("float64"), fmt, backward)
+
+
+class _Experts:
+    """experts[e] view for the oracle: only the sample's experts are held."""
+
+    def __init__(self, E, table):
+        self.E, self.t = E, table
+
+    def __len__(self):
+        return self.E
+
+    def __getitem__(self, e):
+        return self.t[e]
+
+
+def oracle_sample(cfg, passes, x_dev, logits_dev, dy_dev, n_tok):
+    """Host copies of an n_tok-token seeded sample and of its experts' masters."""
+    import moe_inputs as mi
+    from oracle import moe as om
+    tok = mi.sample_tokens(cfg, n_tok)
+    lg = logits_dev[tok].cpu().numpy()
+    idx, _ = om.route(lg, cfg["k"])
+    need = sorted(set(int(e) for e in idx.reshape(-1)))
+    masters = {}
+    for e in need:
+        gu, dn = mi.expert(cfg, e, device=x_dev.device)
+        masters[e] = (gu.float().cpu().numpy(), dn.float().cpu().numpy())
+    sh = mi.shared(cfg, device=x_dev.device)
+    shared = None if sh is None else tuple(mi.to_f64(w) for w in sh)
+    return dict(tok=tok, x=mi.to_f64(x_dev[tok]), logits=lg, dy=None if dy_dev is None else mi.to_f64(dy_dev[tok]),
+                need=need, masters=masters, shared=shared)
+
+
+def oracle_prepare(cfg, passes, sample):
+    """Weight preparation (S0) of the sample's experts by the oracle, in parallel."""
+    jobs = [(e, gu, dn, cfg["fmt"], passes == "fwdbwd") for e, (gu, dn) in sample["masters"].items()]
+    t0 = time.perf_counter()
+    nproc = max(1, min(len(jobs), os.cpu_count() or 1))
+    with mp.get_context("spawn").Pool(nproc) as pool:
+        ops = dict(pool.map(_prep_worker, jobs))
+    table = {e: (sample["masters"][e][0].astype("float64"), sample["masters"][e][1].astype("float64"), ops[e])
+             for e in ops}
+    return _Experts(cfg["E"], table), time.perf_counter() - t0
+
+
+def oracle_step(cfg, passes, sample, experts):
+    from oracle import moe as om
+    y, saved = om.forward(sample["x"], sample["logits"], experts, cfg["k"], cfg["fmt"], shared=sample["shared"])
+    if passes == "fwdbwd":
+        om.backward(sample["dy"], sample["x"], experts, cfg["k"], cfg["fmt"], saved, shared=sample["shared"],
+                    dw_experts=sample["need"])
+    return y
+
+
+def oracle_sample_desc(cfg, passes, n_tok, n_exp):
+    return ("%d seeded token(s) of the %s workload (%s): route, the %d experts they select, %scombine%s, "
+            "float64 NumPy; expert weight preparation (MXFP8 quantisation, S0) done beforehand like the "
+            "GPU side; BLAS threads = all cores, elementwise work single-threaded"
+            % (n_tok, cfg["name"], "fwd+bwd" if passes == "fwdbwd" else "fwd", n_exp,
+               "shared expert, " if cfg["m_shared"] else "",
+               ", full backward incl. the sample's weight gradients" if passes == "fwdbwd" else ""))
+
+
+# ----------------------------------------------------------------------------- main arms
+def build_inputs(cfg, device, passes):
+    import torch
+    import moe_inputs as mi
+    x = mi.tokens(cfg, device)
+    logits = mi.logits(cfg, device)
+    dy = mi.out_grad(cfg, device) if passes == "fwdbwd" else None
+    E, d, m = cfg["E"], cfg["d"], cfg["m"]
+    gu_all = torch.empty((E, 2 * m, d), dtype=torch.bfloat16, device=device)
+    dn_all = torch.empty((E, d, m), dtype=torch.bfloat16, device=device)
+    for e in range(E):
+        gu_all[e], dn_all[e] = mi.expert(cfg, e, device)
+    shared = mi.shared(cfg, device)
+    return x, logits, dy, gu_all, dn_all, shared
+
+
+def time_s0(layer, gu_all, dn_all, stream):
+    """Weight preparation of all experts (the same kernels the layer was built with)."""
+    import torch
+    import mixture_experts_layer_device_gb300 as pkg
+    E, d, m = layer.E, layer.d, layer.m
+    t = layer.tensors
+
+    def run():
+        if layer.mx:
+            pkg.check(pkg.moe_quantize_mx(gu_all, E, 2 * m, d, 0, t["gu"], t["gu_scale"], stream))
+            pkg.check(pkg.moe_quantize_mx(dn_all, E, d, m, 0, t["dn"], t["dn_scale"], stream))
+            if layer.backward_enabled:
+                pkg.check(pkg.moe_quantize_mx(gu_all, E, 2 * m, d, 1, t["gu_t"], t["gu_t_scale"], stream))
+                pkg.check(pkg.moe_quantize_mx(dn_all, E, d, m, 1, t["dn_t"], t["dn_t_scale"], stream))
+        elif layer.backward_enabled:
+            pkg.check(pkg.moe_transpose_bf16(gu_all, E, 2 * m, d, t["gu_t"], stream))
+            pkg.check(pkg.moe_transpose_bf16(dn_all, E, d, m, t["dn_t"], stream))
+
+    run()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    run()
+    b.record(stream)
+    b.synchronize()
+    return a.elapsed_time(b)
+
+
+def run_ours(args, cfg, passes, rank, world, local_rank):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+    import mixture_experts_layer_device_gb300 as pkg
+    from mixture_experts_layer_device_gb300.layer import MoELayer
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    peaks, peaks_src = load_peaks()
+
+    x, logits, dy, gu_all, dn_all, shared = build_inputs(cfg, dev, passes)
+    bwd = passes == "fwdbwd"
+    layer = MoELayer(cfg["T"], cfg["d"], cfg["m"], cfg["E"], cfg["k"], cfg["fmt"], shared=shared, backward=bwd,
+                     device=dev, stacked=(gu_all, dn_all))
+    s0_ms = time_s0(layer, gu_all, dn_all, stream)
+    sample = None
+    want_cpu = rank == 0 and world == 1 and not args.no_cpu_baseline and not args.profile_run
+    n_tok = 1 if bwd else 4
+    if want_cpu:
+        sample = oracle_sample(cfg, passes, x, logits, dy, n_tok)
+    del gu_all, dn_all
+    torch.cuda.empty_cache()
+
+    grads = layer.alloc_grads() if bwd else None
+    y = torch.empty((cfg["T"], cfg["d"]), dtype=torch.bfloat16, device=dev)
+
+    def step():
+        layer.forward(x, logits, y=y, train=bwd, stream=stream)
+        if bwd:
+            layer.backward(dy, x, grads=grads, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    st = layer.status()
+    if st != 0:
+        raise RuntimeError("device status %d after warm-up" % st)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    def timed(fn, K, trace=False):
+        if trace:
+            pkg.check(pkg.moe_trace_enable(K * 64 + 64))
+            pkg.moe_trace_clear()
+        barrier()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(K):
+            fn()
+        b.record(stream)
+        b.synchronize()
+        torch.cuda.synchronize()
+        barrier()
+        ms = a.elapsed_time(b)
+        recs = pkg.moe_trace_records() if trace else []
+        if trace:
+            pkg.moe_trace_enable(0)
+        if world > 1:
+            t = torch.tensor([ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms = float(t.item())
+        return ms, recs
+
+    clocks = Clocks(gpu_index(local_rank))
+    total_ms, recs = timed(step, args.steps, trace=True)
+    clk = clocks.stop()
+    ms_step = total_ms / args.steps
+    tokens = cfg["T"] * world
+    value = tokens * args.steps / (total_ms / 1e3)
+
+    fwd_value = value
+    if args.profile_run:      # one timed region only (keeps profiler launch lists short)
+        per_ms = {}
+        for name, ms in recs:
+            per_ms[name] = per_ms.get(name, 0.0) + ms
+        return {"metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "ms_per_step": round(ms_step, 4),
+                "config": {"workload": cfg["name"], "T": cfg["T"], "E": cfg["E"]}, "profile_run": True,
+                "kernels_ms_per_step": {n: round(t / args.steps, 4) for n, t in per_ms.items()}}
+    if bwd:
+        fms, _ = timed(lambda: layer.forward(x, logits, y=y, train=False, stream=stream), args.steps)
+        fwd_value = tokens * args.steps / (fms / 1e3)
+
+    # e2e: the public API with host buffers, copies inside the timed region
+    xh = x.cpu().pin_memory()
+    lh = logits.cpu().pin_memory()
+    dyh = dy.cpu().pin_memory() if bwd else None
+    yh = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+    dxh = torch.empty(y.shape, dtype=y.dtype).pin_memory() if bwd else None
+    dlh = torch.empty((cfg["T"], cfg["E"]), dtype=torch.float32).pin_memory() if bwd else None
+    xd, ld = torch.empty_like(x), torch.empty_like(logits)
+    dyd = torch.empty_like(dy) if bwd else None
+
+    def e2e_step():
+        xd.copy_(xh, non_blocking=True)
+        ld.copy_(lh, non_blocking=True)
+        if bwd:
+            dyd.copy_(dyh, non_blocking=True)
+        layer.forward(xd, ld, y=y, train=bwd, stream=stream)
+        yh.copy_(y, non_blocking=True)
+        if bwd:
+            layer.backward(dyd, xd, grads=grads, stream=stream)
+            dxh.copy_(grads["dx"], non_blocking=True)
+            dlh.copy_(grads["dlogits"], non_blocking=True)
+
+    e2e_ms, _ = timed(e2e_step, args.steps)
+    h2d = x.numel() * 2 + logits.numel() * 4 + (dy.numel() * 2 if bwd else 0)
+    d2h = y.numel() * 2 + ((y.numel() * 2 + cfg["T"] * cfg["E"] * 4) if bwd else 0)
+    st = layer.status()
+    if st != 0:
+        raise RuntimeError("device status %d after the timed region" % st)
+
+    # per-kernel breakdown of the timed region (library event trace)
+    per = {}
+    launches = 0
+    for name, ms in recs:
+        c, t = per.get(name, (0, 0.0))
+        per[name] = (c + 1, t + ms)
+        launches += 4 if name == "route_schedule" else 1
+    kernel_total = sum(t for _, t in per.values()) or 1.0
+    dom = max(per.items(), key=lambda kv: kv[1][1])[0]
+    bound, work, dom_mx = kernel_work(cfg, dom) or ("tensor", float("nan"), False)
+    cnt, tot = per[dom]
+    avg_ms = tot / cnt
+    if bound == "tensor":
+        peak = peaks["bf16_tflops_sustained"] * (MX_OVER_BF16 if dom_mx else 1.0)
+        achieved = work / (avg_ms / 1e3) / 1e12
+        unit = "TFLOP/s"
+        peak_note = ("MXFP8 = %s sustained BF16 x %.0f (nominal ratio)" if dom_mx else "%s sustained BF16") % (
+            peaks_src, MX_OVER_BF16)
+    else:
+        peak = peaks["hbm_gbs"]
+        achieved = work / (avg_ms / 1e3) / 1e9
+        unit = "GB/s"
+        peak_note = "%s HBM copy bandwidth" % peaks_src
+    traffic = NCU_TRAFFIC.get((cfg["name"], dom))
+    kernels = {n: {"launches_per_step": c / args.steps, "ms_per_step": round(t / args.steps, 4),
+                   "share": round(t / kernel_total, 4)} for n, (c, t) in sorted(per.items(), key=lambda kv: -kv[1][1])}
+    rs = per.get("route_schedule", (0, 0.0))[1] / kernel_total
+
+    # layer roofline (algorithmic work of the whole step)
+    fl_exp, fl_sh, byt = layer_work(cfg, passes)
+    mx = cfg["fmt"] == "mxfp8"
+    t_tensor = fl_exp / (peaks["bf16_tflops_sustained"] * 1e12 * (MX_OVER_BF16 if mx else 1.0)) + \
+        fl_sh / (peaks["bf16_tflops_sustained"] * 1e12)
+    t_hbm = byt / (peaks["hbm_gbs"] * 1e9)
+    t_roof = max(t_tensor, t_hbm)
+
+    out = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "mxfp8" if mx else "bf16",
+        "data": "synthetic (seeded N(0,1) tokens, N(0,1/d)/N(0,1/m) bf16 weights, fp32 logits)",
+        "config": {"workload": cfg["name"], "pass": "fwd+bwd" if bwd else "fwd", "T": cfg["T"], "d": cfg["d"],
+                   "m": cfg["m"], "E": cfg["E"], "k": cfg["k"], "m_shared": cfg["m_shared"],
+                   "experts": cfg["fmt"], "router_bias": cfg["bias"], "parallelism": "replicas" if world > 1 else "1gpu",
+                   "l2": "inputs larger than L2 (%.1f GB of expert weights read per step)"
+                         % (3 * cfg["E"] * cfg["d"] * cfg["m"] * (1.03 if mx else 2) / 1e9)},
+        "fwd_tokens_per_s": round(fwd_value, 1),
+        "layer_roofline": {"tokens_per_s": round(cfg["T"] * world / t_roof, 1), "frac": round(value / (cfg["T"] * world / t_roof), 4),
+                           "bound": "tensor" if t_tensor >= t_hbm else "hbm", "t_tensor_ms": round(t_tensor * 1e3, 3),
+                           "t_hbm_ms": round(t_hbm * 1e3, 3), "peaks": peaks_src},
+        "roofline": {"kernel": dom, "bound": bound, "achieved": round(achieved, 1), "peak": round(peak, 1),
+                     "unit": unit, "frac": round(achieved / peak, 4), "traffic": traffic, "peak_source": peak_note,
+                     "launch_ms": round(avg_ms, 4)},
+        "kernels": kernels,
+        "route_schedule_share": round(rs, 4),
+        "s0_ms": round(s0_ms, 3),
+        "e2e": {"value": round(tokens * args.steps / (e2e_ms / 1e3), 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": launches,
+        "clocks": clk,
+    }
+    if want_cpu:
+        experts, prep_s = oracle_prepare(cfg, passes, sample)
+        t0 = time.perf_counter()
+        oracle_step(cfg, passes, sample, experts)
+        dt = time.perf_counter() - t0
+        out["cpu_baseline"] = {"value": round(n_tok / dt, 4), "unit": "tokens/s", "cores": os.cpu_count(),
+                               "kind": "oracle", "sample": oracle_sample_desc(cfg, passes, n_tok, len(sample["need"])),
+                               "seconds": round(dt, 2), "s0_seconds": round(prep_s, 2)}
+    return out
+
+
+def run_reference(args, cfg, passes):
+    """The oracle as it stands, on the host cores, one bounded sample per step."""
+    import torch
+    dev = torch.device("cuda", 0) if torch.cuda.is_available() else torch.device("cpu")
+    import moe_inputs as mi
+    x = mi.tokens(cfg, dev)
+    logits = mi.logits(cfg, dev)
+    dy = mi.out_grad(cfg, dev) if passes == "fwdbwd" else None
+    n_tok = 1 if passes == "fwdbwd" else 4
+    sample = oracle_sample(cfg, passes, x, logits, dy, n_tok)
+    del x, logits, dy
+    experts, prep_s = oracle_prepare(cfg, passes, sample)
+    from oracle import moe as om
+    for _ in range(args.warmup):          # warm-up: the routing of the sample only
+        om.route(sample["logits"], cfg["k"])
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(cfg, passes, sample, experts)
+    dt = time.perf_counter() - t0
+    value = n_tok * args.steps / dt
+    cores = os.cpu_count()
+    return {"metric": METRIC, "value": round(value, 4), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 1), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": cfg["name"], "pass": "fwd+bwd" if passes == "fwdbwd" else "fwd", "T": cfg["T"],
+                       "d": cfg["d"], "m": cfg["m"], "E": cfg["E"], "k": cfg["k"], "m_shared": cfg["m_shared"],
+                       "experts": cfg["fmt"]},
+            "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": oracle_sample_desc(cfg, passes, n_tok, len(sample["need"])) +
+                             "; warm-up steps route the sample only", "s0_seconds": round(prep_s, 2)},
+            "e2e": {"value": round(value, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="kimi-k2.7")
+    ap.add_argument("--pass", dest="passes", choices=["fwd", "fwdbwd"], default=None)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-run", action="store_true",
+                    help="time the step once (no fwd-only, e2e or CPU legs): for profiler launch lists")
+    ap.add_argument("--override", default="",
+                    help="comma-separated shape overrides, e.g. T=2048,E=16 (smaller cases for profiling)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    cfg = workload(args.workload)
+    for kv in filter(None, args.override.split(",")):
+        key, val = kv.split("=")
+        cfg[key] = int(val)
+    passes = args.passes or ("fwdbwd" if cfg["backward"] else "fwd")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world != args.gpus:
+        ap.error("--gpus %d but WORLD_SIZE=%d (launch N>1 with torch.distributed.run)" % (args.gpus, world))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, cfg, passes)), flush=True)
+        return
+
+    import __graft_entry__
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+        if rank == 0:
+            __graft_entry__.build()
+        dist.barrier()
+    else:
+        __graft_entry__.build()
+    out = run_ours(args, cfg, passes, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

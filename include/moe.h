@@ -200,6 +200,25 @@ int moe_get_status(void *ws, moe_stream_t stream);
 /* Static description of a status code (never NULL). */
 const char *moe_status_string(int status);
 
+/*
+ * Optional per-launch timing (process-wide, for benchmarks and profilers).
+ * moe_trace_enable(n) creates n pairs of CUDA events (n = 0 disables tracing
+ * and destroys them); while enabled, every kernel launch made by moe_route,
+ * moe_forward and moe_backward is bracketed by an event pair recorded on the
+ * call's stream, in launch order, until n launches are recorded.  Tracing
+ * adds two event records per launch and changes nothing else.
+ * moe_trace_clear() restarts at slot 0; moe_trace_count() is the number of
+ * recorded launches; moe_trace_name(i) names launch i (static string, NULL
+ * when i is out of range); moe_trace_ms(i) synchronises on launch i's end
+ * event and returns its duration in milliseconds (negative on error).
+ * Not thread-safe: trace from one host thread.
+ */
+int moe_trace_enable(int capacity);
+void moe_trace_clear(void);
+int moe_trace_count(void);
+const char *moe_trace_name(int i);
+float moe_trace_ms(int i);
+
 #ifdef __cplusplus
 }
 #endif

@@ -34,7 +34,8 @@ class MoeWeights(ctypes.Structure):
 _lib = None
 EXPORTS = ["moe_workspace_bytes", "moe_saved_bytes", "moe_buffer_info", "moe_padded_rows",
            "moe_quantize_mx", "moe_transpose_bf16", "moe_route", "moe_forward", "moe_backward",
-           "moe_get_status", "moe_status_string"]
+           "moe_get_status", "moe_status_string", "moe_trace_enable", "moe_trace_clear", "moe_trace_count",
+           "moe_trace_name", "moe_trace_ms"]
 
 
 def lib():
@@ -61,6 +62,11 @@ def lib():
         L.moe_backward.restype = I
         L.moe_get_status.argtypes, L.moe_get_status.restype = [P, S], I
         L.moe_status_string.argtypes, L.moe_status_string.restype = [I], ctypes.c_char_p
+        L.moe_trace_enable.argtypes, L.moe_trace_enable.restype = [I], I
+        L.moe_trace_clear.argtypes, L.moe_trace_clear.restype = [], None
+        L.moe_trace_count.argtypes, L.moe_trace_count.restype = [], I
+        L.moe_trace_name.argtypes, L.moe_trace_name.restype = [I], ctypes.c_char_p
+        L.moe_trace_ms.argtypes, L.moe_trace_ms.restype = [I], ctypes.c_float
         _lib = L
     return _lib
 
@@ -147,3 +153,17 @@ def moe_backward(cfg, dy, x, W, saved, dx, dlogits, dW_gu, dW_dn, dWs_gu, dWs_dn
 
 def moe_get_status(ws, stream=None):
     return lib().moe_get_status(_ptr(ws), _stream(stream))
+
+
+def moe_trace_enable(capacity):
+    return lib().moe_trace_enable(capacity)
+
+
+def moe_trace_clear():
+    lib().moe_trace_clear()
+
+
+def moe_trace_records():
+    """[(kernel name, milliseconds)] of the launches recorded since the last clear."""
+    L = lib()
+    return [(L.moe_trace_name(i).decode(), L.moe_trace_ms(i)) for i in range(L.moe_trace_count())]

@@ -204,6 +204,40 @@ bool make_map(CUtensorMap *m, const void *base, bool bytes1, uint64_t inner, uin
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// ---------------------------------------------------------------- tracing
+struct Trace {
+  int capacity = 0, count = 0;
+  cudaEvent_t *start = nullptr, *end = nullptr;
+  const char **name = nullptr;
+} g_trace;
+
+void trace_free() {
+  for (int i = 0; i < g_trace.capacity; ++i) {
+    cudaEventDestroy(g_trace.start[i]);
+    cudaEventDestroy(g_trace.end[i]);
+  }
+  delete[] g_trace.start;
+  delete[] g_trace.end;
+  delete[] g_trace.name;
+  g_trace = Trace();
+}
+
+// Brackets one launch with an event pair when tracing is enabled.
+struct Traced {
+  int slot = -1;
+  cudaStream_t s;
+  Traced(const char *name, cudaStream_t st) : s(st) {
+    if (g_trace.count < g_trace.capacity) {
+      slot = g_trace.count++;
+      g_trace.name[slot] = name;
+      cudaEventRecord(g_trace.start[slot], s);
+    }
+  }
+  ~Traced() {
+    if (slot >= 0) cudaEventRecord(g_trace.end[slot], s);
+  }
+};
+
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
 // One GEMM launch: A [a_rows, K] and B [b_rows, K] (K-major) plus arguments.
@@ -219,7 +253,8 @@ struct Gemm {
   long max_tiles;
 };
 
-int run_gemm(const Gemm &q, const DeviceInfo &dev, cudaStream_t s) {
+int run_gemm(const char *name, const Gemm &q, const DeviceInfo &dev, cudaStream_t s) {
+  Traced tr(name, s);
   CUtensorMap ta, tb;
   if (!make_map(&ta, q.a, q.mx, q.K, q.a_rows) || !make_map(&tb, q.b, q.mx, q.K, q.b_rows))
     return MOE_ERR_CUDA;
@@ -325,6 +360,7 @@ int moe_transpose_bf16(const void *src, int batch, int rows, int cols, void *dst
 }
 
 static int route_impl(const Dims &D, const float *logits, const RouteBufs &rb, cudaStream_t s) {
+  Traced tr("route_schedule", s);
   return cuda_status(moe::launch_route(logits, D.T, D.E, D.k, rb, s));
 }
 
@@ -380,8 +416,11 @@ int moe_forward(const moe_config *cfg, const void *x, const float *logits, const
   // S3 dispatch gather (+ MX quantisation of x)
   char *xs = W.ptr(ws, "xs");
   uint8_t *xs_sf = reinterpret_cast<uint8_t *>(W.ptr(ws, "xs_sf"));
-  if ((rc = cuda_status(moe::launch_gather(x, D.T, D.d, D.k, D.E, rb, D.Rp, D.mx, xs, xs_sf, s))) != MOE_OK)
-    return rc;
+  {
+    Traced tr("dispatch_gather", s);
+    rc = cuda_status(moe::launch_gather(x, D.T, D.d, D.k, D.E, rb, D.Rp, D.mx, xs, xs_sf, s));
+  }
+  if (rc != MOE_OK) return rc;
   // S4 gate/up GEMM + SwiGLU (+ MX quantisation of h)
   char *h_bf16 = train ? S.ptr(saved, "h") : (D.mx ? nullptr : W.ptr(ws, "h"));
   char *GU = train ? S.ptr(saved, "GU") : nullptr;
@@ -416,7 +455,7 @@ int moe_forward(const moe_config *cfg, const void *x, const float *logits, const
     q.g.ldq = D.m;
     q.g.m_half = D.m;
     q.max_tiles = (D.Rp / 128) * q.g.n_tiles;
-    if ((rc = run_gemm(q, dev, s)) != MOE_OK) return rc;
+    if ((rc = run_gemm("gemm1_gate_up_swiglu", q, dev, s)) != MOE_OK) return rc;
   }
   // S5 down GEMM
   {
@@ -440,7 +479,7 @@ int moe_forward(const moe_config *cfg, const void *x, const float *logits, const
     q.g.out = o;
     q.g.ldo = D.d;
     q.max_tiles = (D.Rp / 128) * q.g.n_tiles;
-    if ((rc = run_gemm(q, dev, s)) != MOE_OK) return rc;
+    if ((rc = run_gemm("gemm2_down", q, dev, s)) != MOE_OK) return rc;
   }
   // S7 shared expert (BF16, dense over all tokens)
   char *s_out = nullptr;
@@ -469,7 +508,7 @@ int moe_forward(const moe_config *cfg, const void *x, const float *logits, const
     q.g.ldo2 = 2 * D.ms;
     q.g.m_half = D.ms;
     q.max_tiles = (D.Tp / 128) * q.g.n_tiles;
-    if ((rc = run_gemm(q, dev, s)) != MOE_OK) return rc;
+    if ((rc = run_gemm("shared_gemm1_gate_up_swiglu", q, dev, s)) != MOE_OK) return rc;
     Gemm q2;
     q2.mx = false;
     q2.bn = bn_for(D.d);
@@ -487,9 +526,10 @@ int moe_forward(const moe_config *cfg, const void *x, const float *logits, const
     q2.g.out = s_out;
     q2.g.ldo = D.d;
     q2.max_tiles = (D.Tp / 128) * q2.g.n_tiles;
-    if ((rc = run_gemm(q2, dev, s)) != MOE_OK) return rc;
+    if ((rc = run_gemm("shared_gemm2_down", q2, dev, s)) != MOE_OK) return rc;
   }
   // S6 combine
+  Traced tr("combine", s);
   return cuda_status(moe::launch_combine(o, s_out, D.T, D.d, D.k, D.E, rb, y, s));
 }
 
@@ -533,9 +573,12 @@ int moe_backward(const moe_config *cfg, const void *dy, const void *x, const moe
   char *dX = W.ptr(ws, "dX");
 
   // B1 reverse combine: dO = w * dy (bf16; MX row-quantised along d), g = <dy, o>
-  if ((rc = cuda_status(moe::launch_reverse_combine(dy, o, D.T, D.d, D.k, D.E, rb, D.Rp, dO, g, mx,
-                                                    u8("dOq"), u8("dOq_sf"), s))) != MOE_OK)
-    return rc;
+  {
+    Traced tr("reverse_combine", s);
+    rc = cuda_status(moe::launch_reverse_combine(dy, o, D.T, D.d, D.k, D.E, rb, D.Rp, dO, g, mx,
+                                                 u8("dOq"), u8("dOq_sf"), s));
+  }
+  if (rc != MOE_OK) return rc;
   // B2 dgrad of the down projection with the SwiGLU backward in the epilogue
   {
     Gemm q;
@@ -564,7 +607,7 @@ int moe_backward(const moe_config *cfg, const void *dy, const void *x, const moe
     q.g.ld_aux = 2 * D.m;
     q.g.m_half = D.m;
     q.max_tiles = (D.Rp / 128) * q.g.n_tiles;
-    if ((rc = run_gemm(q, dev, s)) != MOE_OK) return rc;
+    if ((rc = run_gemm("dgrad_down_swiglu_bwd", q, dev, s)) != MOE_OK) return rc;
   }
   // B4 dgrad of the gate/up projection
   {
@@ -588,7 +631,7 @@ int moe_backward(const moe_config *cfg, const void *dy, const void *x, const moe
     q.g.out = dX;
     q.g.ldo = D.d;
     q.max_tiles = (D.Rp / 128) * q.g.n_tiles;
-    if ((rc = run_gemm(q, dev, s)) != MOE_OK) return rc;
+    if ((rc = run_gemm("dgrad_gate_up", q, dev, s)) != MOE_OK) return rc;
   }
   // Transposed (column-blocked for MX) wgrad operands, K = padded rows.
   struct Tr {
@@ -600,11 +643,15 @@ int moe_backward(const moe_config *cfg, const void *dy, const void *x, const moe
              {h, D.m, false, "hT", "hT_sf"},
              {dGU, 2 * D.m, false, "dGUT", "dGUT_sf"},
              {x, D.d, true, "xT", "xT_sf"}};
-  for (const Tr &t : trs)
-    if ((rc = cuda_status(moe::launch_transpose_rows(t.src, t.C, 0, nrows_dev, D.Rp, t.gather, D.k,
-                                                     D.E, &rb, D.Rp, mx, W.ptr(ws, t.dst),
-                                                     u8(t.sf), D.Rp, s))) != MOE_OK)
-      return rc;
+  for (const Tr &t : trs) {
+    {
+      Traced tr("transpose_wgrad_operands", s);
+      rc = cuda_status(moe::launch_transpose_rows(t.src, t.C, 0, nrows_dev, D.Rp, t.gather, D.k, D.E,
+                                                  &rb, D.Rp, mx, W.ptr(ws, t.dst), u8(t.sf), D.Rp,
+                                                  s));
+    }
+    if (rc != MOE_OK) return rc;
+  }
   // B3 wgrad of the down projection: dW_dn[e] = dO_e^T h_e
   {
     Gemm q;
@@ -626,7 +673,7 @@ int moe_backward(const moe_config *cfg, const void *dy, const void *x, const moe
     q.g.out = dW_dn;
     q.g.ldo = D.m;
     q.max_tiles = static_cast<long>(D.E) * (D.d / 128) * q.g.n_tiles;
-    if ((rc = run_gemm(q, dev, s)) != MOE_OK) return rc;
+    if ((rc = run_gemm("wgrad_down", q, dev, s)) != MOE_OK) return rc;
   }
   // B5 wgrad of the gate/up projection: dW_gu[e] = dGU_e^T X_e
   {
@@ -649,7 +696,7 @@ int moe_backward(const moe_config *cfg, const void *dy, const void *x, const moe
     q.g.out = dW_gu;
     q.g.ldo = D.d;
     q.max_tiles = static_cast<long>(D.E) * (2 * D.m / 128) * q.g.n_tiles;
-    if ((rc = run_gemm(q, dev, s)) != MOE_OK) return rc;
+    if ((rc = run_gemm("wgrad_gate_up", q, dev, s)) != MOE_OK) return rc;
   }
   // B7 shared expert backward (BF16, dense)
   char *s_dx = nullptr;
@@ -679,7 +726,7 @@ int moe_backward(const moe_config *cfg, const void *dy, const void *x, const moe
       q.g.ld_aux = 2 * D.ms;
       q.g.m_half = D.ms;
       q.max_tiles = (D.Tp / 128) * q.g.n_tiles;
-      if ((rc = run_gemm(q, dev, s)) != MOE_OK) return rc;
+      if ((rc = run_gemm("shared_dgrad_down_swiglu_bwd", q, dev, s)) != MOE_OK) return rc;
     }
     {
       Gemm q;
@@ -699,7 +746,7 @@ int moe_backward(const moe_config *cfg, const void *dy, const void *x, const moe
       q.g.out = s_dx;
       q.g.ldo = D.d;
       q.max_tiles = (D.Tp / 128) * q.g.n_tiles;
-      if ((rc = run_gemm(q, dev, s)) != MOE_OK) return rc;
+      if ((rc = run_gemm("shared_dgrad_gate_up", q, dev, s)) != MOE_OK) return rc;
     }
     struct TrS {
       const void *src;
@@ -710,11 +757,15 @@ int moe_backward(const moe_config *cfg, const void *dy, const void *x, const moe
               {s_h, D.ms, D.Tp, "s_hT"},
               {s_dGU, 2 * D.ms, D.Tp, "s_dGUT"},
               {x, D.d, D.T, "s_xT"}};
-    for (const TrS &t : ts)
-      if ((rc = cuda_status(moe::launch_transpose_rows(t.src, t.C, static_cast<int>(D.Tp), nullptr,
-                                                       t.nsrc, false, D.k, D.E, nullptr, D.Tp, false,
-                                                       W.ptr(ws, t.dst), nullptr, D.Tp, s))) != MOE_OK)
-        return rc;
+    for (const TrS &t : ts) {
+      {
+        Traced tr("shared_transpose_wgrad_operands", s);
+        rc = cuda_status(moe::launch_transpose_rows(t.src, t.C, static_cast<int>(D.Tp), nullptr,
+                                                    t.nsrc, false, D.k, D.E, nullptr, D.Tp, false,
+                                                    W.ptr(ws, t.dst), nullptr, D.Tp, s));
+      }
+      if (rc != MOE_OK) return rc;
+    }
     {
       Gemm q;
       q.mx = false;
@@ -732,7 +783,7 @@ int moe_backward(const moe_config *cfg, const void *dy, const void *x, const moe
       q.g.out = dWs_dn;
       q.g.ldo = D.ms;
       q.max_tiles = (D.d / 128) * q.g.n_tiles;
-      if ((rc = run_gemm(q, dev, s)) != MOE_OK) return rc;
+      if ((rc = run_gemm("shared_wgrad_down", q, dev, s)) != MOE_OK) return rc;
     }
     {
       Gemm q;
@@ -751,10 +802,11 @@ int moe_backward(const moe_config *cfg, const void *dy, const void *x, const moe
       q.g.out = dWs_gu;
       q.g.ldo = D.d;
       q.max_tiles = (2L * D.ms / 128) * q.g.n_tiles;
-      if ((rc = run_gemm(q, dev, s)) != MOE_OK) return rc;
+      if ((rc = run_gemm("shared_wgrad_gate_up", q, dev, s)) != MOE_OK) return rc;
     }
   }
   // B6 reverse dispatch + dlogits
+  Traced tr("reverse_dispatch", s);
   return cuda_status(moe::launch_reverse_dispatch(dX, s_dx, g, D.T, D.d, D.k, D.E, rb, dx, dlogits, s));
 }
 
@@ -765,6 +817,40 @@ int moe_get_status(void *ws, moe_stream_t stream) {
   if (cudaMemcpy(&v, ws, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
   if (cudaMemset(ws, 0, 4) != cudaSuccess) return MOE_ERR_CUDA;
   return (v & moe::kStatusTimeout) ? MOE_ERR_TIMEOUT : MOE_OK;
+}
+
+int moe_trace_enable(int capacity) {
+  if (capacity < 0) return MOE_ERR_ARG;
+  trace_free();
+  if (capacity == 0) return MOE_OK;
+  g_trace.start = new cudaEvent_t[capacity];
+  g_trace.end = new cudaEvent_t[capacity];
+  g_trace.name = new const char *[capacity];
+  for (int i = 0; i < capacity; ++i) {
+    if (cudaEventCreate(&g_trace.start[i]) != cudaSuccess ||
+        cudaEventCreate(&g_trace.end[i]) != cudaSuccess) {
+      g_trace.capacity = i;
+      trace_free();
+      return MOE_ERR_CUDA;
+    }
+    g_trace.name[i] = nullptr;
+  }
+  g_trace.capacity = capacity;
+  return MOE_OK;
+}
+
+void moe_trace_clear(void) { g_trace.count = 0; }
+
+int moe_trace_count(void) { return g_trace.count; }
+
+const char *moe_trace_name(int i) { return (i >= 0 && i < g_trace.count) ? g_trace.name[i] : nullptr; }
+
+float moe_trace_ms(int i) {
+  if (i < 0 || i >= g_trace.count) return -1.f;
+  float ms = -1.f;
+  if (cudaEventSynchronize(g_trace.end[i]) != cudaSuccess) return -1.f;
+  if (cudaEventElapsedTime(&ms, g_trace.start[i], g_trace.end[i]) != cudaSuccess) return -1.f;
+  return ms;
 }
 
 const char *moe_status_string(int status) {

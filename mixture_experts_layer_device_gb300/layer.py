@@ -24,10 +24,12 @@ class MoELayer:
     expert e as device tensors; they are converted expert by expert into the
     layout the kernels read (MXFP8 codes + tiled scales, and for the backward
     the per-expert transposed copies), so the masters never need to be
-    resident all at once.
+    resident all at once.  Alternatively ``stacked=(W_gu [E, 2m, d], W_dn
+    [E, d, m])`` converts all experts with one launch per operand.
     """
 
-    def __init__(self, T, d, m, E, k, fmt, expert, shared=None, backward=False, device="cuda"):
+    def __init__(self, T, d, m, E, k, fmt, expert=None, shared=None, backward=False, device="cuda",
+                 stacked=None):
         self.T, self.d, self.m, self.E, self.k = T, d, m, E, k
         self.fmt = fmt
         self.mx = fmt == "mxfp8"
@@ -39,10 +41,10 @@ class MoELayer:
         self.Rp = moe_padded_rows(self.cfg)
         self.ws = _u8(moe_workspace_bytes(self.cfg), device)
         self.saved = _u8(moe_saved_bytes(self.cfg), device) if backward else None
-        self._prepare(expert, shared)
+        self._prepare(expert, shared, stacked)
 
     # ------------------------------------------------------------ weights
-    def _prepare(self, expert, shared):
+    def _prepare(self, expert, shared, stacked=None):
         d, m, E, dev = self.d, self.m, self.E, self.device
         t = {}
         if self.mx:
@@ -62,7 +64,22 @@ class MoELayer:
                 t["gu_t"] = torch.empty((E, d, 2 * m), dtype=torch.bfloat16, device=dev)
                 t["dn_t"] = torch.empty((E, m, d), dtype=torch.bfloat16, device=dev)
         gsz, dsz = 2 * m * d, d * m
-        for e in range(E):
+        if stacked is not None:
+            gu, dn = (w.contiguous() for w in stacked)
+            assert gu.shape == (E, 2 * m, d) and dn.shape == (E, d, m)
+            if self.mx:
+                check(moe_quantize_mx(gu, E, 2 * m, d, 0, t["gu"], t["gu_scale"]))
+                check(moe_quantize_mx(dn, E, d, m, 0, t["dn"], t["dn_scale"]))
+                if self.backward_enabled:
+                    check(moe_quantize_mx(gu, E, 2 * m, d, 1, t["gu_t"], t["gu_t_scale"]))
+                    check(moe_quantize_mx(dn, E, d, m, 1, t["dn_t"], t["dn_t_scale"]))
+            else:
+                t["gu"].copy_(gu)
+                t["dn"].copy_(dn)
+                if self.backward_enabled:
+                    check(moe_transpose_bf16(gu, E, 2 * m, d, t["gu_t"]))
+                    check(moe_transpose_bf16(dn, E, d, m, t["dn_t"]))
+        for e in range(E if stacked is None else 0):
             gu, dn = expert(e)
             assert gu.is_cuda and gu.dtype == torch.bfloat16 and gu.shape == (2 * m, d)
             assert dn.is_cuda and dn.dtype == torch.bfloat16 and dn.shape == (d, m)

@@ -114,6 +114,35 @@ def schedule(idx, E):
 
 
 # ----------------------------------------------------------------------------
+# 0. weight preparation (S0)
+# ----------------------------------------------------------------------------
+def prepare_expert(W_gu, W_dn, fmt, backward=True):
+    """Operands the expert GEMMs read, from the bf16 masters of one expert.
+
+    MXFP8 is the default expert format ("Mixture-of-Kittens" wiki page, Key
+    claims, MXFP8 bullet): the forward operands are W_gu [2m, d] and W_dn
+    [d, m] quantised along their K (d, m); the backward dgrad operands are
+    W_dn^T [m, d] quantised along d and W_gu^T [d, 2m] quantised along 2m.
+    Values are returned dequantised (float64).  Other formats use the masters.
+    """
+    W_gu = np.asarray(W_gu, dtype=np.float64)
+    W_dn = np.asarray(W_dn, dtype=np.float64)
+    if fmt == "mxfp8":
+        ops = dict(gu_fwd=mx_roundtrip(W_gu, axis=1), dn_fwd=mx_roundtrip(W_dn, axis=1))
+        if backward:
+            ops["dn_bwd"] = mx_roundtrip(W_dn.T, axis=1)
+            ops["gu_bwd"] = mx_roundtrip(W_gu.T, axis=1)
+    else:
+        ops = dict(gu_fwd=W_gu, dn_fwd=W_dn, dn_bwd=W_dn.T, gu_bwd=W_gu.T)
+    return ops
+
+
+def _unpack(item):
+    """experts[e] is (W_gu, W_dn) or (W_gu, W_dn, prepared operands)."""
+    return (item[0], item[1], item[2]) if len(item) == 3 else (item[0], item[1], None)
+
+
+# ----------------------------------------------------------------------------
 # 3./4. one expert
 # ----------------------------------------------------------------------------
 def _col_blocks(a):
@@ -124,22 +153,22 @@ def _col_blocks(a):
     return mx_roundtrip(ap, axis=0)[:n]
 
 
-def expert_forward(X, W_gu, W_dn, fmt):
+def expert_forward(X, W_gu, W_dn, fmt, ops=None):
     """SwiGLU FFN of one expert on its gathered rows.
 
     X [n, d] bf16 values; W_gu [2m, d] (gate rows first); W_dn [d, m].
     MXFP8: X, W_gu and W_dn are quantised along K (d, d, m); h is
-    quantised along m straight from the float64 SwiGLU output.
+    quantised along m straight from the float64 SwiGLU output.  ``ops`` are
+    the expert's prepared operands (:func:`prepare_expert`), computed here
+    when not given.
     Returns dict(G, U (unrounded), GU_saved [n, 2m], h_saved [n, m], o [n, d]).
     """
     m = W_gu.shape[0] // 2
     rnd = _rnd(fmt)
-    if fmt == "mxfp8":
-        Xq = mx_roundtrip(X, axis=1)
-        Wq = mx_roundtrip(W_gu, axis=1)
-        Dq = mx_roundtrip(W_dn, axis=1)
-    else:
-        Xq, Wq, Dq = X, W_gu, W_dn
+    if ops is None:
+        ops = prepare_expert(W_gu, W_dn, fmt, backward=False)
+    Xq = mx_roundtrip(X, axis=1) if fmt == "mxfp8" else X
+    Wq, Dq = ops["gu_fwd"], ops["dn_fwd"]
     G = Xq @ Wq[:m].T
     U = Xq @ Wq[m:].T
     h = silu(G) * U
@@ -184,8 +213,8 @@ def forward(x, logits, experts, k, fmt, shared=None):
         r0, r1 = int(offsets[e]), int(offsets[e + 1])
         if r1 == r0:
             continue
-        W_gu, W_dn = experts[e]
-        res = expert_forward(x[row_tok[r0:r1]], W_gu, W_dn, fmt)
+        W_gu, W_dn, ops = _unpack(experts[e])
+        res = expert_forward(x[row_tok[r0:r1]], W_gu, W_dn, fmt, ops)
         if GU is None:
             m = W_gu.shape[0] // 2
             GU = np.zeros((R, 2 * m))
@@ -220,7 +249,7 @@ def swiglu_backward(dh, G, U):
     return dG, dU
 
 
-def expert_backward(dO, X, GU, h, W_gu, W_dn, fmt):
+def expert_backward(dO, X, GU, h, W_gu, W_dn, fmt, ops=None):
     """Backward of one expert on its rows.
 
     dO [n, d] bf16 values (w * dy), X [n, d], GU [n, 2m] and h [n, m] saved
@@ -231,20 +260,22 @@ def expert_backward(dO, X, GU, h, W_gu, W_dn, fmt):
     """
     m = W_gu.shape[0] // 2
     rnd = _rnd(fmt)
+    if ops is None or "dn_bwd" not in ops:
+        ops = prepare_expert(W_gu, W_dn, fmt, backward=True)
     G, U = GU[:, :m], GU[:, m:]
     if fmt == "mxfp8":
-        dh = mx_roundtrip(dO, axis=1) @ mx_roundtrip(W_dn.T, axis=1).T
+        dh = mx_roundtrip(dO, axis=1) @ ops["dn_bwd"].T
     else:
-        dh = dO @ W_dn
+        dh = dO @ ops["dn_bwd"].T
     dG, dU = swiglu_backward(dh, G, U)
     dGU = rnd(np.concatenate([dG, dU], axis=1))
     if fmt == "mxfp8":
         dW_dn = _col_blocks(dO).T @ _col_blocks(h)
-        dX = mx_roundtrip(dGU, axis=1) @ mx_roundtrip(W_gu.T, axis=1).T
+        dX = mx_roundtrip(dGU, axis=1) @ ops["gu_bwd"].T
         dW_gu = _col_blocks(dGU).T @ _col_blocks(X)
     else:
         dW_dn = dO.T @ h
-        dX = dGU @ W_gu
+        dX = dGU @ ops["gu_bwd"].T
         dW_gu = dGU.T @ X
     return dict(dX=rnd(dX), dW_gu=rnd(dW_gu), dW_dn=rnd(dW_dn), dGU=dGU, dh=dh)
 
@@ -283,14 +314,15 @@ def backward(dy, x, experts, k, fmt, saved, shared=None, dw_experts=None):
     want = set(range(E)) if dw_experts is None else set(dw_experts)
     for e in range(E):
         r0, r1 = int(offsets[e]), int(offsets[e + 1])
-        W_gu, W_dn = experts[e] if (r1 > r0 or e in want) else (None, None)
         if r1 == r0:
             if e in want:
+                W_gu, W_dn, _ = _unpack(experts[e])
                 dW_gu[e] = np.zeros_like(W_gu)
                 dW_dn[e] = np.zeros_like(W_dn)
             continue
+        W_gu, W_dn, ops = _unpack(experts[e])
         res = expert_backward(dO[r0:r1], x[row_tok[r0:r1]], saved["GU"][r0:r1],
-                              saved["h"][r0:r1], W_gu, W_dn, fmt)
+                              saved["h"][r0:r1], W_gu, W_dn, fmt, ops)
         dX[r0:r1] = res["dX"]
         if e in want:
             dW_gu[e] = res["dW_gu"]

@@ -277,3 +277,22 @@ def test_column_blocks_zero_pad():
     a = rng.standard_normal((45, 32))
     ap = np.concatenate([a, np.zeros((19, 32))])
     assert np.array_equal(om._col_blocks(a), nx.mx_roundtrip(ap, axis=0)[:45])
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "mxfp8"])
+def test_prepared_operands_change_nothing(fmt):
+    """Weight preparation (S0) done ahead of time gives bit-identical results."""
+    rng = np.random.default_rng(16)
+    T, d, m, E, k = 37, 64, 32, 4, 2
+    x, logits, experts, _ = rand_layer(rng, T, d, m, E, k)
+    dy = nx.bf16_round(rng.standard_normal((T, d)))
+    prepped = [(g, n, om.prepare_expert(g, n, fmt)) for g, n in experts]
+    y1, s1 = om.forward(x, logits, experts, k, fmt)
+    y2, s2 = om.forward(x, logits, prepped, k, fmt)
+    assert np.array_equal(y1, y2)
+    g1 = om.backward(dy, x, experts, k, fmt, s1)
+    g2 = om.backward(dy, x, prepped, k, fmt, s2)
+    for key in ("dx", "dlogits"):
+        assert np.array_equal(g1[key], g2[key])
+    for e in g1["dW_gu"]:
+        assert np.array_equal(g1["dW_gu"][e], g2["dW_gu"][e]) and np.array_equal(g1["dW_dn"][e], g2["dW_dn"][e])
