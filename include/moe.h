@@ -192,6 +192,30 @@ int moe_backward(const moe_config *cfg, const void *dy, const void *x, const moe
                  const void *saved, void *dx, float *dlogits, void *dW_gu, void *dW_dn,
                  void *dWs_gu, void *dWs_dn, void *ws, moe_stream_t stream);
 
+/*
+ * Router top-k + schedule without a workspace, for callers that cannot call
+ * cudaMalloc: code inside a host framework that owns every device byte through
+ * its own arena, or a latency-critical path on which an allocation (which can
+ * synchronise the device) is not acceptable.  The pages have no counterpart:
+ * this is an extra entry point of this library, not a step of the method.
+ * Computes exactly what moe_route computes (same kernels, same bits); all
+ * seven pointers are required (no output can stay in a workspace).
+ * Scratch: a fixed array in the library's device memory, sized for at most
+ * MOE_ROUTE_NOALLOC_MAX_SLOTS routed slots (T*k) and
+ * MOE_ROUTE_NOALLOC_MAX_EXPERTS experts (about 2 MiB, held by every GPU that
+ * loads the library until the process exits); larger shapes return
+ * MOE_ERR_SHAPE.  Every call shares that array and leaves its contents behind
+ * (nothing in it needs to start at zero): calls that overlap on the GPU (on
+ * different streams, or from several host threads) race and corrupt each
+ * other's results.  Calls on one stream are ordered and safe.  The first call
+ * on a device looks up the array's device address (cudaGetSymbolAddress); make
+ * that first call before any stream capture.  Allocates nothing.
+ */
+#define MOE_ROUTE_NOALLOC_MAX_SLOTS 262144
+#define MOE_ROUTE_NOALLOC_MAX_EXPERTS 1024
+int moe_route_noalloc(const moe_config *cfg, const float *logits, int32_t *idx, float *w,
+                      int32_t *counts, int32_t *offsets, int32_t *perm, moe_stream_t stream);
+
 /* Synchronises `stream`, returns the device status word recorded in `ws`
  * (MOE_OK or MOE_ERR_TIMEOUT) and clears it.  Returns MOE_ERR_CUDA if the
  * stream reports a CUDA error. */

@@ -35,7 +35,7 @@ _lib = None
 EXPORTS = ["moe_workspace_bytes", "moe_saved_bytes", "moe_buffer_info", "moe_padded_rows",
            "moe_quantize_mx", "moe_transpose_bf16", "moe_route", "moe_forward", "moe_backward",
            "moe_get_status", "moe_status_string", "moe_trace_enable", "moe_trace_clear", "moe_trace_count",
-           "moe_trace_name", "moe_trace_ms"]
+           "moe_trace_name", "moe_trace_ms", "moe_route_noalloc"]
 
 
 def lib():
@@ -62,6 +62,7 @@ def lib():
         L.moe_backward.restype = I
         L.moe_get_status.argtypes, L.moe_get_status.restype = [P, S], I
         L.moe_status_string.argtypes, L.moe_status_string.restype = [I], ctypes.c_char_p
+        L.moe_route_noalloc.argtypes, L.moe_route_noalloc.restype = [cfgp, P, P, P, P, P, P, S], I
         L.moe_trace_enable.argtypes, L.moe_trace_enable.restype = [I], I
         L.moe_trace_clear.argtypes, L.moe_trace_clear.restype = [], None
         L.moe_trace_count.argtypes, L.moe_trace_count.restype = [], I
@@ -138,6 +139,11 @@ def moe_transpose_bf16(src, batch, rows, cols, dst, stream=None):
 def moe_route(cfg, logits, idx, w, counts, offsets, perm, ws, stream=None):
     return lib().moe_route(ctypes.byref(cfg), _ptr(logits), _ptr(idx), _ptr(w), _ptr(counts), _ptr(offsets),
                            _ptr(perm), _ptr(ws), _stream(stream))
+
+
+def moe_route_noalloc(cfg, logits, idx, w, counts, offsets, perm, stream=None):
+    return lib().moe_route_noalloc(ctypes.byref(cfg), _ptr(logits), _ptr(idx), _ptr(w), _ptr(counts),
+                                   _ptr(offsets), _ptr(perm), _stream(stream))
 
 
 def moe_forward(cfg, x, logits, W, y, saved, ws, stream=None):
