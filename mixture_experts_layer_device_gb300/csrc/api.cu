@@ -202,6 +202,22 @@ bool make_map(CUtensorMap *m, const void *base, bool bytes1, uint64_t inner, uin
   return r == CUDA_SUCCESS;
 }
 
+// 2-D map for the epilogue's TMA stores: `rows` rows of `inner` elements, row
+// stride `ld` elements, box 32 rows x 64 bytes, 64-byte swizzle.
+bool make_store_map(CUtensorMap *m, const void *base, bool bytes1, uint64_t inner, uint64_t ld,
+                    uint64_t rows) {
+  const uint64_t esz = bytes1 ? 1 : 2;
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {ld * esz};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(64 / esz), 32};
+  cuuint32_t estr[2] = {1, 1};
+  const CUresult r = g_encode(m, bytes1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                              2, const_cast<void *>(base), dims, strides, box, estr,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // ---------------------------------------------------------------- tracing
@@ -240,7 +256,8 @@ struct Traced {
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
-// One GEMM launch: A [a_rows, K] and B [b_rows, K] (K-major) plus arguments.
+// One GEMM launch: A [a_rows, K] and B [b_rows, K] (K-major) plus arguments;
+// the outputs (g.out / out2 / outq) have out_rows rows.
 struct Gemm {
   bool mx;
   int bn, epi;
@@ -251,15 +268,25 @@ struct Gemm {
   long K;
   GemmArgs g;
   long max_tiles;
+  long out_rows;
 };
 
 int run_gemm(const char *name, const Gemm &q, const DeviceInfo &dev, cudaStream_t s) {
   Traced tr(name, s);
-  CUtensorMap ta, tb;
+  CUtensorMap ta, tb, to, to2, tq;
+  memset(&to, 0, sizeof(to));
+  memset(&to2, 0, sizeof(to2));
+  memset(&tq, 0, sizeof(tq));
   if (!make_map(&ta, q.a, q.mx, q.K, q.a_rows) || !make_map(&tb, q.b, q.mx, q.K, q.b_rows))
     return MOE_ERR_CUDA;
+  // Output widths: the stored row length is the row stride for every output.
+  if (q.g.out && !make_store_map(&to, q.g.out, false, q.g.ldo, q.g.ldo, q.out_rows)) return MOE_ERR_CUDA;
+  if (q.g.out2 && !make_store_map(&to2, q.g.out2, false, q.g.ldo2, q.g.ldo2, q.out_rows))
+    return MOE_ERR_CUDA;
+  if (q.g.outq && !make_store_map(&tq, q.g.outq, true, q.g.ldq, q.g.ldq, q.out_rows)) return MOE_ERR_CUDA;
   const long grid = q.max_tiles < dev.num_sms ? q.max_tiles : dev.num_sms;
-  return cuda_status(moe::launch_gemm(q.mx, q.bn, q.epi, ta, tb, q.g, static_cast<int>(grid), s));
+  return cuda_status(
+      moe::launch_gemm(q.mx, q.bn, q.epi, ta, tb, to, to2, tq, q.g, static_cast<int>(grid), s));
 }
 
 int bn_for(long n) { return n % 256 == 0 ? 256 : 128; }
@@ -455,6 +482,7 @@ int moe_forward(const moe_config *cfg, const void *x, const float *logits, const
     q.g.ldq = D.m;
     q.g.m_half = D.m;
     q.max_tiles = (D.Rp / 128) * q.g.n_tiles;
+    q.out_rows = D.Rp;
     if ((rc = run_gemm("gemm1_gate_up_swiglu", q, dev, s)) != MOE_OK) return rc;
   }
   // S5 down GEMM
@@ -479,6 +507,7 @@ int moe_forward(const moe_config *cfg, const void *x, const float *logits, const
     q.g.out = o;
     q.g.ldo = D.d;
     q.max_tiles = (D.Rp / 128) * q.g.n_tiles;
+    q.out_rows = D.Rp;
     if ((rc = run_gemm("gemm2_down", q, dev, s)) != MOE_OK) return rc;
   }
   // S7 shared expert (BF16, dense over all tokens)
@@ -508,6 +537,7 @@ int moe_forward(const moe_config *cfg, const void *x, const float *logits, const
     q.g.ldo2 = 2 * D.ms;
     q.g.m_half = D.ms;
     q.max_tiles = (D.Tp / 128) * q.g.n_tiles;
+    q.out_rows = D.Tp;
     if ((rc = run_gemm("shared_gemm1_gate_up_swiglu", q, dev, s)) != MOE_OK) return rc;
     Gemm q2;
     q2.mx = false;
@@ -526,6 +556,7 @@ int moe_forward(const moe_config *cfg, const void *x, const float *logits, const
     q2.g.out = s_out;
     q2.g.ldo = D.d;
     q2.max_tiles = (D.Tp / 128) * q2.g.n_tiles;
+    q2.out_rows = D.Tp;
     if ((rc = run_gemm("shared_gemm2_down", q2, dev, s)) != MOE_OK) return rc;
   }
   // S6 combine
@@ -607,6 +638,7 @@ int moe_backward(const moe_config *cfg, const void *dy, const void *x, const moe
     q.g.ld_aux = 2 * D.m;
     q.g.m_half = D.m;
     q.max_tiles = (D.Rp / 128) * q.g.n_tiles;
+    q.out_rows = D.Rp;
     if ((rc = run_gemm("dgrad_down_swiglu_bwd", q, dev, s)) != MOE_OK) return rc;
   }
   // B4 dgrad of the gate/up projection
@@ -631,6 +663,7 @@ int moe_backward(const moe_config *cfg, const void *dy, const void *x, const moe
     q.g.out = dX;
     q.g.ldo = D.d;
     q.max_tiles = (D.Rp / 128) * q.g.n_tiles;
+    q.out_rows = D.Rp;
     if ((rc = run_gemm("dgrad_gate_up", q, dev, s)) != MOE_OK) return rc;
   }
   // Transposed (column-blocked for MX) wgrad operands, K = padded rows.
@@ -673,6 +706,7 @@ int moe_backward(const moe_config *cfg, const void *dy, const void *x, const moe
     q.g.out = dW_dn;
     q.g.ldo = D.m;
     q.max_tiles = static_cast<long>(D.E) * (D.d / 128) * q.g.n_tiles;
+    q.out_rows = static_cast<long>(D.E) * (D.d);
     if ((rc = run_gemm("wgrad_down", q, dev, s)) != MOE_OK) return rc;
   }
   // B5 wgrad of the gate/up projection: dW_gu[e] = dGU_e^T X_e
@@ -696,6 +730,7 @@ int moe_backward(const moe_config *cfg, const void *dy, const void *x, const moe
     q.g.out = dW_gu;
     q.g.ldo = D.d;
     q.max_tiles = static_cast<long>(D.E) * (2 * D.m / 128) * q.g.n_tiles;
+    q.out_rows = static_cast<long>(D.E) * (2 * D.m);
     if ((rc = run_gemm("wgrad_gate_up", q, dev, s)) != MOE_OK) return rc;
   }
   // B7 shared expert backward (BF16, dense)
@@ -726,6 +761,7 @@ int moe_backward(const moe_config *cfg, const void *dy, const void *x, const moe
       q.g.ld_aux = 2 * D.ms;
       q.g.m_half = D.ms;
       q.max_tiles = (D.Tp / 128) * q.g.n_tiles;
+      q.out_rows = D.Tp;
       if ((rc = run_gemm("shared_dgrad_down_swiglu_bwd", q, dev, s)) != MOE_OK) return rc;
     }
     {
@@ -746,6 +782,7 @@ int moe_backward(const moe_config *cfg, const void *dy, const void *x, const moe
       q.g.out = s_dx;
       q.g.ldo = D.d;
       q.max_tiles = (D.Tp / 128) * q.g.n_tiles;
+      q.out_rows = D.Tp;
       if ((rc = run_gemm("shared_dgrad_gate_up", q, dev, s)) != MOE_OK) return rc;
     }
     struct TrS {
@@ -783,6 +820,7 @@ int moe_backward(const moe_config *cfg, const void *dy, const void *x, const moe
       q.g.out = dWs_dn;
       q.g.ldo = D.ms;
       q.max_tiles = (D.d / 128) * q.g.n_tiles;
+      q.out_rows = static_cast<long>(1) * (D.d);
       if ((rc = run_gemm("shared_wgrad_down", q, dev, s)) != MOE_OK) return rc;
     }
     {
@@ -802,6 +840,7 @@ int moe_backward(const moe_config *cfg, const void *dy, const void *x, const moe
       q.g.out = dWs_gu;
       q.g.ldo = D.d;
       q.max_tiles = (2L * D.ms / 128) * q.g.n_tiles;
+      q.out_rows = static_cast<long>(1) * (2 * D.ms);
       if ((rc = run_gemm("shared_wgrad_gate_up", q, dev, s)) != MOE_OK) return rc;
     }
   }

@@ -48,10 +48,12 @@ struct Cfg {
   static constexpr int SFB_COL = SFA_COL + 4;
   static constexpr uint32_t TX_BYTES = STAGE_BYTES + SF_STAGE;
   static constexpr uint32_t IDESC = MX ? idesc_mxf8(128, BN) : idesc_bf16(128, BN);
+  // epilogue staging: per epilogue warp two 2 KB halves (32 rows x 64 B, 64-byte swizzle)
+  static constexpr int STAGING_BYTES = 4 * 4096;
   // barriers: full[S], empty[S], tfull[NA], tempty[NA], done
   static constexpr int NBAR = 2 * STAGES + 2 * NUM_ACC + 1;
-  static constexpr size_t SMEM =
-      1024 + static_cast<size_t>(STAGES) * (STAGE_BYTES + SF_STAGE) + NBAR * 8 + 16;
+  static constexpr size_t SMEM = 1024 + static_cast<size_t>(STAGES) * (STAGE_BYTES + SF_STAGE) +
+                                 STAGING_BYTES + NBAR * 8 + 16;
   static_assert(!MX || SFB_COL + BN / 32 <= 512, "TMEM columns");
   static_assert(NUM_ACC * BN <= 512, "TMEM columns");
   static_assert(SMEM <= 232448, "shared memory");
@@ -124,14 +126,6 @@ MOE_DEV Tile decode_tile(const GemmArgs &g, int t) {
   return ti;
 }
 
-MOE_DEV void store_bf16x32(void *base, long row, long ld, long col, const float *v) {
-  uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(base) + row * ld + col);
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-    dst[i] = make_uint4(pack_bf16x2(v[8 * i], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
-                        pack_bf16x2(v[8 * i + 4], v[8 * i + 5]),
-                        pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
-}
 MOE_DEV void load_bf16x32(const void *base, long row, long ld, long col, float *v) {
   const uint4 *src =
       reinterpret_cast<const uint4 *>(reinterpret_cast<const __nv_bfloat16 *>(base) + row * ld + col);
@@ -144,30 +138,79 @@ MOE_DEV void load_bf16x32(const void *base, long row, long ld, long col, float *
     v[8 * i + 6] = bf16lo(q.w); v[8 * i + 7] = bf16hi(q.w);
   }
 }
-// MX-quantise 32 values held by one thread (one block) and store codes + scale.
-MOE_DEV void store_mx32(uint8_t *codes, uint8_t *sf, long row, long ld, long col, const float *v) {
+
+// 32 floats -> 16 words of bf16 pairs (round to nearest even).
+MOE_DEV void bf16x32_words(const float *v, uint32_t *w) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+}
+
+// MX block of 32 values owned by this thread -> 8 code words; returns the scale byte.
+MOE_DEV uint32_t mx_block_words(const float *v, uint32_t *w) {
   float am = 0.f;
 #pragma unroll
   for (int i = 0; i < 32; ++i) am = fmaxf(am, fabsf(v[i]));
   const uint32_t byte = mx_scale_byte(am);
-  uint32_t w[8];
   mx_encode32(v, byte, w);
-  uint4 *dst = reinterpret_cast<uint4 *>(codes + row * ld + col);
-  dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-  dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-  sf[sf_tiled_offset(row, col / 32, ld)] = static_cast<uint8_t>(byte);
+  return byte;
+}
+
+// Per-warp writer of 32-row x 64-byte output pieces: each lane places its row's
+// 64 bytes in a 64-byte-swizzled shared-memory half (conflict-free), then one
+// lane stores the box with TMA.  Two halves alternate so the staging of one
+// piece overlaps the store of the previous one.
+struct Stager {
+  uint8_t *buf;  // 4 KB, 512-byte aligned
+  int n;
+  MOE_DEV void put(const CUtensorMap *map, const uint32_t *w16, int c0, int row0, int lane) {
+    uint8_t *half = buf + (n & 1) * 2048;
+    if (n >= 2 && lane == 0) bulk_wait_read<1>();
+    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int jj = j ^ ((lane >> 1) & 3);
+      *reinterpret_cast<uint4 *>(half + lane * 64 + jj * 16) =
+          make_uint4(w16[4 * j], w16[4 * j + 1], w16[4 * j + 2], w16[4 * j + 3]);
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_2d(map, half, c0, row0);
+      bulk_commit();
+    }
+    ++n;
+  }
+  MOE_DEV void put_bf16(const CUtensorMap *map, const float *v32, int c0, int row0, int lane) {
+    uint32_t w[16];
+    bf16x32_words(v32, w);
+    put(map, w, c0, row0, lane);
+  }
+};
+
+// Two MX blocks (64 values) of one row -> one 64-byte codes piece + 2 scale bytes.
+MOE_DEV void put_mx64(Stager &st, const CUtensorMap *map, uint8_t *sf, long ldq, const float *v64,
+                      int col, int row0, long grow, int lane) {
+  uint32_t w[16];
+  const uint32_t b0 = mx_block_words(v64, w);
+  const uint32_t b1 = mx_block_words(v64 + 32, w + 8);
+  st.put(map, w, col, row0, lane);
+  // (col / 32) is even, so both bytes sit next to each other in one 512-byte atom.
+  *reinterpret_cast<uint16_t *>(sf + sf_tiled_offset(grow, col / 32, ldq)) =
+      static_cast<uint16_t>(b0 | (b1 << 8));
 }
 
 template <bool MX, int BN, int EPI>
 __global__ void __launch_bounds__(192, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                const GemmArgs g) {
+                const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmO2,
+                const __grid_constant__ CUtensorMap tmQ, const GemmArgs g) {
   using C = Cfg<MX, BN>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
   uint8_t *sf_base = smem + C::STAGES * C::STAGE_BYTES;
-  uint64_t *bars = reinterpret_cast<uint64_t *>(sf_base + C::STAGES * C::SF_STAGE);
+  uint8_t *staging = sf_base + C::STAGES * C::SF_STAGE;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(staging + C::STAGING_BYTES);
   uint64_t *full = bars;
   uint64_t *empty = bars + C::STAGES;
   uint64_t *tfull = bars + 2 * C::STAGES;
@@ -310,6 +353,12 @@ __global__ void __launch_bounds__(192, 1)
     // ------------------------------------------------ epilogue (warps 2..5)
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int r = q * 32 + lane;
+    Stager st{staging + (warp - 2) * 4096, 0};
+    if (lane == 0) {
+      if (g.out) prefetch_tensormap(&tmO);
+      if (g.out2) prefetch_tensormap(&tmO2);
+      if (g.outq) prefetch_tensormap(&tmQ);
+    }
     int acc = 0;
     uint32_t aph = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
@@ -318,70 +367,121 @@ __global__ void __launch_bounds__(192, 1)
       tc_fence_after();
       const uint32_t tb =
           tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
+      const int row0 = ti.out_row + q * 32;  // first output row of this warp
       const long grow = ti.out_row + r;
+      auto release = [&]() {
+        tc_fence_before();
+        mbar_arrive(&tempty[acc]);
+      };
       if constexpr (EPI == EPI_STORE) {
-#pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-          float v[32];
-          if (ti.nk > 0) {
-            tmem_ld32(tb + 32 * c, v);
-            tmem_ld_wait();
-          } else {
+        constexpr int NCH = BN / 64;
+        if (ti.nk == 0) {  // empty reduction (an expert with no rows): zeros
+          release();
+          float z[32];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = 0.f;
+          for (int i = 0; i < 32; ++i) z[i] = 0.f;
+#pragma unroll 1
+          for (int c = 0; c < 2 * NCH; ++c) st.put_bf16(&tmO, z, ti.out_col + 32 * c, row0, lane);
+        } else {
+          // Software pipeline: the TMEM load of chunk c+1 is in flight while
+          // chunk c is converted and staged; TMEM is released once the last
+          // chunk has been read.
+          uint32_t buf[2][64];
+          tmem_ld32_async(tb, buf[0]);
+          tmem_ld32_async(tb + 32, buf[0] + 32);
+          tmem_ld_wait();
+          reg_fence<64>(buf[0]);
+#pragma unroll
+          for (int c = 0; c < NCH; ++c) {
+            uint32_t *cur = buf[c & 1];
+            if (c + 1 < NCH) {
+              tmem_ld32_async(tb + 64 * (c + 1), buf[(c + 1) & 1]);
+              tmem_ld32_async(tb + 64 * (c + 1) + 32, buf[(c + 1) & 1] + 32);
+            } else {
+              release();
+            }
+            st.put_bf16(&tmO, reinterpret_cast<const float *>(cur), ti.out_col + 64 * c, row0, lane);
+            st.put_bf16(&tmO, reinterpret_cast<const float *>(cur + 32), ti.out_col + 64 * c + 32, row0,
+                        lane);
+            if (c + 1 < NCH) {
+              tmem_ld_wait();
+              reg_fence<64>(buf[(c + 1) & 1]);
+            }
           }
-          store_bf16x32(g.out, grow, g.ldo, ti.out_col + 32 * c, v);
         }
       } else if constexpr (EPI == EPI_SWIGLU) {
+        // accumulator columns [0,128) = gate G, [128,256) = up U of 128 h columns
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          float gv[32], uv[32];
-          tmem_ld32(tb + 32 * c, gv);
-          tmem_ld32(tb + 128 + 32 * c, uv);
+        for (int c = 0; c < 2; ++c) {
+          uint32_t gr[64], ur[64];
+          tmem_ld32_async(tb + 64 * c, gr);
+          tmem_ld32_async(tb + 64 * c + 32, gr + 32);
+          tmem_ld32_async(tb + 128 + 64 * c, ur);
+          tmem_ld32_async(tb + 128 + 64 * c + 32, ur + 32);
           tmem_ld_wait();
-          const long col = ti.out_col + 32 * c;
+          reg_fence<64>(gr);
+          reg_fence<64>(ur);
+          if (c == 1) release();
+          float *G = reinterpret_cast<float *>(gr);
+          float *U = reinterpret_cast<float *>(ur);
+          const int col = ti.out_col + 64 * c;
           if (g.out2) {
-            store_bf16x32(g.out2, grow, g.ldo2, col, gv);
-            store_bf16x32(g.out2, grow, g.ldo2, g.m_half + col, uv);
+            st.put_bf16(&tmO2, G, col, row0, lane);
+            st.put_bf16(&tmO2, G + 32, col + 32, row0, lane);
+            st.put_bf16(&tmO2, U, g.m_half + col, row0, lane);
+            st.put_bf16(&tmO2, U + 32, g.m_half + col + 32, row0, lane);
           }
-          float h[32];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) h[i] = silu(gv[i]) * uv[i];
-          if (g.out) store_bf16x32(g.out, grow, g.ldo, col, h);
-          if (g.outq) store_mx32(g.outq, g.outq_sf, grow, g.ldq, col, h);
+          for (int i = 0; i < 64; ++i) G[i] = silu(G[i]) * U[i];  // h, in place
+          if (g.out) {
+            st.put_bf16(&tmO, G, col, row0, lane);
+            st.put_bf16(&tmO, G + 32, col + 32, row0, lane);
+          }
+          if (g.outq) put_mx64(st, &tmQ, g.outq_sf, g.ldq, G, col, row0, grow, lane);
         }
-      } else {  // EPI_SWIGLU_BWD
+      } else {  // EPI_SWIGLU_BWD: accumulator = dh; G|U saved in bf16
+        constexpr int NCH = BN / 64;
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-          float dh[32], G[32], U[32];
-          tmem_ld32(tb + 32 * c, dh);
+        for (int c = 0; c < NCH; ++c) {
+          uint32_t hr[64];
+          tmem_ld32_async(tb + 64 * c, hr);
+          tmem_ld32_async(tb + 64 * c + 32, hr + 32);
           tmem_ld_wait();
-          const long col = ti.out_col + 32 * c;
-          load_bf16x32(g.aux, grow, g.ld_aux, col, G);
-          load_bf16x32(g.aux, grow, g.ld_aux, g.m_half + col, U);
+          reg_fence<64>(hr);
+          if (c == NCH - 1) release();
+          const float *dh = reinterpret_cast<const float *>(hr);
+          const int col = ti.out_col + 64 * c;
+          float dG[64], dU[64];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const float s = sigmoidf(G[i]);
-            const float dg = round_bf16(dh[i] * U[i] * s * (1.0f + G[i] * (1.0f - s)));
-            const float du = round_bf16(dh[i] * G[i] * s);
-            G[i] = dg;
-            U[i] = du;
+          for (int hh = 0; hh < 2; ++hh) {
+            float G[32], U[32];
+            load_bf16x32(g.aux, grow, g.ld_aux, col + 32 * hh, G);
+            load_bf16x32(g.aux, grow, g.ld_aux, g.m_half + col + 32 * hh, U);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const float d = dh[32 * hh + i];
+              const float sg = sigmoidf(G[i]);
+              dG[32 * hh + i] = round_bf16(d * U[i] * sg * (1.0f + G[i] * (1.0f - sg)));
+              dU[32 * hh + i] = round_bf16(d * G[i] * sg);
+            }
           }
-          store_bf16x32(g.out, grow, g.ldo, col, G);
-          store_bf16x32(g.out, grow, g.ldo, g.m_half + col, U);
+          st.put_bf16(&tmO, dG, col, row0, lane);
+          st.put_bf16(&tmO, dG + 32, col + 32, row0, lane);
+          st.put_bf16(&tmO, dU, g.m_half + col, row0, lane);
+          st.put_bf16(&tmO, dU + 32, g.m_half + col + 32, row0, lane);
           if (g.outq) {
-            store_mx32(g.outq, g.outq_sf, grow, g.ldq, col, G);
-            store_mx32(g.outq, g.outq_sf, grow, g.ldq, g.m_half + col, U);
+            put_mx64(st, &tmQ, g.outq_sf, g.ldq, dG, col, row0, grow, lane);
+            put_mx64(st, &tmQ, g.outq_sf, g.ldq, dU, g.m_half + col, row0, grow, lane);
           }
         }
       }
-      tc_fence_before();
-      mbar_arrive(&tempty[acc]);
       if (++acc == C::NUM_ACC) {
         acc = 0;
         aph ^= 1u;
       }
     }
+    if (lane == 0) bulk_wait<0>();  // every TMA store of this warp has landed
+    __syncwarp();
   }
 
   __syncthreads();
@@ -392,7 +492,8 @@ __global__ void __launch_bounds__(192, 1)
 }
 
 template <bool MX, int BN, int EPI>
-cudaError_t launch_one(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs &g, int grid,
+cudaError_t launch_one(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &to,
+                       const CUtensorMap &to2, const CUtensorMap &tq, const GemmArgs &g, int grid,
                        cudaStream_t s) {
   using C = Cfg<MX, BN>;
   static bool attr_set = false;  // per instantiation; idempotent, benign if repeated
@@ -403,17 +504,19 @@ cudaError_t launch_one(const CUtensorMap &ta, const CUtensorMap &tb, const GemmA
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  gemm_kernel<MX, BN, EPI><<<grid, 192, C::SMEM, s>>>(ta, tb, g);
+  gemm_kernel<MX, BN, EPI><<<grid, 192, C::SMEM, s>>>(ta, tb, to, to2, tq, g);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_gemm(bool mx, int bn, int epi, const CUtensorMap &ta, const CUtensorMap &tb,
+                        const CUtensorMap &to, const CUtensorMap &to2, const CUtensorMap &tq,
                         const GemmArgs &g, int grid, cudaStream_t s) {
   if (grid <= 0) return cudaSuccess;
 #define MOE_GEMM_CASE(MXV, BNV, EPIV) \
-  if (mx == MXV && bn == BNV && epi == EPIV) return launch_one<MXV, BNV, EPIV>(ta, tb, g, grid, s);
+  if (mx == MXV && bn == BNV && epi == EPIV)  \
+    return launch_one<MXV, BNV, EPIV>(ta, tb, to, to2, tq, g, grid, s);
   MOE_GEMM_CASE(false, 256, EPI_STORE)
   MOE_GEMM_CASE(false, 128, EPI_STORE)
   MOE_GEMM_CASE(false, 256, EPI_SWIGLU)

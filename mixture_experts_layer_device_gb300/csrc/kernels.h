@@ -101,7 +101,11 @@ struct GemmArgs {
 // D = A * B^T with A [rows, K] and B [rows, K] K-major (TMA maps built by the
 // caller, box = 128 rows x 128 bytes, 128-byte swizzle); bn = 128 or 256
 // output columns per tile; `grid` persistent CTAs (<= number of SMs).
+// Outputs are written with TMA stores through maps of box 32 rows x 64 bytes
+// with the 64-byte swizzle: `to` for args.out, `to2` for args.out2, `tq` for
+// args.outq (unused maps may be zero-filled).
 cudaError_t launch_gemm(bool mx, int bn, int epi, const CUtensorMap &ta, const CUtensorMap &tb,
+                        const CUtensorMap &to, const CUtensorMap &to2, const CUtensorMap &tq,
                         const GemmArgs &args, int grid, cudaStream_t s);
 
 }  // namespace moe
