@@ -614,7 +614,7 @@ int moe_backward(const moe_config *cfg, const void *dy, const void *x, const moe
   {
     Gemm q;
     q.mx = mx;
-    q.bn = bn_for(D.m);
+    q.bn = mx ? 128 : bn_for(D.m);  // MXFP8: N=128 tiles leave TMEM for two accumulators
     q.epi = moe::EPI_SWIGLU_BWD;
     q.a = mx ? static_cast<const void *>(u8("dOq")) : dO;
     q.a_rows = D.Rp;

@@ -124,6 +124,10 @@ MOE_DEV void bulk_wait() {
 MOE_DEV void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
+// Asynchronous prefetch of `bytes` (multiple of 16, 16-byte aligned) into L2.
+MOE_DEV void bulk_prefetch_l2(const void *src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
 MOE_DEV void prefetch_tensormap(const CUtensorMap *map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
 }

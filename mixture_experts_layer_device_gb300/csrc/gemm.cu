@@ -363,6 +363,14 @@ __global__ void __launch_bounds__(192, 1)
     uint32_t aph = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
       const Tile ti = decode_tile<C::BK, BN, EPI>(g, t);
+      if constexpr (EPI == EPI_SWIGLU_BWD) {
+        // The saved G|U rows this tile's epilogue reads come from HBM: pull them
+        // into L2 while the main loop runs.
+        const long prow = ti.out_row + r;
+        const __nv_bfloat16 *gu = reinterpret_cast<const __nv_bfloat16 *>(g.aux) + prow * g.ld_aux;
+        bulk_prefetch_l2(gu + ti.out_col, BN * 2);
+        bulk_prefetch_l2(gu + g.m_half + ti.out_col, BN * 2);
+      }
       if (!mbar_wait(&tfull[acc], aph, abort_flag, g.status)) break;
       tc_fence_after();
       const uint32_t tb =
