@@ -82,3 +82,34 @@ def unpack_tiled_scales(sf, rows, K):
     b = np.arange(K // 32)[None, :]
     off = ((r // 128) * (K // 128) + b // 4) * 512 + (r % 32) * 16 + ((r % 128) // 32) * 4 + (b % 4)
     return sf[off]
+
+
+# ---------------------------------------------------------------- full-size sampling
+def _prep_worker(args):
+    e, gu, dn, fmt, backward = args
+    return e, om.prepare_expert(gu.astype(np.float64), dn.astype(np.float64), fmt, backward)
+
+
+class ExpertSubset:
+    """experts[e] for the oracle holding only some experts (weights + prepared operands)."""
+
+    def __init__(self, E, table):
+        self.E, self.t = E, table
+
+    def __len__(self):
+        return self.E
+
+    def __getitem__(self, e):
+        return self.t[e]
+
+
+def prepare_subset(cfg, gu_all, dn_all, experts, backward):
+    """Oracle S0 for a few experts of device-resident bf16 masters (spawned worker pool)."""
+    import multiprocessing as mp
+    import os
+    masters = {int(e): (gu_all[e].float().cpu().numpy(), dn_all[e].float().cpu().numpy()) for e in experts}
+    jobs = [(e, g, d, cfg["fmt"], backward) for e, (g, d) in masters.items()]
+    with mp.get_context("spawn").Pool(max(1, min(len(jobs), os.cpu_count() or 1))) as pool:
+        ops = dict(pool.map(_prep_worker, jobs))
+    table = {e: (masters[e][0].astype(np.float64), masters[e][1].astype(np.float64), ops[e]) for e in masters}
+    return ExpertSubset(cfg["E"], table)

@@ -1,0 +1,85 @@
+"""Parity at the full workload sizes, in the launch configuration bench.py
+times (stacked weight preparation, one moe_forward / moe_backward over all T
+tokens), on outputs the oracle can compute one by one: whole output rows of
+seeded tokens (all their experts and the shared expert), and the weight
+gradients of a seeded lightly loaded expert."""
+import numpy as np
+import pytest
+import torch
+
+import moe_inputs as mi
+from gpu_util import TOL, prepare_subset, rel
+from oracle import moe as om
+
+pytestmark = pytest.mark.gpu
+
+
+def build(name, backward):
+    from mixture_experts_layer_device_gb300.layer import MoELayer
+    cfg = dict(mi.WORKLOADS[name])
+    dev = torch.device("cuda")
+    x, logits = mi.tokens(cfg, dev), mi.logits(cfg, dev)
+    E, d, m = cfg["E"], cfg["d"], cfg["m"]
+    gu_all = torch.empty((E, 2 * m, d), dtype=torch.bfloat16, device=dev)
+    dn_all = torch.empty((E, d, m), dtype=torch.bfloat16, device=dev)
+    for e in range(E):
+        gu_all[e], dn_all[e] = mi.expert(cfg, e, dev)
+    shared = mi.shared(cfg, dev)
+    layer = MoELayer(cfg["T"], d, m, E, cfg["k"], cfg["fmt"], shared=shared, backward=backward, device=dev,
+                     stacked=(gu_all, dn_all))
+    return cfg, x, logits, gu_all, dn_all, shared, layer
+
+
+@pytest.mark.parametrize("name,n_tok", [("qwen3.5-397b", 2), ("glm-5.2", 2), ("kimi-k2.7", 1),
+                                        ("deepseek-v4-pro", 2)])
+def test_full_size_forward_sampled_tokens(name, n_tok):
+    cfg, x, logits, gu_all, dn_all, shared, layer = build(name, backward=False)
+    y = layer.forward(x, logits)
+    assert layer.status() == 0
+    tok = mi.sample_tokens(cfg, n_tok)
+    lg = logits[tok].cpu().numpy()
+    idx, _ = om.route(lg, cfg["k"])
+    experts = prepare_subset(cfg, gu_all, dn_all, sorted(set(idx.reshape(-1).tolist())), backward=False)
+    sh = None if shared is None else tuple(mi.to_f64(w) for w in shared)
+    y_ref, _ = om.forward(mi.to_f64(x[tok]), lg, experts, cfg["k"], cfg["fmt"], shared=sh)
+    y_gpu = mi.to_f64(y[tok])
+    tol = TOL[cfg["fmt"]]
+    for i in range(len(tok)):
+        assert rel(y_gpu[i], y_ref[i]) < tol, "token %d" % tok[i]
+
+
+def test_full_size_backward_sampled():
+    """Kimi-K2.7 shape, MXFP8 + BF16 shared expert: dx and dlogits rows of a
+    seeded token, and dW of a seeded lightly loaded expert (all its rows)."""
+    cfg, x, logits, gu_all, dn_all, shared, layer = build("kimi-k2.7", backward=True)
+    dy = mi.out_grad(cfg, x.device)
+    layer.forward(x, logits, train=True)
+    g = layer.backward(dy, x)
+    assert layer.status() == 0
+    k, fmt, tol = cfg["k"], cfg["fmt"], TOL[cfg["fmt"]]
+    # one token: forward + backward of the oracle on that token alone
+    tok = mi.sample_tokens(cfg, 1)
+    lg = logits[tok].cpu().numpy()
+    idx, _ = om.route(lg, k)
+    counts = layer.view(0, "counts", "i32", (cfg["E"],)).cpu().numpy()
+    e_dw = int(mi.sample_experts(counts, cfg["seed"], n=1, max_rows=256)[0])
+    experts = prepare_subset(cfg, gu_all, dn_all, sorted(set(idx.reshape(-1).tolist()) | {e_dw}), backward=True)
+    sh = None if shared is None else tuple(mi.to_f64(w) for w in shared)
+    xs, dys = mi.to_f64(x[tok]), mi.to_f64(dy[tok])
+    _, saved = om.forward(xs, lg, experts, k, fmt, shared=sh)
+    ref = om.backward(dys, xs, experts, k, fmt, saved, shared=sh, dw_experts=[])
+    assert rel(mi.to_f64(g["dx"][tok]), ref["dx"]) < tol
+    assert rel(g["dlogits"][tok].cpu().numpy().astype(np.float64), ref["dlogits"]) < tol
+    # dW of expert e_dw: every row routed to it, in the schedule's (slot) order
+    idx_all = layer.view(0, "idx", "i32", (cfg["T"], k)).cpu().numpy()
+    w_all = layer.view(0, "w", "f32", (cfg["T"], k)).cpu().numpy().astype(np.float64)
+    slots = np.nonzero(idx_all.reshape(-1) == e_dw)[0]
+    assert slots.size == counts[e_dw] > 0
+    toks = slots // k
+    W_gu, W_dn, ops = experts[e_dw]
+    X = mi.to_f64(x[torch.as_tensor(toks, device=x.device)])
+    fw = om.expert_forward(X, W_gu, W_dn, fmt, ops)
+    dO = om._rnd(fmt)(w_all.reshape(-1)[slots][:, None] * mi.to_f64(dy[torch.as_tensor(toks, device=x.device)]))
+    bw = om.expert_backward(dO, X, fw["GU_saved"], fw["h_saved"], W_gu, W_dn, fmt, ops)
+    assert rel(mi.to_f64(g["dW_gu"][e_dw]), bw["dW_gu"]) < tol
+    assert rel(mi.to_f64(g["dW_dn"][e_dw]), bw["dW_dn"]) < tol
