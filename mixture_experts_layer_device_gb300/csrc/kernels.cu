@@ -383,8 +383,10 @@ __global__ void __launch_bounds__(256) reverse_dispatch_kernel(
 }
 
 // ------------------------------------------------------------ transposes
-// Tile: 32 source rows x 64 columns.  Output rows are source columns; MX
-// output quantises each 32-long output run (one tile's rows) as one block.
+// Block: 32 source rows x 256 columns, as four 64-column sub-tiles whose
+// global loads are all issued up front (16 bytes per thread each).  Output
+// rows are source columns; MX output quantises each 32-long output run (the
+// block's 32 rows) as one block.
 template <bool MX, bool GATHER>
 __global__ void __launch_bounds__(256) transpose_rows_kernel(
     const uint16_t *__restrict__ src, long src_batch_stride, int C, int nrows_host,
@@ -392,45 +394,50 @@ __global__ void __launch_bounds__(256) transpose_rows_kernel(
     long dst_batch_stride, uint8_t *__restrict__ dst_sf, long sf_batch_rows, long ld_dst) {
   __shared__ float tile[32][65];
   const int r0 = blockIdx.x * 32;
-  const int c0 = blockIdx.y * 64;
+  const int cb = blockIdx.y * 256;
   const int bz = blockIdx.z;
   const int nrows = nrows_dev ? __ldg(nrows_dev) : nrows_host;
   if (r0 >= nrows) return;
   src += static_cast<size_t>(bz) * src_batch_stride;
-  {
-    const int rr = threadIdx.x >> 3;          // 0..31
-    const int cc = (threadIdx.x & 7) * 8;     // 0..56
-    const int r = r0 + rr;
-    long srow = r;
-    if constexpr (GATHER) srow = token_of_row(b, E, k, r, nullptr);
-    float f[8];
-    if (srow >= 0 && srow < nsrc) {
-      unpack8(__ldg(reinterpret_cast<const uint4 *>(src + static_cast<size_t>(srow) * C + c0 + cc)), f);
-    } else {
+  const int rr = threadIdx.x >> 3;          // 0..31: source row within the block
+  const int cc = (threadIdx.x & 7) * 8;     // 0..56: column within a sub-tile
+  const int r = r0 + rr;
+  long srow = r;
+  if constexpr (GATHER) srow = token_of_row(b, E, k, r, nullptr);
+  const bool valid = srow >= 0 && srow < nsrc;
+  const int nsub = min(4, (C - cb) / 64);
+  uint4 q[4];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) f[q] = 0.f;
-    }
-#pragma unroll
-    for (int q = 0; q < 8; ++q) tile[rr][cc + q] = f[q];
-  }
-  __syncthreads();
-  const int c = threadIdx.x >> 2;   // output row within tile (0..63)
+  for (int j = 0; j < 4; ++j)
+    q[j] = (valid && j < nsub)
+               ? __ldg(reinterpret_cast<const uint4 *>(src + static_cast<size_t>(srow) * C + cb + 64 * j + cc))
+               : make_uint4(0, 0, 0, 0);
+  const int c = threadIdx.x >> 2;   // output row within a sub-tile (0..63)
   const int part = threadIdx.x & 3; // 8 source rows each
-  float f[8];
 #pragma unroll
-  for (int q = 0; q < 8; ++q) f[q] = tile[part * 8 + q][c];
-  const size_t orow = static_cast<size_t>(c0 + c);
-  if constexpr (!MX) {
-    uint16_t *o = reinterpret_cast<uint16_t *>(dst) + static_cast<size_t>(bz) * dst_batch_stride;
-    *reinterpret_cast<uint4 *>(o + orow * ld_dst + r0 + part * 8) = pack8(f);
-  } else {
-    uint8_t *o = reinterpret_cast<uint8_t *>(dst) + static_cast<size_t>(bz) * dst_batch_stride;
-    uint32_t byte;
-    const uint2 code = mx_encode8_quad(f, &byte);
-    *reinterpret_cast<uint2 *>(o + orow * ld_dst + r0 + part * 8) = code;
-    if (part == 0)
-      dst_sf[sf_tiled_offset(static_cast<long>(bz) * sf_batch_rows + static_cast<long>(orow), r0 / 32,
-                             ld_dst)] = static_cast<uint8_t>(byte);
+  for (int j = 0; j < 4; ++j) {
+    if (j >= nsub) break;
+    if (j) __syncthreads();
+    float f[8];
+    unpack8(q[j], f);
+#pragma unroll
+    for (int t = 0; t < 8; ++t) tile[rr][cc + t] = f[t];
+    __syncthreads();
+#pragma unroll
+    for (int t = 0; t < 8; ++t) f[t] = tile[part * 8 + t][c];
+    const size_t orow = static_cast<size_t>(cb + 64 * j + c);
+    if constexpr (!MX) {
+      uint16_t *o = reinterpret_cast<uint16_t *>(dst) + static_cast<size_t>(bz) * dst_batch_stride;
+      *reinterpret_cast<uint4 *>(o + orow * ld_dst + r0 + part * 8) = pack8(f);
+    } else {
+      uint8_t *o = reinterpret_cast<uint8_t *>(dst) + static_cast<size_t>(bz) * dst_batch_stride;
+      uint32_t byte;
+      const uint2 code = mx_encode8_quad(f, &byte);
+      *reinterpret_cast<uint2 *>(o + orow * ld_dst + r0 + part * 8) = code;
+      if (part == 0)
+        dst_sf[sf_tiled_offset(static_cast<long>(bz) * sf_batch_rows + static_cast<long>(orow), r0 / 32,
+                               ld_dst)] = static_cast<uint8_t>(byte);
+    }
   }
 }
 
@@ -525,7 +532,7 @@ cudaError_t launch_transpose_rows(const void *src, int C, int nrows_out, const i
                                   long nsrc, bool gather, int k, int E, const RouteBufs *b,
                                   int64_t rows_alloc, bool mx, void *dst, uint8_t *dst_sf,
                                   int64_t ld_dst, cudaStream_t s) {
-  const dim3 grid(blocks_for(rows_alloc, 32), C / 64, 1);
+  const dim3 grid(blocks_for(rows_alloc, 32), blocks_for(C, 256), 1);
   const RouteBufs bb = b ? *b : RouteBufs{};
   const uint16_t *sp = static_cast<const uint16_t *>(src);
   const long ns = gather ? (1L << 40) : nsrc;
@@ -554,7 +561,7 @@ cudaError_t launch_quantize_mx(const void *src, int batch, int rows, int cols, b
     quantize_rows_kernel<<<blocks_for(total, 8), 256, 0, s>>>(
         static_cast<const uint4 *>(src), total, cols, reinterpret_cast<uint2 *>(codes), scales);
   } else {
-    const dim3 grid(blocks_for(rows, 32), cols / 64, batch);
+    const dim3 grid(blocks_for(rows, 32), blocks_for(cols, 256), batch);
     transpose_rows_kernel<true, false><<<grid, 256, 0, s>>>(
         static_cast<const uint16_t *>(src), static_cast<long>(rows) * cols, cols, rows, nullptr, rows,
         1, 1, RouteBufs{}, codes, static_cast<long>(rows) * cols, scales, cols, rows);
@@ -564,7 +571,7 @@ cudaError_t launch_quantize_mx(const void *src, int batch, int rows, int cols, b
 
 cudaError_t launch_transpose_bf16(const void *src, int batch, int rows, int cols, void *dst,
                                   cudaStream_t s) {
-  const dim3 grid(blocks_for(rows, 32), cols / 64, batch);
+  const dim3 grid(blocks_for(rows, 32), blocks_for(cols, 256), batch);
   transpose_rows_kernel<false, false><<<grid, 256, 0, s>>>(
       static_cast<const uint16_t *>(src), static_cast<long>(rows) * cols, cols, rows, nullptr, rows, 1,
       1, RouteBufs{}, dst, static_cast<long>(rows) * cols, nullptr, 0, rows);
