@@ -399,8 +399,8 @@ def run_ours(args, cfg, passes, rank, world, local_rank):
         peak = peaks["bf16_tflops_sustained"] * (MX_OVER_BF16 if dom_mx else 1.0)
         achieved = work / (avg_ms / 1e3) / 1e12
         unit = "TFLOP/s"
-        peak_note = ("MXFP8 = %s sustained BF16 x %.0f (nominal ratio)" if dom_mx else "%s sustained BF16") % (
-            peaks_src, MX_OVER_BF16)
+        peak_note = ("MXFP8 = %s sustained BF16 x %.0f (nominal ratio)" % (peaks_src, MX_OVER_BF16) if dom_mx
+                     else "%s sustained BF16" % peaks_src)
     else:
         peak = peaks["hbm_gbs"]
         achieved = work / (avg_ms / 1e3) / 1e9

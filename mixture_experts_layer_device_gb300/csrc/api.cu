@@ -271,8 +271,48 @@ struct Gemm {
   long out_rows;
 };
 
+// 2-D view of a tiled MXFP8 scale buffer as rows of 256 bytes (box: one
+// 512-byte atom = 2 rows), for the pair kernel's TMA scale loads.
+bool make_sf_map(CUtensorMap *m, const void *base, uint64_t bytes) {
+  cuuint64_t dims[2] = {256, bytes / 256};
+  cuuint64_t strides[1] = {256};
+  cuuint32_t box[2] = {256, 2};
+  cuuint32_t estr[2] = {1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Whether a GEMM runs on CTA pairs: BF16 with 256-wide N tiles (and, for
+// weight gradients, an even number of 128-row M tiles per expert).  MXFP8
+// stays on single-CTA tiles: there a 128 x 256 tile already runs the SM's
+// shared-memory traffic (TMA writes + MMA operand reads) near its limit, and
+// the pair's cross-SM coupling measured slower.
+bool use_pair(const Gemm &q) { return q.bn == 256 && !q.mx; }
+
+int run_pair(const Gemm &q, const DeviceInfo &dev, cudaStream_t s) {
+  moe::PairMaps m;
+  memset(&m, 0, sizeof(m));
+  if (!make_map(&m.a, q.a, q.mx, q.K, q.a_rows) || !make_map(&m.b, q.b, q.mx, q.K, q.b_rows))
+    return MOE_ERR_CUDA;
+  if (q.mx && (!make_sf_map(&m.sfa, q.g.sfa, static_cast<uint64_t>(q.a_rows) * q.K / 32) ||
+               !make_sf_map(&m.sfb, q.g.sfb, static_cast<uint64_t>(q.b_rows) * q.K / 32)))
+    return MOE_ERR_CUDA;
+  if (q.g.out && !make_store_map(&m.o, q.g.out, false, q.g.ldo, q.g.ldo, q.out_rows)) return MOE_ERR_CUDA;
+  if (q.g.out2 && !make_store_map(&m.o2, q.g.out2, false, q.g.ldo2, q.g.ldo2, q.out_rows))
+    return MOE_ERR_CUDA;
+  if (q.g.outq && !make_store_map(&m.q, q.g.outq, true, q.g.ldq, q.g.ldq, q.out_rows)) return MOE_ERR_CUDA;
+  const int maxc = moe::pair_max_clusters(q.mx, q.epi);
+  if (maxc <= 0) return MOE_ERR_CUDA;
+  const long pairs = (q.max_tiles + 1) / 2;
+  const long clusters = pairs < maxc ? pairs : maxc;
+  (void)dev;
+  return cuda_status(moe::launch_gemm_pair(q.mx, q.epi, m, q.g, static_cast<int>(clusters), s));
+}
+
 int run_gemm(const char *name, const Gemm &q, const DeviceInfo &dev, cudaStream_t s) {
   Traced tr(name, s);
+  if (use_pair(q) && (q.g.sched != moe::SCHED_GROUP_K || (q.g.M / 128) % 2 == 0)) return run_pair(q, dev, s);
   CUtensorMap ta, tb, to, to2, tq;
   memset(&to, 0, sizeof(to));
   memset(&to2, 0, sizeof(to2));
@@ -614,7 +654,7 @@ int moe_backward(const moe_config *cfg, const void *dy, const void *x, const moe
   {
     Gemm q;
     q.mx = mx;
-    q.bn = mx ? 128 : bn_for(D.m);  // MXFP8: N=128 tiles leave TMEM for two accumulators
+    q.bn = bn_for(D.m);
     q.epi = moe::EPI_SWIGLU_BWD;
     q.a = mx ? static_cast<const void *>(u8("dOq")) : dO;
     q.a_rows = D.Rp;

@@ -23,11 +23,14 @@
 // Every output element is produced by one CTA with a fixed K order, so results
 // are bitwise reproducible.
 #include "common.cuh"
+#include "gemm_common.cuh"
 #include "kernels.h"
 
 namespace moe {
 
 namespace {
+
+using namespace gemm_detail;
 
 template <bool MX, int BN>
 struct Cfg {
@@ -44,8 +47,11 @@ struct Cfg {
   static constexpr int SF_STAGE = SFA_BYTES + SFB_BYTES;
   static constexpr int NUM_ACC = (MX && BN == 256) ? 1 : 2;
   static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr int SFA_COL = NUM_ACC * BN;
-  static constexpr int SFB_COL = SFA_COL + 4;
+  // Scale factors get their own TMEM columns per pipeline stage (4 for A, BN/32
+  // for B), so copying a stage's scales never waits for the MMAs still reading
+  // the previous stage's.
+  static constexpr int SF_COLS = 4 + BN / 32;
+  static constexpr int SF_COL0 = NUM_ACC * BN;
   static constexpr uint32_t TX_BYTES = STAGE_BYTES + SF_STAGE;
   static constexpr uint32_t IDESC = MX ? idesc_mxf8(128, BN) : idesc_bf16(128, BN);
   // epilogue staging: per epilogue warp two 2 KB halves (32 rows x 64 B, 64-byte swizzle)
@@ -54,7 +60,7 @@ struct Cfg {
   static constexpr int NBAR = 2 * STAGES + 2 * NUM_ACC + 1;
   static constexpr size_t SMEM = 1024 + static_cast<size_t>(STAGES) * (STAGE_BYTES + SF_STAGE) +
                                  STAGING_BYTES + NBAR * 8 + 16;
-  static_assert(!MX || SFB_COL + BN / 32 <= 512, "TMEM columns");
+  static_assert(!MX || SF_COL0 + STAGES * SF_COLS <= 512, "TMEM columns");
   static_assert(NUM_ACC * BN <= 512, "TMEM columns");
   static_assert(SMEM <= 232448, "shared memory");
 };
@@ -124,79 +130,6 @@ MOE_DEV Tile decode_tile(const GemmArgs &g, int t) {
     ti.out_col = ntile * BN;
   }
   return ti;
-}
-
-MOE_DEV void load_bf16x32(const void *base, long row, long ld, long col, float *v) {
-  const uint4 *src =
-      reinterpret_cast<const uint4 *>(reinterpret_cast<const __nv_bfloat16 *>(base) + row * ld + col);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint4 q = src[i];
-    v[8 * i + 0] = bf16lo(q.x); v[8 * i + 1] = bf16hi(q.x);
-    v[8 * i + 2] = bf16lo(q.y); v[8 * i + 3] = bf16hi(q.y);
-    v[8 * i + 4] = bf16lo(q.z); v[8 * i + 5] = bf16hi(q.z);
-    v[8 * i + 6] = bf16lo(q.w); v[8 * i + 7] = bf16hi(q.w);
-  }
-}
-
-// 32 floats -> 16 words of bf16 pairs (round to nearest even).
-MOE_DEV void bf16x32_words(const float *v, uint32_t *w) {
-#pragma unroll
-  for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
-}
-
-// MX block of 32 values owned by this thread -> 8 code words; returns the scale byte.
-MOE_DEV uint32_t mx_block_words(const float *v, uint32_t *w) {
-  float am = 0.f;
-#pragma unroll
-  for (int i = 0; i < 32; ++i) am = fmaxf(am, fabsf(v[i]));
-  const uint32_t byte = mx_scale_byte(am);
-  mx_encode32(v, byte, w);
-  return byte;
-}
-
-// Per-warp writer of 32-row x 64-byte output pieces: each lane places its row's
-// 64 bytes in a 64-byte-swizzled shared-memory half (conflict-free), then one
-// lane stores the box with TMA.  Two halves alternate so the staging of one
-// piece overlaps the store of the previous one.
-struct Stager {
-  uint8_t *buf;  // 4 KB, 512-byte aligned
-  int n;
-  MOE_DEV void put(const CUtensorMap *map, const uint32_t *w16, int c0, int row0, int lane) {
-    uint8_t *half = buf + (n & 1) * 2048;
-    if (n >= 2 && lane == 0) bulk_wait_read<1>();
-    __syncwarp();
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int jj = j ^ ((lane >> 1) & 3);
-      *reinterpret_cast<uint4 *>(half + lane * 64 + jj * 16) =
-          make_uint4(w16[4 * j], w16[4 * j + 1], w16[4 * j + 2], w16[4 * j + 3]);
-    }
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) {
-      tma_store_2d(map, half, c0, row0);
-      bulk_commit();
-    }
-    ++n;
-  }
-  MOE_DEV void put_bf16(const CUtensorMap *map, const float *v32, int c0, int row0, int lane) {
-    uint32_t w[16];
-    bf16x32_words(v32, w);
-    put(map, w, c0, row0, lane);
-  }
-};
-
-// Two MX blocks (64 values) of one row -> one 64-byte codes piece + 2 scale bytes.
-MOE_DEV void put_mx64(Stager &st, const CUtensorMap *map, uint8_t *sf, long ldq, const float *v64,
-                      int col, int row0, long grow, int lane) {
-  uint32_t w[16];
-  const uint32_t b0 = mx_block_words(v64, w);
-  const uint32_t b1 = mx_block_words(v64 + 32, w + 8);
-  st.put(map, w, col, row0, lane);
-  // (col / 32) is even, so both bytes sit next to each other in one 512-byte atom.
-  *reinterpret_cast<uint16_t *>(sf + sf_tiled_offset(grow, col / 32, ldq)) =
-      static_cast<uint16_t>(b0 | (b1 << 8));
 }
 
 template <bool MX, int BN, int EPI>
@@ -312,13 +245,14 @@ __global__ void __launch_bounds__(192, 1)
           tc_fence_after();
           const uint32_t sa = smem_u32(smem + stage * C::STAGE_BYTES);
           const uint32_t sb = sa + C::A_BYTES;
+          const uint32_t sfa_col = tmem_base + C::SF_COL0 + stage * C::SF_COLS;
+          const uint32_t sfb_col = sfa_col + 4;
           if constexpr (MX) {
             const uint32_t sfs = smem_u32(sf_base + stage * C::SF_STAGE);
-            tmem_cp_32x128b_warpx4(tmem_base + C::SFA_COL, plain_desc_sbo128(sfs));
+            tmem_cp_32x128b_warpx4(sfa_col, plain_desc_sbo128(sfs));
 #pragma unroll
             for (int c = 0; c < BN / 128; ++c)
-              tmem_cp_32x128b_warpx4(tmem_base + C::SFB_COL + 4 * c,
-                                     plain_desc_sbo128(sfs + 512 + 512 * c));
+              tmem_cp_32x128b_warpx4(sfb_col + 4 * c, plain_desc_sbo128(sfs + 512 + 512 * c));
           }
 #pragma unroll
           for (int k = 0; k < C::KSTEPS; ++k) {
@@ -326,8 +260,7 @@ __global__ void __launch_bounds__(192, 1)
             const uint64_t bd = sw128_desc(sb + 32 * k);
             const uint32_t accum = (kb | k) ? 1u : 0u;
             if constexpr (MX)
-              mma_mxf8(dt, ad, bd, idesc_sf_ids(C::IDESC, k, k), tmem_base + C::SFA_COL,
-                       tmem_base + C::SFB_COL, accum);
+              mma_mxf8(dt, ad, bd, idesc_sf_ids(C::IDESC, k, k), sfa_col, sfb_col, accum);
             else
               mma_bf16(dt, ad, bd, C::IDESC, accum);
           }
@@ -381,108 +314,8 @@ __global__ void __launch_bounds__(192, 1)
         tc_fence_before();
         mbar_arrive(&tempty[acc]);
       };
-      if constexpr (EPI == EPI_STORE) {
-        constexpr int NCH = BN / 64;
-        if (ti.nk == 0) {  // empty reduction (an expert with no rows): zeros
-          release();
-          float z[32];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) z[i] = 0.f;
-#pragma unroll 1
-          for (int c = 0; c < 2 * NCH; ++c) st.put_bf16(&tmO, z, ti.out_col + 32 * c, row0, lane);
-        } else {
-          // Software pipeline: the TMEM load of chunk c+1 is in flight while
-          // chunk c is converted and staged; TMEM is released once the last
-          // chunk has been read.
-          uint32_t buf[2][64];
-          tmem_ld32_async(tb, buf[0]);
-          tmem_ld32_async(tb + 32, buf[0] + 32);
-          tmem_ld_wait();
-          reg_fence<64>(buf[0]);
-#pragma unroll
-          for (int c = 0; c < NCH; ++c) {
-            uint32_t *cur = buf[c & 1];
-            if (c + 1 < NCH) {
-              tmem_ld32_async(tb + 64 * (c + 1), buf[(c + 1) & 1]);
-              tmem_ld32_async(tb + 64 * (c + 1) + 32, buf[(c + 1) & 1] + 32);
-            } else {
-              release();
-            }
-            st.put_bf16(&tmO, reinterpret_cast<const float *>(cur), ti.out_col + 64 * c, row0, lane);
-            st.put_bf16(&tmO, reinterpret_cast<const float *>(cur + 32), ti.out_col + 64 * c + 32, row0,
-                        lane);
-            if (c + 1 < NCH) {
-              tmem_ld_wait();
-              reg_fence<64>(buf[(c + 1) & 1]);
-            }
-          }
-        }
-      } else if constexpr (EPI == EPI_SWIGLU) {
-        // accumulator columns [0,128) = gate G, [128,256) = up U of 128 h columns
-#pragma unroll 1
-        for (int c = 0; c < 2; ++c) {
-          uint32_t gr[64], ur[64];
-          tmem_ld32_async(tb + 64 * c, gr);
-          tmem_ld32_async(tb + 64 * c + 32, gr + 32);
-          tmem_ld32_async(tb + 128 + 64 * c, ur);
-          tmem_ld32_async(tb + 128 + 64 * c + 32, ur + 32);
-          tmem_ld_wait();
-          reg_fence<64>(gr);
-          reg_fence<64>(ur);
-          if (c == 1) release();
-          float *G = reinterpret_cast<float *>(gr);
-          float *U = reinterpret_cast<float *>(ur);
-          const int col = ti.out_col + 64 * c;
-          if (g.out2) {
-            st.put_bf16(&tmO2, G, col, row0, lane);
-            st.put_bf16(&tmO2, G + 32, col + 32, row0, lane);
-            st.put_bf16(&tmO2, U, g.m_half + col, row0, lane);
-            st.put_bf16(&tmO2, U + 32, g.m_half + col + 32, row0, lane);
-          }
-#pragma unroll
-          for (int i = 0; i < 64; ++i) G[i] = silu(G[i]) * U[i];  // h, in place
-          if (g.out) {
-            st.put_bf16(&tmO, G, col, row0, lane);
-            st.put_bf16(&tmO, G + 32, col + 32, row0, lane);
-          }
-          if (g.outq) put_mx64(st, &tmQ, g.outq_sf, g.ldq, G, col, row0, grow, lane);
-        }
-      } else {  // EPI_SWIGLU_BWD: accumulator = dh; G|U saved in bf16
-        constexpr int NCH = BN / 64;
-#pragma unroll 1
-        for (int c = 0; c < NCH; ++c) {
-          uint32_t hr[64];
-          tmem_ld32_async(tb + 64 * c, hr);
-          tmem_ld32_async(tb + 64 * c + 32, hr + 32);
-          tmem_ld_wait();
-          reg_fence<64>(hr);
-          if (c == NCH - 1) release();
-          const float *dh = reinterpret_cast<const float *>(hr);
-          const int col = ti.out_col + 64 * c;
-          float dG[64], dU[64];
-#pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            float G[32], U[32];
-            load_bf16x32(g.aux, grow, g.ld_aux, col + 32 * hh, G);
-            load_bf16x32(g.aux, grow, g.ld_aux, g.m_half + col + 32 * hh, U);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const float d = dh[32 * hh + i];
-              const float sg = sigmoidf(G[i]);
-              dG[32 * hh + i] = round_bf16(d * U[i] * sg * (1.0f + G[i] * (1.0f - sg)));
-              dU[32 * hh + i] = round_bf16(d * G[i] * sg);
-            }
-          }
-          st.put_bf16(&tmO, dG, col, row0, lane);
-          st.put_bf16(&tmO, dG + 32, col + 32, row0, lane);
-          st.put_bf16(&tmO, dU, g.m_half + col, row0, lane);
-          st.put_bf16(&tmO, dU + 32, g.m_half + col + 32, row0, lane);
-          if (g.outq) {
-            put_mx64(st, &tmQ, g.outq_sf, g.ldq, dG, col, row0, grow, lane);
-            put_mx64(st, &tmQ, g.outq_sf, g.ldq, dU, g.m_half + col, row0, grow, lane);
-          }
-        }
-      }
+      epilogue_tile<EPI, BN>(g, &tmO, &tmO2, &tmQ, st, tb, ti.nk, row0, grow, ti.out_col, lane, true,
+                             release);
       if (++acc == C::NUM_ACC) {
         acc = 0;
         aph ^= 1u;

@@ -108,4 +108,19 @@ cudaError_t launch_gemm(bool mx, int bn, int epi, const CUtensorMap &ta, const C
                         const CUtensorMap &to, const CUtensorMap &to2, const CUtensorMap &tq,
                         const GemmArgs &args, int grid, cudaStream_t s);
 
+// Tensor maps of one 2-CTA GEMM launch: operands (box 128 rows x 128 bytes,
+// 128-byte swizzle), MXFP8 scale buffers viewed as rows of 256 bytes (box
+// 2 rows = one 512-byte atom), and the epilogue's store maps.
+struct PairMaps {
+  CUtensorMap a, b, sfa, sfb, o, o2, q;
+};
+
+// D = A * B^T on CTA pairs (tcgen05 cta_group::2): 256 x 256 tiles, two
+// consecutive 128-row M-tiles of one group per pair.  Requires N tiles of 256
+// and, for SCHED_GROUP_K, M a multiple of 256.  `clusters` pairs are launched
+// (<= pair_max_clusters()).
+cudaError_t launch_gemm_pair(bool mx, int epi, const PairMaps &maps, const GemmArgs &args,
+                             int clusters, cudaStream_t s);
+int pair_max_clusters(bool mx, int epi);
+
 }  // namespace moe
