@@ -68,13 +68,20 @@ typedef enum {
 
 /* moe_config.flags bits */
 #define MOE_FLAG_BACKWARD 1 /* size the workspace for moe_backward as well */
+/* Test hook for the device-side failure path: in moe_forward the gate/up
+ * GEMM's load warp issues nothing, so its MMA warp's wait runs out (limit
+ * 50 ms instead of 4 s); the kernels drain and return, moe_get_status then
+ * reports MOE_ERR_TIMEOUT, and the outputs of that call are undefined.  The
+ * CUDA context stays usable. */
+#define MOE_FLAG_DEBUG_STARVE 2
 
 /*
  * Layer shape.  T tokens, hidden d, expert intermediate m, E experts, top-k k.
  * Supported: 1 <= k <= min(E, 16), E <= 1024, d % 256 == 0, m % 128 == 0,
  * m_shared % 128 == 0 (0 = no shared expert), T*k < 2^31 - 127*E.  dtype is
  * the routed experts' arithmetic; the shared expert is always BF16.  flags:
- * MOE_FLAG_BACKWARD or 0 (moe_backward needs a workspace sized with it).
+ * MOE_FLAG_BACKWARD and/or MOE_FLAG_DEBUG_STARVE, or 0 (moe_backward needs a
+ * workspace sized with MOE_FLAG_BACKWARD).
  */
 typedef struct {
   int32_t T, d, m, E, k;

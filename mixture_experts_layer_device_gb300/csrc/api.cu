@@ -20,7 +20,7 @@ using moe::RouteBufs;
 // ---------------------------------------------------------------- shapes
 struct Dims {
   int T, d, m, E, k, ms;
-  bool mx, bwd;
+  bool mx, bwd, starve;
   long R, Rp, Tp;
   int nchunks;
 };
@@ -31,7 +31,7 @@ int check_config(const moe_config *c, Dims *D) {
     return MOE_ERR_ARG;
   if (c->k > c->E || c->k > 16 || c->E > 1024) return MOE_ERR_SHAPE;
   if (c->dtype != MOE_BF16 && c->dtype != MOE_MXFP8) return MOE_ERR_ARG;
-  if ((c->flags & ~MOE_FLAG_BACKWARD) != 0) return MOE_ERR_ARG;
+  if ((c->flags & ~(MOE_FLAG_BACKWARD | MOE_FLAG_DEBUG_STARVE)) != 0) return MOE_ERR_ARG;
   if (c->d % 256 || c->m % 128 || c->m_shared % 128) return MOE_ERR_SHAPE;
   const long R = static_cast<long>(c->T) * c->k;
   const long Rp = (R + 127L * c->E + 127) / 128 * 128;
@@ -44,6 +44,7 @@ int check_config(const moe_config *c, Dims *D) {
   D->ms = c->m_shared;
   D->mx = c->dtype == MOE_MXFP8;
   D->bwd = (c->flags & MOE_FLAG_BACKWARD) != 0;
+  D->starve = (c->flags & MOE_FLAG_DEBUG_STARVE) != 0;
   D->R = R;
   D->Rp = Rp;
   D->Tp = (c->T + 127L) / 128 * 128;
@@ -357,8 +358,13 @@ GemmArgs base_args(int sched, int E, const int *poff, int *status) {
   g.E = E;
   g.poff = poff;
   g.status = status;
+  g.timeout_ns = moe::kWaitTimeoutNs;
   return g;
 }
+
+// MOE_FLAG_DEBUG_STARVE: the gate/up GEMM's producer issues no loads and every
+// wait of that launch gives up after 50 ms.
+constexpr unsigned long long kStarveTimeoutNs = 50000000ull;
 
 }  // namespace
 
@@ -521,6 +527,10 @@ int moe_forward(const moe_config *cfg, const void *x, const float *logits, const
     q.g.outq_sf = hq_sf;
     q.g.ldq = D.m;
     q.g.m_half = D.m;
+    if (D.starve) {
+      q.g.debug_starve = 1;
+      q.g.timeout_ns = kStarveTimeoutNs;
+    }
     q.max_tiles = (D.Rp / 128) * q.g.n_tiles;
     q.out_rows = D.Rp;
     if ((rc = run_gemm("gemm1_gate_up_swiglu", q, dev, s)) != MOE_OK) return rc;

@@ -16,9 +16,9 @@
 
 namespace moe {
 
-// Every spin-wait in a kernel gives up after this much wall-clock time,
-// records kStatusTimeout and lets the kernel drain and return.
-constexpr unsigned long long kWaitTimeoutNs = 4000000000ull;
+// Every spin-wait in a kernel gives up after kWaitTimeoutNs of wall-clock time
+// (unless a launch passes a shorter limit), records kStatusTimeout and lets
+// the kernel drain and return.
 
 MOE_DEV uint32_t smem_u32(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -71,7 +71,8 @@ MOE_DEV bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 // false) when *abort becomes non-zero or after kWaitTimeoutNs; in the latter
 // case it records the timeout in the global status word and raises *abort so
 // the other roles of the CTA stop too.
-MOE_DEV bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort, int *status) {
+MOE_DEV bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort, int *status,
+                       unsigned long long timeout_ns = kWaitTimeoutNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer();
   while (true) {
@@ -79,7 +80,7 @@ MOE_DEV bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort, int 
     for (int i = 0; i < 64; ++i)
       if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
-    if (globaltimer() - t0 > kWaitTimeoutNs) {
+    if (globaltimer() - t0 > timeout_ns) {
       if (status) atomicOr(status, kStatusTimeout);
       *abort = 1;
       return false;
@@ -195,6 +196,16 @@ MOE_DEV void tmem_ld32_async(uint32_t taddr, uint32_t *r) {
         "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
         "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
         "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+// 16-column variant of tmem_ld32_async.
+MOE_DEV void tmem_ld16_async(uint32_t taddr, uint32_t *r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
       : "r"(taddr));
 }
 // Ties registers written by an asynchronous load to a point after its wait, so

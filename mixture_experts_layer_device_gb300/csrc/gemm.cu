@@ -187,10 +187,10 @@ __global__ void __launch_bounds__(192, 1)
       uint32_t ph = 0;
       int armed[C::STAGES];
       for (int s = 0; s < C::STAGES; ++s) armed[s] = -1;
-      for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x) {
+      for (int t = blockIdx.x; t < total && !*abort_flag && !g.debug_starve; t += gridDim.x) {
         const Tile ti = decode_tile<C::BK, BN, EPI>(g, t);
         for (int kb = 0; kb < ti.nk; ++kb) {
-          if (!mbar_wait(&empty[stage], ph ^ 1u, abort_flag, g.status)) break;
+          if (!mbar_wait(&empty[stage], ph ^ 1u, abort_flag, g.status, g.timeout_ns)) break;
           uint8_t *sa = smem + stage * C::STAGE_BYTES;
           uint8_t *sb = sa + C::A_BYTES;
           mbar_arrive_expect_tx(&full[stage], C::TX_BYTES);
@@ -221,7 +221,7 @@ __global__ void __launch_bounds__(192, 1)
       for (int s = 0; s < C::STAGES; ++s)
         if (armed[s] >= 0) {
           volatile int no_abort = 0;
-          mbar_wait(&full[s], static_cast<uint32_t>(armed[s]), &no_abort, g.status);
+          mbar_wait(&full[s], static_cast<uint32_t>(armed[s]), &no_abort, g.status, g.timeout_ns);
         }
     }
   } else if (warp == 1) {
@@ -234,11 +234,11 @@ __global__ void __launch_bounds__(192, 1)
       bool ok = true;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
         const Tile ti = decode_tile<C::BK, BN, EPI>(g, t);
-        if (!mbar_wait(&tempty[acc], aph ^ 1u, abort_flag, g.status)) break;
+        if (!mbar_wait(&tempty[acc], aph ^ 1u, abort_flag, g.status, g.timeout_ns)) break;
         tc_fence_after();
         const uint32_t dt = tmem_base + static_cast<uint32_t>(acc * BN);
         for (int kb = 0; kb < ti.nk; ++kb) {
-          if (!mbar_wait(&full[stage], ph, abort_flag, g.status)) {
+          if (!mbar_wait(&full[stage], ph, abort_flag, g.status, g.timeout_ns)) {
             ok = false;
             break;
           }
@@ -280,7 +280,7 @@ __global__ void __launch_bounds__(192, 1)
       // All MMAs this thread issued must finish before TMEM is released.
       mma_commit(done);
       volatile int no_abort = 0;
-      mbar_wait(done, 0, &no_abort, g.status);
+      mbar_wait(done, 0, &no_abort, g.status, g.timeout_ns);
     }
   } else {
     // ------------------------------------------------ epilogue (warps 2..5)
@@ -304,7 +304,7 @@ __global__ void __launch_bounds__(192, 1)
         bulk_prefetch_l2(gu + ti.out_col, BN * 2);
         bulk_prefetch_l2(gu + g.m_half + ti.out_col, BN * 2);
       }
-      if (!mbar_wait(&tfull[acc], aph, abort_flag, g.status)) break;
+      if (!mbar_wait(&tfull[acc], aph, abort_flag, g.status, g.timeout_ns)) break;
       tc_fence_after();
       const uint32_t tb =
           tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);

@@ -221,11 +221,11 @@ __global__ void __launch_bounds__(192, 1)
       prefetch_tensormap(&tmB);
       int stage = 0;
       uint32_t ph = 0;
-      for (int u = cluster_id; u < total && !*abort_flag; u += num_clusters) {
+      for (int u = cluster_id; u < total && !*abort_flag && !g.debug_starve; u += num_clusters) {
         const PairTile ti = decode_pair<C::BK, EPI>(g, pairoff, u, rank);
         const int b_row = leader ? ti.b_row0 : ti.b_row1;
         for (int kb = 0; kb < ti.nk; ++kb) {
-          if (!mbar_wait(&empty[stage], ph ^ 1u, abort_flag, g.status)) break;
+          if (!mbar_wait(&empty[stage], ph ^ 1u, abort_flag, g.status, g.timeout_ns)) break;
           uint8_t *sa = smem + stage * C::STAGE_BYTES;
           uint8_t *sb = sa + C::A_BYTES;
           if (leader) mbar_arrive_expect_tx(&full[stage], C::TX_BYTES);
@@ -258,11 +258,11 @@ __global__ void __launch_bounds__(192, 1)
       bool ok = true;
       for (int u = cluster_id; u < total && ok; u += num_clusters) {
         const PairTile ti = decode_pair<C::BK, EPI>(g, pairoff, u, rank);
-        if (!mbar_wait(&tempty[acc], aph ^ 1u, abort_flag, g.status)) break;
+        if (!mbar_wait(&tempty[acc], aph ^ 1u, abort_flag, g.status, g.timeout_ns)) break;
         tc_fence_after();
         const uint32_t dt = tmem_base + static_cast<uint32_t>(acc * C::BN);
         for (int kb = 0; kb < ti.nk; ++kb) {
-          if (!mbar_wait(&full[stage], ph, abort_flag, g.status)) {
+          if (!mbar_wait(&full[stage], ph, abort_flag, g.status, g.timeout_ns)) {
             ok = false;
             break;
           }
@@ -302,7 +302,7 @@ __global__ void __launch_bounds__(192, 1)
       }
       mma_commit_pair_mc(done, 1);
       volatile int no_abort = 0;
-      mbar_wait(done, 0, &no_abort, g.status);
+      mbar_wait(done, 0, &no_abort, g.status, g.timeout_ns);
     }
   } else {
     // ------------------------------------------------ epilogue (warps 2..5, both CTAs)
@@ -326,7 +326,7 @@ __global__ void __launch_bounds__(192, 1)
           bulk_prefetch_l2(gu + g.m_half + ti.out_col, C::BN * 2);
         }
       }
-      if (!mbar_wait(&tfull[acc], aph, abort_flag, g.status)) break;
+      if (!mbar_wait(&tfull[acc], aph, abort_flag, g.status, g.timeout_ns)) break;
       tc_fence_after();
       const uint32_t tb =
           tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * C::BN);

@@ -10,6 +10,8 @@ namespace moe {
 
 // Device status word bits (kept in the workspace, read by moe_get_status).
 constexpr int kStatusTimeout = 1;
+// Default limit of every device-side wait.
+constexpr unsigned long long kWaitTimeoutNs = 4000000000ull;
 
 // Chunk of flat slots handled by one warp in the schedule kernels.
 constexpr int kSchedChunk = 1024;
@@ -96,6 +98,8 @@ struct GemmArgs {
   long ld_aux;
   int m_half;         // SWIGLU / SWIGLU_BWD: m
   int *status;
+  unsigned long long timeout_ns;  // limit of every wait in the launch
+  int debug_starve;   // test hook: the producer issues no loads (the MMA wait runs out)
 };
 
 // D = A * B^T with A [rows, K] and B [rows, K] K-major (TMA maps built by the

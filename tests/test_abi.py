@@ -82,6 +82,13 @@ def test_null_and_misaligned_pointers_rejected_on_host(pkg):
     assert pkg.moe_backward(cfg, 16, 16, W, 16, 16, 16, 16, 16, None, None, 16, 0) == -1
 
 
+def test_debug_flag_accepted_unknown_flags_rejected(pkg):
+    cfg = pkg.config(64, 256, 128, 8, 2, 0, "bf16", pkg.MOE_FLAG_BACKWARD | pkg.MOE_FLAG_DEBUG_STARVE)
+    assert pkg.moe_workspace_bytes(cfg) == pkg.moe_workspace_bytes(pkg.config(64, 256, 128, 8, 2, 0, "bf16",
+                                                                              pkg.MOE_FLAG_BACKWARD))
+    assert pkg.moe_workspace_bytes(pkg.config(64, 256, 128, 8, 2, 0, "bf16", 8)) == 0
+
+
 def test_status_strings(pkg):
     L = pkg.lib()
     for c in range(-6, 1):
