@@ -132,8 +132,16 @@ MOE_DEV Tile decode_tile(const GemmArgs &g, int t) {
   return ti;
 }
 
+// Epilogue warps per CTA: 8 (two per TMEM lane quarter, each draining half of
+// the columns) for the bf16-store and SwiGLU epilogues, 4 for SwiGLU backward
+// (whose per-row working set needs the registers of a 192-thread CTA).
+template <int EPI>
+__host__ __device__ constexpr int epi_warps() {
+  return EPI == EPI_SWIGLU_BWD ? 4 : 8;
+}
+
 template <bool MX, int BN, int EPI>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(64 + 32 * epi_warps<EPI>(), 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmO2,
                 const __grid_constant__ CUtensorMap tmQ, const GemmArgs g) {
@@ -162,7 +170,7 @@ __global__ void __launch_bounds__(192, 1)
     }
     for (int a = 0; a < C::NUM_ACC; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 128);
+      mbar_init(&tempty[a], 32 * epi_warps<EPI>());
     }
     mbar_init(done, 1);
     *abort_flag = 0;
@@ -283,10 +291,12 @@ __global__ void __launch_bounds__(192, 1)
       mbar_wait(done, 0, &no_abort, g.status, g.timeout_ns);
     }
   } else {
-    // ------------------------------------------------ epilogue (warps 2..5)
+    // ------------------------------------------------ epilogue (warps 2..)
+    constexpr int NEPI = epi_warps<EPI>();
     const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int part = (warp - 2) >> 2;  // which half of the columns (8 epilogue warps)
     const int r = q * 32 + lane;
-    Stager st{staging + (warp - 2) * 4096, 0};
+    Stager st(staging + (warp - 2) * (C::STAGING_BYTES / NEPI), NEPI == 4 ? 2 : 1);
     if (lane == 0) {
       if (g.out) prefetch_tensormap(&tmO);
       if (g.out2) prefetch_tensormap(&tmO2);
@@ -314,8 +324,12 @@ __global__ void __launch_bounds__(192, 1)
         tc_fence_before();
         mbar_arrive(&tempty[acc]);
       };
-      epilogue_tile<EPI, BN>(g, &tmO, &tmO2, &tmQ, st, tb, ti.nk, row0, grow, ti.out_col, lane, true,
-                             release);
+      if constexpr (NEPI == 8)
+        epilogue_tile_split<EPI, BN>(g, &tmO, &tmO2, &tmQ, st, tb, ti.nk, row0, grow, ti.out_col, lane,
+                                     part, true, release);
+      else
+        epilogue_tile<EPI, BN>(g, &tmO, &tmO2, &tmQ, st, tb, ti.nk, row0, grow, ti.out_col, lane, true,
+                               release);
       if (++acc == C::NUM_ACC) {
         acc = 0;
         aph ^= 1u;
@@ -345,7 +359,7 @@ cudaError_t launch_one(const CUtensorMap &ta, const CUtensorMap &tb, const CUten
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  gemm_kernel<MX, BN, EPI><<<grid, 192, C::SMEM, s>>>(ta, tb, to, to2, tq, g);
+  gemm_kernel<MX, BN, EPI><<<grid, 64 + 32 * epi_warps<EPI>(), C::SMEM, s>>>(ta, tb, to, to2, tq, g);
   return cudaGetLastError();
 }
 

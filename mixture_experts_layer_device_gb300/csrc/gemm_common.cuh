@@ -37,15 +37,20 @@ MOE_DEV uint32_t mx_block_words(const float *v, uint32_t *w) {
 }
 
 // Per-warp writer of 32-row x 64-byte output pieces: each lane places its row's
-// 64 bytes in a 64-byte-swizzled shared-memory half (conflict-free), then one
-// lane stores the box with TMA.  Two halves alternate so the staging of one
-// piece overlaps the store of the previous one.
+// 64 bytes in a 64-byte-swizzled shared-memory buffer (conflict-free), then one
+// lane stores the box with TMA.  With two buffers the staging of one piece
+// overlaps the store of the previous one.
 struct Stager {
-  uint8_t *buf;  // 4 KB, 512-byte aligned
+  uint8_t *buf;  // nbuf x 2 KB, 512-byte aligned
   int n;
+  int nbuf;      // 1 or 2
+  MOE_DEV Stager(uint8_t *b, int buffers) : buf(b), n(0), nbuf(buffers) {}
   MOE_DEV void put(const CUtensorMap *map, const uint32_t *w16, int c0, int row0, int lane) {
-    uint8_t *half = buf + (n & 1) * 2048;
-    if (n >= 2 && lane == 0) bulk_wait_read<1>();
+    uint8_t *half = buf + (nbuf == 2 ? (n & 1) * 2048 : 0);
+    if (lane == 0) {
+      if (nbuf == 2 && n >= 2) bulk_wait_read<1>();
+      if (nbuf == 1 && n >= 1) bulk_wait_read<0>();
+    }
     __syncwarp();
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -228,6 +233,80 @@ MOE_DEV void epilogue_tile(const GemmArgs &g, const CUtensorMap *tmO, const CUte
         put_mx64(st, tmQ, g.outq_sf, g.ldq, dU, g.m_half + col, row0, grow, lane);
       }
     }
+  }
+}
+
+// Epilogue shared by two warps per TMEM lane quarter: warp `part` (0 or 1)
+// drains half of the tile's columns.  The accumulator is read in one round
+// (two warps in parallel) and released before any conversion or store.
+// EPI_STORE and EPI_SWIGLU only.
+template <int EPI, int BN, typename Release>
+MOE_DEV void epilogue_tile_split(const GemmArgs &g, const CUtensorMap *tmO, const CUtensorMap *tmO2,
+                                 const CUtensorMap *tmQ, Stager &st, uint32_t tb, int nk, int row0,
+                                 long grow, int out_col, int lane, int part, bool store,
+                                 Release release) {
+  if constexpr (EPI == EPI_STORE) {
+    constexpr int NC = BN / 2;  // accumulator columns of this warp
+    constexpr int NC32 = NC / 32;
+    const int c0 = part * NC;
+    if (nk == 0) {
+      release();
+      if (store) {
+        float z[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) z[i] = 0.f;
+#pragma unroll 1
+        for (int c = 0; c < NC32; ++c) st.put_bf16(tmO, z, out_col + c0 + 32 * c, row0, lane);
+      }
+      return;
+    }
+    uint32_t pk[NC / 2];
+    uint32_t buf[2][32];
+    tmem_ld32_async(tb + c0, buf[0]);
+    tmem_ld_wait();
+    reg_fence<32>(buf[0]);
+#pragma unroll
+    for (int c = 0; c < NC32; ++c) {
+      if (c + 1 < NC32) tmem_ld32_async(tb + c0 + 32 * (c + 1), buf[(c + 1) & 1]);
+      bf16x32_words(reinterpret_cast<const float *>(buf[c & 1]), pk + 16 * c);
+      if (c + 1 < NC32) {
+        tmem_ld_wait();
+        reg_fence<32>(buf[(c + 1) & 1]);
+      }
+    }
+    release();
+    if (store) {
+#pragma unroll
+      for (int c = 0; c < NC32; ++c) st.put(tmO, pk + 16 * c, out_col + c0 + 32 * c, row0, lane);
+    }
+  } else {  // EPI_SWIGLU: accumulator [0,128) = G, [128,256) = U; this warp: 64 h columns
+    const int hc = part * 64;
+    uint32_t gr[64], ur[64];
+    tmem_ld32_async(tb + hc, gr);
+    tmem_ld32_async(tb + hc + 32, gr + 32);
+    tmem_ld32_async(tb + 128 + hc, ur);
+    tmem_ld32_async(tb + 128 + hc + 32, ur + 32);
+    tmem_ld_wait();
+    reg_fence<64>(gr);
+    reg_fence<64>(ur);
+    release();
+    if (!store) return;
+    float *G = reinterpret_cast<float *>(gr);
+    const float *U = reinterpret_cast<const float *>(ur);
+    const int col = out_col + hc;
+    if (g.out2) {
+      st.put_bf16(tmO2, G, col, row0, lane);
+      st.put_bf16(tmO2, G + 32, col + 32, row0, lane);
+      st.put_bf16(tmO2, U, g.m_half + col, row0, lane);
+      st.put_bf16(tmO2, U + 32, g.m_half + col + 32, row0, lane);
+    }
+#pragma unroll
+    for (int i = 0; i < 64; ++i) G[i] = silu(G[i]) * U[i];  // h, in place
+    if (g.out) {
+      st.put_bf16(tmO, G, col, row0, lane);
+      st.put_bf16(tmO, G + 32, col + 32, row0, lane);
+    }
+    if (g.outq) put_mx64(st, tmQ, g.outq_sf, g.ldq, G, col, row0, grow, lane);
   }
 }
 

@@ -308,7 +308,7 @@ __global__ void __launch_bounds__(192, 1)
     // ------------------------------------------------ epilogue (warps 2..5, both CTAs)
     const int q = warp & 3;
     const int r = q * 32 + lane;
-    Stager st{staging + (warp - 2) * 4096, 0};
+    Stager st(staging + (warp - 2) * 4096, 2);
     if (lane == 0) {
       if (g.out) prefetch_tensormap(&tmO);
       if (g.out2) prefetch_tensormap(&tmO2);
