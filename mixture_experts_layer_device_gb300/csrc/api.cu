@@ -664,7 +664,9 @@ int moe_backward(const moe_config *cfg, const void *dy, const void *x, const moe
   {
     Gemm q;
     q.mx = mx;
-    q.bn = bn_for(D.m);
+    // MXFP8: 128-column tiles keep two TMEM accumulators next to the scale
+    // columns, so this epilogue-heavy GEMM overlaps epilogue and main loop.
+    q.bn = mx ? 128 : bn_for(D.m);
     q.epi = moe::EPI_SWIGLU_BWD;
     q.a = mx ? static_cast<const void *>(u8("dOq")) : dO;
     q.a_rows = D.Rp;

@@ -133,15 +133,15 @@ MOE_DEV Tile decode_tile(const GemmArgs &g, int t) {
 }
 
 // Epilogue warps per CTA: 8 (two per TMEM lane quarter, each draining half of
-// the columns) for the bf16-store and SwiGLU epilogues, 4 for SwiGLU backward
-// (whose per-row working set needs the registers of a 192-thread CTA).
-template <int EPI>
+// the columns), except SwiGLU backward on 256-column tiles, whose per-row
+// working set needs the registers of a 192-thread CTA (4 warps).
+template <int EPI, int BN>
 __host__ __device__ constexpr int epi_warps() {
-  return EPI == EPI_SWIGLU_BWD ? 4 : 8;
+  return (EPI == EPI_SWIGLU_BWD && BN == 256) ? 4 : 8;
 }
 
 template <bool MX, int BN, int EPI>
-__global__ void __launch_bounds__(64 + 32 * epi_warps<EPI>(), 1)
+__global__ void __launch_bounds__(64 + 32 * epi_warps<EPI, BN>(), 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmO2,
                 const __grid_constant__ CUtensorMap tmQ, const GemmArgs g) {
@@ -170,7 +170,7 @@ __global__ void __launch_bounds__(64 + 32 * epi_warps<EPI>(), 1)
     }
     for (int a = 0; a < C::NUM_ACC; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 32 * epi_warps<EPI>());
+      mbar_init(&tempty[a], 32 * epi_warps<EPI, BN>());
     }
     mbar_init(done, 1);
     *abort_flag = 0;
@@ -292,7 +292,7 @@ __global__ void __launch_bounds__(64 + 32 * epi_warps<EPI>(), 1)
     }
   } else {
     // ------------------------------------------------ epilogue (warps 2..)
-    constexpr int NEPI = epi_warps<EPI>();
+    constexpr int NEPI = epi_warps<EPI, BN>();
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int part = (warp - 2) >> 2;  // which half of the columns (8 epilogue warps)
     const int r = q * 32 + lane;
@@ -359,7 +359,7 @@ cudaError_t launch_one(const CUtensorMap &ta, const CUtensorMap &tb, const CUten
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  gemm_kernel<MX, BN, EPI><<<grid, 64 + 32 * epi_warps<EPI>(), C::SMEM, s>>>(ta, tb, to, to2, tq, g);
+  gemm_kernel<MX, BN, EPI><<<grid, 64 + 32 * epi_warps<EPI, BN>(), C::SMEM, s>>>(ta, tb, to, to2, tq, g);
   return cudaGetLastError();
 }
 

@@ -239,7 +239,7 @@ MOE_DEV void epilogue_tile(const GemmArgs &g, const CUtensorMap *tmO, const CUte
 // Epilogue shared by two warps per TMEM lane quarter: warp `part` (0 or 1)
 // drains half of the tile's columns.  The accumulator is read in one round
 // (two warps in parallel) and released before any conversion or store.
-// EPI_STORE and EPI_SWIGLU only.
+// EPI_SWIGLU_BWD needs BN = 128 here (64 dh columns per warp).
 template <int EPI, int BN, typename Release>
 MOE_DEV void epilogue_tile_split(const GemmArgs &g, const CUtensorMap *tmO, const CUtensorMap *tmO2,
                                  const CUtensorMap *tmQ, Stager &st, uint32_t tb, int nk, int row0,
@@ -278,6 +278,49 @@ MOE_DEV void epilogue_tile_split(const GemmArgs &g, const CUtensorMap *tmO, cons
     if (store) {
 #pragma unroll
       for (int c = 0; c < NC32; ++c) st.put(tmO, pk + 16 * c, out_col + c0 + 32 * c, row0, lane);
+    }
+  } else if constexpr (EPI == EPI_SWIGLU_BWD) {
+    static_assert(BN == 128, "split SwiGLU-backward epilogue expects 128-column tiles");
+    const int dc = part * 64;  // this warp's 64 dh columns
+    uint32_t hr[64];
+    tmem_ld32_async(tb + dc, hr);
+    tmem_ld32_async(tb + dc + 32, hr + 32);
+    tmem_ld_wait();
+    reg_fence<64>(hr);
+    release();
+    if (!store) return;
+    const float *dh = reinterpret_cast<const float *>(hr);
+    const int col = out_col + dc;
+    uint32_t cg[16], cu[16];  // MX codes of dG and dU (two blocks each)
+    uint32_t sg[2], su[2];
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      float G[32], U[32];
+      load_bf16x32(g.aux, grow, g.ld_aux, col + 32 * hh, G);
+      load_bf16x32(g.aux, grow, g.ld_aux, g.m_half + col + 32 * hh, U);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const float d = dh[32 * hh + i];
+        const float sgm = sigmoidf(G[i]);
+        const float dg = round_bf16(d * U[i] * sgm * (1.0f + G[i] * (1.0f - sgm)));
+        const float du = round_bf16(d * G[i] * sgm);
+        G[i] = dg;
+        U[i] = du;
+      }
+      st.put_bf16(tmO, G, col + 32 * hh, row0, lane);
+      st.put_bf16(tmO, U, g.m_half + col + 32 * hh, row0, lane);
+      if (g.outq) {
+        sg[hh] = mx_block_words(G, cg + 8 * hh);
+        su[hh] = mx_block_words(U, cu + 8 * hh);
+      }
+    }
+    if (g.outq) {
+      st.put(tmQ, cg, col, row0, lane);
+      st.put(tmQ, cu, g.m_half + col, row0, lane);
+      *reinterpret_cast<uint16_t *>(g.outq_sf + sf_tiled_offset(grow, col / 32, g.ldq)) =
+          static_cast<uint16_t>(sg[0] | (sg[1] << 8));
+      *reinterpret_cast<uint16_t *>(g.outq_sf + sf_tiled_offset(grow, (g.m_half + col) / 32, g.ldq)) =
+          static_cast<uint16_t>(su[0] | (su[1] << 8));
     }
   } else {  // EPI_SWIGLU: accumulator [0,128) = G, [128,256) = U; this warp: 64 h columns
     const int hc = part * 64;
