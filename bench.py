@@ -77,8 +77,12 @@ def layer_work(cfg, passes):
     return fl_exp, fl_sh, byt
 
 
-def kernel_work(cfg, name):
-    """(bound, algorithmic work per launch, is_mx) for a traced kernel name."""
+def kernel_work(cfg, name, train=False):
+    """(bound, algorithmic work per launch, is_mx) for a traced kernel name.
+
+    With MXFP8 experts a training pass's dispatch also writes the transposed
+    codes of x, and its reverse combine both the row- and column-blocked codes
+    of dO."""
     T, d, m, E, k, ms = (cfg[n] for n in ("T", "d", "m", "E", "k", "m_shared"))
     R = T * k
     mx = cfg["fmt"] == "mxfp8"
@@ -96,9 +100,9 @@ def kernel_work(cfg, name):
         "shared_dgrad_gate_up": ("tensor", 2.0 * T * d * 2 * ms, False),
         "shared_wgrad_down": ("tensor", 2.0 * T * d * ms, False),
         "shared_wgrad_gate_up": ("tensor", 2.0 * T * 2 * ms * d, False),
-        "dispatch_gather": ("hbm", R * d * (2 + act), mx),
+        "dispatch_gather": ("hbm", R * d * (2 + act * (2 if mx and train else 1)), mx),
         "combine": ("hbm", R * d * 2 + T * d * 2 * (2 if ms else 1) + R * 8, mx),
-        "reverse_combine": ("hbm", R * d * (6 + (act if mx else 0)), mx),
+        "reverse_combine": ("hbm", R * d * (6 + (2 * act if mx else 0)), mx),
         "reverse_dispatch": ("hbm", R * d * 2 + T * d * 2 * (2 if ms else 1) + T * E * 4, mx),
         "route_schedule": ("hbm", T * E * 4 + R * 4 * 6, mx),
     }
@@ -392,7 +396,7 @@ def run_ours(args, cfg, passes, rank, world, local_rank):
         launches += 4 if name == "route_schedule" else 1
     kernel_total = sum(t for _, t in per.values()) or 1.0
     dom = max(per.items(), key=lambda kv: kv[1][1])[0]
-    bound, work, dom_mx = kernel_work(cfg, dom) or ("tensor", float("nan"), False)
+    bound, work, dom_mx = kernel_work(cfg, dom, bwd) or ("tensor", float("nan"), False)
     cnt, tot = per[dom]
     avg_ms = tot / cnt
     if bound == "tensor":

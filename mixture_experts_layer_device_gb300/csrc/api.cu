@@ -94,6 +94,10 @@ void saved_layout(const Dims &D, Layout &L) {
   L.add("o", D.Rp * D.d * 2);
   L.add("GU", D.Rp * 2 * D.m * 2);
   L.add("h", D.Rp * D.m * 2);
+  if (D.mx) {  // column-blocked codes of the gathered x (written by the dispatch)
+    L.add("xT", D.d * D.Rp);
+    L.add("xT_sf", D.d * D.Rp / 32);
+  }
   if (D.ms) {
     L.add("s_GU", D.Tp * 2 * D.ms * 2);
     L.add("s_h", D.Tp * D.ms * 2);
@@ -120,13 +124,13 @@ void ws_layout(const Dims &D, Layout &L) {
   }
   if (!D.bwd) return;
   L.add("g", D.R * 4);
-  L.add("dO", D.Rp * D.d * 2);
+  if (!D.mx) L.add("dO", D.Rp * D.d * 2);  // MXFP8 keeps dO only as codes
   L.add("dGU", D.Rp * 2 * D.m * 2);
   L.add("dX", D.Rp * D.d * 2);
   L.add("dOT", D.d * D.Rp * eb);
   L.add("hT", D.m * D.Rp * eb);
   L.add("dGUT", 2 * D.m * D.Rp * eb);
-  L.add("xT", D.d * D.Rp * eb);
+  if (!D.mx) L.add("xT", D.d * D.Rp * eb);  // MXFP8: kept in `saved` by the dispatch
   if (D.mx) {
     L.add("dOq", D.Rp * D.d);
     L.add("dOq_sf", D.Rp * D.d / 32);
@@ -135,7 +139,6 @@ void ws_layout(const Dims &D, Layout &L) {
     L.add("dOT_sf", D.d * D.Rp / 32);
     L.add("hT_sf", D.m * D.Rp / 32);
     L.add("dGUT_sf", 2 * D.m * D.Rp / 32);
-    L.add("xT_sf", D.d * D.Rp / 32);
   }
   if (D.ms) {
     L.add("s_dGU", D.Tp * 2 * D.ms * 2);
@@ -491,7 +494,9 @@ int moe_forward(const moe_config *cfg, const void *x, const float *logits, const
   uint8_t *xs_sf = reinterpret_cast<uint8_t *>(W.ptr(ws, "xs_sf"));
   {
     Traced tr("dispatch_gather", s);
-    rc = cuda_status(moe::launch_gather(x, D.T, D.d, D.k, D.E, rb, D.Rp, D.mx, xs, xs_sf, s));
+    uint8_t *xT = (train && D.mx) ? reinterpret_cast<uint8_t *>(S.ptr(saved, "xT")) : nullptr;
+    uint8_t *xT_sf = (train && D.mx) ? reinterpret_cast<uint8_t *>(S.ptr(saved, "xT_sf")) : nullptr;
+    rc = cuda_status(moe::launch_gather(x, D.T, D.d, D.k, D.E, rb, D.Rp, D.mx, xs, xs_sf, xT, xT_sf, s));
   }
   if (rc != MOE_OK) return rc;
   // S4 gate/up GEMM + SwiGLU (+ MX quantisation of h)
@@ -656,8 +661,12 @@ int moe_backward(const moe_config *cfg, const void *dy, const void *x, const moe
   // B1 reverse combine: dO = w * dy (bf16; MX row-quantised along d), g = <dy, o>
   {
     Traced tr("reverse_combine", s);
-    rc = cuda_status(moe::launch_reverse_combine(dy, o, D.T, D.d, D.k, D.E, rb, D.Rp, dO, g, mx,
-                                                 u8("dOq"), u8("dOq_sf"), s));
+    if (mx)  // also writes dO^T's column-blocked codes (the wgrad operand)
+      rc = cuda_status(moe::launch_reverse_combine_mx(dy, o, D.d, D.k, D.E, rb, D.Rp, g, u8("dOq"),
+                                                      u8("dOq_sf"), u8("dOT"), u8("dOT_sf"), s));
+    else
+      rc = cuda_status(moe::launch_reverse_combine(dy, o, D.T, D.d, D.k, D.E, rb, D.Rp, dO, g, mx,
+                                                   u8("dOq"), u8("dOq_sf"), s));
   }
   if (rc != MOE_OK) return rc;
   // B2 dgrad of the down projection with the SwiGLU backward in the epilogue
@@ -724,11 +733,12 @@ int moe_backward(const moe_config *cfg, const void *dy, const void *x, const moe
     int C;
     bool gather;
     const char *dst, *sf;
-  } trs[] = {{dO, D.d, false, "dOT", "dOT_sf"},
+  } trs[] = {{mx ? nullptr : dO, D.d, false, "dOT", "dOT_sf"},  // MXFP8: written by B1
              {h, D.m, false, "hT", "hT_sf"},
              {dGU, 2 * D.m, false, "dGUT", "dGUT_sf"},
-             {x, D.d, true, "xT", "xT_sf"}};
+             {mx ? nullptr : x, D.d, true, "xT", "xT_sf"}};  // MXFP8: written by the dispatch
   for (const Tr &t : trs) {
+    if (!t.src) continue;
     {
       Traced tr("transpose_wgrad_operands", s);
       rc = cuda_status(moe::launch_transpose_rows(t.src, t.C, 0, nrows_dev, D.Rp, t.gather, D.k, D.E,
@@ -769,7 +779,7 @@ int moe_backward(const moe_config *cfg, const void *dy, const void *x, const moe
     q.epi = moe::EPI_STORE;
     q.a = W.ptr(ws, "dGUT");
     q.a_rows = 2L * D.m;
-    q.b = W.ptr(ws, "xT");
+    q.b = mx ? S.ptr(saved, "xT") : W.ptr(ws, "xT");
     q.b_rows = D.d;
     q.K = D.Rp;
     q.g = base_args(moe::SCHED_GROUP_K, D.E, rb.poff, p.status);
@@ -777,7 +787,7 @@ int moe_backward(const moe_config *cfg, const void *dy, const void *x, const moe
     q.g.n_tiles = D.d / q.bn;
     q.g.sfa = u8("dGUT_sf");
     q.g.sfa_kg = static_cast<int>(D.Rp / 128);
-    q.g.sfb = u8("xT_sf");
+    q.g.sfb = mx ? reinterpret_cast<uint8_t *>(S.ptr(saved, "xT_sf")) : u8("xT_sf");
     q.g.sfb_kg = static_cast<int>(D.Rp / 128);
     q.g.out = dW_gu;
     q.g.ldo = D.d;

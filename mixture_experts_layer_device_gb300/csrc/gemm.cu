@@ -54,7 +54,8 @@ struct Cfg {
   static constexpr int SF_COL0 = NUM_ACC * BN;
   static constexpr uint32_t TX_BYTES = STAGE_BYTES + SF_STAGE;
   static constexpr uint32_t IDESC = MX ? idesc_mxf8(128, BN) : idesc_bf16(128, BN);
-  // epilogue staging: per epilogue warp two 2 KB halves (32 rows x 64 B, 64-byte swizzle)
+  // epilogue staging: 2 KB pieces (32 rows x 64 B, 64-byte swizzle), 16 KB split
+  // over the epilogue warps
   static constexpr int STAGING_BYTES = 4 * 4096;
   // barriers: full[S], empty[S], tfull[NA], tempty[NA], done
   static constexpr int NBAR = 2 * STAGES + 2 * NUM_ACC + 1;

@@ -38,18 +38,20 @@ MOE_DEV uint32_t mx_block_words(const float *v, uint32_t *w) {
 
 // Per-warp writer of 32-row x 64-byte output pieces: each lane places its row's
 // 64 bytes in a 64-byte-swizzled shared-memory buffer (conflict-free), then one
-// lane stores the box with TMA.  With two buffers the staging of one piece
-// overlaps the store of the previous one.
+// lane stores the box with TMA.  With several buffers the staging of one piece
+// overlaps the stores of the previous ones; a buffer is reused only after the
+// store that last read it has finished reading shared memory.
 struct Stager {
   uint8_t *buf;  // nbuf x 2 KB, 512-byte aligned
   int n;
-  int nbuf;      // 1 or 2
+  int nbuf;      // 1, 2 or 4
   MOE_DEV Stager(uint8_t *b, int buffers) : buf(b), n(0), nbuf(buffers) {}
   MOE_DEV void put(const CUtensorMap *map, const uint32_t *w16, int c0, int row0, int lane) {
-    uint8_t *half = buf + (nbuf == 2 ? (n & 1) * 2048 : 0);
-    if (lane == 0) {
-      if (nbuf == 2 && n >= 2) bulk_wait_read<1>();
-      if (nbuf == 1 && n >= 1) bulk_wait_read<0>();
+    uint8_t *half = buf + (n & (nbuf - 1)) * 2048;
+    if (lane == 0 && n >= nbuf) {
+      if (nbuf == 4) bulk_wait_read<3>();
+      else if (nbuf == 2) bulk_wait_read<1>();
+      else bulk_wait_read<0>();
     }
     __syncwarp();
 #pragma unroll

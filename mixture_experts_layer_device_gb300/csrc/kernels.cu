@@ -254,6 +254,57 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint4 *__restrict__ x
   }
 }
 
+// MXFP8 dispatch as 32-row tiles: rows of x (by token) are quantised along d
+// into xs codes [Rp, d] (+ tiled scales, K = d) and, when xT is given, the
+// block's 32 rows are also quantised per column into the transposed codes
+// xT [d, ld_t] (+ tiled scales, K = ld_t): the wgrad operand of the backward.
+__global__ void __launch_bounds__(256) gather_mx_tile_kernel(const uint16_t *__restrict__ x, int d, int k,
+                                                             int E, RouteBufs b, uint8_t *__restrict__ xs,
+                                                             uint8_t *__restrict__ xs_sf,
+                                                             uint8_t *__restrict__ xT,
+                                                             uint8_t *__restrict__ xT_sf, long ld_t) {
+  __shared__ float tile[32][65];
+  const int r0 = blockIdx.x * 32;
+  if (r0 >= __ldg(b.poff + E)) return;
+  const int rr = threadIdx.x >> 3;
+  const int cc = (threadIdx.x & 7) * 8;
+  const int pr = r0 + rr;
+  const int tok = token_of_row(b, E, k, pr, nullptr);
+  const uint16_t *xr = x + static_cast<size_t>(tok < 0 ? 0 : tok) * d;
+  const int c = threadIdx.x >> 2;
+  const int part = threadIdx.x & 3;
+  for (int cb = 0; cb < d; cb += 256) {
+    uint4 q[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      q[j] = tok >= 0 ? __ldg(reinterpret_cast<const uint4 *>(xr + cb + 64 * j + cc)) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float f[8];
+      unpack8(q[j], f);
+      const int col = cb + 64 * j + cc;
+      uint32_t byte;
+      const uint2 code = mx_encode8_quad(f, &byte);
+      *reinterpret_cast<uint2 *>(xs + static_cast<size_t>(pr) * d + col) = code;
+      if ((threadIdx.x & 3) == 0) xs_sf[sf_tiled_offset(pr, col >> 5, d)] = static_cast<uint8_t>(byte);
+      if (xT) {
+        __syncthreads();
+#pragma unroll
+        for (int t = 0; t < 8; ++t) tile[rr][cc + t] = f[t];
+        __syncthreads();
+        float v[8];
+#pragma unroll
+        for (int t = 0; t < 8; ++t) v[t] = tile[part * 8 + t][c];
+        const size_t ocol = static_cast<size_t>(cb + 64 * j + c);
+        uint32_t tb;
+        const uint2 tcode = mx_encode8_quad(v, &tb);
+        *reinterpret_cast<uint2 *>(xT + ocol * ld_t + r0 + part * 8) = tcode;
+        if (part == 0) xT_sf[sf_tiled_offset(static_cast<long>(ocol), r0 / 32, ld_t)] = static_cast<uint8_t>(tb);
+      }
+    }
+  }
+}
+
 // ------------------------------------------------------------ S6: combine
 __global__ void __launch_bounds__(256) combine_kernel(const uint4 *__restrict__ o,
                                                       const uint4 *__restrict__ s_out, int T, int d,
@@ -333,6 +384,77 @@ __global__ void __launch_bounds__(256) reverse_combine_kernel(
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
   if (tok >= 0 && lane == 0) g[slot] = dot;
+}
+
+// ------------------------------------------------------------ B1, MXFP8: fused
+// Block: 32 padded rows x all d columns, swept in 256-column chunks (four
+// 64-column sub-tiles, loads issued up front).  Per element dO = bf16(w * dy);
+// written as row-blocked E4M3 codes (the dgrad operand, blocks of 32 along d)
+// and, through a shared-memory transpose, as column-blocked codes of dO^T
+// (the wgrad operand, blocks of the block's 32 rows).  g = <dy, o> per row is
+// accumulated per thread in column order and reduced over the row's 8
+// threads in a fixed shuffle order.
+__global__ void __launch_bounds__(256) reverse_combine_mx_kernel(
+    const uint16_t *__restrict__ dy, const uint16_t *__restrict__ o, int d, int k, int E, RouteBufs b,
+    float *__restrict__ g, uint8_t *__restrict__ dOq, uint8_t *__restrict__ dOq_sf,
+    uint8_t *__restrict__ dOT, uint8_t *__restrict__ dOT_sf, long ld_t) {
+  __shared__ float tile[32][65];
+  const int r0 = blockIdx.x * 32;
+  if (r0 >= __ldg(b.poff + E)) return;
+  const int rr = threadIdx.x >> 3;
+  const int cc = (threadIdx.x & 7) * 8;
+  const int pr = r0 + rr;
+  int slot = 0;
+  const int tok = token_of_row(b, E, k, pr, &slot);
+  const float wv = tok >= 0 ? __ldg(b.w + slot) : 0.f;
+  const uint16_t *dyr = dy + static_cast<size_t>(tok < 0 ? 0 : tok) * d;
+  const uint16_t *orow = o + static_cast<size_t>(pr) * d;
+  const int c = threadIdx.x >> 2;    // transposed output row within a sub-tile
+  const int part = threadIdx.x & 3;  // 8 source rows each
+  float dot = 0.f;
+  for (int cb = 0; cb < d; cb += 256) {
+    uint4 qy[4], qo[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const size_t col = static_cast<size_t>(cb + 64 * j + cc);
+      qy[j] = tok >= 0 ? __ldg(reinterpret_cast<const uint4 *>(dyr + col)) : make_uint4(0, 0, 0, 0);
+      qo[j] = tok >= 0 ? __ldg(reinterpret_cast<const uint4 *>(orow + col)) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float fy[8], fo[8], f[8];
+      unpack8(qy[j], fy);
+      unpack8(qo[j], fo);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        dot = fmaf(fy[q], fo[q], dot);
+        f[q] = round_bf16(wv * fy[q]);
+      }
+      const int col = cb + 64 * j + cc;
+      // row-blocked codes: the 4 threads cc/8 = 4h..4h+3 hold one block of 32
+      uint32_t byte;
+      const uint2 code = mx_encode8_quad(f, &byte);
+      *reinterpret_cast<uint2 *>(dOq + static_cast<size_t>(pr) * d + col) = code;
+      if ((threadIdx.x & 3) == 0) dOq_sf[sf_tiled_offset(pr, col >> 5, d)] = static_cast<uint8_t>(byte);
+      // column-blocked codes of the transpose
+      __syncthreads();
+#pragma unroll
+      for (int q = 0; q < 8; ++q) tile[rr][cc + q] = f[q];
+      __syncthreads();
+      float t[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) t[q] = tile[part * 8 + q][c];
+      const size_t ocol = static_cast<size_t>(cb + 64 * j + c);
+      uint32_t tbyte;
+      const uint2 tcode = mx_encode8_quad(t, &tbyte);
+      *reinterpret_cast<uint2 *>(dOT + ocol * ld_t + r0 + part * 8) = tcode;
+      if (part == 0) dOT_sf[sf_tiled_offset(static_cast<long>(ocol), r0 / 32, ld_t)] = static_cast<uint8_t>(tbyte);
+    }
+  }
+  // g: the 8 threads of a row are lanes 8u..8u+7 of one warp
+#pragma unroll
+  for (int off = 4; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
+  if ((threadIdx.x & 7) == 0 && tok >= 0) g[slot] = dot;
 }
 
 // ------------------------------------------------------------ B6: reverse dispatch
@@ -485,13 +607,15 @@ cudaError_t launch_route(const float *logits, int T, int E, int k, const RouteBu
 }
 
 cudaError_t launch_gather(const void *x, int T, int d, int k, int E, const RouteBufs &b,
-                          int64_t rp_max, bool mx, void *xs, uint8_t *xs_sf, cudaStream_t s) {
+                          int64_t rp_max, bool mx, void *xs, uint8_t *xs_sf, uint8_t *xT, uint8_t *xT_sf,
+                          cudaStream_t s) {
   (void)T;
-  const unsigned grid = blocks_for(rp_max, 8);
   if (mx)
-    gather_kernel<true><<<grid, 256, 0, s>>>(static_cast<const uint4 *>(x), d, k, E, b, rp_max, xs, xs_sf);
+    gather_mx_tile_kernel<<<blocks_for(rp_max, 32), 256, 0, s>>>(
+        static_cast<const uint16_t *>(x), d, k, E, b, static_cast<uint8_t *>(xs), xs_sf, xT, xT_sf, rp_max);
   else
-    gather_kernel<false><<<grid, 256, 0, s>>>(static_cast<const uint4 *>(x), d, k, E, b, rp_max, xs, xs_sf);
+    gather_kernel<false><<<blocks_for(rp_max, 8), 256, 0, s>>>(static_cast<const uint4 *>(x), d, k, E, b,
+                                                                rp_max, xs, xs_sf);
   return cudaGetLastError();
 }
 
@@ -516,6 +640,15 @@ cudaError_t launch_reverse_combine(const void *dy, const void *o, int T, int d, 
     reverse_combine_kernel<false><<<grid, 256, 0, s>>>(
         static_cast<const uint4 *>(dy), static_cast<const uint4 *>(o), d, k, E, b, rp_max,
         static_cast<uint4 *>(dO), g, dOq, dOq_sf);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_reverse_combine_mx(const void *dy, const void *o, int d, int k, int E,
+                                      const RouteBufs &b, int64_t rp_max, float *g, uint8_t *dOq,
+                                      uint8_t *dOq_sf, uint8_t *dOT, uint8_t *dOT_sf, cudaStream_t s) {
+  reverse_combine_mx_kernel<<<blocks_for(rp_max, 32), 256, 0, s>>>(
+      static_cast<const uint16_t *>(dy), static_cast<const uint16_t *>(o), d, k, E, b, g, dOq, dOq_sf,
+      dOT, dOT_sf, rp_max);
   return cudaGetLastError();
 }
 

@@ -31,9 +31,12 @@ cudaError_t launch_route(const float *logits, int T, int E, int k, const RouteBu
                          cudaStream_t s);
 
 // Gather routed rows of x into padded expert-sorted order (zero padding rows).
-// MX: writes E4M3 codes [Rp, d] and tiled scales (K = d) instead of bf16 rows.
+// MX: writes E4M3 codes [Rp, d] and tiled scales (K = d) instead of bf16 rows,
+// and, when xT is not NULL, the column-blocked transposed codes xT [d, Rp]
+// (+ tiled scales, K = Rp) of the same rows.
 cudaError_t launch_gather(const void *x, int T, int d, int k, int E, const RouteBufs &b,
-                          int64_t rp_max, bool mx, void *xs, uint8_t *xs_sf, cudaStream_t s);
+                          int64_t rp_max, bool mx, void *xs, uint8_t *xs_sf, uint8_t *xT, uint8_t *xT_sf,
+                          cudaStream_t s);
 
 // y[t] = bf16( sum_j w[t,j] * o[row(t,j)] + s[t] ), fixed j order.
 cudaError_t launch_combine(const void *o, const void *s_out, int T, int d, int k, int E,
@@ -44,6 +47,14 @@ cudaError_t launch_combine(const void *o, const void *s_out, int T, int d, int k
 cudaError_t launch_reverse_combine(const void *dy, const void *o, int T, int d, int k, int E,
                                    const RouteBufs &b, int64_t rp_max, void *dO, float *g,
                                    bool mx, uint8_t *dOq, uint8_t *dOq_sf, cudaStream_t s);
+
+// Reverse combine, MXFP8, fused with the wgrad operand: g[slot] = <dy[t], o[row]>,
+// dO = bf16(w * dy) written as row-blocked codes dOq [Rp, d] (+ tiled scales,
+// K = d) and column-blocked transposed codes dOT [d, ld_t = Rp] (+ tiled
+// scales, K = Rp); padding rows give zero codes.
+cudaError_t launch_reverse_combine_mx(const void *dy, const void *o, int d, int k, int E,
+                                      const RouteBufs &b, int64_t rp_max, float *g, uint8_t *dOq,
+                                      uint8_t *dOq_sf, uint8_t *dOT, uint8_t *dOT_sf, cudaStream_t s);
 
 // Reverse dispatch: dx[t] = bf16( sum_j dX[row(t,j)] + dxs[t] ); dlogits row.
 cudaError_t launch_reverse_dispatch(const void *dX, const void *dxs, const float *g, int T,
