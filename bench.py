@@ -78,35 +78,66 @@ def layer_work(cfg, passes):
 
 
 def kernel_work(cfg, name, train=False):
-    """(bound, algorithmic work per launch, is_mx) for a traced kernel name.
+    """(FLOPs, algorithmic bytes, is_mx) of one step's launches of a traced
+    kernel name (one launch per step for every GEMM and for the dispatch,
+    combine and reverse kernels; the transposes and the route/schedule are
+    several launches under one name).
 
-    With MXFP8 experts a training pass's dispatch also writes the transposed
-    codes of x, and its reverse combine both the row- and column-blocked codes
-    of dO."""
+    Bytes count every input read once and every output written once (x and
+    dy once per token, not once per routed copy).  With MXFP8 experts a
+    training pass's dispatch also writes the column-blocked codes of x, and its
+    reverse combine both the row- and column-blocked codes of dO; the forward
+    gate/up GEMM of a training pass saves G|U and h in bf16 next to the MXFP8
+    codes of h."""
     T, d, m, E, k, ms = (cfg[n] for n in ("T", "d", "m", "E", "k", "m_shared"))
     R = T * k
     mx = cfg["fmt"] == "mxfp8"
-    act = (1 + 1 / 32) if mx else 2
+    a = (1 + 1 / 32) if mx else 2          # bytes per stored expert operand element
+    h_out = (R * 2 * m * 2 + R * m * 2 + (R * m * a if mx else 0)) if train else R * m * a
+    sh_out = (T * 2 * ms * 2 + T * ms * 2) if train else T * ms * 2
     tbl = {
-        "gemm1_gate_up_swiglu": ("tensor", 2.0 * R * 2 * m * d, mx),
-        "gemm2_down": ("tensor", 2.0 * R * d * m, mx),
-        "dgrad_down_swiglu_bwd": ("tensor", 2.0 * R * m * d, mx),
-        "dgrad_gate_up": ("tensor", 2.0 * R * d * 2 * m, mx),
-        "wgrad_down": ("tensor", 2.0 * R * d * m, mx),
-        "wgrad_gate_up": ("tensor", 2.0 * R * 2 * m * d, mx),
-        "shared_gemm1_gate_up_swiglu": ("tensor", 2.0 * T * 2 * ms * d, False),
-        "shared_gemm2_down": ("tensor", 2.0 * T * d * ms, False),
-        "shared_dgrad_down_swiglu_bwd": ("tensor", 2.0 * T * ms * d, False),
-        "shared_dgrad_gate_up": ("tensor", 2.0 * T * d * 2 * ms, False),
-        "shared_wgrad_down": ("tensor", 2.0 * T * d * ms, False),
-        "shared_wgrad_gate_up": ("tensor", 2.0 * T * 2 * ms * d, False),
-        "dispatch_gather": ("hbm", R * d * (2 + act * (2 if mx and train else 1)), mx),
-        "combine": ("hbm", R * d * 2 + T * d * 2 * (2 if ms else 1) + R * 8, mx),
-        "reverse_combine": ("hbm", R * d * (6 + (2 * act if mx else 0)), mx),
-        "reverse_dispatch": ("hbm", R * d * 2 + T * d * 2 * (2 if ms else 1) + T * E * 4, mx),
-        "route_schedule": ("hbm", T * E * 4 + R * 4 * 6, mx),
+        "gemm1_gate_up_swiglu": (2.0 * R * 2 * m * d, R * d * a + E * 2 * m * d * a + h_out, mx),
+        "gemm2_down": (2.0 * R * d * m, R * m * a + E * d * m * a + R * d * 2, mx),
+        "dgrad_down_swiglu_bwd": (2.0 * R * m * d, R * d * a + E * m * d * a + R * 2 * m * 2 * 2
+                                  + (R * 2 * m * a if mx else 0), mx),
+        "dgrad_gate_up": (2.0 * R * d * 2 * m, R * 2 * m * a + E * d * 2 * m * a + R * d * 2, mx),
+        "wgrad_down": (2.0 * R * d * m, R * d * a + R * m * a + E * d * m * 2, mx),
+        "wgrad_gate_up": (2.0 * R * 2 * m * d, R * 2 * m * a + R * d * a + E * 2 * m * d * 2, mx),
+        "shared_gemm1_gate_up_swiglu": (2.0 * T * 2 * ms * d, T * d * 2 + 2 * ms * d * 2 + sh_out, False),
+        "shared_gemm2_down": (2.0 * T * d * ms, T * ms * 2 + d * ms * 2 + T * d * 2, False),
+        "shared_dgrad_down_swiglu_bwd": (2.0 * T * ms * d, T * d * 2 + ms * d * 2 + 2 * T * 2 * ms * 2, False),
+        "shared_dgrad_gate_up": (2.0 * T * d * 2 * ms, T * 2 * ms * 2 + d * 2 * ms * 2 + T * d * 2, False),
+        "shared_wgrad_down": (2.0 * T * d * ms, T * d * 2 + T * ms * 2 + d * ms * 2, False),
+        "shared_wgrad_gate_up": (2.0 * T * 2 * ms * d, T * 2 * ms * 2 + T * d * 2 + 2 * ms * d * 2, False),
+        "dispatch_gather": (0.0, T * d * 2 + R * d * a * (2 if mx and train else 1), mx),
+        "combine": (0.0, R * d * 2 + R * 8 + T * d * 2 * (2 if ms else 1), mx),
+        "reverse_combine": (0.0, T * d * 2 + R * d * 2 + R * 8 + (2 * R * d * a if mx else R * d * 2), mx),
+        "reverse_dispatch": (0.0, R * d * 2 + R * 8 + T * d * 2 * (2 if ms else 1) + T * E * 4, mx),
+        "route_schedule": (0.0, T * E * 4 + R * 4 * 6, mx),
+        "transpose_wgrad_operands": (0.0, (R * 2 * m * 2 + R * m * 2) + (R * 2 * m + R * m) * a
+                                     + (0 if mx else 2 * (R * d * 2 + R * d * a)), mx),
+        "shared_transpose_wgrad_operands": (0.0, 2 * 2 * T * (ms + d + 2 * ms + d), False),
     }
     return tbl.get(name)
+
+
+def kernel_roofline(cfg, name, train, ms_per_step, peaks):
+    """Bound, achieved and peak of one kernel: the larger of its tensor time
+    (FLOPs at the tensor peak of its arithmetic) and its HBM time (algorithmic
+    bytes at the copy bandwidth) names the bound."""
+    w = kernel_work(cfg, name, train)
+    if w is None or ms_per_step <= 0:
+        return None
+    flops, byts, mx = w
+    tpeak = peaks["bf16_tflops_sustained"] * (MX_OVER_BF16 if mx else 1.0)
+    t_tensor = flops / (tpeak * 1e12)
+    t_hbm = byts / (peaks["hbm_gbs"] * 1e9)
+    sec = ms_per_step / 1e3
+    if t_tensor >= t_hbm:
+        return {"bound": "tensor", "achieved": flops / sec / 1e12, "peak": tpeak, "unit": "TFLOP/s", "mx": mx,
+                "t_tensor_ms": t_tensor * 1e3, "t_hbm_ms": t_hbm * 1e3}
+    return {"bound": "hbm", "achieved": byts / sec / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s", "mx": mx,
+            "t_tensor_ms": t_tensor * 1e3, "t_hbm_ms": t_hbm * 1e3}
 
 
 class Clocks:
@@ -396,23 +427,25 @@ def run_ours(args, cfg, passes, rank, world, local_rank):
         launches += 4 if name == "route_schedule" else 1
     kernel_total = sum(t for _, t in per.values()) or 1.0
     dom = max(per.items(), key=lambda kv: kv[1][1])[0]
-    bound, work, dom_mx = kernel_work(cfg, dom, bwd) or ("tensor", float("nan"), False)
     cnt, tot = per[dom]
     avg_ms = tot / cnt
+    kr = kernel_roofline(cfg, dom, bwd, tot / args.steps, peaks) or {
+        "bound": "tensor", "achieved": float("nan"), "peak": float("nan"), "unit": "TFLOP/s", "mx": False,
+        "t_tensor_ms": float("nan"), "t_hbm_ms": float("nan")}
+    bound, achieved, peak, unit = kr["bound"], kr["achieved"], kr["peak"], kr["unit"]
     if bound == "tensor":
-        peak = peaks["bf16_tflops_sustained"] * (MX_OVER_BF16 if dom_mx else 1.0)
-        achieved = work / (avg_ms / 1e3) / 1e12
-        unit = "TFLOP/s"
-        peak_note = ("MXFP8 = %s sustained BF16 x %.0f (nominal ratio)" % (peaks_src, MX_OVER_BF16) if dom_mx
+        peak_note = ("MXFP8 = %s sustained BF16 x %.0f (nominal ratio)" % (peaks_src, MX_OVER_BF16) if kr["mx"]
                      else "%s sustained BF16" % peaks_src)
     else:
-        peak = peaks["hbm_gbs"]
-        achieved = work / (avg_ms / 1e3) / 1e9
-        unit = "GB/s"
         peak_note = "%s HBM copy bandwidth" % peaks_src
     traffic = NCU_TRAFFIC.get((cfg["name"], dom))
-    kernels = {n: {"launches_per_step": c / args.steps, "ms_per_step": round(t / args.steps, 4),
-                   "share": round(t / kernel_total, 4)} for n, (c, t) in sorted(per.items(), key=lambda kv: -kv[1][1])}
+    kernels = {}
+    for n, (c, t) in sorted(per.items(), key=lambda kv: -kv[1][1]):
+        kernels[n] = {"launches_per_step": c / args.steps, "ms_per_step": round(t / args.steps, 4),
+                      "share": round(t / kernel_total, 4)}
+        r = kernel_roofline(cfg, n, bwd, t / args.steps, peaks)
+        if r is not None:
+            kernels[n].update({"bound": r["bound"], "frac": round(r["achieved"] / r["peak"], 4)})
     rs = per.get("route_schedule", (0, 0.0))[1] / kernel_total
 
     # layer roofline (algorithmic work of the whole step)

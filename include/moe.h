@@ -124,11 +124,14 @@ size_t moe_workspace_bytes(const moe_config *cfg);
 size_t moe_saved_bytes(const moe_config *cfg);
 
 /* Byte offset and size of a named sub-buffer of `saved` (which = 0) or of the
- * workspace (which = 1), for inspection by tests and tools.  Names: "idx",
- * "w", "counts", "offsets", "perm", "inv", "poff", "o", "GU", "h", "xs",
- * "xs_sf", "hq", "hq_sf", "s_out", "s_GU", "s_h", "dO", "dX", "dGU", "g".
- * Row-indexed buffers use padded rows (see moe_forward).  Returns MOE_OK or
- * MOE_ERR_ARG (unknown name / buffer absent for this config). */
+ * workspace (which = 1), for inspection by tests and tools.  Names include
+ * "idx", "w", "counts", "offsets", "perm", "inv", "poff", "o", "GU", "h",
+ * "s_GU", "s_h" and, with MXFP8 experts, "xT", "xT_sf" (saved); "xs",
+ * "xs_sf", "hq", "hq_sf", "s_out", "dX", "dGU", "g", "dOq", "dOq_sf", "dOT",
+ * "dOT_sf" (workspace; "dO" exists only with BF16 experts, whose backward
+ * materialises dO in bf16).  Row-indexed buffers use padded rows (see
+ * moe_forward).  Returns MOE_OK or MOE_ERR_ARG (unknown name / buffer absent
+ * for this config). */
 int moe_buffer_info(const moe_config *cfg, int which, const char *name, size_t *offset,
                     size_t *bytes);
 
