@@ -110,6 +110,9 @@ def kernel_work(cfg, name, train=False):
         "shared_wgrad_down": (2.0 * T * d * ms, T * d * 2 + T * ms * 2 + d * ms * 2, False),
         "shared_wgrad_gate_up": (2.0 * T * 2 * ms * d, T * 2 * ms * 2 + T * d * 2 + 2 * ms * d * 2, False),
         "dispatch_gather": (0.0, T * d * 2 + R * d * a * (2 if mx and train else 1), mx),
+        # ring: dispatch + gate/up GEMM in one launch; the ring itself stays on chip (L2)
+        "dispatch_gemm1_ring": (2.0 * R * 2 * m * d, T * d * 2 + E * 2 * m * d * a + h_out
+                                + (R * d * a if train else 0), mx),
         "combine": (0.0, R * d * 2 + R * 8 + T * d * 2 * (2 if ms else 1), mx),
         "reverse_combine": (0.0, T * d * 2 + R * d * 2 + R * 8 + (2 * R * d * a if mx else R * d * 2), mx),
         "reverse_dispatch": (0.0, R * d * 2 + R * 8 + T * d * 2 * (2 if ms else 1) + T * E * 4, mx),
@@ -316,8 +319,9 @@ def run_ours(args, cfg, passes, rank, world, local_rank):
 
     x, logits, dy, gu_all, dn_all, shared = build_inputs(cfg, dev, passes)
     bwd = passes == "fwdbwd"
+    ring_rows = args.ring if cfg["fmt"] == "mxfp8" else 0
     layer = MoELayer(cfg["T"], cfg["d"], cfg["m"], cfg["E"], cfg["k"], cfg["fmt"], shared=shared, backward=bwd,
-                     device=dev, stacked=(gu_all, dn_all))
+                     device=dev, stacked=(gu_all, dn_all), ring_rows=ring_rows, gather_sms=args.gather_sms)
     s0_ms = time_s0(layer, gu_all, dn_all, stream)
     sample = None
     want_cpu = rank == 0 and world == 1 and not args.no_cpu_baseline and not args.profile_run
@@ -464,6 +468,8 @@ def run_ours(args, cfg, passes, rank, world, local_rank):
         "config": {"workload": cfg["name"], "pass": "fwd+bwd" if bwd else "fwd", "T": cfg["T"], "d": cfg["d"],
                    "m": cfg["m"], "E": cfg["E"], "k": cfg["k"], "m_shared": cfg["m_shared"],
                    "experts": cfg["fmt"], "router_bias": cfg["bias"], "parallelism": "replicas" if world > 1 else "1gpu",
+                   "dispatch": ("ring of %d rows, %d gather SMs" % (layer.cfg.ring_rows, layer.cfg.gather_sms or 8)
+                                if layer.cfg.ring_rows else "materialised"),
                    "l2": "inputs larger than L2 (%.1f GB of expert weights read per step)"
                          % (3 * cfg["E"] * cfg["d"] * cfg["m"] * (1.03 if mx else 2) / 1e9)},
         "fwd_tokens_per_s": round(fwd_value, 1),
@@ -542,6 +548,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile-run", action="store_true",
                     help="time the step once (no fwd-only, e2e or CPU legs): for profiler launch lists")
+    ap.add_argument("--ring", type=int, default=0,
+                    help="MXFP8: dispatch through a ring of this many rows (0 = materialised dispatch)")
+    ap.add_argument("--gather-sms", type=int, default=0, help="gather SMs of the ring launch (0 = default)")
     ap.add_argument("--override", default="",
                     help="comma-separated shape overrides, e.g. T=2048,E=16 (smaller cases for profiling)")
     args = ap.parse_args()

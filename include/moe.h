@@ -69,10 +69,10 @@ typedef enum {
 /* moe_config.flags bits */
 #define MOE_FLAG_BACKWARD 1 /* size the workspace for moe_backward as well */
 /* Test hook for the device-side failure path: in moe_forward the gate/up
- * GEMM's load warp issues nothing, so its MMA warp's wait runs out (limit
- * 50 ms instead of 4 s); the kernels drain and return, moe_get_status then
- * reports MOE_ERR_TIMEOUT, and the outputs of that call are undefined.  The
- * CUDA context stays usable. */
+ * GEMM's load warp issues nothing (with a ring: the gather CTAs publish no
+ * tile), so the waits for its data run out (limit 50 ms instead of 4 s); the
+ * kernels drain and return, moe_get_status then reports MOE_ERR_TIMEOUT, and
+ * the outputs of that call are undefined.  The CUDA context stays usable. */
 #define MOE_FLAG_DEBUG_STARVE 2
 
 /*
@@ -82,12 +82,30 @@ typedef enum {
  * the routed experts' arithmetic; the shared expert is always BF16.  flags:
  * MOE_FLAG_BACKWARD and/or MOE_FLAG_DEBUG_STARVE, or 0 (moe_backward needs a
  * workspace sized with MOE_FLAG_BACKWARD).
+ *
+ * Dispatch ring (MXFP8 only; "Mixture-of-Kittens" wiki page, flowchart, and
+ * daily-ai-frontier summary, TL;DR: a fixed-size token ring between the
+ * dispatch and the expert GEMMs, and an SM split between data movement and
+ * GEMM work handing off through device counters):
+ *   ring_rows  = 0: the dispatch writes every routed row to the workspace
+ *                (one row per routed (token, expert) pair, padded per expert);
+ *              > 0: a multiple of 128.  The forward's dispatch and gate/up
+ *                GEMM run as one persistent launch: `gather_sms` SMs gather
+ *                and quantise 128-row tiles of expert-sorted rows into a ring
+ *                of ring_rows rows in the workspace, the other SMs run the
+ *                GEMM on the ring, and each slot is refilled once every GEMM
+ *                tile has loaded it.  Experts with more rows than the ring
+ *                pass through it in pieces.  Results are bitwise identical to
+ *                ring_rows = 0 for every ring size and SM split.
+ *   gather_sms = gather SMs of the ring launch (0 = 8; at most 64).
  */
 typedef struct {
   int32_t T, d, m, E, k;
   int32_t m_shared;
   int32_t dtype; /* moe_dtype */
   int32_t flags;
+  int32_t ring_rows;
+  int32_t gather_sms;
 } moe_config;
 
 /*

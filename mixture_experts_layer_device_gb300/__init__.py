@@ -25,7 +25,8 @@ WEIGHT_FIELDS = ["gu", "gu_scale", "dn", "dn_scale", "gu_t", "gu_t_scale", "dn_t
 
 
 class MoeConfig(ctypes.Structure):
-    _fields_ = [(n, ctypes.c_int32) for n in ("T", "d", "m", "E", "k", "m_shared", "dtype", "flags")]
+    _fields_ = [(n, ctypes.c_int32) for n in ("T", "d", "m", "E", "k", "m_shared", "dtype", "flags",
+                                              "ring_rows", "gather_sms")]
 
 
 class MoeWeights(ctypes.Structure):
@@ -90,10 +91,10 @@ def _stream(stream):
     return stream.cuda_stream
 
 
-def config(T, d, m, E, k, m_shared=0, dtype=MOE_BF16, flags=0):
+def config(T, d, m, E, k, m_shared=0, dtype=MOE_BF16, flags=0, ring_rows=0, gather_sms=0):
     if isinstance(dtype, str):
         dtype = MOE_MXFP8 if dtype == "mxfp8" else MOE_BF16
-    return MoeConfig(T, d, m, E, k, m_shared, dtype, flags)
+    return MoeConfig(T, d, m, E, k, m_shared, dtype, flags, ring_rows, gather_sms)
 
 
 def weights(**kw):

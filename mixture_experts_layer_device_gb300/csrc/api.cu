@@ -18,9 +18,15 @@ using moe::GemmArgs;
 using moe::RouteBufs;
 
 // ---------------------------------------------------------------- shapes
+// Gather CTAs of the ring kernel when moe_config.gather_sms is 0.
+constexpr int kDefaultGatherCtas = 8;
+
 struct Dims {
   int T, d, m, E, k, ms;
   bool mx, bwd, starve;
+  bool ring;           // MXFP8 forward dispatch through the persistent ring kernel
+  int ring_slots;      // ring capacity in 128-row tiles
+  int gather_ctas;     // gather CTAs of the ring kernel
   long R, Rp, Tp;
   int nchunks;
 };
@@ -33,6 +39,9 @@ int check_config(const moe_config *c, Dims *D) {
   if (c->dtype != MOE_BF16 && c->dtype != MOE_MXFP8) return MOE_ERR_ARG;
   if ((c->flags & ~(MOE_FLAG_BACKWARD | MOE_FLAG_DEBUG_STARVE)) != 0) return MOE_ERR_ARG;
   if (c->d % 256 || c->m % 128 || c->m_shared % 128) return MOE_ERR_SHAPE;
+  if (c->ring_rows < 0 || c->gather_sms < 0 || c->gather_sms > 64) return MOE_ERR_ARG;
+  if (c->ring_rows > 0 && c->dtype != MOE_MXFP8) return MOE_ERR_ARG;
+  if (c->ring_rows % 128) return MOE_ERR_SHAPE;
   const long R = static_cast<long>(c->T) * c->k;
   const long Rp = (R + 127L * c->E + 127) / 128 * 128;
   if (Rp >= (1L << 31)) return MOE_ERR_SHAPE;
@@ -45,6 +54,9 @@ int check_config(const moe_config *c, Dims *D) {
   D->mx = c->dtype == MOE_MXFP8;
   D->bwd = (c->flags & MOE_FLAG_BACKWARD) != 0;
   D->starve = (c->flags & MOE_FLAG_DEBUG_STARVE) != 0;
+  D->ring = c->ring_rows > 0;
+  D->ring_slots = c->ring_rows / 128;
+  D->gather_ctas = c->gather_sms > 0 ? c->gather_sms : kDefaultGatherCtas;
   D->R = R;
   D->Rp = Rp;
   D->Tp = (c->T + 127L) / 128 * 128;
@@ -109,9 +121,15 @@ void ws_layout(const Dims &D, Layout &L) {
   L.add("hist", static_cast<size_t>(D.nchunks) * D.E * 4);
   add_route(D, L);  // used when the forward saves nothing
   const size_t eb = D.mx ? 1 : 2;
-  L.add("xs", D.Rp * D.d * eb);
+  if (D.ring) {  // a fixed ring of 128-row tiles instead of every dispatched row
+    L.add("ring", static_cast<size_t>(D.ring_slots) * 128 * D.d);
+    L.add("ring_sf", static_cast<size_t>(D.ring_slots) * 128 * D.d / 32);
+    L.add("ring_ctrl", (2 * static_cast<size_t>(D.ring_slots) + 1) * 4);
+  } else {
+    L.add("xs", D.Rp * D.d * eb);
+  }
   if (D.mx) {
-    L.add("xs_sf", D.Rp * D.d / 32);
+    if (!D.ring) L.add("xs_sf", D.Rp * D.d / 32);
     L.add("hq", D.Rp * D.m);
     L.add("hq_sf", D.Rp * D.m / 32);
   } else {
@@ -333,6 +351,27 @@ int run_gemm(const char *name, const Gemm &q, const DeviceInfo &dev, cudaStream_
       moe::launch_gemm(q.mx, q.bn, q.epi, ta, tb, to, to2, tq, q.g, static_cast<int>(grid), s));
 }
 
+// The persistent ring launch: one CTA per SM, the first gather_ctas of which
+// gather into the ring (fewer if the device has few SMs).
+int run_gemm_ring(const char *name, const Gemm &q, const Dims &D, const DeviceInfo &dev, cudaStream_t s) {
+  Traced tr(name, s);
+  CUtensorMap ta, tb, to, to2, tq;
+  memset(&to, 0, sizeof(to));
+  memset(&to2, 0, sizeof(to2));
+  memset(&tq, 0, sizeof(tq));
+  if (!make_map(&ta, q.a, true, q.K, q.a_rows) || !make_map(&tb, q.b, true, q.K, q.b_rows)) return MOE_ERR_CUDA;
+  if (q.g.out && !make_store_map(&to, q.g.out, false, q.g.ldo, q.g.ldo, q.out_rows)) return MOE_ERR_CUDA;
+  if (q.g.out2 && !make_store_map(&to2, q.g.out2, false, q.g.ldo2, q.g.ldo2, q.out_rows))
+    return MOE_ERR_CUDA;
+  if (q.g.outq && !make_store_map(&tq, q.g.outq, true, q.g.ldq, q.g.ldq, q.out_rows)) return MOE_ERR_CUDA;
+  int grid = moe::ring_max_ctas();
+  if (grid > dev.num_sms) grid = dev.num_sms;
+  if (grid < 2) return MOE_ERR_CUDA;
+  moe::GemmArgs g = q.g;
+  g.ring.gather_ctas = D.gather_ctas < grid ? D.gather_ctas : grid / 2;
+  return cuda_status(moe::launch_gemm_ring(ta, tb, to, to2, tq, g, grid, s));
+}
+
 int bn_for(long n) { return n % 256 == 0 ? 256 : 128; }
 
 struct Ptrs {
@@ -489,13 +528,14 @@ int moe_forward(const moe_config *cfg, const void *x, const float *logits, const
 
   // S1 + S2
   if ((rc = route_impl(D, logits, rb, s)) != MOE_OK) return rc;
-  // S3 dispatch gather (+ MX quantisation of x)
-  char *xs = W.ptr(ws, "xs");
-  uint8_t *xs_sf = reinterpret_cast<uint8_t *>(W.ptr(ws, "xs_sf"));
-  {
+  // S3 dispatch gather (+ MX quantisation of x); with a ring it runs inside
+  // the gate/up GEMM launch below.
+  char *xs = D.ring ? W.ptr(ws, "ring") : W.ptr(ws, "xs");
+  uint8_t *xs_sf = reinterpret_cast<uint8_t *>(D.ring ? W.ptr(ws, "ring_sf") : W.ptr(ws, "xs_sf"));
+  uint8_t *xT = (train && D.mx) ? reinterpret_cast<uint8_t *>(S.ptr(saved, "xT")) : nullptr;
+  uint8_t *xT_sf = (train && D.mx) ? reinterpret_cast<uint8_t *>(S.ptr(saved, "xT_sf")) : nullptr;
+  if (!D.ring) {
     Traced tr("dispatch_gather", s);
-    uint8_t *xT = (train && D.mx) ? reinterpret_cast<uint8_t *>(S.ptr(saved, "xT")) : nullptr;
-    uint8_t *xT_sf = (train && D.mx) ? reinterpret_cast<uint8_t *>(S.ptr(saved, "xT_sf")) : nullptr;
     rc = cuda_status(moe::launch_gather(x, D.T, D.d, D.k, D.E, rb, D.Rp, D.mx, xs, xs_sf, xT, xT_sf, s));
   }
   if (rc != MOE_OK) return rc;
@@ -511,7 +551,7 @@ int moe_forward(const moe_config *cfg, const void *x, const float *logits, const
     q.bn = 256;
     q.epi = moe::EPI_SWIGLU;
     q.a = xs;
-    q.a_rows = D.Rp;
+    q.a_rows = D.ring ? static_cast<long>(D.ring_slots) * 128 : D.Rp;
     q.b = Wt->gu;
     q.b_rows = static_cast<long>(D.E) * 2 * D.m;
     q.K = D.d;
@@ -538,7 +578,27 @@ int moe_forward(const moe_config *cfg, const void *x, const float *logits, const
     }
     q.max_tiles = (D.Rp / 128) * q.g.n_tiles;
     q.out_rows = D.Rp;
-    if ((rc = run_gemm("gemm1_gate_up_swiglu", q, dev, s)) != MOE_OK) return rc;
+    if (D.ring) {
+      moe::RingArgs &r = q.g.ring;
+      r.x = static_cast<const uint16_t *>(x);
+      r.rb = rb;
+      r.k = D.k;
+      r.slots = D.ring_slots;
+      r.codes = reinterpret_cast<uint8_t *>(xs);
+      r.sf = xs_sf;
+      r.xT = xT;
+      r.xT_sf = xT_sf;
+      r.ld_t = D.Rp;
+      int *ctrl = reinterpret_cast<int *>(W.ptr(ws, "ring_ctrl"));
+      r.ready = ctrl;
+      r.freed = ctrl + D.ring_slots;
+      r.abort = ctrl + 2 * D.ring_slots;
+      if (cudaMemsetAsync(ctrl, 0, (2 * static_cast<size_t>(D.ring_slots) + 1) * 4, s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+      if ((rc = run_gemm_ring("dispatch_gemm1_ring", q, D, dev, s)) != MOE_OK) return rc;
+    } else if ((rc = run_gemm("gemm1_gate_up_swiglu", q, dev, s)) != MOE_OK) {
+      return rc;
+    }
   }
   // S5 down GEMM
   {

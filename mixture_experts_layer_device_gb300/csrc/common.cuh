@@ -88,6 +88,50 @@ MOE_DEV bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort, int 
   }
 }
 
+// ---------------------------------------------------------------- global flags
+// Counters in global memory that CTAs of one (co-resident) launch hand off
+// through: acquire loads, release stores / adds, and a bounded wait.
+MOE_DEV int ld_acquire_gpu(const int *p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+MOE_DEV void st_release_gpu(int *p, int v) {
+  asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+MOE_DEV void red_release_add_gpu(int *p, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Orders this thread's generic-proxy view of global memory with its later (or
+// earlier) async-proxy accesses (TMA loads of data other CTAs wrote).
+MOE_DEV void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+
+// Waits until *p >= target.  Gives up (returns false) when the launch-wide
+// abort word `gabort` or the CTA's `labort` is set, or after timeout_ns; on a
+// timeout it records kStatusTimeout and sets both abort words.
+MOE_DEV bool flag_wait_geq(const int *p, int target, int *gabort, volatile int *labort, int *status,
+                           unsigned long long timeout_ns) {
+  if (ld_acquire_gpu(p) >= target) return true;
+  const unsigned long long t0 = globaltimer();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 16; ++i) {
+      __nanosleep(64);
+      if (ld_acquire_gpu(p) >= target) return true;
+    }
+    if ((labort && *labort) || *reinterpret_cast<volatile int *>(gabort)) {
+      if (labort) *labort = 1;
+      return false;
+    }
+    if (globaltimer() - t0 > timeout_ns) {
+      if (status) atomicOr(status, kStatusTimeout);
+      atomicExch(gabort, 1);
+      if (labort) *labort = 1;
+      return false;
+    }
+  }
+}
+
 // ---------------------------------------------------------------- TMA
 MOE_DEV void tma_load_2d(const CUtensorMap *map, uint64_t *bar, void *dst, int c0, int c1) {
   asm volatile(

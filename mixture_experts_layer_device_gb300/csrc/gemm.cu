@@ -23,6 +23,7 @@
 // Every output element is produced by one CTA with a fixed K order, so results
 // are bitwise reproducible.
 #include "common.cuh"
+#include "dispatch_tile.cuh"
 #include "gemm_common.cuh"
 #include "kernels.h"
 
@@ -133,6 +134,41 @@ MOE_DEV Tile decode_tile(const GemmArgs &g, int t) {
   return ti;
 }
 
+// Gather role of the ring kernel (warps 0..7 of a gather CTA; the other warps
+// leave at once): tiles u = blockIdx.x, + gather_ctas, ... in increasing
+// order.  Before writing tile u into slot u % slots the slot's previous tile
+// (u - slots) must have been loaded by all n_tiles GEMM tiles that read it;
+// after writing, the slot is published with ready[slot] = u + 1 (release).
+// The expert-sorted row order and the per-row quantisation are those of the
+// stand-alone dispatch, so the GEMM sees the same codes.
+MOE_DEV void ring_gather_role(const GemmArgs &g, uint8_t *smem) {
+  const RingArgs &r = g.ring;
+  const int tid = static_cast<int>(threadIdx.x);
+  if (tid >= 256 || g.debug_starve) return;
+  float(*tile)[65] = reinterpret_cast<float(*)[65]>(smem);
+  volatile int *stop = reinterpret_cast<volatile int *>(smem + 32 * 65 * sizeof(float));
+  auto sync = [] { asm volatile("bar.sync 1, 256;" ::: "memory"); };
+  const int tiles = __ldg(r.rb.poff + g.E) >> 7;
+  for (int u = static_cast<int>(blockIdx.x); u < tiles; u += r.gather_ctas) {
+    const int slot = u % r.slots;
+    if (tid == 0)
+      *stop = flag_wait_geq(r.freed + slot, (u / r.slots) * g.n_tiles, r.abort, nullptr, g.status,
+                            g.timeout_ns)
+                  ? 0
+                  : 1;
+    sync();
+    if (*stop) break;
+#pragma unroll 1
+    for (int sub = 0; sub < 4; ++sub)
+      dispatch_rows32(r.x, g.K, r.k, g.E, r.rb, u * 128 + sub * 32, slot * 128 + sub * 32, r.codes, r.sf,
+                      r.xT, r.xT_sf, r.ld_t, tile, tid, sync);
+    __threadfence();
+    fence_proxy_async_global();
+    sync();
+    if (tid == 0) st_release_gpu(r.ready + slot, u + 1);
+  }
+}
+
 // Epilogue warps per CTA: 8 (two per TMEM lane quarter, each draining half of
 // the columns), except SwiGLU backward on 256-column tiles, whose per-row
 // working set needs the registers of a 192-thread CTA (4 warps).
@@ -141,7 +177,7 @@ __host__ __device__ constexpr int epi_warps() {
   return (EPI == EPI_SWIGLU_BWD && BN == 256) ? 4 : 8;
 }
 
-template <bool MX, int BN, int EPI>
+template <bool MX, int BN, int EPI, bool RING = false>
 __global__ void __launch_bounds__(64 + 32 * epi_warps<EPI, BN>(), 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmO2,
@@ -150,6 +186,15 @@ __global__ void __launch_bounds__(64 + 32 * epi_warps<EPI, BN>(), 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
+  if constexpr (RING) {
+    if (static_cast<int>(blockIdx.x) < g.ring.gather_ctas) {
+      ring_gather_role(g, smem);
+      return;
+    }
+  }
+  // GEMM CTAs: this CTA's index among them and their number
+  const int cta = static_cast<int>(blockIdx.x) - (RING ? g.ring.gather_ctas : 0);
+  const int ncta = static_cast<int>(gridDim.x) - (RING ? g.ring.gather_ctas : 0);
   uint8_t *sf_base = smem + C::STAGES * C::STAGE_BYTES;
   uint8_t *staging = sf_base + C::STAGES * C::SF_STAGE;
   uint64_t *bars = reinterpret_cast<uint64_t *>(staging + C::STAGING_BYTES);
@@ -196,8 +241,17 @@ __global__ void __launch_bounds__(64 + 32 * epi_warps<EPI, BN>(), 1)
       uint32_t ph = 0;
       int armed[C::STAGES];
       for (int s = 0; s < C::STAGES; ++s) armed[s] = -1;
-      for (int t = blockIdx.x; t < total && !*abort_flag && !g.debug_starve; t += gridDim.x) {
+      for (int t = cta; t < total && !*abort_flag && (RING || !g.debug_starve); t += ncta) {
         const Tile ti = decode_tile<C::BK, BN, EPI>(g, t);
+        int a_row = ti.a_row;  // row of A to load (the tile's ring slot with a ring)
+        if constexpr (RING) {
+          const int u = ti.a_row >> 7;
+          const int slot = u % g.ring.slots;
+          if (!flag_wait_geq(g.ring.ready + slot, u + 1, g.ring.abort, abort_flag, g.status, g.timeout_ns))
+            break;
+          fence_proxy_async_global();
+          a_row = slot * 128;
+        }
         for (int kb = 0; kb < ti.nk; ++kb) {
           if (!mbar_wait(&empty[stage], ph ^ 1u, abort_flag, g.status, g.timeout_ns)) break;
           uint8_t *sa = smem + stage * C::STAGE_BYTES;
@@ -205,13 +259,13 @@ __global__ void __launch_bounds__(64 + 32 * epi_warps<EPI, BN>(), 1)
           mbar_arrive_expect_tx(&full[stage], C::TX_BYTES);
           armed[stage] = static_cast<int>(ph);
           const int kc = ti.k0 + kb * C::BK;
-          tma_load_2d(&tmA, &full[stage], sa, kc, ti.a_row);
+          tma_load_2d(&tmA, &full[stage], sa, kc, a_row);
           tma_load_2d(&tmB, &full[stage], sb, kc, ti.b_row0);
           if (BN == 256) tma_load_2d(&tmB, &full[stage], sb + 128 * 128, kc, ti.b_row1);
           if constexpr (MX) {
             uint8_t *sfs = sf_base + stage * C::SF_STAGE;
             const int kg = kc >> 7;
-            bulk_load(sfs, g.sfa + (static_cast<size_t>(ti.a_row >> 7) * g.sfa_kg + kg) * 512, 512,
+            bulk_load(sfs, g.sfa + (static_cast<size_t>(a_row >> 7) * g.sfa_kg + kg) * 512, 512,
                       &full[stage]);
             bulk_load(sfs + 512, g.sfb + (static_cast<size_t>(ti.b_row0 >> 7) * g.sfb_kg + kg) * 512,
                       512, &full[stage]);
@@ -241,7 +295,7 @@ __global__ void __launch_bounds__(64 + 32 * epi_warps<EPI, BN>(), 1)
       int acc = 0;
       uint32_t aph = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      for (int t = cta; t < total && ok; t += ncta) {
         const Tile ti = decode_tile<C::BK, BN, EPI>(g, t);
         if (!mbar_wait(&tempty[acc], aph ^ 1u, abort_flag, g.status, g.timeout_ns)) break;
         tc_fence_after();
@@ -280,6 +334,10 @@ __global__ void __launch_bounds__(64 + 32 * epi_warps<EPI, BN>(), 1)
           }
         }
         if (!ok) break;
+        if constexpr (RING) {
+          // Every load of this tile from its ring slot has landed in shared memory.
+          red_release_add_gpu(g.ring.freed + (ti.a_row >> 7) % g.ring.slots, 1);
+        }
         mma_commit(&tfull[acc]);
         if (++acc == C::NUM_ACC) {
           acc = 0;
@@ -305,7 +363,7 @@ __global__ void __launch_bounds__(64 + 32 * epi_warps<EPI, BN>(), 1)
     }
     int acc = 0;
     uint32_t aph = 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+    for (int t = cta; t < total; t += ncta) {
       const Tile ti = decode_tile<C::BK, BN, EPI>(g, t);
       if constexpr (EPI == EPI_SWIGLU_BWD) {
         // The saved G|U rows this tile's epilogue reads come from HBM: pull them
@@ -364,7 +422,45 @@ cudaError_t launch_one(const CUtensorMap &ta, const CUtensorMap &tb, const CUten
   return cudaGetLastError();
 }
 
+int ring_ctas_resident() {
+  using C = Cfg<true, 256>;
+  if (cudaFuncSetAttribute(gemm_kernel<true, 256, EPI_SWIGLU, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(C::SMEM)) != cudaSuccess)
+    return 0;
+  int per_sm = 0, dev = 0, sms = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemm_kernel<true, 256, EPI_SWIGLU, true>,
+                                                    64 + 32 * epi_warps<EPI_SWIGLU, 256>(),
+                                                    C::SMEM) != cudaSuccess ||
+      cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return 0;
+  return per_sm * sms;
+}
+
 }  // namespace
+
+int ring_max_ctas() { return ring_ctas_resident(); }
+
+cudaError_t launch_gemm_ring(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &to,
+                             const CUtensorMap &to2, const CUtensorMap &tq, const GemmArgs &g, int grid,
+                             cudaStream_t s) {
+  using C = Cfg<true, 256>;
+  // Gather and GEMM CTAs wait on each other: all of them must be resident at
+  // once, which the cooperative launch guarantees (or refuses).
+  if (grid <= g.ring.gather_ctas || g.ring.gather_ctas <= 0 || grid > ring_ctas_resident())
+    return cudaErrorInvalidValue;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(64 + 32 * epi_warps<EPI_SWIGLU, 256>(), 1, 1);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gemm_kernel<true, 256, EPI_SWIGLU, true>, ta, tb, to, to2, tq, g);
+}
 
 cudaError_t launch_gemm(bool mx, int bn, int epi, const CUtensorMap &ta, const CUtensorMap &tb,
                         const CUtensorMap &to, const CUtensorMap &to2, const CUtensorMap &tq,

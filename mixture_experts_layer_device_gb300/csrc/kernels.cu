@@ -13,48 +13,12 @@
 #include <math.h>
 
 #include "common.cuh"
+#include "dispatch_tile.cuh"
 #include "kernels.h"
 
 namespace moe {
 
 namespace {
-
-MOE_DEV void unpack8(const uint4 &q, float *f) {
-  f[0] = bf16lo(q.x); f[1] = bf16hi(q.x);
-  f[2] = bf16lo(q.y); f[3] = bf16hi(q.y);
-  f[4] = bf16lo(q.z); f[5] = bf16hi(q.z);
-  f[6] = bf16lo(q.w); f[7] = bf16hi(q.w);
-}
-MOE_DEV uint4 pack8(const float *f) {
-  return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
-                    pack_bf16x2(f[6], f[7]));
-}
-// MX-encode 8 values owned by this lane; the 4 lanes (lane & ~3 .. +3) hold one
-// 32-element block.  Returns the 8 codes; *byte gets the block's scale byte.
-MOE_DEV uint2 mx_encode8_quad(const float *f, uint32_t *byte) {
-  float am = 0.f;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) am = fmaxf(am, fabsf(f[i]));
-  am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
-  am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 2));
-  const uint32_t b = mx_scale_byte(am);
-  const float s = mx_inv_scale(b);
-  uint2 c;
-  c.x = e4m3x2(f[0] * s, f[1] * s) | (e4m3x2(f[2] * s, f[3] * s) << 16);
-  c.y = e4m3x2(f[4] * s, f[5] * s) | (e4m3x2(f[6] * s, f[7] * s) << 16);
-  *byte = b;
-  return c;
-}
-
-// Token of padded expert-sorted row pr, or -1 for a padding row.
-MOE_DEV int token_of_row(const RouteBufs &b, int E, int k, int pr, int *slot_out) {
-  const int e = expert_of_row(b.poff, E, pr);
-  const int local = pr - __ldg(b.poff + e);
-  if (local >= __ldg(b.counts + e)) return -1;
-  const int slot = __ldg(b.inv + __ldg(b.offsets + e) + local);
-  if (slot_out) *slot_out = slot;
-  return slot / k;
-}
 
 // ------------------------------------------------------------ S1: route
 // One warp per token.  Top-k by repeated warp argmax under the total order
@@ -228,30 +192,17 @@ __global__ void __launch_bounds__(128) sched_scatter_kernel(const int *__restric
 }
 
 // ------------------------------------------------------------ S3: dispatch
-// One warp per padded row; rows of x are copied (bf16) or quantised (MXFP8).
-template <bool MX>
-__global__ void __launch_bounds__(256) gather_kernel(const uint4 *__restrict__ x, int d, int k, int E,
-                                                     RouteBufs b, int64_t rp_max, void *xs,
-                                                     uint8_t *__restrict__ xs_sf) {
+// BF16: one warp per padded row copies its token's row of x (zeros for padding rows).
+__global__ void __launch_bounds__(256) gather_bf16_kernel(const uint4 *__restrict__ x, int d, int k, int E,
+                                                          RouteBufs b, int64_t rp_max, uint4 *__restrict__ xs) {
   const int64_t pr = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (pr >= rp_max || pr >= __ldg(b.poff + E)) return;
   const int tok = token_of_row(b, E, k, static_cast<int>(pr), nullptr);
   const int vec = d >> 3;
   const uint4 *src = x + static_cast<size_t>(tok < 0 ? 0 : tok) * vec;
-  for (int i = lane; i < vec; i += 32) {
-    const uint4 q = tok >= 0 ? __ldg(src + i) : make_uint4(0, 0, 0, 0);
-    if constexpr (!MX) {
-      reinterpret_cast<uint4 *>(xs)[static_cast<size_t>(pr) * vec + i] = q;
-    } else {
-      float f[8];
-      unpack8(q, f);
-      uint32_t byte;
-      const uint2 c = mx_encode8_quad(f, &byte);
-      reinterpret_cast<uint2 *>(xs)[static_cast<size_t>(pr) * vec + i] = c;
-      if ((lane & 3) == 0) xs_sf[sf_tiled_offset(pr, i >> 2, d)] = static_cast<uint8_t>(byte);
-    }
-  }
+  for (int i = lane; i < vec; i += 32)
+    xs[static_cast<size_t>(pr) * vec + i] = tok >= 0 ? __ldg(src + i) : make_uint4(0, 0, 0, 0);
 }
 
 // MXFP8 dispatch as 32-row tiles: rows of x (by token) are quantised along d
@@ -266,43 +217,8 @@ __global__ void __launch_bounds__(256) gather_mx_tile_kernel(const uint16_t *__r
   __shared__ float tile[32][65];
   const int r0 = blockIdx.x * 32;
   if (r0 >= __ldg(b.poff + E)) return;
-  const int rr = threadIdx.x >> 3;
-  const int cc = (threadIdx.x & 7) * 8;
-  const int pr = r0 + rr;
-  const int tok = token_of_row(b, E, k, pr, nullptr);
-  const uint16_t *xr = x + static_cast<size_t>(tok < 0 ? 0 : tok) * d;
-  const int c = threadIdx.x >> 2;
-  const int part = threadIdx.x & 3;
-  for (int cb = 0; cb < d; cb += 256) {
-    uint4 q[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-      q[j] = tok >= 0 ? __ldg(reinterpret_cast<const uint4 *>(xr + cb + 64 * j + cc)) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      float f[8];
-      unpack8(q[j], f);
-      const int col = cb + 64 * j + cc;
-      uint32_t byte;
-      const uint2 code = mx_encode8_quad(f, &byte);
-      *reinterpret_cast<uint2 *>(xs + static_cast<size_t>(pr) * d + col) = code;
-      if ((threadIdx.x & 3) == 0) xs_sf[sf_tiled_offset(pr, col >> 5, d)] = static_cast<uint8_t>(byte);
-      if (xT) {
-        __syncthreads();
-#pragma unroll
-        for (int t = 0; t < 8; ++t) tile[rr][cc + t] = f[t];
-        __syncthreads();
-        float v[8];
-#pragma unroll
-        for (int t = 0; t < 8; ++t) v[t] = tile[part * 8 + t][c];
-        const size_t ocol = static_cast<size_t>(cb + 64 * j + c);
-        uint32_t tb;
-        const uint2 tcode = mx_encode8_quad(v, &tb);
-        *reinterpret_cast<uint2 *>(xT + ocol * ld_t + r0 + part * 8) = tcode;
-        if (part == 0) xT_sf[sf_tiled_offset(static_cast<long>(ocol), r0 / 32, ld_t)] = static_cast<uint8_t>(tb);
-      }
-    }
-  }
+  dispatch_rows32(x, d, k, E, b, r0, r0, xs, xs_sf, xT, xT_sf, ld_t, tile, static_cast<int>(threadIdx.x),
+                  [] { __syncthreads(); });
 }
 
 // ------------------------------------------------------------ S6: combine
@@ -614,8 +530,8 @@ cudaError_t launch_gather(const void *x, int T, int d, int k, int E, const Route
     gather_mx_tile_kernel<<<blocks_for(rp_max, 32), 256, 0, s>>>(
         static_cast<const uint16_t *>(x), d, k, E, b, static_cast<uint8_t *>(xs), xs_sf, xT, xT_sf, rp_max);
   else
-    gather_kernel<false><<<blocks_for(rp_max, 8), 256, 0, s>>>(static_cast<const uint4 *>(x), d, k, E, b,
-                                                                rp_max, xs, xs_sf);
+    gather_bf16_kernel<<<blocks_for(rp_max, 8), 256, 0, s>>>(static_cast<const uint4 *>(x), d, k, E, b, rp_max,
+                                                              static_cast<uint4 *>(xs));
   return cudaGetLastError();
 }
 

@@ -83,6 +83,26 @@ cudaError_t launch_transpose_bf16(const void *src, int batch, int rows, int cols
 enum GemmSched { SCHED_GROUP_M = 0, SCHED_DENSE = 1, SCHED_GROUP_K = 2 };
 enum GemmEpi { EPI_STORE = 0, EPI_SWIGLU = 1, EPI_SWIGLU_BWD = 2 };
 
+// Persistent ring dispatch (S3 fused with the MXFP8 gate/up GEMM): the first
+// `gather_ctas` CTAs of the launch gather and quantise 128-row tiles of
+// expert-sorted rows into a ring of `slots` tiles; the other CTAs run the GEMM
+// on the ring.  Tile u (padded rows [128u, 128u + 128)) goes to slot u % slots.
+struct RingArgs {
+  const uint16_t *x;  // [T, d] bf16 tokens
+  RouteBufs rb;       // route / schedule arrays (token of each row)
+  int k;
+  int slots;          // ring capacity in 128-row tiles
+  int gather_ctas;    // CTAs of the launch that gather (the rest compute)
+  uint8_t *codes;     // [slots * 128, d] E4M3 codes: the GEMM's A operand
+  uint8_t *sf;        // tiled scales of `codes` (K = d)
+  uint8_t *xT;        // training: column-blocked codes of x [d, ld_t], else NULL
+  uint8_t *xT_sf;
+  long ld_t;
+  int *ready;         // [slots] index + 1 of the tile last published in the slot
+  int *freed;         // [slots] GEMM tiles whose loads from the slot have landed (cumulative)
+  int *abort;         // launch-wide abort word (set when any wait runs out)
+};
+
 struct GemmArgs {
   int sched;
   int E;              // groups (experts); 1 for dense
@@ -110,7 +130,9 @@ struct GemmArgs {
   int m_half;         // SWIGLU / SWIGLU_BWD: m
   int *status;
   unsigned long long timeout_ns;  // limit of every wait in the launch
-  int debug_starve;   // test hook: the producer issues no loads (the MMA wait runs out)
+  int debug_starve;   // test hook: the producer issues no loads (the MMA wait runs out);
+                      // with a ring, the gather CTAs publish nothing instead
+  RingArgs ring;      // launch_gemm_ring only
 };
 
 // D = A * B^T with A [rows, K] and B [rows, K] K-major (TMA maps built by the
@@ -122,6 +144,16 @@ struct GemmArgs {
 cudaError_t launch_gemm(bool mx, int bn, int epi, const CUtensorMap &ta, const CUtensorMap &tb,
                         const CUtensorMap &to, const CUtensorMap &to2, const CUtensorMap &tq,
                         const GemmArgs &args, int grid, cudaStream_t s);
+
+// The MXFP8 gate/up GEMM with SwiGLU epilogue fed by the ring (args.ring):
+// one cooperative launch of `grid` CTAs (all co-resident, one per SM), of
+// which args.ring.gather_ctas gather.  `ta` maps the ring codes
+// [slots * 128, d].  args.ring.ready / freed / abort must be zero at launch.
+cudaError_t launch_gemm_ring(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &to,
+                             const CUtensorMap &to2, const CUtensorMap &tq, const GemmArgs &args, int grid,
+                             cudaStream_t s);
+// CTAs of the ring GEMM that can be resident at once on the current device.
+int ring_max_ctas();
 
 // Tensor maps of one 2-CTA GEMM launch: operands (box 128 rows x 128 bytes,
 // 128-byte swizzle), MXFP8 scale buffers viewed as rows of 256 bytes (box

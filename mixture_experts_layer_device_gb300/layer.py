@@ -20,6 +20,10 @@ def _u8(nbytes, device):
 class MoELayer:
     """One MoE layer's prepared weights and buffers on one GPU.
 
+    ``ring_rows`` > 0 (MXFP8) runs the forward's dispatch and gate/up GEMM as
+    one persistent launch through a ring of that many rows, ``gather_sms`` of
+    whose SMs gather (0 = the library default).
+
     ``expert(e)`` returns the bf16 masters (W_gu [2m, d], W_dn [d, m]) of
     expert e as device tensors; they are converted expert by expert into the
     layout the kernels read (MXFP8 codes + tiled scales, and for the backward
@@ -29,7 +33,7 @@ class MoELayer:
     """
 
     def __init__(self, T, d, m, E, k, fmt, expert=None, shared=None, backward=False, device="cuda",
-                 stacked=None):
+                 stacked=None, ring_rows=0, gather_sms=0):
         self.T, self.d, self.m, self.E, self.k = T, d, m, E, k
         self.fmt = fmt
         self.mx = fmt == "mxfp8"
@@ -37,7 +41,7 @@ class MoELayer:
         self.backward_enabled = backward
         self.device = device
         self.cfg = config(T, d, m, E, k, self.ms, MOE_MXFP8 if self.mx else MOE_BF16,
-                          MOE_FLAG_BACKWARD if backward else 0)
+                          MOE_FLAG_BACKWARD if backward else 0, ring_rows, gather_sms)
         self.Rp = moe_padded_rows(self.cfg)
         self.ws = _u8(moe_workspace_bytes(self.cfg), device)
         self.saved = _u8(moe_saved_bytes(self.cfg), device) if backward else None

@@ -83,3 +83,23 @@ def test_full_size_backward_sampled():
     bw = om.expert_backward(dO, X, fw["GU_saved"], fw["h_saved"], W_gu, W_dn, fmt, ops)
     assert rel(mi.to_f64(g["dW_gu"][e_dw]), bw["dW_gu"]) < tol
     assert rel(mi.to_f64(g["dW_dn"][e_dw]), bw["dW_dn"]) < tol
+
+
+def test_full_size_ring_bitwise_equal():
+    """DeepSeek-V4-Pro shape through an 8,192-row ring (64 slots, 8 gather SMs),
+    well below the rows of each hot expert: the whole output equals the
+    materialised dispatch's bit for bit, from a much smaller workspace."""
+    import mixture_experts_layer_device_gb300 as pkg
+    cfg, x, logits, gu_all, dn_all, shared, layer = build("deepseek-v4-pro", backward=False)
+    y0 = layer.forward(x, logits)
+    assert layer.status() == 0
+    counts = layer.view(1, "counts", "i32", (cfg["E"],)).cpu().numpy()
+    assert counts.max() > 8192
+    c = layer.cfg
+    rc = pkg.MoeConfig(c.T, c.d, c.m, c.E, c.k, c.m_shared, c.dtype, c.flags, 8192, 8)
+    ws = torch.empty(pkg.moe_workspace_bytes(rc), dtype=torch.uint8, device=x.device)
+    assert ws.numel() < layer.ws.numel()
+    y1 = torch.empty_like(y0)
+    pkg.check(pkg.moe_forward(rc, x, logits, layer.W, y1, None, ws))
+    assert pkg.moe_get_status(ws) == 0
+    assert torch.equal(y0, y1)
