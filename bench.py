@@ -111,8 +111,9 @@ def kernel_work(cfg, name, train=False):
         "shared_wgrad_gate_up": (2.0 * T * 2 * ms * d, T * 2 * ms * 2 + T * d * 2 + 2 * ms * d * 2, False),
         "dispatch_gather": (0.0, T * d * 2 + R * d * a * (2 if mx and train else 1), mx),
         # ring: dispatch + gate/up GEMM in one launch; the ring itself stays on chip (L2)
-        "dispatch_gemm1_ring": (2.0 * R * 2 * m * d, T * d * 2 + E * 2 * m * d * a + h_out
-                                + (R * d * a if train else 0), mx),
+        "quantize_tokens": (0.0, T * d * 2 + T * d * a, mx),
+        "dispatch_xT": (0.0, T * d * 2 + R * d * a, mx),
+        "dispatch_gemm1_ring": (2.0 * R * 2 * m * d, T * d * a + E * 2 * m * d * a + h_out, mx),
         "combine": (0.0, R * d * 2 + R * 8 + T * d * 2 * (2 if ms else 1), mx),
         "reverse_combine": (0.0, T * d * 2 + R * d * 2 + R * 8 + (2 * R * d * a if mx else R * d * 2), mx),
         "reverse_dispatch": (0.0, R * d * 2 + R * 8 + T * d * 2 * (2 if ms else 1) + T * E * 4, mx),

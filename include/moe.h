@@ -98,6 +98,7 @@ typedef enum {
  *                pass through it in pieces.  Results are bitwise identical to
  *                ring_rows = 0 for every ring size and SM split.
  *   gather_sms = gather SMs of the ring launch (0 = 8; at most 64).
+ *   The ring needs d <= 8192 (MOE_ERR_SHAPE otherwise).
  */
 typedef struct {
   int32_t T, d, m, E, k;

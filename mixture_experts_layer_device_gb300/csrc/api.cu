@@ -42,6 +42,7 @@ int check_config(const moe_config *c, Dims *D) {
   if (c->ring_rows < 0 || c->gather_sms < 0 || c->gather_sms > 64) return MOE_ERR_ARG;
   if (c->ring_rows > 0 && c->dtype != MOE_MXFP8) return MOE_ERR_ARG;
   if (c->ring_rows % 128) return MOE_ERR_SHAPE;
+  if (c->ring_rows > 0 && c->d > 8192) return MOE_ERR_SHAPE;  // the ring's gather copies whole rows
   const long R = static_cast<long>(c->T) * c->k;
   const long Rp = (R + 127L * c->E + 127) / 128 * 128;
   if (Rp >= (1L << 31)) return MOE_ERR_SHAPE;
@@ -121,7 +122,9 @@ void ws_layout(const Dims &D, Layout &L) {
   L.add("hist", static_cast<size_t>(D.nchunks) * D.E * 4);
   add_route(D, L);  // used when the forward saves nothing
   const size_t eb = D.mx ? 1 : 2;
-  if (D.ring) {  // a fixed ring of 128-row tiles instead of every dispatched row
+  if (D.ring) {  // per-token codes + a fixed ring of 128-row tiles instead of every dispatched row
+    L.add("xq", static_cast<size_t>(D.T) * D.d);
+    L.add("xq_sf", static_cast<size_t>(D.T) * D.d / 32);
     L.add("ring", static_cast<size_t>(D.ring_slots) * 128 * D.d);
     L.add("ring_sf", static_cast<size_t>(D.ring_slots) * 128 * D.d / 32);
     L.add("ring_ctrl", (2 * static_cast<size_t>(D.ring_slots) + 1) * 4);
@@ -534,9 +537,24 @@ int moe_forward(const moe_config *cfg, const void *x, const float *logits, const
   uint8_t *xs_sf = reinterpret_cast<uint8_t *>(D.ring ? W.ptr(ws, "ring_sf") : W.ptr(ws, "xs_sf"));
   uint8_t *xT = (train && D.mx) ? reinterpret_cast<uint8_t *>(S.ptr(saved, "xT")) : nullptr;
   uint8_t *xT_sf = (train && D.mx) ? reinterpret_cast<uint8_t *>(S.ptr(saved, "xT_sf")) : nullptr;
+  uint8_t *xq = reinterpret_cast<uint8_t *>(W.ptr(ws, "xq"));
+  uint8_t *xq_sf = reinterpret_cast<uint8_t *>(W.ptr(ws, "xq_sf"));
   if (!D.ring) {
     Traced tr("dispatch_gather", s);
     rc = cuda_status(moe::launch_gather(x, D.T, D.d, D.k, D.E, rb, D.Rp, D.mx, xs, xs_sf, xT, xT_sf, s));
+  } else {
+    // row-blocked codes once per token (identical for all k routed copies);
+    // the ring kernel's gather SMs move them.  A training pass also needs the
+    // column-blocked codes of the dispatched rows.
+    {
+      Traced tr("quantize_tokens", s);
+      rc = cuda_status(moe::launch_quantize_tokens(x, D.T, D.d, xq, xq_sf, s));
+    }
+    if (rc == MOE_OK && train) {
+      Traced tr("dispatch_xT", s);
+      rc = cuda_status(
+          moe::launch_gather(x, D.T, D.d, D.k, D.E, rb, D.Rp, true, nullptr, nullptr, xT, xT_sf, s));
+    }
   }
   if (rc != MOE_OK) return rc;
   // S4 gate/up GEMM + SwiGLU (+ MX quantisation of h)
@@ -580,15 +598,13 @@ int moe_forward(const moe_config *cfg, const void *x, const float *logits, const
     q.out_rows = D.Rp;
     if (D.ring) {
       moe::RingArgs &r = q.g.ring;
-      r.x = static_cast<const uint16_t *>(x);
+      r.xq = xq;
+      r.xq_sf = xq_sf;
       r.rb = rb;
       r.k = D.k;
       r.slots = D.ring_slots;
       r.codes = reinterpret_cast<uint8_t *>(xs);
       r.sf = xs_sf;
-      r.xT = xT;
-      r.xT_sf = xT_sf;
-      r.ld_t = D.Rp;
       int *ctrl = reinterpret_cast<int *>(W.ptr(ws, "ring_ctrl"));
       r.ready = ctrl;
       r.freed = ctrl + D.ring_slots;

@@ -154,6 +154,13 @@ MOE_DEV void tma_store_2d(const CUtensorMap *map, const void *src, int c0, int c
       "r"(smem_u32(src)), "r"(c0), "r"(c1)
       : "memory");
 }
+// 1-D bulk copy shared -> global (both addresses and the size multiples of 16 B),
+// tracked by this thread's bulk groups.
+MOE_DEV void bulk_store(void *dst, const void *src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(smem_u32(src)),
+               "r"(bytes)
+               : "memory");
+}
 MOE_DEV void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until at most N committed bulk groups of this thread still read shared memory.
 template <int N>

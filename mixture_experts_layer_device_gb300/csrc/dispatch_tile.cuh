@@ -50,11 +50,12 @@ MOE_DEV int token_of_row(const RouteBufs &b, int E, int k, int pr, int *slot_out
 
 // MXFP8 dispatch of the 32 expert-sorted padded rows [r0, r0 + 32) by 256
 // threads: each row's token is read from x [T, d] (bf16, zeros for padding
-// rows) and quantised along d into codes at dst row q0 + i (row stride d) with
-// tiled scales (K = d).  When xT is given, the same 32 rows are also quantised
-// per column (one 32-row block) into the transposed codes xT [d, ld_t] at
-// columns r0 .. r0 + 31, with tiled scales (K = ld_t).  `tile` is 32 x 65
-// floats of shared memory; `sync()` is a barrier over the 256 threads.
+// rows) and, unless dst is NULL, quantised along d into codes at dst row
+// q0 + i (row stride d) with tiled scales (K = d).  When xT is given, the
+// same 32 rows are also quantised per column (one 32-row block) into the
+// transposed codes xT [d, ld_t] at columns r0 .. r0 + 31, with tiled scales
+// (K = ld_t).  `tile` is 32 x 65 floats of shared memory; `sync()` is a
+// barrier over the 256 threads.
 template <typename Sync>
 MOE_DEV void dispatch_rows32(const uint16_t *__restrict__ x, int d, int k, int E, const RouteBufs &b, int r0,
                              int q0, uint8_t *__restrict__ dst, uint8_t *__restrict__ dst_sf,
@@ -77,11 +78,13 @@ MOE_DEV void dispatch_rows32(const uint16_t *__restrict__ x, int d, int k, int E
     for (int j = 0; j < 4; ++j) {
       float f[8];
       unpack8(q[j], f);
-      const int col = cb + 64 * j + cc;
-      uint32_t byte;
-      const uint2 code = mx_encode8_quad(f, &byte);
-      *reinterpret_cast<uint2 *>(dst + static_cast<size_t>(qr) * d + col) = code;
-      if ((tid & 3) == 0) dst_sf[sf_tiled_offset(qr, col >> 5, d)] = static_cast<uint8_t>(byte);
+      if (dst) {
+        const int col = cb + 64 * j + cc;
+        uint32_t byte;
+        const uint2 code = mx_encode8_quad(f, &byte);
+        *reinterpret_cast<uint2 *>(dst + static_cast<size_t>(qr) * d + col) = code;
+        if ((tid & 3) == 0) dst_sf[sf_tiled_offset(qr, col >> 5, d)] = static_cast<uint8_t>(byte);
+      }
       if (xT) {
         sync();
 #pragma unroll

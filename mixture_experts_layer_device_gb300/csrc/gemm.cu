@@ -134,37 +134,138 @@ MOE_DEV Tile decode_tile(const GemmArgs &g, int t) {
   return ti;
 }
 
-// Gather role of the ring kernel (warps 0..7 of a gather CTA; the other warps
-// leave at once): tiles u = blockIdx.x, + gather_ctas, ... in increasing
-// order.  Before writing tile u into slot u % slots the slot's previous tile
-// (u - slots) must have been loaded by all n_tiles GEMM tiles that read it;
-// after writing, the slot is published with ready[slot] = u + 1 (release).
-// The expert-sorted row order and the per-row quantisation are those of the
-// stand-alone dispatch, so the GEMM sees the same codes.
+// Gather role of the ring kernel: data movement only.  The row-blocked codes
+// of every token were computed once beforehand (xq, with canonical scales
+// xq_sf); a gather CTA copies the rows of tiles u = blockIdx.x, + gather_ctas,
+// ... (increasing) into their ring slots:
+//   warp 8: whole rows, 4 at a time (lane i < 4 moves row i of the group),
+//     with TMA bulk copies global -> shared and shared -> ring (a zero row
+//     for padding rows); 6 buffers, the loads of the next 4 groups in flight
+//     while one is stored.  Whole-row copies keep the number of TMA
+//     operations per tile at 2 x 128;
+//   warps 0..7: scatter each row's scale bytes into the slot's tiled layout
+//     (16 loads in flight per thread before the stores).
+// Before the first write of tile u into slot u % slots the slot's previous
+// tile (u - slots) must have been loaded by all n_tiles GEMM tiles that read
+// it; once the tile's copies are complete the slot is published with
+// ready[slot] = u + 1 (release).  The codes are those of the stand-alone
+// dispatch (row-blocked quantisation along d depends only on the token).
+namespace ring {
+constexpr int NBUF = 6;
+constexpr int LAG = 4;          // groups loaded ahead of the one being stored
+constexpr int GROUP = 4;        // rows per buffer
+constexpr int MAX_D = 8192;     // codes per row (the ring needs d <= MAX_D)
+constexpr int BUF_BYTES = GROUP * MAX_D;
+constexpr int SF_BATCH = 16;
+static_assert(NBUF - LAG - 1 == 1, "the buffer-reuse wait below assumes one newer store");
+}  // namespace ring
+
 MOE_DEV void ring_gather_role(const GemmArgs &g, uint8_t *smem) {
+  using namespace ring;
   const RingArgs &r = g.ring;
   const int tid = static_cast<int>(threadIdx.x);
-  if (tid >= 256 || g.debug_starve) return;
-  float(*tile)[65] = reinterpret_cast<float(*)[65]>(smem);
-  volatile int *stop = reinterpret_cast<volatile int *>(smem + 32 * 65 * sizeof(float));
-  auto sync = [] { asm volatile("bar.sync 1, 256;" ::: "memory"); };
+  const int warp = tid >> 5, lane = tid & 31;
+  const int d = g.K;
+  uint8_t *bufs = smem;                                     // NBUF x GROUP rows of d bytes
+  uint8_t *zrow = smem + NBUF * GROUP * d;                  // d zero bytes
+  int *toks = reinterpret_cast<int *>(zrow + d);            // 128 tokens of the current tile
+  uint64_t *full = reinterpret_cast<uint64_t *>(toks + 128);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(full + NBUF);
+  volatile int *stop = abort_flag + 1;
+  for (int i = tid; i < d / 16; i += blockDim.x) reinterpret_cast<uint4 *>(zrow)[i] = make_uint4(0, 0, 0, 0);
+  if (tid == 0) {
+    for (int b = 0; b < NBUF; ++b) mbar_init(&full[b], 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  fence_proxy_async_smem();  // the zero row is read by TMA stores
+  __syncthreads();
+  if (g.debug_starve) return;  // test hook: nothing is published, the GEMM CTAs' ring waits run out
+
+  constexpr int items = 128 / GROUP;  // row groups of one tile
+  const int ngrp = d / 128;           // 4-byte scale groups per row
   const int tiles = __ldg(r.rb.poff + g.E) >> 7;
+  int gi = 0;                         // buffer uses so far (warp 8)
   for (int u = static_cast<int>(blockIdx.x); u < tiles; u += r.gather_ctas) {
     const int slot = u % r.slots;
+    if (tid < 128) toks[tid] = token_of_row(r.rb, g.E, r.k, u * 128 + tid, nullptr);
     if (tid == 0)
-      *stop = flag_wait_geq(r.freed + slot, (u / r.slots) * g.n_tiles, r.abort, nullptr, g.status,
+      *stop = flag_wait_geq(r.freed + slot, (u / r.slots) * g.n_tiles, r.abort, abort_flag, g.status,
                             g.timeout_ns)
                   ? 0
                   : 1;
-    sync();
+    __syncthreads();
     if (*stop) break;
-#pragma unroll 1
-    for (int sub = 0; sub < 4; ++sub)
-      dispatch_rows32(r.x, g.K, r.k, g.E, r.rb, u * 128 + sub * 32, slot * 128 + sub * 32, r.codes, r.sf,
-                      r.xT, r.xT_sf, r.ld_t, tile, tid, sync);
-    __threadfence();
-    fence_proxy_async_global();
-    sync();
+    uint8_t *dst_rows = r.codes + static_cast<size_t>(slot) * 128 * d;
+    if (warp == 8) {
+      // ---------------------------------------------- codes: TMA in, TMA out
+      // Group j of this tile uses buffer (g0 + j) % NBUF; it is loaded in
+      // iteration j and stored in iteration j + LAG.  The buffer's previous
+      // group (j - NBUF) was stored in iteration j - NBUF + LAG = j - 2, so
+      // before the load at most one newer store of this lane may still be
+      // reading shared memory (NBUF - LAG - 1 = 1).
+      const int g0 = gi;
+      bool ok = true;
+      for (int j = 0; j < items + LAG && ok; ++j) {
+        if (j < items) {
+          const int b = (g0 + j) % NBUF;
+          const int tok = lane < GROUP ? toks[j * GROUP + lane] : -1;
+          if (g0 + j >= NBUF) bulk_wait_read<NBUF - LAG - 1>();
+          const unsigned valid = __ballot_sync(0xffffffffu, tok >= 0);
+          if (lane == 0) mbar_arrive_expect_tx(&full[b], static_cast<uint32_t>(__popc(valid)) * d);
+          __syncwarp();
+          if (tok >= 0)
+            bulk_load(bufs + (b * GROUP + lane) * d, r.xq + static_cast<size_t>(tok) * d,
+                      static_cast<uint32_t>(d), &full[b]);
+        }
+        if (j >= LAG) {  // store group j - LAG
+          const int jp = j - LAG;
+          const int b = (g0 + jp) % NBUF;
+          const uint32_t ph = static_cast<uint32_t>((g0 + jp) / NBUF) & 1u;
+          ok = mbar_wait(&full[b], ph, abort_flag, g.status, g.timeout_ns);
+          ok = __all_sync(0xffffffffu, ok);
+          if (ok && lane < GROUP) {
+            const int tok = toks[jp * GROUP + lane];
+            bulk_store(dst_rows + static_cast<size_t>(jp * GROUP + lane) * d,
+                       tok >= 0 ? bufs + (b * GROUP + lane) * d : zrow, static_cast<uint32_t>(d));
+            bulk_commit();
+          }
+        }
+      }
+      gi = g0 + items;
+      bulk_wait<0>();  // this lane's ring writes are complete
+      fence_proxy_async_global();
+      __threadfence();
+      if (!ok) *abort_flag = 1;
+    } else if (warp < 8) {
+      // ---------------------------------------------- scales: canonical -> tiled
+      const int rows_sf = slot * 128;
+      const int total = 128 * ngrp;
+      for (int base = 0; base < total; base += 256 * SF_BATCH) {
+        uint32_t v[SF_BATCH];
+#pragma unroll
+        for (int q = 0; q < SF_BATCH; ++q) {
+          const int i = base + q * 256 + tid;
+          v[q] = 0u;
+          if (i < total) {
+            const int tok = toks[i / ngrp];
+            if (tok >= 0)
+              v[q] = __ldg(reinterpret_cast<const uint32_t *>(r.xq_sf + static_cast<size_t>(tok) * (d / 32) +
+                                                               4 * (i % ngrp)));
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < SF_BATCH; ++q) {
+          const int i = base + q * 256 + tid;
+          if (i < total)
+            *reinterpret_cast<uint32_t *>(r.sf + sf_tiled_offset(rows_sf + i / ngrp, 4 * (i % ngrp), d)) = v[q];
+        }
+      }
+      __threadfence();
+      fence_proxy_async_global();
+    }
+    __syncthreads();
+    if (*abort_flag) break;
     if (tid == 0) st_release_gpu(r.ready + slot, u + 1);
   }
 }

@@ -479,7 +479,10 @@ __global__ void __launch_bounds__(256) transpose_rows_kernel(
   }
 }
 
-// Row-blocked weight quantisation: src [rows, cols] bf16 -> codes + tiled scales.
+// Row-blocked quantisation: src [rows, cols] bf16 -> codes + scales, tiled
+// (weights, GEMM operands) or canonical [rows, cols/32] (per-token codes that
+// the ring dispatch gathers).
+template <bool TILED>
 __global__ void __launch_bounds__(256) quantize_rows_kernel(const uint4 *__restrict__ src, long rows,
                                                             int cols, uint2 *__restrict__ codes,
                                                             uint8_t *__restrict__ sf) {
@@ -492,7 +495,9 @@ __global__ void __launch_bounds__(256) quantize_rows_kernel(const uint4 *__restr
     unpack8(__ldg(src + static_cast<size_t>(r) * vec + i), f);
     uint32_t byte;
     codes[static_cast<size_t>(r) * vec + i] = mx_encode8_quad(f, &byte);
-    if ((lane & 3) == 0) sf[sf_tiled_offset(r, i >> 2, cols)] = static_cast<uint8_t>(byte);
+    if ((lane & 3) == 0)
+      sf[TILED ? sf_tiled_offset(r, i >> 2, cols) : static_cast<size_t>(r) * (cols / 32) + (i >> 2)] =
+          static_cast<uint8_t>(byte);
   }
 }
 
@@ -607,7 +612,7 @@ cudaError_t launch_quantize_mx(const void *src, int batch, int rows, int cols, b
                                uint8_t *codes, uint8_t *scales, cudaStream_t s) {
   if (!transpose) {
     const long total = static_cast<long>(batch) * rows;
-    quantize_rows_kernel<<<blocks_for(total, 8), 256, 0, s>>>(
+    quantize_rows_kernel<true><<<blocks_for(total, 8), 256, 0, s>>>(
         static_cast<const uint4 *>(src), total, cols, reinterpret_cast<uint2 *>(codes), scales);
   } else {
     const dim3 grid(blocks_for(rows, 32), blocks_for(cols, 256), batch);
@@ -615,6 +620,13 @@ cudaError_t launch_quantize_mx(const void *src, int batch, int rows, int cols, b
         static_cast<const uint16_t *>(src), static_cast<long>(rows) * cols, cols, rows, nullptr, rows,
         1, 1, RouteBufs{}, codes, static_cast<long>(rows) * cols, scales, cols, rows);
   }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_tokens(const void *x, int T, int d, uint8_t *codes, uint8_t *scales,
+                                   cudaStream_t s) {
+  quantize_rows_kernel<false><<<blocks_for(T, 8), 256, 0, s>>>(static_cast<const uint4 *>(x), T, d,
+                                                                reinterpret_cast<uint2 *>(codes), scales);
   return cudaGetLastError();
 }
 

@@ -83,21 +83,24 @@ cudaError_t launch_transpose_bf16(const void *src, int batch, int rows, int cols
 enum GemmSched { SCHED_GROUP_M = 0, SCHED_DENSE = 1, SCHED_GROUP_K = 2 };
 enum GemmEpi { EPI_STORE = 0, EPI_SWIGLU = 1, EPI_SWIGLU_BWD = 2 };
 
+// Row-blocked MXFP8 codes of every token: x [T, d] bf16 -> codes [T, d] and
+// canonical scales [T, d/32] (the ring dispatch gathers these rows).
+cudaError_t launch_quantize_tokens(const void *x, int T, int d, uint8_t *codes, uint8_t *scales,
+                                   cudaStream_t s);
+
 // Persistent ring dispatch (S3 fused with the MXFP8 gate/up GEMM): the first
 // `gather_ctas` CTAs of the launch gather and quantise 128-row tiles of
 // expert-sorted rows into a ring of `slots` tiles; the other CTAs run the GEMM
 // on the ring.  Tile u (padded rows [128u, 128u + 128)) goes to slot u % slots.
 struct RingArgs {
-  const uint16_t *x;  // [T, d] bf16 tokens
-  RouteBufs rb;       // route / schedule arrays (token of each row)
+  const uint8_t *xq;     // [T, d] row-blocked codes of every token (launch_quantize_tokens)
+  const uint8_t *xq_sf;  // [T, d/32] their scales, canonical order
+  RouteBufs rb;          // route / schedule arrays (token of each row)
   int k;
   int slots;          // ring capacity in 128-row tiles
   int gather_ctas;    // CTAs of the launch that gather (the rest compute)
   uint8_t *codes;     // [slots * 128, d] E4M3 codes: the GEMM's A operand
   uint8_t *sf;        // tiled scales of `codes` (K = d)
-  uint8_t *xT;        // training: column-blocked codes of x [d, ld_t], else NULL
-  uint8_t *xT_sf;
-  long ld_t;
   int *ready;         // [slots] index + 1 of the tile last published in the slot
   int *freed;         // [slots] GEMM tiles whose loads from the slot have landed (cumulative)
   int *abort;         // launch-wide abort word (set when any wait runs out)

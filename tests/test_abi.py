@@ -63,7 +63,7 @@ def test_sizes_and_layout(pkg):
     (dict(T=0), -1), (dict(flags=4), -1), (dict(dtype=7), -1), (dict(m_shared=100), -2),
     (dict(ring_rows=256), -1),                          # the ring is MXFP8-only
     (dict(dtype=1, ring_rows=200), -2), (dict(dtype=1, ring_rows=-128), -1),
-    (dict(dtype=1, ring_rows=256, gather_sms=65), -1),
+    (dict(dtype=1, ring_rows=256, gather_sms=65), -1), (dict(dtype=1, d=8448, ring_rows=256), -2),
 ])
 def test_invalid_configs_rejected_on_host(pkg, bad, code):
     args = dict(T=64, d=256, m=128, E=8, k=2, m_shared=0, dtype=0, flags=0, ring_rows=0, gather_sms=0)
@@ -100,8 +100,9 @@ def test_status_strings(pkg):
 
 
 def test_ring_workspace_replaces_the_dispatch_buffer(pkg):
-    """With a ring the workspace holds ring_rows dispatched rows instead of every
-    routed row; the saved activations do not change."""
+    """With a ring the workspace holds ring_rows dispatched rows (plus one row of
+    codes per token) instead of every routed row; the saved activations do not
+    change."""
     full = pkg.config(32768, 7168, 3072, 384, 6, 0, "mxfp8")
     ring = pkg.config(32768, 7168, 3072, 384, 6, 0, "mxfp8", ring_rows=8192, gather_sms=8)
     rows = pkg.moe_padded_rows(full)
@@ -109,7 +110,8 @@ def test_ring_workspace_replaces_the_dispatch_buffer(pkg):
     with pytest.raises(RuntimeError):
         pkg.moe_buffer_info(ring, 1, "xs")
     saved = pkg.moe_workspace_bytes(full) - pkg.moe_workspace_bytes(ring)
-    assert saved >= (rows - 8192) * d * (1 + 1 / 32) - 4096
+    # the ring kernel also keeps the per-token codes (T rows) it gathers from
+    assert saved >= (rows - 8192 - 32768) * d * (1 + 1 / 32) - 8192
     assert pkg.moe_saved_bytes(full) == pkg.moe_saved_bytes(ring)
     off, nb = pkg.moe_buffer_info(ring, 1, "ring")
     assert nb == 8192 * d
