@@ -288,11 +288,7 @@ def time_s0(layer, gu_all, dn_all, stream):
 
     def run():
         if layer.mx:
-            pkg.check(pkg.moe_quantize_mx(gu_all, E, 2 * m, d, 0, t["gu"], t["gu_scale"], stream))
-            pkg.check(pkg.moe_quantize_mx(dn_all, E, d, m, 0, t["dn"], t["dn_scale"], stream))
-            if layer.backward_enabled:
-                pkg.check(pkg.moe_quantize_mx(gu_all, E, 2 * m, d, 1, t["gu_t"], t["gu_t_scale"], stream))
-                pkg.check(pkg.moe_quantize_mx(dn_all, E, d, m, 1, t["dn_t"], t["dn_t_scale"], stream))
+            layer.prepare_stacked(gu_all, dn_all, stream=stream)
         elif layer.backward_enabled:
             pkg.check(pkg.moe_transpose_bf16(gu_all, E, 2 * m, d, t["gu_t"], stream))
             pkg.check(pkg.moe_transpose_bf16(dn_all, E, d, m, t["dn_t"], stream))
@@ -329,8 +325,10 @@ def run_ours(args, cfg, passes, rank, world, local_rank):
     n_tok = 1 if bwd else 4
     if want_cpu:
         sample = oracle_sample(cfg, passes, x, logits, dy, n_tok)
-    del gu_all, dn_all
-    torch.cuda.empty_cache()
+    keep_masters = bwd and layer.mx      # re-quantised every update in the with-S0 step
+    if not keep_masters:
+        del gu_all, dn_all
+        torch.cuda.empty_cache()
 
     grads = layer.alloc_grads() if bwd else None
     y = torch.empty((cfg["T"], cfg["d"]), dtype=torch.bfloat16, device=dev)
@@ -393,6 +391,16 @@ def run_ours(args, cfg, passes, rank, world, local_rank):
     if bwd:
         fms, _ = timed(lambda: layer.forward(x, logits, y=y, train=False, stream=stream), args.steps)
         fwd_value = tokens * args.steps / (fms / 1e3)
+    with_s0 = None
+    if keep_masters:
+        # a training update re-quantises the bf16 masters (S0, both orientations)
+        # before its forward+backward
+        def step_s0():
+            layer.prepare_stacked(gu_all, dn_all, stream=stream)
+            step()
+        s0_total, _ = timed(step_s0, args.steps)
+        with_s0 = {"ms_per_step": round(s0_total / args.steps, 4),
+                   "tokens_per_s": round(tokens * args.steps / (s0_total / 1e3), 1)}
 
     # e2e: the public API with host buffers, copies inside the timed region
     xh = x.cpu().pin_memory()
@@ -483,6 +491,7 @@ def run_ours(args, cfg, passes, rank, world, local_rank):
         "kernels": kernels,
         "route_schedule_share": round(rs, 4),
         "s0_ms": round(s0_ms, 3),
+        "step_with_s0": with_s0,
         "e2e": {"value": round(tokens * args.steps / (e2e_ms / 1e3), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
         "gpu_launches": launches,

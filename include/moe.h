@@ -172,6 +172,13 @@ int64_t moe_padded_rows(const moe_config *cfg);
 int moe_quantize_mx(const void *src, int batch, int rows, int cols, int transpose, void *codes,
                     void *scales, moe_stream_t stream);
 
+/* S0 for a training layer: both orientations from one read of the bf16
+ * masters.  codes/scales exactly as moe_quantize_mx(transpose = 0) and
+ * codes_t/scales_t exactly as moe_quantize_mx(transpose = 1) would write them
+ * (bit-identical).  rows and cols multiples of 128; inputs finite. */
+int moe_quantize_mx_both(const void *src, int batch, int rows, int cols, void *codes, void *scales,
+                         void *codes_t, void *scales_t, moe_stream_t stream);
+
 /* Per-batch transpose of bf16 matrices: src [batch, rows, cols] ->
  * dst [batch, cols, rows] (rows, cols multiples of 32). */
 int moe_transpose_bf16(const void *src, int batch, int rows, int cols, void *dst,

@@ -35,7 +35,7 @@ class MoeWeights(ctypes.Structure):
 
 _lib = None
 EXPORTS = ["moe_workspace_bytes", "moe_saved_bytes", "moe_buffer_info", "moe_padded_rows",
-           "moe_quantize_mx", "moe_transpose_bf16", "moe_route", "moe_forward", "moe_backward",
+           "moe_quantize_mx", "moe_quantize_mx_both", "moe_transpose_bf16", "moe_route", "moe_forward", "moe_backward",
            "moe_get_status", "moe_status_string", "moe_trace_enable", "moe_trace_clear", "moe_trace_count",
            "moe_trace_name", "moe_trace_ms", "moe_route_noalloc"]
 
@@ -56,6 +56,7 @@ def lib():
         L.moe_buffer_info.restype = I
         L.moe_padded_rows.argtypes, L.moe_padded_rows.restype = [cfgp], ctypes.c_int64
         L.moe_quantize_mx.argtypes, L.moe_quantize_mx.restype = [P, I, I, I, I, P, P, S], I
+        L.moe_quantize_mx_both.argtypes, L.moe_quantize_mx_both.restype = [P, I, I, I, P, P, P, P, S], I
         L.moe_transpose_bf16.argtypes, L.moe_transpose_bf16.restype = [P, I, I, I, P, S], I
         L.moe_route.argtypes, L.moe_route.restype = [cfgp, P, P, P, P, P, P, P, S], I
         L.moe_forward.argtypes = [cfgp, P, P, ctypes.POINTER(MoeWeights), P, P, P, S]
@@ -127,6 +128,11 @@ def moe_buffer_info(cfg, which, name):
     off, nb = ctypes.c_size_t(), ctypes.c_size_t()
     check(lib().moe_buffer_info(ctypes.byref(cfg), which, name.encode(), ctypes.byref(off), ctypes.byref(nb)))
     return off.value, nb.value
+
+
+def moe_quantize_mx_both(src, batch, rows, cols, codes, scales, codes_t, scales_t, stream=None):
+    return lib().moe_quantize_mx_both(_ptr(src), batch, rows, cols, _ptr(codes), _ptr(scales), _ptr(codes_t),
+                                      _ptr(scales_t), _stream(stream))
 
 
 def moe_quantize_mx(src, batch, rows, cols, transpose, codes, scales, stream=None):

@@ -466,6 +466,22 @@ int moe_quantize_mx(const void *src, int batch, int rows, int cols, int transpos
                                              static_cast<uint8_t *>(scales), stream));
 }
 
+int moe_quantize_mx_both(const void *src, int batch, int rows, int cols, void *codes, void *scales,
+                         void *codes_t, void *scales_t, moe_stream_t stream) {
+  if (!src || !codes || !scales || !codes_t || !scales_t || batch <= 0 || rows <= 0 || cols <= 0)
+    return MOE_ERR_ARG;
+  if (rows % 128 || cols % 128) return MOE_ERR_SHAPE;
+  if (!aligned16(src) || !aligned16(codes) || !aligned16(scales) || !aligned16(codes_t) ||
+      !aligned16(scales_t))
+    return MOE_ERR_ALIGN;
+  DeviceInfo dev;
+  const int rc = device_info(&dev);
+  if (rc != MOE_OK) return rc;
+  return cuda_status(moe::launch_quantize_mx_both(
+      src, batch, rows, cols, static_cast<uint8_t *>(codes), static_cast<uint8_t *>(scales),
+      static_cast<uint8_t *>(codes_t), static_cast<uint8_t *>(scales_t), stream));
+}
+
 int moe_transpose_bf16(const void *src, int batch, int rows, int cols, void *dst,
                        moe_stream_t stream) {
   if (!src || !dst || batch <= 0 || rows <= 0 || cols <= 0) return MOE_ERR_ARG;

@@ -425,11 +425,15 @@ __global__ void __launch_bounds__(256) reverse_dispatch_kernel(
 // global loads are all issued up front (16 bytes per thread each).  Output
 // rows are source columns; MX output quantises each 32-long output run (the
 // block's 32 rows) as one block.
-template <bool MX, bool GATHER>
+// ROWQ (MX, weights): the tile's source rows are also quantised along C into
+// row-blocked codes rq [batch * nrows, C] with tiled scales (K = C), so one
+// read of the bf16 source gives both operand orientations.
+template <bool MX, bool GATHER, bool ROWQ = false>
 __global__ void __launch_bounds__(256) transpose_rows_kernel(
     const uint16_t *__restrict__ src, long src_batch_stride, int C, int nrows_host,
     const int *__restrict__ nrows_dev, long nsrc, int k, int E, RouteBufs b, void *dst,
-    long dst_batch_stride, uint8_t *__restrict__ dst_sf, long sf_batch_rows, long ld_dst) {
+    long dst_batch_stride, uint8_t *__restrict__ dst_sf, long sf_batch_rows, long ld_dst,
+    uint8_t *__restrict__ rq = nullptr, uint8_t *__restrict__ rq_sf = nullptr) {
   __shared__ float tile[32][65];
   const int r0 = blockIdx.x * 32;
   const int cb = blockIdx.y * 256;
@@ -458,6 +462,14 @@ __global__ void __launch_bounds__(256) transpose_rows_kernel(
     if (j) __syncthreads();
     float f[8];
     unpack8(q[j], f);
+    if constexpr (ROWQ) {
+      const long qrow = static_cast<long>(bz) * nrows + r;
+      const int col = cb + 64 * j + cc;
+      uint32_t byte;
+      const uint2 code = mx_encode8_quad(f, &byte);
+      *reinterpret_cast<uint2 *>(rq + static_cast<size_t>(qrow) * C + col) = code;
+      if ((threadIdx.x & 3) == 0) rq_sf[sf_tiled_offset(qrow, col >> 5, C)] = static_cast<uint8_t>(byte);
+    }
 #pragma unroll
     for (int t = 0; t < 8; ++t) tile[rr][cc + t] = f[t];
     __syncthreads();
@@ -620,6 +632,15 @@ cudaError_t launch_quantize_mx(const void *src, int batch, int rows, int cols, b
         static_cast<const uint16_t *>(src), static_cast<long>(rows) * cols, cols, rows, nullptr, rows,
         1, 1, RouteBufs{}, codes, static_cast<long>(rows) * cols, scales, cols, rows);
   }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_mx_both(const void *src, int batch, int rows, int cols, uint8_t *codes,
+                                    uint8_t *scales, uint8_t *codes_t, uint8_t *scales_t, cudaStream_t s) {
+  const dim3 grid(blocks_for(rows, 32), blocks_for(cols, 256), batch);
+  transpose_rows_kernel<true, false, true><<<grid, 256, 0, s>>>(
+      static_cast<const uint16_t *>(src), static_cast<long>(rows) * cols, cols, rows, nullptr, rows, 1, 1,
+      RouteBufs{}, codes_t, static_cast<long>(rows) * cols, scales_t, cols, rows, codes, scales);
   return cudaGetLastError();
 }
 

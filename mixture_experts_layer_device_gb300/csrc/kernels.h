@@ -83,6 +83,12 @@ cudaError_t launch_transpose_bf16(const void *src, int batch, int rows, int cols
 enum GemmSched { SCHED_GROUP_M = 0, SCHED_DENSE = 1, SCHED_GROUP_K = 2 };
 enum GemmEpi { EPI_STORE = 0, EPI_SWIGLU = 1, EPI_SWIGLU_BWD = 2 };
 
+// Both MXFP8 orientations of bf16 weights [batch, rows, cols] from one read:
+// codes/scales as launch_quantize_mx(transpose = false), codes_t/scales_t as
+// launch_quantize_mx(transpose = true).
+cudaError_t launch_quantize_mx_both(const void *src, int batch, int rows, int cols, uint8_t *codes,
+                                    uint8_t *scales, uint8_t *codes_t, uint8_t *scales_t, cudaStream_t s);
+
 // Row-blocked MXFP8 codes of every token: x [T, d] bf16 -> codes [T, d] and
 // canonical scales [T, d/32] (the ring dispatch gathers these rows).
 cudaError_t launch_quantize_tokens(const void *x, int T, int d, uint8_t *codes, uint8_t *scales,

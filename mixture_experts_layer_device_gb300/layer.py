@@ -7,8 +7,8 @@ library's CUDA kernels; torch only allocates memory and provides the stream.
 import torch
 
 from . import (MOE_BF16, MOE_FLAG_BACKWARD, MOE_MXFP8, check, config, moe_backward, moe_buffer_info,
-               moe_forward, moe_get_status, moe_padded_rows, moe_quantize_mx, moe_saved_bytes,
-               moe_transpose_bf16, moe_workspace_bytes, weights)
+               moe_forward, moe_get_status, moe_padded_rows, moe_quantize_mx, moe_quantize_mx_both,
+               moe_saved_bytes, moe_transpose_bf16, moe_workspace_bytes, weights)
 
 _DT = {"i32": torch.int32, "f32": torch.float32, "bf16": torch.bfloat16, "u8": torch.uint8}
 
@@ -67,16 +67,13 @@ class MoELayer:
             if self.backward_enabled:
                 t["gu_t"] = torch.empty((E, d, 2 * m), dtype=torch.bfloat16, device=dev)
                 t["dn_t"] = torch.empty((E, m, d), dtype=torch.bfloat16, device=dev)
+        self.tensors = t
         gsz, dsz = 2 * m * d, d * m
         if stacked is not None:
             gu, dn = (w.contiguous() for w in stacked)
             assert gu.shape == (E, 2 * m, d) and dn.shape == (E, d, m)
             if self.mx:
-                check(moe_quantize_mx(gu, E, 2 * m, d, 0, t["gu"], t["gu_scale"]))
-                check(moe_quantize_mx(dn, E, d, m, 0, t["dn"], t["dn_scale"]))
-                if self.backward_enabled:
-                    check(moe_quantize_mx(gu, E, 2 * m, d, 1, t["gu_t"], t["gu_t_scale"]))
-                    check(moe_quantize_mx(dn, E, d, m, 1, t["dn_t"], t["dn_t_scale"]))
+                self.prepare_stacked(gu, dn)
             else:
                 t["gu"].copy_(gu)
                 t["dn"].copy_(dn)
@@ -88,15 +85,15 @@ class MoELayer:
             assert gu.is_cuda and gu.dtype == torch.bfloat16 and gu.shape == (2 * m, d)
             assert dn.is_cuda and dn.dtype == torch.bfloat16 and dn.shape == (d, m)
             gu, dn = gu.contiguous(), dn.contiguous()
-            if self.mx:
+            if self.mx and self.backward_enabled:
+                check(moe_quantize_mx_both(gu, 1, 2 * m, d, t["gu"].view(-1)[e * gsz:], t["gu_scale"][e * gsz // 32:],
+                                           t["gu_t"].view(-1)[e * gsz:], t["gu_t_scale"][e * gsz // 32:]))
+                check(moe_quantize_mx_both(dn, 1, d, m, t["dn"].view(-1)[e * dsz:], t["dn_scale"][e * dsz // 32:],
+                                           t["dn_t"].view(-1)[e * dsz:], t["dn_t_scale"][e * dsz // 32:]))
+            elif self.mx:
                 check(moe_quantize_mx(gu, 1, 2 * m, d, 0, t["gu"].view(-1)[e * gsz:],
                                       t["gu_scale"][e * gsz // 32:]))
                 check(moe_quantize_mx(dn, 1, d, m, 0, t["dn"].view(-1)[e * dsz:], t["dn_scale"][e * dsz // 32:]))
-                if self.backward_enabled:
-                    check(moe_quantize_mx(gu, 1, 2 * m, d, 1, t["gu_t"].view(-1)[e * gsz:],
-                                          t["gu_t_scale"][e * gsz // 32:]))
-                    check(moe_quantize_mx(dn, 1, d, m, 1, t["dn_t"].view(-1)[e * dsz:],
-                                          t["dn_t_scale"][e * dsz // 32:]))
             else:
                 t["gu"][e].copy_(gu)
                 t["dn"][e].copy_(dn)
@@ -114,6 +111,19 @@ class MoELayer:
                 check(moe_transpose_bf16(s_dn, 1, d, ms, t["s_dn_t"]))
         self.tensors = t
         self.W = weights(**t)
+
+    def prepare_stacked(self, gu, dn, stream=None):
+        """S0 for all experts from stacked bf16 masters (W_gu [E, 2m, d],
+        W_dn [E, d, m]) into this layer's MXFP8 operands: one launch per
+        master, which also writes the backward's transposed copies of a
+        training layer.  Re-run after every update of the masters."""
+        E, d, m, t = self.E, self.d, self.m, self.tensors
+        if self.backward_enabled:
+            check(moe_quantize_mx_both(gu, E, 2 * m, d, t["gu"], t["gu_scale"], t["gu_t"], t["gu_t_scale"], stream))
+            check(moe_quantize_mx_both(dn, E, d, m, t["dn"], t["dn_scale"], t["dn_t"], t["dn_t_scale"], stream))
+        else:
+            check(moe_quantize_mx(gu, E, 2 * m, d, 0, t["gu"], t["gu_scale"], stream))
+            check(moe_quantize_mx(dn, E, d, m, 0, t["dn"], t["dn_scale"], stream))
 
     # ------------------------------------------------------------ passes
     def forward(self, x, logits, y=None, train=False, stream=None):

@@ -54,6 +54,28 @@ def test_quantize_mx_bit_exact(pkg, transpose):
     assert np.array_equal(unpack_tiled_scales(sf, B * rows, cols), s_ref.reshape(B * rows, cols // 32))
 
 
+@pytest.mark.parametrize("shape", [(2, 256, 384), (3, 384, 128)])
+def test_quantize_mx_both_orientations_bit_exact(pkg, shape):
+    """One read of the masters gives both operand orientations, each
+    bit-identical to the oracle's quantisation of that orientation."""
+    rng = np.random.default_rng(1)
+    v = edge_values(rng, shape)
+    w = torch.from_numpy(v).to(torch.bfloat16)
+    B, rows, cols = shape
+    n = B * rows * cols
+    out = [torch.empty(n, dtype=torch.uint8, device="cuda") for _ in range(2)]
+    osf = [torch.empty(n // 32, dtype=torch.uint8, device="cuda") for _ in range(2)]
+    pkg.check(pkg.moe_quantize_mx_both(w.cuda(), B, rows, cols, out[0], osf[0], out[1], osf[1]))
+    torch.cuda.synchronize()
+    ref = mi.to_f64(w)
+    for transpose in (0, 1):
+        c_ref, s_ref = om.quantize_weights(ref, transpose=bool(transpose))
+        Bq, r, c = c_ref.shape
+        assert np.array_equal(out[transpose].cpu().numpy().reshape(Bq * r, c), c_ref.reshape(Bq * r, c))
+        assert np.array_equal(unpack_tiled_scales(osf[transpose].cpu().numpy(), Bq * r, c),
+                              s_ref.reshape(Bq * r, c // 32))
+
+
 def test_quantize_mx_exhaustive_bf16_patterns(pkg):
     # every finite bf16 bit pattern, in blocks that also carry a large element
     bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
