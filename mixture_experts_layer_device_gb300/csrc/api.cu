@@ -214,11 +214,12 @@ int device_info(DeviceInfo *out) {
 
 // 2-D K-major tensor map: `rows` rows of `inner` elements (bf16 or 1-byte codes),
 // box 128 rows x 128 bytes, 128-byte swizzle, zero fill out of bounds.
-bool make_map(CUtensorMap *m, const void *base, bool bytes1, uint64_t inner, uint64_t rows) {
+bool make_map(CUtensorMap *m, const void *base, bool bytes1, uint64_t inner, uint64_t rows,
+              uint32_t box_rows = 128) {
   const uint64_t esz = bytes1 ? 1 : 2;
   cuuint64_t dims[2] = {inner, rows};
   cuuint64_t strides[1] = {inner * esz};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / esz), 128};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / esz), box_rows};
   cuuint32_t estr[2] = {1, 1};
   const CUresult r = g_encode(m, bytes1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                               2, const_cast<void *>(base), dims, strides, box, estr,
@@ -315,6 +316,12 @@ bool make_sf_map(CUtensorMap *m, const void *base, uint64_t bytes) {
 // the pair's cross-SM coupling measured slower.
 bool use_pair(const Gemm &q) { return q.bn == 256 && !q.mx; }
 
+// MXFP8 GEMMs run on clusters of two CTAs sharing the A tile (TMA multicast)
+// whenever the N-tiles pair up.
+bool use_mc(const Gemm &q) {
+  return q.mx && q.g.n_tiles % 2 == 0 && moe::gemm_mc_max_clusters(q.mx, q.bn, q.epi) > 0;
+}
+
 int run_pair(const Gemm &q, const DeviceInfo &dev, cudaStream_t s) {
   moe::PairMaps m;
   memset(&m, 0, sizeof(m));
@@ -349,6 +356,17 @@ int run_gemm(const char *name, const Gemm &q, const DeviceInfo &dev, cudaStream_
   if (q.g.out2 && !make_store_map(&to2, q.g.out2, false, q.g.ldo2, q.g.ldo2, q.out_rows))
     return MOE_ERR_CUDA;
   if (q.g.outq && !make_store_map(&tq, q.g.outq, true, q.g.ldq, q.g.ldq, q.out_rows)) return MOE_ERR_CUDA;
+  if (use_mc(q)) {
+    // clusters of two sharing A: A is loaded in 64-row halves
+    CUtensorMap ta_half;
+    if (!make_map(&ta_half, q.a, q.mx, q.K, q.a_rows, 64)) return MOE_ERR_CUDA;
+    const int maxc = moe::gemm_mc_max_clusters(q.mx, q.bn, q.epi);
+    if (maxc <= 0) return MOE_ERR_CUDA;
+    long clusters = (q.max_tiles / 2) < (dev.num_sms / 2) ? q.max_tiles / 2 : dev.num_sms / 2;
+    if (clusters > maxc) clusters = maxc;
+    return cuda_status(moe::launch_gemm_mc(q.mx, q.bn, q.epi, ta_half, tb, to, to2, tq, q.g,
+                                           static_cast<int>(clusters), s));
+  }
   const long grid = q.max_tiles < dev.num_sms ? q.max_tiles : dev.num_sms;
   return cuda_status(
       moe::launch_gemm(q.mx, q.bn, q.epi, ta, tb, to, to2, tq, q.g, static_cast<int>(grid), s));

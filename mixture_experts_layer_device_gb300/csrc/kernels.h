@@ -154,6 +154,16 @@ cudaError_t launch_gemm(bool mx, int bn, int epi, const CUtensorMap &ta, const C
                         const CUtensorMap &to, const CUtensorMap &to2, const CUtensorMap &tq,
                         const GemmArgs &args, int grid, cudaStream_t s);
 
+// The same GEMM on clusters of two CTAs sharing the A tile (MXFP8, for the
+// (bn, epi) pairs gemm_mc_max_clusters() is non-zero for): the two CTAs of a
+// cluster compute adjacent N-tiles of one M-tile and each loads one 64-row
+// half of A for both (TMA multicast).  `ta_half` maps A with a 64-row box;
+// args.n_tiles must be even.  `clusters` <= gemm_mc_max_clusters().
+cudaError_t launch_gemm_mc(bool mx, int bn, int epi, const CUtensorMap &ta_half, const CUtensorMap &tb,
+                           const CUtensorMap &to, const CUtensorMap &to2, const CUtensorMap &tq,
+                           const GemmArgs &args, int clusters, cudaStream_t s);
+int gemm_mc_max_clusters(bool mx, int bn, int epi);
+
 // The MXFP8 gate/up GEMM with SwiGLU epilogue fed by the ring (args.ring):
 // one cooperative launch of `grid` CTAs (all co-resident, one per SM), of
 // which args.ring.gather_ctas gather.  `ta` maps the ring codes
