@@ -228,22 +228,6 @@ bool make_map(CUtensorMap *m, const void *base, bool bytes1, uint64_t inner, uin
   return r == CUDA_SUCCESS;
 }
 
-// 2-D map for the epilogue's TMA stores: `rows` rows of `inner` elements, row
-// stride `ld` elements, box 32 rows x 64 bytes, 64-byte swizzle.
-bool make_store_map(CUtensorMap *m, const void *base, bool bytes1, uint64_t inner, uint64_t ld,
-                    uint64_t rows) {
-  const uint64_t esz = bytes1 ? 1 : 2;
-  cuuint64_t dims[2] = {inner, rows};
-  cuuint64_t strides[1] = {ld * esz};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(64 / esz), 32};
-  cuuint32_t estr[2] = {1, 1};
-  const CUresult r = g_encode(m, bytes1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                              2, const_cast<void *>(base), dims, strides, box, estr,
-                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
-                              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // ---------------------------------------------------------------- tracing
@@ -330,32 +314,23 @@ int run_pair(const Gemm &q, const DeviceInfo &dev, cudaStream_t s) {
   if (q.mx && (!make_sf_map(&m.sfa, q.g.sfa, static_cast<uint64_t>(q.a_rows) * q.K / 32) ||
                !make_sf_map(&m.sfb, q.g.sfb, static_cast<uint64_t>(q.b_rows) * q.K / 32)))
     return MOE_ERR_CUDA;
-  if (q.g.out && !make_store_map(&m.o, q.g.out, false, q.g.ldo, q.g.ldo, q.out_rows)) return MOE_ERR_CUDA;
-  if (q.g.out2 && !make_store_map(&m.o2, q.g.out2, false, q.g.ldo2, q.g.ldo2, q.out_rows))
-    return MOE_ERR_CUDA;
-  if (q.g.outq && !make_store_map(&m.q, q.g.outq, true, q.g.ldq, q.g.ldq, q.out_rows)) return MOE_ERR_CUDA;
   const int maxc = moe::pair_max_clusters(q.mx, q.epi);
   if (maxc <= 0) return MOE_ERR_CUDA;
   const long pairs = (q.max_tiles + 1) / 2;
   const long clusters = pairs < maxc ? pairs : maxc;
   (void)dev;
-  return cuda_status(moe::launch_gemm_pair(q.mx, q.epi, m, q.g, static_cast<int>(clusters), s));
+  moe::GemmArgs g = q.g;
+  g.out_rows = q.out_rows;
+  return cuda_status(moe::launch_gemm_pair(q.mx, q.epi, m, g, static_cast<int>(clusters), s));
 }
 
 int run_gemm(const char *name, const Gemm &q, const DeviceInfo &dev, cudaStream_t s) {
   Traced tr(name, s);
   if (use_pair(q) && (q.g.sched != moe::SCHED_GROUP_K || (q.g.M / 128) % 2 == 0)) return run_pair(q, dev, s);
-  CUtensorMap ta, tb, to, to2, tq;
-  memset(&to, 0, sizeof(to));
-  memset(&to2, 0, sizeof(to2));
-  memset(&tq, 0, sizeof(tq));
-  if (!make_map(&ta, q.a, q.mx, q.K, q.a_rows) || !make_map(&tb, q.b, q.mx, q.K, q.b_rows))
-    return MOE_ERR_CUDA;
-  // Output widths: the stored row length is the row stride for every output.
-  if (q.g.out && !make_store_map(&to, q.g.out, false, q.g.ldo, q.g.ldo, q.out_rows)) return MOE_ERR_CUDA;
-  if (q.g.out2 && !make_store_map(&to2, q.g.out2, false, q.g.ldo2, q.g.ldo2, q.out_rows))
-    return MOE_ERR_CUDA;
-  if (q.g.outq && !make_store_map(&tq, q.g.outq, true, q.g.ldq, q.g.ldq, q.out_rows)) return MOE_ERR_CUDA;
+  CUtensorMap tb;
+  if (!make_map(&tb, q.b, q.mx, q.K, q.b_rows)) return MOE_ERR_CUDA;
+  moe::GemmArgs g = q.g;
+  g.out_rows = q.out_rows;
   if (use_mc(q)) {
     // clusters of two sharing A: A is loaded in 64-row halves
     CUtensorMap ta_half;
@@ -364,33 +339,27 @@ int run_gemm(const char *name, const Gemm &q, const DeviceInfo &dev, cudaStream_
     if (maxc <= 0) return MOE_ERR_CUDA;
     long clusters = (q.max_tiles / 2) < (dev.num_sms / 2) ? q.max_tiles / 2 : dev.num_sms / 2;
     if (clusters > maxc) clusters = maxc;
-    return cuda_status(moe::launch_gemm_mc(q.mx, q.bn, q.epi, ta_half, tb, to, to2, tq, q.g,
-                                           static_cast<int>(clusters), s));
+    return cuda_status(moe::launch_gemm_mc(q.mx, q.bn, q.epi, ta_half, tb, g, static_cast<int>(clusters), s));
   }
+  CUtensorMap ta;
+  if (!make_map(&ta, q.a, q.mx, q.K, q.a_rows)) return MOE_ERR_CUDA;
   const long grid = q.max_tiles < dev.num_sms ? q.max_tiles : dev.num_sms;
-  return cuda_status(
-      moe::launch_gemm(q.mx, q.bn, q.epi, ta, tb, to, to2, tq, q.g, static_cast<int>(grid), s));
+  return cuda_status(moe::launch_gemm(q.mx, q.bn, q.epi, ta, tb, g, static_cast<int>(grid), s));
 }
 
 // The persistent ring launch: one CTA per SM, the first gather_ctas of which
 // gather into the ring (fewer if the device has few SMs).
 int run_gemm_ring(const char *name, const Gemm &q, const Dims &D, const DeviceInfo &dev, cudaStream_t s) {
   Traced tr(name, s);
-  CUtensorMap ta, tb, to, to2, tq;
-  memset(&to, 0, sizeof(to));
-  memset(&to2, 0, sizeof(to2));
-  memset(&tq, 0, sizeof(tq));
+  CUtensorMap ta, tb;
   if (!make_map(&ta, q.a, true, q.K, q.a_rows) || !make_map(&tb, q.b, true, q.K, q.b_rows)) return MOE_ERR_CUDA;
-  if (q.g.out && !make_store_map(&to, q.g.out, false, q.g.ldo, q.g.ldo, q.out_rows)) return MOE_ERR_CUDA;
-  if (q.g.out2 && !make_store_map(&to2, q.g.out2, false, q.g.ldo2, q.g.ldo2, q.out_rows))
-    return MOE_ERR_CUDA;
-  if (q.g.outq && !make_store_map(&tq, q.g.outq, true, q.g.ldq, q.g.ldq, q.out_rows)) return MOE_ERR_CUDA;
   int grid = moe::ring_max_ctas();
   if (grid > dev.num_sms) grid = dev.num_sms;
   if (grid < 2) return MOE_ERR_CUDA;
   moe::GemmArgs g = q.g;
+  g.out_rows = q.out_rows;
   g.ring.gather_ctas = D.gather_ctas < grid ? D.gather_ctas : grid / 2;
-  return cuda_status(moe::launch_gemm_ring(ta, tb, to, to2, tq, g, grid, s));
+  return cuda_status(moe::launch_gemm_ring(ta, tb, g, grid, s));
 }
 
 int bn_for(long n) { return n % 256 == 0 ? 256 : 128; }
@@ -785,7 +754,7 @@ int moe_backward(const moe_config *cfg, const void *dy, const void *x, const moe
     q.mx = mx;
     // MXFP8: 128-column tiles keep two TMEM accumulators next to the scale
     // columns, so this epilogue-heavy GEMM overlaps epilogue and main loop.
-    q.bn = mx ? 128 : bn_for(D.m);
+    q.bn = bn_for(D.m);
     q.epi = moe::EPI_SWIGLU_BWD;
     q.a = mx ? static_cast<const void *>(u8("dOq")) : dO;
     q.a_rows = D.Rp;

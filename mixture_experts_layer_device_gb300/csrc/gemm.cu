@@ -270,12 +270,12 @@ MOE_DEV void ring_gather_role(const GemmArgs &g, uint8_t *smem) {
   }
 }
 
-// Epilogue warps per CTA: 8 (two per TMEM lane quarter, each draining half of
-// the columns), except SwiGLU backward on 256-column tiles, whose per-row
-// working set needs the registers of a 192-thread CTA (4 warps).
+// Epilogue warps per CTA: 8, two per TMEM lane quarter, each draining half of
+// the columns (the SwiGLU backward 64 columns at a time, so its per-row working
+// set fits the registers of 320 threads at any tile width).
 template <int EPI, int BN>
 __host__ __device__ constexpr int epi_warps() {
-  return (EPI == EPI_SWIGLU_BWD && BN == 256) ? 4 : 8;
+  return 8;
 }
 
 // MC: clusters of two CTAs compute the same 128-row M-tile for two adjacent
@@ -287,8 +287,7 @@ __host__ __device__ constexpr int epi_warps() {
 template <bool MX, int BN, int EPI, bool RING = false, bool MC = false>
 __global__ void __launch_bounds__(64 + 32 * epi_warps<EPI, BN>(), 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmO2,
-                const __grid_constant__ CUtensorMap tmQ, const GemmArgs g) {
+                const GemmArgs g) {
   using C = Cfg<MX, BN>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -476,11 +475,11 @@ __global__ void __launch_bounds__(64 + 32 * epi_warps<EPI, BN>(), 1)
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int part = (warp - 2) >> 2;  // which half of the columns (8 epilogue warps)
     const int r = q * 32 + lane;
-    Stager st(staging + (warp - 2) * (C::STAGING_BYTES / NEPI), NEPI == 4 ? 2 : 1);
+    Stager st(staging + (warp - 2) * (C::STAGING_BYTES / NEPI));
+    const OutView vO = out_view(g.out, g.ldo, g.out_rows, 2);
+    const OutView vO2 = out_view(g.out2, g.ldo2, g.out_rows, 2);
+    const OutView vQ = out_view(g.outq, g.ldq, g.out_rows, 1);
     if (lane == 0) {
-      if (g.out) prefetch_tensormap(&tmO);
-      if (g.out2) prefetch_tensormap(&tmO2);
-      if (g.outq) prefetch_tensormap(&tmQ);
     }
     int acc = 0;
     uint32_t aph = 0;
@@ -504,19 +503,13 @@ __global__ void __launch_bounds__(64 + 32 * epi_warps<EPI, BN>(), 1)
         tc_fence_before();
         mbar_arrive(&tempty[acc]);
       };
-      if constexpr (NEPI == 8)
-        epilogue_tile_split<EPI, BN>(g, &tmO, &tmO2, &tmQ, st, tb, ti.nk, row0, grow, ti.out_col, lane,
-                                     part, true, release);
-      else
-        epilogue_tile<EPI, BN>(g, &tmO, &tmO2, &tmQ, st, tb, ti.nk, row0, grow, ti.out_col, lane, true,
-                               release);
+      epilogue_tile_split<EPI, BN>(g, vO, vO2, vQ, st, tb, ti.nk, row0, grow, ti.out_col, lane, part, true,
+                                   release);
       if (++acc == C::NUM_ACC) {
         acc = 0;
         aph ^= 1u;
       }
     }
-    if (lane == 0) bulk_wait<0>();  // every TMA store of this warp has landed
-    __syncwarp();
   }
 
   __syncthreads();
@@ -528,8 +521,7 @@ __global__ void __launch_bounds__(64 + 32 * epi_warps<EPI, BN>(), 1)
 }
 
 template <bool MX, int BN, int EPI>
-cudaError_t launch_one(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &to,
-                       const CUtensorMap &to2, const CUtensorMap &tq, const GemmArgs &g, int grid,
+cudaError_t launch_one(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs &g, int grid,
                        cudaStream_t s) {
   using C = Cfg<MX, BN>;
   static bool attr_set = false;  // per instantiation; idempotent, benign if repeated
@@ -540,14 +532,13 @@ cudaError_t launch_one(const CUtensorMap &ta, const CUtensorMap &tb, const CUten
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  gemm_kernel<MX, BN, EPI><<<grid, 64 + 32 * epi_warps<EPI, BN>(), C::SMEM, s>>>(ta, tb, to, to2, tq, g);
+  gemm_kernel<MX, BN, EPI><<<grid, 64 + 32 * epi_warps<EPI, BN>(), C::SMEM, s>>>(ta, tb, g);
   return cudaGetLastError();
 }
 
 // Clusters of two (MC): grid = 2 x clusters.
 template <bool MX, int BN, int EPI>
-cudaError_t launch_one_mc(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &to,
-                          const CUtensorMap &to2, const CUtensorMap &tq, const GemmArgs &g, int clusters,
+cudaError_t launch_one_mc(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs &g, int clusters,
                           cudaStream_t s) {
   using C = Cfg<MX, BN>;
   static bool attr_set = false;
@@ -570,7 +561,7 @@ cudaError_t launch_one_mc(const CUtensorMap &ta, const CUtensorMap &tb, const CU
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemm_kernel<MX, BN, EPI, false, true>, ta, tb, to, to2, tq, g);
+  return cudaLaunchKernelEx(&cfg, gemm_kernel<MX, BN, EPI, false, true>, ta, tb, g);
 }
 
 template <bool MX, int BN, int EPI>
@@ -615,13 +606,13 @@ int ring_ctas_resident() {
 int ring_max_ctas() { return ring_ctas_resident(); }
 
 cudaError_t launch_gemm_mc(bool mx, int bn, int epi, const CUtensorMap &ta_half, const CUtensorMap &tb,
-                           const CUtensorMap &to, const CUtensorMap &to2, const CUtensorMap &tq,
                            const GemmArgs &g, int clusters, cudaStream_t s) {
   if (clusters <= 0) return cudaSuccess;
 #define MOE_GEMM_MC(BNV, EPIV) \
-  if (mx && bn == BNV && epi == EPIV) return launch_one_mc<true, BNV, EPIV>(ta_half, tb, to, to2, tq, g, clusters, s);
+  if (mx && bn == BNV && epi == EPIV) return launch_one_mc<true, BNV, EPIV>(ta_half, tb, g, clusters, s);
   MOE_GEMM_MC(256, EPI_STORE)
   MOE_GEMM_MC(256, EPI_SWIGLU)
+  MOE_GEMM_MC(256, EPI_SWIGLU_BWD)
   MOE_GEMM_MC(128, EPI_SWIGLU_BWD)
 #undef MOE_GEMM_MC
   return cudaErrorInvalidValue;
@@ -630,12 +621,12 @@ cudaError_t launch_gemm_mc(bool mx, int bn, int epi, const CUtensorMap &ta_half,
 int gemm_mc_max_clusters(bool mx, int bn, int epi) {
   if (mx && bn == 256 && epi == EPI_STORE) return max_clusters_mc<true, 256, EPI_STORE>();
   if (mx && bn == 256 && epi == EPI_SWIGLU) return max_clusters_mc<true, 256, EPI_SWIGLU>();
+  if (mx && bn == 256 && epi == EPI_SWIGLU_BWD) return max_clusters_mc<true, 256, EPI_SWIGLU_BWD>();
   if (mx && bn == 128 && epi == EPI_SWIGLU_BWD) return max_clusters_mc<true, 128, EPI_SWIGLU_BWD>();
   return 0;
 }
 
-cudaError_t launch_gemm_ring(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &to,
-                             const CUtensorMap &to2, const CUtensorMap &tq, const GemmArgs &g, int grid,
+cudaError_t launch_gemm_ring(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs &g, int grid,
                              cudaStream_t s) {
   using C = Cfg<true, 256>;
   // Gather and GEMM CTAs wait on each other: all of them must be resident at
@@ -652,16 +643,15 @@ cudaError_t launch_gemm_ring(const CUtensorMap &ta, const CUtensorMap &tb, const
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemm_kernel<true, 256, EPI_SWIGLU, true>, ta, tb, to, to2, tq, g);
+  return cudaLaunchKernelEx(&cfg, gemm_kernel<true, 256, EPI_SWIGLU, true>, ta, tb, g);
 }
 
 cudaError_t launch_gemm(bool mx, int bn, int epi, const CUtensorMap &ta, const CUtensorMap &tb,
-                        const CUtensorMap &to, const CUtensorMap &to2, const CUtensorMap &tq,
                         const GemmArgs &g, int grid, cudaStream_t s) {
   if (grid <= 0) return cudaSuccess;
 #define MOE_GEMM_CASE(MXV, BNV, EPIV) \
   if (mx == MXV && bn == BNV && epi == EPIV)  \
-    return launch_one<MXV, BNV, EPIV>(ta, tb, to, to2, tq, g, grid, s);
+    return launch_one<MXV, BNV, EPIV>(ta, tb, g, grid, s);
   MOE_GEMM_CASE(false, 256, EPI_STORE)
   MOE_GEMM_CASE(false, 128, EPI_STORE)
   MOE_GEMM_CASE(false, 256, EPI_SWIGLU)

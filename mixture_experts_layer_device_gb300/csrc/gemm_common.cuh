@@ -36,52 +36,61 @@ MOE_DEV uint32_t mx_block_words(const float *v, uint32_t *w) {
   return byte;
 }
 
+// One epilogue output: base pointer, row stride (bytes), rows that exist,
+// element size.
+struct OutView {
+  uint8_t *p;
+  long ld;
+  long rows;
+  int esz;
+};
+
+MOE_DEV OutView out_view(void *p, long ld_elems, long rows, int esz) {
+  return OutView{static_cast<uint8_t *>(p), ld_elems * esz, rows, esz};
+}
+
 // Per-warp writer of 32-row x 64-byte output pieces: each lane places its row's
-// 64 bytes in a 64-byte-swizzled shared-memory buffer (conflict-free), then one
-// lane stores the box with TMA.  With several buffers the staging of one piece
-// overlaps the stores of the previous ones; a buffer is reused only after the
-// store that last read it has finished reading shared memory.
+// 64 bytes in a 64-byte-swizzled shared-memory buffer (conflict-free); the
+// warp reads the piece back transposed, 8 rows x 64 bytes per instruction, and
+// writes it with coalesced 16-byte global stores.  The buffer is free again as
+// soon as the read-back is done, so a multi-piece epilogue never waits for an
+// earlier store, and the stores do not queue behind the producer's TMA loads.
 struct Stager {
-  uint8_t *buf;  // nbuf x 2 KB, 512-byte aligned
-  int n;
-  int nbuf;      // 1, 2 or 4
-  MOE_DEV Stager(uint8_t *b, int buffers) : buf(b), n(0), nbuf(buffers) {}
-  MOE_DEV void put(const CUtensorMap *map, const uint32_t *w16, int c0, int row0, int lane) {
-    uint8_t *half = buf + (n & (nbuf - 1)) * 2048;
-    if (lane == 0 && n >= nbuf) {
-      if (nbuf == 4) bulk_wait_read<3>();
-      else if (nbuf == 2) bulk_wait_read<1>();
-      else bulk_wait_read<0>();
-    }
-    __syncwarp();
+  uint8_t *buf;  // 2 KB, 16-byte aligned
+  MOE_DEV explicit Stager(uint8_t *b) : buf(b) {}
+  MOE_DEV void put(const OutView &o, const uint32_t *w16, int c0, int row0, int lane) {
+    __syncwarp();  // every lane has read back the previous piece
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int jj = j ^ ((lane >> 1) & 3);
-      *reinterpret_cast<uint4 *>(half + lane * 64 + jj * 16) =
+      *reinterpret_cast<uint4 *>(buf + lane * 64 + jj * 16) =
           make_uint4(w16[4 * j], w16[4 * j + 1], w16[4 * j + 2], w16[4 * j + 3]);
     }
-    fence_proxy_async_smem();
     __syncwarp();
-    if (lane == 0) {
-      tma_store_2d(map, half, c0, row0);
-      bulk_commit();
+    const int j = lane & 3;
+    uint8_t *colp = o.p + static_cast<long>(c0) * o.esz + j * 16;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int r = 8 * i + (lane >> 2);
+      const uint4 v = *reinterpret_cast<const uint4 *>(buf + r * 64 + ((j ^ ((r >> 1) & 3)) * 16));
+      const long row = static_cast<long>(row0) + r;
+      if (row < o.rows) *reinterpret_cast<uint4 *>(colp + row * o.ld) = v;
     }
-    ++n;
   }
-  MOE_DEV void put_bf16(const CUtensorMap *map, const float *v32, int c0, int row0, int lane) {
+  MOE_DEV void put_bf16(const OutView &o, const float *v32, int c0, int row0, int lane) {
     uint32_t w[16];
     bf16x32_words(v32, w);
-    put(map, w, c0, row0, lane);
+    put(o, w, c0, row0, lane);
   }
 };
 
 // Two MX blocks (64 values) of one row -> one 64-byte codes piece + 2 scale bytes.
-MOE_DEV void put_mx64(Stager &st, const CUtensorMap *map, uint8_t *sf, long ldq, const float *v64,
+MOE_DEV void put_mx64(Stager &st, const OutView &vq, uint8_t *sf, long ldq, const float *v64,
                       int col, int row0, long grow, int lane) {
   uint32_t w[16];
   const uint32_t b0 = mx_block_words(v64, w);
   const uint32_t b1 = mx_block_words(v64 + 32, w + 8);
-  st.put(map, w, col, row0, lane);
+  st.put(vq, w, col, row0, lane);
   // (col / 32) is even, so both bytes sit next to each other in one 512-byte atom.
   *reinterpret_cast<uint16_t *>(sf + sf_tiled_offset(grow, col / 32, ldq)) =
       static_cast<uint16_t>(b0 | (b1 << 8));
@@ -94,8 +103,8 @@ MOE_DEV void put_mx64(Stager &st, const CUtensorMap *map, uint8_t *sf, long ldq,
 // store == false the accumulator is drained and released but nothing is
 // written (the idle half of a 2-CTA tile).
 template <int EPI, int BN, typename Release>
-MOE_DEV void epilogue_tile(const GemmArgs &g, const CUtensorMap *tmO, const CUtensorMap *tmO2,
-                           const CUtensorMap *tmQ, Stager &st, uint32_t tb, int nk, int row0,
+MOE_DEV void epilogue_tile(const GemmArgs &g, const OutView &vO, const OutView &vO2,
+                           const OutView &vQ, Stager &st, uint32_t tb, int nk, int row0,
                            long grow, int out_col, int lane, bool store, Release release) {
   if constexpr (EPI == EPI_STORE) {
     constexpr int NCH = BN / 64;
@@ -106,7 +115,7 @@ MOE_DEV void epilogue_tile(const GemmArgs &g, const CUtensorMap *tmO, const CUte
 #pragma unroll
         for (int i = 0; i < 32; ++i) z[i] = 0.f;
 #pragma unroll 1
-        for (int c = 0; c < 2 * NCH; ++c) st.put_bf16(tmO, z, out_col + 32 * c, row0, lane);
+        for (int c = 0; c < 2 * NCH; ++c) st.put_bf16(vO, z, out_col + 32 * c, row0, lane);
       }
       return;
     }
@@ -132,7 +141,7 @@ MOE_DEV void epilogue_tile(const GemmArgs &g, const CUtensorMap *tmO, const CUte
     release();
     if (store) {
 #pragma unroll
-      for (int c = 0; c < NC32; ++c) st.put(tmO, pk + 16 * c, out_col + 32 * c, row0, lane);
+      for (int c = 0; c < NC32; ++c) st.put(vO, pk + 16 * c, out_col + 32 * c, row0, lane);
     }
   } else if constexpr (EPI == EPI_SWIGLU) {
     // accumulator columns [0,128) = gate G, [128,256) = up U of 128 h columns
@@ -163,7 +172,7 @@ MOE_DEV void epilogue_tile(const GemmArgs &g, const CUtensorMap *tmO, const CUte
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           const int col = out_col + 64 * c;
-          st.put(tmQ, cw + 16 * c, col, row0, lane);
+          st.put(vQ, cw + 16 * c, col, row0, lane);
           *reinterpret_cast<uint16_t *>(g.outq_sf + sf_tiled_offset(grow, col / 32, g.ldq)) =
               static_cast<uint16_t>(sb[2 * c] | (sb[2 * c + 1] << 8));
         }
@@ -186,18 +195,18 @@ MOE_DEV void epilogue_tile(const GemmArgs &g, const CUtensorMap *tmO, const CUte
       float *U = reinterpret_cast<float *>(ur);
       const int col = out_col + 64 * c;
       if (g.out2) {
-        st.put_bf16(tmO2, G, col, row0, lane);
-        st.put_bf16(tmO2, G + 32, col + 32, row0, lane);
-        st.put_bf16(tmO2, U, g.m_half + col, row0, lane);
-        st.put_bf16(tmO2, U + 32, g.m_half + col + 32, row0, lane);
+        st.put_bf16(vO2, G, col, row0, lane);
+        st.put_bf16(vO2, G + 32, col + 32, row0, lane);
+        st.put_bf16(vO2, U, g.m_half + col, row0, lane);
+        st.put_bf16(vO2, U + 32, g.m_half + col + 32, row0, lane);
       }
 #pragma unroll
       for (int i = 0; i < 64; ++i) G[i] = silu(G[i]) * U[i];  // h, in place
       if (g.out) {
-        st.put_bf16(tmO, G, col, row0, lane);
-        st.put_bf16(tmO, G + 32, col + 32, row0, lane);
+        st.put_bf16(vO, G, col, row0, lane);
+        st.put_bf16(vO, G + 32, col + 32, row0, lane);
       }
-      if (g.outq) put_mx64(st, tmQ, g.outq_sf, g.ldq, G, col, row0, grow, lane);
+      if (g.outq) put_mx64(st, vQ, g.outq_sf, g.ldq, G, col, row0, grow, lane);
     }
   } else {  // EPI_SWIGLU_BWD: accumulator = dh; G|U saved in bf16
     constexpr int NCH = BN / 64;
@@ -226,25 +235,25 @@ MOE_DEV void epilogue_tile(const GemmArgs &g, const CUtensorMap *tmO, const CUte
           dU[32 * hh + i] = round_bf16(d * G[i] * sg);
         }
       }
-      st.put_bf16(tmO, dG, col, row0, lane);
-      st.put_bf16(tmO, dG + 32, col + 32, row0, lane);
-      st.put_bf16(tmO, dU, g.m_half + col, row0, lane);
-      st.put_bf16(tmO, dU + 32, g.m_half + col + 32, row0, lane);
+      st.put_bf16(vO, dG, col, row0, lane);
+      st.put_bf16(vO, dG + 32, col + 32, row0, lane);
+      st.put_bf16(vO, dU, g.m_half + col, row0, lane);
+      st.put_bf16(vO, dU + 32, g.m_half + col + 32, row0, lane);
       if (g.outq) {
-        put_mx64(st, tmQ, g.outq_sf, g.ldq, dG, col, row0, grow, lane);
-        put_mx64(st, tmQ, g.outq_sf, g.ldq, dU, g.m_half + col, row0, grow, lane);
+        put_mx64(st, vQ, g.outq_sf, g.ldq, dG, col, row0, grow, lane);
+        put_mx64(st, vQ, g.outq_sf, g.ldq, dU, g.m_half + col, row0, grow, lane);
       }
     }
   }
 }
 
 // Epilogue shared by two warps per TMEM lane quarter: warp `part` (0 or 1)
-// drains half of the tile's columns.  The accumulator is read in one round
-// (two warps in parallel) and released before any conversion or store.
-// EPI_SWIGLU_BWD needs BN = 128 here (64 dh columns per warp).
+// drains half of the tile's columns.  For the store and SwiGLU epilogues the
+// accumulator is read in one round (two warps in parallel) and released before
+// any conversion or store; the SwiGLU backward reads its columns 64 at a time.
 template <int EPI, int BN, typename Release>
-MOE_DEV void epilogue_tile_split(const GemmArgs &g, const CUtensorMap *tmO, const CUtensorMap *tmO2,
-                                 const CUtensorMap *tmQ, Stager &st, uint32_t tb, int nk, int row0,
+MOE_DEV void epilogue_tile_split(const GemmArgs &g, const OutView &vO, const OutView &vO2,
+                                 const OutView &vQ, Stager &st, uint32_t tb, int nk, int row0,
                                  long grow, int out_col, int lane, int part, bool store,
                                  Release release) {
   if constexpr (EPI == EPI_STORE) {
@@ -258,7 +267,7 @@ MOE_DEV void epilogue_tile_split(const GemmArgs &g, const CUtensorMap *tmO, cons
 #pragma unroll
         for (int i = 0; i < 32; ++i) z[i] = 0.f;
 #pragma unroll 1
-        for (int c = 0; c < NC32; ++c) st.put_bf16(tmO, z, out_col + c0 + 32 * c, row0, lane);
+        for (int c = 0; c < NC32; ++c) st.put_bf16(vO, z, out_col + c0 + 32 * c, row0, lane);
       }
       return;
     }
@@ -279,50 +288,55 @@ MOE_DEV void epilogue_tile_split(const GemmArgs &g, const CUtensorMap *tmO, cons
     release();
     if (store) {
 #pragma unroll
-      for (int c = 0; c < NC32; ++c) st.put(tmO, pk + 16 * c, out_col + c0 + 32 * c, row0, lane);
+      for (int c = 0; c < NC32; ++c) st.put(vO, pk + 16 * c, out_col + c0 + 32 * c, row0, lane);
     }
   } else if constexpr (EPI == EPI_SWIGLU_BWD) {
-    static_assert(BN == 128, "split SwiGLU-backward epilogue expects 128-column tiles");
-    const int dc = part * 64;  // this warp's 64 dh columns
-    uint32_t hr[64];
-    tmem_ld32_async(tb + dc, hr);
-    tmem_ld32_async(tb + dc + 32, hr + 32);
-    tmem_ld_wait();
-    reg_fence<64>(hr);
-    release();
-    if (!store) return;
-    const float *dh = reinterpret_cast<const float *>(hr);
-    const int col = out_col + dc;
-    uint32_t cg[16], cu[16];  // MX codes of dG and dU (two blocks each)
-    uint32_t sg[2], su[2];
+    // This warp's BN/2 dh columns, 64 at a time: each chunk is read from TMEM,
+    // then processed; TMEM is released once the last chunk has been read.
+    constexpr int NCH = BN / 128;
+#pragma unroll 1
+    for (int ch = 0; ch < NCH; ++ch) {
+      const int dc = part * (BN / 2) + 64 * ch;  // accumulator column of this chunk
+      uint32_t hr[64];
+      tmem_ld32_async(tb + dc, hr);
+      tmem_ld32_async(tb + dc + 32, hr + 32);
+      tmem_ld_wait();
+      reg_fence<64>(hr);
+      if (ch == NCH - 1) release();
+      if (!store) continue;
+      const float *dh = reinterpret_cast<const float *>(hr);
+      const int col = out_col + dc;
+      uint32_t cg[16], cu[16];  // MX codes of dG and dU (two blocks each)
+      uint32_t sg[2], su[2];
 #pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      float G[32], U[32];
-      load_bf16x32(g.aux, grow, g.ld_aux, col + 32 * hh, G);
-      load_bf16x32(g.aux, grow, g.ld_aux, g.m_half + col + 32 * hh, U);
+      for (int hh = 0; hh < 2; ++hh) {
+        float G[32], U[32];
+        load_bf16x32(g.aux, grow, g.ld_aux, col + 32 * hh, G);
+        load_bf16x32(g.aux, grow, g.ld_aux, g.m_half + col + 32 * hh, U);
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const float d = dh[32 * hh + i];
-        const float sgm = sigmoidf(G[i]);
-        const float dg = round_bf16(d * U[i] * sgm * (1.0f + G[i] * (1.0f - sgm)));
-        const float du = round_bf16(d * G[i] * sgm);
-        G[i] = dg;
-        U[i] = du;
+        for (int i = 0; i < 32; ++i) {
+          const float d = dh[32 * hh + i];
+          const float sgm = sigmoidf(G[i]);
+          const float dg = round_bf16(d * U[i] * sgm * (1.0f + G[i] * (1.0f - sgm)));
+          const float du = round_bf16(d * G[i] * sgm);
+          G[i] = dg;
+          U[i] = du;
+        }
+        st.put_bf16(vO, G, col + 32 * hh, row0, lane);
+        st.put_bf16(vO, U, g.m_half + col + 32 * hh, row0, lane);
+        if (g.outq) {
+          sg[hh] = mx_block_words(G, cg + 8 * hh);
+          su[hh] = mx_block_words(U, cu + 8 * hh);
+        }
       }
-      st.put_bf16(tmO, G, col + 32 * hh, row0, lane);
-      st.put_bf16(tmO, U, g.m_half + col + 32 * hh, row0, lane);
       if (g.outq) {
-        sg[hh] = mx_block_words(G, cg + 8 * hh);
-        su[hh] = mx_block_words(U, cu + 8 * hh);
+        st.put(vQ, cg, col, row0, lane);
+        st.put(vQ, cu, g.m_half + col, row0, lane);
+        *reinterpret_cast<uint16_t *>(g.outq_sf + sf_tiled_offset(grow, col / 32, g.ldq)) =
+            static_cast<uint16_t>(sg[0] | (sg[1] << 8));
+        *reinterpret_cast<uint16_t *>(g.outq_sf + sf_tiled_offset(grow, (g.m_half + col) / 32, g.ldq)) =
+            static_cast<uint16_t>(su[0] | (su[1] << 8));
       }
-    }
-    if (g.outq) {
-      st.put(tmQ, cg, col, row0, lane);
-      st.put(tmQ, cu, g.m_half + col, row0, lane);
-      *reinterpret_cast<uint16_t *>(g.outq_sf + sf_tiled_offset(grow, col / 32, g.ldq)) =
-          static_cast<uint16_t>(sg[0] | (sg[1] << 8));
-      *reinterpret_cast<uint16_t *>(g.outq_sf + sf_tiled_offset(grow, (g.m_half + col) / 32, g.ldq)) =
-          static_cast<uint16_t>(su[0] | (su[1] << 8));
     }
   } else {  // EPI_SWIGLU: accumulator [0,128) = G, [128,256) = U; this warp: 64 h columns
     const int hc = part * 64;
@@ -340,18 +354,18 @@ MOE_DEV void epilogue_tile_split(const GemmArgs &g, const CUtensorMap *tmO, cons
     const float *U = reinterpret_cast<const float *>(ur);
     const int col = out_col + hc;
     if (g.out2) {
-      st.put_bf16(tmO2, G, col, row0, lane);
-      st.put_bf16(tmO2, G + 32, col + 32, row0, lane);
-      st.put_bf16(tmO2, U, g.m_half + col, row0, lane);
-      st.put_bf16(tmO2, U + 32, g.m_half + col + 32, row0, lane);
+      st.put_bf16(vO2, G, col, row0, lane);
+      st.put_bf16(vO2, G + 32, col + 32, row0, lane);
+      st.put_bf16(vO2, U, g.m_half + col, row0, lane);
+      st.put_bf16(vO2, U + 32, g.m_half + col + 32, row0, lane);
     }
 #pragma unroll
     for (int i = 0; i < 64; ++i) G[i] = silu(G[i]) * U[i];  // h, in place
     if (g.out) {
-      st.put_bf16(tmO, G, col, row0, lane);
-      st.put_bf16(tmO, G + 32, col + 32, row0, lane);
+      st.put_bf16(vO, G, col, row0, lane);
+      st.put_bf16(vO, G + 32, col + 32, row0, lane);
     }
-    if (g.outq) put_mx64(st, tmQ, g.outq_sf, g.ldq, G, col, row0, grow, lane);
+    if (g.outq) put_mx64(st, vQ, g.outq_sf, g.ldq, G, col, row0, grow, lane);
   }
 }
 

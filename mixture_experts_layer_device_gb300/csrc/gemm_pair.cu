@@ -145,10 +145,7 @@ template <bool MX, int EPI, int NUM_ACC>
 __global__ void __launch_bounds__(192, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmSFA,
-                     const __grid_constant__ CUtensorMap tmSFB,
-                     const __grid_constant__ CUtensorMap tmO,
-                     const __grid_constant__ CUtensorMap tmO2,
-                     const __grid_constant__ CUtensorMap tmQ, const GemmArgs g) {
+                     const __grid_constant__ CUtensorMap tmSFB, const GemmArgs g) {
   using C = PairCfg<MX, NUM_ACC>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -308,11 +305,11 @@ __global__ void __launch_bounds__(192, 1)
     // ------------------------------------------------ epilogue (warps 2..5, both CTAs)
     const int q = warp & 3;
     const int r = q * 32 + lane;
-    Stager st(staging + (warp - 2) * 4096, 2);
+    Stager st(staging + (warp - 2) * 4096);
+    const OutView vO = out_view(g.out, g.ldo, g.out_rows, 2);
+    const OutView vO2 = out_view(g.out2, g.ldo2, g.out_rows, 2);
+    const OutView vQ = out_view(g.outq, g.ldq, g.out_rows, 1);
     if (lane == 0) {
-      if (g.out) prefetch_tensormap(&tmO);
-      if (g.out2) prefetch_tensormap(&tmO2);
-      if (g.outq) prefetch_tensormap(&tmQ);
     }
     int acc = 0;
     uint32_t aph = 0;
@@ -338,15 +335,13 @@ __global__ void __launch_bounds__(192, 1)
         if (leader) mbar_arrive(&tempty[acc]);
         else mbar_arrive_remote(peer_smem(tempty_addr, 0));
       };
-      epilogue_tile<EPI, C::BN>(g, &tmO, &tmO2, &tmQ, st, tb, ti.nk, row0, grow, ti.out_col, lane,
+      epilogue_tile<EPI, C::BN>(g, vO, vO2, vQ, st, tb, ti.nk, row0, grow, ti.out_col, lane,
                                 ti.store, release);
       if (++acc == NUM_ACC) {
         acc = 0;
         aph ^= 1u;
       }
     }
-    if (lane == 0) bulk_wait<0>();
-    __syncwarp();
   }
 
   __syncthreads();
@@ -380,8 +375,7 @@ cudaError_t launch_pair_one(const PairMaps &m, const GemmArgs &g, int clusters, 
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemm_pair_kernel<MX, EPI, NUM_ACC>, m.a, m.b, m.sfa, m.sfb, m.o,
-                            m.o2, m.q, g);
+  return cudaLaunchKernelEx(&cfg, gemm_pair_kernel<MX, EPI, NUM_ACC>, m.a, m.b, m.sfa, m.sfb, g);
 }
 
 }  // namespace

@@ -131,6 +131,7 @@ struct GemmArgs {
   long ldo;
   void *out2;         // SWIGLU: G|U save [rows, 2m] bf16 (may be NULL)
   long ldo2;
+  long out_rows;      // rows of out / out2 / outq (stores beyond are skipped)
   uint8_t *outq;      // SWIGLU / SWIGLU_BWD MX codes (may be NULL)
   uint8_t *outq_sf;   // tiled scales of outq
   long ldq;           // row stride of outq (= its K)
@@ -146,12 +147,10 @@ struct GemmArgs {
 
 // D = A * B^T with A [rows, K] and B [rows, K] K-major (TMA maps built by the
 // caller, box = 128 rows x 128 bytes, 128-byte swizzle); bn = 128 or 256
-// output columns per tile; `grid` persistent CTAs (<= number of SMs).
-// Outputs are written with TMA stores through maps of box 32 rows x 64 bytes
-// with the 64-byte swizzle: `to` for args.out, `to2` for args.out2, `tq` for
-// args.outq (unused maps may be zero-filled).
+// output columns per tile; `grid` persistent CTAs (<= number of SMs).  The
+// epilogue writes args.out / out2 / outq (row strides ldo / ldo2 / ldq) with
+// coalesced global stores, rows < args.out_rows.
 cudaError_t launch_gemm(bool mx, int bn, int epi, const CUtensorMap &ta, const CUtensorMap &tb,
-                        const CUtensorMap &to, const CUtensorMap &to2, const CUtensorMap &tq,
                         const GemmArgs &args, int grid, cudaStream_t s);
 
 // The same GEMM on clusters of two CTAs sharing the A tile (MXFP8, for the
@@ -160,7 +159,6 @@ cudaError_t launch_gemm(bool mx, int bn, int epi, const CUtensorMap &ta, const C
 // half of A for both (TMA multicast).  `ta_half` maps A with a 64-row box;
 // args.n_tiles must be even.  `clusters` <= gemm_mc_max_clusters().
 cudaError_t launch_gemm_mc(bool mx, int bn, int epi, const CUtensorMap &ta_half, const CUtensorMap &tb,
-                           const CUtensorMap &to, const CUtensorMap &to2, const CUtensorMap &tq,
                            const GemmArgs &args, int clusters, cudaStream_t s);
 int gemm_mc_max_clusters(bool mx, int bn, int epi);
 
@@ -168,17 +166,16 @@ int gemm_mc_max_clusters(bool mx, int bn, int epi);
 // one cooperative launch of `grid` CTAs (all co-resident, one per SM), of
 // which args.ring.gather_ctas gather.  `ta` maps the ring codes
 // [slots * 128, d].  args.ring.ready / freed / abort must be zero at launch.
-cudaError_t launch_gemm_ring(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &to,
-                             const CUtensorMap &to2, const CUtensorMap &tq, const GemmArgs &args, int grid,
+cudaError_t launch_gemm_ring(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs &args, int grid,
                              cudaStream_t s);
 // CTAs of the ring GEMM that can be resident at once on the current device.
 int ring_max_ctas();
 
 // Tensor maps of one 2-CTA GEMM launch: operands (box 128 rows x 128 bytes,
-// 128-byte swizzle), MXFP8 scale buffers viewed as rows of 256 bytes (box
-// 2 rows = one 512-byte atom), and the epilogue's store maps.
+// 128-byte swizzle) and MXFP8 scale buffers viewed as rows of 256 bytes (box
+// 2 rows = one 512-byte atom).
 struct PairMaps {
-  CUtensorMap a, b, sfa, sfb, o, o2, q;
+  CUtensorMap a, b, sfa, sfb;
 };
 
 // D = A * B^T on CTA pairs (tcgen05 cta_group::2): 256 x 256 tiles, two
