@@ -125,13 +125,41 @@ class MoELayer:
             check(moe_quantize_mx(gu, E, 2 * m, d, 0, t["gu"], t["gu_scale"], stream))
             check(moe_quantize_mx(dn, E, d, m, 0, t["dn"], t["dn_scale"], stream))
 
+    def prepare_from(self, gu, dn, s_gu=None, s_dn=None, stream=None):
+        """Re-derive every operand the kernels read from the current bf16
+        masters (W_gu [E, 2m, d], W_dn [E, d, m], shared W_s_gu [2m_s, d],
+        W_s_dn [d, m_s]): MXFP8 codes (both orientations for training) or bf16
+        copies and transposes.  Run after every update of the masters."""
+        E, d, m, t = self.E, self.d, self.m, self.tensors
+        gu, dn = gu.contiguous(), dn.contiguous()
+        if self.mx:
+            self.prepare_stacked(gu, dn, stream)
+        else:
+            t["gu"].copy_(gu)
+            t["dn"].copy_(dn)
+            if self.backward_enabled:
+                check(moe_transpose_bf16(gu, E, 2 * m, d, t["gu_t"], stream))
+                check(moe_transpose_bf16(dn, E, d, m, t["dn_t"], stream))
+        if self.ms:
+            t["s_gu"], t["s_dn"] = s_gu.contiguous(), s_dn.contiguous()
+            if self.backward_enabled:
+                check(moe_transpose_bf16(t["s_gu"], 1, 2 * self.ms, d, t["s_gu_t"], stream))
+                check(moe_transpose_bf16(t["s_dn"], 1, d, self.ms, t["s_dn_t"], stream))
+        self.W = weights(**t)
+
+    def new_saved(self):
+        """A fresh buffer for the activations one training forward keeps."""
+        return _u8(moe_saved_bytes(self.cfg), self.device)
+
     # ------------------------------------------------------------ passes
-    def forward(self, x, logits, y=None, train=False, stream=None):
+    def forward(self, x, logits, y=None, train=False, stream=None, saved=None):
         if y is None:
             y = torch.empty((self.T, self.d), dtype=torch.bfloat16, device=self.device)
-        if train and self.saved is None:
-            raise ValueError("layer was built without backward support")
-        check(moe_forward(self.cfg, x, logits, self.W, y, self.saved if train else None, self.ws, stream))
+        if train and saved is None:
+            if self.saved is None:
+                raise ValueError("layer was built without backward support")
+            saved = self.saved
+        check(moe_forward(self.cfg, x, logits, self.W, y, saved if train else None, self.ws, stream))
         return y
 
     def alloc_grads(self):
@@ -146,10 +174,10 @@ class MoELayer:
             g["dWs_dn"] = torch.empty((d, ms), dtype=torch.bfloat16, device=dev)
         return g
 
-    def backward(self, dy, x, grads=None, stream=None):
+    def backward(self, dy, x, grads=None, stream=None, saved=None):
         g = grads or self.alloc_grads()
-        check(moe_backward(self.cfg, dy, x, self.W, self.saved, g["dx"], g["dlogits"], g["dW_gu"], g["dW_dn"],
-                           g["dWs_gu"], g["dWs_dn"], self.ws, stream))
+        check(moe_backward(self.cfg, dy, x, self.W, self.saved if saved is None else saved, g["dx"], g["dlogits"],
+                           g["dW_gu"], g["dW_dn"], g["dWs_gu"], g["dWs_dn"], self.ws, stream))
         return g
 
     def status(self, stream=None):
