@@ -99,6 +99,17 @@ typedef enum {
  *                ring_rows = 0 for every ring size and SM split.
  *   gather_sms = gather SMs of the ring launch (0 = 8; at most 64).
  *   The ring needs d <= 8192 (MOE_ERR_SHAPE otherwise).
+ *
+ * Load-balancing term (aux_alpha > 0; the pages define none, so this is the
+ * Switch-Transformer auxiliary loss taken over the k routed slots):
+ *   L = aux_alpha * E * sum_e f_e * P_e,  f_e = counts_e / (T k),
+ *   P_e = (1/T) sum_t softmax(logits_t)_e over all E experts.
+ * moe_forward computes it after the schedule (fixed-order sums, bitwise
+ * reproducible) into the workspace buffer "aux" = [L, P[E], f[E]] fp32
+ * (moe_buffer_info); a training forward also keeps dL/dlogits =
+ * aux_alpha E / T * p (f - sum_e f_e p_e), which moe_backward adds to
+ * dlogits (the loss enters the objective with weight 1; f is piecewise
+ * constant, so no gradient flows through the counts).
  */
 typedef struct {
   int32_t T, d, m, E, k;
@@ -107,6 +118,7 @@ typedef struct {
   int32_t flags;
   int32_t ring_rows;
   int32_t gather_sms;
+  float aux_alpha; /* 0 = no load-balancing term */
 } moe_config;
 
 /*
@@ -199,6 +211,27 @@ int moe_transpose_bf16(const void *src, int batch, int rows, int cols, void *dst
  */
 int moe_route(const moe_config *cfg, const float *logits, int32_t *idx, float *w, int32_t *counts,
               int32_t *offsets, int32_t *perm, void *ws, moe_stream_t stream);
+
+/*
+ * Router projection in front of the layer (daily-ai-frontier summary, TL;DR:
+ * routing is the first fused stage; the pages do not define the projection,
+ * so it is a bias-free linear map): logits [T, E] fp32 = x [T, d] bf16 *
+ * W_r [E, d] bf16 ^T with fp32 accumulation.  A plain GEMM, run by cuBLAS on
+ * `stream` with its workspace inside `ws` (a cuBLAS handle is created once per
+ * device on first use).  Deterministic for a given device.
+ */
+int moe_router_forward(const moe_config *cfg, const void *x, const void *W_r, float *logits, void *ws,
+                       moe_stream_t stream);
+
+/*
+ * Router backward: dlogits [T, E] fp32 (moe_backward's output, including the
+ * load-balancing term) is rounded to bf16 g; then dx [T, d] bf16 is updated in
+ * place to bf16(dx + g W_r) (the layer's dx plus the router's, one rounding)
+ * and dW_r [E, d] bf16 = bf16(g^T x).  ws must be sized with
+ * MOE_FLAG_BACKWARD.
+ */
+int moe_router_backward(const moe_config *cfg, const float *dlogits, const void *x, const void *W_r, void *dx,
+                        void *dW_r, void *ws, moe_stream_t stream);
 
 /*
  * Forward pass: route -> schedule -> dispatch gather (MXFP8: x quantised in

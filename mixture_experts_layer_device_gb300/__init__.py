@@ -26,7 +26,7 @@ WEIGHT_FIELDS = ["gu", "gu_scale", "dn", "dn_scale", "gu_t", "gu_t_scale", "dn_t
 
 class MoeConfig(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in ("T", "d", "m", "E", "k", "m_shared", "dtype", "flags",
-                                              "ring_rows", "gather_sms")]
+                                              "ring_rows", "gather_sms")] + [("aux_alpha", ctypes.c_float)]
 
 
 class MoeWeights(ctypes.Structure):
@@ -37,7 +37,7 @@ _lib = None
 EXPORTS = ["moe_workspace_bytes", "moe_saved_bytes", "moe_buffer_info", "moe_padded_rows",
            "moe_quantize_mx", "moe_quantize_mx_both", "moe_transpose_bf16", "moe_route", "moe_forward", "moe_backward",
            "moe_get_status", "moe_status_string", "moe_trace_enable", "moe_trace_clear", "moe_trace_count",
-           "moe_trace_name", "moe_trace_ms", "moe_route_noalloc"]
+           "moe_trace_name", "moe_trace_ms", "moe_route_noalloc", "moe_router_forward", "moe_router_backward"]
 
 
 def lib():
@@ -66,6 +66,8 @@ def lib():
         L.moe_get_status.argtypes, L.moe_get_status.restype = [P, S], I
         L.moe_status_string.argtypes, L.moe_status_string.restype = [I], ctypes.c_char_p
         L.moe_route_noalloc.argtypes, L.moe_route_noalloc.restype = [cfgp, P, P, P, P, P, P, S], I
+        L.moe_router_forward.argtypes, L.moe_router_forward.restype = [cfgp, P, P, P, P, S], I
+        L.moe_router_backward.argtypes, L.moe_router_backward.restype = [cfgp, P, P, P, P, P, P, S], I
         L.moe_trace_enable.argtypes, L.moe_trace_enable.restype = [I], I
         L.moe_trace_clear.argtypes, L.moe_trace_clear.restype = [], None
         L.moe_trace_count.argtypes, L.moe_trace_count.restype = [], I
@@ -92,10 +94,19 @@ def _stream(stream):
     return stream.cuda_stream
 
 
-def config(T, d, m, E, k, m_shared=0, dtype=MOE_BF16, flags=0, ring_rows=0, gather_sms=0):
+def config(T, d, m, E, k, m_shared=0, dtype=MOE_BF16, flags=0, ring_rows=0, gather_sms=0, aux_alpha=0.0):
     if isinstance(dtype, str):
         dtype = MOE_MXFP8 if dtype == "mxfp8" else MOE_BF16
-    return MoeConfig(T, d, m, E, k, m_shared, dtype, flags, ring_rows, gather_sms)
+    return MoeConfig(T, d, m, E, k, m_shared, dtype, flags, ring_rows, gather_sms, aux_alpha)
+
+
+def moe_router_forward(cfg, x, W_r, logits, ws, stream=None):
+    return lib().moe_router_forward(ctypes.byref(cfg), _ptr(x), _ptr(W_r), _ptr(logits), _ptr(ws), _stream(stream))
+
+
+def moe_router_backward(cfg, dlogits, x, W_r, dx, dW_r, ws, stream=None):
+    return lib().moe_router_backward(ctypes.byref(cfg), _ptr(dlogits), _ptr(x), _ptr(W_r), _ptr(dx), _ptr(dW_r),
+                                     _ptr(ws), _stream(stream))
 
 
 def weights(**kw):

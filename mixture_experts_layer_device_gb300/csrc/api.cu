@@ -3,6 +3,7 @@
 // the launch sequence of the forward and backward passes.  Nothing here
 // allocates memory or synchronises the host with the device (except
 // moe_get_status, which exists to do exactly that).
+#include <cublas_v2.h>
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <string.h>
@@ -20,11 +21,14 @@ using moe::RouteBufs;
 // ---------------------------------------------------------------- shapes
 // Gather CTAs of the ring kernel when moe_config.gather_sms is 0.
 constexpr int kDefaultGatherCtas = 8;
+// Workspace handed to cuBLAS for the router GEMMs.
+constexpr size_t kCublasWorkspace = 32u << 20;
 
 struct Dims {
   int T, d, m, E, k, ms;
   bool mx, bwd, starve;
   bool ring;           // MXFP8 forward dispatch through the persistent ring kernel
+  float aux_alpha;     // load-balancing term weight (0 = none)
   int ring_slots;      // ring capacity in 128-row tiles
   int gather_ctas;     // gather CTAs of the ring kernel
   long R, Rp, Tp;
@@ -43,6 +47,7 @@ int check_config(const moe_config *c, Dims *D) {
   if (c->ring_rows > 0 && c->dtype != MOE_MXFP8) return MOE_ERR_ARG;
   if (c->ring_rows % 128) return MOE_ERR_SHAPE;
   if (c->ring_rows > 0 && c->d > 8192) return MOE_ERR_SHAPE;  // the ring's gather copies whole rows
+  if (!(c->aux_alpha >= 0.0f) || !(c->aux_alpha < 1e30f)) return MOE_ERR_ARG;  // finite, non-negative
   const long R = static_cast<long>(c->T) * c->k;
   const long Rp = (R + 127L * c->E + 127) / 128 * 128;
   if (Rp >= (1L << 31)) return MOE_ERR_SHAPE;
@@ -56,6 +61,7 @@ int check_config(const moe_config *c, Dims *D) {
   D->bwd = (c->flags & MOE_FLAG_BACKWARD) != 0;
   D->starve = (c->flags & MOE_FLAG_DEBUG_STARVE) != 0;
   D->ring = c->ring_rows > 0;
+  D->aux_alpha = c->aux_alpha;
   D->ring_slots = c->ring_rows / 128;
   D->gather_ctas = c->gather_sms > 0 ? c->gather_sms : kDefaultGatherCtas;
   D->R = R;
@@ -115,11 +121,17 @@ void saved_layout(const Dims &D, Layout &L) {
     L.add("s_GU", D.Tp * 2 * D.ms * 2);
     L.add("s_h", D.Tp * D.ms * 2);
   }
+  if (D.aux_alpha > 0.f) L.add("aux_grad", static_cast<size_t>(D.T) * D.E * 4);  // dL/dlogits
 }
 
 void ws_layout(const Dims &D, Layout &L) {
   L.add("status", 16);
   L.add("hist", static_cast<size_t>(D.nchunks) * D.E * 4);
+  if (D.aux_alpha > 0.f) {
+    L.add("aux", (1 + 2 * static_cast<size_t>(D.E)) * 4);  // [L, P[E], f[E]]
+    L.add("aux_part", static_cast<size_t>(moe::balance_blocks(D.T)) * D.E * 4);
+  }
+  L.add("cublas_ws", kCublasWorkspace);  // the router GEMMs
   add_route(D, L);  // used when the forward saves nothing
   const size_t eb = D.mx ? 1 : 2;
   if (D.ring) {  // per-token codes + a fixed ring of 128-row tiles instead of every dispatched row
@@ -144,6 +156,7 @@ void ws_layout(const Dims &D, Layout &L) {
     L.add("s_out", D.Tp * D.d * 2);
   }
   if (!D.bwd) return;
+  L.add("router_g", static_cast<size_t>(D.T) * D.E * 2);  // bf16 dlogits for the router backward
   L.add("g", D.R * 4);
   if (!D.mx) L.add("dO", D.Rp * D.d * 2);  // MXFP8 keeps dO only as codes
   L.add("dGU", D.Rp * 2 * D.m * 2);
@@ -534,6 +547,15 @@ int moe_forward(const moe_config *cfg, const void *x, const float *logits, const
 
   // S1 + S2
   if ((rc = route_impl(D, logits, rb, s)) != MOE_OK) return rc;
+  // load-balancing term (after the schedule: needs the counts)
+  if (D.aux_alpha > 0.f) {
+    Traced tr("balance_loss", s);
+    float *grad = train ? reinterpret_cast<float *>(S.ptr(saved, "aux_grad")) : nullptr;
+    rc = cuda_status(moe::launch_balance(logits, D.T, D.E, D.k, rb.counts, D.aux_alpha,
+                                         reinterpret_cast<float *>(W.ptr(ws, "aux_part")), grad,
+                                         reinterpret_cast<float *>(W.ptr(ws, "aux")), s));
+    if (rc != MOE_OK) return rc;
+  }
   // S3 dispatch gather (+ MX quantisation of x); with a ring it runs inside
   // the gate/up GEMM launch below.
   char *xs = D.ring ? W.ptr(ws, "ring") : W.ptr(ws, "xs");
@@ -987,7 +1009,81 @@ int moe_backward(const moe_config *cfg, const void *dy, const void *x, const moe
   }
   // B6 reverse dispatch + dlogits
   Traced tr("reverse_dispatch", s);
-  return cuda_status(moe::launch_reverse_dispatch(dX, s_dx, g, D.T, D.d, D.k, D.E, rb, dx, dlogits, s));
+  const float *aux_grad = D.aux_alpha > 0.f ? reinterpret_cast<const float *>(S.ptr(saved, "aux_grad")) : nullptr;
+  return cuda_status(
+      moe::launch_reverse_dispatch(dX, s_dx, g, D.T, D.d, D.k, D.E, rb, dx, dlogits, aux_grad, s));
+}
+
+// ---------------------------------------------------------------- router (cuBLAS)
+namespace {
+std::mutex g_blas_mu;
+cublasHandle_t g_blas[64] = {};
+
+// The calling device's cuBLAS handle bound to `s`, with its workspace inside ws.
+int blas_handle(cublasHandle_t *out, void *ws_part, cudaStream_t s) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_blas_mu);
+  if (!g_blas[dev] && cublasCreate(&g_blas[dev]) != CUBLAS_STATUS_SUCCESS) return MOE_ERR_CUDA;
+  cublasHandle_t h = g_blas[dev];
+  if (cublasSetStream(h, s) != CUBLAS_STATUS_SUCCESS ||
+      cublasSetWorkspace(h, ws_part, kCublasWorkspace) != CUBLAS_STATUS_SUCCESS ||
+      cublasSetMathMode(h, CUBLAS_DEFAULT_MATH) != CUBLAS_STATUS_SUCCESS)
+    return MOE_ERR_CUDA;
+  *out = h;
+  return MOE_OK;
+}
+
+int blas_status(cublasStatus_t st) { return st == CUBLAS_STATUS_SUCCESS ? MOE_OK : MOE_ERR_CUDA; }
+}  // namespace
+
+int moe_router_forward(const moe_config *cfg, const void *x, const void *W_r, float *logits, void *ws,
+                       moe_stream_t stream) {
+  Dims D;
+  int rc = check_config(cfg, &D);
+  if (rc != MOE_OK) return rc;
+  if (!x || !W_r || !logits || !ws) return MOE_ERR_ARG;
+  if (!aligned16(x) || !aligned16(W_r) || !aligned16(logits) || !aligned16(ws)) return MOE_ERR_ALIGN;
+  Layout W;
+  ws_layout(D, W);
+  cublasHandle_t h;
+  if ((rc = blas_handle(&h, W.ptr(ws, "cublas_ws"), stream)) != MOE_OK) return rc;
+  Traced tr("router_forward", stream);
+  // row-major logits [T, E] = x [T, d] W_r^T, i.e. column-major [E, T] = W_r^(T) x
+  const float one = 1.f, zero = 0.f;
+  return blas_status(cublasGemmEx(h, CUBLAS_OP_T, CUBLAS_OP_N, D.E, D.T, D.d, &one, W_r, CUDA_R_16BF, D.d, x,
+                                  CUDA_R_16BF, D.d, &zero, logits, CUDA_R_32F, D.E, CUBLAS_COMPUTE_32F,
+                                  CUBLAS_GEMM_DEFAULT));
+}
+
+int moe_router_backward(const moe_config *cfg, const float *dlogits, const void *x, const void *W_r, void *dx,
+                        void *dW_r, void *ws, moe_stream_t stream) {
+  Dims D;
+  int rc = check_config(cfg, &D);
+  if (rc != MOE_OK) return rc;
+  if (!dlogits || !x || !W_r || !dx || !dW_r || !ws) return MOE_ERR_ARG;
+  if (!D.bwd) return MOE_ERR_ARG;
+  if (!aligned16(dlogits) || !aligned16(x) || !aligned16(W_r) || !aligned16(dx) || !aligned16(dW_r) ||
+      !aligned16(ws))
+    return MOE_ERR_ALIGN;
+  Layout W;
+  ws_layout(D, W);
+  cublasHandle_t h;
+  if ((rc = blas_handle(&h, W.ptr(ws, "cublas_ws"), stream)) != MOE_OK) return rc;
+  Traced tr("router_backward", stream);
+  void *gb = W.ptr(ws, "router_g");
+  if ((rc = cuda_status(moe::launch_to_bf16(dlogits, static_cast<long>(D.T) * D.E, gb, stream))) != MOE_OK)
+    return rc;
+  const float one = 1.f, zero = 0.f;
+  // dx [T, d] += g [T, E] W_r [E, d]  (column-major: dx^T [d, T] += W_r^T [d, E] g^T [E, T])
+  rc = blas_status(cublasGemmEx(h, CUBLAS_OP_N, CUBLAS_OP_N, D.d, D.T, D.E, &one, W_r, CUDA_R_16BF, D.d, gb,
+                                CUDA_R_16BF, D.E, &one, dx, CUDA_R_16BF, D.d, CUBLAS_COMPUTE_32F,
+                                CUBLAS_GEMM_DEFAULT));
+  if (rc != MOE_OK) return rc;
+  // dW_r [E, d] = g^T [E, T] x [T, d]  (column-major: dW_r^T [d, E] = x^T [d, T] g [T, E])
+  return blas_status(cublasGemmEx(h, CUBLAS_OP_N, CUBLAS_OP_T, D.d, D.E, D.T, &one, x, CUDA_R_16BF, D.d, gb,
+                                  CUDA_R_16BF, D.E, &zero, dW_r, CUDA_R_16BF, D.d, CUBLAS_COMPUTE_32F,
+                                  CUBLAS_GEMM_DEFAULT));
 }
 
 int moe_get_status(void *ws, moe_stream_t stream) {

@@ -373,10 +373,113 @@ __global__ void __launch_bounds__(256) reverse_combine_mx_kernel(
   if ((threadIdx.x & 7) == 0 && tok >= 0) g[slot] = dot;
 }
 
+// ------------------------------------------------------------ load-balancing term
+// Warp per token: the softmax over all E experts, p = exp(l - max) / sum, with
+// the max and the sum reduced by a fixed xor tree.  Each warp adds its tokens'
+// p in token order; the block's 8 warp sums are added in warp order into the
+// block's partial P, so P is bitwise reproducible.  With the schedule's counts
+// the token's gradient row alpha E / T * p (f - sum_e f_e p_e) is written too.
+template <int VPL>
+__global__ void __launch_bounds__(256) balance_kernel(const float *__restrict__ logits, int T, int E, int k,
+                                                      const int *__restrict__ counts, float alpha, int tpb,
+                                                      float *__restrict__ part, float *__restrict__ grad) {
+  extern __shared__ float wsum[];  // [8][E]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const float inv_slots = 1.0f / (static_cast<float>(T) * static_cast<float>(k));
+  const float c = alpha * static_cast<float>(E) / static_cast<float>(T);
+  float acc[VPL], f[VPL];
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    const int e = lane + 32 * i;
+    acc[i] = 0.f;
+    f[i] = e < E ? static_cast<float>(__ldg(counts + e)) * inv_slots : 0.f;
+  }
+  const int t0 = blockIdx.x * tpb;
+  for (int tt = warp; tt < tpb; tt += 8) {
+    const int t = t0 + tt;
+    if (t >= T) break;
+    const float *row = logits + static_cast<size_t>(t) * E;
+    float v[VPL];
+    float mx = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+      const int e = lane + 32 * i;
+      v[i] = e < E ? __ldg(row + e) : -INFINITY;
+      mx = fmaxf(mx, v[i]);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    float sum = 0.f;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+      v[i] = (lane + 32 * i) < E ? expf(v[i] - mx) : 0.f;
+      sum += v[i];
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    float fs = 0.f;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+      v[i] = v[i] / sum;  // p
+      acc[i] += v[i];
+      fs = fmaf(f[i], v[i], fs);
+    }
+    if (grad) {
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) fs += __shfl_xor_sync(0xffffffffu, fs, off);
+      float *grow = grad + static_cast<size_t>(t) * E;
+#pragma unroll
+      for (int i = 0; i < VPL; ++i) {
+        const int e = lane + 32 * i;
+        if (e < E) grow[e] = c * v[i] * (f[i] - fs);
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    const int e = lane + 32 * i;
+    if (e < E) wsum[warp * E + e] = acc[i];
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    float sp = 0.f;
+    for (int w = 0; w < 8; ++w) sp += wsum[w * E + e];
+    part[static_cast<size_t>(blockIdx.x) * E + e] = sp;
+  }
+}
+
+// P_e = (1/T) sum over blocks (block order) of the partials; f_e = counts_e / (T k);
+// out = [loss, P[0..E), f[0..E)] with loss = alpha E sum_e f_e P_e (expert order).
+__global__ void __launch_bounds__(1024) balance_finish_kernel(const float *__restrict__ part, int nblk, int T,
+                                                              int E, int k, const int *__restrict__ counts,
+                                                              float alpha, float *__restrict__ out) {
+  const float inv_slots = 1.0f / (static_cast<float>(T) * static_cast<float>(k));
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    float s = 0.f;
+    for (int b = 0; b < nblk; ++b) s += __ldg(part + static_cast<size_t>(b) * E + e);
+    out[1 + e] = s / static_cast<float>(T);
+    out[1 + E + e] = static_cast<float>(__ldg(counts + e)) * inv_slots;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float acc = 0.f;
+    for (int e = 0; e < E; ++e) acc = fmaf(out[1 + E + e], out[1 + e], acc);
+    out[0] = alpha * static_cast<float>(E) * acc;
+  }
+}
+
+// bf16 copy of fp32 values (the router backward's dlogits operand).
+__global__ void __launch_bounds__(256) to_bf16_kernel(const float *__restrict__ src, long n,
+                                                      uint16_t *__restrict__ dst) {
+  const long i = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i < n) dst[i] = static_cast<uint16_t>(pack_bf16x2(src[i], 0.f) & 0xFFFFu);  // low half = src[i]
+}
+
 // ------------------------------------------------------------ B6: reverse dispatch
 __global__ void __launch_bounds__(256) reverse_dispatch_kernel(
     const uint4 *__restrict__ dX, const uint4 *__restrict__ dxs, const float *__restrict__ g, int T,
-    int d, int k, int E, RouteBufs b, uint4 *__restrict__ dx, float *__restrict__ dlogits) {
+    int d, int k, int E, RouteBufs b, uint4 *__restrict__ dx, float *__restrict__ dlogits,
+    const float *__restrict__ aux_grad) {
   const int t = static_cast<int>((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
@@ -394,10 +497,12 @@ __global__ void __launch_bounds__(256) reverse_dispatch_kernel(
   for (int j = 0; j < k; ++j)
     S = fmaf(__shfl_sync(0xffffffffu, my_w, j), __shfl_sync(0xffffffffu, my_g, j), S);
   const float dl = my_w * (my_g - S);
+  // plus, with a load-balancing term, its gradient row (dense over E)
   float *drow = dlogits + static_cast<size_t>(t) * E;
-  for (int e = lane; e < E; e += 32) drow[e] = 0.f;
+  const float *arow = aux_grad ? aux_grad + static_cast<size_t>(t) * E : nullptr;
+  for (int e = lane; e < E; e += 32) drow[e] = arow ? __ldg(arow + e) : 0.f;
   __syncwarp();
-  if (lane < k) drow[my_e] = dl;
+  if (lane < k) drow[my_e] = arow ? dl + __ldg(arow + my_e) : dl;
   const int vec = d >> 3;
   for (int i = lane; i < vec; i += 32) {
     float acc[8];
@@ -587,10 +692,10 @@ cudaError_t launch_reverse_combine_mx(const void *dy, const void *o, int d, int 
 
 cudaError_t launch_reverse_dispatch(const void *dX, const void *dxs, const float *g, int T,
                                     int d, int k, int E, const RouteBufs &b, void *dx,
-                                    float *dlogits, cudaStream_t s) {
+                                    float *dlogits, const float *aux_grad, cudaStream_t s) {
   reverse_dispatch_kernel<<<blocks_for(T, 8), 256, 0, s>>>(
       static_cast<const uint4 *>(dX), static_cast<const uint4 *>(dxs), g, T, d, k, E, b,
-      static_cast<uint4 *>(dx), dlogits);
+      static_cast<uint4 *>(dx), dlogits, aux_grad);
   return cudaGetLastError();
 }
 
@@ -632,6 +737,31 @@ cudaError_t launch_quantize_mx(const void *src, int batch, int rows, int cols, b
         static_cast<const uint16_t *>(src), static_cast<long>(rows) * cols, cols, rows, nullptr, rows,
         1, 1, RouteBufs{}, codes, static_cast<long>(rows) * cols, scales, cols, rows);
   }
+  return cudaGetLastError();
+}
+
+int balance_blocks(int T) { return static_cast<int>((T + kBalanceTokensPerBlock - 1) / kBalanceTokensPerBlock); }
+
+cudaError_t launch_balance(const float *logits, int T, int E, int k, const int *counts, float alpha, float *part,
+                           float *grad, float *out, cudaStream_t s) {
+  const int nblk = balance_blocks(T);
+  const int vpl = (E + 31) / 32;
+  const size_t smem = 8 * static_cast<size_t>(E) * sizeof(float);
+#define MOE_BAL(V) \
+  balance_kernel<V><<<nblk, 256, smem, s>>>(logits, T, E, k, counts, alpha, kBalanceTokensPerBlock, part, grad)
+  if (vpl <= 1) MOE_BAL(1);
+  else if (vpl <= 2) MOE_BAL(2);
+  else if (vpl <= 4) MOE_BAL(4);
+  else if (vpl <= 8) MOE_BAL(8);
+  else if (vpl <= 16) MOE_BAL(16);
+  else MOE_BAL(32);
+#undef MOE_BAL
+  balance_finish_kernel<<<1, 1024, 0, s>>>(part, nblk, T, E, k, counts, alpha, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_to_bf16(const float *src, long n, void *dst, cudaStream_t s) {
+  to_bf16_kernel<<<blocks_for(n, 256), 256, 0, s>>>(src, n, static_cast<uint16_t *>(dst));
   return cudaGetLastError();
 }
 

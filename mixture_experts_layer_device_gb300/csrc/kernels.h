@@ -56,10 +56,11 @@ cudaError_t launch_reverse_combine_mx(const void *dy, const void *o, int d, int 
                                       const RouteBufs &b, int64_t rp_max, float *g, uint8_t *dOq,
                                       uint8_t *dOq_sf, uint8_t *dOT, uint8_t *dOT_sf, cudaStream_t s);
 
-// Reverse dispatch: dx[t] = bf16( sum_j dX[row(t,j)] + dxs[t] ); dlogits row.
+// Reverse dispatch: dx[t] = bf16( sum_j dX[row(t,j)] + dxs[t] ); dlogits row
+// (+ aux_grad row when given: the load-balancing term's gradient).
 cudaError_t launch_reverse_dispatch(const void *dX, const void *dxs, const float *g, int T,
                                     int d, int k, int E, const RouteBufs &b, void *dx,
-                                    float *dlogits, cudaStream_t s);
+                                    float *dlogits, const float *aux_grad, cudaStream_t s);
 
 // Transpose of a row block: src [*, C] (row stride C) -> dst [C, ld_dst],
 // dst[c][r] = src[row(r)][c] for r < nrows (device count *nrows_dev when not
@@ -88,6 +89,17 @@ enum GemmEpi { EPI_STORE = 0, EPI_SWIGLU = 1, EPI_SWIGLU_BWD = 2 };
 // launch_quantize_mx(transpose = true).
 cudaError_t launch_quantize_mx_both(const void *src, int batch, int rows, int cols, uint8_t *codes,
                                     uint8_t *scales, uint8_t *codes_t, uint8_t *scales_t, cudaStream_t s);
+
+// Load-balancing term (Switch-style, over the routed slots): per-block partial
+// sums of the full softmax (part [balance_blocks(T), E]), the gradient rows
+// [T, E] (grad, may be NULL) and out = [loss, P[E], f[E]], all fp32 and
+// bitwise reproducible.
+constexpr int kBalanceTokensPerBlock = 64;
+int balance_blocks(int T);
+cudaError_t launch_balance(const float *logits, int T, int E, int k, const int *counts, float alpha, float *part,
+                           float *grad, float *out, cudaStream_t s);
+// dst[i] = bf16(src[i]) (round to nearest even), n values.
+cudaError_t launch_to_bf16(const float *src, long n, void *dst, cudaStream_t s);
 
 // Row-blocked MXFP8 codes of every token: x [T, d] bf16 -> codes [T, d] and
 // canonical scales [T, d/32] (the ring dispatch gathers these rows).
