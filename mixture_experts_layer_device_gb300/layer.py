@@ -8,7 +8,8 @@ import torch
 
 from . import (MOE_BF16, MOE_FLAG_BACKWARD, MOE_MXFP8, check, config, moe_backward, moe_buffer_info,
                moe_forward, moe_get_status, moe_padded_rows, moe_quantize_mx, moe_quantize_mx_both,
-               moe_saved_bytes, moe_transpose_bf16, moe_workspace_bytes, weights)
+               moe_router_backward, moe_router_forward, moe_saved_bytes, moe_transpose_bf16,
+               moe_workspace_bytes, weights)
 
 _DT = {"i32": torch.int32, "f32": torch.float32, "bf16": torch.bfloat16, "u8": torch.uint8}
 
@@ -33,7 +34,7 @@ class MoELayer:
     """
 
     def __init__(self, T, d, m, E, k, fmt, expert=None, shared=None, backward=False, device="cuda",
-                 stacked=None, ring_rows=0, gather_sms=0):
+                 stacked=None, ring_rows=0, gather_sms=0, aux_alpha=0.0):
         self.T, self.d, self.m, self.E, self.k = T, d, m, E, k
         self.fmt = fmt
         self.mx = fmt == "mxfp8"
@@ -41,7 +42,7 @@ class MoELayer:
         self.backward_enabled = backward
         self.device = device
         self.cfg = config(T, d, m, E, k, self.ms, MOE_MXFP8 if self.mx else MOE_BF16,
-                          MOE_FLAG_BACKWARD if backward else 0, ring_rows, gather_sms)
+                          MOE_FLAG_BACKWARD if backward else 0, ring_rows, gather_sms, aux_alpha)
         self.Rp = moe_padded_rows(self.cfg)
         self.ws = _u8(moe_workspace_bytes(self.cfg), device)
         self.saved = _u8(moe_saved_bytes(self.cfg), device) if backward else None
@@ -146,6 +147,17 @@ class MoELayer:
                 check(moe_transpose_bf16(t["s_gu"], 1, 2 * self.ms, d, t["s_gu_t"], stream))
                 check(moe_transpose_bf16(t["s_dn"], 1, d, self.ms, t["s_dn_t"], stream))
         self.W = weights(**t)
+
+    def router_logits(self, x, W_r, logits=None, stream=None):
+        """logits [T, E] fp32 = x W_r^T (the router projection)."""
+        if logits is None:
+            logits = torch.empty((self.T, self.E), dtype=torch.float32, device=self.device)
+        check(moe_router_forward(self.cfg, x, W_r, logits, self.ws, stream))
+        return logits
+
+    def router_backward(self, dlogits, x, W_r, dx, dW_r, stream=None):
+        """dx += bf16(dlogits) W_r in place (one rounding); dW_r = bf16(dlogits)^T x."""
+        check(moe_router_backward(self.cfg, dlogits, x, W_r, dx, dW_r, self.ws, stream))
 
     def new_saved(self):
         """A fresh buffer for the activations one training forward keeps."""

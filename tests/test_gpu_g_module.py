@@ -86,3 +86,39 @@ def test_module_sees_optimizer_steps_and_two_forwards():
                      stacked=(moe.W_gu.detach(), moe.W_dn.detach()))
     assert torch.equal(y3, fresh.forward(x, logits, train=True))
     assert not torch.equal(y3, y1)
+
+
+def test_module_with_router_and_balance_term_matches_direct_calls():
+    """router=True, aux_alpha > 0: the fused function's outputs and gradients
+    equal the chain router_forward -> forward -> backward -> router_backward,
+    and the load-balancing loss is exposed."""
+    from mixture_experts_layer_device_gb300.layer import MoELayer
+    from mixture_experts_layer_device_gb300.module import MoE
+    cfg = dict(mi.SMALL["kimi-k2.7"])
+    T, d, m, E, k, ms = (cfg[n] for n in ("T", "d", "m", "E", "k", "m_shared"))
+    dev, alpha = "cuda", 0.01
+    torch.manual_seed(9)
+    moe = MoE(T, d, m, E, k, cfg["fmt"], m_shared=ms, device=dev, router=True, aux_alpha=alpha)
+    x, dy = mi.tokens(cfg).to(dev), mi.out_grad(cfg).to(dev)
+    xr = x.clone().requires_grad_(True)
+    y = moe(xr)
+    aux = float(moe.aux_loss())
+    (y.float() * dy.float()).sum().backward()
+
+    shared = (moe.Ws_gu.detach(), moe.Ws_dn.detach())
+    ref = MoELayer(T, d, m, E, k, cfg["fmt"], shared=shared, backward=True, device=dev,
+                   stacked=(moe.W_gu.detach(), moe.W_dn.detach()), aux_alpha=alpha)
+    W_r = moe.W_r.detach()
+    logits = ref.router_logits(x, W_r)
+    y_ref = ref.forward(x, logits, train=True)
+    aux_ref = float(ref.view(1, "aux", "f32", (1,))[0])
+    g = ref.backward(dy, x)
+    dW_r = torch.empty_like(W_r)
+    ref.router_backward(g["dlogits"], x, W_r, g["dx"], dW_r)
+    assert torch.equal(y, y_ref)
+    assert aux == aux_ref and aux > 0
+    assert torch.equal(xr.grad, g["dx"])
+    assert torch.equal(moe.W_r.grad, dW_r)
+    assert torch.equal(moe.W_gu.grad, g["dW_gu"])
+    assert torch.equal(moe.W_dn.grad, g["dW_dn"])
+    assert torch.equal(moe.Ws_gu.grad, g["dWs_gu"])
