@@ -125,6 +125,32 @@ def kernel_work(cfg, name, train=False):
     return tbl.get(name)
 
 
+def output_bytes(cfg, name):
+    """Bytes a kernel name writes per step when its output write dominates (the
+    expert weight gradients write bf16 dW for every expert)."""
+    d, m, E = cfg["d"], cfg["m"], cfg["E"]
+    return {"wgrad_gate_up": E * 2 * m * d * 2, "wgrad_down": E * d * m * 2}.get(name)
+
+
+def write_probe_gbs(dev):
+    """Write-only HBM bandwidth of this GPU: a device memset of 8 GB (taken
+    before the timed region; context for write-dominated kernels)."""
+    import torch
+    buf = torch.empty(8 << 30, dtype=torch.uint8, device=dev)
+    buf.zero_()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(3):
+        buf.zero_()
+    b.record()
+    b.synchronize()
+    gbs = 3 * buf.numel() / (a.elapsed_time(b) / 1e3) / 1e9
+    del buf
+    torch.cuda.empty_cache()
+    return gbs
+
+
 def kernel_roofline(cfg, name, train, ms_per_step, peaks):
     """Bound, achieved and peak of one kernel: the larger of its tensor time
     (FLOPs at the tensor peak of its arithmetic) and its HBM time (algorithmic
@@ -373,6 +399,7 @@ def run_ours(args, cfg, passes, rank, world, local_rank):
             ms = float(t.item())
         return ms, recs
 
+    write_gbs = write_probe_gbs(dev)
     clocks = Clocks(gpu_index(local_rank))
     total_ms, recs = timed(step, args.steps, trace=True)
     clk = clocks.stop()
@@ -402,29 +429,72 @@ def run_ours(args, cfg, passes, rank, world, local_rank):
         with_s0 = {"ms_per_step": round(s0_total / args.steps, 4),
                    "tokens_per_s": round(tokens * args.steps / (s0_total / 1e3), 1)}
 
-    # e2e: the public API with host buffers, copies inside the timed region
+    # e2e: the public API with host buffers, copies inside the timed region.
+    # Two sets of device buffers: while step i computes on `stream`, a copy
+    # stream uploads step i+1's inputs and downloads step i-1's results (as a
+    # training loop prefetching its next batch would); every step still moves
+    # all of its own bytes inside the timed region.
     xh = x.cpu().pin_memory()
     lh = logits.cpu().pin_memory()
     dyh = dy.cpu().pin_memory() if bwd else None
     yh = torch.empty(y.shape, dtype=y.dtype).pin_memory()
     dxh = torch.empty(y.shape, dtype=y.dtype).pin_memory() if bwd else None
     dlh = torch.empty((cfg["T"], cfg["E"]), dtype=torch.float32).pin_memory() if bwd else None
-    xd, ld = torch.empty_like(x), torch.empty_like(logits)
-    dyd = torch.empty_like(dy) if bwd else None
+    cstream = torch.cuda.Stream(device=dev)
+    sets = []
+    for _ in range(2):
+        sets.append(dict(x=torch.empty_like(x), l=torch.empty_like(logits),
+                         dy=torch.empty_like(dy) if bwd else None, y=torch.empty_like(y),
+                         g=layer.alloc_grads() if bwd else None,
+                         up=torch.cuda.Event(), done=torch.cuda.Event(), down=torch.cuda.Event()))
+    e2e_state = {"i": 0}
+
+    def upload(bs):
+        with torch.cuda.stream(cstream):
+            cstream.wait_event(bs["down"])          # the set's previous results have left
+            bs["x"].copy_(xh, non_blocking=True)
+            bs["l"].copy_(lh, non_blocking=True)
+            if bwd:
+                bs["dy"].copy_(dyh, non_blocking=True)
+            bs["up"].record(cstream)
+
+    def download(bs):
+        with torch.cuda.stream(cstream):
+            cstream.wait_event(bs["done"])
+            yh.copy_(bs["y"], non_blocking=True)
+            if bwd:
+                dxh.copy_(bs["g"]["dx"], non_blocking=True)
+                dlh.copy_(bs["g"]["dlogits"], non_blocking=True)
+            bs["down"].record(cstream)
 
     def e2e_step():
-        xd.copy_(xh, non_blocking=True)
-        ld.copy_(lh, non_blocking=True)
+        i = e2e_state["i"]
+        cur, nxt = sets[i % 2], sets[(i + 1) % 2]
+        if i == 0:
+            upload(cur)
+        stream.wait_event(cur["up"])
+        layer.forward(cur["x"], cur["l"], y=cur["y"], train=bwd, stream=stream)
         if bwd:
-            dyd.copy_(dyh, non_blocking=True)
-        layer.forward(xd, ld, y=y, train=bwd, stream=stream)
-        yh.copy_(y, non_blocking=True)
-        if bwd:
-            layer.backward(dyd, xd, grads=grads, stream=stream)
-            dxh.copy_(grads["dx"], non_blocking=True)
-            dlh.copy_(grads["dlogits"], non_blocking=True)
+            layer.backward(cur["dy"], cur["x"], grads=cur["g"], stream=stream)
+        cur["done"].record(stream)
+        upload(nxt)                                 # overlaps this step's compute
+        download(cur)
+        e2e_state["i"] = i + 1
 
-    e2e_ms, _ = timed(e2e_step, args.steps)
+    def e2e_drain():
+        stream.wait_stream(cstream)                 # the last results are on the host
+
+    for _ in range(2):                              # warm the pipeline (not timed)
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_state["i"] = 0
+
+    def e2e_run():
+        e2e_step()
+        if e2e_state["i"] == args.steps:
+            e2e_drain()
+
+    e2e_ms, _ = timed(e2e_run, args.steps)
     h2d = x.numel() * 2 + logits.numel() * 4 + (dy.numel() * 2 if bwd else 0)
     d2h = y.numel() * 2 + ((y.numel() * 2 + cfg["T"] * cfg["E"] * 4) if bwd else 0)
     st = layer.status()
@@ -487,7 +557,13 @@ def run_ours(args, cfg, passes, rank, world, local_rank):
                            "t_hbm_ms": round(t_hbm * 1e3, 3), "peaks": peaks_src},
         "roofline": {"kernel": dom, "bound": bound, "achieved": round(achieved, 1), "peak": round(peak, 1),
                      "unit": unit, "frac": round(achieved / peak, 4), "traffic": traffic, "peak_source": peak_note,
-                     "launch_ms": round(avg_ms, 4)},
+                     "launch_ms": round(avg_ms, 4),
+                     "write_probe": None if output_bytes(cfg, dom) is None else {
+                         "note": "output-write-dominated kernel: its bf16 dW write rate against this GPU's "
+                                 "write-only bandwidth (device memset, measured before the timed region)",
+                         "written_gbs": round(output_bytes(cfg, dom) / (tot / args.steps / 1e3) / 1e9, 1),
+                         "memset_gbs": round(write_gbs, 1),
+                         "frac": round(output_bytes(cfg, dom) / (tot / args.steps / 1e3) / 1e9 / write_gbs, 4)}},
         "kernels": kernels,
         "route_schedule_share": round(rs, 4),
         "s0_ms": round(s0_ms, 3),
