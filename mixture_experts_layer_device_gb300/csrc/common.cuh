@@ -30,17 +30,7 @@ MOE_DEV unsigned long long globaltimer() {
   return t;
 }
 
-MOE_DEV uint32_t lane_id() { return threadIdx.x & 31u; }
 
-MOE_DEV uint32_t elect_one_sync() {
-  uint32_t pred = 0;
-  asm volatile(
-      "{\n .reg .b32 rx;\n .reg .pred px;\n"
-      " elect.sync rx|px, %1;\n selp.b32 %0, 1, 0, px;\n}\n"
-      : "=r"(pred)
-      : "r"(0xffffffffu));
-  return pred;
-}
 
 // ---------------------------------------------------------------- mbarrier
 MOE_DEV void mbar_init(uint64_t *bar, uint32_t count) {
@@ -157,13 +147,6 @@ MOE_DEV void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar
       "l"(src), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
 }
-// TMA store of a shared-memory box to global memory (bulk-group completion).
-MOE_DEV void tma_store_2d(const CUtensorMap *map, const void *src, int c0, int c1) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(map),
-      "r"(smem_u32(src)), "r"(c0), "r"(c1)
-      : "memory");
-}
 // 1-D bulk copy shared -> global (both addresses and the size multiples of 16 B),
 // tracked by this thread's bulk groups.
 MOE_DEV void bulk_store(void *dst, const void *src, uint32_t bytes) {
@@ -267,16 +250,6 @@ MOE_DEV void tmem_ld32_async(uint32_t taddr, uint32_t *r) {
         "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr));
 }
-// 16-column variant of tmem_ld32_async.
-MOE_DEV void tmem_ld16_async(uint32_t taddr, uint32_t *r) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-}
 // Ties registers written by an asynchronous load to a point after its wait, so
 // the compiler cannot move their uses above the wait.
 template <int N>
@@ -285,22 +258,6 @@ MOE_DEV void reg_fence(uint32_t *r) {
   for (int i = 0; i < N; ++i) asm volatile("" : "+r"(r[i])::"memory");
 }
 
-// Load 32 consecutive fp32 columns of this warp's 32 TMEM lanes.
-MOE_DEV void tmem_ld32(uint32_t taddr, float *v) {
-  uint32_t r[32];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
-        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
-        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
 MOE_DEV void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // Shared-memory matrix descriptor for a K-major operand tile stored with the

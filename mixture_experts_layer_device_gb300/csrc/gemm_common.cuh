@@ -98,7 +98,7 @@ MOE_DEV void put_mx64(Stager &st, const OutView &vq, uint8_t *sf, long ldq, cons
 
 
 // Drains one tile's accumulator (this warp's 32 TMEM lanes at `tb`) and writes
-// the epilogue's outputs with TMA stores.  `release()` is called once the last
+// the epilogue's outputs through the stager.  `release()` is called once the last
 // accumulator column has been read (the MMA may then reuse it).  With
 // store == false the accumulator is drained and released but nothing is
 // written (the idle half of a 2-CTA tile).
@@ -122,7 +122,7 @@ MOE_DEV void epilogue_tile(const GemmArgs &g, const OutView &vO, const OutView &
     // The whole row is drained into registers as packed bf16 pairs (TMEM loads
     // of 32 columns ping-pong with the conversion), TMEM is released, and only
     // then are the pieces staged and stored: the accumulator is never held
-    // while TMA stores queue behind the producer's loads.
+    // while the stores drain.
     constexpr int NC32 = BN / 32;
     uint32_t pk[BN / 2];
     uint32_t buf[2][32];
