@@ -103,13 +103,31 @@ class ExpertSubset:
         return self.t[e]
 
 
+def _compact(op):
+    """A prepared operand (dequantised MXFP8 or bf16 values) held in fp32, which
+    represents it exactly (checked); the oracle still computes in fp64."""
+    o32 = np.asarray(op, dtype=np.float32)
+    assert np.array_equal(o32.astype(np.float64), op), "prepared operand not exact in fp32"
+    return o32
+
+
 def prepare_subset(cfg, gu_all, dn_all, experts, backward):
-    """Oracle S0 for a few experts of device-resident bf16 masters (spawned worker pool)."""
+    """Oracle S0 for some experts of device-resident bf16 masters (spawned
+    worker pool).  With prepared operands the oracle reads the masters only for
+    their shapes, so zero-stride stand-ins of the right shape replace them and
+    the operands are kept in fp32: many experts fit in host memory."""
     import multiprocessing as mp
     import os
-    masters = {int(e): (gu_all[e].float().cpu().numpy(), dn_all[e].float().cpu().numpy()) for e in experts}
-    jobs = [(e, g, d, cfg["fmt"], backward) for e, (g, d) in masters.items()]
-    with mp.get_context("spawn").Pool(max(1, min(len(jobs), os.cpu_count() or 1))) as pool:
-        ops = dict(pool.map(_prep_worker, jobs))
-    table = {e: (masters[e][0].astype(np.float64), masters[e][1].astype(np.float64), ops[e]) for e in masters}
+    experts = [int(e) for e in experts]
+    table = {}
+    nproc = max(1, min(len(experts), os.cpu_count() or 1))
+    with mp.get_context("spawn").Pool(nproc) as pool:
+        for i in range(0, len(experts), nproc):          # bounded batches of masters in flight
+            batch = experts[i:i + nproc]
+            jobs = [(e, gu_all[e].float().cpu().numpy(), dn_all[e].float().cpu().numpy(), cfg["fmt"], backward)
+                    for e in batch]
+            for e, ops in pool.map(_prep_worker, jobs):
+                shape_gu, shape_dn = tuple(gu_all[e].shape), tuple(dn_all[e].shape)
+                table[e] = (np.broadcast_to(np.float64(0.0), shape_gu), np.broadcast_to(np.float64(0.0), shape_dn),
+                            {k: _compact(v) for k, v in ops.items()})
     return ExpertSubset(cfg["E"], table)

@@ -1,8 +1,9 @@
 """Parity at the full workload sizes, in the launch configuration bench.py
 times (stacked weight preparation, one moe_forward / moe_backward over all T
 tokens), on outputs the oracle can compute one by one: whole output rows of
-seeded tokens (all their experts and the shared expert), and the weight
-gradients of a seeded lightly loaded expert."""
+8 seeded tokens per workload (all their experts and the shared expert), dx and
+dlogits rows of 4 seeded tokens, and the weight gradients of 4 seeded lightly
+loaded experts."""
 import numpy as np
 import pytest
 import torch
@@ -30,8 +31,8 @@ def build(name, backward):
     return cfg, x, logits, gu_all, dn_all, shared, layer
 
 
-@pytest.mark.parametrize("name,n_tok", [("qwen3.5-397b", 2), ("glm-5.2", 2), ("kimi-k2.7", 1),
-                                        ("deepseek-v4-pro", 2)])
+@pytest.mark.parametrize("name,n_tok", [("qwen3.5-397b", 8), ("glm-5.2", 8), ("kimi-k2.7", 8),
+                                        ("deepseek-v4-pro", 8)])
 def test_full_size_forward_sampled_tokens(name, n_tok):
     cfg, x, logits, gu_all, dn_all, shared, layer = build(name, backward=False)
     y = layer.forward(x, logits)
@@ -49,40 +50,46 @@ def test_full_size_forward_sampled_tokens(name, n_tok):
 
 
 def test_full_size_backward_sampled():
-    """Kimi-K2.7 shape, MXFP8 + BF16 shared expert: dx and dlogits rows of a
-    seeded token, and dW of a seeded lightly loaded expert (all its rows)."""
+    """Kimi-K2.7 shape, MXFP8 + BF16 shared expert: dx and dlogits rows of
+    seeded tokens, and dW of four seeded experts of at most 256 rows each (all
+    their rows)."""
     cfg, x, logits, gu_all, dn_all, shared, layer = build("kimi-k2.7", backward=True)
     dy = mi.out_grad(cfg, x.device)
     layer.forward(x, logits, train=True)
     g = layer.backward(dy, x)
     assert layer.status() == 0
     k, fmt, tol = cfg["k"], cfg["fmt"], TOL[cfg["fmt"]]
-    # one token: forward + backward of the oracle on that token alone
-    tok = mi.sample_tokens(cfg, 1)
+    # seeded tokens: forward + backward of the oracle on those tokens alone
+    tok = mi.sample_tokens(cfg, 4)
     lg = logits[tok].cpu().numpy()
     idx, _ = om.route(lg, k)
     counts = layer.view(0, "counts", "i32", (cfg["E"],)).cpu().numpy()
-    e_dw = int(mi.sample_experts(counts, cfg["seed"], n=1, max_rows=256)[0])
-    experts = prepare_subset(cfg, gu_all, dn_all, sorted(set(idx.reshape(-1).tolist()) | {e_dw}), backward=True)
+    e_dws = [int(e) for e in mi.sample_experts(counts, cfg["seed"], n=4, max_rows=256)]
+    assert len(e_dws) == 4
+    experts = prepare_subset(cfg, gu_all, dn_all, sorted(set(idx.reshape(-1).tolist()) | set(e_dws)),
+                             backward=True)
     sh = None if shared is None else tuple(mi.to_f64(w) for w in shared)
     xs, dys = mi.to_f64(x[tok]), mi.to_f64(dy[tok])
     _, saved = om.forward(xs, lg, experts, k, fmt, shared=sh)
     ref = om.backward(dys, xs, experts, k, fmt, saved, shared=sh, dw_experts=[])
-    assert rel(mi.to_f64(g["dx"][tok]), ref["dx"]) < tol
-    assert rel(g["dlogits"][tok].cpu().numpy().astype(np.float64), ref["dlogits"]) < tol
-    # dW of expert e_dw: every row routed to it, in the schedule's (slot) order
+    for i in range(len(tok)):
+        assert rel(mi.to_f64(g["dx"][tok[i]]), ref["dx"][i]) < tol, "dx of token %d" % tok[i]
+        assert rel(g["dlogits"][tok[i]].cpu().numpy().astype(np.float64), ref["dlogits"][i]) < tol
+    # dW of each sampled expert: every row routed to it, in the schedule's (slot) order
     idx_all = layer.view(0, "idx", "i32", (cfg["T"], k)).cpu().numpy()
     w_all = layer.view(0, "w", "f32", (cfg["T"], k)).cpu().numpy().astype(np.float64)
-    slots = np.nonzero(idx_all.reshape(-1) == e_dw)[0]
-    assert slots.size == counts[e_dw] > 0
-    toks = slots // k
-    W_gu, W_dn, ops = experts[e_dw]
-    X = mi.to_f64(x[torch.as_tensor(toks, device=x.device)])
-    fw = om.expert_forward(X, W_gu, W_dn, fmt, ops)
-    dO = om._rnd(fmt)(w_all.reshape(-1)[slots][:, None] * mi.to_f64(dy[torch.as_tensor(toks, device=x.device)]))
-    bw = om.expert_backward(dO, X, fw["GU_saved"], fw["h_saved"], W_gu, W_dn, fmt, ops)
-    assert rel(mi.to_f64(g["dW_gu"][e_dw]), bw["dW_gu"]) < tol
-    assert rel(mi.to_f64(g["dW_dn"][e_dw]), bw["dW_dn"]) < tol
+    for e_dw in e_dws:
+        slots = np.nonzero(idx_all.reshape(-1) == e_dw)[0]
+        assert slots.size == counts[e_dw] > 0
+        toks = slots // k
+        W_gu, W_dn, ops = experts[e_dw]
+        X = mi.to_f64(x[torch.as_tensor(toks, device=x.device)])
+        fw = om.expert_forward(X, W_gu, W_dn, fmt, ops)
+        dO = om._rnd(fmt)(w_all.reshape(-1)[slots][:, None] *
+                          mi.to_f64(dy[torch.as_tensor(toks, device=x.device)]))
+        bw = om.expert_backward(dO, X, fw["GU_saved"], fw["h_saved"], W_gu, W_dn, fmt, ops)
+        assert rel(mi.to_f64(g["dW_gu"][e_dw]), bw["dW_gu"]) < tol, "dW_gu of expert %d" % e_dw
+        assert rel(mi.to_f64(g["dW_dn"][e_dw]), bw["dW_dn"]) < tol, "dW_dn of expert %d" % e_dw
 
 
 def test_full_size_ring_bitwise_equal():
