@@ -565,7 +565,7 @@ cudaError_t launch_one_mc(const CUtensorMap &ta, const CUtensorMap &tb, const Ge
 }
 
 template <bool MX, int BN, int EPI>
-int max_clusters_mc() {
+int max_clusters_mc_query() {
   using C = Cfg<MX, BN>;
   if (cudaFuncSetAttribute(gemm_kernel<MX, BN, EPI, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(C::SMEM)) != cudaSuccess)
@@ -586,7 +586,13 @@ int max_clusters_mc() {
   return n;
 }
 
-int ring_ctas_resident() {
+template <bool MX, int BN, int EPI>
+int max_clusters_mc() {
+  static int memo[64] = {};
+  return per_device_memo(memo, max_clusters_mc_query<MX, BN, EPI>);
+}
+
+int ring_ctas_query() {
   using C = Cfg<true, 256>;
   if (cudaFuncSetAttribute(gemm_kernel<true, 256, EPI_SWIGLU, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(C::SMEM)) != cudaSuccess)
@@ -599,6 +605,11 @@ int ring_ctas_resident() {
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return 0;
   return per_sm * sms;
+}
+
+int ring_ctas_resident() {
+  static int memo[64] = {};
+  return per_device_memo(memo, ring_ctas_query);
 }
 
 }  // namespace

@@ -5,6 +5,18 @@
 #include "kernels.h"
 
 namespace moe {
+
+// Per-device memo of a launch-configuration query (the answer depends only on
+// the kernel and the device): the query runs once per device, outside any
+// stream capture that follows.  0 means "not known yet" (answers are >= 1).
+template <typename F>
+inline int per_device_memo(int (&slot)[64], F query) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return query();
+  if (slot[dev] <= 0) slot[dev] = query();
+  return slot[dev];
+}
+
 namespace gemm_detail {
 
 MOE_DEV void load_bf16x32(const void *base, long row, long ld, long col, float *v) {

@@ -398,7 +398,7 @@ cudaError_t launch_gemm_pair(bool mx, int epi, const PairMaps &m, const GemmArgs
 
 namespace {
 template <bool MX, int EPI, int NUM_ACC>
-int max_clusters_one() {
+int max_clusters_one_query() {
   using C = PairCfg<MX, NUM_ACC>;
   if (cudaFuncSetAttribute(gemm_pair_kernel<MX, EPI, NUM_ACC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(C::SMEM)) != cudaSuccess)
@@ -417,6 +417,11 @@ int max_clusters_one() {
   int n = 0;
   if (cudaOccupancyMaxActiveClusters(&n, gemm_pair_kernel<MX, EPI, NUM_ACC>, &cfg) != cudaSuccess) return 0;
   return n;
+}
+template <bool MX, int EPI, int NUM_ACC>
+int max_clusters_one() {
+  static int memo[64] = {};
+  return per_device_memo(memo, max_clusters_one_query<MX, EPI, NUM_ACC>);
 }
 }  // namespace
 
