@@ -133,10 +133,12 @@ def output_bytes(cfg, name):
 
 
 def write_probe_gbs(dev):
-    """Write-only HBM bandwidth of this GPU: a device memset of 8 GB (taken
-    before the timed region; context for write-dominated kernels)."""
+    """Write-only HBM bandwidth of this GPU: a device fill of 8 GB (taken
+    before the timed region; context for write-dominated kernels).  The fill
+    runs on 8-byte elements: torch's fill of 1- and 2-byte elements issues
+    narrow stores and reaches only about half the write bandwidth."""
     import torch
-    buf = torch.empty(8 << 30, dtype=torch.uint8, device=dev)
+    buf = torch.empty(1 << 30, dtype=torch.int64, device=dev)
     buf.zero_()
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -145,7 +147,7 @@ def write_probe_gbs(dev):
         buf.zero_()
     b.record()
     b.synchronize()
-    gbs = 3 * buf.numel() / (a.elapsed_time(b) / 1e3) / 1e9
+    gbs = 3 * buf.numel() * 8 / (a.elapsed_time(b) / 1e3) / 1e9
     del buf
     torch.cuda.empty_cache()
     return gbs
@@ -593,9 +595,9 @@ def run_ours(args, cfg, passes, rank, world, local_rank):
                      "launch_ms": round(avg_ms, 4),
                      "write_probe": None if output_bytes(cfg, dom) is None else {
                          "note": "output-write-dominated kernel: its bf16 dW write rate against this GPU's "
-                                 "write-only bandwidth (device memset, measured before the timed region)",
+                                 "write-only bandwidth (device fill of 8 GB, measured before the timed region)",
                          "written_gbs": round(output_bytes(cfg, dom) / (tot / args.steps / 1e3) / 1e9, 1),
-                         "memset_gbs": round(write_gbs, 1),
+                         "fill_gbs": round(write_gbs, 1),
                          "frac": round(output_bytes(cfg, dom) / (tot / args.steps / 1e3) / 1e9 / write_gbs, 4)}},
         "kernels": kernels,
         "route_schedule_share": round(rs, 4),

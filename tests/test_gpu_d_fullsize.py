@@ -56,7 +56,11 @@ def test_full_size_backward_sampled():
     cfg, x, logits, gu_all, dn_all, shared, layer = build("kimi-k2.7", backward=True)
     dy = mi.out_grad(cfg, x.device)
     layer.forward(x, logits, train=True)
-    g = layer.backward(dy, x)
+    grads = layer.alloc_grads()
+    for v in grads.values():
+        if v is not None:
+            v.fill_(float("nan"))  # every element must be written by the backward
+    g = layer.backward(dy, x, grads=grads)
     assert layer.status() == 0
     k, fmt, tol = cfg["k"], cfg["fmt"], TOL[cfg["fmt"]]
     # seeded tokens: forward + backward of the oracle on those tokens alone
@@ -90,6 +94,19 @@ def test_full_size_backward_sampled():
         bw = om.expert_backward(dO, X, fw["GU_saved"], fw["h_saved"], W_gu, W_dn, fmt, ops)
         assert rel(mi.to_f64(g["dW_gu"][e_dw]), bw["dW_gu"]) < tol, "dW_gu of expert %d" % e_dw
         assert rel(mi.to_f64(g["dW_dn"][e_dw]), bw["dW_dn"]) < tol, "dW_dn of expert %d" % e_dw
+    # every dW element is written, and an expert that received no rows has an
+    # all-zero gradient (the Zipf-biased router leaves many experts empty)
+    empty = torch.as_tensor(counts == 0, device=x.device)
+    assert bool(empty.any())
+    for name in ("dW_gu", "dW_dn"):
+        for e0 in range(0, cfg["E"], 32):
+            blk = g[name][e0:e0 + 32]
+            assert not bool(torch.isnan(blk).any()), "%s: unwritten elements near expert %d" % (name, e0)
+            z = empty[e0:e0 + 32]
+            if bool(z.any()):
+                assert not bool(blk[z].any()), "%s of an empty expert near %d" % (name, e0)
+    for name in ("dx", "dlogits", "dWs_gu", "dWs_dn"):
+        assert not bool(torch.isnan(g[name]).any()), name
 
 
 def test_full_size_ring_bitwise_equal():
