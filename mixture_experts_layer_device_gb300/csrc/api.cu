@@ -127,6 +127,7 @@ void saved_layout(const Dims &D, Layout &L) {
 void ws_layout(const Dims &D, Layout &L) {
   L.add("status", 16);
   L.add("hist", static_cast<size_t>(D.nchunks) * D.E * 4);
+  L.add("tile_order", static_cast<size_t>(D.Rp / 32) * 4);
   if (D.aux_alpha > 0.f) {
     L.add("aux", (1 + 2 * static_cast<size_t>(D.E)) * 4);  // [L, P[E], f[E]]
     L.add("aux_part", static_cast<size_t>(moe::balance_blocks(D.T)) * D.E * 4);
@@ -134,9 +135,11 @@ void ws_layout(const Dims &D, Layout &L) {
   L.add("cublas_ws", kCublasWorkspace);  // the router GEMMs
   add_route(D, L);  // used when the forward saves nothing
   const size_t eb = D.mx ? 1 : 2;
-  if (D.ring) {  // per-token codes + a fixed ring of 128-row tiles instead of every dispatched row
+  if (D.mx) {  // row-blocked codes of every token (the dispatch copies them per routed row)
     L.add("xq", static_cast<size_t>(D.T) * D.d);
     L.add("xq_sf", static_cast<size_t>(D.T) * D.d / 32);
+  }
+  if (D.ring) {  // a fixed ring of 128-row tiles instead of every dispatched row
     L.add("ring", static_cast<size_t>(D.ring_slots) * 128 * D.d);
     L.add("ring_sf", static_cast<size_t>(D.ring_slots) * 128 * D.d / 32);
     L.add("ring_ctrl", (2 * static_cast<size_t>(D.ring_slots) + 1) * 4);
@@ -392,6 +395,7 @@ Ptrs route_ptrs(const Layout &L, void *base, void *ws, const Layout &W) {
   p.rb.inv = reinterpret_cast<int *>(L.ptr(base, "inv"));
   p.rb.poff = reinterpret_cast<int *>(L.ptr(base, "poff"));
   p.rb.hist = reinterpret_cast<int *>(W.ptr(ws, "hist"));
+  p.rb.tile_order = reinterpret_cast<int *>(W.ptr(ws, "tile_order"));
   p.status = reinterpret_cast<int *>(W.ptr(ws, "status"));
   return p;
 }
@@ -566,7 +570,8 @@ int moe_forward(const moe_config *cfg, const void *x, const float *logits, const
   uint8_t *xq_sf = reinterpret_cast<uint8_t *>(W.ptr(ws, "xq_sf"));
   if (!D.ring) {
     Traced tr("dispatch_gather", s);
-    rc = cuda_status(moe::launch_gather(x, D.T, D.d, D.k, D.E, rb, D.Rp, D.mx, xs, xs_sf, xT, xT_sf, s));
+    rc = cuda_status(
+        moe::launch_gather(x, D.T, D.d, D.k, D.E, rb, D.Rp, D.mx, xs, xs_sf, xT, xT_sf, xq, xq_sf, s));
   } else {
     // row-blocked codes once per token (identical for all k routed copies);
     // the ring kernel's gather SMs move them.  A training pass also needs the
@@ -578,7 +583,8 @@ int moe_forward(const moe_config *cfg, const void *x, const float *logits, const
     if (rc == MOE_OK && train) {
       Traced tr("dispatch_xT", s);
       rc = cuda_status(
-          moe::launch_gather(x, D.T, D.d, D.k, D.E, rb, D.Rp, true, nullptr, nullptr, xT, xT_sf, s));
+          moe::launch_gather(x, D.T, D.d, D.k, D.E, rb, D.Rp, true, nullptr, nullptr, xT, xT_sf, nullptr,
+                             nullptr, s));
     }
   }
   if (rc != MOE_OK) return rc;
@@ -763,7 +769,7 @@ int moe_backward(const moe_config *cfg, const void *dy, const void *x, const moe
   {
     Traced tr("reverse_combine", s);
     if (mx)  // also writes dO^T's column-blocked codes (the wgrad operand)
-      rc = cuda_status(moe::launch_reverse_combine_mx(dy, o, D.d, D.k, D.E, rb, D.Rp, g, u8("dOq"),
+      rc = cuda_status(moe::launch_reverse_combine_mx(dy, o, D.T, D.d, D.k, D.E, rb, D.Rp, g, u8("dOq"),
                                                       u8("dOq_sf"), u8("dOT"), u8("dOT_sf"), s));
     else
       rc = cuda_status(moe::launch_reverse_combine(dy, o, D.T, D.d, D.k, D.E, rb, D.Rp, dO, g, mx,

@@ -1,6 +1,6 @@
-// Dispatch helpers shared by the stand-alone dispatch kernel and the gather
-// CTAs of the persistent ring kernel: bf16 unpacking, 4-lane MXFP8 block
-// encoding, the token of an expert-sorted row, and the 32-row dispatch tile.
+// Dispatch helpers: bf16 unpacking, 4-lane MXFP8 block encoding, the token of
+// an expert-sorted row (also used by the gather CTAs of the persistent ring
+// kernel), column-blocked codes of a 32-row tile, and the 32-row dispatch tile.
 //
 // Method reference ("Mixture-of-Kittens" wiki page, Key claims, MXFP8 bullet):
 // activations are quantised to MXFP8 inside the dispatch.
@@ -48,58 +48,124 @@ MOE_DEV int token_of_row(const RouteBufs &b, int E, int k, int pr, int *slot_out
   return slot / k;
 }
 
+// 32 bytes to global memory at a 16-byte-aligned address: one 32-byte store
+// (a full sector) when the address allows it, else two 16-byte stores.
+MOE_DEV void st_global_32B(void *p, const uint32_t *w) {
+  if ((reinterpret_cast<uintptr_t>(p) & 31u) == 0) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]), "r"(w[1]),
+                 "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                 : "memory");
+  } else {
+    reinterpret_cast<uint4 *>(p)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    reinterpret_cast<uint4 *>(p)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  }
+}
+
+// Column-blocked MXFP8 codes of one 256-column chunk of a 32-row tile held in
+// shared memory as bf16 (tile[row][col], 256 columns per row): thread c (of
+// 256) owns column c, i.e. one 32-value block, and writes its 32 codes to row
+// col0 + c of the transposed codes (row stride ld_t) at columns r0 .. r0 + 31,
+// and the block's scale byte into the tiled scales (K = ld_t).
+MOE_DEV void column_block_codes(const uint16_t (*tile)[256], int c, long col0, int r0, uint8_t *__restrict__ dT,
+                                uint8_t *__restrict__ dT_sf, long ld_t) {
+  float v[32];
+  float am = 0.f;
+#pragma unroll
+  for (int r = 0; r < 32; ++r) {
+    v[r] = __uint_as_float(static_cast<uint32_t>(tile[r][c]) << 16);
+    am = fmaxf(am, fabsf(v[r]));
+  }
+  const uint32_t byte = mx_scale_byte(am);
+  uint32_t w[8];
+  mx_encode32(v, byte, w);
+  const long ocol = col0 + c;
+  st_global_32B(dT + ocol * ld_t + r0, w);
+  dT_sf[sf_tiled_offset(ocol, r0 / 32, ld_t)] = static_cast<uint8_t>(byte);
+}
+
 // MXFP8 dispatch of the 32 expert-sorted padded rows [r0, r0 + 32) by 256
-// threads: each row's token is read from x [T, d] (bf16, zeros for padding
-// rows) and, unless dst is NULL, quantised along d into codes at dst row
-// q0 + i (row stride d) with tiled scales (K = d).  When xT is given, the
-// same 32 rows are also quantised per column (one 32-row block) into the
-// transposed codes xT [d, ld_t] at columns r0 .. r0 + 31, with tiled scales
-// (K = ld_t).  `tile` is 32 x 65 floats of shared memory; `sync()` is a
-// barrier over the 256 threads.
-template <typename Sync>
-MOE_DEV void dispatch_rows32(const uint16_t *__restrict__ x, int d, int k, int E, const RouteBufs &b, int r0,
-                             int q0, uint8_t *__restrict__ dst, uint8_t *__restrict__ dst_sf,
-                             uint8_t *__restrict__ xT, uint8_t *__restrict__ xT_sf, long ld_t,
-                             float (*tile)[65], int tid, Sync sync) {
-  const int rr = tid >> 3;
-  const int cc = (tid & 7) * 8;
+// threads.  Unless dst is NULL, the row-blocked codes (blocks of 32 along d)
+// of each row's token go to dst rows r0 .. r0 + 31 (row stride d) with tiled
+// scales (K = d), zeros for padding rows: with xq given they are copied from
+// the codes every token got once beforehand (xq [T, d], canonical scales
+// xq_sf [T, d / 32]); otherwise they are encoded here from x [T, d] (bf16).
+// When xT is given, the same 32 rows of x are also quantised per column (one
+// 32-row block) into the transposed codes xT [d, ld_t] at columns r0 .. r0 +
+// 31, with tiled scales (K = ld_t), through `tile` (two 32 x 256 bf16 buffers,
+// one barrier per 256-column chunk).  Columns are swept 256 at a time with the
+// next chunk's loads in flight.  COPY: xq is given, dst is not NULL and xT is
+// NULL (inference).
+template <bool COPY>
+MOE_DEV void dispatch_rows32(const uint16_t *__restrict__ x, const uint8_t *__restrict__ xq,
+                             const uint8_t *__restrict__ xq_sf, int d, int k, int E, const RouteBufs &b, int r0,
+                             uint8_t *__restrict__ dst, uint8_t *__restrict__ dst_sf, uint8_t *__restrict__ xT,
+                             uint8_t *__restrict__ xT_sf, long ld_t, uint16_t (*tile)[32][256], int tid) {
+  constexpr bool copy = COPY;    // row codes copied from the per-token codes
+  constexpr bool need_x = !COPY;  // bf16 rows read (row encode and/or column codes)
+  const int rr = tid >> 3;                // row of this thread's loads
+  const int c8 = tid & 7;
   const int pr = r0 + rr;
-  const int qr = q0 + rr;
   const int tok = token_of_row(b, E, k, pr, nullptr);
   const uint16_t *xr = x + static_cast<size_t>(tok < 0 ? 0 : tok) * d;
-  const int c = tid >> 2;
-  const int part = tid & 3;
+  const uint8_t *qr = COPY ? xq + static_cast<size_t>(tok < 0 ? 0 : tok) * d : nullptr;
+  // scales (copy): threads 0..63 move one 4-byte group (4 blocks of 32) of row tid / 2
+  const int srow = tid >> 1;
+  const int stok = (copy && tid < 64) ? token_of_row(b, E, k, r0 + srow, nullptr) : -1;
+  auto load = [&](int cb, uint4 *q, uint4 *c, uint32_t *sw) {
+    const bool in = cb < d;
+    if constexpr (need_x) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        q[j] = (in && tok >= 0) ? __ldg(reinterpret_cast<const uint4 *>(xr + cb + 64 * j + 8 * c8))
+                                : make_uint4(0, 0, 0, 0);
+    }
+    if constexpr (COPY) {
+#pragma unroll
+      for (int j = 0; j < 2; ++j)
+        c[j] = (in && tok >= 0) ? __ldg(reinterpret_cast<const uint4 *>(qr + cb + 128 * j + 16 * c8))
+                                : make_uint4(0, 0, 0, 0);
+      *sw = (in && tid < 64 && stok >= 0)
+                ? __ldg(reinterpret_cast<const uint32_t *>(xq_sf + static_cast<size_t>(stok) * (d / 32) + cb / 32 +
+                                                            4 * (tid & 1)))
+                : 0u;
+    }
+  };
+  uint4 q[4], c[2], qn[4], cn[2];
+  uint32_t sw = 0u, swn = 0u;
+  load(0, q, c, &sw);
+  int buf = 0;
   for (int cb = 0; cb < d; cb += 256) {
-    uint4 q[4];
+    load(cb + 256, qn, cn, &swn);  // the next chunk's loads in flight while this one is written
+    if constexpr (COPY) {
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
-      q[j] = tok >= 0 ? __ldg(reinterpret_cast<const uint4 *>(xr + cb + 64 * j + cc)) : make_uint4(0, 0, 0, 0);
+      for (int j = 0; j < 2; ++j)
+        *reinterpret_cast<uint4 *>(dst + static_cast<size_t>(pr) * d + cb + 128 * j + 16 * c8) = c[j];
+      if (tid < 64)
+        *reinterpret_cast<uint32_t *>(dst_sf + sf_tiled_offset(r0 + srow, cb / 32 + 4 * (tid & 1), d)) = sw;
+    } else if (dst) {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      float f[8];
-      unpack8(q[j], f);
-      if (dst) {
-        const int col = cb + 64 * j + cc;
+      for (int j = 0; j < 4; ++j) {
+        const int col = cb + 64 * j + 8 * c8;
+        float f[8];
+        unpack8(q[j], f);
         uint32_t byte;
-        const uint2 code = mx_encode8_quad(f, &byte);
-        *reinterpret_cast<uint2 *>(dst + static_cast<size_t>(qr) * d + col) = code;
-        if ((tid & 3) == 0) dst_sf[sf_tiled_offset(qr, col >> 5, d)] = static_cast<uint8_t>(byte);
-      }
-      if (xT) {
-        sync();
-#pragma unroll
-        for (int t = 0; t < 8; ++t) tile[rr][cc + t] = f[t];
-        sync();
-        float v[8];
-#pragma unroll
-        for (int t = 0; t < 8; ++t) v[t] = tile[part * 8 + t][c];
-        const size_t ocol = static_cast<size_t>(cb + 64 * j + c);
-        uint32_t tb;
-        const uint2 tcode = mx_encode8_quad(v, &tb);
-        *reinterpret_cast<uint2 *>(xT + ocol * ld_t + r0 + part * 8) = tcode;
-        if (part == 0) xT_sf[sf_tiled_offset(static_cast<long>(ocol), r0 / 32, ld_t)] = static_cast<uint8_t>(tb);
+        const uint2 code = mx_encode8_quad(f, &byte);  // the 4 threads of a 32-column block
+        *reinterpret_cast<uint2 *>(dst + static_cast<size_t>(pr) * d + col) = code;
+        if ((tid & 3) == 0) dst_sf[sf_tiled_offset(pr, col >> 5, d)] = static_cast<uint8_t>(byte);
       }
     }
+    if (!COPY && xT) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) *reinterpret_cast<uint4 *>(&tile[buf][rr][64 * j + 8 * c8]) = q[j];
+      __syncthreads();
+      column_block_codes(tile[buf], tid, cb, r0, xT, xT_sf, ld_t);
+      buf ^= 1;
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) q[j] = qn[j];
+    c[0] = cn[0];
+    c[1] = cn[1];
+    sw = swn;
   }
 }
 

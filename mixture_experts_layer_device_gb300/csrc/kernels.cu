@@ -209,16 +209,77 @@ __global__ void __launch_bounds__(256) gather_bf16_kernel(const uint4 *__restric
 // into xs codes [Rp, d] (+ tiled scales, K = d) and, when xT is given, the
 // block's 32 rows are also quantised per column into the transposed codes
 // xT [d, ld_t] (+ tiled scales, K = ld_t): the wgrad operand of the backward.
-__global__ void __launch_bounds__(256) gather_mx_tile_kernel(const uint16_t *__restrict__ x, int d, int k,
-                                                             int E, RouteBufs b, uint8_t *__restrict__ xs,
-                                                             uint8_t *__restrict__ xs_sf,
-                                                             uint8_t *__restrict__ xT,
-                                                             uint8_t *__restrict__ xT_sf, long ld_t) {
-  __shared__ float tile[32][65];
-  const int r0 = blockIdx.x * 32;
-  if (r0 >= __ldg(b.poff + E)) return;
-  dispatch_rows32(x, d, k, E, b, r0, r0, xs, xs_sf, xT, xT_sf, ld_t, tile, static_cast<int>(threadIdx.x),
-                  [] { __syncthreads(); });
+// Processing order of the 32-row tiles of the expert-sorted rows, for the
+// kernels that read one token row per routed row (MXFP8 dispatch and reverse
+// combine): tiles sorted by the token of their first row, by a counting sort
+// over kOrderBuckets token ranges (all-padding tiles last).  Tiles of
+// different experts that hold the same tokens then run at about the same
+// time, and the token rows they share come from L2 instead of HBM; in expert
+// order every hot expert sweeps all T token rows again.  Only the order in
+// which blocks take tiles changes: each tile is still written by one block,
+// with the same values.  One block of kOrderBuckets threads.
+constexpr int kOrderBuckets = 1024;
+
+__global__ void __launch_bounds__(kOrderBuckets) tile_order_kernel(RouteBufs b, int T, int E, int k,
+                                                                   int *__restrict__ order) {
+  __shared__ int cnt[kOrderBuckets];
+  __shared__ int wsum[kOrderBuckets / 32];
+  const int tid = static_cast<int>(threadIdx.x);
+  const int lane = tid & 31, warp = tid >> 5;
+  const int ntiles = __ldg(b.poff + E) >> 5;
+  auto key = [&](int t) {
+    const int tok = token_of_row(b, E, k, t * 32, nullptr);
+    return tok < 0 ? kOrderBuckets - 1
+                   : static_cast<int>(static_cast<long long>(tok) * kOrderBuckets / T);
+  };
+  cnt[tid] = 0;
+  __syncthreads();
+  for (int t = tid; t < ntiles; t += kOrderBuckets) atomicAdd(&cnt[key(t)], 1);
+  __syncthreads();
+  // exclusive scan of the bucket counts, one bucket per thread
+  const int v = cnt[tid];
+  int x = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, off);
+    if (lane >= off) x += y;
+  }
+  if (lane == 31) wsum[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = wsum[lane];
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, w, off);
+      if (lane >= off) w += y;
+    }
+    wsum[lane] = w;
+  }
+  __syncthreads();
+  cnt[tid] = x - v + (warp > 0 ? wsum[warp - 1] : 0);  // first position of the bucket
+  __syncthreads();
+  for (int t = tid; t < ntiles; t += kOrderBuckets) order[atomicAdd(&cnt[key(t)], 1)] = t;
+}
+
+// First row of the tile block `blk` takes, or -1 past the last tile.
+MOE_DEV int tile_row0(const RouteBufs &b, int E, int blk) {
+  if (blk >= (__ldg(b.poff + E) >> 5)) return -1;
+  return 32 * (b.tile_order ? __ldg(b.tile_order + blk) : blk);
+}
+
+template <bool COPY>
+__global__ void __launch_bounds__(256, 4) gather_mx_tile_kernel(const uint16_t *__restrict__ x,
+                                                                const uint8_t *__restrict__ xq,
+                                                                const uint8_t *__restrict__ xq_sf, int d, int k,
+                                                                int E, RouteBufs b, uint8_t *__restrict__ xs,
+                                                                uint8_t *__restrict__ xs_sf,
+                                                                uint8_t *__restrict__ xT,
+                                                                uint8_t *__restrict__ xT_sf, long ld_t) {
+  __shared__ __align__(16) uint16_t tile[2][32][256];
+  const int r0 = tile_row0(b, E, static_cast<int>(blockIdx.x));
+  if (r0 < 0) return;
+  dispatch_rows32<COPY>(x, xq, xq_sf, d, k, E, b, r0, xs, xs_sf, xT, xT_sf, ld_t, tile,
+                        static_cast<int>(threadIdx.x));
 }
 
 // ------------------------------------------------------------ S6: combine
@@ -303,39 +364,45 @@ __global__ void __launch_bounds__(256) reverse_combine_kernel(
 }
 
 // ------------------------------------------------------------ B1, MXFP8: fused
-// Block: 32 padded rows x all d columns, swept in 256-column chunks (four
-// 64-column sub-tiles, loads issued up front).  Per element dO = bf16(w * dy);
-// written as row-blocked E4M3 codes (the dgrad operand, blocks of 32 along d)
-// and, through a shared-memory transpose, as column-blocked codes of dO^T
-// (the wgrad operand, blocks of the block's 32 rows).  g = <dy, o> per row is
-// accumulated per thread in column order and reduced over the row's 8
-// threads in a fixed shuffle order.
-__global__ void __launch_bounds__(256) reverse_combine_mx_kernel(
+// Block: 32 padded rows x all d columns, swept in 256-column chunks with the
+// next chunk's loads in flight.  Per element dO = bf16(w * dy); written as
+// row-blocked E4M3 codes (the dgrad operand, blocks of 32 along d, encoded by
+// the 4 threads holding a block) and, through a shared-memory tile of the
+// chunk (two buffers, one barrier per chunk), as column-blocked codes of dO^T
+// (the wgrad operand, one 32-row block per column, encoded by the thread
+// owning the column).  g = <dy, o> per row is accumulated per thread in column
+// order and reduced over the row's 8 threads in a fixed shuffle order.
+__global__ void __launch_bounds__(256, 3) reverse_combine_mx_kernel(
     const uint16_t *__restrict__ dy, const uint16_t *__restrict__ o, int d, int k, int E, RouteBufs b,
     float *__restrict__ g, uint8_t *__restrict__ dOq, uint8_t *__restrict__ dOq_sf,
     uint8_t *__restrict__ dOT, uint8_t *__restrict__ dOT_sf, long ld_t) {
-  __shared__ float tile[32][65];
-  const int r0 = blockIdx.x * 32;
-  if (r0 >= __ldg(b.poff + E)) return;
-  const int rr = threadIdx.x >> 3;
-  const int cc = (threadIdx.x & 7) * 8;
+  __shared__ __align__(16) uint16_t tile[2][32][256];
+  const int r0 = tile_row0(b, E, static_cast<int>(blockIdx.x));
+  if (r0 < 0) return;
+  const int tid = static_cast<int>(threadIdx.x);
+  const int rr = tid >> 3;
+  const int cc = (tid & 7) * 8;
   const int pr = r0 + rr;
   int slot = 0;
   const int tok = token_of_row(b, E, k, pr, &slot);
   const float wv = tok >= 0 ? __ldg(b.w + slot) : 0.f;
   const uint16_t *dyr = dy + static_cast<size_t>(tok < 0 ? 0 : tok) * d;
   const uint16_t *orow = o + static_cast<size_t>(pr) * d;
-  const int c = threadIdx.x >> 2;    // transposed output row within a sub-tile
-  const int part = threadIdx.x & 3;  // 8 source rows each
-  float dot = 0.f;
-  for (int cb = 0; cb < d; cb += 256) {
-    uint4 qy[4], qo[4];
+  auto load = [&](int cb, uint4 *qy, uint4 *qo) {
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
+      const bool ok = tok >= 0 && cb < d;
       const size_t col = static_cast<size_t>(cb + 64 * j + cc);
-      qy[j] = tok >= 0 ? __ldg(reinterpret_cast<const uint4 *>(dyr + col)) : make_uint4(0, 0, 0, 0);
-      qo[j] = tok >= 0 ? __ldg(reinterpret_cast<const uint4 *>(orow + col)) : make_uint4(0, 0, 0, 0);
+      qy[j] = ok ? __ldg(reinterpret_cast<const uint4 *>(dyr + col)) : make_uint4(0, 0, 0, 0);
+      qo[j] = ok ? __ldg(reinterpret_cast<const uint4 *>(orow + col)) : make_uint4(0, 0, 0, 0);
     }
+  };
+  uint4 qy[4], qo[4], ny[4], no[4];
+  load(0, qy, qo);
+  float dot = 0.f;
+  int buf = 0;
+  for (int cb = 0; cb < d; cb += 256) {
+    load(cb + 256, ny, no);
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       float fy[8], fo[8], f[8];
@@ -344,33 +411,30 @@ __global__ void __launch_bounds__(256) reverse_combine_mx_kernel(
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
         dot = fmaf(fy[q], fo[q], dot);
-        f[q] = round_bf16(wv * fy[q]);
+        f[q] = wv * fy[q];
       }
+      const uint4 pk = pack8(f);  // dO = bf16(w * dy), one conversion per pair
+      unpack8(pk, f);
       const int col = cb + 64 * j + cc;
-      // row-blocked codes: the 4 threads cc/8 = 4h..4h+3 hold one block of 32
       uint32_t byte;
       const uint2 code = mx_encode8_quad(f, &byte);
       *reinterpret_cast<uint2 *>(dOq + static_cast<size_t>(pr) * d + col) = code;
-      if ((threadIdx.x & 3) == 0) dOq_sf[sf_tiled_offset(pr, col >> 5, d)] = static_cast<uint8_t>(byte);
-      // column-blocked codes of the transpose
-      __syncthreads();
+      if ((tid & 3) == 0) dOq_sf[sf_tiled_offset(pr, col >> 5, d)] = static_cast<uint8_t>(byte);
+      *reinterpret_cast<uint4 *>(&tile[buf][rr][64 * j + cc]) = pk;
+    }
+    __syncthreads();
+    column_block_codes(tile[buf], tid, cb, r0, dOT, dOT_sf, ld_t);
+    buf ^= 1;
 #pragma unroll
-      for (int q = 0; q < 8; ++q) tile[rr][cc + q] = f[q];
-      __syncthreads();
-      float t[8];
-#pragma unroll
-      for (int q = 0; q < 8; ++q) t[q] = tile[part * 8 + q][c];
-      const size_t ocol = static_cast<size_t>(cb + 64 * j + c);
-      uint32_t tbyte;
-      const uint2 tcode = mx_encode8_quad(t, &tbyte);
-      *reinterpret_cast<uint2 *>(dOT + ocol * ld_t + r0 + part * 8) = tcode;
-      if (part == 0) dOT_sf[sf_tiled_offset(static_cast<long>(ocol), r0 / 32, ld_t)] = static_cast<uint8_t>(tbyte);
+    for (int j = 0; j < 4; ++j) {
+      qy[j] = ny[j];
+      qo[j] = no[j];
     }
   }
   // g: the 8 threads of a row are lanes 8u..8u+7 of one warp
 #pragma unroll
   for (int off = 4; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
-  if ((threadIdx.x & 7) == 0 && tok >= 0) g[slot] = dot;
+  if ((tid & 7) == 0 && tok >= 0) g[slot] = dot;
 }
 
 // ------------------------------------------------------------ load-balancing term
@@ -646,12 +710,28 @@ cudaError_t launch_route(const float *logits, int T, int E, int k, const RouteBu
 
 cudaError_t launch_gather(const void *x, int T, int d, int k, int E, const RouteBufs &b,
                           int64_t rp_max, bool mx, void *xs, uint8_t *xs_sf, uint8_t *xT, uint8_t *xT_sf,
-                          cudaStream_t s) {
-  (void)T;
-  if (mx)
-    gather_mx_tile_kernel<<<blocks_for(rp_max, 32), 256, 0, s>>>(
-        static_cast<const uint16_t *>(x), d, k, E, b, static_cast<uint8_t *>(xs), xs_sf, xT, xT_sf, rp_max);
-  else
+                          uint8_t *xq, uint8_t *xq_sf, cudaStream_t s) {
+  if (mx) {
+    // Inference: every token's row codes once, then the dispatch copies them
+    // per routed row.  Training reads the bf16 rows anyway (for the column-
+    // blocked codes) and encodes the row codes from the same registers.
+    if (xs && !xT) {
+      quantize_rows_kernel<false><<<blocks_for(T, 8), 256, 0, s>>>(static_cast<const uint4 *>(x), T, d,
+                                                                    reinterpret_cast<uint2 *>(xq), xq_sf);
+    } else {
+      xq = nullptr;
+      xq_sf = nullptr;
+    }
+    if (b.tile_order) tile_order_kernel<<<1, kOrderBuckets, 0, s>>>(b, T, E, k, b.tile_order);
+    if (xq)
+      gather_mx_tile_kernel<true><<<blocks_for(rp_max, 32), 256, 0, s>>>(
+          static_cast<const uint16_t *>(x), xq, xq_sf, d, k, E, b, static_cast<uint8_t *>(xs), xs_sf, xT, xT_sf,
+          rp_max);
+    else
+      gather_mx_tile_kernel<false><<<blocks_for(rp_max, 32), 256, 0, s>>>(
+          static_cast<const uint16_t *>(x), xq, xq_sf, d, k, E, b, static_cast<uint8_t *>(xs), xs_sf, xT, xT_sf,
+          rp_max);
+  } else
     gather_bf16_kernel<<<blocks_for(rp_max, 8), 256, 0, s>>>(static_cast<const uint4 *>(x), d, k, E, b, rp_max,
                                                               static_cast<uint4 *>(xs));
   return cudaGetLastError();
@@ -681,9 +761,10 @@ cudaError_t launch_reverse_combine(const void *dy, const void *o, int T, int d, 
   return cudaGetLastError();
 }
 
-cudaError_t launch_reverse_combine_mx(const void *dy, const void *o, int d, int k, int E,
+cudaError_t launch_reverse_combine_mx(const void *dy, const void *o, int T, int d, int k, int E,
                                       const RouteBufs &b, int64_t rp_max, float *g, uint8_t *dOq,
                                       uint8_t *dOq_sf, uint8_t *dOT, uint8_t *dOT_sf, cudaStream_t s) {
+  if (b.tile_order) tile_order_kernel<<<1, kOrderBuckets, 0, s>>>(b, T, E, k, b.tile_order);
   reverse_combine_mx_kernel<<<blocks_for(rp_max, 32), 256, 0, s>>>(
       static_cast<const uint16_t *>(dy), static_cast<const uint16_t *>(o), d, k, E, b, g, dOq, dOq_sf,
       dOT, dOT_sf, rp_max);

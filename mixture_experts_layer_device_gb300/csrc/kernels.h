@@ -25,18 +25,23 @@ struct RouteBufs {
   int *inv;       // [R]  row -> slot
   int *poff;      // [E+1] padded offsets (multiples of 128)
   int *hist;      // [nchunks * E] scratch
+  int *tile_order;  // [Rp / 32] processing order of 32-row tiles (may be NULL: row order)
 };
 
 cudaError_t launch_route(const float *logits, int T, int E, int k, const RouteBufs &b,
                          cudaStream_t s);
 
 // Gather routed rows of x into padded expert-sorted order (zero padding rows).
-// MX: writes E4M3 codes [Rp, d] and tiled scales (K = d) instead of bf16 rows,
-// and, when xT is not NULL, the column-blocked transposed codes xT [d, Rp]
-// (+ tiled scales, K = Rp) of the same rows.
+// MX: when xs is not NULL, writes the row-blocked codes of each routed row to
+// xs [Rp, d] with tiled scales (K = d); when xT is not NULL, also the
+// column-blocked transposed codes xT [d, Rp] (+ tiled scales, K = Rp) of the
+// same rows.  Without xT (inference) every token is first quantised once into
+// xq [T, d] (canonical scales xq_sf [T, d / 32]) and the dispatch copies those
+// codes; with xT the row codes are encoded from the bf16 rows it reads anyway.
+// BF16: copies rows of x to xs.
 cudaError_t launch_gather(const void *x, int T, int d, int k, int E, const RouteBufs &b,
                           int64_t rp_max, bool mx, void *xs, uint8_t *xs_sf, uint8_t *xT, uint8_t *xT_sf,
-                          cudaStream_t s);
+                          uint8_t *xq, uint8_t *xq_sf, cudaStream_t s);
 
 // y[t] = bf16( sum_j w[t,j] * o[row(t,j)] + s[t] ), fixed j order.
 cudaError_t launch_combine(const void *o, const void *s_out, int T, int d, int k, int E,
@@ -52,7 +57,7 @@ cudaError_t launch_reverse_combine(const void *dy, const void *o, int T, int d, 
 // dO = bf16(w * dy) written as row-blocked codes dOq [Rp, d] (+ tiled scales,
 // K = d) and column-blocked transposed codes dOT [d, ld_t = Rp] (+ tiled
 // scales, K = Rp); padding rows give zero codes.
-cudaError_t launch_reverse_combine_mx(const void *dy, const void *o, int d, int k, int E,
+cudaError_t launch_reverse_combine_mx(const void *dy, const void *o, int T, int d, int k, int E,
                                       const RouteBufs &b, int64_t rp_max, float *g, uint8_t *dOq,
                                       uint8_t *dOq_sf, uint8_t *dOT, uint8_t *dOT_sf, cudaStream_t s);
 

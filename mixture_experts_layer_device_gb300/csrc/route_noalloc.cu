@@ -68,7 +68,7 @@ extern "C" int moe_route_noalloc(const moe_config *cfg, const float *logits, int
   const int rc = scratch_address(&base);
   if (rc != MOE_OK) return rc;
   char *b = static_cast<char *>(base);
-  moe::RouteBufs rb;
+  moe::RouteBufs rb = {};
   rb.idx = idx;
   rb.w = w;
   rb.counts = counts;
