@@ -61,18 +61,25 @@ MOE_DEV void st_global_32B(void *p, const uint32_t *w) {
   }
 }
 
+// Column of element (r, c) in a 32 x 256 bf16 shared-memory tile: the 16-byte
+// chunks of rows 8 apart are swizzled (chunk index XOR (r / 8) % 4), so that
+// four threads reading one column at rows 0, 8, 16, 24 hit different banks,
+// while a row's aligned 128-byte runs stay contiguous for 16-byte writes.
+MOE_DEV int tcol(int r, int c) { return (((c >> 3) ^ ((r >> 3) & 3)) << 3) | (c & 7); }
+
 // Column-blocked MXFP8 codes of one 256-column chunk of a 32-row tile held in
-// shared memory as bf16 (tile[row][col], 256 columns per row): thread c (of
+// shared memory as bf16 (tile[row][tcol(row, col)]): thread c (of
 // 256) owns column c, i.e. one 32-value block, and writes its 32 codes to row
 // col0 + c of the transposed codes (row stride ld_t) at columns r0 .. r0 + 31,
-// and the block's scale byte into the tiled scales (K = ld_t).
+// and the block's scale byte into the tiled scales (K = ld_t) at row
+// sf_row0 + col0 + c.
 MOE_DEV void column_block_codes(const uint16_t (*tile)[256], int c, long col0, int r0, uint8_t *__restrict__ dT,
-                                uint8_t *__restrict__ dT_sf, long ld_t) {
+                                uint8_t *__restrict__ dT_sf, long ld_t, long sf_row0 = 0) {
   float v[32];
   float am = 0.f;
 #pragma unroll
   for (int r = 0; r < 32; ++r) {
-    v[r] = __uint_as_float(static_cast<uint32_t>(tile[r][c]) << 16);
+    v[r] = __uint_as_float(static_cast<uint32_t>(tile[r][tcol(r, c)]) << 16);
     am = fmaxf(am, fabsf(v[r]));
   }
   const uint32_t byte = mx_scale_byte(am);
@@ -80,7 +87,7 @@ MOE_DEV void column_block_codes(const uint16_t (*tile)[256], int c, long col0, i
   mx_encode32(v, byte, w);
   const long ocol = col0 + c;
   st_global_32B(dT + ocol * ld_t + r0, w);
-  dT_sf[sf_tiled_offset(ocol, r0 / 32, ld_t)] = static_cast<uint8_t>(byte);
+  dT_sf[sf_tiled_offset(sf_row0 + ocol, r0 / 32, ld_t)] = static_cast<uint8_t>(byte);
 }
 
 // MXFP8 dispatch of the 32 expert-sorted padded rows [r0, r0 + 32) by 256
@@ -156,7 +163,7 @@ MOE_DEV void dispatch_rows32(const uint16_t *__restrict__ x, const uint8_t *__re
     }
     if (!COPY && xT) {
 #pragma unroll
-      for (int j = 0; j < 4; ++j) *reinterpret_cast<uint4 *>(&tile[buf][rr][64 * j + 8 * c8]) = q[j];
+      for (int j = 0; j < 4; ++j) *reinterpret_cast<uint4 *>(&tile[buf][rr][tcol(rr, 64 * j + 8 * c8)]) = q[j];
       __syncthreads();
       column_block_codes(tile[buf], tid, cb, r0, xT, xT_sf, ld_t);
       buf ^= 1;

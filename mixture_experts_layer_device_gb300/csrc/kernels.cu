@@ -420,7 +420,7 @@ __global__ void __launch_bounds__(256, 3) reverse_combine_mx_kernel(
       const uint2 code = mx_encode8_quad(f, &byte);
       *reinterpret_cast<uint2 *>(dOq + static_cast<size_t>(pr) * d + col) = code;
       if ((tid & 3) == 0) dOq_sf[sf_tiled_offset(pr, col >> 5, d)] = static_cast<uint8_t>(byte);
-      *reinterpret_cast<uint4 *>(&tile[buf][rr][64 * j + cc]) = pk;
+      *reinterpret_cast<uint4 *>(&tile[buf][rr][tcol(rr, 64 * j + cc)]) = pk;
     }
     __syncthreads();
     column_block_codes(tile[buf], tid, cb, r0, dOT, dOT_sf, ld_t);
@@ -590,10 +590,11 @@ __global__ void __launch_bounds__(256) reverse_dispatch_kernel(
 }
 
 // ------------------------------------------------------------ transposes
-// Block: 32 source rows x 256 columns, as four 64-column sub-tiles whose
-// global loads are all issued up front (16 bytes per thread each).  Output
-// rows are source columns; MX output quantises each 32-long output run (the
-// block's 32 rows) as one block.
+// Block: 32 source rows x 256 columns, loaded up front (four 16-byte loads per
+// thread) into a bf16 shared-memory tile; after one barrier the output rows
+// (source columns) are written: for MX thread c owns output row c, one
+// 32-value block, and writes its 32 codes plus the scale byte; bf16 output
+// rows are written 64 bytes at a time by 4 threads each.
 // ROWQ (MX, weights): the tile's source rows are also quantised along C into
 // row-blocked codes rq [batch * nrows, C] with tiled scales (K = C), so one
 // read of the bf16 source gives both operand orientations.
@@ -603,15 +604,16 @@ __global__ void __launch_bounds__(256) transpose_rows_kernel(
     const int *__restrict__ nrows_dev, long nsrc, int k, int E, RouteBufs b, void *dst,
     long dst_batch_stride, uint8_t *__restrict__ dst_sf, long sf_batch_rows, long ld_dst,
     uint8_t *__restrict__ rq = nullptr, uint8_t *__restrict__ rq_sf = nullptr) {
-  __shared__ float tile[32][65];
+  __shared__ __align__(16) uint16_t tile[32][256];
   const int r0 = blockIdx.x * 32;
   const int cb = blockIdx.y * 256;
   const int bz = blockIdx.z;
   const int nrows = nrows_dev ? __ldg(nrows_dev) : nrows_host;
   if (r0 >= nrows) return;
   src += static_cast<size_t>(bz) * src_batch_stride;
-  const int rr = threadIdx.x >> 3;          // 0..31: source row within the block
-  const int cc = (threadIdx.x & 7) * 8;     // 0..56: column within a sub-tile
+  const int tid = static_cast<int>(threadIdx.x);
+  const int rr = tid >> 3;          // 0..31: source row within the block
+  const int cc = (tid & 7) * 8;     // 0..56: column within a 64-column sub-tile
   const int r = r0 + rr;
   long srow = r;
   if constexpr (GATHER) srow = token_of_row(b, E, k, r, nullptr);
@@ -623,39 +625,41 @@ __global__ void __launch_bounds__(256) transpose_rows_kernel(
     q[j] = (valid && j < nsub)
                ? __ldg(reinterpret_cast<const uint4 *>(src + static_cast<size_t>(srow) * C + cb + 64 * j + cc))
                : make_uint4(0, 0, 0, 0);
-  const int c = threadIdx.x >> 2;   // output row within a sub-tile (0..63)
-  const int part = threadIdx.x & 3; // 8 source rows each
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     if (j >= nsub) break;
-    if (j) __syncthreads();
-    float f[8];
-    unpack8(q[j], f);
     if constexpr (ROWQ) {
+      float f[8];
+      unpack8(q[j], f);
       const long qrow = static_cast<long>(bz) * nrows + r;
       const int col = cb + 64 * j + cc;
       uint32_t byte;
       const uint2 code = mx_encode8_quad(f, &byte);
       *reinterpret_cast<uint2 *>(rq + static_cast<size_t>(qrow) * C + col) = code;
-      if ((threadIdx.x & 3) == 0) rq_sf[sf_tiled_offset(qrow, col >> 5, C)] = static_cast<uint8_t>(byte);
+      if ((tid & 3) == 0) rq_sf[sf_tiled_offset(qrow, col >> 5, C)] = static_cast<uint8_t>(byte);
     }
+    *reinterpret_cast<uint4 *>(&tile[rr][tcol(rr, 64 * j + cc)]) = q[j];
+  }
+  __syncthreads();
+  if constexpr (MX) {
+    // thread c: source column cb + c = output row cb + c, one 32-value block
+    if (tid < 64 * nsub)
+      column_block_codes(tile, tid, cb, r0,
+                         reinterpret_cast<uint8_t *>(dst) + static_cast<size_t>(bz) * dst_batch_stride, dst_sf,
+                         ld_dst, static_cast<long>(bz) * sf_batch_rows);
+  } else {
+    // 4 threads per output row (8 source rows each), 64 output rows per round:
+    // a warp writes 8 output rows x 64 contiguous bytes per instruction
+    const int c = tid >> 2, part = tid & 3;
+    uint16_t *o = reinterpret_cast<uint16_t *>(dst) + static_cast<size_t>(bz) * dst_batch_stride + r0 + part * 8;
+    for (int j = 0; j < nsub; ++j) {
+      const int col = 64 * j + c;
+      uint32_t w[4];
 #pragma unroll
-    for (int t = 0; t < 8; ++t) tile[rr][cc + t] = f[t];
-    __syncthreads();
-#pragma unroll
-    for (int t = 0; t < 8; ++t) f[t] = tile[part * 8 + t][c];
-    const size_t orow = static_cast<size_t>(cb + 64 * j + c);
-    if constexpr (!MX) {
-      uint16_t *o = reinterpret_cast<uint16_t *>(dst) + static_cast<size_t>(bz) * dst_batch_stride;
-      *reinterpret_cast<uint4 *>(o + orow * ld_dst + r0 + part * 8) = pack8(f);
-    } else {
-      uint8_t *o = reinterpret_cast<uint8_t *>(dst) + static_cast<size_t>(bz) * dst_batch_stride;
-      uint32_t byte;
-      const uint2 code = mx_encode8_quad(f, &byte);
-      *reinterpret_cast<uint2 *>(o + orow * ld_dst + r0 + part * 8) = code;
-      if (part == 0)
-        dst_sf[sf_tiled_offset(static_cast<long>(bz) * sf_batch_rows + static_cast<long>(orow), r0 / 32,
-                               ld_dst)] = static_cast<uint8_t>(byte);
+      for (int h = 0; h < 4; ++h)
+        w[h] = static_cast<uint32_t>(tile[part * 8 + 2 * h][tcol(part * 8 + 2 * h, col)]) |
+               (static_cast<uint32_t>(tile[part * 8 + 2 * h + 1][tcol(part * 8 + 2 * h + 1, col)]) << 16);
+      *reinterpret_cast<uint4 *>(o + static_cast<size_t>(cb + col) * ld_dst) = make_uint4(w[0], w[1], w[2], w[3]);
     }
   }
 }
