@@ -382,8 +382,12 @@ MOE_DEV void tmem_cp_pair_32x128b_warpx4(uint32_t taddr, uint64_t sdesc) {
 }
 
 // ---------------------------------------------------------------- numerics
-MOE_DEV float silu(float g) { return g / (1.0f + expf(-g)); }
-MOE_DEV float sigmoidf(float g) { return 1.0f / (1.0f + expf(-g)); }
+// SiLU and the logistic sigmoid through the hardware exponential and
+// reciprocal (a few ulp of fp32; every use rounds the result to bf16 or
+// MXFP8).  For g < -87 the denominator overflows to +inf or beyond 2^126 and
+// the quotient is 0, the limit of both functions.
+MOE_DEV float silu(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
+MOE_DEV float sigmoidf(float g) { return __fdividef(1.0f, 1.0f + __expf(-g)); }
 
 MOE_DEV uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);  // .x = lo (low half)
