@@ -87,13 +87,13 @@ def kernel_work(cfg, name, train=False):
     dy once per token, not once per routed copy).  With MXFP8 experts a
     training pass's dispatch also writes the column-blocked codes of x, and its
     reverse combine both the row- and column-blocked codes of dO; the forward
-    gate/up GEMM of a training pass saves G|U and h in bf16 next to the MXFP8
-    codes of h."""
+    gate/up GEMM of a training pass saves G|U in bf16 and, with MXFP8, h as
+    row- and column-blocked codes (with BF16, h in bf16)."""
     T, d, m, E, k, ms = (cfg[n] for n in ("T", "d", "m", "E", "k", "m_shared"))
     R = T * k
     mx = cfg["fmt"] == "mxfp8"
     a = (1 + 1 / 32) if mx else 2          # bytes per stored expert operand element
-    h_out = (R * 2 * m * 2 + R * m * 2 + (R * m * a if mx else 0)) if train else R * m * a
+    h_out = (R * 2 * m * 2 + (2 * R * m * a if mx else R * m * 2)) if train else R * m * a
     sh_out = (T * 2 * ms * 2 + T * ms * 2) if train else T * ms * 2
     tbl = {
         "gemm1_gate_up_swiglu": (2.0 * R * 2 * m * d, R * d * a + E * 2 * m * d * a + h_out, mx),
@@ -118,8 +118,9 @@ def kernel_work(cfg, name, train=False):
         "reverse_combine": (0.0, T * d * 2 + R * d * 2 + R * 8 + (2 * R * d * a if mx else R * d * 2), mx),
         "reverse_dispatch": (0.0, R * d * 2 + R * 8 + T * d * 2 * (2 if ms else 1) + T * E * 4, mx),
         "route_schedule": (0.0, T * E * 4 + R * 4 * 6, mx),
-        "transpose_wgrad_operands": (0.0, (R * 2 * m * 2 + R * m * 2) + (R * 2 * m + R * m) * a
-                                     + (0 if mx else 2 * (R * d * 2 + R * d * a)), mx),
+        # MXFP8: dGU^T only (x^T, dO^T and h^T come from the dispatch, B1 and S4)
+        "transpose_wgrad_operands": (0.0, (R * 2 * m * (2 + a)) if mx
+                                     else (R * 2 * m + R * m + 2 * R * d) * (2 + a), mx),
         "shared_transpose_wgrad_operands": (0.0, 2 * 2 * T * (ms + d + 2 * ms + d), False),
     }
     return tbl.get(name)

@@ -156,8 +156,9 @@ size_t moe_saved_bytes(const moe_config *cfg);
 
 /* Byte offset and size of a named sub-buffer of `saved` (which = 0) or of the
  * workspace (which = 1), for inspection by tests and tools.  Names include
- * "idx", "w", "counts", "offsets", "perm", "inv", "poff", "o", "GU", "h",
- * "s_GU", "s_h" and, with MXFP8 experts, "xT", "xT_sf" (saved); "xs",
+ * "idx", "w", "counts", "offsets", "perm", "inv", "poff", "o", "GU", "s_GU",
+ * "s_h", with BF16 experts "h" and with MXFP8 experts "xT", "xT_sf", "hT",
+ * "hT_sf" (saved: column-blocked codes of the wgrad operands); "xs",
  * "xs_sf", "hq", "hq_sf", "s_out", "dX", "dGU", "g", "dOq", "dOq_sf", "dOT",
  * "dOT_sf" (workspace; "dO" exists only with BF16 experts, whose backward
  * materialises dO in bf16).  Row-indexed buffers use padded rows (see

@@ -112,10 +112,15 @@ void saved_layout(const Dims &D, Layout &L) {
   add_route(D, L);
   L.add("o", D.Rp * D.d * 2);
   L.add("GU", D.Rp * 2 * D.m * 2);
-  L.add("h", D.Rp * D.m * 2);
-  if (D.mx) {  // column-blocked codes of the gathered x (written by the dispatch)
+  if (D.mx) {
+    // column-blocked codes of the gathered x (written by the dispatch) and of
+    // h (written by the gate/up GEMM's epilogue): the wgrad operands
     L.add("xT", D.d * D.Rp);
     L.add("xT_sf", D.d * D.Rp / 32);
+    L.add("hT", D.m * D.Rp);
+    L.add("hT_sf", D.m * D.Rp / 32);
+  } else {
+    L.add("h", D.Rp * D.m * 2);
   }
   if (D.ms) {
     L.add("s_GU", D.Tp * 2 * D.ms * 2);
@@ -165,7 +170,7 @@ void ws_layout(const Dims &D, Layout &L) {
   L.add("dGU", D.Rp * 2 * D.m * 2);
   L.add("dX", D.Rp * D.d * 2);
   L.add("dOT", D.d * D.Rp * eb);
-  L.add("hT", D.m * D.Rp * eb);
+  if (!D.mx) L.add("hT", D.m * D.Rp * eb);  // MXFP8: kept in `saved` by the gate/up GEMM
   L.add("dGUT", 2 * D.m * D.Rp * eb);
   if (!D.mx) L.add("xT", D.d * D.Rp * eb);  // MXFP8: kept in `saved` by the dispatch
   if (D.mx) {
@@ -174,7 +179,6 @@ void ws_layout(const Dims &D, Layout &L) {
     L.add("dGUq", D.Rp * 2 * D.m);
     L.add("dGUq_sf", D.Rp * 2 * D.m / 32);
     L.add("dOT_sf", D.d * D.Rp / 32);
-    L.add("hT_sf", D.m * D.Rp / 32);
     L.add("dGUT_sf", 2 * D.m * D.Rp / 32);
   }
   if (D.ms) {
@@ -589,7 +593,7 @@ int moe_forward(const moe_config *cfg, const void *x, const float *logits, const
   }
   if (rc != MOE_OK) return rc;
   // S4 gate/up GEMM + SwiGLU (+ MX quantisation of h)
-  char *h_bf16 = train ? S.ptr(saved, "h") : (D.mx ? nullptr : W.ptr(ws, "h"));
+  char *h_bf16 = D.mx ? nullptr : (train ? S.ptr(saved, "h") : W.ptr(ws, "h"));
   char *GU = train ? S.ptr(saved, "GU") : nullptr;
   uint8_t *hq = reinterpret_cast<uint8_t *>(W.ptr(ws, "hq"));
   uint8_t *hq_sf = reinterpret_cast<uint8_t *>(W.ptr(ws, "hq_sf"));
@@ -620,6 +624,11 @@ int moe_forward(const moe_config *cfg, const void *x, const float *logits, const
     q.g.outq = D.mx ? hq : nullptr;
     q.g.outq_sf = hq_sf;
     q.g.ldq = D.m;
+    if (train && D.mx) {
+      q.g.outT = reinterpret_cast<uint8_t *>(S.ptr(saved, "hT"));
+      q.g.outT_sf = reinterpret_cast<uint8_t *>(S.ptr(saved, "hT_sf"));
+      q.g.ldT = D.Rp;
+    }
     q.g.m_half = D.m;
     if (D.starve) {
       q.g.debug_starve = 1;
@@ -842,7 +851,7 @@ int moe_backward(const moe_config *cfg, const void *dy, const void *x, const moe
     bool gather;
     const char *dst, *sf;
   } trs[] = {{mx ? nullptr : dO, D.d, false, "dOT", "dOT_sf"},  // MXFP8: written by B1
-             {h, D.m, false, "hT", "hT_sf"},
+             {mx ? nullptr : h, D.m, false, "hT", "hT_sf"},  // MXFP8: written by the gate/up GEMM
              {dGU, 2 * D.m, false, "dGUT", "dGUT_sf"},
              {mx ? nullptr : x, D.d, true, "xT", "xT_sf"}};  // MXFP8: written by the dispatch
   for (const Tr &t : trs) {
@@ -863,7 +872,7 @@ int moe_backward(const moe_config *cfg, const void *dy, const void *x, const moe
     q.epi = moe::EPI_STORE;
     q.a = W.ptr(ws, "dOT");
     q.a_rows = D.d;
-    q.b = W.ptr(ws, "hT");
+    q.b = mx ? S.ptr(saved, "hT") : W.ptr(ws, "hT");
     q.b_rows = D.m;
     q.K = D.Rp;
     q.g = base_args(moe::SCHED_GROUP_K, D.E, rb.poff, p.status);
@@ -871,7 +880,7 @@ int moe_backward(const moe_config *cfg, const void *dy, const void *x, const moe
     q.g.n_tiles = D.m / q.bn;
     q.g.sfa = u8("dOT_sf");
     q.g.sfa_kg = static_cast<int>(D.Rp / 128);
-    q.g.sfb = u8("hT_sf");
+    q.g.sfb = mx ? reinterpret_cast<uint8_t *>(S.ptr(saved, "hT_sf")) : nullptr;
     q.g.sfb_kg = static_cast<int>(D.Rp / 128);
     q.g.out = dW_dn;
     q.g.ldo = D.m;

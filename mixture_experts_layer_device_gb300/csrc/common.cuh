@@ -426,6 +426,19 @@ MOE_DEV void mx_encode32(const float *v, uint32_t byte, uint32_t *out8) {
   }
 }
 
+// 32 bytes to global memory at a 16-byte-aligned address: one 32-byte store
+// (a full sector) when the address allows it, else two 16-byte stores.
+MOE_DEV void st_global_32B(void *p, const uint32_t *w) {
+  if ((reinterpret_cast<uintptr_t>(p) & 31u) == 0) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]), "r"(w[1]),
+                 "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                 : "memory");
+  } else {
+    reinterpret_cast<uint4 *>(p)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    reinterpret_cast<uint4 *>(p)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  }
+}
+
 // Byte offset of the scale of (row r, 32-block b) in the tiled scale layout
 // of a matrix with reduction length K (both multiples of 128).
 __host__ __device__ __forceinline__ size_t sf_tiled_offset(long r, long b, long K) {

@@ -48,19 +48,6 @@ MOE_DEV int token_of_row(const RouteBufs &b, int E, int k, int pr, int *slot_out
   return slot / k;
 }
 
-// 32 bytes to global memory at a 16-byte-aligned address: one 32-byte store
-// (a full sector) when the address allows it, else two 16-byte stores.
-MOE_DEV void st_global_32B(void *p, const uint32_t *w) {
-  if ((reinterpret_cast<uintptr_t>(p) & 31u) == 0) {
-    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]), "r"(w[1]),
-                 "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
-                 : "memory");
-  } else {
-    reinterpret_cast<uint4 *>(p)[0] = make_uint4(w[0], w[1], w[2], w[3]);
-    reinterpret_cast<uint4 *>(p)[1] = make_uint4(w[4], w[5], w[6], w[7]);
-  }
-}
-
 // Column of element (r, c) in a 32 x 256 bf16 shared-memory tile: the 16-byte
 // chunks of rows 8 apart are swizzled (chunk index XOR (r / 8) % 4), so that
 // four threads reading one column at rows 0, 8, 16, 24 hit different banks,

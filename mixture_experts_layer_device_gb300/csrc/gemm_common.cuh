@@ -94,6 +94,39 @@ struct Stager {
     bf16x32_words(v32, w);
     put(o, w, c0, row0, lane);
   }
+  // Column-blocked MXFP8 codes of a 32 x 32 piece: each lane's 32 values (its
+  // row, columns c0 .. c0 + 31) are rounded to bf16 and staged; lane c then
+  // reads column c0 + c over the 32 rows (one 32-row block, rows row0 ..
+  // row0 + 31) and writes its 32 codes to row c0 + c of dT (row stride ldT)
+  // and the scale byte to the tiled scales dT_sf (K = ldT).
+  MOE_DEV void put_col_codes(const float *v32, uint8_t *dT, uint8_t *dT_sf, long ldT, int c0, int row0,
+                             int lane) {
+    uint32_t w[16];
+    bf16x32_words(v32, w);
+    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int jj = j ^ ((lane >> 1) & 3);
+      *reinterpret_cast<uint4 *>(buf + lane * 64 + jj * 16) =
+          make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+    }
+    __syncwarp();
+    float v[32];
+    float am = 0.f;
+#pragma unroll
+    for (int r = 0; r < 32; ++r) {
+      const uint16_t b = *reinterpret_cast<const uint16_t *>(
+          buf + r * 64 + (((lane >> 3) ^ ((r >> 1) & 3)) * 16) + (lane & 7) * 2);
+      v[r] = __uint_as_float(static_cast<uint32_t>(b) << 16);
+      am = fmaxf(am, fabsf(v[r]));
+    }
+    const uint32_t byte = mx_scale_byte(am);
+    uint32_t cw[8];
+    mx_encode32(v, byte, cw);
+    const long orow = static_cast<long>(c0) + lane;
+    st_global_32B(dT + orow * ldT + row0, cw);
+    dT_sf[sf_tiled_offset(orow, row0 / 32, ldT)] = static_cast<uint8_t>(byte);
+  }
 };
 
 // Two MX blocks (64 values) of one row -> one 64-byte codes piece + 2 scale bytes.
@@ -376,6 +409,10 @@ MOE_DEV void epilogue_tile_split(const GemmArgs &g, const OutView &vO, const Out
     if (g.out) {
       st.put_bf16(vO, G, col, row0, lane);
       st.put_bf16(vO, G + 32, col + 32, row0, lane);
+    }
+    if (g.outT) {  // the wgrad operand h^T, column-blocked, from the bf16 h
+      st.put_col_codes(G, g.outT, g.outT_sf, g.ldT, col, row0, lane);
+      st.put_col_codes(G + 32, g.outT, g.outT_sf, g.ldT, col + 32, row0, lane);
     }
     if (g.outq) put_mx64(st, vQ, g.outq_sf, g.ldq, G, col, row0, grow, lane);
   }

@@ -152,6 +152,9 @@ struct GemmArgs {
   uint8_t *outq;      // SWIGLU / SWIGLU_BWD MX codes (may be NULL)
   uint8_t *outq_sf;   // tiled scales of outq
   long ldq;           // row stride of outq (= its K)
+  uint8_t *outT;      // SWIGLU (MXFP8 training): column-blocked codes of h^T [m, ldT] (may be NULL)
+  uint8_t *outT_sf;   // tiled scales of outT (K = ldT)
+  long ldT;           // row stride of outT (padded rows)
   const void *aux;    // SWIGLU_BWD: saved G|U bf16
   long ld_aux;
   int m_half;         // SWIGLU / SWIGLU_BWD: m

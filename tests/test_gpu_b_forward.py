@@ -8,6 +8,7 @@ import torch
 
 import moe_inputs as mi
 from gpu_util import TOL, Case, padded_rows, rel, unpack_tiled_scales
+from oracle import moe as om
 from oracle import numerics as nx
 
 pytestmark = pytest.mark.gpu
@@ -31,6 +32,28 @@ def saved_rows(case, name, width, dtype="bf16"):
     return t.float().cpu().numpy().astype(np.float64)
 
 
+def check_saved_h(case, s, pr, tol):
+    """The h a training forward keeps for the backward: bf16 rows (BF16), or
+    for MXFP8 the column-blocked codes h^T [m, Rp] (blocks of 32 padded rows
+    of one expert), compared after decoding with the oracle's column-blocked
+    MX round trip of its own h, expert by expert."""
+    cfg, L = case.cfg, case.layer
+    m = cfg["m"]
+    if cfg["fmt"] == "bf16":
+        assert rel(saved_rows(case, "h", m)[pr], s["h"]) < tol
+        return
+    codes = L.view(0, "hT", "u8", (m, L.Rp)).cpu().numpy()
+    sf = unpack_tiled_scales(case.buffer(0, "hT_sf"), m, L.Rp)
+    h_gpu = nx.mx_dequantize(codes, sf, axis=1).T                  # [Rp, m]
+    ref = np.zeros_like(s["h"])
+    offs = s["offsets"]
+    for e in range(cfg["E"]):
+        r0, r1 = int(offs[e]), int(offs[e + 1])
+        if r1 > r0:
+            ref[r0:r1] = om._col_blocks(s["h"][r0:r1])
+    assert rel(h_gpu[pr], ref) < tol
+
+
 @pytest.mark.parametrize("fmt", ["bf16", "mxfp8"])
 def test_single_expert_ffn(fmt):
     """E = 1, k = 1: the layer is one SwiGLU FFN; checks GEMM1, SwiGLU and GEMM2 alone."""
@@ -42,6 +65,7 @@ def test_single_expert_ffn(fmt):
     assert list(poff) == [0, 256]
     pr = padded_rows(counts, offsets, poff)
     assert rel(saved_rows(c, "GU", 2 * cfg["m"])[pr], s["GU"]) < TOL[fmt] / 5, "gate/up GEMM"
+    check_saved_h(c, s, pr, TOL[fmt])
     assert rel(saved_rows(c, "o", cfg["d"])[pr], s["o"]) < TOL[fmt], "down GEMM"
     assert rel(y, y_ref) < TOL[fmt]
 
@@ -58,7 +82,7 @@ def test_forward_matches_oracle(name):
     pr = padded_rows(counts, offsets, poff)
     tol = TOL[cfg["fmt"]]
     assert rel(saved_rows(c, "GU", 2 * cfg["m"])[pr], s["GU"]) < tol
-    assert rel(saved_rows(c, "h", cfg["m"])[pr], s["h"]) < tol
+    check_saved_h(c, s, pr, tol)
     assert rel(saved_rows(c, "o", cfg["d"])[pr], s["o"]) < tol
     assert rel(y, y_ref) < tol
     # elementwise: no single output is far off (catches a wrong row or block)
