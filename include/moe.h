@@ -159,9 +159,10 @@ size_t moe_saved_bytes(const moe_config *cfg);
  * "idx", "w", "counts", "offsets", "perm", "inv", "poff", "o", "GU", "s_GU",
  * "s_h", with BF16 experts "h" and with MXFP8 experts "xT", "xT_sf", "hT",
  * "hT_sf" (saved: column-blocked codes of the wgrad operands); "xs",
- * "xs_sf", "hq", "hq_sf", "s_out", "dX", "dGU", "g", "dOq", "dOq_sf", "dOT",
- * "dOT_sf" (workspace; "dO" exists only with BF16 experts, whose backward
- * materialises dO in bf16).  Row-indexed buffers use padded rows (see
+ * "xs_sf", "hq", "hq_sf", "s_out", "dX", "g" and, with MXFP8 experts,
+ * "dOq", "dOq_sf", "dOT", "dOT_sf", "dGUq", "dGUq_sf", "dGUT", "dGUT_sf"
+ * (workspace; "dO" and "dGU" exist only with BF16 experts, whose backward
+ * materialises them in bf16).  Row-indexed buffers use padded rows (see
  * moe_forward).  Returns MOE_OK or MOE_ERR_ARG (unknown name / buffer absent
  * for this config). */
 int moe_buffer_info(const moe_config *cfg, int which, const char *name, size_t *offset,

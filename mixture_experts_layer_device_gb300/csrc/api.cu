@@ -167,7 +167,7 @@ void ws_layout(const Dims &D, Layout &L) {
   L.add("router_g", static_cast<size_t>(D.T) * D.E * 2);  // bf16 dlogits for the router backward
   L.add("g", D.R * 4);
   if (!D.mx) L.add("dO", D.Rp * D.d * 2);  // MXFP8 keeps dO only as codes
-  L.add("dGU", D.Rp * 2 * D.m * 2);
+  if (!D.mx) L.add("dGU", D.Rp * 2 * D.m * 2);  // MXFP8 keeps dGU only as codes
   L.add("dX", D.Rp * D.d * 2);
   L.add("dOT", D.d * D.Rp * eb);
   if (!D.mx) L.add("hT", D.m * D.Rp * eb);  // MXFP8: kept in `saved` by the gate/up GEMM
@@ -807,11 +807,18 @@ int moe_backward(const moe_config *cfg, const void *dy, const void *x, const moe
     q.g.sfa_kg = D.d / 128;
     q.g.sfb = static_cast<const uint8_t *>(Wt->dn_t_scale);
     q.g.sfb_kg = D.d / 128;
-    q.g.out = dGU;
+    // MXFP8: dGU only as codes, row-blocked (gate/up dgrad) and column-blocked
+    // (gate/up wgrad); BF16: dGU in bf16
+    q.g.out = mx ? nullptr : dGU;
     q.g.ldo = 2 * D.m;
     q.g.outq = mx ? u8("dGUq") : nullptr;
     q.g.outq_sf = u8("dGUq_sf");
     q.g.ldq = 2 * D.m;
+    if (mx) {
+      q.g.outT = u8("dGUT");
+      q.g.outT_sf = u8("dGUT_sf");
+      q.g.ldT = D.Rp;
+    }
     q.g.aux = GU;
     q.g.ld_aux = 2 * D.m;
     q.g.m_half = D.m;
@@ -852,7 +859,7 @@ int moe_backward(const moe_config *cfg, const void *dy, const void *x, const moe
     const char *dst, *sf;
   } trs[] = {{mx ? nullptr : dO, D.d, false, "dOT", "dOT_sf"},  // MXFP8: written by B1
              {mx ? nullptr : h, D.m, false, "hT", "hT_sf"},  // MXFP8: written by the gate/up GEMM
-             {dGU, 2 * D.m, false, "dGUT", "dGUT_sf"},
+             {mx ? nullptr : dGU, 2 * D.m, false, "dGUT", "dGUT_sf"},  // MXFP8: written by B2
              {mx ? nullptr : x, D.d, true, "xT", "xT_sf"}};  // MXFP8: written by the dispatch
   for (const Tr &t : trs) {
     if (!t.src) continue;

@@ -367,8 +367,14 @@ MOE_DEV void epilogue_tile_split(const GemmArgs &g, const OutView &vO, const Out
           G[i] = dg;
           U[i] = du;
         }
-        st.put_bf16(vO, G, col + 32 * hh, row0, lane);
-        st.put_bf16(vO, U, g.m_half + col + 32 * hh, row0, lane);
+        if (g.out) {
+          st.put_bf16(vO, G, col + 32 * hh, row0, lane);
+          st.put_bf16(vO, U, g.m_half + col + 32 * hh, row0, lane);
+        }
+        if (g.outT) {  // the gate/up wgrad operand dGU^T, column-blocked, from the bf16 dG, dU
+          st.put_col_codes(G, g.outT, g.outT_sf, g.ldT, col + 32 * hh, row0, lane);
+          st.put_col_codes(U, g.outT, g.outT_sf, g.ldT, g.m_half + col + 32 * hh, row0, lane);
+        }
         if (g.outq) {
           sg[hh] = mx_block_words(G, cg + 8 * hh);
           su[hh] = mx_block_words(U, cu + 8 * hh);

@@ -152,7 +152,8 @@ struct GemmArgs {
   uint8_t *outq;      // SWIGLU / SWIGLU_BWD MX codes (may be NULL)
   uint8_t *outq_sf;   // tiled scales of outq
   long ldq;           // row stride of outq (= its K)
-  uint8_t *outT;      // SWIGLU (MXFP8 training): column-blocked codes of h^T [m, ldT] (may be NULL)
+  uint8_t *outT;      // MXFP8 training, column-blocked codes (may be NULL): SWIGLU h^T [m, ldT],
+                      // SWIGLU_BWD dGU^T [2m, ldT]
   uint8_t *outT_sf;   // tiled scales of outT (K = ldT)
   long ldT;           // row stride of outT (padded rows)
   const void *aux;    // SWIGLU_BWD: saved G|U bf16
