@@ -133,6 +133,24 @@ def output_bytes(cfg, name):
     return {"wgrad_gate_up": E * 2 * m * d * 2, "wgrad_down": E * d * m * 2}.get(name)
 
 
+def kernels_in_region(name, cfg, train):
+    """Kernel launches inside one traced region of the library: route + the
+    three schedule kernels; with MXFP8 experts the dispatch and the reverse
+    combine also run the one-block tile-order sort first, and an inference
+    dispatch quantises every token once before it; the balance term is a
+    partial and a finishing kernel."""
+    mx = cfg["fmt"] == "mxfp8"
+    if name == "route_schedule":
+        return 4
+    if name == "dispatch_gather" and mx:
+        return 2 if train else 3
+    if name in ("reverse_combine", "dispatch_xT") and mx:
+        return 2
+    if name == "balance_loss":
+        return 2
+    return 1
+
+
 def write_probe_gbs(dev):
     """Write-only HBM bandwidth of this GPU: a device fill of 8 GB (taken
     before the timed region; context for write-dominated kernels).  The fill
@@ -543,7 +561,7 @@ def run_ours(args, cfg, passes, rank, world, local_rank):
     for name, ms in recs:
         c, t = per.get(name, (0, 0.0))
         per[name] = (c + 1, t + ms)
-        launches += 4 if name == "route_schedule" else 1
+        launches += kernels_in_region(name, cfg, bwd)
     kernel_total = sum(t for _, t in per.values()) or 1.0
     dom = max(per.items(), key=lambda kv: kv[1][1])[0]
     cnt, tot = per[dom]
