@@ -124,3 +124,27 @@ def test_forward_bitwise_deterministic(name):
     pr = torch.as_tensor(padded_rows(counts, offsets, poff), device="cuda")
     o3 = c.layer.view(0, "o", "bf16", (c.layer.Rp, cfg["d"]))
     assert torch.equal(o1[pr].view(torch.int16), o3[pr].view(torch.int16))
+
+
+@pytest.mark.parametrize("name", ["kimi-k2.7", "deepseek-v4-pro"])
+def test_tile_order_is_a_token_sorted_permutation(name):
+    """The MXFP8 dispatch takes its 32-row tiles in the order of their first
+    row's token ("tile_order" in the workspace): a permutation of the tiles
+    whose token buckets (1,024 over T) never decrease, all-padding tiles last.
+    It is a processing order only; the outputs are checked by the parity tests."""
+    cfg = small(name)
+    c = Case(cfg, backward=False)
+    run_forward(c, train=False)
+    counts, offsets, poff, inv = c.route_views(1)
+    T, k = cfg["T"], cfg["k"]
+    ntiles = int(poff[-1]) // 32
+    order = np.frombuffer(c.buffer(1, "tile_order").tobytes(), dtype=np.int32)[:ntiles]
+    assert np.array_equal(np.sort(order), np.arange(ntiles))
+    tok = np.full(ntiles, -1)                      # token of each tile's first row, -1: padding
+    for e in range(cfg["E"]):
+        for t in range(int(poff[e]) // 32, int(poff[e + 1]) // 32):
+            local = t * 32 - int(poff[e])
+            if local < counts[e]:
+                tok[t] = inv[offsets[e] + local] // k
+    key = np.where(tok < 0, 1023, tok * 1024 // T)
+    assert np.all(np.diff(key[order]) >= 0)
