@@ -133,6 +133,25 @@ def output_bytes(cfg, name):
     return {"wgrad_gate_up": E * 2 * m * d * 2, "wgrad_down": E * d * m * 2}.get(name)
 
 
+def max_over_ranks(ms, world, device):
+    """The slowest rank's time; every rank receives it (replicas are timed by
+    the last one to finish)."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(tokens_per_rank, world, steps, total_ms):
+    """Whole-job tokens/s of `world` independent replicas that each processed
+    tokens_per_rank tokens per step for `steps` steps in total_ms (the max over
+    ranks): weak scaling, every rank's tokens count."""
+    return tokens_per_rank * world * steps / (total_ms / 1e3)
+
+
 def kernels_in_region(name, cfg, train):
     """Kernel launches inside one traced region of the library: route + the
     three schedule kernels; with MXFP8 experts the dispatch and the reverse
@@ -414,10 +433,7 @@ def run_ours(args, cfg, passes, rank, world, local_rank):
         recs = pkg.moe_trace_records() if trace else []
         if trace:
             pkg.moe_trace_enable(0)
-        if world > 1:
-            t = torch.tensor([ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms = float(t.item())
+        ms = max_over_ranks(ms, world, dev)
         return ms, recs
 
     write_gbs = write_probe_gbs(dev)
@@ -433,7 +449,7 @@ def run_ours(args, cfg, passes, rank, world, local_rank):
         _, recs = timed(step, args.steps, trace=True)
     ms_step = total_ms / args.steps
     tokens = cfg["T"] * world
-    value = tokens * args.steps / (total_ms / 1e3)
+    value = replica_throughput(cfg["T"], world, args.steps, total_ms)
 
     fwd_value = value
     if args.profile_run:      # one timed region only (keeps profiler launch lists short)
