@@ -316,24 +316,21 @@ MOE_DEV void epilogue_tile_split(const GemmArgs &g, const OutView &vO, const Out
       }
       return;
     }
-    uint32_t pk[NC / 2];
-    uint32_t buf[2][32];
-    tmem_ld32_async(tb + c0, buf[0]);
-    tmem_ld_wait();
-    reg_fence<32>(buf[0]);
+    // All of this warp's columns are read with back-to-back TMEM loads and one
+    // wait, TMEM is released, and only then are they packed (in place) and
+    // stored: the next tile's MMAs wait only for the loads.
+    uint32_t raw[NC];
 #pragma unroll
-    for (int c = 0; c < NC32; ++c) {
-      if (c + 1 < NC32) tmem_ld32_async(tb + c0 + 32 * (c + 1), buf[(c + 1) & 1]);
-      bf16x32_words(reinterpret_cast<const float *>(buf[c & 1]), pk + 16 * c);
-      if (c + 1 < NC32) {
-        tmem_ld_wait();
-        reg_fence<32>(buf[(c + 1) & 1]);
-      }
-    }
+    for (int c = 0; c < NC32; ++c) tmem_ld32_async(tb + c0 + 32 * c, raw + 32 * c);
+    tmem_ld_wait();
+    reg_fence<NC>(raw);
     release();
+#pragma unroll
+    for (int i = 0; i < NC / 2; ++i)
+      raw[i] = pack_bf16x2(__uint_as_float(raw[2 * i]), __uint_as_float(raw[2 * i + 1]));
     if (store) {
 #pragma unroll
-      for (int c = 0; c < NC32; ++c) st.put(vO, pk + 16 * c, out_col + c0 + 32 * c, row0, lane);
+      for (int c = 0; c < NC32; ++c) st.put(vO, raw + 16 * c, out_col + c0 + 32 * c, row0, lane);
     }
   } else if constexpr (EPI == EPI_SWIGLU_BWD) {
     // This warp's BN/2 dh columns, 64 at a time: each chunk is read from TMEM,
