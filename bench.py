@@ -38,7 +38,11 @@ MX_OVER_BF16 = 2.0   # nominal dense MXFP8 : BF16 tensor-core ratio (4.5 : 2.25 
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from the
 # ncu capture summarised in profiles/, keyed by (workload, kernel).  An entry is
 # removed whenever the kernel changes after the capture.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    # profiles/dram_traffic_dominant_kernels.md (full-size launches, one-pass capture)
+    ("kimi-k2.7", "wgrad_gate_up"): 5_097_356_800 + 22_494_661_120,
+    ("deepseek-v4-pro", "gemm1_gate_up_swiglu"): 20_051_618_816 + 694_565_632,
+}
 
 
 # ----------------------------------------------------------------------------- helpers
