@@ -590,23 +590,24 @@ __global__ void __launch_bounds__(256) reverse_dispatch_kernel(
 }
 
 // ------------------------------------------------------------ transposes
-// Block: 32 source rows x 256 columns, loaded up front (four 16-byte loads per
-// thread) into a bf16 shared-memory tile; after one barrier the output rows
+// Block: 32 source rows x CH chunks of 256 columns, loaded up front (four
+// 16-byte loads per thread and chunk) into bf16 shared-memory tiles; after one
+// barrier the output rows
 // (source columns) are written: for MX thread c owns output row c, one
 // 32-value block, and writes its 32 codes plus the scale byte; bf16 output
 // rows are written 64 bytes at a time by 4 threads each.
 // ROWQ (MX, weights): the tile's source rows are also quantised along C into
 // row-blocked codes rq [batch * nrows, C] with tiled scales (K = C), so one
 // read of the bf16 source gives both operand orientations.
-template <bool MX, bool GATHER, bool ROWQ = false>
+template <bool MX, bool GATHER, bool ROWQ = false, int CH = 1>
 __global__ void __launch_bounds__(256) transpose_rows_kernel(
     const uint16_t *__restrict__ src, long src_batch_stride, int C, int nrows_host,
     const int *__restrict__ nrows_dev, long nsrc, int k, int E, RouteBufs b, void *dst,
     long dst_batch_stride, uint8_t *__restrict__ dst_sf, long sf_batch_rows, long ld_dst,
     uint8_t *__restrict__ rq = nullptr, uint8_t *__restrict__ rq_sf = nullptr) {
-  __shared__ __align__(16) uint16_t tile[32][256];
+  __shared__ __align__(16) uint16_t tile[CH][32][256];
   const int r0 = blockIdx.x * 32;
-  const int cb = blockIdx.y * 256;
+  const int cb0 = blockIdx.y * 256 * CH;
   const int bz = blockIdx.z;
   const int nrows = nrows_dev ? __ldg(nrows_dev) : nrows_host;
   if (r0 >= nrows) return;
@@ -618,48 +619,60 @@ __global__ void __launch_bounds__(256) transpose_rows_kernel(
   long srow = r;
   if constexpr (GATHER) srow = token_of_row(b, E, k, r, nullptr);
   const bool valid = srow >= 0 && srow < nsrc;
-  const int nsub = min(4, (C - cb) / 64);
-  uint4 q[4];
+  int nsub[CH];
 #pragma unroll
-  for (int j = 0; j < 4; ++j)
-    q[j] = (valid && j < nsub)
-               ? __ldg(reinterpret_cast<const uint4 *>(src + static_cast<size_t>(srow) * C + cb + 64 * j + cc))
-               : make_uint4(0, 0, 0, 0);
+  for (int h = 0; h < CH; ++h) nsub[h] = max(0, min(4, (C - cb0 - 256 * h) / 64));
+  uint4 q[CH][4];
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    if (j >= nsub) break;
-    if constexpr (ROWQ) {
-      float f[8];
-      unpack8(q[j], f);
-      const long qrow = static_cast<long>(bz) * nrows + r;
-      const int col = cb + 64 * j + cc;
-      uint32_t byte;
-      const uint2 code = mx_encode8_quad(f, &byte);
-      *reinterpret_cast<uint2 *>(rq + static_cast<size_t>(qrow) * C + col) = code;
-      if ((tid & 3) == 0) rq_sf[sf_tiled_offset(qrow, col >> 5, C)] = static_cast<uint8_t>(byte);
+  for (int h = 0; h < CH; ++h)
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      q[h][j] = (valid && j < nsub[h])
+                    ? __ldg(reinterpret_cast<const uint4 *>(src + static_cast<size_t>(srow) * C + cb0 + 256 * h +
+                                                            64 * j + cc))
+                    : make_uint4(0, 0, 0, 0);
+#pragma unroll
+  for (int h = 0; h < CH; ++h) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (j >= nsub[h]) break;
+      if constexpr (ROWQ) {
+        float f[8];
+        unpack8(q[h][j], f);
+        const long qrow = static_cast<long>(bz) * nrows + r;
+        const int col = cb0 + 256 * h + 64 * j + cc;
+        uint32_t byte;
+        const uint2 code = mx_encode8_quad(f, &byte);
+        *reinterpret_cast<uint2 *>(rq + static_cast<size_t>(qrow) * C + col) = code;
+        if ((tid & 3) == 0) rq_sf[sf_tiled_offset(qrow, col >> 5, C)] = static_cast<uint8_t>(byte);
+      }
+      *reinterpret_cast<uint4 *>(&tile[h][rr][tcol(rr, 64 * j + cc)]) = q[h][j];
     }
-    *reinterpret_cast<uint4 *>(&tile[rr][tcol(rr, 64 * j + cc)]) = q[j];
   }
   __syncthreads();
-  if constexpr (MX) {
-    // thread c: source column cb + c = output row cb + c, one 32-value block
-    if (tid < 64 * nsub)
-      column_block_codes(tile, tid, cb, r0,
-                         reinterpret_cast<uint8_t *>(dst) + static_cast<size_t>(bz) * dst_batch_stride, dst_sf,
-                         ld_dst, static_cast<long>(bz) * sf_batch_rows);
-  } else {
-    // 4 threads per output row (8 source rows each), 64 output rows per round:
-    // a warp writes 8 output rows x 64 contiguous bytes per instruction
-    const int c = tid >> 2, part = tid & 3;
-    uint16_t *o = reinterpret_cast<uint16_t *>(dst) + static_cast<size_t>(bz) * dst_batch_stride + r0 + part * 8;
-    for (int j = 0; j < nsub; ++j) {
-      const int col = 64 * j + c;
-      uint32_t w[4];
 #pragma unroll
-      for (int h = 0; h < 4; ++h)
-        w[h] = static_cast<uint32_t>(tile[part * 8 + 2 * h][tcol(part * 8 + 2 * h, col)]) |
-               (static_cast<uint32_t>(tile[part * 8 + 2 * h + 1][tcol(part * 8 + 2 * h + 1, col)]) << 16);
-      *reinterpret_cast<uint4 *>(o + static_cast<size_t>(cb + col) * ld_dst) = make_uint4(w[0], w[1], w[2], w[3]);
+  for (int h = 0; h < CH; ++h) {
+    const int cb = cb0 + 256 * h;
+    if constexpr (MX) {
+      // thread c: source column cb + c = output row cb + c, one 32-value block
+      if (tid < 64 * nsub[h])
+        column_block_codes(tile[h], tid, cb, r0,
+                           reinterpret_cast<uint8_t *>(dst) + static_cast<size_t>(bz) * dst_batch_stride, dst_sf,
+                           ld_dst, static_cast<long>(bz) * sf_batch_rows);
+    } else {
+      // 4 threads per output row (8 source rows each), 64 output rows per round:
+      // a warp writes 8 output rows x 64 contiguous bytes per instruction
+      const int c = tid >> 2, part = tid & 3;
+      uint16_t *o = reinterpret_cast<uint16_t *>(dst) + static_cast<size_t>(bz) * dst_batch_stride + r0 + part * 8;
+      for (int j = 0; j < nsub[h]; ++j) {
+        const int col = 64 * j + c;
+        uint32_t w[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t)
+          w[t] = static_cast<uint32_t>(tile[h][part * 8 + 2 * t][tcol(part * 8 + 2 * t, col)]) |
+                 (static_cast<uint32_t>(tile[h][part * 8 + 2 * t + 1][tcol(part * 8 + 2 * t + 1, col)]) << 16);
+        *reinterpret_cast<uint4 *>(o + static_cast<size_t>(cb + col) * ld_dst) = make_uint4(w[0], w[1], w[2], w[3]);
+      }
     }
   }
 }
@@ -852,10 +865,18 @@ cudaError_t launch_to_bf16(const float *src, long n, void *dst, cudaStream_t s) 
 
 cudaError_t launch_quantize_mx_both(const void *src, int batch, int rows, int cols, uint8_t *codes,
                                     uint8_t *scales, uint8_t *codes_t, uint8_t *scales_t, cudaStream_t s) {
-  const dim3 grid(blocks_for(rows, 32), blocks_for(cols, 256), batch);
-  transpose_rows_kernel<true, false, true><<<grid, 256, 0, s>>>(
-      static_cast<const uint16_t *>(src), static_cast<long>(rows) * cols, cols, rows, nullptr, rows, 1, 1,
-      RouteBufs{}, codes_t, static_cast<long>(rows) * cols, scales_t, cols, rows, codes, scales);
+  // two 256-column chunks per block (twice the loads in flight) when they tile cols
+  if (cols % 512 == 0) {
+    const dim3 grid(blocks_for(rows, 32), blocks_for(cols, 512), batch);
+    transpose_rows_kernel<true, false, true, 2><<<grid, 256, 0, s>>>(
+        static_cast<const uint16_t *>(src), static_cast<long>(rows) * cols, cols, rows, nullptr, rows, 1, 1,
+        RouteBufs{}, codes_t, static_cast<long>(rows) * cols, scales_t, cols, rows, codes, scales);
+  } else {
+    const dim3 grid(blocks_for(rows, 32), blocks_for(cols, 256), batch);
+    transpose_rows_kernel<true, false, true><<<grid, 256, 0, s>>>(
+        static_cast<const uint16_t *>(src), static_cast<long>(rows) * cols, cols, rows, nullptr, rows, 1, 1,
+        RouteBufs{}, codes_t, static_cast<long>(rows) * cols, scales_t, cols, rows, codes, scales);
+  }
   return cudaGetLastError();
 }
 
