@@ -781,8 +781,7 @@ int moe_backward(const moe_config *cfg, const void *dy, const void *x, const moe
       rc = cuda_status(moe::launch_reverse_combine_mx(dy, o, D.T, D.d, D.k, D.E, rb, D.Rp, g, u8("dOq"),
                                                       u8("dOq_sf"), u8("dOT"), u8("dOT_sf"), s));
     else
-      rc = cuda_status(moe::launch_reverse_combine(dy, o, D.T, D.d, D.k, D.E, rb, D.Rp, dO, g, mx,
-                                                   u8("dOq"), u8("dOq_sf"), s));
+      rc = cuda_status(moe::launch_reverse_combine(dy, o, D.T, D.d, D.k, D.E, rb, D.Rp, dO, g, s));
   }
   if (rc != MOE_OK) return rc;
   // B2 dgrad of the down projection with the SwiGLU backward in the epilogue
@@ -851,23 +850,22 @@ int moe_backward(const moe_config *cfg, const void *dy, const void *x, const moe
     q.out_rows = D.Rp;
     if ((rc = run_gemm("dgrad_gate_up", q, dev, s)) != MOE_OK) return rc;
   }
-  // Transposed (column-blocked for MX) wgrad operands, K = padded rows.
+  // Transposed bf16 wgrad operands of BF16 experts, K = padded rows.  With
+  // MXFP8 experts their column-blocked codes were written by the kernels that
+  // produced them: x^T by the dispatch, h^T by the gate/up GEMM, dO^T by B1,
+  // dGU^T by B2.
   struct Tr {
     const void *src;
     int C;
     bool gather;
-    const char *dst, *sf;
-  } trs[] = {{mx ? nullptr : dO, D.d, false, "dOT", "dOT_sf"},  // MXFP8: written by B1
-             {mx ? nullptr : h, D.m, false, "hT", "hT_sf"},  // MXFP8: written by the gate/up GEMM
-             {mx ? nullptr : dGU, 2 * D.m, false, "dGUT", "dGUT_sf"},  // MXFP8: written by B2
-             {mx ? nullptr : x, D.d, true, "xT", "xT_sf"}};  // MXFP8: written by the dispatch
+    const char *dst;
+  } trs[] = {{dO, D.d, false, "dOT"}, {h, D.m, false, "hT"}, {dGU, 2 * D.m, false, "dGUT"}, {x, D.d, true, "xT"}};
   for (const Tr &t : trs) {
-    if (!t.src) continue;
+    if (mx) break;
     {
       Traced tr("transpose_wgrad_operands", s);
       rc = cuda_status(moe::launch_transpose_rows(t.src, t.C, 0, nrows_dev, D.Rp, t.gather, D.k, D.E,
-                                                  &rb, D.Rp, mx, W.ptr(ws, t.dst), u8(t.sf), D.Rp,
-                                                  s));
+                                                  &rb, D.Rp, W.ptr(ws, t.dst), D.Rp, s));
     }
     if (rc != MOE_OK) return rc;
   }
@@ -984,8 +982,8 @@ int moe_backward(const moe_config *cfg, const void *dy, const void *x, const moe
       {
         Traced tr("shared_transpose_wgrad_operands", s);
         rc = cuda_status(moe::launch_transpose_rows(t.src, t.C, static_cast<int>(D.Tp), nullptr,
-                                                    t.nsrc, false, D.k, D.E, nullptr, D.Tp, false,
-                                                    W.ptr(ws, t.dst), nullptr, D.Tp, s));
+                                                    t.nsrc, false, D.k, D.E, nullptr, D.Tp,
+                                                    W.ptr(ws, t.dst), D.Tp, s));
       }
       if (rc != MOE_OK) return rc;
     }

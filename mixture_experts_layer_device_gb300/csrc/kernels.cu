@@ -321,12 +321,10 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint4 *__restrict__ 
   }
 }
 
-// ------------------------------------------------------------ B1: reverse combine
-template <bool MX>
+// ------------------------------------------------------------ B1: reverse combine (BF16 experts)
 __global__ void __launch_bounds__(256) reverse_combine_kernel(
     const uint4 *__restrict__ dy, const uint4 *__restrict__ o, int d, int k, int E, RouteBufs b,
-    int64_t rp_max, uint4 *__restrict__ dO, float *__restrict__ g, uint8_t *__restrict__ dOq,
-    uint8_t *__restrict__ dOq_sf) {
+    int64_t rp_max, uint4 *__restrict__ dO, float *__restrict__ g) {
   const int64_t pr = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (pr >= rp_max || pr >= __ldg(b.poff + E)) return;
@@ -351,12 +349,6 @@ __global__ void __launch_bounds__(256) reverse_combine_kernel(
       for (int q = 0; q < 8; ++q) f[q] = 0.f;
     }
     dO[static_cast<size_t>(pr) * vec + i] = pack8(f);
-    if constexpr (MX) {
-      uint32_t byte;
-      const uint2 c = mx_encode8_quad(f, &byte);
-      reinterpret_cast<uint2 *>(dOq)[static_cast<size_t>(pr) * vec + i] = c;
-      if ((lane & 3) == 0) dOq_sf[sf_tiled_offset(pr, i >> 2, d)] = static_cast<uint8_t>(byte);
-    }
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
@@ -763,18 +755,11 @@ cudaError_t launch_combine(const void *o, const void *s_out, int T, int d, int k
 }
 
 cudaError_t launch_reverse_combine(const void *dy, const void *o, int T, int d, int k, int E,
-                                   const RouteBufs &b, int64_t rp_max, void *dO, float *g,
-                                   bool mx, uint8_t *dOq, uint8_t *dOq_sf, cudaStream_t s) {
+                                   const RouteBufs &b, int64_t rp_max, void *dO, float *g, cudaStream_t s) {
   (void)T;
-  const unsigned grid = blocks_for(rp_max, 8);
-  if (mx)
-    reverse_combine_kernel<true><<<grid, 256, 0, s>>>(
-        static_cast<const uint4 *>(dy), static_cast<const uint4 *>(o), d, k, E, b, rp_max,
-        static_cast<uint4 *>(dO), g, dOq, dOq_sf);
-  else
-    reverse_combine_kernel<false><<<grid, 256, 0, s>>>(
-        static_cast<const uint4 *>(dy), static_cast<const uint4 *>(o), d, k, E, b, rp_max,
-        static_cast<uint4 *>(dO), g, dOq, dOq_sf);
+  reverse_combine_kernel<<<blocks_for(rp_max, 8), 256, 0, s>>>(static_cast<const uint4 *>(dy),
+                                                               static_cast<const uint4 *>(o), d, k, E, b, rp_max,
+                                                               static_cast<uint4 *>(dO), g);
   return cudaGetLastError();
 }
 
@@ -799,27 +784,17 @@ cudaError_t launch_reverse_dispatch(const void *dX, const void *dxs, const float
 
 cudaError_t launch_transpose_rows(const void *src, int C, int nrows_out, const int *nrows_dev,
                                   long nsrc, bool gather, int k, int E, const RouteBufs *b,
-                                  int64_t rows_alloc, bool mx, void *dst, uint8_t *dst_sf,
-                                  int64_t ld_dst, cudaStream_t s) {
+                                  int64_t rows_alloc, void *dst, int64_t ld_dst, cudaStream_t s) {
   const dim3 grid(blocks_for(rows_alloc, 32), blocks_for(C, 256), 1);
   const RouteBufs bb = b ? *b : RouteBufs{};
   const uint16_t *sp = static_cast<const uint16_t *>(src);
   const long ns = gather ? (1L << 40) : nsrc;
-  if (mx) {
-    if (gather)
-      transpose_rows_kernel<true, true><<<grid, 256, 0, s>>>(sp, 0, C, nrows_out, nrows_dev, ns, k, E,
-                                                             bb, dst, 0, dst_sf, 0, ld_dst);
-    else
-      transpose_rows_kernel<true, false><<<grid, 256, 0, s>>>(sp, 0, C, nrows_out, nrows_dev, ns, k, E,
-                                                              bb, dst, 0, dst_sf, 0, ld_dst);
-  } else {
-    if (gather)
-      transpose_rows_kernel<false, true><<<grid, 256, 0, s>>>(sp, 0, C, nrows_out, nrows_dev, ns, k, E,
-                                                              bb, dst, 0, dst_sf, 0, ld_dst);
-    else
-      transpose_rows_kernel<false, false><<<grid, 256, 0, s>>>(sp, 0, C, nrows_out, nrows_dev, ns, k,
-                                                               E, bb, dst, 0, dst_sf, 0, ld_dst);
-  }
+  if (gather)
+    transpose_rows_kernel<false, true><<<grid, 256, 0, s>>>(sp, 0, C, nrows_out, nrows_dev, ns, k, E, bb, dst,
+                                                            0, nullptr, 0, ld_dst);
+  else
+    transpose_rows_kernel<false, false><<<grid, 256, 0, s>>>(sp, 0, C, nrows_out, nrows_dev, ns, k, E, bb, dst,
+                                                             0, nullptr, 0, ld_dst);
   return cudaGetLastError();
 }
 

@@ -47,11 +47,10 @@ cudaError_t launch_gather(const void *x, int T, int d, int k, int E, const Route
 cudaError_t launch_combine(const void *o, const void *s_out, int T, int d, int k, int E,
                            const RouteBufs &b, void *y, cudaStream_t s);
 
-// Reverse combine: dO[row] = bf16(w * dy[t]) (zero on padding rows), g[slot] =
-// <dy[t], o[row]>; MX: dO also row-quantised along d into codes + tiled scales.
+// Reverse combine, BF16 experts: dO[row] = bf16(w * dy[t]) (zero on padding
+// rows), g[slot] = <dy[t], o[row]>.
 cudaError_t launch_reverse_combine(const void *dy, const void *o, int T, int d, int k, int E,
-                                   const RouteBufs &b, int64_t rp_max, void *dO, float *g,
-                                   bool mx, uint8_t *dOq, uint8_t *dOq_sf, cudaStream_t s);
+                                   const RouteBufs &b, int64_t rp_max, void *dO, float *g, cudaStream_t s);
 
 // Reverse combine, MXFP8, fused with the wgrad operand: g[slot] = <dy[t], o[row]>,
 // dO = bf16(w * dy) written as row-blocked codes dOq [Rp, d] (+ tiled scales,
@@ -71,13 +70,11 @@ cudaError_t launch_reverse_dispatch(const void *dX, const void *dxs, const float
 // dst[c][r] = src[row(r)][c] for r < nrows (device count *nrows_dev when not
 // NULL, else nrows_out, a multiple of 32).  With `gather`, row(r) is the token
 // of padded expert row r (x re-gathered; -1 on padding rows), else row(r) = r;
-// rows with row(r) < 0 or row(r) >= nsrc read as zero.  bf16 output, or (mx)
-// E4M3 codes quantised in blocks of 32 along r with tiled scales
-// (K = ld_dst).  Rows beyond nrows are not written.
+// rows with row(r) < 0 or row(r) >= nsrc read as zero.  bf16 output (the BF16
+// wgrad operands; MXFP8 ones are written by the kernels that produce them).
 cudaError_t launch_transpose_rows(const void *src, int C, int nrows_out, const int *nrows_dev,
                                   long nsrc, bool gather, int k, int E, const RouteBufs *b,
-                                  int64_t rows_alloc, bool mx, void *dst, uint8_t *dst_sf,
-                                  int64_t ld_dst, cudaStream_t s);
+                                  int64_t rows_alloc, void *dst, int64_t ld_dst, cudaStream_t s);
 
 // Weight preparation.
 cudaError_t launch_quantize_mx(const void *src, int batch, int rows, int cols, bool transpose,
