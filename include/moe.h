@@ -186,6 +186,20 @@ int64_t moe_padded_rows(const moe_config *cfg);
 int moe_quantize_mx(const void *src, int batch, int rows, int cols, int transpose, void *codes,
                     void *scales, moe_stream_t stream);
 
+/* S0 in the layer's own terms: the MXFP8 codes of the layer's stacked expert
+ * weights, one bf16 master matrix [rows, cols] per expert (cfg->E of them,
+ * back to back at w_bf16).
+ *   blocks_along_rows = 0: the forward operand, blocks of 32 along cols
+ *     (W_gu [E*2m, d] with rows = 2m, cols = d; W_dn [E*d, m]): as
+ *     moe_quantize_mx(w_bf16, cfg->E, rows, cols, 0, ...).
+ *   blocks_along_rows = 1: the backward operand, each expert's matrix
+ *     transposed and quantised in blocks of 32 along its rows (W_gu^T
+ *     [E*d, 2m], W_dn^T [E*m, d]): as moe_quantize_mx(..., 1, ...).
+ * cfg must be a valid MXFP8 config (MOE_ERR_ARG otherwise); rows and cols
+ * multiples of 128; inputs finite.  Asynchronous on `stream`. */
+int moe_quantize_weights(const moe_config *cfg, const void *w_bf16, int rows, int cols, int blocks_along_rows,
+                         void *codes, void *scales, moe_stream_t stream);
+
 /* S0 for a training layer: both orientations from one read of the bf16
  * masters.  codes/scales exactly as moe_quantize_mx(transpose = 0) and
  * codes_t/scales_t exactly as moe_quantize_mx(transpose = 1) would write them

@@ -35,7 +35,8 @@ class MoeWeights(ctypes.Structure):
 
 _lib = None
 EXPORTS = ["moe_workspace_bytes", "moe_saved_bytes", "moe_buffer_info", "moe_padded_rows",
-           "moe_quantize_mx", "moe_quantize_mx_both", "moe_transpose_bf16", "moe_route", "moe_forward", "moe_backward",
+           "moe_quantize_weights", "moe_quantize_mx", "moe_quantize_mx_both", "moe_transpose_bf16", "moe_route",
+           "moe_forward", "moe_backward",
            "moe_get_status", "moe_status_string", "moe_trace_enable", "moe_trace_clear", "moe_trace_count",
            "moe_trace_name", "moe_trace_ms", "moe_route_noalloc", "moe_router_forward", "moe_router_backward"]
 
@@ -55,6 +56,7 @@ def lib():
         L.moe_buffer_info.argtypes = [cfgp, I, ctypes.c_char_p, ctypes.POINTER(Z), ctypes.POINTER(Z)]
         L.moe_buffer_info.restype = I
         L.moe_padded_rows.argtypes, L.moe_padded_rows.restype = [cfgp], ctypes.c_int64
+        L.moe_quantize_weights.argtypes, L.moe_quantize_weights.restype = [cfgp, P, I, I, I, P, P, S], I
         L.moe_quantize_mx.argtypes, L.moe_quantize_mx.restype = [P, I, I, I, I, P, P, S], I
         L.moe_quantize_mx_both.argtypes, L.moe_quantize_mx_both.restype = [P, I, I, I, P, P, P, P, S], I
         L.moe_transpose_bf16.argtypes, L.moe_transpose_bf16.restype = [P, I, I, I, P, S], I
@@ -144,6 +146,11 @@ def moe_buffer_info(cfg, which, name):
 def moe_quantize_mx_both(src, batch, rows, cols, codes, scales, codes_t, scales_t, stream=None):
     return lib().moe_quantize_mx_both(_ptr(src), batch, rows, cols, _ptr(codes), _ptr(scales), _ptr(codes_t),
                                       _ptr(scales_t), _stream(stream))
+
+
+def moe_quantize_weights(cfg, w_bf16, rows, cols, blocks_along_rows, codes, scales, stream=None):
+    return lib().moe_quantize_weights(ctypes.byref(cfg), _ptr(w_bf16), rows, cols, int(blocks_along_rows),
+                                      _ptr(codes), _ptr(scales), _stream(stream))
 
 
 def moe_quantize_mx(src, batch, rows, cols, transpose, codes, scales, stream=None):

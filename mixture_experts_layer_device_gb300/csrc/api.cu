@@ -474,6 +474,15 @@ int moe_quantize_mx(const void *src, int batch, int rows, int cols, int transpos
                                              static_cast<uint8_t *>(scales), stream));
 }
 
+int moe_quantize_weights(const moe_config *cfg, const void *w_bf16, int rows, int cols, int blocks_along_rows,
+                         void *codes, void *scales, moe_stream_t stream) {
+  Dims D;
+  const int rc = check_config(cfg, &D);
+  if (rc != MOE_OK) return rc;
+  if (!D.mx) return MOE_ERR_ARG;
+  return moe_quantize_mx(w_bf16, cfg->E, rows, cols, blocks_along_rows != 0, codes, scales, stream);
+}
+
 int moe_quantize_mx_both(const void *src, int batch, int rows, int cols, void *codes, void *scales,
                          void *codes_t, void *scales_t, moe_stream_t stream) {
   if (!src || !codes || !scales || !codes_t || !scales_t || batch <= 0 || rows <= 0 || cols <= 0)

@@ -82,6 +82,12 @@ def test_null_and_misaligned_pointers_rejected_on_host(pkg):
     assert pkg.moe_forward(cfg, 1 << 12, 1 << 12, W, 1 << 12, None, (1 << 12) + 4, 0) == -3
     assert pkg.moe_quantize_mx(16, 1, 100, 128, 0, 16, 16, 0) == -2
     assert pkg.moe_quantize_mx(8, 1, 128, 128, 0, 16, 16, 0) == -3
+    # the layer-level weight entry: MXFP8 configs only, then the same checks
+    mx = pkg.config(64, 256, 128, 8, 2, 0, "mxfp8")
+    assert pkg.moe_quantize_weights(cfg, 16, 256, 256, 0, 16, 16, 0) == -1
+    assert pkg.moe_quantize_weights(mx, None, 256, 256, 0, 16, 16, 0) == -1
+    assert pkg.moe_quantize_weights(mx, 16, 100, 256, 1, 16, 16, 0) == -2
+    assert pkg.moe_quantize_weights(mx, 8, 256, 256, 0, 16, 16, 0) == -3
     # backward without a backward-sized workspace
     assert pkg.moe_backward(cfg, 16, 16, W, 16, 16, 16, 16, 16, None, None, 16, 0) == -1
 

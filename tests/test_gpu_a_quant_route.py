@@ -140,3 +140,25 @@ def test_route_ties_and_degenerate_loads(pkg):
     l[20, :] = -0.0
     l[21, ::2] = 0.0
     _check_route(pkg, l.contiguous(), k)
+
+
+@pytest.mark.parametrize("blocks_along_rows", [0, 1])
+def test_quantize_weights_layer_entry_bit_exact(pkg, blocks_along_rows):
+    """moe_quantize_weights: the layer's stacked expert masters (cfg.E of
+    them) in either operand orientation, bit-identical to the oracle; a BF16
+    config is refused."""
+    E, rows, cols = 3, 256, 512
+    c = pkg.config(64, cols, rows // 2, E, 2, 0, "mxfp8", 0)
+    rng = np.random.default_rng(5)
+    w = torch.from_numpy(edge_values(rng, (E, rows, cols))).to(torch.bfloat16)
+    wg = w.cuda()
+    codes = torch.empty(E * rows * cols, dtype=torch.uint8, device="cuda")
+    sf = torch.empty(E * rows * cols // 32, dtype=torch.uint8, device="cuda")
+    pkg.check(pkg.moe_quantize_weights(c, wg, rows, cols, blocks_along_rows, codes, sf))
+    torch.cuda.synchronize()
+    c_ref, s_ref = om.quantize_weights(mi.to_f64(w), transpose=bool(blocks_along_rows))
+    B, r2, c2 = c_ref.shape
+    assert np.array_equal(codes.cpu().numpy().reshape(B * r2, c2), c_ref.reshape(B * r2, c2))
+    assert np.array_equal(unpack_tiled_scales(sf.cpu().numpy(), B * r2, c2), s_ref.reshape(B * r2, c2 // 32))
+    cb = pkg.config(64, cols, rows // 2, E, 2, 0, "bf16", 0)
+    assert pkg.moe_quantize_weights(cb, wg, rows, cols, blocks_along_rows, codes, sf) == -1  # MOE_ERR_ARG
