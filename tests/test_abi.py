@@ -58,6 +58,31 @@ def test_sizes_and_layout(pkg):
     assert nb == pkg.moe_padded_rows(cmx) * 256 // 32
 
 
+def test_saved_wgrad_operands_by_format(pkg):
+    """A training forward keeps the down wgrad's h operand as bf16 rows
+    with BF16 experts and as column-blocked MXFP8 codes h^T with MXFP8 experts;
+    the MXFP8 backward keeps dO and dGU only as codes."""
+    T, d, m, E, k = 256, 256, 128, 8, 2
+    bf = pkg.config(T, d, m, E, k, 0, "bf16", pkg.MOE_FLAG_BACKWARD)
+    mx = pkg.config(T, d, m, E, k, 0, "mxfp8", pkg.MOE_FLAG_BACKWARD)
+    rp = pkg.moe_padded_rows(mx)
+    assert pkg.moe_buffer_info(bf, 0, "h")[1] == pkg.moe_padded_rows(bf) * m * 2
+    for name in ("hT", "hT_sf"):
+        with pytest.raises(RuntimeError):
+            pkg.moe_buffer_info(bf, 0, name)
+    assert pkg.moe_buffer_info(mx, 0, "hT")[1] == m * rp
+    assert pkg.moe_buffer_info(mx, 0, "hT_sf")[1] == m * rp // 32
+    with pytest.raises(RuntimeError):
+        pkg.moe_buffer_info(mx, 0, "h")
+    for name in ("dO", "dGU"):
+        assert pkg.moe_buffer_info(bf, 1, name)[1] > 0
+        with pytest.raises(RuntimeError):
+            pkg.moe_buffer_info(mx, 1, name)
+    assert pkg.moe_buffer_info(mx, 1, "dGUT")[1] == 2 * m * rp
+    assert pkg.moe_buffer_info(mx, 1, "dGUq")[1] == rp * 2 * m
+    assert pkg.moe_buffer_info(mx, 1, "tile_order")[1] == rp // 32 * 4
+
+
 @pytest.mark.parametrize("bad,code", [
     (dict(d=100), -2), (dict(m=64), -2), (dict(k=9), -2), (dict(k=0), -1), (dict(E=2000), -2),
     (dict(T=0), -1), (dict(flags=4), -1), (dict(dtype=7), -1), (dict(m_shared=100), -2),
