@@ -127,13 +127,15 @@ typedef struct {
  * bf16; the *_scale pointers are unused.
  * MXFP8 path: `gu` = E4M3 codes [E*2m, d] with tiled scales `gu_scale`
  * (rows E*2m, K d); `dn` = codes [E*d, m], `dn_scale` (rows E*d, K m) --
- * both from moe_quantize_mx(transpose=0) of the bf16 masters.
+ * both from moe_quantize_weights(blocks_along_rows = 0) (or
+ * moe_quantize_mx(transpose = 0)) of the bf16 masters.
  * Backward operands (NULL for a forward-only layer):
  *   BF16:  gu_t = [E, d, 2m] bf16 = per-expert transpose of gu,
  *          dn_t = [E, m, d] bf16 = per-expert transpose of dn
  *          (moe_transpose_bf16);
  *   MXFP8: gu_t = codes [E*d, 2m] + gu_t_scale, dn_t = codes [E*m, d] +
- *          dn_t_scale (moe_quantize_mx(transpose=1) of the masters).
+ *          dn_t_scale (moe_quantize_weights(blocks_along_rows = 1) of the
+ *          masters; moe_quantize_mx_both writes both orientations at once).
  * Shared expert (BF16 always; NULL when m_shared == 0): s_gu [2m_s, d],
  * s_dn [d, m_s]; for backward also s_gu_t [d, 2m_s], s_dn_t [m_s, d].
  */
