@@ -299,6 +299,11 @@ struct Gemm {
   GemmArgs g;
   long max_tiles;
   long out_rows;
+  // weight gradients: the empty experts' all-zero dW, written by a plain
+  // store kernel inside the same traced region (single-CTA path only)
+  void *zero_dst = nullptr;
+  long zero_expert_bytes = 0;
+  const int *zero_counts = nullptr;
 };
 
 // 2-D view of a tiled MXFP8 scale buffer as rows of 256 bytes (box: one
@@ -351,6 +356,12 @@ int run_gemm(const char *name, const Gemm &q, const DeviceInfo &dev, cudaStream_
   if (!make_map(&tb, q.b, q.mx, q.K, q.b_rows)) return MOE_ERR_CUDA;
   moe::GemmArgs g = q.g;
   g.out_rows = q.out_rows;
+  if (q.zero_dst) {
+    const int rc = cuda_status(moe::launch_zero_empty_experts(q.zero_dst, q.g.E, q.zero_expert_bytes,
+                                                              q.zero_counts, s));
+    if (rc != MOE_OK) return rc;
+    g.skip_empty = 1;
+  }
   if (use_mc(q)) {
     // clusters of two sharing A: A is loaded in 64-row halves
     CUtensorMap ta_half;
@@ -900,6 +911,9 @@ int moe_backward(const moe_config *cfg, const void *dy, const void *x, const moe
     q.g.ldo = D.m;
     q.max_tiles = static_cast<long>(D.E) * (D.d / 128) * q.g.n_tiles;
     q.out_rows = static_cast<long>(D.E) * (D.d);
+    q.zero_dst = dW_dn;
+    q.zero_expert_bytes = static_cast<long>(D.d) * D.m * 2;
+    q.zero_counts = rb.counts;
     if ((rc = run_gemm("wgrad_down", q, dev, s)) != MOE_OK) return rc;
   }
   // B5 wgrad of the gate/up projection: dW_gu[e] = dGU_e^T X_e
@@ -924,6 +938,9 @@ int moe_backward(const moe_config *cfg, const void *dy, const void *x, const moe
     q.g.ldo = D.d;
     q.max_tiles = static_cast<long>(D.E) * (2 * D.m / 128) * q.g.n_tiles;
     q.out_rows = static_cast<long>(D.E) * (2 * D.m);
+    q.zero_dst = dW_gu;
+    q.zero_expert_bytes = 2L * D.m * D.d * 2;
+    q.zero_counts = rb.counts;
     if ((rc = run_gemm("wgrad_gate_up", q, dev, s)) != MOE_OK) return rc;
   }
   // B7 shared expert backward (BF16, dense)

@@ -414,6 +414,7 @@ __global__ void __launch_bounds__(64 + 32 * epi_warps<EPI, BN>(), 1)
       bool ok = true;
       for (int i = cta; i < total && ok; i += ncta) {
         const Tile ti = decode_tile<C::BK, BN, EPI>(g, tile_of(i));
+        if (ti.nk == 0 && g.skip_empty) continue;  // zeros written by another launch
         if (!mbar_wait(&tempty[acc], aph ^ 1u, abort_flag, g.status, g.timeout_ns)) break;
         tc_fence_after();
         const uint32_t dt = tmem_base + static_cast<uint32_t>(acc * BN);
@@ -485,6 +486,7 @@ __global__ void __launch_bounds__(64 + 32 * epi_warps<EPI, BN>(), 1)
     uint32_t aph = 0;
     for (int i = cta; i < total; i += ncta) {
       const Tile ti = decode_tile<C::BK, BN, EPI>(g, tile_of(i));
+      if (ti.nk == 0 && g.skip_empty) continue;  // zeros written by another launch
       if constexpr (EPI == EPI_SWIGLU_BWD) {
         // The saved G|U rows this tile's epilogue reads come from HBM: pull them
         // into L2 while the main loop runs.

@@ -691,6 +691,21 @@ __global__ void __launch_bounds__(256) quantize_rows_kernel(const uint4 *__restr
   }
 }
 
+// Zeros of the empty experts' weight gradients: block (x, e) clears bytes
+// [x MB, (x + 1) MB) of expert e's matrix when the expert received no rows.
+constexpr long kZeroPiece = 1L << 20;
+
+__global__ void __launch_bounds__(512) zero_empty_experts_kernel(uint8_t *__restrict__ dW, long expert_bytes,
+                                                                 const int *__restrict__ counts) {
+  const int e = static_cast<int>(blockIdx.y);
+  if (__ldg(counts + e) != 0) return;
+  const long u0 = static_cast<long>(blockIdx.x) * kZeroPiece / 16;
+  const long u1 = min(u0 + kZeroPiece / 16, expert_bytes / 16);
+  uint4 *p = reinterpret_cast<uint4 *>(dW + static_cast<long>(e) * expert_bytes);
+  const uint4 z = make_uint4(0, 0, 0, 0);
+  for (long u = u0 + threadIdx.x; u < u1; u += blockDim.x) p[u] = z;
+}
+
 inline unsigned blocks_for(long n, int per_block) {
   return static_cast<unsigned>((n + per_block - 1) / per_block);
 }
@@ -743,6 +758,12 @@ cudaError_t launch_gather(const void *x, int T, int d, int k, int E, const Route
   } else
     gather_bf16_kernel<<<blocks_for(rp_max, 8), 256, 0, s>>>(static_cast<const uint4 *>(x), d, k, E, b, rp_max,
                                                               static_cast<uint4 *>(xs));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_zero_empty_experts(void *dW, int E, long expert_bytes, const int *counts, cudaStream_t s) {
+  const dim3 grid(static_cast<unsigned>((expert_bytes + kZeroPiece - 1) / kZeroPiece), static_cast<unsigned>(E));
+  zero_empty_experts_kernel<<<grid, 512, 0, s>>>(static_cast<uint8_t *>(dW), expert_bytes, counts);
   return cudaGetLastError();
 }
 

@@ -156,12 +156,18 @@ struct GemmArgs {
   const void *aux;    // SWIGLU_BWD: saved G|U bf16
   long ld_aux;
   int m_half;         // SWIGLU / SWIGLU_BWD: m
+  int skip_empty;     // GROUP_K: tiles with an empty reduction are left to launch_zero_empty_experts
   int *status;
   unsigned long long timeout_ns;  // limit of every wait in the launch
   int debug_starve;   // test hook: the producer issues no loads (the MMA wait runs out);
                       // with a ring, the gather CTAs publish nothing instead
   RingArgs ring;      // launch_gemm_ring only
 };
+
+// Zeros for the weight gradients of experts that received no rows: dW holds E
+// matrices of expert_bytes (a multiple of 16) each; expert e's is cleared when
+// counts[e] == 0.  Plain 16-byte stores from a grid of 1 MB pieces.
+cudaError_t launch_zero_empty_experts(void *dW, int E, long expert_bytes, const int *counts, cudaStream_t s);
 
 // D = A * B^T with A [rows, K] and B [rows, K] K-major (TMA maps built by the
 // caller, box = 128 rows x 128 bytes, 128-byte swizzle); bn = 128 or 256
