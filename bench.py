@@ -40,6 +40,8 @@ MX_OVER_BF16 = 2.0   # nominal dense MXFP8 : BF16 tensor-core ratio (4.5 : 2.25 
 # removed whenever the kernel changes after the capture.
 NCU_TRAFFIC = {
     # profiles/dram_traffic_dominant_kernels.md (full-size launches, one-pass capture)
+    # Kimi-K2.7 gate/up wgrad: the empty experts' zero fill plus the GEMM, read + write
+    ("kimi-k2.7", "wgrad_gate_up"): (687_360 + 4_921_171_456) + (8_860_089_344 + 13_564_724_224),
     ("deepseek-v4-pro", "gemm1_gate_up_swiglu"): 20_051_618_816 + 694_565_632,
 }
 

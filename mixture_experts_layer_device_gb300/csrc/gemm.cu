@@ -19,7 +19,9 @@
 //            the expert's weight panel hot in L2 while its rows stream.
 //   DENSE    one group (shared expert).
 //   GROUP_K  weight gradients: the reduction runs over one expert's padded
-//            rows [poff[e], poff[e+1]) of two transposed operands.
+//            rows [poff[e], poff[e+1]) of two transposed operands.  An
+//            expert with no rows gets all-zero tiles, or, with skip_empty,
+//            no tiles at all (a plain store kernel writes its zeros).
 // Every output element is produced by one CTA with a fixed K order, so results
 // are bitwise reproducible.
 #include "common.cuh"
