@@ -762,6 +762,9 @@ cudaError_t launch_gather(const void *x, int T, int d, int k, int E, const Route
 }
 
 cudaError_t launch_zero_empty_experts(void *dW, int E, long expert_bytes, const int *counts, cudaStream_t s) {
+  if (!dW || !counts || E <= 0 || E > 65535 || expert_bytes <= 0 || expert_bytes % 16 != 0 ||
+      reinterpret_cast<uintptr_t>(dW) % 16 != 0)
+    return cudaErrorInvalidValue;
   const dim3 grid(static_cast<unsigned>((expert_bytes + kZeroPiece - 1) / kZeroPiece), static_cast<unsigned>(E));
   zero_empty_experts_kernel<<<grid, 512, 0, s>>>(static_cast<uint8_t *>(dW), expert_bytes, counts);
   return cudaGetLastError();
