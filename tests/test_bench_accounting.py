@@ -1,0 +1,87 @@
+"""Host arithmetic behind the bench's roofline figures, on CPU.
+
+The layer figures are pinned to numbers worked out by hand from the layer
+shapes (6·d·m FLOPs per routed (token, expert) pair plus 6·d·m_s per token for
+the shared expert; weights once in their stored format plus the layer-boundary
+activations), written here to three significant figures.  The per-kernel work
+is pinned by invariants: the expert GEMMs of one pass add up to the layer's
+FLOPs, and the backward's four GEMMs are twice the forward's two."""
+import pytest
+
+import bench
+
+# (FLOPs fwd, algorithmic GB fwd, GB fwd+bwd or None)
+HAND = {
+    "qwen3.5-397b": (2.27e12, 13.06, None),
+    "glm-5.2": (9.90e12, 10.39, None),
+    "kimi-k2.7": (1.30e13, 18.0, 70.0),
+    "deepseek-v4-pro": (2.60e13, 27.15, None),
+}
+
+
+@pytest.mark.parametrize("name", list(HAND))
+def test_layer_work_matches_hand_figures(name):
+    cfg = bench.workload(name)
+    flops, gb, gb_bwd = HAND[name]
+    f, fs, b = bench.layer_work(cfg, "fwd")
+    assert f + fs == pytest.approx(flops, rel=5e-3)
+    assert b / 1e9 == pytest.approx(gb, rel=5e-3)
+    if gb_bwd is not None:
+        f3, fs3, b3 = bench.layer_work(cfg, "fwdbwd")
+        assert f3 + fs3 == pytest.approx(3 * (f + fs))
+        assert b3 / 1e9 == pytest.approx(gb_bwd, rel=5e-3)
+
+
+FWD = ("gemm1_gate_up_swiglu", "gemm2_down")
+BWD = ("dgrad_down_swiglu_bwd", "dgrad_gate_up", "wgrad_down", "wgrad_gate_up")
+
+
+@pytest.mark.parametrize("name", ["tiny", "kimi-k2.7", "deepseek-v4-pro"])
+def test_kernel_flops_add_up_to_the_layer(name):
+    cfg = bench.workload(name)
+    fl_exp, fl_sh, _ = bench.layer_work(cfg, "fwd")
+    fwd = sum(bench.kernel_work(cfg, n, False)[0] for n in FWD)
+    bwd = sum(bench.kernel_work(cfg, n, True)[0] for n in BWD)
+    assert fwd == pytest.approx(fl_exp)
+    assert bwd == pytest.approx(2 * fl_exp)
+    if cfg["m_shared"]:
+        sh = sum(bench.kernel_work(cfg, "shared_" + n, False)[0] for n in FWD)
+        sh_b = sum(bench.kernel_work(cfg, "shared_" + n, True)[0] for n in BWD)
+        assert sh == pytest.approx(fl_sh)
+        assert sh_b == pytest.approx(2 * fl_sh)
+
+
+def test_kernel_roofline_takes_the_longer_bound():
+    cfg = bench.workload("kimi-k2.7")
+    peaks = {"hbm_gbs": 6757.9, "bf16_tflops_sustained": 1661.6}
+    # the gate/up wgrad writes 22.5 GB of bf16 dW: HBM-bound at this shape
+    r = bench.kernel_roofline(cfg, "wgrad_gate_up", True, 6.0, peaks)
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s"
+    byts = bench.kernel_work(cfg, "wgrad_gate_up", True)[1]
+    assert r["achieved"] == pytest.approx(byts / 6.0e-3 / 1e9)
+    # the forward gate/up GEMM is tensor-bound, at the MXFP8 rate
+    r = bench.kernel_roofline(cfg, "gemm1_gate_up_swiglu", False, 3.6, peaks)
+    assert r["bound"] == "tensor" and r["mx"]
+    assert r["peak"] == pytest.approx(1661.6 * bench.MX_OVER_BF16)
+    assert bench.kernel_roofline(cfg, "no_such_kernel", True, 1.0, peaks) is None
+
+
+def test_launches_per_traced_region():
+    mx = bench.workload("kimi-k2.7")
+    bf = bench.workload("qwen3.5-397b")
+    assert bench.kernels_in_region("route_schedule", mx, True) == 4
+    assert bench.kernels_in_region("dispatch_gather", mx, True) == 2
+    assert bench.kernels_in_region("dispatch_gather", mx, False) == 3
+    assert bench.kernels_in_region("dispatch_gather", bf, False) == 1
+    assert bench.kernels_in_region("wgrad_gate_up", mx, True) == 2
+    assert bench.kernels_in_region("gemm1_gate_up_swiglu", mx, True) == 1
+
+
+def test_recorded_traffic_names_a_known_kernel():
+    for (wl, kernel), traffic in bench.NCU_TRAFFIC.items():
+        cfg = bench.workload(wl)
+        w = bench.kernel_work(cfg, kernel, cfg["backward"])
+        assert w is not None
+        # DRAM traffic of a full-size launch: at least the algorithmic bytes
+        # (less only by what L2 still holds at the end), and not wildly above
+        assert 0.95 * w[1] < traffic < 1.5 * w[1]
