@@ -146,3 +146,55 @@ def test_ring_workspace_replaces_the_dispatch_buffer(pkg):
     assert pkg.moe_saved_bytes(full) == pkg.moe_saved_bytes(ring)
     off, nb = pkg.moe_buffer_info(ring, 1, "ring")
     assert nb == 8192 * d
+
+
+def _declarations():
+    """(name, [parameter declarations]) of every function in the header."""
+    src = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    out = {}
+    for m in re.finditer(r"^[A-Za-z_][\w \*]*?\b(moe_\w+)\s*\(([^)]*)\)\s*;", src, flags=re.M):
+        params = [p.strip() for p in m.group(2).replace("\n", " ").split(",")]
+        out[m.group(1)] = [] if params == ["void"] else params
+    return out
+
+
+def _kind_of_decl(p):
+    if "*" in p or p.startswith("moe_stream_t"):
+        return "ptr"
+    base = p.rsplit(None, 1)[0].replace("const", "").strip()
+    return {"int": "int", "int32_t": "int", "int64_t": "i64", "size_t": "size", "float": "float"}[base]
+
+
+def _kind_of_ctype(t):
+    if t in (ctypes.c_void_p, ctypes.c_char_p) or issubclass(t, ctypes._Pointer):
+        return "ptr"
+    # c_int and c_int32 are the same type, as are c_size_t and c_ulong/c_uint64 on LP64
+    return {ctypes.c_int: "int", ctypes.c_int64: "i64", ctypes.c_size_t: "size", ctypes.c_float: "float"}[t]
+
+
+def test_binding_argtypes_match_the_header(pkg):
+    L = pkg.lib()
+    decls = _declarations()
+    assert sorted(decls) == declared_functions()
+    for name, params in decls.items():
+        want = [_kind_of_decl(p) for p in params]
+        got = [_kind_of_ctype(t) for t in getattr(L, name).argtypes]
+        assert got == want, name
+
+
+def _struct_fields(tag):
+    """Field names of a `typedef struct { ... } tag;` in declaration order."""
+    src = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    body = re.search(r"typedef struct \{([^}]*)\}\s*" + tag + r"\s*;", src).group(1)
+    names = []
+    for decl in filter(None, (x.strip() for x in body.split(";"))):
+        first, *rest = decl.split(",")
+        names.append(re.split(r"[\s\*]+", first.strip())[-1])   # type + first declarator
+        names += [r.strip().lstrip("*").strip() for r in rest]   # further declarators
+    return names
+
+
+def test_binding_structs_match_the_header(pkg):
+    assert [f[0] for f in pkg.MoeConfig._fields_] == _struct_fields("moe_config")
+    assert [f[0] for f in pkg.MoeWeights._fields_] == _struct_fields("moe_weights")
+    assert ctypes.sizeof(pkg.MoeConfig) == 11 * 4
