@@ -231,6 +231,12 @@ class Clocks:
                                       stdout=self.f, stderr=subprocess.DEVNULL)
         except OSError:
             self.p = None
+        # the first sample is on file before the caller starts timing (at most 3 s)
+        t0 = time.time()
+        while self.p is not None and self.p.poll() is None and time.time() - t0 < 3.0:
+            if os.path.getsize(self.f.name) > 0:
+                break
+            time.sleep(0.05)
 
     def stop(self):
         if self.p is None:
@@ -257,6 +263,20 @@ class Clocks:
         os.unlink(self.f.name)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
                 "samples": len(sm), "reasons": sorted(reasons)}
+
+
+REJECTING_REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown")
+
+
+def clocks_rejected(clk):
+    """Whether a timed region's clock record disqualifies its number: a
+    hardware or thermal slowdown was active, or the SM clock sat well below its
+    maximum with no reason given (a clock lock left by someone else).
+    sw_power_cap alone is normal under a dense load and is kept."""
+    if any(r in clk.get("reasons", []) for r in REJECTING_REASONS):
+        return True
+    sm, smax = clk.get("sm_mhz"), clk.get("sm_max_mhz")
+    return bool(sm and smax and sm < 0.8 * smax and not clk.get("reasons"))
 
 
 def gpu_index(local_rank):
@@ -451,6 +471,14 @@ def run_ours(args, cfg, passes, rank, world, local_rank):
     else:
         total_ms, _ = timed(step, args.steps)
         clk = clocks.stop()
+        # measured once more (every rank, if any rank's record rejects it); the
+        # second record is reported
+        if max_over_ranks(float(clocks_rejected(clk)), world, dev) > 0:
+            first = clk
+            clocks = Clocks(gpu_index(local_rank))
+            total_ms, _ = timed(step, args.steps)
+            clk = clocks.stop()
+            clk["remeasured_after"] = {"sm_mhz": first["sm_mhz"], "reasons": first["reasons"]}
         # per-kernel breakdown from a second, traced run (its event records would
         # add gaps between launches to the headline timing)
         _, recs = timed(step, args.steps, trace=True)

@@ -6,6 +6,8 @@ the shared expert; weights once in their stored format plus the layer-boundary
 activations), written here to three significant figures.  The per-kernel work
 is pinned by invariants: the expert GEMMs of one pass add up to the layer's
 FLOPs, and the backward's four GEMMs are twice the forward's two."""
+import os
+
 import pytest
 
 import bench
@@ -85,3 +87,38 @@ def test_recorded_traffic_names_a_known_kernel():
         # DRAM traffic of a full-size launch: at least the algorithmic bytes
         # (less only by what L2 still holds at the end), and not wildly above
         assert 0.95 * w[1] < traffic < 1.5 * w[1]
+
+
+def test_clock_records_that_reject_a_number():
+    ok = {"sm_mhz": 2040.0, "sm_max_mhz": 2070.0, "reasons": []}
+    capped = {"sm_mhz": 1950.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"]}
+    thermal = {"sm_mhz": 1900.0, "sm_max_mhz": 2070.0, "reasons": ["hw_thermal_slowdown", "sw_power_cap"]}
+    locked = {"sm_mhz": 1200.0, "sm_max_mhz": 2070.0, "reasons": []}
+    low_capped = {"sm_mhz": 1200.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"]}
+    unknown = {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+    assert not bench.clocks_rejected(ok)
+    assert not bench.clocks_rejected(capped)
+    assert bench.clocks_rejected(thermal)
+    assert bench.clocks_rejected(locked)
+    assert not bench.clocks_rejected(low_capped)
+    assert not bench.clocks_rejected(unknown)
+
+
+def test_clock_sampler_against_a_fake_nvidia_smi(tmp_path, monkeypatch):
+    """The sampler waits for the first sample, then parses the query's CSV
+    (index, sm, max sm, power, active, four reason columns)."""
+    fake = tmp_path / "nvidia-smi"
+    fake.write_text("#!/bin/sh\n"
+                    "i=0\n"
+                    "while [ $i -lt 50 ]; do\n"
+                    "  echo '0, 1980, 2070, 900.5, 0x4, Not Active, Not Active, Not Active, Active'\n"
+                    "  i=$((i+1)); sleep 0.05\n"
+                    "done\n")
+    fake.chmod(0o755)
+    monkeypatch.setenv("PATH", str(tmp_path) + os.pathsep + os.environ["PATH"])
+    clk = bench.Clocks(0)
+    assert os.path.getsize(clk.f.name) > 0          # a sample was on file before timing
+    rec = clk.stop()
+    assert rec["sm_mhz"] == 1980.0 and rec["sm_max_mhz"] == 2070.0
+    assert rec["reasons"] == ["sw_power_cap"] and rec["samples"] >= 1
+    assert not bench.clocks_rejected(rec)
