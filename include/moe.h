@@ -271,9 +271,10 @@ int moe_forward(const moe_config *cfg, const void *x, const float *logits, const
  * GEMMs' dgrad/wgrad, then reverse-dispatch).  Inputs: dy [T, d] bf16, the
  * forward's x, weights (including the backward operands) and `saved`.
  * Outputs: dx [T, d] bf16; dlogits [T, E] fp32 (w_j (g_j - sum_i w_i g_i) at
- * the chosen experts, g_j = <dy_t, o_j>, 0 elsewhere); dW_gu [E, 2m, d] bf16;
- * dW_dn [E, d, m] bf16 (zero for experts with no rows); dWs_gu [2m_s, d],
- * dWs_dn [d, m_s] bf16 (shared expert; NULL when absent).
+ * the chosen experts, g_j = <dy_t, o_j>, 0 elsewhere); dW_gu [E, 2m, d] and
+ * dW_dn [E, d, m] bf16, every element written (all zeros for an expert that
+ * received no rows, so the buffers need no clearing beforehand); dWs_gu
+ * [2m_s, d], dWs_dn [d, m_s] bf16 (shared expert; NULL when absent).
  */
 int moe_backward(const moe_config *cfg, const void *dy, const void *x, const moe_weights *W,
                  const void *saved, void *dx, float *dlogits, void *dW_gu, void *dW_dn,
