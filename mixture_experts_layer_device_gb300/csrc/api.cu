@@ -3,6 +3,13 @@
 // the launch sequence of the forward and backward passes.  Nothing here
 // allocates memory or synchronises the host with the device (except
 // moe_get_status, which exists to do exactly that).
+//
+// The launch sequence follows the method's pipeline ("Mixture-of-Kittens" wiki
+// page, flowchart): route, device-side schedule, dispatch with fused MXFP8
+// quantisation, expert grouped GEMMs with fused SwiGLU, fixed-order combine,
+// the BF16 shared expert (Key claims, MXFP8 bullet); the backward runs the
+// reverse combine first and the reverse dispatch last (Key claims,
+// communication-direction bullet).
 #include <cublas_v2.h>
 #include <cuda.h>
 #include <cuda_runtime.h>

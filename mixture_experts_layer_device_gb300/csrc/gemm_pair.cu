@@ -1,4 +1,6 @@
-// Grouped expert GEMMs on CTA pairs (tcgen05 cta_group::2).
+// Grouped expert GEMMs on CTA pairs (tcgen05 cta_group::2): the BF16 expert
+// GEMMs and the shared expert, which stays in BF16 ("Mixture-of-Kittens" wiki
+// page, Key claims, MXFP8 bullet).
 //
 // A cluster of two CTAs on two SMs computes a 256 x 256 output tile: each CTA
 // loads 128 rows of A and one 128-row half of B into its own shared memory and
