@@ -32,7 +32,7 @@ def _rank_main(rank, world, port, out):
 @pytest.mark.parametrize("world", [2])
 def test_max_over_ranks_and_replica_throughput_gloo(world):
     port = _free_port()
-    mgr = tmp.Manager()
+    mgr = tmp.get_context("spawn").Manager()   # no fork of a multi-threaded process
     out = mgr.dict()
     tmp.spawn(_rank_main, args=(world, port, out), nprocs=world, join=True)
     slowest = 100.0 + 7.5 * (world - 1)
