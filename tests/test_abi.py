@@ -198,3 +198,35 @@ def test_binding_structs_match_the_header(pkg):
     assert [f[0] for f in pkg.MoeConfig._fields_] == _struct_fields("moe_config")
     assert [f[0] for f in pkg.MoeWeights._fields_] == _struct_fields("moe_weights")
     assert ctypes.sizeof(pkg.MoeConfig) == 11 * 4
+
+
+def test_product_path_never_reaches_the_oracle():
+    """The package imports nothing from oracle/; in bench.py only the CPU
+    baseline and reference-arm helpers do."""
+    import ast
+    pkg_dir = os.path.join(ROOT, "mixture_experts_layer_device_gb300")
+    for dirpath, _, files in os.walk(pkg_dir):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                src = open(os.path.join(dirpath, f)).read()
+                assert not re.search(r"^\s*(from|import)\s+oracle\b", src, flags=re.M), f
+    tree = ast.parse(open(os.path.join(ROOT, "bench.py")).read())
+    users = set()
+    for fn in ast.walk(tree):
+        if isinstance(fn, ast.FunctionDef):
+            for node in ast.walk(fn):
+                if isinstance(node, ast.ImportFrom) and (node.module or "").split(".")[0] == "oracle":
+                    users.add(fn.name)
+                if isinstance(node, ast.Import) and any(a.name.split(".")[0] == "oracle" for a in node.names):
+                    users.add(fn.name)
+    assert users <= {"_prep_worker", "oracle_sample", "oracle_prepare", "oracle_step", "run_reference"}, users
+    top = [n for n in tree.body if isinstance(n, (ast.Import, ast.ImportFrom))]
+    assert not any("oracle" in ast.dump(n) for n in top)
+
+
+def test_binding_raises_without_the_library(monkeypatch):
+    import mixture_experts_layer_device_gb300 as m
+    monkeypatch.setattr(m, "_lib", None)
+    monkeypatch.setattr(m, "LIB_PATH", os.path.join(ROOT, "no_such_dir", "libmoe_gb300.so"))
+    with pytest.raises(RuntimeError):
+        m.lib()
