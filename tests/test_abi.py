@@ -230,3 +230,37 @@ def test_binding_raises_without_the_library(monkeypatch):
     monkeypatch.setattr(m, "LIB_PATH", os.path.join(ROOT, "no_such_dir", "libmoe_gb300.so"))
     with pytest.raises(RuntimeError):
         m.lib()
+
+
+def test_header_is_plain_c_and_links_from_c(pkg, tmp_path):
+    """include/moe.h compiles as C99 and C++17, and a C program links against
+    the library and calls a host-only entry point."""
+    import shutil
+    import subprocess
+    gcc, gxx = shutil.which("gcc"), shutil.which("g++")
+    if not gcc or not gxx:
+        pytest.skip("no host C compiler")
+    inc = os.path.join(ROOT, "include")
+    for cc, lang, std in ((gcc, "c", "-std=c99"), (gxx, "c++", "-std=c++17")):
+        r = subprocess.run([cc, std, "-Wall", "-Wextra", "-Werror", "-fsyntax-only", "-x", lang, HEADER],
+                           capture_output=True, text=True)
+        assert r.returncode == 0, r.stderr
+    src = tmp_path / "use_abi.c"
+    src.write_text('#include <stdio.h>\n#include "moe.h"\n'
+                   "int main(void) {\n"
+                   "  moe_config c = {256, 256, 128, 8, 2, 0, MOE_BF16, MOE_FLAG_BACKWARD, 0, 0, 0.0f};\n"
+                   "  size_t ws = moe_workspace_bytes(&c);\n"
+                   "  c.k = 9; /* k > E */\n"
+                   "  printf(\"%zu %zu\\n\", ws, moe_workspace_bytes(&c));\n"
+                   "  return 0;\n}\n")
+    exe = tmp_path / "use_abi"
+    libdir = os.path.dirname(pkg.LIB_PATH)
+    r = subprocess.run([gcc, "-std=c99", "-Wall", "-Werror", "-I", inc, str(src), "-o", str(exe), "-L", libdir,
+                        "-l:" + os.path.basename(pkg.LIB_PATH), "-Wl,-rpath," + libdir],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0, r.stderr
+    ws, bad = (int(v) for v in r.stdout.split())
+    cfg = pkg.config(256, 256, 128, 8, 2, 0, "bf16", pkg.MOE_FLAG_BACKWARD)
+    assert ws == pkg.moe_workspace_bytes(cfg) > 0 and bad == 0
