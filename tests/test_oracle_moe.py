@@ -272,11 +272,19 @@ def test_backward_rounded_formats_close_to_exact(fmt, tol):
     assert rel(g["dWs_gu"], g64["dWs_gu"]) < tol
 
 
-def test_column_blocks_zero_pad():
+def test_column_blocks_start_at_first_row_and_pad_at_end():
+    """Column blocks are rows [0, 32), [32, 64), ... of the expert, the last one
+    zero-padded: rows 0..31 scaled by 2**8 and rows 32..44 by 2**-8 are exact
+    in those blocks, while any block straddling row 32 (padding in front, or
+    blocks counted from the last row) mixes scales 16 binades apart and loses
+    bits."""
     rng = np.random.default_rng(15)
-    a = rng.standard_normal((45, 32))
-    ap = np.concatenate([a, np.zeros((19, 32))])
-    assert np.array_equal(om._col_blocks(a), nx.mx_roundtrip(ap, axis=0)[:45])
+    a = _mant(rng, (45, 32)) * 2.0 ** rng.integers(-2, 3, (1, 32))
+    a[:32] *= 2.0 ** 8
+    a[32:] *= 2.0 ** -8
+    assert np.array_equal(om._col_blocks(a), a)
+    front = np.concatenate([np.zeros((19, 32)), a])
+    assert not np.array_equal(nx.mx_roundtrip(front, axis=0)[19:], a)
 
 
 @pytest.mark.parametrize("fmt", ["bf16", "mxfp8"])
@@ -296,3 +304,106 @@ def test_prepared_operands_change_nothing(fmt):
         assert np.array_equal(g1[key], g2[key])
     for e in g1["dW_gu"]:
         assert np.array_equal(g1["dW_gu"][e], g2["dW_gu"][e]) and np.array_equal(g1["dW_dn"][e], g2["dW_dn"][e])
+
+
+# ---------------------------------------------------------------- MXFP8 quantisation axes
+# Each test below builds operands that are exactly representable in MXFP8 along
+# the axis the reading names (blocks of 32 along the GEMM's K for dgrad and the
+# forward; blocks of 32 rows of one expert for wgrad) and wildly scaled along
+# the other axis, so the quantised products equal the unquantised float64 ones
+# exactly, while quantising along the other axis would lose bits.  The
+# "wrong axis is lossy" premise of every operand is asserted too.
+def _mant(rng, shape):
+    """Signed values with 3 fraction bits in [1, 1.75]: E4M3 mantissas that
+    never saturate at the top of a block."""
+    return (rng.integers(8, 15, shape) * rng.choice([-1, 1], shape)) / 8.0
+
+
+def _row_exact(a):
+    return np.array_equal(nx.mx_roundtrip(a, axis=1), a)
+
+
+def _col_exact(a):
+    return np.array_equal(om._col_blocks(a), a)
+
+
+def test_mx_h_quantised_along_m():
+    """Forward: h is quantised along m (its GEMM's K) straight from the SwiGLU
+    output.  G = 64 everywhere makes silu(G) = G exactly in float64 (exp(-64)
+    vanishes against 1), and U = X[:, 1:m+1], so h = 64 * X[:, 1:m+1]: rows of
+    one binade range each, rows 2**-9 .. 2**9 apart."""
+    rng = np.random.default_rng(31)
+    n, d, m = 64, 64, 32
+    X = np.zeros((n, d))
+    X[:, 0] = 1.0
+    X[:, 1:m + 1] = _mant(rng, (n, m)) * 2.0 ** rng.integers(-9, 10, (n, 1))
+    W_gu = np.zeros((2 * m, d))
+    W_gu[:m, 0] = 64.0                                  # gate: G = 64 * x[:, 0]
+    W_gu[m + np.arange(m), 1 + np.arange(m)] = 1.0      # up: U = X[:, 1:m+1]
+    W_dn = _mant(rng, (d, m)) * 2.0 ** rng.integers(-2, 3, (d, 1))
+    h = 64.0 * X[:, 1:m + 1]
+    assert _row_exact(X) and _row_exact(W_gu) and _row_exact(W_dn)
+    assert _row_exact(h) and not _col_exact(h)
+    res = om.expert_forward(X, W_gu, W_dn, "mxfp8")
+    assert np.array_equal(res["G"], np.full((n, m), 64.0)) and np.array_equal(res["U"], X[:, 1:m + 1])
+    assert np.array_equal(res["o"], nx.bf16_round(h @ W_dn.T))
+
+
+def _bwd_ops(dn_bwd, gu_bwd):
+    return dict(gu_fwd=None, dn_fwd=None, dn_bwd=dn_bwd, gu_bwd=gu_bwd)
+
+
+def test_mx_dgrad_operands_quantised_along_k():
+    """Backward dgrads: dO is quantised along d (the down dgrad's K) and dGU
+    along 2m (the gate/up dgrad's K).  dO rows are 2**-9 .. 2**9 apart; the
+    down weight copy W_dn^T = [I | 0] makes dh = dO[:, :m]; G = 0 makes the
+    SwiGLU backward dG = dh * U / 2 (silu'(0) = 1/2) and dU = 0 (silu(0) = 0),
+    with U = 2**b per row, so dGU keeps dO's per-row scales."""
+    rng = np.random.default_rng(32)
+    n, d, m = 64, 64, 32
+    dO = _mant(rng, (n, d)) * 2.0 ** rng.integers(-9, 10, (n, 1))
+    U = np.broadcast_to(2.0 ** rng.integers(-4, 5, (n, 1)), (n, m))
+    GU = np.concatenate([np.zeros((n, m)), U], axis=1)
+    dn_bwd = np.eye(m, d)
+    gu_bwd = _mant(rng, (d, 2 * m)) * 2.0 ** rng.integers(-1, 2, (d, 1))
+    dGU = np.concatenate([dO[:, :m] * U / 2.0, np.zeros((n, m))], axis=1)
+    assert _row_exact(dO) and not _col_exact(dO)
+    assert _row_exact(dGU) and not _col_exact(dGU)
+    X = nx.bf16_round(rng.standard_normal((n, d)))
+    h = nx.bf16_round(rng.standard_normal((n, m)))
+    res = om.expert_backward(dO, X, GU, h, np.zeros((2 * m, d)), np.zeros((d, m)), "mxfp8",
+                             _bwd_ops(dn_bwd, gu_bwd))
+    assert np.array_equal(res["dh"], dO[:, :m])
+    assert np.array_equal(res["dGU"], dGU)
+    assert np.array_equal(res["dX"], nx.bf16_round(dGU @ gu_bwd.T))
+
+
+def test_mx_wgrad_operands_quantised_in_column_blocks():
+    """Backward wgrads: dO, h, dGU and X are quantised in blocks of 32
+    consecutive rows of the expert (the wgrad's K), the last block zero-padded
+    (n = 50: blocks of 32 and 18 rows).  Columns are 2**-9 .. 2**9 apart; the
+    first m columns of dO (which feed dh through W_dn^T = [I | 0]) stay within
+    a 3-binade range per row so that dh = dO[:, :m] exactly, and U = 2**u per
+    column gives dG = dh * U / 2 per-column scales.  Rows 0..31 carry an extra
+    2**9 and rows 32..49 2**-9, so blocks that do not start at rows 0 and 32
+    would mix scales 18 binades apart."""
+    rng = np.random.default_rng(33)
+    n, d, m = 50, 64, 32
+    blk = np.where(np.arange(n) < 32, 2.0 ** 9, 2.0 ** -9)[:, None]
+    dO = _mant(rng, (n, d)) * 2.0 ** rng.integers(-9, 10, (1, d)) * blk
+    dO[:, :m] = _mant(rng, (n, m)) * 2.0 ** rng.integers(-1, 2, (n, 1)) * blk
+    h = _mant(rng, (n, m)) * 2.0 ** rng.integers(-9, 10, (1, m)) * blk
+    X = _mant(rng, (n, d)) * 2.0 ** rng.integers(-9, 10, (1, d)) * blk
+    U = np.broadcast_to(2.0 ** rng.integers(-9, 10, (1, m)), (n, m))
+    GU = np.concatenate([np.zeros((n, m)), U], axis=1)
+    dGU = np.concatenate([dO[:, :m] * U / 2.0, np.zeros((n, m))], axis=1)
+    for a in (dO, h, X, dGU):
+        assert _col_exact(a) and not _row_exact(a)
+        shifted = np.concatenate([np.zeros((14, a.shape[1])), a])       # blocks counted from the end
+        assert not np.array_equal(nx.mx_roundtrip(shifted, axis=0)[14:], a)
+    assert _row_exact(dO[:, :m])
+    res = om.expert_backward(dO, X, GU, h, np.zeros((2 * m, d)), np.zeros((d, m)), "mxfp8",
+                             _bwd_ops(np.eye(m, d), np.zeros((d, 2 * m))))
+    assert np.array_equal(res["dGU"], dGU)
+    assert np.array_equal(res["dW_dn"], nx.bf16_round(dO.T @ h))
+    assert np.array_equal(res["dW_gu"], nx.bf16_round(dGU.T @ X))
