@@ -12,9 +12,8 @@ copies) happens once per weight update, so it is timed separately ("s0_ms").
 
 Default workload: the Kimi-K2.7-shaped layer (E=384, d=7168, m=2048, top-8,
 T=16384, MXFP8 experts + BF16 shared expert of intermediate 2048), forward +
-backward -- the one workload that runs every step of the path.  N > 1 runs
-independent replicas (one per GPU, weak scaling): the layer has no exchange
-step on a single GPU.
+backward -- the one workload that runs every step of the path.  The layer
+runs on one GPU and has no exchange step, so --gpus must be 1.
 """
 import argparse
 import json
@@ -35,14 +34,10 @@ METRIC = "MoE-layer tokens/s fwd & fwd+bwd on 1 GB300; % of GEMM/HBM roofline"
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 MX_OVER_BF16 = 2.0   # nominal dense MXFP8 : BF16 tensor-core ratio (4.5 : 2.25 PFLOP/s)
 
-# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from the
-# ncu capture summarised in profiles/, keyed by (workload, kernel).  An entry is
-# removed whenever the kernel changes after the capture.
+# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from an
+# ncu capture, keyed by (workload, kernel).  An entry is removed whenever the
+# kernel changes after the capture.
 NCU_TRAFFIC = {
-    # profiles/dram_traffic_dominant_kernels.md (full-size launches, one-pass capture)
-    # Kimi-K2.7 gate/up wgrad: the empty experts' zero fill plus the GEMM, read + write
-    ("kimi-k2.7", "wgrad_gate_up"): (687_360 + 4_921_171_456) + (8_860_089_344 + 13_564_724_224),
-    ("deepseek-v4-pro", "gemm1_gate_up_swiglu"): 20_051_618_816 + 694_565_632,
 }
 
 
@@ -136,25 +131,6 @@ def output_bytes(cfg, name):
     expert weight gradients write bf16 dW for every expert)."""
     d, m, E = cfg["d"], cfg["m"], cfg["E"]
     return {"wgrad_gate_up": E * 2 * m * d * 2, "wgrad_down": E * d * m * 2}.get(name)
-
-
-def max_over_ranks(ms, world, device):
-    """The slowest rank's time; every rank receives it (replicas are timed by
-    the last one to finish)."""
-    if world <= 1:
-        return ms
-    import torch
-    import torch.distributed as dist
-    t = torch.tensor([ms], dtype=torch.float64, device=device)
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return float(t.item())
-
-
-def replica_throughput(tokens_per_rank, world, steps, total_ms):
-    """Whole-job tokens/s of `world` independent replicas that each processed
-    tokens_per_rank tokens per step for `steps` steps in total_ms (the max over
-    ranks): weak scaling, every rank's tokens count."""
-    return tokens_per_rank * world * steps / (total_ms / 1e3)
 
 
 def kernels_in_region(name, cfg, train):
@@ -279,13 +255,14 @@ def clocks_rejected(clk):
     return bool(sm and smax and sm < 0.8 * smax and not clk.get("reasons"))
 
 
-def gpu_index(local_rank):
+def gpu_index():
+    """nvidia-smi index of the device torch calls cuda:0."""
     vis = os.environ.get("CUDA_VISIBLE_DEVICES")
     if vis:
         ids = [v.strip() for v in vis.split(",") if v.strip()]
-        if local_rank < len(ids) and ids[local_rank].isdigit():
-            return int(ids[local_rank])
-    return local_rank
+        if ids and ids[0].isdigit():
+            return int(ids[0])
+    return 0
 
 
 # ----------------------------------------------------------------------------- oracle (CPU)
@@ -395,14 +372,13 @@ def time_s0(layer, gu_all, dn_all, stream):
     return a.elapsed_time(b)
 
 
-def run_ours(args, cfg, passes, rank, world, local_rank):
+def run_ours(args, cfg, passes):
     import numpy as np
     import torch
-    import torch.distributed as dist
     import mixture_experts_layer_device_gb300 as pkg
     from mixture_experts_layer_device_gb300.layer import MoELayer
 
-    dev = torch.device("cuda", local_rank)
+    dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream()
     peaks, peaks_src = load_peaks()
@@ -414,7 +390,7 @@ def run_ours(args, cfg, passes, rank, world, local_rank):
                      device=dev, stacked=(gu_all, dn_all), ring_rows=ring_rows, gather_sms=args.gather_sms)
     s0_ms = time_s0(layer, gu_all, dn_all, stream)
     sample = None
-    want_cpu = rank == 0 and world == 1 and not args.no_cpu_baseline and not args.profile_run
+    want_cpu = not args.no_cpu_baseline and not args.profile_run
     n_tok = 1 if bwd else 4
     if want_cpu:
         sample = oracle_sample(cfg, passes, x, logits, dy, n_tok)
@@ -438,15 +414,10 @@ def run_ours(args, cfg, passes, rank, world, local_rank):
     if st != 0:
         raise RuntimeError("device status %d after warm-up" % st)
 
-    def barrier():
-        if world > 1:
-            dist.barrier()
-
     def timed(fn, K, trace=False):
         if trace:
             pkg.check(pkg.moe_trace_enable(K * 64 + 64))
             pkg.moe_trace_clear()
-        barrier()
         torch.cuda.synchronize()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
@@ -455,27 +426,25 @@ def run_ours(args, cfg, passes, rank, world, local_rank):
         b.record(stream)
         b.synchronize()
         torch.cuda.synchronize()
-        barrier()
         ms = a.elapsed_time(b)
         recs = pkg.moe_trace_records() if trace else []
         if trace:
             pkg.moe_trace_enable(0)
-        ms = max_over_ranks(ms, world, dev)
         return ms, recs
 
     write_gbs = write_probe_gbs(dev)
-    clocks = Clocks(gpu_index(local_rank))
+    clocks = Clocks(gpu_index())
     if args.profile_run:      # a single, traced timed region (short profiler launch lists)
         total_ms, recs = timed(step, args.steps, trace=True)
         clk = clocks.stop()
     else:
         total_ms, _ = timed(step, args.steps)
         clk = clocks.stop()
-        # measured once more (every rank, if any rank's record rejects it); the
-        # second record is reported
-        if max_over_ranks(float(clocks_rejected(clk)), world, dev) > 0:
+        # measured once more if the clock record rejects it; the second record
+        # is reported
+        if clocks_rejected(clk):
             first = clk
-            clocks = Clocks(gpu_index(local_rank))
+            clocks = Clocks(gpu_index())
             total_ms, _ = timed(step, args.steps)
             clk = clocks.stop()
             clk["remeasured_after"] = {"sm_mhz": first["sm_mhz"], "reasons": first["reasons"]}
@@ -483,8 +452,8 @@ def run_ours(args, cfg, passes, rank, world, local_rank):
         # add gaps between launches to the headline timing)
         _, recs = timed(step, args.steps, trace=True)
     ms_step = total_ms / args.steps
-    tokens = cfg["T"] * world
-    value = replica_throughput(cfg["T"], world, args.steps, total_ms)
+    tokens = cfg["T"]
+    value = tokens * args.steps / (total_ms / 1e3)
 
     fwd_value = value
     if args.profile_run:      # one timed region only (keeps profiler launch lists short)
@@ -645,19 +614,19 @@ def run_ours(args, cfg, passes, rank, world, local_rank):
     t_roof = max(t_tensor, t_hbm)
 
     out = {
-        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "mxfp8" if mx else "bf16",
         "data": "synthetic (seeded N(0,1) tokens, N(0,1/d)/N(0,1/m) bf16 weights, fp32 logits)",
         "config": {"workload": cfg["name"], "pass": "fwd+bwd" if bwd else "fwd", "T": cfg["T"], "d": cfg["d"],
                    "m": cfg["m"], "E": cfg["E"], "k": cfg["k"], "m_shared": cfg["m_shared"],
-                   "experts": cfg["fmt"], "router_bias": cfg["bias"], "parallelism": "replicas" if world > 1 else "1gpu",
+                   "experts": cfg["fmt"], "router_bias": cfg["bias"], "parallelism": "1gpu",
                    "dispatch": ("ring of %d rows, %d gather SMs" % (layer.cfg.ring_rows, layer.cfg.gather_sms or 8)
                                 if layer.cfg.ring_rows else "materialised"),
                    "l2": "inputs larger than L2 (%.1f GB of expert weights read per step)"
                          % (3 * cfg["E"] * cfg["d"] * cfg["m"] * (1.03 if mx else 2) / 1e9)},
         "fwd_tokens_per_s": round(fwd_value, 1),
-        "layer_roofline": {"tokens_per_s": round(cfg["T"] * world / t_roof, 1), "frac": round(value / (cfg["T"] * world / t_roof), 4),
+        "layer_roofline": {"tokens_per_s": round(cfg["T"] / t_roof, 1), "frac": round(value / (cfg["T"] / t_roof), 4),
                            "bound": "tensor" if t_tensor >= t_hbm else "hbm", "t_tensor_ms": round(t_tensor * 1e3, 3),
                            "t_hbm_ms": round(t_hbm * 1e3, 3), "peaks": peaks_src},
         "roofline": {"kernel": dom, "bound": bound, "achieved": round(achieved, 1), "peak": round(peak, 1),
@@ -756,32 +725,19 @@ def main():
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
-    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
-    if world != args.gpus:
-        ap.error("--gpus %d but WORLD_SIZE=%d (launch N>1 with torch.distributed.run)" % (args.gpus, world))
-
     if args.impl == "reference":
+        # the oracle on the host cores: rank 0 alone runs it
         if rank == 0:
             print(json.dumps(run_reference(args, cfg, passes)), flush=True)
         return
+    if args.gpus != 1 or world != 1:
+        ap.error("the layer runs on one GPU (no sharding, no exchange step): --gpus must be 1 and "
+                 "WORLD_SIZE unset or 1 (got --gpus %d, WORLD_SIZE=%d)" % (args.gpus, world))
 
     import __graft_entry__
-    if world > 1:
-        import torch
-        import torch.distributed as dist
-        torch.cuda.set_device(local_rank)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
-        if rank == 0:
-            __graft_entry__.build()
-        dist.barrier()
-    else:
-        __graft_entry__.build()
-    out = run_ours(args, cfg, passes, rank, world, local_rank)
-    if rank == 0:
-        print(json.dumps(out), flush=True)
-    if world > 1:
-        import torch.distributed as dist
-        dist.destroy_process_group()
+    __graft_entry__.build()
+    out = run_ours(args, cfg, passes)
+    print(json.dumps(out), flush=True)
 
 
 if __name__ == "__main__":

@@ -74,14 +74,23 @@ typedef enum {
  * kernels drain and return, moe_get_status then reports MOE_ERR_TIMEOUT, and
  * the outputs of that call are undefined.  The CUDA context stays usable. */
 #define MOE_FLAG_DEBUG_STARVE 2
+/* Test hook for the fused quantisation points (MXFP8 experts; ignored with
+ * BF16 experts): moe_forward also stores the fp32 SwiGLU output h -- the
+ * values the gate/up GEMM's epilogue quantises -- in the workspace buffer
+ * "h_dump" [padded rows, m] fp32, and moe_backward stores the bf16 dG|dU
+ * values the SwiGLU-backward epilogue quantises in "dGU_dump" [padded rows,
+ * 2m] bf16 (moe_buffer_info gives their offsets).  Quantising those dumps
+ * with the format's definition must reproduce the codes and scales the
+ * kernels wrote, byte for byte.  Nothing else changes. */
+#define MOE_FLAG_DEBUG_DUMP 4
 
 /*
  * Layer shape.  T tokens, hidden d, expert intermediate m, E experts, top-k k.
  * Supported: 1 <= k <= min(E, 16), E <= 1024, d % 256 == 0, m % 128 == 0,
  * m_shared % 128 == 0 (0 = no shared expert), T*k < 2^31 - 127*E.  dtype is
  * the routed experts' arithmetic; the shared expert is always BF16.  flags:
- * MOE_FLAG_BACKWARD and/or MOE_FLAG_DEBUG_STARVE, or 0 (moe_backward needs a
- * workspace sized with MOE_FLAG_BACKWARD).
+ * any of MOE_FLAG_BACKWARD, MOE_FLAG_DEBUG_STARVE and MOE_FLAG_DEBUG_DUMP, or 0
+ * (moe_backward needs a workspace sized with MOE_FLAG_BACKWARD).
  *
  * Dispatch ring (MXFP8 only; "Mixture-of-Kittens" wiki page, flowchart, and
  * daily-ai-frontier summary, TL;DR: a fixed-size token ring between the
@@ -163,6 +172,7 @@ size_t moe_saved_bytes(const moe_config *cfg);
  * "hT_sf" (saved: column-blocked codes of the wgrad operands); "xs",
  * "xs_sf", "hq", "hq_sf", "s_out", "dX", "g" and, with MXFP8 experts,
  * "dOq", "dOq_sf", "dOT", "dOT_sf", "dGUq", "dGUq_sf", "dGUT", "dGUT_sf"
+ * and, with MOE_FLAG_DEBUG_DUMP, "h_dump" and "dGU_dump"
  * (workspace; "dO" and "dGU" exist only with BF16 experts, whose backward
  * materialises them in bf16).  Row-indexed buffers use padded rows (see
  * moe_forward).  Returns MOE_OK or MOE_ERR_ARG (unknown name / buffer absent
@@ -297,7 +307,10 @@ int moe_backward(const moe_config *cfg, const void *dy, const void *x, const moe
  * different streams, or from several host threads) race and corrupt each
  * other's results.  Calls on one stream are ordered and safe.  The first call
  * on a device looks up the array's device address (cudaGetSymbolAddress); make
- * that first call before any stream capture.  Allocates nothing.
+ * that first call before any stream capture.  The address is kept for the life
+ * of the process: calls made after cudaDeviceReset (or anything else that
+ * destroys and re-creates the device's primary context) are not supported.
+ * Allocates nothing.
  */
 #define MOE_ROUTE_NOALLOC_MAX_SLOTS 262144
 #define MOE_ROUTE_NOALLOC_MAX_EXPERTS 1024

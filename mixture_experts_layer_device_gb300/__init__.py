@@ -17,6 +17,7 @@ LIB_PATH = _build.LIB
 MOE_BF16, MOE_MXFP8 = 0, 1
 MOE_FLAG_BACKWARD = 1
 MOE_FLAG_DEBUG_STARVE = 2
+MOE_FLAG_DEBUG_DUMP = 4
 STATUS = {0: "ok", -1: "invalid argument", -2: "unsupported shape", -3: "pointer not 16-byte aligned",
           -4: "CUDA error", -5: "device is not sm_103", -6: "a device-side wait timed out"}
 

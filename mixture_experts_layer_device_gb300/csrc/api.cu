@@ -34,6 +34,7 @@ constexpr size_t kCublasWorkspace = 32u << 20;
 struct Dims {
   int T, d, m, E, k, ms;
   bool mx, bwd, starve;
+  bool dump;           // MOE_FLAG_DEBUG_DUMP with MXFP8 experts
   bool ring;           // MXFP8 forward dispatch through the persistent ring kernel
   float aux_alpha;     // load-balancing term weight (0 = none)
   int ring_slots;      // ring capacity in 128-row tiles
@@ -48,7 +49,7 @@ int check_config(const moe_config *c, Dims *D) {
     return MOE_ERR_ARG;
   if (c->k > c->E || c->k > 16 || c->E > 1024) return MOE_ERR_SHAPE;
   if (c->dtype != MOE_BF16 && c->dtype != MOE_MXFP8) return MOE_ERR_ARG;
-  if ((c->flags & ~(MOE_FLAG_BACKWARD | MOE_FLAG_DEBUG_STARVE)) != 0) return MOE_ERR_ARG;
+  if ((c->flags & ~(MOE_FLAG_BACKWARD | MOE_FLAG_DEBUG_STARVE | MOE_FLAG_DEBUG_DUMP)) != 0) return MOE_ERR_ARG;
   if (c->d % 256 || c->m % 128 || c->m_shared % 128) return MOE_ERR_SHAPE;
   if (c->ring_rows < 0 || c->gather_sms < 0 || c->gather_sms > 64) return MOE_ERR_ARG;
   if (c->ring_rows > 0 && c->dtype != MOE_MXFP8) return MOE_ERR_ARG;
@@ -67,6 +68,7 @@ int check_config(const moe_config *c, Dims *D) {
   D->mx = c->dtype == MOE_MXFP8;
   D->bwd = (c->flags & MOE_FLAG_BACKWARD) != 0;
   D->starve = (c->flags & MOE_FLAG_DEBUG_STARVE) != 0;
+  D->dump = D->mx && (c->flags & MOE_FLAG_DEBUG_DUMP) != 0;
   D->ring = c->ring_rows > 0;
   D->aux_alpha = c->aux_alpha;
   D->ring_slots = c->ring_rows / 128;
@@ -170,7 +172,9 @@ void ws_layout(const Dims &D, Layout &L) {
     L.add("s_h", D.Tp * D.ms * 2);
     L.add("s_out", D.Tp * D.d * 2);
   }
+  if (D.dump) L.add("h_dump", D.Rp * D.m * 4);  // fp32 h before its quantisation (test hook)
   if (!D.bwd) return;
+  if (D.dump) L.add("dGU_dump", D.Rp * 2 * D.m * 2);  // bf16 dG|dU before their quantisation
   L.add("router_g", static_cast<size_t>(D.T) * D.E * 2);  // bf16 dlogits for the router backward
   L.add("g", D.R * 4);
   if (!D.mx) L.add("dO", D.Rp * D.d * 2);  // MXFP8 keeps dO only as codes
@@ -241,12 +245,11 @@ int device_info(DeviceInfo *out) {
 
 // 2-D K-major tensor map: `rows` rows of `inner` elements (bf16 or 1-byte codes),
 // box 128 rows x 128 bytes, 128-byte swizzle, zero fill out of bounds.
-bool make_map(CUtensorMap *m, const void *base, bool bytes1, uint64_t inner, uint64_t rows,
-              uint32_t box_rows = 128) {
+bool make_map(CUtensorMap *m, const void *base, bool bytes1, uint64_t inner, uint64_t rows) {
   const uint64_t esz = bytes1 ? 1 : 2;
   cuuint64_t dims[2] = {inner, rows};
   cuuint64_t strides[1] = {inner * esz};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / esz), box_rows};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / esz), 128};
   cuuint32_t estr[2] = {1, 1};
   const CUresult r = g_encode(m, bytes1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                               2, const_cast<void *>(base), dims, strides, box, estr,
@@ -332,12 +335,6 @@ bool make_sf_map(CUtensorMap *m, const void *base, uint64_t bytes) {
 // the pair's cross-SM coupling measured slower.
 bool use_pair(const Gemm &q) { return q.bn == 256 && !q.mx; }
 
-// MXFP8 GEMMs run on clusters of two CTAs sharing the A tile (TMA multicast)
-// whenever the N-tiles pair up.
-bool use_mc(const Gemm &q) {
-  return q.mx && q.g.n_tiles % 2 == 0 && moe::gemm_mc_max_clusters(q.mx, q.bn, q.epi) > 0;
-}
-
 int run_pair(const Gemm &q, const DeviceInfo &dev, cudaStream_t s) {
   moe::PairMaps m;
   memset(&m, 0, sizeof(m));
@@ -368,16 +365,6 @@ int run_gemm(const char *name, const Gemm &q, const DeviceInfo &dev, cudaStream_
                                                               q.zero_counts, s));
     if (rc != MOE_OK) return rc;
     g.skip_empty = 1;
-  }
-  if (use_mc(q)) {
-    // clusters of two sharing A: A is loaded in 64-row halves
-    CUtensorMap ta_half;
-    if (!make_map(&ta_half, q.a, q.mx, q.K, q.a_rows, 64)) return MOE_ERR_CUDA;
-    const int maxc = moe::gemm_mc_max_clusters(q.mx, q.bn, q.epi);
-    if (maxc <= 0) return MOE_ERR_CUDA;
-    long clusters = (q.max_tiles / 2) < (dev.num_sms / 2) ? q.max_tiles / 2 : dev.num_sms / 2;
-    if (clusters > maxc) clusters = maxc;
-    return cuda_status(moe::launch_gemm_mc(q.mx, q.bn, q.epi, ta_half, tb, g, static_cast<int>(clusters), s));
   }
   CUtensorMap ta;
   if (!make_map(&ta, q.a, q.mx, q.K, q.a_rows)) return MOE_ERR_CUDA;
@@ -657,6 +644,10 @@ int moe_forward(const moe_config *cfg, const void *x, const float *logits, const
       q.g.ldT = D.Rp;
     }
     q.g.m_half = D.m;
+    if (D.dump) {
+      q.g.dump = reinterpret_cast<float *>(W.ptr(ws, "h_dump"));
+      q.g.ld_dump = D.m;
+    }
     if (D.starve) {
       q.g.debug_starve = 1;
       q.g.timeout_ns = kStarveTimeoutNs;
@@ -834,8 +825,8 @@ int moe_backward(const moe_config *cfg, const void *dy, const void *x, const moe
     q.g.sfb = static_cast<const uint8_t *>(Wt->dn_t_scale);
     q.g.sfb_kg = D.d / 128;
     // MXFP8: dGU only as codes, row-blocked (gate/up dgrad) and column-blocked
-    // (gate/up wgrad); BF16: dGU in bf16
-    q.g.out = mx ? nullptr : dGU;
+    // (gate/up wgrad), plus the bf16 values with the dump flag; BF16: dGU in bf16
+    q.g.out = mx ? (D.dump ? W.ptr(ws, "dGU_dump") : nullptr) : dGU;
     q.g.ldo = 2 * D.m;
     q.g.outq = mx ? u8("dGUq") : nullptr;
     q.g.outq_sf = u8("dGUq_sf");

@@ -130,16 +130,6 @@ MOE_DEV void tma_load_2d(const CUtensorMap *map, uint64_t *bar, void *dst, int c
       "l"(map), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
       : "memory");
 }
-// 2-D TMA load multicast to the CTAs of `mask` in the cluster: the box lands at
-// `dst`'s offset in each of them and completes bytes on the mbarrier at
-// `bar`'s offset in each.
-MOE_DEV void tma_load_2d_mc(const CUtensorMap *map, uint64_t *bar, void *dst, int c0, int c1, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
-      "l"(map), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "h"(mask)
-      : "memory");
-}
 MOE_DEV void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
   asm volatile(
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
@@ -218,14 +208,6 @@ MOE_DEV void mma_commit(uint64_t *bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
           smem_u32(bar))
-      : "memory");
-}
-// Commit to the mbarrier at `bar`'s offset in every CTA of `mask` (cluster).
-MOE_DEV void mma_commit_mc(uint64_t *bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-          smem_u32(bar)),
-      "h"(mask)
       : "memory");
 }
 // Copy 32 rows x 16 bytes of shared memory into TMEM, replicated into all four

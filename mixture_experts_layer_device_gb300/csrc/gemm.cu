@@ -280,13 +280,7 @@ __host__ __device__ constexpr int epi_warps() {
   return 8;
 }
 
-// MC: clusters of two CTAs compute the same 128-row M-tile for two adjacent
-// N-tiles (t = 2i + cluster rank); each loads one 64-row half of the A tile
-// and multicasts it to both, so an SM loads 0.5 A + B per stage instead of
-// A + B.  A stage of one CTA is refilled only after both CTAs' MMAs released
-// it (empty barriers count two arrivals; commits are multicast).  tmA then has
-// a 64-row box.
-template <bool MX, int BN, int EPI, bool RING = false, bool MC = false>
+template <bool MX, int BN, int EPI, bool RING = false>
 __global__ void __launch_bounds__(64 + 32 * epi_warps<EPI, BN>(), 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const GemmArgs g) {
@@ -300,15 +294,9 @@ __global__ void __launch_bounds__(64 + 32 * epi_warps<EPI, BN>(), 1)
       return;
     }
   }
-  static_assert(!(RING && MC), "the ring launch is not clustered");
-  // GEMM CTAs (clusters with MC): this one's index among them and their number
-  const uint32_t crank = MC ? cluster_rank() : 0u;
-  const int cta = MC ? static_cast<int>(blockIdx.x >> 1)
-                     : static_cast<int>(blockIdx.x) - (RING ? g.ring.gather_ctas : 0);
-  const int ncta = MC ? static_cast<int>(gridDim.x >> 1)
-                      : static_cast<int>(gridDim.x) - (RING ? g.ring.gather_ctas : 0);
-  // work item i -> tile (MC: the pair of adjacent N-tiles 2i, 2i + 1)
-  auto tile_of = [&](int i) { return MC ? 2 * i + static_cast<int>(crank) : i; };
+  // GEMM CTAs: this one's index among them and their number
+  const int cta = static_cast<int>(blockIdx.x) - (RING ? g.ring.gather_ctas : 0);
+  const int ncta = static_cast<int>(gridDim.x) - (RING ? g.ring.gather_ctas : 0);
   uint8_t *sf_base = smem + C::STAGES * C::STAGE_BYTES;
   uint8_t *staging = sf_base + C::STAGES * C::SF_STAGE;
   uint64_t *bars = reinterpret_cast<uint64_t *>(staging + C::STAGING_BYTES);
@@ -326,7 +314,7 @@ __global__ void __launch_bounds__(64 + 32 * epi_warps<EPI, BN>(), 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], MC ? 2 : 1);
+      mbar_init(&empty[s], 1);
     }
     for (int a = 0; a < C::NUM_ACC; ++a) {
       mbar_init(&tfull[a], 1);
@@ -342,10 +330,9 @@ __global__ void __launch_bounds__(64 + 32 * epi_warps<EPI, BN>(), 1)
     tc_fence_before();
   }
   __syncthreads();
-  if constexpr (MC) cluster_sync();  // the peer's barriers exist before any multicast or commit
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  const int total = total_tiles<C::BK, BN, EPI>(g) / (MC ? 2 : 1);  // work items
+  const int total = total_tiles<C::BK, BN, EPI>(g);
 
   if (warp == 0) {
     // ------------------------------------------------ TMA producer
@@ -357,7 +344,7 @@ __global__ void __launch_bounds__(64 + 32 * epi_warps<EPI, BN>(), 1)
       int armed[C::STAGES];
       for (int s = 0; s < C::STAGES; ++s) armed[s] = -1;
       for (int i = cta; i < total && !*abort_flag && (RING || !g.debug_starve); i += ncta) {
-        const Tile ti = decode_tile<C::BK, BN, EPI>(g, tile_of(i));
+        const Tile ti = decode_tile<C::BK, BN, EPI>(g, i);
         int a_row = ti.a_row;  // row of A to load (the tile's ring slot with a ring)
         if constexpr (RING) {
           const int u = ti.a_row >> 7;
@@ -374,11 +361,7 @@ __global__ void __launch_bounds__(64 + 32 * epi_warps<EPI, BN>(), 1)
           mbar_arrive_expect_tx(&full[stage], C::TX_BYTES);
           armed[stage] = static_cast<int>(ph);
           const int kc = ti.k0 + kb * C::BK;
-          if constexpr (MC)
-            tma_load_2d_mc(&tmA, &full[stage], sa + crank * 64 * 128, kc, a_row + static_cast<int>(crank) * 64,
-                           0x3);
-          else
-            tma_load_2d(&tmA, &full[stage], sa, kc, a_row);
+          tma_load_2d(&tmA, &full[stage], sa, kc, a_row);
           tma_load_2d(&tmB, &full[stage], sb, kc, ti.b_row0);
           if (BN == 256) tma_load_2d(&tmB, &full[stage], sb + 128 * 128, kc, ti.b_row1);
           if constexpr (MX) {
@@ -415,7 +398,7 @@ __global__ void __launch_bounds__(64 + 32 * epi_warps<EPI, BN>(), 1)
       uint32_t aph = 0;
       bool ok = true;
       for (int i = cta; i < total && ok; i += ncta) {
-        const Tile ti = decode_tile<C::BK, BN, EPI>(g, tile_of(i));
+        const Tile ti = decode_tile<C::BK, BN, EPI>(g, i);
         if (ti.nk == 0 && g.skip_empty) continue;  // zeros written by another launch
         if (!mbar_wait(&tempty[acc], aph ^ 1u, abort_flag, g.status, g.timeout_ns)) break;
         tc_fence_after();
@@ -447,10 +430,7 @@ __global__ void __launch_bounds__(64 + 32 * epi_warps<EPI, BN>(), 1)
             else
               mma_bf16(dt, ad, bd, C::IDESC, accum);
           }
-          if constexpr (MC)
-            mma_commit_mc(&empty[stage], 0x3);  // both CTAs' copies of this stage are free
-          else
-            mma_commit(&empty[stage]);
+          mma_commit(&empty[stage]);
           if (++stage == C::STAGES) {
             stage = 0;
             ph ^= 1u;
@@ -487,7 +467,7 @@ __global__ void __launch_bounds__(64 + 32 * epi_warps<EPI, BN>(), 1)
     int acc = 0;
     uint32_t aph = 0;
     for (int i = cta; i < total; i += ncta) {
-      const Tile ti = decode_tile<C::BK, BN, EPI>(g, tile_of(i));
+      const Tile ti = decode_tile<C::BK, BN, EPI>(g, i);
       if (ti.nk == 0 && g.skip_empty) continue;  // zeros written by another launch
       if constexpr (EPI == EPI_SWIGLU_BWD) {
         // The saved G|U rows this tile's epilogue reads come from HBM: pull them
@@ -517,7 +497,6 @@ __global__ void __launch_bounds__(64 + 32 * epi_warps<EPI, BN>(), 1)
   }
 
   __syncthreads();
-  if constexpr (MC) cluster_sync();  // no CTA leaves while its peer may still multicast into it
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, C::TMEM_COLS);
@@ -538,62 +517,6 @@ cudaError_t launch_one(const CUtensorMap &ta, const CUtensorMap &tb, const GemmA
   }
   gemm_kernel<MX, BN, EPI><<<grid, 64 + 32 * epi_warps<EPI, BN>(), C::SMEM, s>>>(ta, tb, g);
   return cudaGetLastError();
-}
-
-// Clusters of two (MC): grid = 2 x clusters.
-template <bool MX, int BN, int EPI>
-cudaError_t launch_one_mc(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs &g, int clusters,
-                          cudaStream_t s) {
-  using C = Cfg<MX, BN>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    const cudaError_t e = cudaFuncSetAttribute(gemm_kernel<MX, BN, EPI, false, true>,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               static_cast<int>(C::SMEM));
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2 * clusters, 1, 1);
-  cfg.blockDim = dim3(64 + 32 * epi_warps<EPI, BN>(), 1, 1);
-  cfg.dynamicSmemBytes = C::SMEM;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemm_kernel<MX, BN, EPI, false, true>, ta, tb, g);
-}
-
-template <bool MX, int BN, int EPI>
-int max_clusters_mc_query() {
-  using C = Cfg<MX, BN>;
-  if (cudaFuncSetAttribute(gemm_kernel<MX, BN, EPI, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(C::SMEM)) != cudaSuccess)
-    return 0;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2, 1, 1);
-  cfg.blockDim = dim3(64 + 32 * epi_warps<EPI, BN>(), 1, 1);
-  cfg.dynamicSmemBytes = C::SMEM;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, gemm_kernel<MX, BN, EPI, false, true>, &cfg) != cudaSuccess) return 0;
-  return n;
-}
-
-template <bool MX, int BN, int EPI>
-int max_clusters_mc() {
-  static int memo[64] = {};
-  return per_device_memo(memo, max_clusters_mc_query<MX, BN, EPI>);
 }
 
 int ring_ctas_query() {
@@ -619,27 +542,6 @@ int ring_ctas_resident() {
 }  // namespace
 
 int ring_max_ctas() { return ring_ctas_resident(); }
-
-cudaError_t launch_gemm_mc(bool mx, int bn, int epi, const CUtensorMap &ta_half, const CUtensorMap &tb,
-                           const GemmArgs &g, int clusters, cudaStream_t s) {
-  if (clusters <= 0) return cudaSuccess;
-#define MOE_GEMM_MC(BNV, EPIV) \
-  if (mx && bn == BNV && epi == EPIV) return launch_one_mc<true, BNV, EPIV>(ta_half, tb, g, clusters, s);
-  MOE_GEMM_MC(256, EPI_STORE)
-  MOE_GEMM_MC(256, EPI_SWIGLU)
-  MOE_GEMM_MC(256, EPI_SWIGLU_BWD)
-  MOE_GEMM_MC(128, EPI_SWIGLU_BWD)
-#undef MOE_GEMM_MC
-  return cudaErrorInvalidValue;
-}
-
-int gemm_mc_max_clusters(bool mx, int bn, int epi) {
-  if (mx && bn == 256 && epi == EPI_STORE) return max_clusters_mc<true, 256, EPI_STORE>();
-  if (mx && bn == 256 && epi == EPI_SWIGLU) return max_clusters_mc<true, 256, EPI_SWIGLU>();
-  if (mx && bn == 256 && epi == EPI_SWIGLU_BWD) return max_clusters_mc<true, 256, EPI_SWIGLU_BWD>();
-  if (mx && bn == 128 && epi == EPI_SWIGLU_BWD) return max_clusters_mc<true, 128, EPI_SWIGLU_BWD>();
-  return 0;
-}
 
 cudaError_t launch_gemm_ring(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs &g, int grid,
                              cudaStream_t s) {

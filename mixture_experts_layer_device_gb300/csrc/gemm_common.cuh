@@ -409,6 +409,11 @@ MOE_DEV void epilogue_tile_split(const GemmArgs &g, const OutView &vO, const Out
     }
 #pragma unroll
     for (int i = 0; i < 64; ++i) G[i] = silu(G[i]) * U[i];  // h, in place
+    if (g.dump) {  // test hook: the fp32 h the quantisers below read
+      const OutView vD = out_view(g.dump, g.ld_dump, g.out_rows, 4);
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) st.put(vD, gr + 16 * c, col + 16 * c, row0, lane);
+    }
     if (g.out) {
       st.put_bf16(vO, G, col, row0, lane);
       st.put_bf16(vO, G + 32, col + 32, row0, lane);

@@ -156,6 +156,8 @@ struct GemmArgs {
   const void *aux;    // SWIGLU_BWD: saved G|U bf16
   long ld_aux;
   int m_half;         // SWIGLU / SWIGLU_BWD: m
+  float *dump;        // SWIGLU (tests): fp32 h before quantisation [rows, ld_dump] (may be NULL)
+  long ld_dump;
   int skip_empty;     // GROUP_K: tiles with an empty reduction are left to launch_zero_empty_experts
   int *status;
   unsigned long long timeout_ns;  // limit of every wait in the launch
@@ -176,15 +178,6 @@ cudaError_t launch_zero_empty_experts(void *dW, int E, long expert_bytes, const 
 // coalesced global stores, rows < args.out_rows.
 cudaError_t launch_gemm(bool mx, int bn, int epi, const CUtensorMap &ta, const CUtensorMap &tb,
                         const GemmArgs &args, int grid, cudaStream_t s);
-
-// The same GEMM on clusters of two CTAs sharing the A tile (MXFP8, for the
-// (bn, epi) pairs gemm_mc_max_clusters() is non-zero for): the two CTAs of a
-// cluster compute adjacent N-tiles of one M-tile and each loads one 64-row
-// half of A for both (TMA multicast).  `ta_half` maps A with a 64-row box;
-// args.n_tiles must be even.  `clusters` <= gemm_mc_max_clusters().
-cudaError_t launch_gemm_mc(bool mx, int bn, int epi, const CUtensorMap &ta_half, const CUtensorMap &tb,
-                           const GemmArgs &args, int clusters, cudaStream_t s);
-int gemm_mc_max_clusters(bool mx, int bn, int epi);
 
 // The MXFP8 gate/up GEMM with SwiGLU epilogue fed by the ring (args.ring):
 // one cooperative launch of `grid` CTAs (all co-resident, one per SM), of

@@ -30,7 +30,8 @@ std::mutex g_mu;
 void *g_scratch_dev[64] = {};
 
 // Device address of the scratch array on the current device, looked up once per
-// device (the first call on a device does this set-up).
+// device (the first call on a device does this set-up) and kept for the life of
+// the process; it is not looked up again after a device reset.
 int scratch_address(void **out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;

@@ -23,7 +23,8 @@ class MoELayer:
 
     ``ring_rows`` > 0 (MXFP8) runs the forward's dispatch and gate/up GEMM as
     one persistent launch through a ring of that many rows, ``gather_sms`` of
-    whose SMs gather (0 = the library default).
+    whose SMs gather (0 = the library default).  ``flags`` adds moe_config
+    flag bits (the test hooks MOE_FLAG_DEBUG_STARVE / MOE_FLAG_DEBUG_DUMP).
 
     ``expert(e)`` returns the bf16 masters (W_gu [2m, d], W_dn [d, m]) of
     expert e as device tensors; they are converted expert by expert into the
@@ -34,7 +35,7 @@ class MoELayer:
     """
 
     def __init__(self, T, d, m, E, k, fmt, expert=None, shared=None, backward=False, device="cuda",
-                 stacked=None, ring_rows=0, gather_sms=0, aux_alpha=0.0):
+                 stacked=None, ring_rows=0, gather_sms=0, aux_alpha=0.0, flags=0):
         self.T, self.d, self.m, self.E, self.k = T, d, m, E, k
         self.fmt = fmt
         self.mx = fmt == "mxfp8"
@@ -42,7 +43,7 @@ class MoELayer:
         self.backward_enabled = backward
         self.device = device
         self.cfg = config(T, d, m, E, k, self.ms, MOE_MXFP8 if self.mx else MOE_BF16,
-                          MOE_FLAG_BACKWARD if backward else 0, ring_rows, gather_sms, aux_alpha)
+                          (MOE_FLAG_BACKWARD if backward else 0) | flags, ring_rows, gather_sms, aux_alpha)
         self.Rp = moe_padded_rows(self.cfg)
         self.ws = _u8(moe_workspace_bytes(self.cfg), device)
         self.saved = _u8(moe_saved_bytes(self.cfg), device) if backward else None

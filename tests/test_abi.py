@@ -85,7 +85,7 @@ def test_saved_wgrad_operands_by_format(pkg):
 
 @pytest.mark.parametrize("bad,code", [
     (dict(d=100), -2), (dict(m=64), -2), (dict(k=9), -2), (dict(k=0), -1), (dict(E=2000), -2),
-    (dict(T=0), -1), (dict(flags=4), -1), (dict(dtype=7), -1), (dict(m_shared=100), -2),
+    (dict(T=0), -1), (dict(flags=8), -1), (dict(dtype=7), -1), (dict(m_shared=100), -2),
     (dict(ring_rows=256), -1),                          # the ring is MXFP8-only
     (dict(dtype=1, ring_rows=200), -2), (dict(dtype=1, ring_rows=-128), -1),
     (dict(dtype=1, ring_rows=256, gather_sms=65), -1), (dict(dtype=1, d=8448, ring_rows=256), -2),
@@ -122,6 +122,26 @@ def test_debug_flag_accepted_unknown_flags_rejected(pkg):
     assert pkg.moe_workspace_bytes(cfg) == pkg.moe_workspace_bytes(pkg.config(64, 256, 128, 8, 2, 0, "bf16",
                                                                               pkg.MOE_FLAG_BACKWARD))
     assert pkg.moe_workspace_bytes(pkg.config(64, 256, 128, 8, 2, 0, "bf16", 8)) == 0
+
+
+def test_dump_flag_adds_the_dump_buffers_only_with_mxfp8(pkg):
+    T, d, m, E, k = 300, 256, 128, 8, 2
+    for fmt in ("bf16", "mxfp8"):
+        base = pkg.config(T, d, m, E, k, 0, fmt, pkg.MOE_FLAG_BACKWARD)
+        dump = pkg.config(T, d, m, E, k, 0, fmt, pkg.MOE_FLAG_BACKWARD | pkg.MOE_FLAG_DEBUG_DUMP)
+        if fmt == "bf16":
+            assert pkg.moe_workspace_bytes(dump) == pkg.moe_workspace_bytes(base)
+            with pytest.raises(Exception):
+                pkg.moe_buffer_info(dump, 1, "h_dump")
+            continue
+        Rp = pkg.moe_padded_rows(dump)
+        assert pkg.moe_buffer_info(dump, 1, "h_dump")[1] == Rp * m * 4
+        assert pkg.moe_buffer_info(dump, 1, "dGU_dump")[1] == Rp * 2 * m * 2
+        assert pkg.moe_workspace_bytes(dump) >= pkg.moe_workspace_bytes(base) + Rp * m * 6
+        fwd_only = pkg.config(T, d, m, E, k, 0, fmt, pkg.MOE_FLAG_DEBUG_DUMP)
+        pkg.moe_buffer_info(fwd_only, 1, "h_dump")
+        with pytest.raises(Exception):
+            pkg.moe_buffer_info(fwd_only, 1, "dGU_dump")
 
 
 def test_status_strings(pkg):

@@ -27,8 +27,11 @@ def run_forward(case, train=True):
 
 
 def saved_rows(case, name, width, dtype="bf16"):
+    """Rows [0, poff[E]) of a saved row buffer (the rows past the last expert's
+    padded block are never written)."""
     L = case.layer
-    t = L.view(0, name, dtype, (L.Rp, width))
+    n = int(L.view(0, "poff", "i32", (L.E + 1,))[L.E].item())
+    t = L.view(0, name, dtype, (L.Rp, width))[:n]
     return t.float().cpu().numpy().astype(np.float64)
 
 
