@@ -33,6 +33,8 @@ if ROOT not in sys.path:
 METRIC = "MoE-layer tokens/s fwd & fwd+bwd on 1 GB300; % of GEMM/HBM roofline"
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 MX_OVER_BF16 = 2.0   # nominal dense MXFP8 : BF16 tensor-core ratio (4.5 : 2.25 PFLOP/s)
+# GB300's published dense peaks (context column of every fraction)
+NOMINAL = {"hbm_gbs": 7900.0, "bf16_tflops": 2250.0, "mx_tflops": 4500.0}
 
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from an
 # ncu capture, keyed by (workload, kernel).  An entry is removed whenever the
@@ -174,23 +176,125 @@ def write_probe_gbs(dev):
     return gbs
 
 
-def kernel_roofline(cfg, name, train, ms_per_step, peaks):
+def mxfp8_peak_probe(dev):
+    """Dense MXFP8 GEMM rate of this GPU: the vendor library's block-scaled
+    E4M3 GEMM (torch._scaled_mm with E8M0 scales) at 8192^3, as a burst (best
+    of 10 single calls) and sustained (calls back to back for about 3 s, under
+    the power cap).  Taken before the timed region; None fields if the library
+    path is unavailable."""
+    import torch
+    M = N = K = 8192
+    try:
+        g = torch.Generator(device=dev).manual_seed(0)
+        a = torch.randn((M, K), device=dev, generator=g).to(torch.float8_e4m3fn)
+        b = torch.randn((N, K), device=dev, generator=g).to(torch.float8_e4m3fn)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        best, f_best = float("inf"), None
+        for shape_a, shape_b in (((M * K // 32,), (N * K // 32,)), ((M, K // 32), (N, K // 32))):
+            sa = torch.full(shape_a, 127, dtype=torch.uint8, device=dev).view(torch.float8_e8m0fnu)
+            sb = torch.full(shape_b, 127, dtype=torch.uint8, device=dev).view(torch.float8_e8m0fnu)
+
+            def f(sa=sa, sb=sb):
+                return torch._scaled_mm(a, b.t(), scale_a=sa, scale_b=sb, out_dtype=torch.bfloat16)
+
+            try:
+                for _ in range(3):
+                    f()
+                torch.cuda.synchronize()
+            except Exception:     # this scale layout is not accepted by this torch build
+                continue
+            for _ in range(10):
+                ev[0].record()
+                f()
+                ev[1].record()
+                ev[1].synchronize()
+                ms = ev[0].elapsed_time(ev[1])
+                if ms < best:
+                    best, f_best = ms, f
+        if f_best is None:
+            raise RuntimeError("no block-scaled MXFP8 GEMM path")
+        f = f_best
+        n, t0 = 0, time.time()
+        ev[0].record()
+        while time.time() - t0 < 3.0:
+            for _ in range(20):
+                f()
+            n += 20
+            torch.cuda.synchronize()
+        ev[1].record()
+        ev[1].synchronize()
+        sus = ev[0].elapsed_time(ev[1]) / n
+        fl = 2.0 * M * N * K
+        return {"burst_tflops": round(fl / (best / 1e3) / 1e12, 1), "sustained_tflops": round(fl / (sus / 1e3) / 1e12, 1),
+                "how": "torch._scaled_mm E4M3 x E4M3 with E8M0 block scales (vendor library), 8192^3, flat and 2-D "
+                       "scale tensors; burst = best of 10 calls each, sustained = back to back for 3 s"}
+    except Exception as exc:  # no block-scaled library path here: fall back, and say so
+        return {"burst_tflops": None, "sustained_tflops": None, "how": "unavailable: %s" % str(exc)[:160]}
+
+
+def tensor_peaks(peaks, peaks_src, mxp):
+    """Denominators of every fraction: HBM copy bandwidth, BF16 and MXFP8
+    dense tensor rates, each measured on this GPU.  The primary fraction uses
+    the burst rates (the stricter ones); sustained and published-nominal
+    fractions are reported beside it."""
+    P = {"hbm": peaks["hbm_gbs"], "bf16": peaks["bf16_tflops"], "bf16_s": peaks["bf16_tflops_sustained"],
+         "src": peaks_src}
+    if mxp and mxp.get("burst_tflops"):
+        P.update(mx=mxp["burst_tflops"], mx_s=mxp["sustained_tflops"], mx_src="measured MXFP8 GEMM (%s)" % mxp["how"])
+    else:
+        P.update(mx=MX_OVER_BF16 * P["bf16"], mx_s=MX_OVER_BF16 * P["bf16_s"],
+                 mx_src="%.0f x %s BF16 (MXFP8 probe unavailable)" % (MX_OVER_BF16, peaks_src))
+    return P
+
+
+def kernel_roofline(cfg, name, train, ms_per_step, P):
     """Bound, achieved and peak of one kernel: the larger of its tensor time
     (FLOPs at the tensor peak of its arithmetic) and its HBM time (algorithmic
-    bytes at the copy bandwidth) names the bound."""
+    bytes at the copy bandwidth) names the bound.  `frac_sustained` and
+    `frac_nominal` divide the same achieved rate by the sustained tensor rate
+    and by GB300's published dense peaks."""
     w = kernel_work(cfg, name, train)
     if w is None or ms_per_step <= 0:
         return None
     flops, byts, mx = w
-    tpeak = peaks["bf16_tflops_sustained"] * (MX_OVER_BF16 if mx else 1.0)
+    tpeak = P["mx"] if mx else P["bf16"]
     t_tensor = flops / (tpeak * 1e12)
-    t_hbm = byts / (peaks["hbm_gbs"] * 1e9)
+    t_hbm = byts / (P["hbm"] * 1e9)
     sec = ms_per_step / 1e3
     if t_tensor >= t_hbm:
-        return {"bound": "tensor", "achieved": flops / sec / 1e12, "peak": tpeak, "unit": "TFLOP/s", "mx": mx,
+        ach = flops / sec / 1e12
+        return {"bound": "tensor", "achieved": ach, "peak": tpeak, "unit": "TFLOP/s", "mx": mx,
+                "frac": ach / tpeak, "frac_sustained": ach / (P["mx_s"] if mx else P["bf16_s"]),
+                "frac_nominal": ach / (NOMINAL["mx_tflops"] if mx else NOMINAL["bf16_tflops"]),
                 "t_tensor_ms": t_tensor * 1e3, "t_hbm_ms": t_hbm * 1e3}
-    return {"bound": "hbm", "achieved": byts / sec / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s", "mx": mx,
+    ach = byts / sec / 1e9
+    return {"bound": "hbm", "achieved": ach, "peak": P["hbm"], "unit": "GB/s", "mx": mx,
+            "frac": ach / P["hbm"], "frac_sustained": ach / P["hbm"], "frac_nominal": ach / NOMINAL["hbm_gbs"],
             "t_tensor_ms": t_tensor * 1e3, "t_hbm_ms": t_hbm * 1e3}
+
+
+def layer_roofline(cfg, passes, ms_step, P):
+    """The whole step against max(FLOPs / tensor peak, algorithmic bytes / HBM):
+    `frac` at the measured burst rates, beside it at the sustained rates and at
+    GB300's published dense peaks."""
+    fl_exp, fl_sh, byt = layer_work(cfg, passes)
+    mx = cfg["fmt"] == "mxfp8"
+
+    def roof(t_mx, t_bf, hbm):
+        t_t = fl_exp / (t_mx if mx else t_bf) / 1e12 + fl_sh / t_bf / 1e12
+        t_h = byt / hbm / 1e9
+        return max(t_t, t_h), t_t, t_h
+
+    t_roof, t_tensor, t_hbm = roof(P["mx"], P["bf16"], P["hbm"])
+    t_s = roof(P["mx_s"], P["bf16_s"], P["hbm"])[0]
+    t_n = roof(NOMINAL["mx_tflops"], NOMINAL["bf16_tflops"], NOMINAL["hbm_gbs"])[0]
+    sec = ms_step / 1e3
+    return {"tokens_per_s": round(cfg["T"] / t_roof, 1), "frac": round(t_roof / sec, 4),
+            "frac_sustained": round(t_s / sec, 4), "frac_nominal": round(t_n / sec, 4),
+            "bound": "tensor" if t_tensor >= t_hbm else "hbm", "t_tensor_ms": round(t_tensor * 1e3, 3),
+            "t_hbm_ms": round(t_hbm * 1e3, 3),
+            "peaks": "HBM %.1f GB/s, BF16 %.1f TFLOP/s (%s, burst), MXFP8 %.1f TFLOP/s (%s)"
+                     % (P["hbm"], P["bf16"], P["src"], P["mx"], P["mx_src"])}
 
 
 class Clocks:
@@ -267,9 +371,15 @@ def gpu_index():
 
 # ----------------------------------------------------------------------------- oracle (CPU)
 def _prep_worker(args):
+    import numpy as np
     from oracle import moe as om
-    e, gu, dn, fmt, backward = args
-    return e, om.prepare_expert(gu.astype("float64"), dn.astype("float64"), fmt, backward)
+    e, gu, dn, fmt, forward, backward = args
+    ops = om.prepare_expert(gu.astype(np.float64), dn.astype(np.float64), fmt, backward=backward, forward=forward)
+    out = {}
+    for key, v in ops.items():                  # held in fp32 where that is exact (the oracle computes in fp64)
+        v32 = v.astype(np.float32)
+        out[key] = v32 if np.array_equal(v32, v) else v
+    return e, out
 
 
 class _Experts:
@@ -300,19 +410,47 @@ def oracle_sample(cfg, passes, x_dev, logits_dev, dy_dev, n_tok):
     sh = mi.shared(cfg, device=x_dev.device)
     shared = None if sh is None else tuple(mi.to_f64(w) for w in sh)
     return dict(tok=tok, x=mi.to_f64(x_dev[tok]), logits=lg, dy=None if dy_dev is None else mi.to_f64(dy_dev[tok]),
-                need=need, masters=masters, shared=shared)
+                need=need, masters=masters, shared=shared, passes=passes)
 
 
-def oracle_prepare(cfg, passes, sample):
-    """Weight preparation (S0) of the sample's experts by the oracle, in parallel."""
-    jobs = [(e, gu, dn, cfg["fmt"], passes == "fwdbwd") for e, (gu, dn) in sample["masters"].items()]
+def oracle_prepare(cfg, sample):
+    """Weight preparation (S0) of the sample's experts by the oracle, in parallel
+    (the masters themselves are not kept: with prepared operands the oracle
+    reads them only for their shapes)."""
+    import numpy as np
+    bwd = sample["passes"] == "fwdbwd"
+    jobs = [(e, gu, dn, cfg["fmt"], True, bwd) for e, (gu, dn) in sample["masters"].items()]
     t0 = time.perf_counter()
     nproc = max(1, min(len(jobs), os.cpu_count() or 1))
     with mp.get_context("spawn").Pool(nproc) as pool:
         ops = dict(pool.map(_prep_worker, jobs))
-    table = {e: (sample["masters"][e][0].astype("float64"), sample["masters"][e][1].astype("float64"), ops[e])
-             for e in ops}
+    table = {e: (np.broadcast_to(np.float64(0.0), sample["masters"][e][0].shape),
+                 np.broadcast_to(np.float64(0.0), sample["masters"][e][1].shape), ops[e]) for e in ops}
+    sample["masters"] = None
     return _Experts(cfg["E"], table), time.perf_counter() - t0
+
+
+def blas_threads(n):
+    """Sets the thread count of numpy's OpenBLAS in this process through the
+    library's own setter (ctypes); returns the previous count, or None where no
+    such library or setter is found."""
+    import ctypes
+    import glob
+    import numpy
+    root = os.path.dirname(numpy.__file__)
+    libs = glob.glob(os.path.join(os.path.dirname(root), "numpy.libs", "*openblas*")) + \
+        glob.glob(os.path.join(root, ".libs", "*openblas*"))
+    for path in libs:
+        try:
+            L = ctypes.CDLL(path)
+        except OSError:
+            continue
+        for sfx in ("scipy_openblas_%s_num_threads64_", "openblas_%s_num_threads64_", "openblas_%s_num_threads"):
+            if hasattr(L, sfx % "set") and hasattr(L, sfx % "get"):
+                prev = getattr(L, sfx % "get")()
+                getattr(L, sfx % "set")(int(n))
+                return prev
+    return None
 
 
 def oracle_step(cfg, passes, sample, experts):
@@ -327,7 +465,7 @@ def oracle_step(cfg, passes, sample, experts):
 def oracle_sample_desc(cfg, passes, n_tok, n_exp):
     return ("%d seeded token(s) of the %s workload (%s): route, the %d experts they select, %scombine%s, "
             "float64 NumPy; expert weight preparation (MXFP8 quantisation, S0) done beforehand like the "
-            "GPU side; BLAS threads = all cores, elementwise work single-threaded"
+            "GPU side"
             % (n_tok, cfg["name"], "fwd+bwd" if passes == "fwdbwd" else "fwd", n_exp,
                "shared expert, " if cfg["m_shared"] else "",
                ", full backward incl. the sample's weight gradients" if passes == "fwdbwd" else ""))
@@ -372,6 +510,136 @@ def time_s0(layer, gu_all, dn_all, stream):
     return a.elapsed_time(b)
 
 
+def workload_desc(cfg, bwd, layer=None):
+    mx = cfg["fmt"] == "mxfp8"
+    ring = layer.cfg.ring_rows if layer is not None else 0
+    return {"workload": cfg["name"], "pass": "fwd+bwd" if bwd else "fwd", "T": cfg["T"], "d": cfg["d"],
+            "m": cfg["m"], "E": cfg["E"], "k": cfg["k"], "m_shared": cfg["m_shared"],
+            "experts": cfg["fmt"], "router_bias": cfg["bias"], "parallelism": "1gpu",
+            "dispatch": ("ring of %d rows, %d gather SMs" % (ring, layer.cfg.gather_sms or 8)
+                         if ring else "materialised"),
+            "l2": "inputs larger than L2 (%.1f GB of expert weights read per step)"
+                  % (3 * cfg["E"] * cfg["d"] * cfg["m"] * (1.03 if mx else 2) / 1e9)}
+
+
+def summarize(cfg, train, recs, steps, total_ms, P, write_gbs):
+    """Per-kernel breakdown of a traced timed region (the library's event trace:
+    (name, ms) per traced launch), the dominant kernel's roofline and the
+    number of kernel launches."""
+    per = {}
+    launches = 0
+    for name, ms in recs:
+        c, t = per.get(name, (0, 0.0))
+        per[name] = (c + 1, t + ms)
+        launches += kernels_in_region(name, cfg, train)
+    kernel_total = sum(t for _, t in per.values()) or 1.0
+    dom = max(per.items(), key=lambda kv: kv[1][1])[0]
+    cnt, tot = per[dom]
+    kr = kernel_roofline(cfg, dom, train, tot / steps, P)
+    if kr is None:
+        roof = {"kernel": dom, "bound": None, "achieved": None, "peak": None, "unit": None, "frac": None,
+                "traffic": None}
+    else:
+        if kr["bound"] == "tensor":
+            note = P["mx_src"] if kr["mx"] else "%s BF16 GEMM, burst" % P["src"]
+        else:
+            note = "%s HBM copy bandwidth" % P["src"]
+        ob = output_bytes(cfg, dom)
+        roof = {"kernel": dom, "bound": kr["bound"], "achieved": round(kr["achieved"], 1), "peak": round(kr["peak"], 1),
+                "unit": kr["unit"], "frac": round(kr["frac"], 4), "frac_sustained": round(kr["frac_sustained"], 4),
+                "frac_nominal": round(kr["frac_nominal"], 4), "traffic": NCU_TRAFFIC.get((cfg["name"], dom)),
+                "peak_source": note, "launch_ms": round(tot / cnt, 4),
+                "write_probe": None if ob is None else {
+                    "note": "output-write-dominated kernel: its bf16 dW write rate against this GPU's "
+                            "write-only bandwidth (device fill of 8 GB, measured before the timed region)",
+                    "written_gbs": round(ob / (tot / steps / 1e3) / 1e9, 1), "fill_gbs": round(write_gbs, 1),
+                    "frac": round(ob / (tot / steps / 1e3) / 1e9 / write_gbs, 4)}}
+    kernels = {}
+    for n, (c, t) in sorted(per.items(), key=lambda kv: -kv[1][1]):
+        kernels[n] = {"launches_per_step": c / steps, "ms_per_step": round(t / steps, 4),
+                      "share": round(t / kernel_total, 4)}
+        r = kernel_roofline(cfg, n, train, t / steps, P)
+        if r is not None:
+            kernels[n].update({"bound": r["bound"], "frac": round(r["frac"], 4),
+                               "frac_sustained": round(r["frac_sustained"], 4),
+                               "frac_nominal": round(r["frac_nominal"], 4)})
+    rs = per.get("route_schedule", (0, 0.0))[1] / kernel_total
+    return {"roofline": roof, "kernels": kernels, "route_schedule_share": round(rs, 4),
+            "gpu_launches": launches}
+
+
+def timed_region(stream, fn, K, trace=False):
+    """K calls of fn between CUDA events on `stream`, synchronised on both
+    sides; with `trace`, the library's per-launch event records as well."""
+    import torch
+    import mixture_experts_layer_device_gb300 as pkg
+    if trace:
+        pkg.check(pkg.moe_trace_enable(K * 64 + 64))
+        pkg.moe_trace_clear()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(K):
+        fn()
+    b.record(stream)
+    b.synchronize()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b)
+    recs = pkg.moe_trace_records() if trace else []
+    if trace:
+        pkg.moe_trace_enable(0)
+    return ms, recs
+
+
+TARGET = "deepseek-v4-pro"
+
+
+def run_target(args, P):
+    """The target leg: the MXFP8 forward of the largest workload (DeepSeek-V4-Pro
+    shape, 8 hot experts), built after the main workload's buffers are freed,
+    with its own timed region, clock record, per-kernel trace and rooflines."""
+    import torch
+    from mixture_experts_layer_device_gb300.layer import MoELayer
+    cfg = workload(TARGET)
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream()
+    x, logits, _, gu_all, dn_all, shared = build_inputs(cfg, dev, "fwd")
+    layer = MoELayer(cfg["T"], cfg["d"], cfg["m"], cfg["E"], cfg["k"], cfg["fmt"], shared=shared, backward=False,
+                     device=dev, stacked=(gu_all, dn_all))
+    del gu_all, dn_all
+    torch.cuda.empty_cache()
+    y = torch.empty((cfg["T"], cfg["d"]), dtype=torch.bfloat16, device=dev)
+
+    def step():
+        layer.forward(x, logits, y=y, train=False, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if layer.status() != 0:
+        raise RuntimeError("device status after the target leg's warm-up")
+    clocks = Clocks(gpu_index())
+    total_ms, _ = timed_region(stream, step, args.steps)
+    clk = clocks.stop()
+    if clocks_rejected(clk):
+        first = clk
+        clocks = Clocks(gpu_index())
+        total_ms, _ = timed_region(stream, step, args.steps)
+        clk = clocks.stop()
+        clk["remeasured_after"] = {"sm_mhz": first["sm_mhz"], "reasons": first["reasons"]}
+    _, recs = timed_region(stream, step, args.steps, trace=True)
+    if layer.status() != 0:
+        raise RuntimeError("device status after the target leg")
+    ms = total_ms / args.steps
+    summ = summarize(cfg, False, recs, args.steps, total_ms, P, 0.0)
+    return {"note": "MXFP8 forward of the largest workload; target: layer_roofline.frac >= 0.60",
+            "value": round(cfg["T"] / (ms / 1e3), 1), "unit": "tokens/s", "ms_per_step": round(ms, 4),
+            "steps": args.steps, "warmup": args.warmup, "config": workload_desc(cfg, False, layer),
+            "layer_roofline": layer_roofline(cfg, "fwd", ms, P), "roofline": summ["roofline"],
+            "kernels": summ["kernels"], "route_schedule_share": summ["route_schedule_share"],
+            "gpu_launches": summ["gpu_launches"], "clocks": clk}
+
+
 def run_ours(args, cfg, passes):
     import numpy as np
     import torch
@@ -382,6 +650,8 @@ def run_ours(args, cfg, passes):
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream()
     peaks, peaks_src = load_peaks()
+    mxp = None if args.profile_run else mxfp8_peak_probe(dev)   # profiler launch lists stay the layer's
+    P = tensor_peaks(peaks, peaks_src, mxp)
 
     x, logits, dy, gu_all, dn_all, shared = build_inputs(cfg, dev, passes)
     bwd = passes == "fwdbwd"
@@ -392,8 +662,10 @@ def run_ours(args, cfg, passes):
     sample = None
     want_cpu = not args.no_cpu_baseline and not args.profile_run
     n_tok = 1 if bwd else 4
+    sample256 = None
     if want_cpu:
         sample = oracle_sample(cfg, passes, x, logits, dy, n_tok)
+        sample256 = oracle_sample(cfg, "fwd", x, logits, None, 256)
     keep_masters = bwd and layer.mx      # re-quantised every update in the with-S0 step
     if not keep_masters:
         del gu_all, dn_all
@@ -415,22 +687,7 @@ def run_ours(args, cfg, passes):
         raise RuntimeError("device status %d after warm-up" % st)
 
     def timed(fn, K, trace=False):
-        if trace:
-            pkg.check(pkg.moe_trace_enable(K * 64 + 64))
-            pkg.moe_trace_clear()
-        torch.cuda.synchronize()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for _ in range(K):
-            fn()
-        b.record(stream)
-        b.synchronize()
-        torch.cuda.synchronize()
-        ms = a.elapsed_time(b)
-        recs = pkg.moe_trace_records() if trace else []
-        if trace:
-            pkg.moe_trace_enable(0)
-        return ms, recs
+        return timed_region(stream, fn, K, trace)
 
     write_gbs = write_probe_gbs(dev)
     clocks = Clocks(gpu_index())
@@ -462,7 +719,7 @@ def run_ours(args, cfg, passes):
             per_ms[name] = per_ms.get(name, 0.0) + ms
         return {"metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "ms_per_step": round(ms_step, 4),
                 "config": {"workload": cfg["name"], "T": cfg["T"], "E": cfg["E"]}, "profile_run": True,
-                "kernels_ms_per_step": {n: round(t / args.steps, 4) for n, t in per_ms.items()}}
+                "kernels_ms_per_step": {n: round(t / args.steps, 4) for n, t in per_ms.items()}}, P
     if bwd:
         fms, _ = timed(lambda: layer.forward(x, logits, y=y, train=False, stream=stream), args.steps)
         fwd_value = tokens * args.steps / (fms / 1e3)
@@ -575,94 +832,73 @@ def run_ours(args, cfg, passes):
     if st != 0:
         raise RuntimeError("device status %d after the timed region" % st)
 
-    # per-kernel breakdown of the timed region (library event trace)
-    per = {}
-    launches = 0
-    for name, ms in recs:
-        c, t = per.get(name, (0, 0.0))
-        per[name] = (c + 1, t + ms)
-        launches += kernels_in_region(name, cfg, bwd)
-    kernel_total = sum(t for _, t in per.values()) or 1.0
-    dom = max(per.items(), key=lambda kv: kv[1][1])[0]
-    cnt, tot = per[dom]
-    avg_ms = tot / cnt
-    kr = kernel_roofline(cfg, dom, bwd, tot / args.steps, peaks) or {
-        "bound": "tensor", "achieved": float("nan"), "peak": float("nan"), "unit": "TFLOP/s", "mx": False,
-        "t_tensor_ms": float("nan"), "t_hbm_ms": float("nan")}
-    bound, achieved, peak, unit = kr["bound"], kr["achieved"], kr["peak"], kr["unit"]
-    if bound == "tensor":
-        peak_note = ("MXFP8 = %s sustained BF16 x %.0f (nominal ratio)" % (peaks_src, MX_OVER_BF16) if kr["mx"]
-                     else "%s sustained BF16" % peaks_src)
-    else:
-        peak_note = "%s HBM copy bandwidth" % peaks_src
-    traffic = NCU_TRAFFIC.get((cfg["name"], dom))
-    kernels = {}
-    for n, (c, t) in sorted(per.items(), key=lambda kv: -kv[1][1]):
-        kernels[n] = {"launches_per_step": c / args.steps, "ms_per_step": round(t / args.steps, 4),
-                      "share": round(t / kernel_total, 4)}
-        r = kernel_roofline(cfg, n, bwd, t / args.steps, peaks)
-        if r is not None:
-            kernels[n].update({"bound": r["bound"], "frac": round(r["achieved"] / r["peak"], 4)})
-    rs = per.get("route_schedule", (0, 0.0))[1] / kernel_total
-
-    # layer roofline (algorithmic work of the whole step)
-    fl_exp, fl_sh, byt = layer_work(cfg, passes)
+    summ = summarize(cfg, bwd, recs, args.steps, total_ms, P, write_gbs)
     mx = cfg["fmt"] == "mxfp8"
-    t_tensor = fl_exp / (peaks["bf16_tflops_sustained"] * 1e12 * (MX_OVER_BF16 if mx else 1.0)) + \
-        fl_sh / (peaks["bf16_tflops_sustained"] * 1e12)
-    t_hbm = byt / (peaks["hbm_gbs"] * 1e9)
-    t_roof = max(t_tensor, t_hbm)
-
     out = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "mxfp8" if mx else "bf16",
         "data": "synthetic (seeded N(0,1) tokens, N(0,1/d)/N(0,1/m) bf16 weights, fp32 logits)",
-        "config": {"workload": cfg["name"], "pass": "fwd+bwd" if bwd else "fwd", "T": cfg["T"], "d": cfg["d"],
-                   "m": cfg["m"], "E": cfg["E"], "k": cfg["k"], "m_shared": cfg["m_shared"],
-                   "experts": cfg["fmt"], "router_bias": cfg["bias"], "parallelism": "1gpu",
-                   "dispatch": ("ring of %d rows, %d gather SMs" % (layer.cfg.ring_rows, layer.cfg.gather_sms or 8)
-                                if layer.cfg.ring_rows else "materialised"),
-                   "l2": "inputs larger than L2 (%.1f GB of expert weights read per step)"
-                         % (3 * cfg["E"] * cfg["d"] * cfg["m"] * (1.03 if mx else 2) / 1e9)},
+        "config": workload_desc(cfg, bwd, layer),
         "fwd_tokens_per_s": round(fwd_value, 1),
-        "layer_roofline": {"tokens_per_s": round(cfg["T"] / t_roof, 1), "frac": round(value / (cfg["T"] / t_roof), 4),
-                           "bound": "tensor" if t_tensor >= t_hbm else "hbm", "t_tensor_ms": round(t_tensor * 1e3, 3),
-                           "t_hbm_ms": round(t_hbm * 1e3, 3), "peaks": peaks_src},
-        "roofline": {"kernel": dom, "bound": bound, "achieved": round(achieved, 1), "peak": round(peak, 1),
-                     "unit": unit, "frac": round(achieved / peak, 4), "traffic": traffic, "peak_source": peak_note,
-                     "launch_ms": round(avg_ms, 4),
-                     "write_probe": None if output_bytes(cfg, dom) is None else {
-                         "note": "output-write-dominated kernel: its bf16 dW write rate against this GPU's "
-                                 "write-only bandwidth (device fill of 8 GB, measured before the timed region)",
-                         "written_gbs": round(output_bytes(cfg, dom) / (tot / args.steps / 1e3) / 1e9, 1),
-                         "fill_gbs": round(write_gbs, 1),
-                         "frac": round(output_bytes(cfg, dom) / (tot / args.steps / 1e3) / 1e9 / write_gbs, 4)}},
-        "kernels": kernels,
-        "route_schedule_share": round(rs, 4),
+        "layer_roofline": layer_roofline(cfg, passes, total_ms / args.steps, P),
+        "roofline": summ["roofline"],
+        "kernels": summ["kernels"],
+        "route_schedule_share": summ["route_schedule_share"],
         "s0_ms": round(s0_ms, 3),
         "step_with_s0": with_s0,
         "cuda_graph": graph_info,
         "e2e": {"value": round(tokens * args.steps / (e2e_ms / 1e3), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
-        "gpu_launches": launches,
+        "gpu_launches": summ["gpu_launches"],
         "clocks": clk,
+        "mxfp8_peak_probe": mxp,
     }
     if want_cpu:
-        experts, prep_s = oracle_prepare(cfg, passes, sample)
+        out["cpu_baseline"] = cpu_baseline(cfg, passes, sample, sample256, n_tok)
+    return out, P
+
+
+def cpu_baseline(cfg, passes, sample, sample256, n_tok):
+    """The oracle as it stands on the host cores: the bounded n_tok-token step
+    (the bench's metric, repeated to about 10 s) with BLAS on all cores and
+    again on one thread, and the 256-token seeded forward subset once."""
+    cores = os.cpu_count()
+
+    def repeat(experts):
         reps, t0 = 0, time.perf_counter()
-        while True:                       # the same sample, repeated to ~10 s of CPU work
+        while True:
             oracle_step(cfg, passes, sample, experts)
             reps += 1
             dt = time.perf_counter() - t0
             if dt >= 10.0 or reps >= 1000:
-                break
-        out["cpu_baseline"] = {"value": round(n_tok * reps / dt, 4), "unit": "tokens/s", "cores": os.cpu_count(),
-                               "kind": "oracle",
-                               "sample": oracle_sample_desc(cfg, passes, n_tok, len(sample["need"])) +
-                               "; run %d times back to back" % reps,
-                               "seconds": round(dt, 2), "s0_seconds": round(prep_s, 2)}
-    return out
+                return reps, dt
+
+    experts, prep_s = oracle_prepare(cfg, sample)
+    reps, dt = repeat(experts)
+    res = {"value": round(n_tok * reps / dt, 4), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+           "sample": oracle_sample_desc(cfg, passes, n_tok, len(sample["need"])) +
+           "; run %d times back to back with BLAS threads = all %d cores" % (reps, cores),
+           "seconds": round(dt, 2), "s0_seconds": round(prep_s, 2)}
+    prev = blas_threads(1)
+    if prev is not None:
+        reps1, dt1 = repeat(experts)
+        blas_threads(prev)
+        res["one_thread"] = {"value": round(n_tok * reps1 / dt1, 4), "unit": "tokens/s", "cores": 1,
+                             "seconds": round(dt1, 2), "runs": reps1}
+    else:
+        res["one_thread"] = {"unavailable": "no OpenBLAS thread setter found in numpy's libraries"}
+    del experts
+    if sample256 is not None:
+        from oracle import moe as om
+        ex256, prep256 = oracle_prepare(cfg, sample256)
+        t0 = time.perf_counter()
+        om.forward(sample256["x"], sample256["logits"], ex256, cfg["k"], cfg["fmt"], shared=sample256["shared"])
+        dt = time.perf_counter() - t0
+        res["fwd_256"] = {"value": round(256 / dt, 4), "unit": "tokens/s (forward)", "cores": cores,
+                          "seconds": round(dt, 2), "s0_seconds": round(prep256, 2),
+                          "sample": oracle_sample_desc(cfg, "fwd", 256, len(sample256["need"])) + "; run once"}
+    return res
 
 
 def run_reference(args, cfg, passes):
@@ -676,7 +912,7 @@ def run_reference(args, cfg, passes):
     n_tok = 1 if passes == "fwdbwd" else 4
     sample = oracle_sample(cfg, passes, x, logits, dy, n_tok)
     del x, logits, dy
-    experts, prep_s = oracle_prepare(cfg, passes, sample)
+    experts, prep_s = oracle_prepare(cfg, sample)
     from oracle import moe as om
     for _ in range(args.warmup):          # warm-up: the routing of the sample only
         om.route(sample["logits"], cfg["k"])
@@ -689,9 +925,7 @@ def run_reference(args, cfg, passes):
     return {"metric": METRIC, "value": round(value, 4), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 1), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
-            "config": {"workload": cfg["name"], "pass": "fwd+bwd" if passes == "fwdbwd" else "fwd", "T": cfg["T"],
-                       "d": cfg["d"], "m": cfg["m"], "E": cfg["E"], "k": cfg["k"], "m_shared": cfg["m_shared"],
-                       "experts": cfg["fmt"]},
+            "config": workload_desc(cfg, passes == "fwdbwd"),
             "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s", "cores": cores, "kind": "oracle",
                              "sample": oracle_sample_desc(cfg, passes, n_tok, len(sample["need"])) +
                              "; warm-up steps route the sample only", "s0_seconds": round(prep_s, 2)},
@@ -707,6 +941,8 @@ def main():
     ap.add_argument("--workload", default="kimi-k2.7")
     ap.add_argument("--pass", dest="passes", choices=["fwd", "fwdbwd"], default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-target", action="store_true",
+                    help="skip the target leg (the MXFP8 forward of the largest workload)")
     ap.add_argument("--profile-run", action="store_true",
                     help="time the step once (no fwd-only, e2e or CPU legs): for profiler launch lists")
     ap.add_argument("--ring", type=int, default=0,
@@ -736,7 +972,13 @@ def main():
 
     import __graft_entry__
     __graft_entry__.build()
-    out = run_ours(args, cfg, passes)
+    out, P = run_ours(args, cfg, passes)
+    if not (args.no_target or args.profile_run or args.override or cfg["name"] == TARGET):
+        import gc
+        import torch
+        gc.collect()
+        torch.cuda.empty_cache()
+        out["target"] = run_target(args, P)
     print(json.dumps(out), flush=True)
 
 

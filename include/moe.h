@@ -34,13 +34,18 @@
  * exponent is floor(log2(amax)) - 8, clamped to [-127, 127] (an all-zero
  * block gets byte 0); codes are round-to-nearest-even and saturate to +-448.
  *
- * MXFP8 scale layout ("tiled"): a matrix with `rows` rows and reduction
- * length K (rows and K multiples of 128) has rows*K/32 scale bytes; the
- * scale of (row r, block b = column/32) is at byte
- *     ((r / 128) * (K / 128) + b / 4) * 512
- *       + (r % 32) * 16 + ((r % 128) / 32) * 4 + (b % 4)
- * i.e. 512-byte atoms covering 128 rows x 4 blocks, in the order the tensor
- * cores' scale-factor copy reads them.  Batched matrices stack along rows.
+ * MXFP8 scale layouts.  A matrix with `rows` rows and reduction length K has
+ * rows*K/32 scale bytes.
+ *   Canonical (every scale this ABI takes from or returns to the caller):
+ *     [rows, K/32] row-major, the scale of (row r, block b = column/32) at
+ *     byte r*(K/32) + b.  Batched matrices stack along rows.
+ *   Prepared (the expert GEMMs' operand layout; internal): the same bytes in
+ *     the order the tensor cores' scale-factor copy reads them, made from
+ *     canonical scales by moe_prepare_scales and turned back by
+ *     moe_canonical_scales (rows and K multiples of 128).  moe_weights'
+ *     *_scale fields and the scale buffers inside the workspace use it.  For
+ *     reference, byte ((r/128)*(K/128) + b/4)*512 + (r%32)*16 + ((r%128)/32)*4
+ *     + b%4 holds the scale of (r, b): 512-byte atoms of 128 rows x 4 blocks.
  */
 #ifndef MOE_H
 #define MOE_H
@@ -134,17 +139,20 @@ typedef struct {
  * Expert weights.  BF16 path: `gu` [E, 2m, d] bf16 (rows 0..m-1 of each
  * expert are the gate projection, m..2m-1 the up projection), `dn` [E, d, m]
  * bf16; the *_scale pointers are unused.
- * MXFP8 path: `gu` = E4M3 codes [E*2m, d] with tiled scales `gu_scale`
+ * MXFP8 path: `gu` = E4M3 codes [E*2m, d] with prepared scales `gu_scale`
  * (rows E*2m, K d); `dn` = codes [E*d, m], `dn_scale` (rows E*d, K m) --
- * both from moe_quantize_weights(blocks_along_rows = 0) (or
- * moe_quantize_mx(transpose = 0)) of the bf16 masters.
+ * the codes from moe_quantize_weights(blocks_along_rows = 0) (or
+ * moe_quantize_mx(transpose = 0)) of the bf16 masters, the scales that call's
+ * canonical scales passed through moe_prepare_scales (an MXFP8 checkpoint's
+ * codes and canonical scales can be used the same way).
  * Backward operands (NULL for a forward-only layer):
  *   BF16:  gu_t = [E, d, 2m] bf16 = per-expert transpose of gu,
  *          dn_t = [E, m, d] bf16 = per-expert transpose of dn
  *          (moe_transpose_bf16);
- *   MXFP8: gu_t = codes [E*d, 2m] + gu_t_scale, dn_t = codes [E*m, d] +
- *          dn_t_scale (moe_quantize_weights(blocks_along_rows = 1) of the
- *          masters; moe_quantize_mx_both writes both orientations at once).
+ *   MXFP8: gu_t = codes [E*d, 2m] + prepared gu_t_scale, dn_t = codes
+ *          [E*m, d] + prepared dn_t_scale (moe_quantize_weights(
+ *          blocks_along_rows = 1) of the masters, then moe_prepare_scales;
+ *          moe_quantize_mx_both writes both orientations at once).
  * Shared expert (BF16 always; NULL when m_shared == 0): s_gu [2m_s, d],
  * s_dn [d, m_s]; for backward also s_gu_t [d, 2m_s], s_dn_t [m_s, d].
  */
@@ -189,10 +197,10 @@ int64_t moe_padded_rows(const moe_config *cfg);
  * MXFP8 bullet: MXFP8 is the default expert format).
  * src: [batch, rows, cols] bf16.
  *   transpose = 0: codes [batch*rows, cols], blocks of 32 along cols;
- *                  scales tiled with rows' = batch*rows, K = cols.
+ *                  canonical scales [batch*rows, cols/32].
  *   transpose = 1: codes [batch*cols, rows] = per-batch transpose, blocks of
- *                  32 along the original rows; scales tiled with
- *                  rows' = batch*cols, K = rows.
+ *                  32 along the original rows; canonical scales
+ *                  [batch*cols, rows/32].
  * rows and cols must be multiples of 128.  Inputs must be finite.
  */
 int moe_quantize_mx(const void *src, int batch, int rows, int cols, int transpose, void *codes,
@@ -215,9 +223,42 @@ int moe_quantize_weights(const moe_config *cfg, const void *w_bf16, int rows, in
 /* S0 for a training layer: both orientations from one read of the bf16
  * masters.  codes/scales exactly as moe_quantize_mx(transpose = 0) and
  * codes_t/scales_t exactly as moe_quantize_mx(transpose = 1) would write them
- * (bit-identical).  rows and cols multiples of 128; inputs finite. */
+ * (bit-identical, canonical scales).  rows and cols multiples of 128; inputs
+ * finite. */
 int moe_quantize_mx_both(const void *src, int batch, int rows, int cols, void *codes, void *scales,
                          void *codes_t, void *scales_t, moe_stream_t stream);
+
+/* S0 for the whole layer, straight into the operands moe_forward and
+ * moe_backward read (one read of each bf16 master; "Mixture-of-Kittens" wiki
+ * page, Key claims, MXFP8 bullet: MXFP8 expert weights with BF16 masters).
+ * w_gu [E, 2m, d] and w_dn [E, d, m] bf16 masters of cfg's experts.
+ *   MXFP8: gu / dn = E4M3 codes [E*2m, d] / [E*d, m] with PREPARED scales
+ *     gu_scale / dn_scale (as moe_quantize_weights(blocks_along_rows = 0)
+ *     followed by moe_prepare_scales, bit for bit); with gu_t and dn_t given,
+ *     also the backward operands gu_t [E*d, 2m] + gu_t_scale and dn_t [E*m, d]
+ *     + dn_t_scale (blocks_along_rows = 1), from the same read of the masters.
+ *   BF16: the masters are the forward operands (copied into gu / dn when
+ *     those name other buffers; NULL = use the masters); with gu_t and dn_t
+ *     given, the per-expert transposes of the masters (the *_scale pointers are
+ *     unused).
+ * gu_t and dn_t are both NULL (forward only) or both given (MOE_ERR_ARG
+ * otherwise).  Re-run after every update of the masters.  Asynchronous on
+ * `stream`. */
+int moe_prepare_weights(const moe_config *cfg, const void *w_gu, const void *w_dn, void *gu, void *gu_scale,
+                        void *dn, void *dn_scale, void *gu_t, void *gu_t_scale, void *dn_t, void *dn_t_scale,
+                        moe_stream_t stream);
+
+/* MXFP8 scales from the canonical order to the prepared operand layout that
+ * moe_weights' *_scale fields take (a permutation of bytes, part of S0):
+ * scales [rows, K/32] -> prepared (rows*K/32 bytes).  rows and K multiples of
+ * 128 (MOE_ERR_SHAPE otherwise); the two buffers must not overlap
+ * (MOE_ERR_ARG if they are the same pointer).  Asynchronous on `stream`. */
+int moe_prepare_scales(const void *scales, int64_t rows, int32_t K, void *prepared, moe_stream_t stream);
+
+/* The inverse of moe_prepare_scales: prepared -> canonical [rows, K/32]
+ * (e.g. to read the scale buffers moe_buffer_info names, or to save prepared
+ * weights in the format's own order).  Same rules. */
+int moe_canonical_scales(const void *prepared, int64_t rows, int32_t K, void *scales, moe_stream_t stream);
 
 /* Per-batch transpose of bf16 matrices: src [batch, rows, cols] ->
  * dst [batch, cols, rows] (rows, cols multiples of 32). */
@@ -244,9 +285,9 @@ int moe_route(const moe_config *cfg, const float *logits, int32_t *idx, float *w
  * Router projection in front of the layer (daily-ai-frontier summary, TL;DR:
  * routing is the first fused stage; the pages do not define the projection,
  * so it is a bias-free linear map): logits [T, E] fp32 = x [T, d] bf16 *
- * W_r [E, d] bf16 ^T with fp32 accumulation.  A plain GEMM, run by cuBLAS on
- * `stream` with its workspace inside `ws` (a cuBLAS handle is created once per
- * device on first use).  Deterministic for a given device.
+ * W_r [E, d] bf16 ^T with fp32 accumulation, on the library's own tcgen05
+ * GEMM (fp32 epilogue) through a zero-padded [roundup(T,128), roundup(E,128)]
+ * buffer inside `ws`.  Bitwise reproducible.
  */
 int moe_router_forward(const moe_config *cfg, const void *x, const void *W_r, float *logits, void *ws,
                        moe_stream_t stream);
@@ -255,8 +296,9 @@ int moe_router_forward(const moe_config *cfg, const void *x, const void *W_r, fl
  * Router backward: dlogits [T, E] fp32 (moe_backward's output, including the
  * load-balancing term) is rounded to bf16 g; then dx [T, d] bf16 is updated in
  * place to bf16(dx + g W_r) (the layer's dx plus the router's, one rounding)
- * and dW_r [E, d] bf16 = bf16(g^T x).  ws must be sized with
- * MOE_FLAG_BACKWARD.
+ * and dW_r [E, d] bf16 = bf16(g^T x).  Both on the library's own tcgen05 GEMM
+ * (the first with an add-into-bf16 epilogue), over zero-padded copies of g,
+ * g^T, W_r^T and x^T inside `ws`, which must be sized with MOE_FLAG_BACKWARD.
  */
 int moe_router_backward(const moe_config *cfg, const float *dlogits, const void *x, const void *W_r, void *dx,
                         void *dW_r, void *ws, moe_stream_t stream);

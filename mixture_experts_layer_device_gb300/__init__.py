@@ -36,7 +36,9 @@ class MoeWeights(ctypes.Structure):
 
 _lib = None
 EXPORTS = ["moe_workspace_bytes", "moe_saved_bytes", "moe_buffer_info", "moe_padded_rows",
-           "moe_quantize_weights", "moe_quantize_mx", "moe_quantize_mx_both", "moe_transpose_bf16", "moe_route",
+           "moe_quantize_weights", "moe_quantize_mx", "moe_quantize_mx_both", "moe_prepare_weights",
+           "moe_prepare_scales",
+           "moe_canonical_scales", "moe_transpose_bf16", "moe_route",
            "moe_forward", "moe_backward",
            "moe_get_status", "moe_status_string", "moe_trace_enable", "moe_trace_clear", "moe_trace_count",
            "moe_trace_name", "moe_trace_ms", "moe_route_noalloc", "moe_router_forward", "moe_router_backward"]
@@ -60,6 +62,11 @@ def lib():
         L.moe_quantize_weights.argtypes, L.moe_quantize_weights.restype = [cfgp, P, I, I, I, P, P, S], I
         L.moe_quantize_mx.argtypes, L.moe_quantize_mx.restype = [P, I, I, I, I, P, P, S], I
         L.moe_quantize_mx_both.argtypes, L.moe_quantize_mx_both.restype = [P, I, I, I, P, P, P, P, S], I
+        L.moe_prepare_weights.argtypes = [cfgp, P, P, P, P, P, P, P, P, P, P, S]
+        L.moe_prepare_weights.restype = I
+        L.moe_prepare_scales.argtypes, L.moe_prepare_scales.restype = [P, ctypes.c_int64, ctypes.c_int32, P, S], I
+        L.moe_canonical_scales.argtypes = [P, ctypes.c_int64, ctypes.c_int32, P, S]
+        L.moe_canonical_scales.restype = I
         L.moe_transpose_bf16.argtypes, L.moe_transpose_bf16.restype = [P, I, I, I, P, S], I
         L.moe_route.argtypes, L.moe_route.restype = [cfgp, P, P, P, P, P, P, P, S], I
         L.moe_forward.argtypes = [cfgp, P, P, ctypes.POINTER(MoeWeights), P, P, P, S]
@@ -157,6 +164,21 @@ def moe_quantize_weights(cfg, w_bf16, rows, cols, blocks_along_rows, codes, scal
 def moe_quantize_mx(src, batch, rows, cols, transpose, codes, scales, stream=None):
     return lib().moe_quantize_mx(_ptr(src), batch, rows, cols, int(transpose), _ptr(codes), _ptr(scales),
                                  _stream(stream))
+
+
+def moe_prepare_weights(cfg, w_gu, w_dn, gu, gu_scale, dn, dn_scale, gu_t=None, gu_t_scale=None, dn_t=None,
+                        dn_t_scale=None, stream=None):
+    return lib().moe_prepare_weights(ctypes.byref(cfg), _ptr(w_gu), _ptr(w_dn), _ptr(gu), _ptr(gu_scale), _ptr(dn),
+                                     _ptr(dn_scale), _ptr(gu_t), _ptr(gu_t_scale), _ptr(dn_t), _ptr(dn_t_scale),
+                                     _stream(stream))
+
+
+def moe_prepare_scales(scales, rows, K, prepared, stream=None):
+    return lib().moe_prepare_scales(_ptr(scales), rows, K, _ptr(prepared), _stream(stream))
+
+
+def moe_canonical_scales(prepared, rows, K, scales, stream=None):
+    return lib().moe_canonical_scales(_ptr(prepared), rows, K, _ptr(scales), _stream(stream))
 
 
 def moe_transpose_bf16(src, batch, rows, cols, dst, stream=None):

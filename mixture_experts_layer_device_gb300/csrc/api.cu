@@ -10,7 +10,6 @@
 // the BF16 shared expert (Key claims, MXFP8 bullet); the backward runs the
 // reverse combine first and the reverse dispatch last (Key claims,
 // communication-direction bullet).
-#include <cublas_v2.h>
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <string.h>
@@ -28,8 +27,6 @@ using moe::RouteBufs;
 // ---------------------------------------------------------------- shapes
 // Gather CTAs of the ring kernel when moe_config.gather_sms is 0.
 constexpr int kDefaultGatherCtas = 8;
-// Workspace handed to cuBLAS for the router GEMMs.
-constexpr size_t kCublasWorkspace = 32u << 20;
 
 struct Dims {
   int T, d, m, E, k, ms;
@@ -146,7 +143,9 @@ void ws_layout(const Dims &D, Layout &L) {
     L.add("aux", (1 + 2 * static_cast<size_t>(D.E)) * 4);  // [L, P[E], f[E]]
     L.add("aux_part", static_cast<size_t>(moe::balance_blocks(D.T)) * D.E * 4);
   }
-  L.add("cublas_ws", kCublasWorkspace);  // the router GEMMs
+  // router projection: its logits before cropping, [Tp, E rounded up to 128] fp32
+  const size_t Ep = (static_cast<size_t>(D.E) + 127) / 128 * 128;
+  L.add("router_lpad", static_cast<size_t>(D.Tp) * Ep * 4);
   add_route(D, L);  // used when the forward saves nothing
   const size_t eb = D.mx ? 1 : 2;
   if (D.mx) {  // row-blocked codes of every token (the dispatch copies them per routed row)
@@ -175,7 +174,11 @@ void ws_layout(const Dims &D, Layout &L) {
   if (D.dump) L.add("h_dump", D.Rp * D.m * 4);  // fp32 h before its quantisation (test hook)
   if (!D.bwd) return;
   if (D.dump) L.add("dGU_dump", D.Rp * 2 * D.m * 2);  // bf16 dG|dU before their quantisation
-  L.add("router_g", static_cast<size_t>(D.T) * D.E * 2);  // bf16 dlogits for the router backward
+  // router backward: bf16 dlogits [Tp, Ep], its transpose, W_r^T [d, Ep], x^T [d, Tp] (zero-padded)
+  L.add("router_g", static_cast<size_t>(D.Tp) * Ep * 2);
+  L.add("router_gT", Ep * static_cast<size_t>(D.Tp) * 2);
+  L.add("router_WrT", static_cast<size_t>(D.d) * Ep * 2);
+  L.add("router_xT", static_cast<size_t>(D.d) * D.Tp * 2);
   L.add("g", D.R * 4);
   if (!D.mx) L.add("dO", D.Rp * D.d * 2);  // MXFP8 keeps dO only as codes
   if (!D.mx) L.add("dGU", D.Rp * 2 * D.m * 2);  // MXFP8 keeps dGU only as codes
@@ -372,6 +375,17 @@ int run_gemm(const char *name, const Gemm &q, const DeviceInfo &dev, cudaStream_
   return cuda_status(moe::launch_gemm(q.mx, q.bn, q.epi, ta, tb, g, static_cast<int>(grid), s));
 }
 
+// A GEMM on the single-CTA kernel (the router's fp32-store and add-into-bf16
+// epilogues exist only there); untraced, inside its caller's traced region.
+int run_gemm_single(const Gemm &q, const DeviceInfo &dev, cudaStream_t s) {
+  CUtensorMap ta, tb;
+  if (!make_map(&ta, q.a, q.mx, q.K, q.a_rows) || !make_map(&tb, q.b, q.mx, q.K, q.b_rows)) return MOE_ERR_CUDA;
+  moe::GemmArgs g = q.g;
+  g.out_rows = q.out_rows;
+  const long grid = q.max_tiles < dev.num_sms ? q.max_tiles : dev.num_sms;
+  return cuda_status(moe::launch_gemm(q.mx, q.bn, q.epi, ta, tb, g, static_cast<int>(grid), s));
+}
+
 // The persistent ring launch: one CTA per SM, the first gather_ctas of which
 // gather into the ring (fewer if the device has few SMs).
 int run_gemm_ring(const char *name, const Gemm &q, const Dims &D, const DeviceInfo &dev, cudaStream_t s) {
@@ -476,7 +490,7 @@ int moe_quantize_mx(const void *src, int batch, int rows, int cols, int transpos
   if (rc != MOE_OK) return rc;
   return cuda_status(moe::launch_quantize_mx(src, batch, rows, cols, transpose != 0,
                                              static_cast<uint8_t *>(codes),
-                                             static_cast<uint8_t *>(scales), stream));
+                                             static_cast<uint8_t *>(scales), true, stream));
 }
 
 int moe_quantize_weights(const moe_config *cfg, const void *w_bf16, int rows, int cols, int blocks_along_rows,
@@ -501,7 +515,71 @@ int moe_quantize_mx_both(const void *src, int batch, int rows, int cols, void *c
   if (rc != MOE_OK) return rc;
   return cuda_status(moe::launch_quantize_mx_both(
       src, batch, rows, cols, static_cast<uint8_t *>(codes), static_cast<uint8_t *>(scales),
-      static_cast<uint8_t *>(codes_t), static_cast<uint8_t *>(scales_t), stream));
+      static_cast<uint8_t *>(codes_t), static_cast<uint8_t *>(scales_t), true, stream));
+}
+
+int moe_prepare_weights(const moe_config *cfg, const void *w_gu, const void *w_dn, void *gu, void *gu_scale,
+                        void *dn, void *dn_scale, void *gu_t, void *gu_t_scale, void *dn_t, void *dn_t_scale,
+                        moe_stream_t stream) {
+  Dims D;
+  int rc = check_config(cfg, &D);
+  if (rc != MOE_OK) return rc;
+  if (!w_gu || !w_dn) return MOE_ERR_ARG;
+  const bool bwd = gu_t != nullptr;
+  if ((dn_t != nullptr) != bwd) return MOE_ERR_ARG;
+  if (D.mx && (!gu || !gu_scale || !dn || !dn_scale || (bwd && (!gu_t_scale || !dn_t_scale)))) return MOE_ERR_ARG;
+  const void *ptrs[] = {w_gu, w_dn, gu, gu_scale, dn, dn_scale, gu_t, gu_t_scale, dn_t, dn_t_scale};
+  for (const void *q : ptrs)
+    if (q && !aligned16(q)) return MOE_ERR_ALIGN;
+  DeviceInfo dev;
+  if ((rc = device_info(&dev)) != MOE_OK) return rc;
+  const int E = D.E, d = D.d, m = D.m;
+  auto u8 = [](void *p) { return static_cast<uint8_t *>(p); };
+  if (D.mx) {
+    if (bwd) {
+      if ((rc = cuda_status(moe::launch_quantize_mx_both(w_gu, E, 2 * m, d, u8(gu), u8(gu_scale), u8(gu_t),
+                                                         u8(gu_t_scale), false, stream))) != MOE_OK)
+        return rc;
+      return cuda_status(moe::launch_quantize_mx_both(w_dn, E, d, m, u8(dn), u8(dn_scale), u8(dn_t), u8(dn_t_scale),
+                                                      false, stream));
+    }
+    if ((rc = cuda_status(moe::launch_quantize_mx(w_gu, E, 2 * m, d, false, u8(gu), u8(gu_scale), false, stream))) !=
+        MOE_OK)
+      return rc;
+    return cuda_status(moe::launch_quantize_mx(w_dn, E, d, m, false, u8(dn), u8(dn_scale), false, stream));
+  }
+  // BF16 experts: the masters are the forward operands (copied when gu / dn name
+  // other buffers); the backward reads per-expert transposes
+  if (gu && gu != w_gu &&
+      cudaMemcpyAsync(gu, w_gu, static_cast<size_t>(E) * 2 * m * d * 2, cudaMemcpyDeviceToDevice, stream) !=
+          cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (dn && dn != w_dn &&
+      cudaMemcpyAsync(dn, w_dn, static_cast<size_t>(E) * d * m * 2, cudaMemcpyDeviceToDevice, stream) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (!bwd) return MOE_OK;
+  if ((rc = cuda_status(moe::launch_transpose_bf16(w_gu, E, 2 * m, d, gu_t, stream))) != MOE_OK) return rc;
+  return cuda_status(moe::launch_transpose_bf16(w_dn, E, d, m, dn_t, stream));
+}
+
+static int scales_layout(const void *src, int64_t rows, int32_t K, bool to_tiled, void *dst,
+                         moe_stream_t stream) {
+  if (!src || !dst || rows <= 0 || K <= 0) return MOE_ERR_ARG;
+  if (src == dst) return MOE_ERR_ARG;
+  if (rows % 128 || K % 128) return MOE_ERR_SHAPE;
+  if (!aligned16(src) || !aligned16(dst)) return MOE_ERR_ALIGN;
+  DeviceInfo dev;
+  const int rc = device_info(&dev);
+  if (rc != MOE_OK) return rc;
+  return cuda_status(moe::launch_scales_layout(src, static_cast<long>(rows), K, to_tiled, dst, stream));
+}
+
+int moe_prepare_scales(const void *scales, int64_t rows, int32_t K, void *prepared, moe_stream_t stream) {
+  return scales_layout(scales, rows, K, true, prepared, stream);
+}
+
+int moe_canonical_scales(const void *prepared, int64_t rows, int32_t K, void *scales, moe_stream_t stream) {
+  return scales_layout(prepared, rows, K, false, scales, stream);
 }
 
 int moe_transpose_bf16(const void *src, int batch, int rows, int cols, void *dst,
@@ -1059,28 +1137,12 @@ int moe_backward(const moe_config *cfg, const void *dy, const void *x, const moe
       moe::launch_reverse_dispatch(dX, s_dx, g, D.T, D.d, D.k, D.E, rb, dx, dlogits, aux_grad, s));
 }
 
-// ---------------------------------------------------------------- router (cuBLAS)
-namespace {
-std::mutex g_blas_mu;
-cublasHandle_t g_blas[64] = {};
-
-// The calling device's cuBLAS handle bound to `s`, with its workspace inside ws.
-int blas_handle(cublasHandle_t *out, void *ws_part, cudaStream_t s) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(g_blas_mu);
-  if (!g_blas[dev] && cublasCreate(&g_blas[dev]) != CUBLAS_STATUS_SUCCESS) return MOE_ERR_CUDA;
-  cublasHandle_t h = g_blas[dev];
-  if (cublasSetStream(h, s) != CUBLAS_STATUS_SUCCESS ||
-      cublasSetWorkspace(h, ws_part, kCublasWorkspace) != CUBLAS_STATUS_SUCCESS ||
-      cublasSetMathMode(h, CUBLAS_DEFAULT_MATH) != CUBLAS_STATUS_SUCCESS)
-    return MOE_ERR_CUDA;
-  *out = h;
-  return MOE_OK;
-}
-
-int blas_status(cublasStatus_t st) { return st == CUBLAS_STATUS_SUCCESS ? MOE_OK : MOE_ERR_CUDA; }
-}  // namespace
+// ---------------------------------------------------------------- router projection
+// The router GEMMs run on the library's own tcgen05 GEMM (DENSE schedule,
+// single-CTA kernel).  Shapes the tiles do not cover (E not a multiple of the
+// tile width, T not a multiple of 128) go through zero-padded copies in the
+// workspace: Ep = E rounded up to 128, Tp = T rounded up to 128.
+static long router_ep(const Dims &D) { return (D.E + 127L) / 128 * 128; }
 
 int moe_router_forward(const moe_config *cfg, const void *x, const void *W_r, float *logits, void *ws,
                        moe_stream_t stream) {
@@ -1089,16 +1151,34 @@ int moe_router_forward(const moe_config *cfg, const void *x, const void *W_r, fl
   if (rc != MOE_OK) return rc;
   if (!x || !W_r || !logits || !ws) return MOE_ERR_ARG;
   if (!aligned16(x) || !aligned16(W_r) || !aligned16(logits) || !aligned16(ws)) return MOE_ERR_ALIGN;
+  DeviceInfo dev;
+  if ((rc = device_info(&dev)) != MOE_OK) return rc;
   Layout W;
   ws_layout(D, W);
-  cublasHandle_t h;
-  if ((rc = blas_handle(&h, W.ptr(ws, "cublas_ws"), stream)) != MOE_OK) return rc;
   Traced tr("router_forward", stream);
-  // row-major logits [T, E] = x [T, d] W_r^T, i.e. column-major [E, T] = W_r^(T) x
-  const float one = 1.f, zero = 0.f;
-  return blas_status(cublasGemmEx(h, CUBLAS_OP_T, CUBLAS_OP_N, D.E, D.T, D.d, &one, W_r, CUDA_R_16BF, D.d, x,
-                                  CUDA_R_16BF, D.d, &zero, logits, CUDA_R_32F, D.E, CUBLAS_COMPUTE_32F,
-                                  CUBLAS_GEMM_DEFAULT));
+  const long Ep = router_ep(D);
+  float *lpad = reinterpret_cast<float *>(W.ptr(ws, "router_lpad"));  // [Tp, Ep]
+  // logits [T, E] = x [T, d] W_r [E, d]^T, fp32 accumulation and output
+  Gemm q;
+  q.mx = false;
+  q.bn = bn_for(Ep);
+  q.epi = moe::EPI_STORE_F32;
+  q.a = x;
+  q.a_rows = D.T;
+  q.b = W_r;
+  q.b_rows = D.E;  // rows E .. Ep - 1 of the B tiles read as zero
+  q.K = D.d;
+  q.g = base_args(moe::SCHED_DENSE, 1, nullptr, reinterpret_cast<int *>(W.ptr(ws, "status")));
+  q.g.M = D.T;
+  q.g.K = D.d;
+  q.g.n_tiles = static_cast<int>(Ep / q.bn);
+  q.g.b_rows_per_group = static_cast<int>(Ep);
+  q.g.out = lpad;
+  q.g.ldo = Ep;
+  q.max_tiles = (D.Tp / 128) * q.g.n_tiles;
+  q.out_rows = D.Tp;
+  if ((rc = run_gemm_single(q, dev, stream)) != MOE_OK) return rc;
+  return cuda_status(moe::launch_crop_f32(lpad, D.T, D.E, Ep, logits, stream));
 }
 
 int moe_router_backward(const moe_config *cfg, const float *dlogits, const void *x, const void *W_r, void *dx,
@@ -1111,24 +1191,73 @@ int moe_router_backward(const moe_config *cfg, const float *dlogits, const void 
   if (!aligned16(dlogits) || !aligned16(x) || !aligned16(W_r) || !aligned16(dx) || !aligned16(dW_r) ||
       !aligned16(ws))
     return MOE_ERR_ALIGN;
+  DeviceInfo dev;
+  if ((rc = device_info(&dev)) != MOE_OK) return rc;
   Layout W;
   ws_layout(D, W);
-  cublasHandle_t h;
-  if ((rc = blas_handle(&h, W.ptr(ws, "cublas_ws"), stream)) != MOE_OK) return rc;
   Traced tr("router_backward", stream);
-  void *gb = W.ptr(ws, "router_g");
-  if ((rc = cuda_status(moe::launch_to_bf16(dlogits, static_cast<long>(D.T) * D.E, gb, stream))) != MOE_OK)
+  const long Ep = router_ep(D), Tp = D.Tp;
+  int *status = reinterpret_cast<int *>(W.ptr(ws, "status"));
+  char *G = W.ptr(ws, "router_g");      // [Tp, Ep] bf16(dlogits), zero-padded
+  char *GT = W.ptr(ws, "router_gT");    // [Ep, Tp]
+  char *WrT = W.ptr(ws, "router_WrT");  // [d, Ep] = W_r^T, zero-padded
+  char *xT = W.ptr(ws, "router_xT");    // [d, Tp] = x^T, zero-padded
+  if ((rc = cuda_status(moe::launch_pad_to_bf16(dlogits, D.T, D.E, static_cast<int>(Tp), static_cast<int>(Ep), G,
+                                                stream))) != MOE_OK)
     return rc;
-  const float one = 1.f, zero = 0.f;
-  // dx [T, d] += g [T, E] W_r [E, d]  (column-major: dx^T [d, T] += W_r^T [d, E] g^T [E, T])
-  rc = blas_status(cublasGemmEx(h, CUBLAS_OP_N, CUBLAS_OP_N, D.d, D.T, D.E, &one, W_r, CUDA_R_16BF, D.d, gb,
-                                CUDA_R_16BF, D.E, &one, dx, CUDA_R_16BF, D.d, CUBLAS_COMPUTE_32F,
-                                CUBLAS_GEMM_DEFAULT));
-  if (rc != MOE_OK) return rc;
-  // dW_r [E, d] = g^T [E, T] x [T, d]  (column-major: dW_r^T [d, E] = x^T [d, T] g [T, E])
-  return blas_status(cublasGemmEx(h, CUBLAS_OP_N, CUBLAS_OP_T, D.d, D.E, D.T, &one, x, CUDA_R_16BF, D.d, gb,
-                                  CUDA_R_16BF, D.E, &zero, dW_r, CUDA_R_16BF, D.d, CUBLAS_COMPUTE_32F,
-                                  CUBLAS_GEMM_DEFAULT));
+  if ((rc = cuda_status(moe::launch_transpose_rows(W_r, D.d, static_cast<int>(Ep), nullptr, D.E, false, D.k, D.E,
+                                                   nullptr, Ep, WrT, Ep, stream))) != MOE_OK)
+    return rc;
+  // dx [T, d] = bf16(dx + g W_r): A = g [Tp, Ep], B = W_r^T [d, Ep], K = Ep
+  {
+    Gemm q;
+    q.mx = false;
+    q.bn = bn_for(D.d);
+    q.epi = moe::EPI_ADD_BF16;
+    q.a = G;
+    q.a_rows = Tp;
+    q.b = WrT;
+    q.b_rows = D.d;
+    q.K = Ep;
+    q.g = base_args(moe::SCHED_DENSE, 1, nullptr, status);
+    q.g.M = D.T;
+    q.g.K = static_cast<int>(Ep);
+    q.g.n_tiles = D.d / q.bn;
+    q.g.b_rows_per_group = D.d;
+    q.g.out = dx;
+    q.g.ldo = D.d;
+    q.g.aux = dx;
+    q.g.ld_aux = D.d;
+    q.max_tiles = (Tp / 128) * q.g.n_tiles;
+    q.out_rows = D.T;
+    if ((rc = run_gemm_single(q, dev, stream)) != MOE_OK) return rc;
+  }
+  // dW_r [E, d] = bf16(g^T x): A = g^T [Ep, Tp], B = x^T [d, Tp], K = Tp
+  if ((rc = cuda_status(moe::launch_transpose_rows(G, static_cast<int>(Ep), static_cast<int>(Tp), nullptr, Tp,
+                                                   false, D.k, D.E, nullptr, Tp, GT, Tp, stream))) != MOE_OK)
+    return rc;
+  if ((rc = cuda_status(moe::launch_transpose_rows(x, D.d, static_cast<int>(Tp), nullptr, D.T, false, D.k, D.E,
+                                                   nullptr, Tp, xT, Tp, stream))) != MOE_OK)
+    return rc;
+  Gemm q;
+  q.mx = false;
+  q.bn = bn_for(D.d);
+  q.epi = moe::EPI_STORE;
+  q.a = GT;
+  q.a_rows = Ep;
+  q.b = xT;
+  q.b_rows = D.d;
+  q.K = Tp;
+  q.g = base_args(moe::SCHED_DENSE, 1, nullptr, status);
+  q.g.M = static_cast<int>(Ep);
+  q.g.K = static_cast<int>(Tp);
+  q.g.n_tiles = D.d / q.bn;
+  q.g.b_rows_per_group = D.d;
+  q.g.out = dW_r;
+  q.g.ldo = D.d;
+  q.max_tiles = (Ep / 128) * q.g.n_tiles;
+  q.out_rows = D.E;
+  return run_gemm_single(q, dev, stream);
 }
 
 int moe_get_status(void *ws, moe_stream_t stream) {

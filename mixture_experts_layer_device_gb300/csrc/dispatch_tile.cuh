@@ -60,6 +60,7 @@ MOE_DEV int tcol(int r, int c) { return (((c >> 3) ^ ((r >> 3) & 3)) << 3) | (c 
 // col0 + c of the transposed codes (row stride ld_t) at columns r0 .. r0 + 31,
 // and the block's scale byte into the tiled scales (K = ld_t) at row
 // sf_row0 + col0 + c.
+template <bool CANON = false>
 MOE_DEV void column_block_codes(const uint16_t (*tile)[256], int c, long col0, int r0, uint8_t *__restrict__ dT,
                                 uint8_t *__restrict__ dT_sf, long ld_t, long sf_row0 = 0) {
   float v[32];
@@ -74,7 +75,9 @@ MOE_DEV void column_block_codes(const uint16_t (*tile)[256], int c, long col0, i
   mx_encode32(v, byte, w);
   const long ocol = col0 + c;
   st_global_32B(dT + ocol * ld_t + r0, w);
-  dT_sf[sf_tiled_offset(sf_row0 + ocol, r0 / 32, ld_t)] = static_cast<uint8_t>(byte);
+  const long srow = sf_row0 + ocol;
+  dT_sf[CANON ? static_cast<size_t>(srow) * (ld_t / 32) + r0 / 32 : sf_tiled_offset(srow, r0 / 32, ld_t)] =
+      static_cast<uint8_t>(byte);
 }
 
 // MXFP8 dispatch of the 32 expert-sorted padded rows [r0, r0 + 32) by 256

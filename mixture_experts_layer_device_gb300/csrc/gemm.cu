@@ -459,7 +459,7 @@ __global__ void __launch_bounds__(64 + 32 * epi_warps<EPI, BN>(), 1)
     const int part = (warp - 2) >> 2;  // which half of the columns (8 epilogue warps)
     const int r = q * 32 + lane;
     Stager st(staging + (warp - 2) * (C::STAGING_BYTES / NEPI));
-    const OutView vO = out_view(g.out, g.ldo, g.out_rows, 2);
+    const OutView vO = out_view(g.out, g.ldo, g.out_rows, EPI == EPI_STORE_F32 ? 4 : 2);
     const OutView vO2 = out_view(g.out2, g.ldo2, g.out_rows, 2);
     const OutView vQ = out_view(g.outq, g.ldq, g.out_rows, 1);
     if (lane == 0) {
@@ -574,6 +574,10 @@ cudaError_t launch_gemm(bool mx, int bn, int epi, const CUtensorMap &ta, const C
   MOE_GEMM_CASE(false, 256, EPI_SWIGLU)
   MOE_GEMM_CASE(false, 256, EPI_SWIGLU_BWD)
   MOE_GEMM_CASE(false, 128, EPI_SWIGLU_BWD)
+  MOE_GEMM_CASE(false, 256, EPI_STORE_F32)
+  MOE_GEMM_CASE(false, 128, EPI_STORE_F32)
+  MOE_GEMM_CASE(false, 256, EPI_ADD_BF16)
+  MOE_GEMM_CASE(false, 128, EPI_ADD_BF16)
   MOE_GEMM_CASE(true, 256, EPI_STORE)
   MOE_GEMM_CASE(true, 128, EPI_STORE)
   MOE_GEMM_CASE(true, 256, EPI_SWIGLU)

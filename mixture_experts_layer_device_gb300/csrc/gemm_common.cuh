@@ -332,6 +332,39 @@ MOE_DEV void epilogue_tile_split(const GemmArgs &g, const OutView &vO, const Out
 #pragma unroll
       for (int c = 0; c < NC32; ++c) st.put(vO, raw + 16 * c, out_col + c0 + 32 * c, row0, lane);
     }
+  } else if constexpr (EPI == EPI_STORE_F32 || EPI == EPI_ADD_BF16) {
+    // This warp's BN/2 columns in one round of TMEM loads, then TMEM is
+    // released.  STORE_F32 writes the fp32 accumulator (16 values per 64-byte
+    // piece); ADD_BF16 adds the current bf16 output row (read through aux, the
+    // same buffer) and rounds the sum to bf16 once.
+    constexpr int NC = BN / 2;
+    const int c0 = part * NC;
+    uint32_t raw[NC];
+#pragma unroll
+    for (int c = 0; c < NC / 32; ++c) tmem_ld32_async(tb + c0 + 32 * c, raw + 32 * c);
+    tmem_ld_wait();
+    reg_fence<NC>(raw);
+    release();
+    if (!store) return;
+    if constexpr (EPI == EPI_STORE_F32) {
+#pragma unroll
+      for (int c = 0; c < NC / 16; ++c) st.put(vO, raw + 16 * c, out_col + c0 + 16 * c, row0, lane);
+    } else {
+      const bool in = grow < g.out_rows;
+#pragma unroll 1
+      for (int c = 0; c < NC / 32; ++c) {
+        float v[32];
+        if (in) {
+          load_bf16x32(g.aux, grow, g.ld_aux, out_col + c0 + 32 * c, v);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] += __uint_as_float(raw[32 * c + i]);
+        st.put_bf16(vO, v, out_col + c0 + 32 * c, row0, lane);
+      }
+    }
   } else if constexpr (EPI == EPI_SWIGLU_BWD) {
     // This warp's BN/2 dh columns, 64 at a time: each chunk is read from TMEM,
     // then processed; TMEM is released once the last chunk has been read.

@@ -589,9 +589,11 @@ __global__ void __launch_bounds__(256) reverse_dispatch_kernel(
 // 32-value block, and writes its 32 codes plus the scale byte; bf16 output
 // rows are written 64 bytes at a time by 4 threads each.
 // ROWQ (MX, weights): the tile's source rows are also quantised along C into
-// row-blocked codes rq [batch * nrows, C] with tiled scales (K = C), so one
-// read of the bf16 source gives both operand orientations.
-template <bool MX, bool GATHER, bool ROWQ = false, int CH = 1>
+// row-blocked codes rq [batch * nrows, C] with scales over K = C, so one read
+// of the bf16 source gives both operand orientations.
+// CANON (MX): every scale byte goes to the canonical [rows, K/32] position
+// instead of the tiled operand layout (the C ABI's weight quantisers).
+template <bool MX, bool GATHER, bool ROWQ = false, int CH = 1, bool CANON = false>
 __global__ void __launch_bounds__(256) transpose_rows_kernel(
     const uint16_t *__restrict__ src, long src_batch_stride, int C, int nrows_host,
     const int *__restrict__ nrows_dev, long nsrc, int k, int E, RouteBufs b, void *dst,
@@ -636,7 +638,9 @@ __global__ void __launch_bounds__(256) transpose_rows_kernel(
         uint32_t byte;
         const uint2 code = mx_encode8_quad(f, &byte);
         *reinterpret_cast<uint2 *>(rq + static_cast<size_t>(qrow) * C + col) = code;
-        if ((tid & 3) == 0) rq_sf[sf_tiled_offset(qrow, col >> 5, C)] = static_cast<uint8_t>(byte);
+        if ((tid & 3) == 0)
+          rq_sf[CANON ? static_cast<size_t>(qrow) * (C / 32) + (col >> 5) : sf_tiled_offset(qrow, col >> 5, C)] =
+              static_cast<uint8_t>(byte);
       }
       *reinterpret_cast<uint4 *>(&tile[h][rr][tcol(rr, 64 * j + cc)]) = q[h][j];
     }
@@ -648,7 +652,7 @@ __global__ void __launch_bounds__(256) transpose_rows_kernel(
     if constexpr (MX) {
       // thread c: source column cb + c = output row cb + c, one 32-value block
       if (tid < 64 * nsub[h])
-        column_block_codes(tile[h], tid, cb, r0,
+        column_block_codes<CANON>(tile[h], tid, cb, r0,
                            reinterpret_cast<uint8_t *>(dst) + static_cast<size_t>(bz) * dst_batch_stride, dst_sf,
                            ld_dst, static_cast<long>(bz) * sf_batch_rows);
     } else {
@@ -689,6 +693,21 @@ __global__ void __launch_bounds__(256) quantize_rows_kernel(const uint4 *__restr
       sf[TILED ? sf_tiled_offset(r, i >> 2, cols) : static_cast<size_t>(r) * (cols / 32) + (i >> 2)] =
           static_cast<uint8_t>(byte);
   }
+}
+
+// MXFP8 scales between the canonical order [rows, K/32] and the tiled operand
+// layout, one 4-byte word (4 consecutive blocks of a row = 4 consecutive
+// bytes in both layouts) per thread, threads in canonical order.
+template <bool TO_TILED>
+__global__ void __launch_bounds__(256) scales_layout_kernel(const uint32_t *__restrict__ src,
+                                                            uint32_t *__restrict__ dst, long rows, int K) {
+  const long kw = K / 128;  // words per row
+  const long i = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= rows * kw) return;
+  const long r = i / kw, j = i % kw;
+  const size_t t = sf_tiled_offset(r, 4 * j, K) / 4;
+  if (TO_TILED) dst[t] = __ldg(src + i);
+  else dst[i] = __ldg(src + t);
 }
 
 // Zeros of the empty experts' weight gradients: block (x, e) clears bytes
@@ -823,16 +842,24 @@ cudaError_t launch_transpose_rows(const void *src, int C, int nrows_out, const i
 }
 
 cudaError_t launch_quantize_mx(const void *src, int batch, int rows, int cols, bool transpose,
-                               uint8_t *codes, uint8_t *scales, cudaStream_t s) {
+                               uint8_t *codes, uint8_t *scales, bool canon, cudaStream_t s) {
   if (!transpose) {
     const long total = static_cast<long>(batch) * rows;
-    quantize_rows_kernel<true><<<blocks_for(total, 8), 256, 0, s>>>(
-        static_cast<const uint4 *>(src), total, cols, reinterpret_cast<uint2 *>(codes), scales);
+    if (canon)
+      quantize_rows_kernel<false><<<blocks_for(total, 8), 256, 0, s>>>(
+          static_cast<const uint4 *>(src), total, cols, reinterpret_cast<uint2 *>(codes), scales);
+    else
+      quantize_rows_kernel<true><<<blocks_for(total, 8), 256, 0, s>>>(
+          static_cast<const uint4 *>(src), total, cols, reinterpret_cast<uint2 *>(codes), scales);
   } else {
     const dim3 grid(blocks_for(rows, 32), blocks_for(cols, 256), batch);
-    transpose_rows_kernel<true, false><<<grid, 256, 0, s>>>(
-        static_cast<const uint16_t *>(src), static_cast<long>(rows) * cols, cols, rows, nullptr, rows,
-        1, 1, RouteBufs{}, codes, static_cast<long>(rows) * cols, scales, cols, rows);
+#define MOE_QT(CANON)                                                                                       \
+  transpose_rows_kernel<true, false, false, 1, CANON><<<grid, 256, 0, s>>>(                                  \
+      static_cast<const uint16_t *>(src), static_cast<long>(rows) * cols, cols, rows, nullptr, rows, 1, 1, \
+      RouteBufs{}, codes, static_cast<long>(rows) * cols, scales, cols, rows)
+    if (canon) MOE_QT(true);
+    else MOE_QT(false);
+#undef MOE_QT
   }
   return cudaGetLastError();
 }
@@ -857,25 +884,75 @@ cudaError_t launch_balance(const float *logits, int T, int E, int k, const int *
   return cudaGetLastError();
 }
 
+// Thread per 8 output columns of one row (one 16-byte store).
+__global__ void __launch_bounds__(256) pad_to_bf16_kernel(const float *__restrict__ src, int rows, int cols,
+                                                          int rows_p, int cols_p, uint4 *__restrict__ dst) {
+  const long i = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int per_row = cols_p / 8;
+  if (i >= static_cast<long>(rows_p) * per_row) return;
+  const int r = static_cast<int>(i / per_row);
+  const int c0 = static_cast<int>(i % per_row) * 8;
+  float f[8];
+#pragma unroll
+  for (int q = 0; q < 8; ++q)
+    f[q] = (r < rows && c0 + q < cols) ? __ldg(src + static_cast<size_t>(r) * cols + c0 + q) : 0.f;
+  dst[i] = pack8(f);
+}
+
+__global__ void __launch_bounds__(256) crop_f32_kernel(const float *__restrict__ src, int rows, int cols,
+                                                       long ld_src, float *__restrict__ dst) {
+  const long i = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= static_cast<long>(rows) * cols) return;
+  const long r = i / cols, c = i % cols;
+  dst[i] = __ldg(src + r * ld_src + c);
+}
+
+cudaError_t launch_pad_to_bf16(const float *src, int rows, int cols, int rows_p, int cols_p, void *dst,
+                               cudaStream_t s) {
+  const long n = static_cast<long>(rows_p) * (cols_p / 8);
+  pad_to_bf16_kernel<<<blocks_for(n, 256), 256, 0, s>>>(src, rows, cols, rows_p, cols_p, static_cast<uint4 *>(dst));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_crop_f32(const float *src, int rows, int cols, long ld_src, float *dst, cudaStream_t s) {
+  crop_f32_kernel<<<blocks_for(static_cast<long>(rows) * cols, 256), 256, 0, s>>>(src, rows, cols, ld_src, dst);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_to_bf16(const float *src, long n, void *dst, cudaStream_t s) {
   to_bf16_kernel<<<blocks_for(n, 256), 256, 0, s>>>(src, n, static_cast<uint16_t *>(dst));
   return cudaGetLastError();
 }
 
 cudaError_t launch_quantize_mx_both(const void *src, int batch, int rows, int cols, uint8_t *codes,
-                                    uint8_t *scales, uint8_t *codes_t, uint8_t *scales_t, cudaStream_t s) {
+                                    uint8_t *scales, uint8_t *codes_t, uint8_t *scales_t, bool canon,
+                                    cudaStream_t s) {
   // two 256-column chunks per block (twice the loads in flight) when they tile cols
+#define MOE_QB(CH, CANON)                                                                                    \
+  transpose_rows_kernel<true, false, true, CH, CANON><<<grid, 256, 0, s>>>(                                  \
+      static_cast<const uint16_t *>(src), static_cast<long>(rows) * cols, cols, rows, nullptr, rows, 1, 1,  \
+      RouteBufs{}, codes_t, static_cast<long>(rows) * cols, scales_t, cols, rows, codes, scales)
   if (cols % 512 == 0) {
     const dim3 grid(blocks_for(rows, 32), blocks_for(cols, 512), batch);
-    transpose_rows_kernel<true, false, true, 2><<<grid, 256, 0, s>>>(
-        static_cast<const uint16_t *>(src), static_cast<long>(rows) * cols, cols, rows, nullptr, rows, 1, 1,
-        RouteBufs{}, codes_t, static_cast<long>(rows) * cols, scales_t, cols, rows, codes, scales);
+    if (canon) MOE_QB(2, true);
+    else MOE_QB(2, false);
   } else {
     const dim3 grid(blocks_for(rows, 32), blocks_for(cols, 256), batch);
-    transpose_rows_kernel<true, false, true><<<grid, 256, 0, s>>>(
-        static_cast<const uint16_t *>(src), static_cast<long>(rows) * cols, cols, rows, nullptr, rows, 1, 1,
-        RouteBufs{}, codes_t, static_cast<long>(rows) * cols, scales_t, cols, rows, codes, scales);
+    if (canon) MOE_QB(1, true);
+    else MOE_QB(1, false);
   }
+#undef MOE_QB
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scales_layout(const void *src, long rows, int K, bool to_tiled, void *dst, cudaStream_t s) {
+  const long n = rows * (K / 128);
+  if (to_tiled)
+    scales_layout_kernel<true><<<blocks_for(n, 256), 256, 0, s>>>(static_cast<const uint32_t *>(src),
+                                                                   static_cast<uint32_t *>(dst), rows, K);
+  else
+    scales_layout_kernel<false><<<blocks_for(n, 256), 256, 0, s>>>(static_cast<const uint32_t *>(src),
+                                                                    static_cast<uint32_t *>(dst), rows, K);
   return cudaGetLastError();
 }
 

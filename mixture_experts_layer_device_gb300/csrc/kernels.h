@@ -76,21 +76,30 @@ cudaError_t launch_transpose_rows(const void *src, int C, int nrows_out, const i
                                   long nsrc, bool gather, int k, int E, const RouteBufs *b,
                                   int64_t rows_alloc, void *dst, int64_t ld_dst, cudaStream_t s);
 
-// Weight preparation.
+// Weight preparation: scales canonical [rows, K/32] (canon) or in the tiled
+// operand layout the GEMMs read.
 cudaError_t launch_quantize_mx(const void *src, int batch, int rows, int cols, bool transpose,
-                               uint8_t *codes, uint8_t *scales, cudaStream_t s);
+                               uint8_t *codes, uint8_t *scales, bool canon, cudaStream_t s);
 cudaError_t launch_transpose_bf16(const void *src, int batch, int rows, int cols, void *dst,
                                   cudaStream_t s);
 
 // ---------------------------------------------------------------- GEMM
 enum GemmSched { SCHED_GROUP_M = 0, SCHED_DENSE = 1, SCHED_GROUP_K = 2 };
-enum GemmEpi { EPI_STORE = 0, EPI_SWIGLU = 1, EPI_SWIGLU_BWD = 2 };
+// EPI_STORE_F32: fp32 output (the router logits); EPI_ADD_BF16: out = bf16(out +
+// acc) with `out` read back through aux (the router's dx contribution).  Both
+// run on the single-CTA kernel only.
+enum GemmEpi { EPI_STORE = 0, EPI_SWIGLU = 1, EPI_SWIGLU_BWD = 2, EPI_STORE_F32 = 3, EPI_ADD_BF16 = 4 };
+
+// MXFP8 scales [rows, K/32] canonical -> tiled operand layout (to_tiled) or back;
+// rows and K multiples of 128.
+cudaError_t launch_scales_layout(const void *src, long rows, int K, bool to_tiled, void *dst, cudaStream_t s);
 
 // Both MXFP8 orientations of bf16 weights [batch, rows, cols] from one read:
 // codes/scales as launch_quantize_mx(transpose = false), codes_t/scales_t as
 // launch_quantize_mx(transpose = true).
 cudaError_t launch_quantize_mx_both(const void *src, int batch, int rows, int cols, uint8_t *codes,
-                                    uint8_t *scales, uint8_t *codes_t, uint8_t *scales_t, cudaStream_t s);
+                                    uint8_t *scales, uint8_t *codes_t, uint8_t *scales_t, bool canon,
+                                    cudaStream_t s);
 
 // Load-balancing term (Switch-style, over the routed slots): per-block partial
 // sums of the full softmax (part [balance_blocks(T), E]), the gradient rows
@@ -102,6 +111,12 @@ cudaError_t launch_balance(const float *logits, int T, int E, int k, const int *
                            float *grad, float *out, cudaStream_t s);
 // dst[i] = bf16(src[i]) (round to nearest even), n values.
 cudaError_t launch_to_bf16(const float *src, long n, void *dst, cudaStream_t s);
+// dst [rows_p, cols_p] bf16 = bf16(src [rows, cols] fp32), zero beyond rows / cols
+// (cols_p a multiple of 8).
+cudaError_t launch_pad_to_bf16(const float *src, int rows, int cols, int rows_p, int cols_p, void *dst,
+                               cudaStream_t s);
+// dst [rows, cols] fp32 = the top-left corner of src [*, ld_src] fp32.
+cudaError_t launch_crop_f32(const float *src, int rows, int cols, long ld_src, float *dst, cudaStream_t s);
 
 // Row-blocked MXFP8 codes of every token: x [T, d] bf16 -> codes [T, d] and
 // canonical scales [T, d/32] (the ring dispatch gathers these rows).

@@ -7,7 +7,7 @@ library's CUDA kernels; torch only allocates memory and provides the stream.
 import torch
 
 from . import (MOE_BF16, MOE_FLAG_BACKWARD, MOE_MXFP8, check, config, moe_backward, moe_buffer_info,
-               moe_forward, moe_get_status, moe_padded_rows, moe_quantize_mx, moe_quantize_mx_both,
+               moe_forward, moe_get_status, moe_padded_rows, moe_prepare_weights,
                moe_router_backward, moe_router_forward, moe_saved_bytes, moe_transpose_bf16,
                moe_workspace_bytes, weights)
 
@@ -28,7 +28,7 @@ class MoELayer:
 
     ``expert(e)`` returns the bf16 masters (W_gu [2m, d], W_dn [d, m]) of
     expert e as device tensors; they are converted expert by expert into the
-    layout the kernels read (MXFP8 codes + tiled scales, and for the backward
+    layout the kernels read (MXFP8 codes + prepared scales, and for the backward
     the per-expert transposed copies), so the masters never need to be
     resident all at once.  Alternatively ``stacked=(W_gu [E, 2m, d], W_dn
     [E, d, m])`` converts all experts with one launch per operand.
@@ -87,15 +87,10 @@ class MoELayer:
             assert gu.is_cuda and gu.dtype == torch.bfloat16 and gu.shape == (2 * m, d)
             assert dn.is_cuda and dn.dtype == torch.bfloat16 and dn.shape == (d, m)
             gu, dn = gu.contiguous(), dn.contiguous()
-            if self.mx and self.backward_enabled:
-                check(moe_quantize_mx_both(gu, 1, 2 * m, d, t["gu"].view(-1)[e * gsz:], t["gu_scale"][e * gsz // 32:],
-                                           t["gu_t"].view(-1)[e * gsz:], t["gu_t_scale"][e * gsz // 32:]))
-                check(moe_quantize_mx_both(dn, 1, d, m, t["dn"].view(-1)[e * dsz:], t["dn_scale"][e * dsz // 32:],
-                                           t["dn_t"].view(-1)[e * dsz:], t["dn_t_scale"][e * dsz // 32:]))
-            elif self.mx:
-                check(moe_quantize_mx(gu, 1, 2 * m, d, 0, t["gu"].view(-1)[e * gsz:],
-                                      t["gu_scale"][e * gsz // 32:]))
-                check(moe_quantize_mx(dn, 1, d, m, 0, t["dn"].view(-1)[e * dsz:], t["dn_scale"][e * dsz // 32:]))
+            if self.mx:
+                # one expert: codes into its slice of the operands, canonical scales
+                # into scratch, then into its slice of the prepared scales
+                self._s0_mx(gu, dn, 1, e * gsz, e * dsz, None)
             else:
                 t["gu"][e].copy_(gu)
                 t["dn"][e].copy_(dn)
@@ -119,13 +114,22 @@ class MoELayer:
         W_dn [E, d, m]) into this layer's MXFP8 operands: one launch per
         master, which also writes the backward's transposed copies of a
         training layer.  Re-run after every update of the masters."""
-        E, d, m, t = self.E, self.d, self.m, self.tensors
-        if self.backward_enabled:
-            check(moe_quantize_mx_both(gu, E, 2 * m, d, t["gu"], t["gu_scale"], t["gu_t"], t["gu_t_scale"], stream))
-            check(moe_quantize_mx_both(dn, E, d, m, t["dn"], t["dn_scale"], t["dn_t"], t["dn_t_scale"], stream))
-        else:
-            check(moe_quantize_mx(gu, E, 2 * m, d, 0, t["gu"], t["gu_scale"], stream))
-            check(moe_quantize_mx(dn, E, d, m, 0, t["dn"], t["dn_scale"], stream))
+        self._s0_mx(gu, dn, self.E, 0, 0, stream)
+
+    def _s0_mx(self, gu, dn, n, off_gu, off_dn, stream):
+        """MXFP8 S0 of n experts' masters (gu [n, 2m, d], dn [n, d, m]) straight
+        into the operands (codes and prepared scales) at element offsets off_gu /
+        off_dn: one moe_prepare_weights call, which for a training layer also
+        writes the backward orientation from the same read of each master."""
+        d, m, t, c = self.d, self.m, self.tensors, self.cfg
+        cfg = c if n == self.E else config(c.T, d, m, n, 1, c.m_shared, c.dtype, 0)
+        bw = self.backward_enabled
+        check(moe_prepare_weights(cfg, gu, dn, t["gu"].view(-1)[off_gu:], t["gu_scale"][off_gu // 32:],
+                                  t["dn"].view(-1)[off_dn:], t["dn_scale"][off_dn // 32:],
+                                  t["gu_t"].view(-1)[off_gu:] if bw else None,
+                                  t["gu_t_scale"][off_gu // 32:] if bw else None,
+                                  t["dn_t"].view(-1)[off_dn:] if bw else None,
+                                  t["dn_t_scale"][off_dn // 32:] if bw else None, stream))
 
     def prepare_from(self, gu, dn, s_gu=None, s_dn=None, stream=None):
         """Re-derive every operand the kernels read from the current bf16

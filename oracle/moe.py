@@ -116,7 +116,7 @@ def schedule(idx, E):
 # ----------------------------------------------------------------------------
 # 0. weight preparation (S0)
 # ----------------------------------------------------------------------------
-def prepare_expert(W_gu, W_dn, fmt, backward=True):
+def prepare_expert(W_gu, W_dn, fmt, backward=True, forward=True):
     """Operands the expert GEMMs read, from the bf16 masters of one expert.
 
     MXFP8 is the default expert format ("Mixture-of-Kittens" wiki page, Key
@@ -124,16 +124,23 @@ def prepare_expert(W_gu, W_dn, fmt, backward=True):
     [d, m] quantised along their K (d, m); the backward dgrad operands are
     W_dn^T [m, d] quantised along d and W_gu^T [d, 2m] quantised along 2m.
     Values are returned dequantised (float64).  Other formats use the masters.
+    ``forward`` / ``backward`` select which of the two pairs are made.
     """
     W_gu = np.asarray(W_gu, dtype=np.float64)
     W_dn = np.asarray(W_dn, dtype=np.float64)
+    ops = {}
     if fmt == "mxfp8":
-        ops = dict(gu_fwd=mx_roundtrip(W_gu, axis=1), dn_fwd=mx_roundtrip(W_dn, axis=1))
+        if forward:
+            ops["gu_fwd"] = mx_roundtrip(W_gu, axis=1)
+            ops["dn_fwd"] = mx_roundtrip(W_dn, axis=1)
         if backward:
             ops["dn_bwd"] = mx_roundtrip(W_dn.T, axis=1)
             ops["gu_bwd"] = mx_roundtrip(W_gu.T, axis=1)
     else:
-        ops = dict(gu_fwd=W_gu, dn_fwd=W_dn, dn_bwd=W_dn.T, gu_bwd=W_gu.T)
+        if forward:
+            ops.update(gu_fwd=W_gu, dn_fwd=W_dn)
+        if backward:
+            ops.update(dn_bwd=W_dn.T, gu_bwd=W_gu.T)
     return ops
 
 
@@ -290,7 +297,8 @@ def backward(dy, x, experts, k, fmt, saved, shared=None, dw_experts=None):
     """Layer backward.
 
     dy [T, d] bf16 values.  Returns dict(dx [T, d], dlogits [T, E] fp64,
-    dW_gu {e: [2m, d]}, dW_dn {e: [d, m]}, dWs_gu, dWs_dn).  ``dw_experts``
+    dW_gu {e: [2m, d]}, dW_dn {e: [d, m]}, dWs_gu, dWs_dn, and the
+    expert-sorted intermediates dO [R, d], dX [R, d], dGU [R, 2m], g [T, k]).  ``dw_experts``
     restricts which experts get weight gradients (all when None); dx and
     dlogits always cover every token.
     """
@@ -310,6 +318,7 @@ def backward(dy, x, experts, k, fmt, saved, shared=None, dw_experts=None):
     g = g_rows[perm].reshape(T, k)
     # B2-B5 per expert
     dX = np.zeros((R, d))
+    dGU = None
     dW_gu, dW_dn = {}, {}
     want = set(range(E)) if dw_experts is None else set(dw_experts)
     for e in range(E):
@@ -324,6 +333,9 @@ def backward(dy, x, experts, k, fmt, saved, shared=None, dw_experts=None):
         res = expert_backward(dO[r0:r1], x[row_tok[r0:r1]], saved["GU"][r0:r1],
                               saved["h"][r0:r1], W_gu, W_dn, fmt, ops)
         dX[r0:r1] = res["dX"]
+        if dGU is None:
+            dGU = np.zeros((R, res["dGU"].shape[1]))
+        dGU[r0:r1] = res["dGU"]
         if e in want:
             dW_gu[e] = res["dW_gu"]
             dW_dn[e] = res["dW_dn"]
@@ -345,7 +357,7 @@ def backward(dy, x, experts, k, fmt, saved, shared=None, dw_experts=None):
     dlogits = np.zeros((T, E))
     np.put_along_axis(dlogits, idx, dl_sel, axis=1)
     return dict(dx=dx, dlogits=dlogits, dW_gu=dW_gu, dW_dn=dW_dn, dWs_gu=dWs_gu,
-                dWs_dn=dWs_dn, dO=dO, g=g, dX=dX)
+                dWs_dn=dWs_dn, dO=dO, g=g, dX=dX, dGU=dGU)
 
 
 # ----------------------------------------------------------------------------

@@ -22,7 +22,7 @@ TOL = {"bf16": 5e-3, "mxfp8": 3e-2}
 class Case:
     """Inputs drawn on the CPU (small workloads), a GPU layer, and oracle views."""
 
-    def __init__(self, cfg, backward=False, device="cuda"):
+    def __init__(self, cfg, backward=False, device="cuda", flags=0):
         from mixture_experts_layer_device_gb300.layer import MoELayer
         self.cfg = cfg
         self.logits = mi.logits(cfg)
@@ -33,7 +33,7 @@ class Case:
         self.layer = MoELayer(cfg["T"], cfg["d"], cfg["m"], cfg["E"], cfg["k"], cfg["fmt"],
                               lambda e: (self.gu[e].to(device), self.dn[e].to(device)),
                               shared=None if self.shared is None else tuple(w.to(device) for w in self.shared),
-                              backward=backward, device=device)
+                              backward=backward, device=device, flags=flags)
         self.xg = self.x.to(device)
         self.lg = self.logits.to(device)
         self.dyg = self.dy.to(device)
@@ -131,3 +131,62 @@ def prepare_subset(cfg, gu_all, dn_all, experts, backward):
                 table[e] = (np.broadcast_to(np.float64(0.0), shape_gu), np.broadcast_to(np.float64(0.0), shape_dn),
                             {k: _compact(v) for k, v in ops.items()})
     return ExpertSubset(cfg["E"], table)
+
+
+# ---------------------------------------------------------------- streamed oracle experts
+def _bf16_bits(t):
+    """Raw bf16 bits of a device tensor as a host uint16 array (half the bytes of fp32)."""
+    return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def _stream_worker(args):
+    e, gu_bits, dn_bits, fmt, forward, backward = args
+    ops = om.prepare_expert(nx.bf16_from_bits(gu_bits), nx.bf16_from_bits(dn_bits), fmt,
+                            backward=backward, forward=forward)
+    return e, {k: _compact(v) for k, v in ops.items()}
+
+
+class StreamedExperts:
+    """experts[e] for the oracle at the full workload sizes, prepared (S0) by a
+    pool of spawned workers a bounded number of experts ahead, in the order the
+    oracle asks for them (increasing expert index).  Host memory holds the
+    operands of the expert in use plus the pool's read-ahead, not of all
+    experts.  Each pass (forward, then backward) is announced with ``expect``:
+    the experts it will ask for, in order, and which operand pair it needs."""
+
+    def __init__(self, cfg, gu_all, dn_all):
+        import multiprocessing as mp
+        import os
+        self.cfg, self.E = cfg, cfg["E"]
+        self.gu_all, self.dn_all = gu_all, dn_all
+        self.nproc = max(1, os.cpu_count() or 1)
+        self.pool = mp.get_context("spawn").Pool(self.nproc)
+        self.pending, self.queue = {}, []
+        self.shape_gu = tuple(gu_all.shape[1:])
+        self.shape_dn = tuple(dn_all.shape[1:])
+
+    def expect(self, experts, forward, backward):
+        assert not self.pending, "the previous pass did not consume every expert"
+        self.queue = [int(e) for e in sorted(experts)]
+        self.parts = (forward, backward)
+        self._fill()
+
+    def _fill(self):
+        while self.queue and len(self.pending) < self.nproc + 2:
+            e = self.queue.pop(0)
+            job = (e, _bf16_bits(self.gu_all[e]), _bf16_bits(self.dn_all[e]), self.cfg["fmt"], *self.parts)
+            self.pending[e] = self.pool.apply_async(_stream_worker, (job,))
+
+    def __len__(self):
+        return self.E
+
+    def __getitem__(self, e):
+        r = self.pending.pop(int(e))        # KeyError: an expert outside the announced pass
+        _, ops = r.get()
+        self._fill()
+        return (np.broadcast_to(np.float64(0.0), self.shape_gu), np.broadcast_to(np.float64(0.0), self.shape_dn),
+                ops)
+
+    def close(self):
+        self.pool.terminate()
+        self.pool.join()

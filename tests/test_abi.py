@@ -144,6 +144,27 @@ def test_dump_flag_adds_the_dump_buffers_only_with_mxfp8(pkg):
             pkg.moe_buffer_info(fwd_only, 1, "dGU_dump")
 
 
+def test_scale_layout_calls_check_arguments_on_host(pkg):
+    for f in (pkg.moe_prepare_scales, pkg.moe_canonical_scales):
+        assert f(None, 128, 128, 1 << 12, 0) == -1
+        assert f(1 << 12, 0, 128, 1 << 16, 0) == -1
+        assert f(1 << 12, 128, 128, 1 << 12, 0) == -1          # same buffer
+        assert f(1 << 12, 100, 128, 1 << 16, 0) == -2
+        assert f(1 << 12, 128, 160, 1 << 16, 0) == -2
+        assert f((1 << 12) + 4, 128, 128, 1 << 16, 0) == -3
+
+
+def test_prepare_weights_checks_arguments_on_host(pkg):
+    mx = pkg.config(64, 256, 128, 8, 2, 0, "mxfp8")
+    P = 1 << 12
+    assert pkg.moe_prepare_weights(mx, None, P, P, P, P, P, stream=0) == -1
+    assert pkg.moe_prepare_weights(mx, P, P, None, P, P, P, stream=0) == -1          # MXFP8 needs codes + scales
+    assert pkg.moe_prepare_weights(mx, P, P, P, P, P, P, P, P, None, None, stream=0) == -1   # gu_t without dn_t
+    assert pkg.moe_prepare_weights(mx, P + 8, P, P, P, P, P, stream=0) == -3
+    bad = pkg.config(64, 100, 128, 8, 2, 0, "mxfp8")
+    assert pkg.moe_prepare_weights(bad, P, P, P, P, P, P, stream=0) == -2
+
+
 def test_status_strings(pkg):
     L = pkg.lib()
     for c in range(-6, 1):
@@ -239,7 +260,8 @@ def test_product_path_never_reaches_the_oracle():
                     users.add(fn.name)
                 if isinstance(node, ast.Import) and any(a.name.split(".")[0] == "oracle" for a in node.names):
                     users.add(fn.name)
-    assert users <= {"_prep_worker", "oracle_sample", "oracle_prepare", "oracle_step", "run_reference"}, users
+    assert users <= {"_prep_worker", "oracle_sample", "oracle_prepare", "oracle_step", "run_reference",
+                     "cpu_baseline"}, users
     top = [n for n in tree.body if isinstance(n, (ast.Import, ast.ImportFrom))]
     assert not any("oracle" in ast.dump(n) for n in top)
 

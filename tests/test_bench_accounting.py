@@ -55,16 +55,41 @@ def test_kernel_flops_add_up_to_the_layer(name):
 
 def test_kernel_roofline_takes_the_longer_bound():
     cfg = bench.workload("kimi-k2.7")
-    peaks = {"hbm_gbs": 6757.9, "bf16_tflops_sustained": 1661.6}
+    measured = {"hbm_gbs": 6757.9, "bf16_tflops": 1856.7, "bf16_tflops_sustained": 1661.6}
+    peaks = bench.tensor_peaks(measured, "measured", {"burst_tflops": 3771.5, "sustained_tflops": 3400.0,
+                                                      "how": "test"})
     # the gate/up wgrad writes 22.5 GB of bf16 dW: HBM-bound at this shape
     r = bench.kernel_roofline(cfg, "wgrad_gate_up", True, 6.0, peaks)
     assert r["bound"] == "hbm" and r["unit"] == "GB/s"
     byts = bench.kernel_work(cfg, "wgrad_gate_up", True)[1]
     assert r["achieved"] == pytest.approx(byts / 6.0e-3 / 1e9)
-    # the forward gate/up GEMM is tensor-bound, at the MXFP8 rate
+    assert r["frac"] == pytest.approx(r["achieved"] / 6757.9)
+    assert r["frac_nominal"] == pytest.approx(r["achieved"] / bench.NOMINAL["hbm_gbs"])
+    # the forward gate/up GEMM is tensor-bound, at the measured MXFP8 rate
     r = bench.kernel_roofline(cfg, "gemm1_gate_up_swiglu", False, 3.6, peaks)
     assert r["bound"] == "tensor" and r["mx"]
-    assert r["peak"] == pytest.approx(1661.6 * bench.MX_OVER_BF16)
+    assert r["peak"] == pytest.approx(3771.5)
+    assert r["frac_sustained"] == pytest.approx(r["achieved"] / 3400.0)
+    assert r["frac_nominal"] == pytest.approx(r["achieved"] / 4500.0)
+    # a BF16 GEMM (shared expert) against the burst BF16 rate
+    r = bench.kernel_roofline(cfg, "shared_gemm2_down", False, 0.25, peaks)
+    assert r["bound"] == "tensor" and not r["mx"] and r["peak"] == pytest.approx(1856.7)
+    # without the MXFP8 probe the ratio of the measured BF16 rates stands in, labelled so
+    fb = bench.tensor_peaks(measured, "measured", {"burst_tflops": None})
+    assert fb["mx"] == pytest.approx(2 * 1856.7) and "unavailable" in fb["mx_src"]
+
+
+def test_layer_roofline_fractions():
+    cfg = bench.workload("deepseek-v4-pro")
+    peaks = bench.tensor_peaks({"hbm_gbs": 6757.9, "bf16_tflops": 1856.7, "bf16_tflops_sustained": 1661.6},
+                               "measured", {"burst_tflops": 3771.5, "sustained_tflops": 3400.0, "how": "test"})
+    fl_exp, fl_sh, byt = bench.layer_work(cfg, "fwd")
+    t_roof = max(fl_exp / 3771.5e12, byt / 6757.9e9)
+    lr = bench.layer_roofline(cfg, "fwd", 12.0, peaks)
+    assert lr["bound"] == "tensor"
+    assert lr["frac"] == pytest.approx(t_roof / 12.0e-3, abs=1e-4)
+    assert lr["frac_nominal"] == pytest.approx(max(fl_exp / 4500e12, byt / 7900e9) / 12.0e-3, abs=1e-4)
+    cfg = bench.workload("kimi-k2.7")
     assert bench.kernel_roofline(cfg, "no_such_kernel", True, 1.0, peaks) is None
 
 

@@ -51,7 +51,7 @@ def test_quantize_mx_bit_exact(pkg, transpose):
     c_ref, s_ref = om.quantize_weights(ref, transpose=bool(transpose))
     B, rows, cols = c_ref.shape
     assert np.array_equal(codes.reshape(B * rows, cols), c_ref.reshape(B * rows, cols))
-    assert np.array_equal(unpack_tiled_scales(sf, B * rows, cols), s_ref.reshape(B * rows, cols // 32))
+    assert np.array_equal(sf.reshape(B * rows, cols // 32), s_ref.reshape(B * rows, cols // 32))   # canonical
 
 
 @pytest.mark.parametrize("shape", [(2, 256, 384), (3, 384, 128)])
@@ -72,7 +72,7 @@ def test_quantize_mx_both_orientations_bit_exact(pkg, shape):
         c_ref, s_ref = om.quantize_weights(ref, transpose=bool(transpose))
         Bq, r, c = c_ref.shape
         assert np.array_equal(out[transpose].cpu().numpy().reshape(Bq * r, c), c_ref.reshape(Bq * r, c))
-        assert np.array_equal(unpack_tiled_scales(osf[transpose].cpu().numpy(), Bq * r, c),
+        assert np.array_equal(osf[transpose].cpu().numpy().reshape(Bq * r, c // 32),
                               s_ref.reshape(Bq * r, c // 32))
 
 
@@ -88,7 +88,58 @@ def test_quantize_mx_exhaustive_bf16_patterns(pkg):
     codes, sf = _quant(pkg, w.cuda(), 0)
     c_ref, s_ref = nx.mx_quantize(mi.to_f64(w)[0], axis=1)
     assert np.array_equal(codes.reshape(c_ref.shape), c_ref)
-    assert np.array_equal(unpack_tiled_scales(sf, c_ref.shape[0], 128), s_ref)
+    assert np.array_equal(sf.reshape(s_ref.shape), s_ref)
+
+
+@pytest.mark.parametrize("rows,K", [(128, 128), (384, 512), (1024, 7168)])
+def test_prepare_and_canonical_scales_bit_exact(pkg, rows, K):
+    """moe_prepare_scales is the permutation the prepared layout defines (index
+    arithmetic written out in the tests' helper) and moe_canonical_scales its
+    inverse; a same-pointer call and shapes off the 128 grid are refused."""
+    rng = np.random.default_rng(rows + K)
+    canon = rng.integers(0, 256, (rows, K // 32), dtype=np.uint8)
+    src = torch.from_numpy(canon).cuda()
+    prep = torch.empty(rows * K // 32, dtype=torch.uint8, device="cuda")
+    back = torch.empty_like(src)
+    pkg.check(pkg.moe_prepare_scales(src, rows, K, prep))
+    pkg.check(pkg.moe_canonical_scales(prep, rows, K, back))
+    torch.cuda.synchronize()
+    p = prep.cpu().numpy()
+    assert np.array_equal(unpack_tiled_scales(p, rows, K), canon)
+    assert np.array_equal(back.cpu().numpy(), canon)
+    assert sorted(p.tolist()) == sorted(canon.reshape(-1).tolist())
+    assert pkg.moe_prepare_scales(src, rows, K, src) == -1
+    assert pkg.moe_prepare_scales(src, rows + 32, K, prep) == -2
+    assert pkg.moe_canonical_scales(prep, rows, K + 32, back) == -2
+
+
+@pytest.mark.parametrize("backward", [False, True])
+def test_prepare_weights_equals_quantise_then_prepare(pkg, backward):
+    """moe_prepare_weights (the layer's S0, one read per master, prepared scales
+    written directly) gives the bytes of moe_quantize_weights followed by
+    moe_prepare_scales, in both orientations."""
+    E, d, m = 3, 512, 256
+    c = pkg.config(64, d, m, E, 2, 0, "mxfp8", pkg.MOE_FLAG_BACKWARD if backward else 0)
+    rng = np.random.default_rng(9)
+    gu = torch.from_numpy(edge_values(rng, (E, 2 * m, d))).to(torch.bfloat16).cuda()
+    dn = torch.from_numpy(edge_values(rng, (E, d, m))).to(torch.bfloat16).cuda()
+    u8 = lambda n: torch.empty(n, dtype=torch.uint8, device="cuda")
+    n_gu, n_dn = E * 2 * m * d, E * d * m
+    out = dict(gu=u8(n_gu), gu_scale=u8(n_gu // 32), dn=u8(n_dn), dn_scale=u8(n_dn // 32))
+    if backward:
+        out.update(gu_t=u8(n_gu), gu_t_scale=u8(n_gu // 32), dn_t=u8(n_dn), dn_t_scale=u8(n_dn // 32))
+    pkg.check(pkg.moe_prepare_weights(c, gu, dn, **out))
+    for key, w, rows, cols in (("gu", gu, 2 * m, d), ("dn", dn, d, m)):
+        for t in ((0, 1) if backward else (0,)):
+            name = key + ("_t" if t else "")
+            codes, sc, prep = u8(E * rows * cols), u8(E * rows * cols // 32), u8(E * rows * cols // 32)
+            pkg.check(pkg.moe_quantize_weights(c, w, rows, cols, t, codes, sc))
+            pkg.check(pkg.moe_prepare_scales(sc, E * (cols if t else rows), rows if t else cols, prep))
+            assert torch.equal(out[name], codes), name
+            assert torch.equal(out[name + "_scale"], prep), name + "_scale"
+    # one backward operand alone is refused
+    assert pkg.moe_prepare_weights(c, gu, dn, out["gu"], out["gu_scale"], out["dn"], out["dn_scale"],
+                                   out["gu"], out["gu_scale"], None, None) == -1
 
 
 def _route(pkg, logits, k):
@@ -159,6 +210,6 @@ def test_quantize_weights_layer_entry_bit_exact(pkg, blocks_along_rows):
     c_ref, s_ref = om.quantize_weights(mi.to_f64(w), transpose=bool(blocks_along_rows))
     B, r2, c2 = c_ref.shape
     assert np.array_equal(codes.cpu().numpy().reshape(B * r2, c2), c_ref.reshape(B * r2, c2))
-    assert np.array_equal(unpack_tiled_scales(sf.cpu().numpy(), B * r2, c2), s_ref.reshape(B * r2, c2 // 32))
+    assert np.array_equal(sf.cpu().numpy().reshape(B * r2, c2 // 32), s_ref.reshape(B * r2, c2 // 32))
     cb = pkg.config(64, cols, rows // 2, E, 2, 0, "bf16", 0)
     assert pkg.moe_quantize_weights(cb, wg, rows, cols, blocks_along_rows, codes, sf) == -1  # MOE_ERR_ARG
