@@ -86,7 +86,8 @@ typedef enum {
  * values the SwiGLU-backward epilogue quantises in "dGU_dump" [padded rows,
  * 2m] bf16 (moe_buffer_info gives their offsets).  Quantising those dumps
  * with the format's definition must reproduce the codes and scales the
- * kernels wrote, byte for byte.  Nothing else changes. */
+ * kernels wrote, byte for byte.  Nothing else changes.  Not available with a
+ * dispatch ring (ring_rows > 0: MOE_ERR_ARG). */
 #define MOE_FLAG_DEBUG_DUMP 4
 
 /*

@@ -52,6 +52,7 @@ int check_config(const moe_config *c, Dims *D) {
   if (c->ring_rows > 0 && c->dtype != MOE_MXFP8) return MOE_ERR_ARG;
   if (c->ring_rows % 128) return MOE_ERR_SHAPE;
   if (c->ring_rows > 0 && c->d > 8192) return MOE_ERR_SHAPE;  // the ring's gather copies whole rows
+  if (c->ring_rows > 0 && (c->flags & MOE_FLAG_DEBUG_DUMP)) return MOE_ERR_ARG;  // no dump in the ring launch
   if (!(c->aux_alpha >= 0.0f) || !(c->aux_alpha < 1e30f)) return MOE_ERR_ARG;  // finite, non-negative
   const long R = static_cast<long>(c->T) * c->k;
   const long Rp = (R + 127L * c->E + 127) / 128 * 128;

@@ -280,7 +280,7 @@ __host__ __device__ constexpr int epi_warps() {
   return 8;
 }
 
-template <bool MX, int BN, int EPI, bool RING = false>
+template <bool MX, int BN, int EPI, bool RING = false, bool DUMP = false>
 __global__ void __launch_bounds__(64 + 32 * epi_warps<EPI, BN>(), 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const GemmArgs g) {
@@ -487,8 +487,8 @@ __global__ void __launch_bounds__(64 + 32 * epi_warps<EPI, BN>(), 1)
         tc_fence_before();
         mbar_arrive(&tempty[acc]);
       };
-      epilogue_tile_split<EPI, BN>(g, vO, vO2, vQ, st, tb, ti.nk, row0, grow, ti.out_col, lane, part, true,
-                                   release);
+      epilogue_tile_split<EPI, BN, DUMP>(g, vO, vO2, vQ, st, tb, ti.nk, row0, grow, ti.out_col, lane, part,
+                                         true, release);
       if (++acc == C::NUM_ACC) {
         acc = 0;
         aph ^= 1u;
@@ -503,19 +503,19 @@ __global__ void __launch_bounds__(64 + 32 * epi_warps<EPI, BN>(), 1)
   }
 }
 
-template <bool MX, int BN, int EPI>
+template <bool MX, int BN, int EPI, bool DUMP = false>
 cudaError_t launch_one(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs &g, int grid,
                        cudaStream_t s) {
   using C = Cfg<MX, BN>;
   static bool attr_set = false;  // per instantiation; idempotent, benign if repeated
   if (!attr_set) {
-    const cudaError_t e = cudaFuncSetAttribute(gemm_kernel<MX, BN, EPI>,
+    const cudaError_t e = cudaFuncSetAttribute(gemm_kernel<MX, BN, EPI, false, DUMP>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                static_cast<int>(C::SMEM));
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  gemm_kernel<MX, BN, EPI><<<grid, 64 + 32 * epi_warps<EPI, BN>(), C::SMEM, s>>>(ta, tb, g);
+  gemm_kernel<MX, BN, EPI, false, DUMP><<<grid, 64 + 32 * epi_warps<EPI, BN>(), C::SMEM, s>>>(ta, tb, g);
   return cudaGetLastError();
 }
 
@@ -566,6 +566,10 @@ cudaError_t launch_gemm_ring(const CUtensorMap &ta, const CUtensorMap &tb, const
 cudaError_t launch_gemm(bool mx, int bn, int epi, const CUtensorMap &ta, const CUtensorMap &tb,
                         const GemmArgs &g, int grid, cudaStream_t s) {
   if (grid <= 0) return cudaSuccess;
+  if (g.dump) {  // test hook: the MXFP8 gate/up GEMM that also stores its fp32 h
+    if (mx && bn == 256 && epi == EPI_SWIGLU) return launch_one<true, 256, EPI_SWIGLU, true>(ta, tb, g, grid, s);
+    return cudaErrorInvalidValue;
+  }
 #define MOE_GEMM_CASE(MXV, BNV, EPIV) \
   if (mx == MXV && bn == BNV && epi == EPIV)  \
     return launch_one<MXV, BNV, EPIV>(ta, tb, g, grid, s);

@@ -296,7 +296,9 @@ MOE_DEV void epilogue_tile(const GemmArgs &g, const OutView &vO, const OutView &
 // drains half of the tile's columns.  For the store and SwiGLU epilogues the
 // accumulator is read in one round (two warps in parallel) and released before
 // any conversion or store; the SwiGLU backward reads its columns 64 at a time.
-template <int EPI, int BN, typename Release>
+// DUMP (SwiGLU, a separate instantiation so the normal kernel carries none of
+// its register pressure): also store the fp32 h to g.dump.
+template <int EPI, int BN, bool DUMP = false, typename Release>
 MOE_DEV void epilogue_tile_split(const GemmArgs &g, const OutView &vO, const OutView &vO2,
                                  const OutView &vQ, Stager &st, uint32_t tb, int nk, int row0,
                                  long grow, int out_col, int lane, int part, bool store,
@@ -351,7 +353,7 @@ MOE_DEV void epilogue_tile_split(const GemmArgs &g, const OutView &vO, const Out
       for (int c = 0; c < NC / 16; ++c) st.put(vO, raw + 16 * c, out_col + c0 + 16 * c, row0, lane);
     } else {
       const bool in = grow < g.out_rows;
-#pragma unroll 1
+#pragma unroll
       for (int c = 0; c < NC / 32; ++c) {
         float v[32];
         if (in) {
@@ -442,10 +444,12 @@ MOE_DEV void epilogue_tile_split(const GemmArgs &g, const OutView &vO, const Out
     }
 #pragma unroll
     for (int i = 0; i < 64; ++i) G[i] = silu(G[i]) * U[i];  // h, in place
-    if (g.dump) {  // test hook: the fp32 h the quantisers below read
-      const OutView vD = out_view(g.dump, g.ld_dump, g.out_rows, 4);
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) st.put(vD, gr + 16 * c, col + 16 * c, row0, lane);
+    if constexpr (DUMP) {  // test hook: the fp32 h the quantisers below read
+      if (grow < g.out_rows) {
+        float4 *dst = reinterpret_cast<float4 *>(g.dump + grow * g.ld_dump + col);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) dst[i] = make_float4(G[4 * i], G[4 * i + 1], G[4 * i + 2], G[4 * i + 3]);
+      }
     }
     if (g.out) {
       st.put_bf16(vO, G, col, row0, lane);

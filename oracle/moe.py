@@ -54,8 +54,9 @@ notes of the repository):
 import numpy as np
 
 from .numerics import bf16_round, mx_roundtrip, MX_BLOCK
+from .nvfp4 import global_scale, nvfp4_roundtrip
 
-FORMATS = ("bf16", "mxfp8", "fp64")
+FORMATS = ("bf16", "mxfp8", "nvfp4", "fp64")
 
 
 def _rnd(fmt):
@@ -123,13 +124,22 @@ def prepare_expert(W_gu, W_dn, fmt, backward=True, forward=True):
     claims, MXFP8 bullet): the forward operands are W_gu [2m, d] and W_dn
     [d, m] quantised along their K (d, m); the backward dgrad operands are
     W_dn^T [m, d] quantised along d and W_gu^T [d, 2m] quantised along 2m.
-    Values are returned dequantised (float64).  Other formats use the masters.
-    ``forward`` / ``backward`` select which of the two pairs are made.
+    NVFP4 (forward only; the NVFP4 variant of the expert GEMMs): each
+    expert matrix is one tensor with its own second-level scale, quantised in
+    blocks of 16 along K.  Values are returned dequantised (float64).  Other
+    formats use the masters.  ``forward`` / ``backward`` select which of the
+    two pairs are made.
     """
     W_gu = np.asarray(W_gu, dtype=np.float64)
     W_dn = np.asarray(W_dn, dtype=np.float64)
     ops = {}
-    if fmt == "mxfp8":
+    if fmt == "nvfp4":
+        if backward:
+            raise NotImplementedError("the NVFP4 variant is forward only")
+        if forward:
+            ops["gu_fwd"] = nvfp4_roundtrip(W_gu, global_scale(np.abs(W_gu).max()), axis=1)
+            ops["dn_fwd"] = nvfp4_roundtrip(W_dn, global_scale(np.abs(W_dn).max()), axis=1)
+    elif fmt == "mxfp8":
         if forward:
             ops["gu_fwd"] = mx_roundtrip(W_gu, axis=1)
             ops["dn_fwd"] = mx_roundtrip(W_dn, axis=1)
@@ -160,27 +170,37 @@ def _col_blocks(a):
     return mx_roundtrip(ap, axis=0)[:n]
 
 
-def expert_forward(X, W_gu, W_dn, fmt, ops=None):
+def expert_forward(X, W_gu, W_dn, fmt, ops=None, x_scale=None):
     """SwiGLU FFN of one expert on its gathered rows.
 
     X [n, d] bf16 values; W_gu [2m, d] (gate rows first); W_dn [d, m].
     MXFP8: X, W_gu and W_dn are quantised along K (d, d, m); h is
-    quantised along m straight from the float64 SwiGLU output.  ``ops`` are
-    the expert's prepared operands (:func:`prepare_expert`), computed here
-    when not given.
+    quantised along m straight from the float64 SwiGLU output.
+    NVFP4: the same axes in blocks of 16; X with the second-level scale
+    ``x_scale`` of the layer's whole x (from X itself when not given), h
+    rounded to fp32 and quantised with second-level scale 1.
+    ``ops`` are the expert's prepared operands (:func:`prepare_expert`),
+    computed here when not given.
     Returns dict(G, U (unrounded), GU_saved [n, 2m], h_saved [n, m], o [n, d]).
     """
     m = W_gu.shape[0] // 2
     rnd = _rnd(fmt)
     if ops is None:
         ops = prepare_expert(W_gu, W_dn, fmt, backward=False)
-    Xq = mx_roundtrip(X, axis=1) if fmt == "mxfp8" else X
+    if fmt == "mxfp8":
+        Xq = mx_roundtrip(X, axis=1)
+    elif fmt == "nvfp4":
+        Xq = nvfp4_roundtrip(X, global_scale(np.abs(X).max()) if x_scale is None else x_scale, axis=1)
+    else:
+        Xq = X
     Wq, Dq = ops["gu_fwd"], ops["dn_fwd"]
     G = Xq @ Wq[:m].T
     U = Xq @ Wq[m:].T
     h = silu(G) * U
     if fmt == "mxfp8":
         h_op = mx_roundtrip(h, axis=1)
+    elif fmt == "nvfp4":
+        h_op = nvfp4_roundtrip(h.astype(np.float32).astype(np.float64), 1.0, axis=1)
     else:
         h_op = rnd(h)
     o = rnd(h_op @ Dq.T)
@@ -196,16 +216,20 @@ def shared_forward(x, Ws_gu, Ws_dn, fmt):
 # ----------------------------------------------------------------------------
 # full forward
 # ----------------------------------------------------------------------------
-def forward(x, logits, experts, k, fmt, shared=None):
+def forward(x, logits, experts, k, fmt, shared=None, x_scale=None):
     """Layer forward.
 
     x [T, d] (bf16 values as float64); logits [T, E] fp32; ``experts[e]``
     returns (W_gu [2m, d], W_dn [d, m]) float64 and ``len(experts)`` is E;
     ``shared`` is None or (Ws_gu [2m_s, d], Ws_dn [d, m_s]).
+    NVFP4: ``x_scale`` is the second-level scale of x (computed from x when
+    not given; a caller passing a subset of the tokens passes the whole x's).
     Returns (y [T, d], saved dict).
     """
     assert fmt in FORMATS
     x = np.asarray(x, dtype=np.float64)
+    if fmt == "nvfp4" and x_scale is None:
+        x_scale = global_scale(np.abs(x).max())
     T, d = x.shape
     E = len(experts)
     R = T * k
@@ -221,7 +245,7 @@ def forward(x, logits, experts, k, fmt, shared=None):
         if r1 == r0:
             continue
         W_gu, W_dn, ops = _unpack(experts[e])
-        res = expert_forward(x[row_tok[r0:r1]], W_gu, W_dn, fmt, ops)
+        res = expert_forward(x[row_tok[r0:r1]], W_gu, W_dn, fmt, ops, x_scale=x_scale)
         if GU is None:
             m = W_gu.shape[0] // 2
             GU = np.zeros((R, 2 * m))

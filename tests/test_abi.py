@@ -89,6 +89,7 @@ def test_saved_wgrad_operands_by_format(pkg):
     (dict(ring_rows=256), -1),                          # the ring is MXFP8-only
     (dict(dtype=1, ring_rows=200), -2), (dict(dtype=1, ring_rows=-128), -1),
     (dict(dtype=1, ring_rows=256, gather_sms=65), -1), (dict(dtype=1, d=8448, ring_rows=256), -2),
+    (dict(dtype=1, ring_rows=256, flags=4), -1),          # no pre-quantisation dump through the ring
 ])
 def test_invalid_configs_rejected_on_host(pkg, bad, code):
     args = dict(T=64, d=256, m=128, E=8, k=2, m_shared=0, dtype=0, flags=0, ring_rows=0, gather_sms=0)
