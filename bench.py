@@ -33,8 +33,9 @@ if ROOT not in sys.path:
 METRIC = "MoE-layer tokens/s fwd & fwd+bwd on 1 GB300; % of GEMM/HBM roofline"
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 MX_OVER_BF16 = 2.0   # nominal dense MXFP8 : BF16 tensor-core ratio (4.5 : 2.25 PFLOP/s)
+NV_OVER_MX = 3.0     # nominal dense NVFP4 : MXFP8 ratio (13.5 : 4.5 PFLOP/s)
 # GB300's published dense peaks (context column of every fraction)
-NOMINAL = {"hbm_gbs": 7900.0, "bf16_tflops": 2250.0, "mx_tflops": 4500.0}
+NOMINAL = {"hbm_gbs": 7900.0, "bf16_tflops": 2250.0, "mx_tflops": 4500.0, "nv_tflops": 13500.0}
 
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from an
 # ncu capture, keyed by (workload, kernel).  An entry is removed whenever the
@@ -68,7 +69,7 @@ def layer_work(cfg, passes):
     mult = 3 if passes == "fwdbwd" else 1
     fl_exp = 6.0 * d * m * R * mult
     fl_sh = 6.0 * d * ms * T * mult
-    wb = 1 + 1 / 32 if mx else 2                     # stored bytes per weight element
+    wb = elem_bytes(cfg)                             # stored bytes per weight element
     wts = E * 3 * d * m * wb
     byt = wts + T * d * 2 + T * E * 4 + T * d * 2 + (3 * d * ms * 2 if ms else 0)
     if passes == "fwdbwd":
@@ -77,6 +78,12 @@ def layer_work(cfg, passes):
         byt += E * 3 * d * m * 2 + 3 * d * ms * 2    # weight gradients (bf16)
         byt += 3 * d * ms * 2                        # shared weights re-read
     return fl_exp, fl_sh, byt
+
+
+def elem_bytes(cfg):
+    """Stored bytes per expert-operand element: MXFP8 1 + 1/32 (E8M0 per 32),
+    NVFP4 1/2 + 1/16 (E4M3 per 16), BF16 2."""
+    return {"mxfp8": 1 + 1 / 32, "nvfp4": 0.5 + 1 / 16}.get(cfg["fmt"], 2)
 
 
 def kernel_work(cfg, name, train=False):
@@ -93,8 +100,8 @@ def kernel_work(cfg, name, train=False):
     row- and column-blocked codes (with BF16, h in bf16)."""
     T, d, m, E, k, ms = (cfg[n] for n in ("T", "d", "m", "E", "k", "m_shared"))
     R = T * k
-    mx = cfg["fmt"] == "mxfp8"
-    a = (1 + 1 / 32) if mx else 2          # bytes per stored expert operand element
+    mx = cfg["fmt"] in ("mxfp8", "nvfp4")  # block-scaled expert operands
+    a = elem_bytes(cfg)                    # bytes per stored expert operand element
     h_out = (R * 2 * m * 2 + (2 * R * m * a if mx else R * m * 2)) if train else R * m * a
     sh_out = (T * 2 * ms * 2 + T * ms * 2) if train else T * ms * 2
     tbl = {
@@ -244,7 +251,20 @@ def tensor_peaks(peaks, peaks_src, mxp):
     else:
         P.update(mx=MX_OVER_BF16 * P["bf16"], mx_s=MX_OVER_BF16 * P["bf16_s"],
                  mx_src="%.0f x %s BF16 (MXFP8 probe unavailable)" % (MX_OVER_BF16, peaks_src))
+    # no NVFP4 GEMM rate is measured here: the nominal dense ratio to MXFP8
+    P.update(nv=NV_OVER_MX * P["mx"], nv_s=NV_OVER_MX * P["mx_s"],
+             nv_src="%.0f x the MXFP8 rate above (nominal dense NVFP4 : MXFP8, 13.5 : 4.5; no NVFP4 GEMM measured)"
+                    % NV_OVER_MX)
     return P
+
+
+def _tensor_peak(cfg, mx, P, kind=""):
+    """(peak, sustained peak, nominal peak) of a kernel's arithmetic."""
+    if not mx:
+        return P["bf16"], P["bf16_s"], NOMINAL["bf16_tflops"]
+    if cfg["fmt"] == "nvfp4":
+        return P["nv"], P["nv_s"], NOMINAL["nv_tflops"]
+    return P["mx"], P["mx_s"], NOMINAL["mx_tflops"]
 
 
 def kernel_roofline(cfg, name, train, ms_per_step, P):
@@ -257,15 +277,14 @@ def kernel_roofline(cfg, name, train, ms_per_step, P):
     if w is None or ms_per_step <= 0:
         return None
     flops, byts, mx = w
-    tpeak = P["mx"] if mx else P["bf16"]
+    tpeak, tpeak_s, tpeak_n = _tensor_peak(cfg, mx, P)
     t_tensor = flops / (tpeak * 1e12)
     t_hbm = byts / (P["hbm"] * 1e9)
     sec = ms_per_step / 1e3
     if t_tensor >= t_hbm:
         ach = flops / sec / 1e12
         return {"bound": "tensor", "achieved": ach, "peak": tpeak, "unit": "TFLOP/s", "mx": mx,
-                "frac": ach / tpeak, "frac_sustained": ach / (P["mx_s"] if mx else P["bf16_s"]),
-                "frac_nominal": ach / (NOMINAL["mx_tflops"] if mx else NOMINAL["bf16_tflops"]),
+                "frac": ach / tpeak, "frac_sustained": ach / tpeak_s, "frac_nominal": ach / tpeak_n,
                 "t_tensor_ms": t_tensor * 1e3, "t_hbm_ms": t_hbm * 1e3}
     ach = byts / sec / 1e9
     return {"bound": "hbm", "achieved": ach, "peak": P["hbm"], "unit": "GB/s", "mx": mx,
@@ -278,23 +297,25 @@ def layer_roofline(cfg, passes, ms_step, P):
     `frac` at the measured burst rates, beside it at the sustained rates and at
     GB300's published dense peaks."""
     fl_exp, fl_sh, byt = layer_work(cfg, passes)
-    mx = cfg["fmt"] == "mxfp8"
+    pk, pk_s, pk_n = _tensor_peak(cfg, cfg["fmt"] != "bf16", P)
 
-    def roof(t_mx, t_bf, hbm):
-        t_t = fl_exp / (t_mx if mx else t_bf) / 1e12 + fl_sh / t_bf / 1e12
+    def roof(t_exp, t_bf, hbm):
+        t_t = fl_exp / t_exp / 1e12 + fl_sh / t_bf / 1e12
         t_h = byt / hbm / 1e9
         return max(t_t, t_h), t_t, t_h
 
-    t_roof, t_tensor, t_hbm = roof(P["mx"], P["bf16"], P["hbm"])
-    t_s = roof(P["mx_s"], P["bf16_s"], P["hbm"])[0]
-    t_n = roof(NOMINAL["mx_tflops"], NOMINAL["bf16_tflops"], NOMINAL["hbm_gbs"])[0]
+    t_roof, t_tensor, t_hbm = roof(pk, P["bf16"], P["hbm"])
+    t_s = roof(pk_s, P["bf16_s"], P["hbm"])[0]
+    t_n = roof(pk_n, NOMINAL["bf16_tflops"], NOMINAL["hbm_gbs"])[0]
     sec = ms_step / 1e3
     return {"tokens_per_s": round(cfg["T"] / t_roof, 1), "frac": round(t_roof / sec, 4),
             "frac_sustained": round(t_s / sec, 4), "frac_nominal": round(t_n / sec, 4),
             "bound": "tensor" if t_tensor >= t_hbm else "hbm", "t_tensor_ms": round(t_tensor * 1e3, 3),
             "t_hbm_ms": round(t_hbm * 1e3, 3),
-            "peaks": "HBM %.1f GB/s, BF16 %.1f TFLOP/s (%s, burst), MXFP8 %.1f TFLOP/s (%s)"
-                     % (P["hbm"], P["bf16"], P["src"], P["mx"], P["mx_src"])}
+            "peaks": "HBM %.1f GB/s, BF16 %.1f TFLOP/s (%s, burst), %s"
+                     % (P["hbm"], P["bf16"], P["src"],
+                        ("NVFP4 %.1f TFLOP/s (%s)" % (P["nv"], P["nv_src"])) if cfg["fmt"] == "nvfp4"
+                        else "MXFP8 %.1f TFLOP/s (%s)" % (P["mx"], P["mx_src"]))}
 
 
 class Clocks:
@@ -495,7 +516,7 @@ def time_s0(layer, gu_all, dn_all, stream):
     t = layer.tensors
 
     def run():
-        if layer.mx:
+        if layer.mx or layer.nv:
             layer.prepare_stacked(gu_all, dn_all, stream=stream)
         elif layer.backward_enabled:
             pkg.check(pkg.moe_transpose_bf16(gu_all, E, 2 * m, d, t["gu_t"], stream))
@@ -519,7 +540,7 @@ def workload_desc(cfg, bwd, layer=None):
             "dispatch": ("ring of %d rows, %d gather SMs" % (ring, layer.cfg.gather_sms or 8)
                          if ring else "materialised"),
             "l2": "inputs larger than L2 (%.1f GB of expert weights read per step)"
-                  % (3 * cfg["E"] * cfg["d"] * cfg["m"] * (1.03 if mx else 2) / 1e9)}
+                  % (3 * cfg["E"] * cfg["d"] * cfg["m"] * elem_bytes(cfg) / 1e9)}
 
 
 def summarize(cfg, train, recs, steps, total_ms, P, write_gbs):
@@ -541,7 +562,8 @@ def summarize(cfg, train, recs, steps, total_ms, P, write_gbs):
                 "traffic": None}
     else:
         if kr["bound"] == "tensor":
-            note = P["mx_src"] if kr["mx"] else "%s BF16 GEMM, burst" % P["src"]
+            note = ((P["nv_src"] if cfg["fmt"] == "nvfp4" else P["mx_src"]) if kr["mx"]
+                    else "%s BF16 GEMM, burst" % P["src"])
         else:
             note = "%s HBM copy bandwidth" % P["src"]
         ob = output_bytes(cfg, dom)
@@ -837,7 +859,7 @@ def run_ours(args, cfg, passes):
     out = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "mxfp8" if mx else "bf16",
+        "scaling": "weak", "vs_baseline": None, "dtype": cfg["fmt"],
         "data": "synthetic (seeded N(0,1) tokens, N(0,1/d)/N(0,1/m) bf16 weights, fp32 logits)",
         "config": workload_desc(cfg, bwd, layer),
         "fwd_tokens_per_s": round(fwd_value, 1),
@@ -948,6 +970,8 @@ def main():
     ap.add_argument("--ring", type=int, default=0,
                     help="MXFP8: dispatch through a ring of this many rows (0 = materialised dispatch)")
     ap.add_argument("--gather-sms", type=int, default=0, help="gather SMs of the ring launch (0 = default)")
+    ap.add_argument("--experts", choices=["bf16", "mxfp8", "nvfp4"], default=None,
+                    help="the routed experts' format (default: the workload's own); nvfp4 is forward only")
     ap.add_argument("--override", default="",
                     help="comma-separated shape overrides, e.g. T=2048,E=16 (smaller cases for profiling)")
     args = ap.parse_args()
@@ -957,6 +981,10 @@ def main():
     for kv in filter(None, args.override.split(",")):
         key, val = kv.split("=")
         cfg[key] = int(val)
+    if args.experts:
+        cfg["fmt"] = args.experts
+        if args.experts == "nvfp4":
+            cfg["backward"] = False
     passes = args.passes or ("fwdbwd" if cfg["backward"] else "fwd")
 
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -59,7 +59,7 @@ extern "C" {
 
 typedef struct CUstream_st *moe_stream_t; /* same type as cudaStream_t */
 
-typedef enum { MOE_BF16 = 0, MOE_MXFP8 = 1 } moe_dtype;
+typedef enum { MOE_BF16 = 0, MOE_MXFP8 = 1, MOE_NVFP4 = 2 } moe_dtype;
 
 typedef enum {
   MOE_OK = 0,
@@ -94,7 +94,14 @@ typedef enum {
  * Layer shape.  T tokens, hidden d, expert intermediate m, E experts, top-k k.
  * Supported: 1 <= k <= min(E, 16), E <= 1024, d % 256 == 0, m % 128 == 0,
  * m_shared % 128 == 0 (0 = no shared expert), T*k < 2^31 - 127*E.  dtype is
- * the routed experts' arithmetic; the shared expert is always BF16.  flags:
+ * the routed experts' arithmetic; the shared expert is always BF16.
+ * MOE_NVFP4 (the NVFP4 variant of the expert GEMMs; the pages say the method
+ * has none -- "Mixture-of-Kittens" wiki page, Key claims, MXFP8 bullet -- so
+ * the format is NVIDIA's published NVFP4): packed E2M1 codes with an E4M3
+ * scale per 16 along K and an fp32 second-level scale per tensor (2688 /
+ * amax): x's over all T tokens, each expert matrix's own, and 1 for h.
+ * Forward only (inference: MOE_FLAG_BACKWARD, a ring or a `saved` buffer give
+ * MOE_ERR_ARG) and m % 256 == 0.  flags:
  * any of MOE_FLAG_BACKWARD, MOE_FLAG_DEBUG_STARVE and MOE_FLAG_DEBUG_DUMP, or 0
  * (moe_backward needs a workspace sized with MOE_FLAG_BACKWARD).
  *
@@ -154,6 +161,10 @@ typedef struct {
  *          [E*m, d] + prepared dn_t_scale (moe_quantize_weights(
  *          blocks_along_rows = 1) of the masters, then moe_prepare_scales;
  *          moe_quantize_mx_both writes both orientations at once).
+ * NVFP4 path: `gu` = packed E2M1 codes [E*2m, d/2] (element 2i in the low
+ * nibble of byte i) with prepared E4M3 scales `gu_scale` (rows E*2m, 16-blocks
+ * along d), `dn` = [E*d, m/2] with `dn_scale`, and the experts' second-level
+ * scales gu_gscale [E], dn_gscale [E] fp32 -- all from moe_prepare_weights.
  * Shared expert (BF16 always; NULL when m_shared == 0): s_gu [2m_s, d],
  * s_dn [d, m_s]; for backward also s_gu_t [d, 2m_s], s_dn_t [m_s, d].
  */
@@ -164,6 +175,7 @@ typedef struct {
   const void *dn_t, *dn_t_scale;
   const void *s_gu, *s_dn;
   const void *s_gu_t, *s_dn_t;
+  const float *gu_gscale, *dn_gscale; /* NVFP4 only: second-level scales [E] */
 } moe_weights;
 
 /* Bytes of scratch (`ws`) that moe_route / moe_forward / moe_backward need
@@ -242,12 +254,16 @@ int moe_quantize_mx_both(const void *src, int batch, int rows, int cols, void *c
  *     those name other buffers; NULL = use the masters); with gu_t and dn_t
  *     given, the per-expert transposes of the masters (the *_scale pointers are
  *     unused).
+ *   NVFP4: gu / dn = packed codes [E*2m, d/2] / [E*d, m/2] with prepared
+ *     scales and the experts' second-level scales gu_gscale / dn_gscale [E]
+ *     fp32 (2688 / the expert matrix's amax); no backward operands.
  * gu_t and dn_t are both NULL (forward only) or both given (MOE_ERR_ARG
- * otherwise).  Re-run after every update of the masters.  Asynchronous on
- * `stream`. */
+ * otherwise).  gu_gscale / dn_gscale are required with NVFP4 (4-byte
+ * aligned suffices: they hold one fp32 per expert) and ignored otherwise.
+ * Re-run after every update of the masters.  Asynchronous on `stream`. */
 int moe_prepare_weights(const moe_config *cfg, const void *w_gu, const void *w_dn, void *gu, void *gu_scale,
                         void *dn, void *dn_scale, void *gu_t, void *gu_t_scale, void *dn_t, void *dn_t_scale,
-                        moe_stream_t stream);
+                        float *gu_gscale, float *dn_gscale, moe_stream_t stream);
 
 /* MXFP8 scales from the canonical order to the prepared operand layout that
  * moe_weights' *_scale fields take (a permutation of bytes, part of S0):

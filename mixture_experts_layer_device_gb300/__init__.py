@@ -14,7 +14,8 @@ from . import build as _build
 
 LIB_PATH = _build.LIB
 
-MOE_BF16, MOE_MXFP8 = 0, 1
+MOE_BF16, MOE_MXFP8, MOE_NVFP4 = 0, 1, 2
+DTYPES = {"bf16": MOE_BF16, "mxfp8": MOE_MXFP8, "nvfp4": MOE_NVFP4}
 MOE_FLAG_BACKWARD = 1
 MOE_FLAG_DEBUG_STARVE = 2
 MOE_FLAG_DEBUG_DUMP = 4
@@ -22,7 +23,7 @@ STATUS = {0: "ok", -1: "invalid argument", -2: "unsupported shape", -3: "pointer
           -4: "CUDA error", -5: "device is not sm_103", -6: "a device-side wait timed out"}
 
 WEIGHT_FIELDS = ["gu", "gu_scale", "dn", "dn_scale", "gu_t", "gu_t_scale", "dn_t", "dn_t_scale",
-                 "s_gu", "s_dn", "s_gu_t", "s_dn_t"]
+                 "s_gu", "s_dn", "s_gu_t", "s_dn_t", "gu_gscale", "dn_gscale"]
 
 
 class MoeConfig(ctypes.Structure):
@@ -62,7 +63,7 @@ def lib():
         L.moe_quantize_weights.argtypes, L.moe_quantize_weights.restype = [cfgp, P, I, I, I, P, P, S], I
         L.moe_quantize_mx.argtypes, L.moe_quantize_mx.restype = [P, I, I, I, I, P, P, S], I
         L.moe_quantize_mx_both.argtypes, L.moe_quantize_mx_both.restype = [P, I, I, I, P, P, P, P, S], I
-        L.moe_prepare_weights.argtypes = [cfgp, P, P, P, P, P, P, P, P, P, P, S]
+        L.moe_prepare_weights.argtypes = [cfgp, P, P, P, P, P, P, P, P, P, P, P, P, S]
         L.moe_prepare_weights.restype = I
         L.moe_prepare_scales.argtypes, L.moe_prepare_scales.restype = [P, ctypes.c_int64, ctypes.c_int32, P, S], I
         L.moe_canonical_scales.argtypes = [P, ctypes.c_int64, ctypes.c_int32, P, S]
@@ -106,7 +107,7 @@ def _stream(stream):
 
 def config(T, d, m, E, k, m_shared=0, dtype=MOE_BF16, flags=0, ring_rows=0, gather_sms=0, aux_alpha=0.0):
     if isinstance(dtype, str):
-        dtype = MOE_MXFP8 if dtype == "mxfp8" else MOE_BF16
+        dtype = DTYPES[dtype]
     return MoeConfig(T, d, m, E, k, m_shared, dtype, flags, ring_rows, gather_sms, aux_alpha)
 
 
@@ -167,10 +168,10 @@ def moe_quantize_mx(src, batch, rows, cols, transpose, codes, scales, stream=Non
 
 
 def moe_prepare_weights(cfg, w_gu, w_dn, gu, gu_scale, dn, dn_scale, gu_t=None, gu_t_scale=None, dn_t=None,
-                        dn_t_scale=None, stream=None):
+                        dn_t_scale=None, gu_gscale=None, dn_gscale=None, stream=None):
     return lib().moe_prepare_weights(ctypes.byref(cfg), _ptr(w_gu), _ptr(w_dn), _ptr(gu), _ptr(gu_scale), _ptr(dn),
                                      _ptr(dn_scale), _ptr(gu_t), _ptr(gu_t_scale), _ptr(dn_t), _ptr(dn_t_scale),
-                                     _stream(stream))
+                                     _ptr(gu_gscale), _ptr(dn_gscale), _stream(stream))
 
 
 def moe_prepare_scales(scales, rows, K, prepared, stream=None):

@@ -31,6 +31,7 @@ constexpr int kDefaultGatherCtas = 8;
 struct Dims {
   int T, d, m, E, k, ms;
   bool mx, bwd, starve;
+  bool nv;             // NVFP4 experts (forward only)
   bool dump;           // MOE_FLAG_DEBUG_DUMP with MXFP8 experts
   bool ring;           // MXFP8 forward dispatch through the persistent ring kernel
   float aux_alpha;     // load-balancing term weight (0 = none)
@@ -45,7 +46,9 @@ int check_config(const moe_config *c, Dims *D) {
   if (c->T <= 0 || c->d <= 0 || c->m <= 0 || c->E <= 0 || c->k <= 0 || c->m_shared < 0)
     return MOE_ERR_ARG;
   if (c->k > c->E || c->k > 16 || c->E > 1024) return MOE_ERR_SHAPE;
-  if (c->dtype != MOE_BF16 && c->dtype != MOE_MXFP8) return MOE_ERR_ARG;
+  if (c->dtype != MOE_BF16 && c->dtype != MOE_MXFP8 && c->dtype != MOE_NVFP4) return MOE_ERR_ARG;
+  if (c->dtype == MOE_NVFP4 && (c->flags & MOE_FLAG_BACKWARD)) return MOE_ERR_ARG;  // forward only
+  if (c->dtype == MOE_NVFP4 && c->m % 256) return MOE_ERR_SHAPE;  // 256-deep stages along K = m
   if ((c->flags & ~(MOE_FLAG_BACKWARD | MOE_FLAG_DEBUG_STARVE | MOE_FLAG_DEBUG_DUMP)) != 0) return MOE_ERR_ARG;
   if (c->d % 256 || c->m % 128 || c->m_shared % 128) return MOE_ERR_SHAPE;
   if (c->ring_rows < 0 || c->gather_sms < 0 || c->gather_sms > 64) return MOE_ERR_ARG;
@@ -64,6 +67,7 @@ int check_config(const moe_config *c, Dims *D) {
   D->k = c->k;
   D->ms = c->m_shared;
   D->mx = c->dtype == MOE_MXFP8;
+  D->nv = c->dtype == MOE_NVFP4;
   D->bwd = (c->flags & MOE_FLAG_BACKWARD) != 0;
   D->starve = (c->flags & MOE_FLAG_DEBUG_STARVE) != 0;
   D->dump = D->mx && (c->flags & MOE_FLAG_DEBUG_DUMP) != 0;
@@ -149,18 +153,30 @@ void ws_layout(const Dims &D, Layout &L) {
   L.add("router_lpad", static_cast<size_t>(D.Tp) * Ep * 4);
   add_route(D, L);  // used when the forward saves nothing
   const size_t eb = D.mx ? 1 : 2;
-  if (D.mx) {  // row-blocked codes of every token (the dispatch copies them per routed row)
+  if (D.nv) {
+    // NVFP4: x's second-level scale, every token's packed codes (canonical
+    // scales), the dispatched rows and h (packed codes, tiled scales)
+    L.add("x_gscale", 16);
+    L.add("xq", static_cast<size_t>(D.T) * D.d / 2);
+    L.add("xq_sf", static_cast<size_t>(D.T) * D.d / 16);
+    L.add("xs", D.Rp * D.d / 2);
+    L.add("xs_sf", D.Rp * D.d / 16);
+    L.add("hq", D.Rp * D.m / 2);
+    L.add("hq_sf", D.Rp * D.m / 16);
+  } else if (D.mx) {  // row-blocked codes of every token (the dispatch copies them per routed row)
     L.add("xq", static_cast<size_t>(D.T) * D.d);
     L.add("xq_sf", static_cast<size_t>(D.T) * D.d / 32);
   }
-  if (D.ring) {  // a fixed ring of 128-row tiles instead of every dispatched row
+  if (D.nv) {
+  } else if (D.ring) {  // a fixed ring of 128-row tiles instead of every dispatched row
     L.add("ring", static_cast<size_t>(D.ring_slots) * 128 * D.d);
     L.add("ring_sf", static_cast<size_t>(D.ring_slots) * 128 * D.d / 32);
     L.add("ring_ctrl", (2 * static_cast<size_t>(D.ring_slots) + 1) * 4);
   } else {
     L.add("xs", D.Rp * D.d * eb);
   }
-  if (D.mx) {
+  if (D.nv) {
+  } else if (D.mx) {
     if (!D.ring) L.add("xs_sf", D.Rp * D.d / 32);
     L.add("hq", D.Rp * D.m);
     L.add("hq_sf", D.Rp * D.m / 32);
@@ -303,7 +319,8 @@ int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA
 // One GEMM launch: A [a_rows, K] and B [b_rows, K] (K-major) plus arguments;
 // the outputs (g.out / out2 / outq) have out_rows rows.
 struct Gemm {
-  bool mx;
+  bool mx;          // block-scaled byte operands (MXFP8, or NVFP4 with nv)
+  bool nv = false;  // NVFP4: packed E2M1 codes, K / 2 bytes per row
   int bn, epi;
   const void *a;
   long a_rows;
@@ -357,11 +374,15 @@ int run_pair(const Gemm &q, const DeviceInfo &dev, cudaStream_t s) {
   return cuda_status(moe::launch_gemm_pair(q.mx, q.epi, m, g, static_cast<int>(clusters), s));
 }
 
+int gemm_fmt(const Gemm &q) { return q.nv ? moe::FMT_NVFP4 : (q.mx ? moe::FMT_MXFP8 : moe::FMT_BF16); }
+// Elements of the tensor maps' inner dimension: NVFP4 rows hold two codes per byte.
+uint64_t map_inner(const Gemm &q) { return q.nv ? q.K / 2 : q.K; }
+
 int run_gemm(const char *name, const Gemm &q, const DeviceInfo &dev, cudaStream_t s) {
   Traced tr(name, s);
   if (use_pair(q) && (q.g.sched != moe::SCHED_GROUP_K || (q.g.M / 128) % 2 == 0)) return run_pair(q, dev, s);
   CUtensorMap tb;
-  if (!make_map(&tb, q.b, q.mx, q.K, q.b_rows)) return MOE_ERR_CUDA;
+  if (!make_map(&tb, q.b, q.mx, map_inner(q), q.b_rows)) return MOE_ERR_CUDA;
   moe::GemmArgs g = q.g;
   g.out_rows = q.out_rows;
   if (q.zero_dst) {
@@ -371,9 +392,9 @@ int run_gemm(const char *name, const Gemm &q, const DeviceInfo &dev, cudaStream_
     g.skip_empty = 1;
   }
   CUtensorMap ta;
-  if (!make_map(&ta, q.a, q.mx, q.K, q.a_rows)) return MOE_ERR_CUDA;
+  if (!make_map(&ta, q.a, q.mx, map_inner(q), q.a_rows)) return MOE_ERR_CUDA;
   const long grid = q.max_tiles < dev.num_sms ? q.max_tiles : dev.num_sms;
-  return cuda_status(moe::launch_gemm(q.mx, q.bn, q.epi, ta, tb, g, static_cast<int>(grid), s));
+  return cuda_status(moe::launch_gemm(gemm_fmt(q), q.bn, q.epi, ta, tb, g, static_cast<int>(grid), s));
 }
 
 // A GEMM on the single-CTA kernel (the router's fp32-store and add-into-bf16
@@ -384,7 +405,7 @@ int run_gemm_single(const Gemm &q, const DeviceInfo &dev, cudaStream_t s) {
   moe::GemmArgs g = q.g;
   g.out_rows = q.out_rows;
   const long grid = q.max_tiles < dev.num_sms ? q.max_tiles : dev.num_sms;
-  return cuda_status(moe::launch_gemm(q.mx, q.bn, q.epi, ta, tb, g, static_cast<int>(grid), s));
+  return cuda_status(moe::launch_gemm(gemm_fmt(q), q.bn, q.epi, ta, tb, g, static_cast<int>(grid), s));
 }
 
 // The persistent ring launch: one CTA per SM, the first gather_ctas of which
@@ -521,13 +542,33 @@ int moe_quantize_mx_both(const void *src, int batch, int rows, int cols, void *c
 
 int moe_prepare_weights(const moe_config *cfg, const void *w_gu, const void *w_dn, void *gu, void *gu_scale,
                         void *dn, void *dn_scale, void *gu_t, void *gu_t_scale, void *dn_t, void *dn_t_scale,
-                        moe_stream_t stream) {
+                        float *gu_gscale, float *dn_gscale, moe_stream_t stream) {
   Dims D;
   int rc = check_config(cfg, &D);
   if (rc != MOE_OK) return rc;
   if (!w_gu || !w_dn) return MOE_ERR_ARG;
   const bool bwd = gu_t != nullptr;
   if ((dn_t != nullptr) != bwd) return MOE_ERR_ARG;
+  if (D.nv) {
+    if (bwd || !gu || !gu_scale || !dn || !dn_scale || !gu_gscale || !dn_gscale) return MOE_ERR_ARG;
+    const void *p[] = {w_gu, w_dn, gu, gu_scale, dn, dn_scale};
+    for (const void *q : p)
+      if (!aligned16(q)) return MOE_ERR_ALIGN;
+    // one fp32 per expert: 4-byte alignment (an expert's slot of a per-layer array)
+    if ((reinterpret_cast<uintptr_t>(gu_gscale) & 3u) || (reinterpret_cast<uintptr_t>(dn_gscale) & 3u))
+      return MOE_ERR_ALIGN;
+    DeviceInfo dev;
+    if ((rc = device_info(&dev)) != MOE_OK) return rc;
+    const long E = D.E, d = D.d, m = D.m;
+    if ((rc = cuda_status(moe::launch_nv_global_scales(w_gu, D.E, 2 * m * d, gu_gscale, stream))) != MOE_OK ||
+        (rc = cuda_status(moe::launch_nv_global_scales(w_dn, D.E, d * m, dn_gscale, stream))) != MOE_OK ||
+        (rc = cuda_status(moe::launch_nv_quantize_rows(w_gu, E * 2 * m, D.d, 2 * m, gu_gscale,
+                                                       static_cast<uint8_t *>(gu), static_cast<uint8_t *>(gu_scale),
+                                                       true, stream))) != MOE_OK)
+      return rc;
+    return cuda_status(moe::launch_nv_quantize_rows(w_dn, E * d, D.m, d, dn_gscale, static_cast<uint8_t *>(dn),
+                                                    static_cast<uint8_t *>(dn_scale), true, stream));
+  }
   if (D.mx && (!gu || !gu_scale || !dn || !dn_scale || (bwd && (!gu_t_scale || !dn_t_scale)))) return MOE_ERR_ARG;
   const void *ptrs[] = {w_gu, w_dn, gu, gu_scale, dn, dn_scale, gu_t, gu_t_scale, dn_t, dn_t_scale};
   for (const void *q : ptrs)
@@ -626,11 +667,12 @@ int moe_forward(const moe_config *cfg, const void *x, const float *logits, const
   int rc = check_config(cfg, &D);
   if (rc != MOE_OK) return rc;
   if (!x || !logits || !Wt || !y || !ws || !Wt->gu || !Wt->dn) return MOE_ERR_ARG;
-  if (D.mx && (!Wt->gu_scale || !Wt->dn_scale)) return MOE_ERR_ARG;
+  if ((D.mx || D.nv) && (!Wt->gu_scale || !Wt->dn_scale)) return MOE_ERR_ARG;
+  if (D.nv && (!Wt->gu_gscale || !Wt->dn_gscale || saved)) return MOE_ERR_ARG;  // NVFP4: inference only
   if (D.ms && (!Wt->s_gu || !Wt->s_dn)) return MOE_ERR_ARG;
   if (!aligned16(x) || !aligned16(logits) || !aligned16(y) || !aligned16(ws) ||
       !aligned16(Wt->gu) || !aligned16(Wt->dn) || (saved && !aligned16(saved)) ||
-      (D.mx && (!aligned16(Wt->gu_scale) || !aligned16(Wt->dn_scale))) ||
+      ((D.mx || D.nv) && (!aligned16(Wt->gu_scale) || !aligned16(Wt->dn_scale))) ||
       (D.ms && (!aligned16(Wt->s_gu) || !aligned16(Wt->s_dn))))
     return MOE_ERR_ALIGN;
   DeviceInfo dev;
@@ -665,7 +707,17 @@ int moe_forward(const moe_config *cfg, const void *x, const float *logits, const
   uint8_t *xT_sf = (train && D.mx) ? reinterpret_cast<uint8_t *>(S.ptr(saved, "xT_sf")) : nullptr;
   uint8_t *xq = reinterpret_cast<uint8_t *>(W.ptr(ws, "xq"));
   uint8_t *xq_sf = reinterpret_cast<uint8_t *>(W.ptr(ws, "xq_sf"));
-  if (!D.ring) {
+  if (D.nv) {
+    // NVFP4: x's second-level scale, every token's codes once, then the rows
+    Traced tr("dispatch_gather", s);
+    float *xg = reinterpret_cast<float *>(W.ptr(ws, "x_gscale"));
+    rc = cuda_status(moe::launch_nv_global_scales(x, 1, static_cast<long>(D.T) * D.d, xg, s));
+    if (rc == MOE_OK)
+      rc = cuda_status(moe::launch_nv_quantize_rows(x, D.T, D.d, D.T, xg, xq, xq_sf, false, s));
+    if (rc == MOE_OK)
+      rc = cuda_status(moe::launch_nv_gather(xq, xq_sf, D.d, D.k, D.E, rb, D.Rp, reinterpret_cast<uint8_t *>(xs),
+                                             xs_sf, s));
+  } else if (!D.ring) {
     Traced tr("dispatch_gather", s);
     rc = cuda_status(
         moe::launch_gather(x, D.T, D.d, D.k, D.E, rb, D.Rp, D.mx, xs, xs_sf, xT, xT_sf, xq, xq_sf, s));
@@ -686,7 +738,7 @@ int moe_forward(const moe_config *cfg, const void *x, const float *logits, const
   }
   if (rc != MOE_OK) return rc;
   // S4 gate/up GEMM + SwiGLU (+ MX quantisation of h)
-  char *h_bf16 = D.mx ? nullptr : (train ? S.ptr(saved, "h") : W.ptr(ws, "h"));
+  char *h_bf16 = (D.mx || D.nv) ? nullptr : (train ? S.ptr(saved, "h") : W.ptr(ws, "h"));
   char *GU = train ? S.ptr(saved, "GU") : nullptr;
   uint8_t *hq = reinterpret_cast<uint8_t *>(W.ptr(ws, "hq"));
   uint8_t *hq_sf = reinterpret_cast<uint8_t *>(W.ptr(ws, "hq_sf"));
@@ -714,9 +766,15 @@ int moe_forward(const moe_config *cfg, const void *x, const float *logits, const
     q.g.ldo = D.m;
     q.g.out2 = GU;
     q.g.ldo2 = 2 * D.m;
-    q.g.outq = D.mx ? hq : nullptr;
+    q.g.outq = (D.mx || D.nv) ? hq : nullptr;
     q.g.outq_sf = hq_sf;
     q.g.ldq = D.m;
+    if (D.nv) {  // packed E2M1 operands: K-groups of the tiled scales are 64 wide
+      q.mx = q.nv = true;
+      q.g.sfa_kg = q.g.sfb_kg = D.d / 64;
+      q.g.a_gscale = reinterpret_cast<const float *>(W.ptr(ws, "x_gscale"));
+      q.g.b_gscale = Wt->gu_gscale;
+    }
     if (train && D.mx) {
       q.g.outT = reinterpret_cast<uint8_t *>(S.ptr(saved, "hT"));
       q.g.outT_sf = reinterpret_cast<uint8_t *>(S.ptr(saved, "hT_sf"));
@@ -774,6 +832,12 @@ int moe_forward(const moe_config *cfg, const void *x, const float *logits, const
     q.g.sfb_kg = D.m / 128;
     q.g.out = o;
     q.g.ldo = D.d;
+    if (D.nv) {  // h carries second-level scale 1 (a_gscale NULL)
+      q.mx = q.nv = true;
+      q.a = hq;
+      q.g.sfa_kg = q.g.sfb_kg = D.m / 64;
+      q.g.b_gscale = Wt->dn_gscale;
+    }
     q.max_tiles = (D.Rp / 128) * q.g.n_tiles;
     q.out_rows = D.Rp;
     if ((rc = run_gemm("gemm2_down", q, dev, s)) != MOE_OK) return rc;

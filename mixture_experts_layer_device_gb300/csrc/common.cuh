@@ -5,7 +5,9 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp4.h>
 #include <cuda_fp8.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -203,6 +205,17 @@ MOE_DEV void mma_mxf8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t 
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
       : "memory");
 }
+// Block-scaled NVFP4 (E2M1 x E2M1, packed two per byte, UE4M3 scales per 16
+// along K; K = 64 per instruction).
+MOE_DEV void mma_nvf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t sfa_tmem,
+                      uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n}\n" ::
+          "r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
 // Arrive on an mbarrier once all previously issued tcgen05 ops of this thread finish.
 MOE_DEV void mma_commit(uint64_t *bar) {
   asm volatile(
@@ -280,6 +293,14 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
 }
 __host__ __device__ constexpr uint32_t idesc_mxf8(int M, int N) {
   return (static_cast<uint32_t>(N >> 3) << 17) | (1u << 23) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+//   kind::mxf4nvf4.block_scale (NVFP4): A/B fmt E2M1 (1) at [7,10) / [10,13),
+//                N>>3 at [17,23), scale fmt UE4M3 (0) at bit 23, M>>4 at
+//                [24,29); scale ids 0 (with scale_vec::4X each MMA reads a
+//                whole 32-bit word: four scales of 16 elements).
+__host__ __device__ constexpr uint32_t idesc_nvf4(int M, int N) {
+  return (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
          (static_cast<uint32_t>(M >> 4) << 24);
 }
 MOE_DEV uint32_t idesc_sf_ids(uint32_t idesc, uint32_t a_id, uint32_t b_id) {
@@ -407,6 +428,44 @@ MOE_DEV void mx_encode32(const float *v, uint32_t byte, uint32_t *out8) {
     out8[i] = lo | (hi << 16);
   }
 }
+
+// ---------------------------------------------------------------- NVFP4
+// E4M3 code of a non-negative float (round to nearest even, saturating to
+// 448) and its value; two floats -> two E2M1 codes in one byte (x in the low
+// nibble; round to nearest even, saturating to 6).
+MOE_DEV uint32_t e4m3_code(float t) {
+  return static_cast<uint32_t>(__nv_cvt_float_to_fp8(t, __NV_SATFINITE, __NV_E4M3));
+}
+MOE_DEV float e4m3_value(uint32_t code) {
+  return __half2float(__half(__nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(code), __NV_E4M3)));
+}
+MOE_DEV uint32_t e2m1x2(float lo, float hi) {
+  return static_cast<uint32_t>(__nv_cvt_float2_to_fp4x2(make_float2(lo, hi), __NV_E2M1, cudaRoundNearest));
+}
+// One NVFP4 block of 16 values with second-level scale s_enc: the scale code
+// E4M3(amax / 6 * s_enc) is returned and the 16 codes E2M1(v * (s_enc /
+// scale)) go to w[0..1] (element 2i in the low nibble of byte i), every step
+// one IEEE fp32 operation (a zero scale stores signed zeros).
+MOE_DEV uint32_t nv_block16(const float *v, float s_enc, uint32_t *w) {
+  float am = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) am = fmaxf(am, fabsf(v[i]));
+  const uint32_t sf = e4m3_code(__fmul_rn(__fdiv_rn(am, 6.0f), s_enc));
+  const float sv = e4m3_value(sf);
+  const float inv = sv > 0.f ? __fdiv_rn(s_enc, sv) : 0.f;
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    uint32_t x = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      x |= e2m1x2(__fmul_rn(v[8 * q + 2 * j], inv), __fmul_rn(v[8 * q + 2 * j + 1], inv)) << (8 * j);
+    w[q] = x;
+  }
+  return sf;
+}
+// Second-level NVFP4 scale of a tensor from its absolute maximum: 448 * 6 /
+// amax (one IEEE division), 1 for an all-zero tensor.
+MOE_DEV float nv_global_scale(float amax) { return amax > 0.f ? __fdiv_rn(2688.0f, amax) : 1.0f; }
 
 // 32 bytes to global memory at a 16-byte-aligned address: one 32-byte store
 // (a full sector) when the address allows it, else two 16-byte stores.

@@ -35,28 +35,40 @@ namespace {
 
 using namespace gemm_detail;
 
-template <bool MX, int BN>
+// Operand formats of the single-CTA GEMM: BF16 (kind::f16), MXFP8 (E4M3 with
+// an E8M0 scale per 32 along K, kind::mxf8f6f4) and NVFP4 (packed E2M1 with an
+// E4M3 scale per 16 along K, kind::mxf4nvf4 with scale_vec::4X; the
+// accumulator is multiplied by the two operands' second-level scales in the
+// epilogue).  Every format moves 128-byte rows of A and B per stage.
+template <int F, int BN>
 struct Cfg {
+  static constexpr bool MX = F != FMT_BF16;  // block-scaled operands
+  static constexpr bool NV = F == FMT_NVFP4;
   static constexpr int BM = 128;
-  static constexpr int BK = MX ? 128 : 64;  // elements per 128-byte smem row
-  static constexpr int UK = MX ? 32 : 16;   // K per tcgen05.mma
+  static constexpr int BK = NV ? 256 : (MX ? 128 : 64);  // elements per 128-byte smem row
+  static constexpr int UK = NV ? 64 : (MX ? 32 : 16);    // K per tcgen05.mma
   static constexpr int KSTEPS = BK / UK;
   static constexpr int A_BYTES = BM * 128;
   static constexpr int B_BYTES = BN * 128;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = BN == 256 ? 4 : 6;
-  static constexpr int SFA_BYTES = MX ? 512 : 0;
-  static constexpr int SFB_BYTES = MX ? (BN / 128) * 512 : 0;
+  // 512-byte scale atoms (128 rows x 4 blocks) per 128 rows and stage: one
+  // MXFP8 atom spans 128 of K, an NVFP4 atom 64, so an NVFP4 stage needs four
+  static constexpr int SF_ATOMS = NV ? 4 : 1;
+  static constexpr int STAGES = NV ? (BN == 256 ? 3 : 5) : (BN == 256 ? 4 : 6);
+  static constexpr int SFA_BYTES = MX ? 512 * SF_ATOMS : 0;
+  static constexpr int SFB_BYTES = MX ? (BN / 128) * 512 * SF_ATOMS : 0;
   static constexpr int SF_STAGE = SFA_BYTES + SFB_BYTES;
   static constexpr int NUM_ACC = (MX && BN == 256) ? 1 : 2;
   static constexpr uint32_t TMEM_COLS = 512;
   // Scale factors get their own TMEM columns per pipeline stage (4 for A, BN/32
-  // for B), so copying a stage's scales never waits for the MMAs still reading
-  // the previous stage's.
-  static constexpr int SF_COLS = 4 + BN / 32;
+  // for B, per atom), so copying a stage's scales never waits for the MMAs
+  // still reading the previous stage's.  MMA k of an NVFP4 stage reads atom k:
+  // A at columns 4k, B at 4 SF_ATOMS + k BN/32 of the stage's block.
+  static constexpr int SFA_COLS = 4 * SF_ATOMS;
+  static constexpr int SF_COLS = SF_ATOMS * (4 + BN / 32);
   static constexpr int SF_COL0 = NUM_ACC * BN;
   static constexpr uint32_t TX_BYTES = STAGE_BYTES + SF_STAGE;
-  static constexpr uint32_t IDESC = MX ? idesc_mxf8(128, BN) : idesc_bf16(128, BN);
+  static constexpr uint32_t IDESC = NV ? idesc_nvf4(128, BN) : (MX ? idesc_mxf8(128, BN) : idesc_bf16(128, BN));
   // epilogue staging: 2 KB pieces (32 rows x 64 B, 64-byte swizzle), 16 KB split
   // over the epilogue warps
   static constexpr int STAGING_BYTES = 4 * 4096;
@@ -71,6 +83,7 @@ struct Cfg {
 
 struct Tile {
   int a_row, k0, nk, b_row0, b_row1, out_row, out_col;
+  int e;  // group (expert) of the tile
 };
 
 template <int BK, int BN, int EPI>
@@ -124,6 +137,7 @@ MOE_DEV Tile decode_tile(const GemmArgs &g, int t) {
     }
     ti.out_row = e * g.M + mt * 128;
   }
+  ti.e = e;
   if (EPI == EPI_SWIGLU) {
     ti.b_row0 = e * g.b_rows_per_group + ntile * 128;
     ti.b_row1 = ti.b_row0 + g.b_split;
@@ -280,11 +294,13 @@ __host__ __device__ constexpr int epi_warps() {
   return 8;
 }
 
-template <bool MX, int BN, int EPI, bool RING = false, bool DUMP = false>
+template <int F, int BN, int EPI, bool RING = false, bool DUMP = false>
 __global__ void __launch_bounds__(64 + 32 * epi_warps<EPI, BN>(), 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const GemmArgs g) {
-  using C = Cfg<MX, BN>;
+  using C = Cfg<F, BN>;
+  constexpr bool MX = C::MX;
+  constexpr bool NV = C::NV;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
@@ -361,19 +377,19 @@ __global__ void __launch_bounds__(64 + 32 * epi_warps<EPI, BN>(), 1)
           mbar_arrive_expect_tx(&full[stage], C::TX_BYTES);
           armed[stage] = static_cast<int>(ph);
           const int kc = ti.k0 + kb * C::BK;
-          tma_load_2d(&tmA, &full[stage], sa, kc, a_row);
-          tma_load_2d(&tmB, &full[stage], sb, kc, ti.b_row0);
-          if (BN == 256) tma_load_2d(&tmB, &full[stage], sb + 128 * 128, kc, ti.b_row1);
+          const int kx = NV ? kc / 2 : kc;  // tensor-map coordinate: NVFP4 maps count bytes
+          tma_load_2d(&tmA, &full[stage], sa, kx, a_row);
+          tma_load_2d(&tmB, &full[stage], sb, kx, ti.b_row0);
+          if (BN == 256) tma_load_2d(&tmB, &full[stage], sb + 128 * 128, kx, ti.b_row1);
           if constexpr (MX) {
+            constexpr uint32_t ab = 512u * C::SF_ATOMS;  // one stage's atoms of 128 rows, contiguous
             uint8_t *sfs = sf_base + stage * C::SF_STAGE;
-            const int kg = kc >> 7;
-            bulk_load(sfs, g.sfa + (static_cast<size_t>(a_row >> 7) * g.sfa_kg + kg) * 512, 512,
+            const int kg = NV ? kc >> 6 : kc >> 7;
+            bulk_load(sfs, g.sfa + (static_cast<size_t>(a_row >> 7) * g.sfa_kg + kg) * 512, ab, &full[stage]);
+            bulk_load(sfs + ab, g.sfb + (static_cast<size_t>(ti.b_row0 >> 7) * g.sfb_kg + kg) * 512, ab,
                       &full[stage]);
-            bulk_load(sfs + 512, g.sfb + (static_cast<size_t>(ti.b_row0 >> 7) * g.sfb_kg + kg) * 512,
-                      512, &full[stage]);
             if (BN == 256)
-              bulk_load(sfs + 1024,
-                        g.sfb + (static_cast<size_t>(ti.b_row1 >> 7) * g.sfb_kg + kg) * 512, 512,
+              bulk_load(sfs + 2 * ab, g.sfb + (static_cast<size_t>(ti.b_row1 >> 7) * g.sfb_kg + kg) * 512, ab,
                         &full[stage]);
           }
           if (++stage == C::STAGES) {
@@ -412,20 +428,27 @@ __global__ void __launch_bounds__(64 + 32 * epi_warps<EPI, BN>(), 1)
           const uint32_t sa = smem_u32(smem + stage * C::STAGE_BYTES);
           const uint32_t sb = sa + C::A_BYTES;
           const uint32_t sfa_col = tmem_base + C::SF_COL0 + stage * C::SF_COLS;
-          const uint32_t sfb_col = sfa_col + 4;
+          const uint32_t sfb_col = sfa_col + C::SFA_COLS;
           if constexpr (MX) {
+            constexpr uint32_t ab = 512u * C::SF_ATOMS;
             const uint32_t sfs = smem_u32(sf_base + stage * C::SF_STAGE);
-            tmem_cp_32x128b_warpx4(sfa_col, plain_desc_sbo128(sfs));
 #pragma unroll
-            for (int c = 0; c < BN / 128; ++c)
-              tmem_cp_32x128b_warpx4(sfb_col + 4 * c, plain_desc_sbo128(sfs + 512 + 512 * c));
+            for (int a = 0; a < C::SF_ATOMS; ++a) {
+              tmem_cp_32x128b_warpx4(sfa_col + 4 * a, plain_desc_sbo128(sfs + 512 * a));
+#pragma unroll
+              for (int c = 0; c < BN / 128; ++c)
+                tmem_cp_32x128b_warpx4(sfb_col + a * (BN / 32) + 4 * c,
+                                       plain_desc_sbo128(sfs + ab + ab * c + 512 * a));
+            }
           }
 #pragma unroll
           for (int k = 0; k < C::KSTEPS; ++k) {
             const uint64_t ad = sw128_desc(sa + 32 * k);
             const uint64_t bd = sw128_desc(sb + 32 * k);
             const uint32_t accum = (kb | k) ? 1u : 0u;
-            if constexpr (MX)
+            if constexpr (NV)  // 4X: all four scale bytes of a row's word feed MMA k (scale ids 0)
+              mma_nvf4(dt, ad, bd, C::IDESC, sfa_col + 4 * k, sfb_col + k * (BN / 32), accum);
+            else if constexpr (MX)
               mma_mxf8(dt, ad, bd, idesc_sf_ids(C::IDESC, k, k), sfa_col, sfb_col, accum);
             else
               mma_bf16(dt, ad, bd, C::IDESC, accum);
@@ -487,8 +510,10 @@ __global__ void __launch_bounds__(64 + 32 * epi_warps<EPI, BN>(), 1)
         tc_fence_before();
         mbar_arrive(&tempty[acc]);
       };
-      epilogue_tile_split<EPI, BN, DUMP>(g, vO, vO2, vQ, st, tb, ti.nk, row0, grow, ti.out_col, lane, part,
-                                         true, release);
+      float sc = 1.0f;  // NVFP4: the inverse of both operands' second-level scales
+      if constexpr (NV) sc = 1.0f / ((g.a_gscale ? __ldg(g.a_gscale) : 1.0f) * __ldg(g.b_gscale + ti.e));
+      epilogue_tile_split<EPI, BN, DUMP, NV>(g, vO, vO2, vQ, st, tb, ti.nk, row0, grow, ti.out_col, lane, part,
+                                             true, release, sc);
       if (++acc == C::NUM_ACC) {
         acc = 0;
         aph ^= 1u;
@@ -503,29 +528,29 @@ __global__ void __launch_bounds__(64 + 32 * epi_warps<EPI, BN>(), 1)
   }
 }
 
-template <bool MX, int BN, int EPI, bool DUMP = false>
+template <int F, int BN, int EPI, bool DUMP = false>
 cudaError_t launch_one(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs &g, int grid,
                        cudaStream_t s) {
-  using C = Cfg<MX, BN>;
+  using C = Cfg<F, BN>;
   static bool attr_set = false;  // per instantiation; idempotent, benign if repeated
   if (!attr_set) {
-    const cudaError_t e = cudaFuncSetAttribute(gemm_kernel<MX, BN, EPI, false, DUMP>,
+    const cudaError_t e = cudaFuncSetAttribute(gemm_kernel<F, BN, EPI, false, DUMP>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                static_cast<int>(C::SMEM));
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  gemm_kernel<MX, BN, EPI, false, DUMP><<<grid, 64 + 32 * epi_warps<EPI, BN>(), C::SMEM, s>>>(ta, tb, g);
+  gemm_kernel<F, BN, EPI, false, DUMP><<<grid, 64 + 32 * epi_warps<EPI, BN>(), C::SMEM, s>>>(ta, tb, g);
   return cudaGetLastError();
 }
 
 int ring_ctas_query() {
-  using C = Cfg<true, 256>;
-  if (cudaFuncSetAttribute(gemm_kernel<true, 256, EPI_SWIGLU, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  using C = Cfg<FMT_MXFP8, 256>;
+  if (cudaFuncSetAttribute(gemm_kernel<FMT_MXFP8, 256, EPI_SWIGLU, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(C::SMEM)) != cudaSuccess)
     return 0;
   int per_sm = 0, dev = 0, sms = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemm_kernel<true, 256, EPI_SWIGLU, true>,
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemm_kernel<FMT_MXFP8, 256, EPI_SWIGLU, true>,
                                                     64 + 32 * epi_warps<EPI_SWIGLU, 256>(),
                                                     C::SMEM) != cudaSuccess ||
       cudaGetDevice(&dev) != cudaSuccess ||
@@ -545,7 +570,7 @@ int ring_max_ctas() { return ring_ctas_resident(); }
 
 cudaError_t launch_gemm_ring(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs &g, int grid,
                              cudaStream_t s) {
-  using C = Cfg<true, 256>;
+  using C = Cfg<FMT_MXFP8, 256>;
   // Gather and GEMM CTAs wait on each other: all of them must be resident at
   // once, which the cooperative launch guarantees (or refuses).
   if (grid <= g.ring.gather_ctas || g.ring.gather_ctas <= 0 || grid > ring_ctas_resident())
@@ -560,33 +585,37 @@ cudaError_t launch_gemm_ring(const CUtensorMap &ta, const CUtensorMap &tb, const
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemm_kernel<true, 256, EPI_SWIGLU, true>, ta, tb, g);
+  return cudaLaunchKernelEx(&cfg, gemm_kernel<FMT_MXFP8, 256, EPI_SWIGLU, true>, ta, tb, g);
 }
 
-cudaError_t launch_gemm(bool mx, int bn, int epi, const CUtensorMap &ta, const CUtensorMap &tb,
+cudaError_t launch_gemm(int fmt, int bn, int epi, const CUtensorMap &ta, const CUtensorMap &tb,
                         const GemmArgs &g, int grid, cudaStream_t s) {
   if (grid <= 0) return cudaSuccess;
   if (g.dump) {  // test hook: the MXFP8 gate/up GEMM that also stores its fp32 h
-    if (mx && bn == 256 && epi == EPI_SWIGLU) return launch_one<true, 256, EPI_SWIGLU, true>(ta, tb, g, grid, s);
+    if (fmt == FMT_MXFP8 && bn == 256 && epi == EPI_SWIGLU)
+      return launch_one<FMT_MXFP8, 256, EPI_SWIGLU, true>(ta, tb, g, grid, s);
     return cudaErrorInvalidValue;
   }
-#define MOE_GEMM_CASE(MXV, BNV, EPIV) \
-  if (mx == MXV && bn == BNV && epi == EPIV)  \
-    return launch_one<MXV, BNV, EPIV>(ta, tb, g, grid, s);
-  MOE_GEMM_CASE(false, 256, EPI_STORE)
-  MOE_GEMM_CASE(false, 128, EPI_STORE)
-  MOE_GEMM_CASE(false, 256, EPI_SWIGLU)
-  MOE_GEMM_CASE(false, 256, EPI_SWIGLU_BWD)
-  MOE_GEMM_CASE(false, 128, EPI_SWIGLU_BWD)
-  MOE_GEMM_CASE(false, 256, EPI_STORE_F32)
-  MOE_GEMM_CASE(false, 128, EPI_STORE_F32)
-  MOE_GEMM_CASE(false, 256, EPI_ADD_BF16)
-  MOE_GEMM_CASE(false, 128, EPI_ADD_BF16)
-  MOE_GEMM_CASE(true, 256, EPI_STORE)
-  MOE_GEMM_CASE(true, 128, EPI_STORE)
-  MOE_GEMM_CASE(true, 256, EPI_SWIGLU)
-  MOE_GEMM_CASE(true, 256, EPI_SWIGLU_BWD)
-  MOE_GEMM_CASE(true, 128, EPI_SWIGLU_BWD)
+#define MOE_GEMM_CASE(FV, BNV, EPIV) \
+  if (fmt == FV && bn == BNV && epi == EPIV) \
+    return launch_one<FV, BNV, EPIV>(ta, tb, g, grid, s);
+  MOE_GEMM_CASE(FMT_BF16, 256, EPI_STORE)
+  MOE_GEMM_CASE(FMT_BF16, 128, EPI_STORE)
+  MOE_GEMM_CASE(FMT_BF16, 256, EPI_SWIGLU)
+  MOE_GEMM_CASE(FMT_BF16, 256, EPI_SWIGLU_BWD)
+  MOE_GEMM_CASE(FMT_BF16, 128, EPI_SWIGLU_BWD)
+  MOE_GEMM_CASE(FMT_BF16, 256, EPI_STORE_F32)
+  MOE_GEMM_CASE(FMT_BF16, 128, EPI_STORE_F32)
+  MOE_GEMM_CASE(FMT_BF16, 256, EPI_ADD_BF16)
+  MOE_GEMM_CASE(FMT_BF16, 128, EPI_ADD_BF16)
+  MOE_GEMM_CASE(FMT_MXFP8, 256, EPI_STORE)
+  MOE_GEMM_CASE(FMT_MXFP8, 128, EPI_STORE)
+  MOE_GEMM_CASE(FMT_MXFP8, 256, EPI_SWIGLU)
+  MOE_GEMM_CASE(FMT_MXFP8, 256, EPI_SWIGLU_BWD)
+  MOE_GEMM_CASE(FMT_MXFP8, 128, EPI_SWIGLU_BWD)
+  MOE_GEMM_CASE(FMT_NVFP4, 256, EPI_STORE)
+  MOE_GEMM_CASE(FMT_NVFP4, 128, EPI_STORE)
+  MOE_GEMM_CASE(FMT_NVFP4, 256, EPI_SWIGLU)
 #undef MOE_GEMM_CASE
   return cudaErrorInvalidValue;
 }

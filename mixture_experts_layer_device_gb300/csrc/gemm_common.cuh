@@ -129,6 +129,19 @@ struct Stager {
   }
 };
 
+// Four NVFP4 blocks (64 values) of one row, second-level scale 1 -> 32 bytes of
+// packed codes (one 32-byte store, the lane's own row) + 4 scale bytes (next to
+// each other in one 512-byte atom of the NVFP4 layout: K' = 2 ldq).
+MOE_DEV void put_nv64(const GemmArgs &g, const float *v64, int col, long grow) {
+  if (grow >= g.out_rows) return;
+  uint32_t w[8];
+  uint32_t sfw = 0;
+#pragma unroll
+  for (int b = 0; b < 4; ++b) sfw |= nv_block16(v64 + 16 * b, 1.0f, w + 2 * b) << (8 * b);
+  st_global_32B(g.outq + grow * (g.ldq / 2) + col / 2, w);
+  *reinterpret_cast<uint32_t *>(g.outq_sf + sf_tiled_offset(grow, col / 16, 2 * g.ldq)) = sfw;
+}
+
 // Two MX blocks (64 values) of one row -> one 64-byte codes piece + 2 scale bytes.
 MOE_DEV void put_mx64(Stager &st, const OutView &vq, uint8_t *sf, long ldq, const float *v64,
                       int col, int row0, long grow, int lane) {
@@ -298,11 +311,14 @@ MOE_DEV void epilogue_tile(const GemmArgs &g, const OutView &vO, const OutView &
 // any conversion or store; the SwiGLU backward reads its columns 64 at a time.
 // DUMP (SwiGLU, a separate instantiation so the normal kernel carries none of
 // its register pressure): also store the fp32 h to g.dump.
-template <int EPI, int BN, bool DUMP = false, typename Release>
+// NV (NVFP4 operands): the accumulator is multiplied by `sc` (the inverse of
+// the operands' second-level scales) first, and the SwiGLU epilogue writes h
+// as NVFP4 (store and SwiGLU epilogues only).
+template <int EPI, int BN, bool DUMP = false, bool NV = false, typename Release>
 MOE_DEV void epilogue_tile_split(const GemmArgs &g, const OutView &vO, const OutView &vO2,
                                  const OutView &vQ, Stager &st, uint32_t tb, int nk, int row0,
                                  long grow, int out_col, int lane, int part, bool store,
-                                 Release release) {
+                                 Release release, float sc = 1.0f) {
   if constexpr (EPI == EPI_STORE) {
     constexpr int NC = BN / 2;  // accumulator columns of this warp
     constexpr int NC32 = NC / 32;
@@ -327,9 +343,15 @@ MOE_DEV void epilogue_tile_split(const GemmArgs &g, const OutView &vO, const Out
     tmem_ld_wait();
     reg_fence<NC>(raw);
     release();
+    if constexpr (NV) {
 #pragma unroll
-    for (int i = 0; i < NC / 2; ++i)
-      raw[i] = pack_bf16x2(__uint_as_float(raw[2 * i]), __uint_as_float(raw[2 * i + 1]));
+      for (int i = 0; i < NC / 2; ++i)
+        raw[i] = pack_bf16x2(__uint_as_float(raw[2 * i]) * sc, __uint_as_float(raw[2 * i + 1]) * sc);
+    } else {
+#pragma unroll
+      for (int i = 0; i < NC / 2; ++i)
+        raw[i] = pack_bf16x2(__uint_as_float(raw[2 * i]), __uint_as_float(raw[2 * i + 1]));
+    }
     if (store) {
 #pragma unroll
       for (int c = 0; c < NC32; ++c) st.put(vO, raw + 16 * c, out_col + c0 + 32 * c, row0, lane);
@@ -434,7 +456,14 @@ MOE_DEV void epilogue_tile_split(const GemmArgs &g, const OutView &vO, const Out
     release();
     if (!store) return;
     float *G = reinterpret_cast<float *>(gr);
-    const float *U = reinterpret_cast<const float *>(ur);
+    float *U = reinterpret_cast<float *>(ur);
+    if constexpr (NV) {
+#pragma unroll
+      for (int i = 0; i < 64; ++i) {
+        G[i] *= sc;
+        U[i] *= sc;
+      }
+    }
     const int col = out_col + hc;
     if (g.out2) {
       st.put_bf16(vO2, G, col, row0, lane);
@@ -459,7 +488,10 @@ MOE_DEV void epilogue_tile_split(const GemmArgs &g, const OutView &vO, const Out
       st.put_col_codes(G, g.outT, g.outT_sf, g.ldT, col, row0, lane);
       st.put_col_codes(G + 32, g.outT, g.outT_sf, g.ldT, col + 32, row0, lane);
     }
-    if (g.outq) put_mx64(st, vQ, g.outq_sf, g.ldq, G, col, row0, grow, lane);
+    if (g.outq) {
+      if constexpr (NV) put_nv64(g, G, col, grow);
+      else put_mx64(st, vQ, g.outq_sf, g.ldq, G, col, row0, grow, lane);
+    }
   }
 }
 

@@ -710,6 +710,78 @@ __global__ void __launch_bounds__(256) scales_layout_kernel(const uint32_t *__re
   else dst[i] = __ldg(src + t);
 }
 
+// ------------------------------------------------------------ NVFP4
+// Absolute maximum of each of `batch` bf16 tensors of n values (n a multiple of
+// 8): blocks of grid.x stride over a tensor (grid.y), the warps' maxima are
+// combined with an integer atomicMax on the fp32 bits (|v| >= 0, so the bit
+// patterns order like the values; the result does not depend on the order).
+// `out` must be zero beforehand.
+__global__ void __launch_bounds__(256) amax_kernel(const uint4 *__restrict__ src, long n, unsigned *out) {
+  const long vec = n / 8;
+  const uint4 *p = src + static_cast<long>(blockIdx.y) * vec;
+  float am = 0.f;
+  for (long i = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x; i < vec;
+       i += static_cast<long>(gridDim.x) * blockDim.x) {
+    float f[8];
+    unpack8(__ldg(p + i), f);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) am = fmaxf(am, fabsf(f[q]));
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, off));
+  if ((threadIdx.x & 31) == 0) atomicMax(out + blockIdx.y, __float_as_uint(am));
+}
+
+// In place: the fp32 bits of n tensors' absolute maxima -> their NVFP4
+// second-level scales 2688 / amax (1 for an all-zero tensor).
+__global__ void nv_scale_from_amax_kernel(unsigned *amax_then_scale, int n) {
+  const int i = static_cast<int>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i < n) amax_then_scale[i] = __float_as_uint(nv_global_scale(__uint_as_float(amax_then_scale[i])));
+}
+
+// NVFP4 rows: src [rows, cols] bf16 -> packed codes [rows, cols / 2] and scale
+// codes (tiled: the GEMM operand layout, K' = 2 cols; else canonical [rows,
+// cols / 16]); thread per block of 16.  Row r's tensor has the second-level
+// scale gscale[r / rows_per_tensor].
+template <bool TILED>
+__global__ void __launch_bounds__(256) nv_quantize_rows_kernel(const uint4 *__restrict__ src, long rows, int cols,
+                                                               long rows_per_tensor, const float *__restrict__ gscale,
+                                                               uint2 *__restrict__ codes, uint8_t *__restrict__ sf) {
+  const int nb = cols / 16;
+  const long i = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= rows * nb) return;
+  const long r = i / nb;
+  const int b = static_cast<int>(i % nb);
+  const float s = __ldg(gscale + r / rows_per_tensor);
+  float v[16];
+  unpack8(__ldg(src + 2 * i), v);
+  unpack8(__ldg(src + 2 * i + 1), v + 8);
+  uint32_t w[2];
+  const uint32_t code = nv_block16(v, s, w);
+  codes[i] = make_uint2(w[0], w[1]);
+  sf[TILED ? sf_tiled_offset(r, b, 2L * cols) : static_cast<size_t>(i)] = static_cast<uint8_t>(code);
+}
+
+// NVFP4 dispatch: padded expert-sorted row pr <- the token's codes (xq [T, d/2],
+// canonical scales xq_sf [T, d/16]), zeros on padding rows; scales go to the
+// tiled layout of xs (K' = 2 d), 4 blocks (one word) per thread.  Warp per row.
+__global__ void __launch_bounds__(256) nv_gather_kernel(const uint4 *__restrict__ xq,
+                                                        const uint32_t *__restrict__ xq_sf, int d, int k, int E,
+                                                        RouteBufs b, long rows, uint4 *__restrict__ xs,
+                                                        uint8_t *__restrict__ xs_sf) {
+  const long pr = static_cast<long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (pr >= rows || pr >= __ldg(b.poff + E)) return;
+  const int tok = token_of_row(b, E, k, static_cast<int>(pr), nullptr);
+  const int vec = d / 32;  // 16-byte pieces of a row of codes
+  for (int i = lane; i < vec; i += 32)
+    xs[pr * vec + i] = tok >= 0 ? __ldg(xq + static_cast<long>(tok) * vec + i) : make_uint4(0, 0, 0, 0);
+  const int words = d / 64;  // scale words (4 blocks of 16) of a row
+  for (int j = lane; j < words; j += 32)
+    *reinterpret_cast<uint32_t *>(xs_sf + sf_tiled_offset(pr, 4 * j, 2L * d)) =
+        tok >= 0 ? __ldg(xq_sf + static_cast<long>(tok) * words + j) : 0u;
+}
+
 // Zeros of the empty experts' weight gradients: block (x, e) clears bytes
 // [x MB, (x + 1) MB) of expert e's matrix when the expert received no rows.
 constexpr long kZeroPiece = 1L << 20;
@@ -953,6 +1025,39 @@ cudaError_t launch_scales_layout(const void *src, long rows, int K, bool to_tile
   else
     scales_layout_kernel<false><<<blocks_for(n, 256), 256, 0, s>>>(static_cast<const uint32_t *>(src),
                                                                     static_cast<uint32_t *>(dst), rows, K);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_nv_global_scales(const void *src, int batch, long n, float *gscale, cudaStream_t s) {
+  unsigned *g = reinterpret_cast<unsigned *>(gscale);
+  const cudaError_t e = cudaMemsetAsync(g, 0, static_cast<size_t>(batch) * sizeof(unsigned), s);
+  if (e != cudaSuccess) return e;
+  long blocks = (n / 8 + 255) / 256;
+  if (blocks > 1024) blocks = 1024;
+  amax_kernel<<<dim3(static_cast<unsigned>(blocks), batch), 256, 0, s>>>(static_cast<const uint4 *>(src), n, g);
+  nv_scale_from_amax_kernel<<<blocks_for(batch, 256), 256, 0, s>>>(g, batch);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_nv_quantize_rows(const void *src, long rows, int cols, long rows_per_tensor, const float *gscale,
+                                    uint8_t *codes, uint8_t *scales, bool tiled, cudaStream_t s) {
+  const long n = rows * (cols / 16);
+  if (tiled)
+    nv_quantize_rows_kernel<true><<<blocks_for(n, 256), 256, 0, s>>>(
+        static_cast<const uint4 *>(src), rows, cols, rows_per_tensor, gscale, reinterpret_cast<uint2 *>(codes),
+        scales);
+  else
+    nv_quantize_rows_kernel<false><<<blocks_for(n, 256), 256, 0, s>>>(
+        static_cast<const uint4 *>(src), rows, cols, rows_per_tensor, gscale, reinterpret_cast<uint2 *>(codes),
+        scales);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_nv_gather(const uint8_t *xq, const uint8_t *xq_sf, int d, int k, int E, const RouteBufs &b,
+                             long rows, uint8_t *xs, uint8_t *xs_sf, cudaStream_t s) {
+  nv_gather_kernel<<<blocks_for(rows, 8), 256, 0, s>>>(reinterpret_cast<const uint4 *>(xq),
+                                                       reinterpret_cast<const uint32_t *>(xq_sf), d, k, E, b, rows,
+                                                       reinterpret_cast<uint4 *>(xs), xs_sf);
   return cudaGetLastError();
 }
 

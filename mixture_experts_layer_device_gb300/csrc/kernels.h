@@ -85,6 +85,9 @@ cudaError_t launch_transpose_bf16(const void *src, int batch, int rows, int cols
 
 // ---------------------------------------------------------------- GEMM
 enum GemmSched { SCHED_GROUP_M = 0, SCHED_DENSE = 1, SCHED_GROUP_K = 2 };
+// Operand formats of launch_gemm.
+enum GemmFmt { FMT_BF16 = 0, FMT_MXFP8 = 1, FMT_NVFP4 = 2 };
+
 // EPI_STORE_F32: fp32 output (the router logits); EPI_ADD_BF16: out = bf16(out +
 // acc) with `out` read back through aux (the router's dx contribution).  Both
 // run on the single-CTA kernel only.
@@ -117,6 +120,20 @@ cudaError_t launch_pad_to_bf16(const float *src, int rows, int cols, int rows_p,
                                cudaStream_t s);
 // dst [rows, cols] fp32 = the top-left corner of src [*, ld_src] fp32.
 cudaError_t launch_crop_f32(const float *src, int rows, int cols, long ld_src, float *dst, cudaStream_t s);
+
+// NVFP4 second-level scales of `batch` bf16 tensors of n values each (n a
+// multiple of 8): gscale[t] = 2688 / amax(|tensor t|), 1 for an all-zero one.
+cudaError_t launch_nv_global_scales(const void *src, int batch, long n, float *gscale, cudaStream_t s);
+// NVFP4 rows src [rows, cols] bf16 (cols a multiple of 64) -> packed codes
+// [rows, cols / 2] and scale codes (tiled operand layout with K' = 2 cols, or
+// canonical [rows, cols / 16]); row r's tensor has second-level scale
+// gscale[r / rows_per_tensor].
+cudaError_t launch_nv_quantize_rows(const void *src, long rows, int cols, long rows_per_tensor, const float *gscale,
+                                    uint8_t *codes, uint8_t *scales, bool tiled, cudaStream_t s);
+// NVFP4 dispatch: padded expert-sorted rows [0, rows) <- their tokens' codes
+// (xq [T, d / 2], canonical scales [T, d / 16]), tiled scales (K' = 2 d).
+cudaError_t launch_nv_gather(const uint8_t *xq, const uint8_t *xq_sf, int d, int k, int E, const RouteBufs &b,
+                             long rows, uint8_t *xs, uint8_t *xs_sf, cudaStream_t s);
 
 // Row-blocked MXFP8 codes of every token: x [T, d] bf16 -> codes [T, d] and
 // canonical scales [T, d/32] (the ring dispatch gathers these rows).
@@ -171,6 +188,8 @@ struct GemmArgs {
   const void *aux;    // SWIGLU_BWD: saved G|U bf16
   long ld_aux;
   int m_half;         // SWIGLU / SWIGLU_BWD: m
+  const float *a_gscale;  // NVFP4: second-level scale of A (one value; NULL = 1)
+  const float *b_gscale;  // NVFP4: second-level scale of B per group [E]
   float *dump;        // SWIGLU (tests): fp32 h before quantisation [rows, ld_dump] (may be NULL)
   long ld_dump;
   int skip_empty;     // GROUP_K: tiles with an empty reduction are left to launch_zero_empty_experts
@@ -191,7 +210,7 @@ cudaError_t launch_zero_empty_experts(void *dW, int E, long expert_bytes, const 
 // output columns per tile; `grid` persistent CTAs (<= number of SMs).  The
 // epilogue writes args.out / out2 / outq (row strides ldo / ldo2 / ldq) with
 // coalesced global stores, rows < args.out_rows.
-cudaError_t launch_gemm(bool mx, int bn, int epi, const CUtensorMap &ta, const CUtensorMap &tb,
+cudaError_t launch_gemm(int fmt, int bn, int epi, const CUtensorMap &ta, const CUtensorMap &tb,
                         const GemmArgs &args, int grid, cudaStream_t s);
 
 // The MXFP8 gate/up GEMM with SwiGLU epilogue fed by the ring (args.ring):

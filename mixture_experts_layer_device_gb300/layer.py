@@ -6,7 +6,7 @@ library's CUDA kernels; torch only allocates memory and provides the stream.
 """
 import torch
 
-from . import (MOE_BF16, MOE_FLAG_BACKWARD, MOE_MXFP8, check, config, moe_backward, moe_buffer_info,
+from . import (DTYPES, MOE_FLAG_BACKWARD, check, config, moe_backward, moe_buffer_info,
                moe_forward, moe_get_status, moe_padded_rows, moe_prepare_weights,
                moe_router_backward, moe_router_forward, moe_saved_bytes, moe_transpose_bf16,
                moe_workspace_bytes, weights)
@@ -39,10 +39,11 @@ class MoELayer:
         self.T, self.d, self.m, self.E, self.k = T, d, m, E, k
         self.fmt = fmt
         self.mx = fmt == "mxfp8"
+        self.nv = fmt == "nvfp4"          # forward only
         self.ms = 0 if shared is None else shared[1].shape[1]
         self.backward_enabled = backward
         self.device = device
-        self.cfg = config(T, d, m, E, k, self.ms, MOE_MXFP8 if self.mx else MOE_BF16,
+        self.cfg = config(T, d, m, E, k, self.ms, DTYPES[fmt],
                           (MOE_FLAG_BACKWARD if backward else 0) | flags, ring_rows, gather_sms, aux_alpha)
         self.Rp = moe_padded_rows(self.cfg)
         self.ws = _u8(moe_workspace_bytes(self.cfg), device)
@@ -53,7 +54,14 @@ class MoELayer:
     def _prepare(self, expert, shared, stacked=None):
         d, m, E, dev = self.d, self.m, self.E, self.device
         t = {}
-        if self.mx:
+        if self.nv:
+            t["gu"] = torch.empty((E * 2 * m, d // 2), dtype=torch.uint8, device=dev)
+            t["gu_scale"] = torch.empty((E * 2 * m * d // 16,), dtype=torch.uint8, device=dev)
+            t["dn"] = torch.empty((E * d, m // 2), dtype=torch.uint8, device=dev)
+            t["dn_scale"] = torch.empty((E * d * m // 16,), dtype=torch.uint8, device=dev)
+            t["gu_gscale"] = torch.empty((E,), dtype=torch.float32, device=dev)
+            t["dn_gscale"] = torch.empty((E,), dtype=torch.float32, device=dev)
+        elif self.mx:
             t["gu"] = torch.empty((E * 2 * m, d), dtype=torch.uint8, device=dev)
             t["gu_scale"] = torch.empty((E * 2 * m * d // 32,), dtype=torch.uint8, device=dev)
             t["dn"] = torch.empty((E * d, m), dtype=torch.uint8, device=dev)
@@ -74,7 +82,7 @@ class MoELayer:
         if stacked is not None:
             gu, dn = (w.contiguous() for w in stacked)
             assert gu.shape == (E, 2 * m, d) and dn.shape == (E, d, m)
-            if self.mx:
+            if self.mx or self.nv:
                 self.prepare_stacked(gu, dn)
             else:
                 t["gu"].copy_(gu)
@@ -87,10 +95,8 @@ class MoELayer:
             assert gu.is_cuda and gu.dtype == torch.bfloat16 and gu.shape == (2 * m, d)
             assert dn.is_cuda and dn.dtype == torch.bfloat16 and dn.shape == (d, m)
             gu, dn = gu.contiguous(), dn.contiguous()
-            if self.mx:
-                # one expert: codes into its slice of the operands, canonical scales
-                # into scratch, then into its slice of the prepared scales
-                self._s0_mx(gu, dn, 1, e * gsz, e * dsz, None)
+            if self.mx or self.nv:
+                self._s0_q(gu, dn, 1, e, None)      # one expert into its slices of the operands
             else:
                 t["gu"][e].copy_(gu)
                 t["dn"][e].copy_(dn)
@@ -111,25 +117,30 @@ class MoELayer:
 
     def prepare_stacked(self, gu, dn, stream=None):
         """S0 for all experts from stacked bf16 masters (W_gu [E, 2m, d],
-        W_dn [E, d, m]) into this layer's MXFP8 operands: one launch per
-        master, which also writes the backward's transposed copies of a
-        training layer.  Re-run after every update of the masters."""
-        self._s0_mx(gu, dn, self.E, 0, 0, stream)
+        W_dn [E, d, m]) into this layer's MXFP8 or NVFP4 operands: one read of
+        each master, which for an MXFP8 training layer also writes the
+        backward's transposed copies.  Re-run after every update of the
+        masters."""
+        self._s0_q(gu, dn, self.E, 0, stream)
 
-    def _s0_mx(self, gu, dn, n, off_gu, off_dn, stream):
-        """MXFP8 S0 of n experts' masters (gu [n, 2m, d], dn [n, d, m]) straight
-        into the operands (codes and prepared scales) at element offsets off_gu /
-        off_dn: one moe_prepare_weights call, which for a training layer also
-        writes the backward orientation from the same read of each master."""
+    def _s0_q(self, gu, dn, n, e0, stream):
+        """S0 of n experts' masters (gu [n, 2m, d], dn [n, d, m]) straight into
+        the operands of experts e0 .. e0 + n - 1 (codes, prepared scales and,
+        with NVFP4, the second-level scales): one moe_prepare_weights call."""
         d, m, t, c = self.d, self.m, self.tensors, self.cfg
         cfg = c if n == self.E else config(c.T, d, m, n, 1, c.m_shared, c.dtype, 0)
-        bw = self.backward_enabled
-        check(moe_prepare_weights(cfg, gu, dn, t["gu"].view(-1)[off_gu:], t["gu_scale"][off_gu // 32:],
-                                  t["dn"].view(-1)[off_dn:], t["dn_scale"][off_dn // 32:],
-                                  t["gu_t"].view(-1)[off_gu:] if bw else None,
-                                  t["gu_t_scale"][off_gu // 32:] if bw else None,
-                                  t["dn_t"].view(-1)[off_dn:] if bw else None,
-                                  t["dn_t_scale"][off_dn // 32:] if bw else None, stream))
+        eb = 0.5 if self.nv else 1                      # code bytes per element
+        sb = 16 if self.nv else 32                      # elements per scale byte
+        og, od = e0 * 2 * m * d, e0 * d * m             # element offsets of the expert's matrices
+        bw = self.backward_enabled and self.mx
+        check(moe_prepare_weights(cfg, gu, dn, t["gu"].view(-1)[int(og * eb):], t["gu_scale"][og // sb:],
+                                  t["dn"].view(-1)[int(od * eb):], t["dn_scale"][od // sb:],
+                                  t["gu_t"].view(-1)[og:] if bw else None,
+                                  t["gu_t_scale"][og // 32:] if bw else None,
+                                  t["dn_t"].view(-1)[od:] if bw else None,
+                                  t["dn_t_scale"][od // 32:] if bw else None,
+                                  t["gu_gscale"][e0:] if self.nv else None,
+                                  t["dn_gscale"][e0:] if self.nv else None, stream))
 
     def prepare_from(self, gu, dn, s_gu=None, s_dn=None, stream=None):
         """Re-derive every operand the kernels read from the current bf16
@@ -138,7 +149,7 @@ class MoELayer:
         copies and transposes.  Run after every update of the masters."""
         E, d, m, t = self.E, self.d, self.m, self.tensors
         gu, dn = gu.contiguous(), dn.contiguous()
-        if self.mx:
+        if self.mx or self.nv:
             self.prepare_stacked(gu, dn, stream)
         else:
             t["gu"].copy_(gu)
