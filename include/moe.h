@@ -68,7 +68,9 @@ typedef enum {
   MOE_ERR_ALIGN = -3,   /* a pointer is not 16-byte aligned */
   MOE_ERR_CUDA = -4,    /* a CUDA runtime / driver call or a launch failed */
   MOE_ERR_DEVICE = -5,  /* current device is not sm_103 / sm_100 family */
-  MOE_ERR_TIMEOUT = -6  /* device side: a bounded wait inside a kernel ran out */
+  MOE_ERR_TIMEOUT = -6, /* device side: a bounded wait inside a kernel ran out */
+  MOE_ERR_BOUNDS = -7   /* device side, debug builds only (compiled with -DMOE_DEBUG): an index
+                           read from a buffer fell outside its range; the access was skipped */
 } moe_status;
 
 /* moe_config.flags bits */
@@ -377,8 +379,9 @@ int moe_route_noalloc(const moe_config *cfg, const float *logits, int32_t *idx, 
                       int32_t *counts, int32_t *offsets, int32_t *perm, moe_stream_t stream);
 
 /* Synchronises `stream`, returns the device status word recorded in `ws`
- * (MOE_OK or MOE_ERR_TIMEOUT) and clears it.  Returns MOE_ERR_CUDA if the
- * stream reports a CUDA error. */
+ * (MOE_OK, MOE_ERR_TIMEOUT, or in a debug build MOE_ERR_BOUNDS; a timeout is
+ * reported first when both happened) and clears it.  Returns MOE_ERR_CUDA if
+ * the stream reports a CUDA error. */
 int moe_get_status(void *ws, moe_stream_t stream);
 
 /* Static description of a status code (never NULL). */

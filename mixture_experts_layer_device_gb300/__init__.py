@@ -12,7 +12,9 @@ import os
 
 from . import build as _build
 
-LIB_PATH = _build.LIB
+# MOE_GB300_LIB names another build of the library (e.g. the bounds-checked
+# debug build, build.build(debug=True)) for this process.
+LIB_PATH = os.environ.get("MOE_GB300_LIB") or _build.LIB
 
 MOE_BF16, MOE_MXFP8, MOE_NVFP4 = 0, 1, 2
 DTYPES = {"bf16": MOE_BF16, "mxfp8": MOE_MXFP8, "nvfp4": MOE_NVFP4}
@@ -20,7 +22,8 @@ MOE_FLAG_BACKWARD = 1
 MOE_FLAG_DEBUG_STARVE = 2
 MOE_FLAG_DEBUG_DUMP = 4
 STATUS = {0: "ok", -1: "invalid argument", -2: "unsupported shape", -3: "pointer not 16-byte aligned",
-          -4: "CUDA error", -5: "device is not sm_103", -6: "a device-side wait timed out"}
+          -4: "CUDA error", -5: "device is not sm_103", -6: "a device-side wait timed out",
+          -7: "a device-side bounds check failed (debug build)"}
 
 WEIGHT_FIELDS = ["gu", "gu_scale", "dn", "dn_scale", "gu_t", "gu_t_scale", "dn_t", "dn_t_scale",
                  "s_gu", "s_dn", "s_gu_t", "s_dn_t", "gu_gscale", "dn_gscale"]

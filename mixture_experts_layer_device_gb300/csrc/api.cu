@@ -375,6 +375,16 @@ int run_pair(const Gemm &q, const DeviceInfo &dev, cudaStream_t s) {
 }
 
 int gemm_fmt(const Gemm &q) { return q.nv ? moe::FMT_NVFP4 : (q.mx ? moe::FMT_MXFP8 : moe::FMT_BF16); }
+// The GEMM's arguments with the output rows and the scale buffers' sizes (the
+// latter for the bounds checks of debug builds).
+moe::GemmArgs launch_args(const Gemm &q) {
+  moe::GemmArgs g = q.g;
+  g.out_rows = q.out_rows;
+  const long blk = q.nv ? 16 : 32;
+  g.sfa_bytes = (q.a_rows + 127) / 128 * 128 * q.K / blk;
+  g.sfb_bytes = (q.b_rows + 127) / 128 * 128 * q.K / blk;
+  return g;
+}
 // Elements of the tensor maps' inner dimension: NVFP4 rows hold two codes per byte.
 uint64_t map_inner(const Gemm &q) { return q.nv ? q.K / 2 : q.K; }
 
@@ -383,8 +393,7 @@ int run_gemm(const char *name, const Gemm &q, const DeviceInfo &dev, cudaStream_
   if (use_pair(q) && (q.g.sched != moe::SCHED_GROUP_K || (q.g.M / 128) % 2 == 0)) return run_pair(q, dev, s);
   CUtensorMap tb;
   if (!make_map(&tb, q.b, q.mx, map_inner(q), q.b_rows)) return MOE_ERR_CUDA;
-  moe::GemmArgs g = q.g;
-  g.out_rows = q.out_rows;
+  moe::GemmArgs g = launch_args(q);
   if (q.zero_dst) {
     const int rc = cuda_status(moe::launch_zero_empty_experts(q.zero_dst, q.g.E, q.zero_expert_bytes,
                                                               q.zero_counts, s));
@@ -402,8 +411,7 @@ int run_gemm(const char *name, const Gemm &q, const DeviceInfo &dev, cudaStream_
 int run_gemm_single(const Gemm &q, const DeviceInfo &dev, cudaStream_t s) {
   CUtensorMap ta, tb;
   if (!make_map(&ta, q.a, q.mx, q.K, q.a_rows) || !make_map(&tb, q.b, q.mx, q.K, q.b_rows)) return MOE_ERR_CUDA;
-  moe::GemmArgs g = q.g;
-  g.out_rows = q.out_rows;
+  moe::GemmArgs g = launch_args(q);
   const long grid = q.max_tiles < dev.num_sms ? q.max_tiles : dev.num_sms;
   return cuda_status(moe::launch_gemm(gemm_fmt(q), q.bn, q.epi, ta, tb, g, static_cast<int>(grid), s));
 }
@@ -417,8 +425,7 @@ int run_gemm_ring(const char *name, const Gemm &q, const Dims &D, const DeviceIn
   int grid = moe::ring_max_ctas();
   if (grid > dev.num_sms) grid = dev.num_sms;
   if (grid < 2) return MOE_ERR_CUDA;
-  moe::GemmArgs g = q.g;
-  g.out_rows = q.out_rows;
+  moe::GemmArgs g = launch_args(q);
   g.ring.gather_ctas = D.gather_ctas < grid ? D.gather_ctas : grid / 2;
   return cuda_status(moe::launch_gemm_ring(ta, tb, g, grid, s));
 }
@@ -430,7 +437,7 @@ struct Ptrs {
   int *status;
 };
 
-Ptrs route_ptrs(const Layout &L, void *base, void *ws, const Layout &W) {
+Ptrs route_ptrs(const Dims &D, const Layout &L, void *base, void *ws, const Layout &W) {
   Ptrs p;
   p.rb.idx = reinterpret_cast<int *>(L.ptr(base, "idx"));
   p.rb.w = reinterpret_cast<float *>(L.ptr(base, "w"));
@@ -442,6 +449,10 @@ Ptrs route_ptrs(const Layout &L, void *base, void *ws, const Layout &W) {
   p.rb.hist = reinterpret_cast<int *>(W.ptr(ws, "hist"));
   p.rb.tile_order = reinterpret_cast<int *>(W.ptr(ws, "tile_order"));
   p.status = reinterpret_cast<int *>(W.ptr(ws, "status"));
+  p.rb.n_tok = D.T;
+  p.rb.n_slots = D.R;
+  p.rb.n_rows = D.Rp;
+  p.rb.status = p.status;
   return p;
 }
 
@@ -651,7 +662,7 @@ int moe_route(const moe_config *cfg, const float *logits, int32_t *idx, float *w
   if ((rc = device_info(&dev)) != MOE_OK) return rc;
   Layout W;
   ws_layout(D, W);
-  Ptrs p = route_ptrs(W, ws, ws, W);
+  Ptrs p = route_ptrs(D, W, ws, ws, W);
   if (idx) p.rb.idx = idx;
   if (w) p.rb.w = w;
   if (counts) p.rb.counts = counts;
@@ -684,7 +695,7 @@ int moe_forward(const moe_config *cfg, const void *x, const float *logits, const
   const bool train = saved != nullptr;
   const Layout &RL = train ? S : W;
   void *rbase = train ? saved : ws;
-  Ptrs p = route_ptrs(RL, rbase, ws, W);
+  Ptrs p = route_ptrs(D, RL, rbase, ws, W);
   const RouteBufs &rb = p.rb;
   if (cudaMemsetAsync(p.status, 0, 4, s) != cudaSuccess) return MOE_ERR_CUDA;
 
@@ -921,7 +932,7 @@ int moe_backward(const moe_config *cfg, const void *dy, const void *x, const moe
   Layout W, S;
   ws_layout(D, W);
   saved_layout(D, S);
-  Ptrs p = route_ptrs(S, saved, ws, W);
+  Ptrs p = route_ptrs(D, S, saved, ws, W);
   const RouteBufs &rb = p.rb;
   const int *nrows_dev = rb.poff + D.E;
   const bool mx = D.mx;
@@ -1331,7 +1342,8 @@ int moe_get_status(void *ws, moe_stream_t stream) {
   int v = 0;
   if (cudaMemcpy(&v, ws, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
   if (cudaMemset(ws, 0, 4) != cudaSuccess) return MOE_ERR_CUDA;
-  return (v & moe::kStatusTimeout) ? MOE_ERR_TIMEOUT : MOE_OK;
+  if (v & moe::kStatusTimeout) return MOE_ERR_TIMEOUT;
+  return (v & moe::kStatusBounds) ? MOE_ERR_BOUNDS : MOE_OK;
 }
 
 int moe_trace_enable(int capacity) {
@@ -1377,6 +1389,7 @@ const char *moe_status_string(int status) {
     case MOE_ERR_CUDA: return "CUDA error";
     case MOE_ERR_DEVICE: return "device is not sm_103";
     case MOE_ERR_TIMEOUT: return "a device-side wait timed out";
+    case MOE_ERR_BOUNDS: return "a device-side bounds check failed (debug build)";
     default: return "unknown status";
   }
 }

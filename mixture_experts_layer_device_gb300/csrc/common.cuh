@@ -34,6 +34,21 @@ MOE_DEV unsigned long long globaltimer() {
 
 
 
+// ---------------------------------------------------------------- debug bounds checks
+// Debug builds (-DMOE_DEBUG) check indices read from buffers (schedule arrays,
+// tile coordinates) against the range they must fall in before they are used;
+// a failed check is recorded in the status word (kStatusBounds) and the access
+// is skipped or clamped.  Release builds compile the checks away.
+MOE_DEV bool bounds_ok(bool ok, int *status) {
+  if (!ok && status) atomicOr(status, kStatusBounds);
+  return ok;
+}
+#ifdef MOE_DEBUG
+#define MOE_BOUNDS_OK(cond, status) ::moe::bounds_ok((cond), (status))
+#else
+#define MOE_BOUNDS_OK(cond, status) true
+#endif
+
 // ---------------------------------------------------------------- mbarrier
 MOE_DEV void mbar_init(uint64_t *bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));

@@ -43,7 +43,9 @@ MOE_DEV int token_of_row(const RouteBufs &b, int E, int k, int pr, int *slot_out
   const int e = expert_of_row(b.poff, E, pr);
   const int local = pr - __ldg(b.poff + e);
   if (local >= __ldg(b.counts + e)) return -1;
+  if (!MOE_BOUNDS_OK(local >= 0 && __ldg(b.offsets + e) + local < b.n_slots, b.status)) return -1;
   const int slot = __ldg(b.inv + __ldg(b.offsets + e) + local);
+  if (!MOE_BOUNDS_OK(slot >= 0 && slot < b.n_slots && slot / k < b.n_tok, b.status)) return -1;
   if (slot_out) *slot_out = slot;
   return slot / k;
 }

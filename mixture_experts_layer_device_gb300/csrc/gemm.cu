@@ -385,12 +385,16 @@ __global__ void __launch_bounds__(64 + 32 * epi_warps<EPI, BN>(), 1)
             constexpr uint32_t ab = 512u * C::SF_ATOMS;  // one stage's atoms of 128 rows, contiguous
             uint8_t *sfs = sf_base + stage * C::SF_STAGE;
             const int kg = NV ? kc >> 6 : kc >> 7;
-            bulk_load(sfs, g.sfa + (static_cast<size_t>(a_row >> 7) * g.sfa_kg + kg) * 512, ab, &full[stage]);
-            bulk_load(sfs + ab, g.sfb + (static_cast<size_t>(ti.b_row0 >> 7) * g.sfb_kg + kg) * 512, ab,
-                      &full[stage]);
-            if (BN == 256)
-              bulk_load(sfs + 2 * ab, g.sfb + (static_cast<size_t>(ti.b_row1 >> 7) * g.sfb_kg + kg) * 512, ab,
-                        &full[stage]);
+            size_t oa = (static_cast<size_t>(a_row >> 7) * g.sfa_kg + kg) * 512;
+            size_t ob0 = (static_cast<size_t>(ti.b_row0 >> 7) * g.sfb_kg + kg) * 512;
+            size_t ob1 = (static_cast<size_t>(ti.b_row1 >> 7) * g.sfb_kg + kg) * 512;
+            // debug builds: a scale atom past its buffer is recorded and read from offset 0
+            if (!MOE_BOUNDS_OK(oa + ab <= static_cast<size_t>(g.sfa_bytes), g.status)) oa = 0;
+            if (!MOE_BOUNDS_OK(ob0 + ab <= static_cast<size_t>(g.sfb_bytes), g.status)) ob0 = 0;
+            if (BN == 256 && !MOE_BOUNDS_OK(ob1 + ab <= static_cast<size_t>(g.sfb_bytes), g.status)) ob1 = 0;
+            bulk_load(sfs, g.sfa + oa, ab, &full[stage]);
+            bulk_load(sfs + ab, g.sfb + ob0, ab, &full[stage]);
+            if (BN == 256) bulk_load(sfs + 2 * ab, g.sfb + ob1, ab, &full[stage]);
           }
           if (++stage == C::STAGES) {
             stage = 0;

@@ -81,7 +81,7 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float *__restrict
 // ------------------------------------------------------------ S2: schedule
 // (a) per-chunk expert histograms (integer counts: order-independent).
 __global__ void __launch_bounds__(128) sched_hist_kernel(const int *__restrict__ idx, int R, int E,
-                                                         int nchunks, int *__restrict__ hist) {
+                                                         int nchunks, int *__restrict__ hist, int *status) {
   extern __shared__ int cnt[];
   const int wib = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c = blockIdx.x * (blockDim.x >> 5) + wib;
@@ -92,7 +92,10 @@ __global__ void __launch_bounds__(128) sched_hist_kernel(const int *__restrict__
   const int base = c * kSchedChunk;
   for (int i = lane; i < kSchedChunk; i += 32) {
     const int s = base + i;
-    if (s < R) atomicAdd(&my[__ldg(idx + s)], 1);
+    if (s < R) {
+      const int e = __ldg(idx + s);
+      if (MOE_BOUNDS_OK(e >= 0 && e < E, status)) atomicAdd(&my[e], 1);
+    }
   }
   __syncwarp();
   for (int e = lane; e < E; e += 32) hist[static_cast<size_t>(c) * E + e] = my[e];
@@ -166,7 +169,7 @@ __global__ void __launch_bounds__(128) sched_scatter_kernel(const int *__restric
                                                             const int *__restrict__ hist_excl,
                                                             const int *__restrict__ offsets,
                                                             int *__restrict__ perm,
-                                                            int *__restrict__ inv) {
+                                                            int *__restrict__ inv, int *status) {
   extern __shared__ int cnt[];
   const int wib = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c = blockIdx.x * (blockDim.x >> 5) + wib;
@@ -177,14 +180,15 @@ __global__ void __launch_bounds__(128) sched_scatter_kernel(const int *__restric
   const int base = c * kSchedChunk;
   for (int it = 0; it < kSchedChunk; it += 32) {
     const int s = base + it + lane;
-    const int e = s < R ? __ldg(idx + s) : -1;
+    int e = s < R ? __ldg(idx + s) : -1;
+    if (s < R && !MOE_BOUNDS_OK(e >= 0 && e < E, status)) e = -1;
     const unsigned peers = __match_any_sync(0xffffffffu, e);
     const int rank = __popc(peers & ((1u << lane) - 1u));
     const int row = e >= 0 ? my[e] + rank : 0;
     __syncwarp();
     if (e >= 0 && rank == 0) my[e] += __popc(peers);
     __syncwarp();
-    if (e >= 0) {
+    if (e >= 0 && MOE_BOUNDS_OK(row >= 0 && row < R, status)) {
       perm[s] = row;
       inv[row] = s;
     }
@@ -295,8 +299,11 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint4 *__restrict__ 
   if (lane < k) {
     const int slot = t * k + lane;
     const int e = __ldg(b.idx + slot);
-    my_row = __ldg(b.poff + e) + __ldg(b.perm + slot) - __ldg(b.offsets + e);
-    my_w = __ldg(b.w + slot);
+    if (MOE_BOUNDS_OK(e >= 0 && e < E, b.status)) {
+      my_row = __ldg(b.poff + e) + __ldg(b.perm + slot) - __ldg(b.offsets + e);
+      my_w = __ldg(b.w + slot);
+      if (!MOE_BOUNDS_OK(my_row >= 0 && my_row < b.n_rows, b.status)) my_row = 0, my_w = 0.f;
+    }
   }
   const int vec = d >> 3;
   for (int i = lane; i < vec; i += 32) {
@@ -544,9 +551,14 @@ __global__ void __launch_bounds__(256) reverse_dispatch_kernel(
   if (lane < k) {
     const int slot = t * k + lane;
     my_e = __ldg(b.idx + slot);
-    my_row = __ldg(b.poff + my_e) + __ldg(b.perm + slot) - __ldg(b.offsets + my_e);
-    my_w = __ldg(b.w + slot);
-    my_g = __ldg(g + slot);
+    if (MOE_BOUNDS_OK(my_e >= 0 && my_e < E, b.status)) {
+      my_row = __ldg(b.poff + my_e) + __ldg(b.perm + slot) - __ldg(b.offsets + my_e);
+      my_w = __ldg(b.w + slot);
+      my_g = __ldg(g + slot);
+      if (!MOE_BOUNDS_OK(my_row >= 0 && my_row < b.n_rows, b.status)) my_row = 0;
+    } else {
+      my_e = 0;
+    }
   }
   // dlogits: softmax-over-k gradient w_j (g_j - sum_i w_i g_i), slot order sum.
   float S = 0.f;
@@ -816,10 +828,10 @@ cudaError_t launch_route(const float *logits, int T, int E, int k, const RouteBu
   const int R = T * k;
   const int nchunks = (R + kSchedChunk - 1) / kSchedChunk;
   const size_t smem = 4 * static_cast<size_t>(E) * sizeof(int);
-  sched_hist_kernel<<<blocks_for(nchunks, 4), 128, smem, s>>>(b.idx, R, E, nchunks, b.hist);
+  sched_hist_kernel<<<blocks_for(nchunks, 4), 128, smem, s>>>(b.idx, R, E, nchunks, b.hist, b.status);
   sched_scan_kernel<<<1, 1024, 0, s>>>(b.hist, nchunks, E, b.counts, b.offsets, b.poff);
   sched_scatter_kernel<<<blocks_for(nchunks, 4), 128, smem, s>>>(b.idx, R, E, nchunks, b.hist,
-                                                                  b.offsets, b.perm, b.inv);
+                                                                  b.offsets, b.perm, b.inv, b.status);
   return cudaGetLastError();
 }
 

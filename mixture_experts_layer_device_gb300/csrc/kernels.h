@@ -10,6 +10,7 @@ namespace moe {
 
 // Device status word bits (kept in the workspace, read by moe_get_status).
 constexpr int kStatusTimeout = 1;
+constexpr int kStatusBounds = 2;  // a debug-build bounds check failed
 // Default limit of every device-side wait.
 constexpr unsigned long long kWaitTimeoutNs = 4000000000ull;
 
@@ -26,6 +27,11 @@ struct RouteBufs {
   int *poff;      // [E+1] padded offsets (multiples of 128)
   int *hist;      // [nchunks * E] scratch
   int *tile_order;  // [Rp / 32] processing order of 32-row tiles (may be NULL: row order)
+  // extents and the status word for the bounds checks of debug builds
+  int n_tok;      // T
+  long n_slots;   // T * k
+  long n_rows;    // padded rows Rp
+  int *status;    // may be NULL (nothing recorded)
 };
 
 cudaError_t launch_route(const float *logits, int T, int E, int k, const RouteBufs &b,
@@ -188,6 +194,7 @@ struct GemmArgs {
   const void *aux;    // SWIGLU_BWD: saved G|U bf16
   long ld_aux;
   int m_half;         // SWIGLU / SWIGLU_BWD: m
+  long sfa_bytes, sfb_bytes;  // sizes of the scale buffers (bounds checks of debug builds)
   const float *a_gscale;  // NVFP4: second-level scale of A (one value; NULL = 1)
   const float *b_gscale;  // NVFP4: second-level scale of B per group [E]
   float *dump;        // SWIGLU (tests): fp32 h before quantisation [rows, ld_dump] (may be NULL)

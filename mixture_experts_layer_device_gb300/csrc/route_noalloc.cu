@@ -78,6 +78,8 @@ extern "C" int moe_route_noalloc(const moe_config *cfg, const float *logits, int
   rb.hist = reinterpret_cast<int *>(b);
   rb.inv = reinterpret_cast<int *>(b + kHistBytes);
   rb.poff = reinterpret_cast<int *>(b + kHistBytes + kInvBytes);
+  rb.n_tok = cfg->T;
+  rb.n_slots = static_cast<long>(cfg->T) * cfg->k;
   return moe::launch_route(logits, cfg->T, cfg->E, cfg->k, rb, stream) == cudaSuccess ? MOE_OK
                                                                                      : MOE_ERR_CUDA;
 }

@@ -104,11 +104,12 @@ class ExpertSubset:
 
 
 def _compact(op):
-    """A prepared operand (dequantised MXFP8 or bf16 values) held in fp32, which
-    represents it exactly (checked); the oracle still computes in fp64."""
+    """A prepared operand held in fp32 where that represents it exactly
+    (dequantised MXFP8 or bf16 values), else kept in float64 (NVFP4 values are
+    divided by a second-level scale that is not a power of two); the oracle
+    computes in fp64 either way."""
     o32 = np.asarray(op, dtype=np.float32)
-    assert np.array_equal(o32.astype(np.float64), op), "prepared operand not exact in fp32"
-    return o32
+    return o32 if np.array_equal(o32.astype(np.float64), op) else np.asarray(op, dtype=np.float64)
 
 
 def prepare_subset(cfg, gu_all, dn_all, experts, backward):
