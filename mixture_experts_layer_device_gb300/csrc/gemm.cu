@@ -17,6 +17,14 @@
 //            128-row tile belongs to one expert; B is that expert's weights.
 //            Tiles of one expert are consecutive (m-tile major), which keeps
 //            the expert's weight panel hot in L2 while its rows stream.
+//            When the load is bimodal -- a few experts with many m-tiles and
+//            the rest with one or two -- the light experts' tiles (which
+//            stream their weight panel from HBM for at most 256 rows) are
+//            spread evenly among the heavy experts' tiles (which re-read
+//            theirs from L2), each kind still in expert order, so HBM streams
+//            while the tensor cores work; their B loads carry L2 evict-first
+//            and the heavy experts' evict-last, so the streamed panels do not
+//            push the heavy panels out of L2.
 //   DENSE    one group (shared expert).
 //   GROUP_K  weight gradients: the reduction runs over one expert's padded
 //            rows [poff[e], poff[e+1]) of two transposed operands.  An
@@ -78,13 +86,22 @@ struct Cfg {
                                  STAGING_BYTES + NBAR * 8 + 16;
   static_assert(!MX || SF_COL0 + STAGES * SF_COLS <= 512, "TMEM columns");
   static_assert(NUM_ACC * BN <= 512, "TMEM columns");
-  static_assert(SMEM <= 232448, "shared memory");
+  // dynamic + the kernel's static shared memory (the interleave tables)
+  static_assert(SMEM + 8 * 1025 + 16 <= 232448, "shared memory");
 };
 
 struct Tile {
   int a_row, k0, nk, b_row0, b_row1, out_row, out_col;
   int e;  // group (expert) of the tile
+  bool light;  // GROUP_M, interleaved order: a light expert's tile
 };
+
+// Interleaved GROUP_M order: experts with fewer than kLightMTiles m-tiles are
+// light; it is used when every other active expert has at least
+// kHeavyMinMTiles m-tiles (a bimodal load) and E <= kMaxInterleaveE.
+constexpr int kLightMTiles = 3;
+constexpr int kHeavyMinMTiles = 16;
+constexpr int kMaxInterleaveE = 1024;
 
 template <int BK, int BN, int EPI>
 MOE_DEV int total_tiles(const GemmArgs &g) {
@@ -93,12 +110,41 @@ MOE_DEV int total_tiles(const GemmArgs &g) {
   return g.E * (g.M >> 7) * g.n_tiles;
 }
 
+// il (GROUP_M, interleaved order, else NULL): the exclusive prefix sums of the
+// heavy experts' m-tiles [E + 1] followed by the light experts' [E + 1].  Tile
+// t is light when floor((t + 1) L / T) > floor(t L / T) (T tiles, L of them
+// light), so the light tiles are spread evenly; the number before t indexes the
+// light order, the rest the heavy order.
 template <int BK, int BN, int EPI>
-MOE_DEV Tile decode_tile(const GemmArgs &g, int t) {
+MOE_DEV Tile decode_tile(const GemmArgs &g, int t, const int *il) {
   Tile ti;
+  ti.light = false;
   const int nt = g.n_tiles;
   int e = 0, mt, ntile;
-  if (g.sched == SCHED_GROUP_M) {
+  if (g.sched == SCHED_GROUP_M && il) {
+    const int *hoff = il, *loff = il + g.E + 1;
+    const long LT = static_cast<long>(loff[g.E]) * nt;
+    const long TT = static_cast<long>(hoff[g.E] + loff[g.E]) * nt;
+    const long j0 = static_cast<long>(t) * LT / TT;
+    const long j1 = static_cast<long>(t + 1) * LT / TT;
+    ti.light = j1 > j0;
+    const int idx = ti.light ? static_cast<int>(j0) : t - static_cast<int>(j0);
+    const int *off = ti.light ? loff : hoff;
+    const int lm = idx / nt;
+    ntile = idx % nt;
+    int lo = 0, hi = g.E - 1;  // the last expert whose range starts at or before lm
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (off[mid] <= lm) lo = mid;
+      else hi = mid - 1;
+    }
+    e = lo;
+    mt = lm - off[e];
+    ti.a_row = ((__ldg(g.poff + e) >> 7) + mt) * 128;
+    ti.k0 = 0;
+    ti.nk = g.K / BK;
+    ti.out_row = ti.a_row;
+  } else if (g.sched == SCHED_GROUP_M) {
     int lo = 0, hi = g.E - 1;
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
@@ -340,6 +386,47 @@ __global__ void __launch_bounds__(64 + 32 * epi_warps<EPI, BN>(), 1)
     *abort_flag = 0;
     fence_mbar_init();
   }
+  // Interleaved GROUP_M order: prefix sums of the heavy and light experts'
+  // m-tiles and the bimodality test, by one epilogue warp before the roles
+  // split (the ring's tiles keep expert order).
+  __shared__ int il_off[2 * (kMaxInterleaveE + 1)];
+  __shared__ int il_on;
+  if (warp == 2) {
+    bool on = false;
+    if (!RING && g.sched == SCHED_GROUP_M && g.E <= kMaxInterleaveE) {
+      int runh = 0, runl = 0, min_heavy = 1 << 30;
+      for (int base = 0; base < g.E; base += 32) {
+        const int e = base + lane;
+        const int c = e < g.E ? (__ldg(g.poff + e + 1) >> 7) - (__ldg(g.poff + e) >> 7) : 0;
+        const int ch = c >= kLightMTiles ? c : 0;
+        const int cl = c >= kLightMTiles ? 0 : c;
+        int ih = ch, il_inc = cl, mn = ch > 0 ? ch : (1 << 30);
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int a = __shfl_up_sync(0xffffffffu, ih, o);
+          const int b = __shfl_up_sync(0xffffffffu, il_inc, o);
+          if (lane >= o) {
+            ih += a;
+            il_inc += b;
+          }
+          mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+        }
+        if (e < g.E) {
+          il_off[e] = runh + ih - ch;
+          il_off[g.E + 1 + e] = runl + il_inc - cl;
+        }
+        runh += __shfl_sync(0xffffffffu, ih, 31);
+        runl += __shfl_sync(0xffffffffu, il_inc, 31);
+        min_heavy = min(min_heavy, mn);
+      }
+      if (lane == 0) {
+        il_off[g.E] = runh;
+        il_off[2 * g.E + 1] = runl;
+      }
+      on = runh > 0 && runl > 0 && min_heavy >= kHeavyMinMTiles;
+    }
+    if (lane == 0) il_on = on ? 1 : 0;
+  }
   if (warp == 1) {
     tmem_alloc(tmem_slot, C::TMEM_COLS);
     tmem_relinquish();
@@ -348,6 +435,7 @@ __global__ void __launch_bounds__(64 + 32 * epi_warps<EPI, BN>(), 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  const int *il = il_on ? il_off : nullptr;
   const int total = total_tiles<C::BK, BN, EPI>(g);
 
   if (warp == 0) {
@@ -360,7 +448,7 @@ __global__ void __launch_bounds__(64 + 32 * epi_warps<EPI, BN>(), 1)
       int armed[C::STAGES];
       for (int s = 0; s < C::STAGES; ++s) armed[s] = -1;
       for (int i = cta; i < total && !*abort_flag && (RING || !g.debug_starve); i += ncta) {
-        const Tile ti = decode_tile<C::BK, BN, EPI>(g, i);
+        const Tile ti = decode_tile<C::BK, BN, EPI>(g, i, il);
         int a_row = ti.a_row;  // row of A to load (the tile's ring slot with a ring)
         if constexpr (RING) {
           const int u = ti.a_row >> 7;
@@ -379,8 +467,14 @@ __global__ void __launch_bounds__(64 + 32 * epi_warps<EPI, BN>(), 1)
           const int kc = ti.k0 + kb * C::BK;
           const int kx = NV ? kc / 2 : kc;  // tensor-map coordinate: NVFP4 maps count bytes
           tma_load_2d(&tmA, &full[stage], sa, kx, a_row);
-          tma_load_2d(&tmB, &full[stage], sb, kx, ti.b_row0);
-          if (BN == 256) tma_load_2d(&tmB, &full[stage], sb + 128 * 128, kx, ti.b_row1);
+          if (il) {  // interleaved: streamed light panels leave L2 first
+            const uint64_t pol = ti.light ? l2_policy_evict_first() : l2_policy_evict_last();
+            tma_load_2d_hint(&tmB, &full[stage], sb, kx, ti.b_row0, pol);
+            if (BN == 256) tma_load_2d_hint(&tmB, &full[stage], sb + 128 * 128, kx, ti.b_row1, pol);
+          } else {
+            tma_load_2d(&tmB, &full[stage], sb, kx, ti.b_row0);
+            if (BN == 256) tma_load_2d(&tmB, &full[stage], sb + 128 * 128, kx, ti.b_row1);
+          }
           if constexpr (MX) {
             constexpr uint32_t ab = 512u * C::SF_ATOMS;  // one stage's atoms of 128 rows, contiguous
             uint8_t *sfs = sf_base + stage * C::SF_STAGE;
@@ -418,7 +512,7 @@ __global__ void __launch_bounds__(64 + 32 * epi_warps<EPI, BN>(), 1)
       uint32_t aph = 0;
       bool ok = true;
       for (int i = cta; i < total && ok; i += ncta) {
-        const Tile ti = decode_tile<C::BK, BN, EPI>(g, i);
+        const Tile ti = decode_tile<C::BK, BN, EPI>(g, i, il);
         if (ti.nk == 0 && g.skip_empty) continue;  // zeros written by another launch
         if (!mbar_wait(&tempty[acc], aph ^ 1u, abort_flag, g.status, g.timeout_ns)) break;
         tc_fence_after();
@@ -494,7 +588,7 @@ __global__ void __launch_bounds__(64 + 32 * epi_warps<EPI, BN>(), 1)
     int acc = 0;
     uint32_t aph = 0;
     for (int i = cta; i < total; i += ncta) {
-      const Tile ti = decode_tile<C::BK, BN, EPI>(g, i);
+      const Tile ti = decode_tile<C::BK, BN, EPI>(g, i, il);
       if (ti.nk == 0 && g.skip_empty) continue;  // zeros written by another launch
       if constexpr (EPI == EPI_SWIGLU_BWD) {
         // The saved G|U rows this tile's epilogue reads come from HBM: pull them
