@@ -41,6 +41,16 @@ NOMINAL = {"hbm_gbs": 7900.0, "bf16_tflops": 2250.0, "mx_tflops": 4500.0, "nv_tf
 # ncu capture, keyed by (workload, kernel).  An entry is removed whenever the
 # kernel changes after the capture.
 NCU_TRAFFIC = {
+    # full-size launches of the timed step, one-pass capture of dram__bytes_read.sum and
+    # dram__bytes_write.sum; the gate/up wgrad is the empty experts' zero fill plus the GEMM
+    ("kimi-k2.7", "wgrad_gate_up"): (91_904 + 8_860_727_040) + (4_866_291_456 + 13_564_775_424),
+    ("kimi-k2.7", "wgrad_down"): (819_456 + 4_397_618_944) + (1_653_164_800 + 6_752_859_904),
+    ("kimi-k2.7", "gemm1_gate_up_swiglu"): 8_762_271_744 + 1_974_972_416,
+    ("kimi-k2.7", "dgrad_gate_up"): 7_788_438_016 + 2_209_938_688,
+    ("kimi-k2.7", "dgrad_down_swiglu_bwd"): 6_789_948_160 + 1_518_551_552,
+    ("kimi-k2.7", "gemm2_down"): 3_840_576_256 + 2_204_741_632,
+    ("deepseek-v4-pro", "gemm1_gate_up_swiglu"): 23_420_308_992 + 679_740_928,
+    ("deepseek-v4-pro", "gemm2_down"): 9_990_749_440 + 2_930_241_792,
 }
 
 
@@ -61,6 +71,20 @@ def workload(name):
     return cfg
 
 
+def active_experts(cfg):
+    """Experts that receive rows (the step's routing, set by the bench after its
+    warm-up; all E before): only their weights are read.  Every expert's dW is
+    written, zeros for the empty ones."""
+    return cfg.get("E_active", cfg["E"])
+
+
+def experts_with_rows(layer, which):
+    """Experts the layer's last routing gave rows to (its per-expert counts in
+    `saved`, which=0, after a training forward, else in the workspace)."""
+    counts = layer.view(which, "counts", "i32", (layer.E,))
+    return int((counts > 0).sum().item())
+
+
 def layer_work(cfg, passes):
     """Algorithmic FLOPs (split by arithmetic) and bytes of one step."""
     T, d, m, E, k, ms = (cfg[n] for n in ("T", "d", "m", "E", "k", "m_shared"))
@@ -70,7 +94,7 @@ def layer_work(cfg, passes):
     fl_exp = 6.0 * d * m * R * mult
     fl_sh = 6.0 * d * ms * T * mult
     wb = elem_bytes(cfg)                             # stored bytes per weight element
-    wts = E * 3 * d * m * wb
+    wts = active_experts(cfg) * 3 * d * m * wb
     byt = wts + T * d * 2 + T * E * 4 + T * d * 2 + (3 * d * ms * 2 if ms else 0)
     if passes == "fwdbwd":
         byt += wts if mx else 0                      # backward operand copies
@@ -99,17 +123,18 @@ def kernel_work(cfg, name, train=False):
     gate/up GEMM of a training pass saves G|U in bf16 and, with MXFP8, h as
     row- and column-blocked codes (with BF16, h in bf16)."""
     T, d, m, E, k, ms = (cfg[n] for n in ("T", "d", "m", "E", "k", "m_shared"))
+    Ea = active_experts(cfg)               # weights read: experts with rows only
     R = T * k
     mx = cfg["fmt"] in ("mxfp8", "nvfp4")  # block-scaled expert operands
     a = elem_bytes(cfg)                    # bytes per stored expert operand element
     h_out = (R * 2 * m * 2 + (2 * R * m * a if mx else R * m * 2)) if train else R * m * a
     sh_out = (T * 2 * ms * 2 + T * ms * 2) if train else T * ms * 2
     tbl = {
-        "gemm1_gate_up_swiglu": (2.0 * R * 2 * m * d, R * d * a + E * 2 * m * d * a + h_out, mx),
-        "gemm2_down": (2.0 * R * d * m, R * m * a + E * d * m * a + R * d * 2, mx),
-        "dgrad_down_swiglu_bwd": (2.0 * R * m * d, R * d * a + E * m * d * a + R * 2 * m * 2 * 2
+        "gemm1_gate_up_swiglu": (2.0 * R * 2 * m * d, R * d * a + Ea * 2 * m * d * a + h_out, mx),
+        "gemm2_down": (2.0 * R * d * m, R * m * a + Ea * d * m * a + R * d * 2, mx),
+        "dgrad_down_swiglu_bwd": (2.0 * R * m * d, R * d * a + Ea * m * d * a + R * 2 * m * 2 * 2
                                   + (R * 2 * m * a if mx else 0), mx),
-        "dgrad_gate_up": (2.0 * R * d * 2 * m, R * 2 * m * a + E * d * 2 * m * a + R * d * 2, mx),
+        "dgrad_gate_up": (2.0 * R * d * 2 * m, R * 2 * m * a + Ea * d * 2 * m * a + R * d * 2, mx),
         "wgrad_down": (2.0 * R * d * m, R * d * a + R * m * a + E * d * m * 2, mx),
         "wgrad_gate_up": (2.0 * R * 2 * m * d, R * 2 * m * a + R * d * a + E * 2 * m * d * 2, mx),
         "shared_gemm1_gate_up_swiglu": (2.0 * T * 2 * ms * d, T * d * 2 + 2 * ms * d * 2 + sh_out, False),
@@ -122,7 +147,7 @@ def kernel_work(cfg, name, train=False):
         # ring: dispatch + gate/up GEMM in one launch; the ring itself stays on chip (L2)
         "quantize_tokens": (0.0, T * d * 2 + T * d * a, mx),
         "dispatch_xT": (0.0, T * d * 2 + R * d * a, mx),
-        "dispatch_gemm1_ring": (2.0 * R * 2 * m * d, T * d * a + E * 2 * m * d * a + h_out, mx),
+        "dispatch_gemm1_ring": (2.0 * R * 2 * m * d, T * d * a + Ea * 2 * m * d * a + h_out, mx),
         "combine": (0.0, R * d * 2 + R * 8 + T * d * 2 * (2 if ms else 1), mx),
         "reverse_combine": (0.0, T * d * 2 + R * d * 2 + R * 8 + (2 * R * d * a if mx else R * d * 2), mx),
         "reverse_dispatch": (0.0, R * d * 2 + R * 8 + T * d * 2 * (2 if ms else 1) + T * E * 4, mx),
@@ -309,6 +334,7 @@ def layer_roofline(cfg, passes, ms_step, P):
     t_n = roof(pk_n, NOMINAL["bf16_tflops"], NOMINAL["hbm_gbs"])[0]
     sec = ms_step / 1e3
     return {"tokens_per_s": round(cfg["T"] / t_roof, 1), "frac": round(t_roof / sec, 4),
+            "experts_with_rows": active_experts(cfg),
             "frac_sustained": round(t_s / sec, 4), "frac_nominal": round(t_n / sec, 4),
             "bound": "tensor" if t_tensor >= t_hbm else "hbm", "t_tensor_ms": round(t_tensor * 1e3, 3),
             "t_hbm_ms": round(t_hbm * 1e3, 3),
@@ -539,7 +565,7 @@ def workload_desc(cfg, bwd, layer=None):
             "experts": cfg["fmt"], "router_bias": cfg["bias"], "parallelism": "1gpu",
             "dispatch": ("ring of %d rows, %d gather SMs" % (ring, layer.cfg.gather_sms or 8)
                          if ring else "materialised"),
-            "l2": "inputs larger than L2 (%.1f GB of expert weights read per step)"
+            "l2": "inputs larger than L2 (%.1f GB of expert weights stored)"
                   % (3 * cfg["E"] * cfg["d"] * cfg["m"] * elem_bytes(cfg) / 1e9)}
 
 
@@ -640,6 +666,7 @@ def run_target(args, P):
     torch.cuda.synchronize()
     if layer.status() != 0:
         raise RuntimeError("device status after the target leg's warm-up")
+    cfg["E_active"] = experts_with_rows(layer, 1)
     clocks = Clocks(gpu_index())
     total_ms, _ = timed_region(stream, step, args.steps)
     clk = clocks.stop()
@@ -707,6 +734,7 @@ def run_ours(args, cfg, passes):
     st = layer.status()
     if st != 0:
         raise RuntimeError("device status %d after warm-up" % st)
+    cfg["E_active"] = experts_with_rows(layer, 0 if bwd else 1)
 
     def timed(fn, K, trace=False):
         return timed_region(stream, fn, K, trace)

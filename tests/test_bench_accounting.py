@@ -104,14 +104,44 @@ def test_launches_per_traced_region():
     assert bench.kernels_in_region("gemm1_gate_up_swiglu", mx, True) == 1
 
 
+def _experts_with_rows(wl):
+    """Experts the workload's routing gives rows to, from the oracle's top-k of
+    the seeded logits (the GPU's routing is bit-exact with it)."""
+    import numpy as np
+    import torch
+    import moe_inputs as mi
+    from oracle import moe as om
+    cfg = dict(mi.WORKLOADS[wl])
+    idx, _ = om.route(mi.logits(cfg, torch.device("cpu")).numpy(), cfg["k"])
+    return int((np.bincount(idx.reshape(-1), minlength=cfg["E"]) > 0).sum())
+
+
 def test_recorded_traffic_names_a_known_kernel():
+    active = {}
     for (wl, kernel), traffic in bench.NCU_TRAFFIC.items():
         cfg = bench.workload(wl)
+        if wl not in active:
+            active[wl] = _experts_with_rows(wl)
+        cfg["E_active"] = active[wl]
         w = bench.kernel_work(cfg, kernel, cfg["backward"])
         assert w is not None
         # DRAM traffic of a full-size launch: at least the algorithmic bytes
         # (less only by what L2 still holds at the end), and not wildly above
-        assert 0.95 * w[1] < traffic < 1.5 * w[1]
+        assert 0.95 * w[1] < traffic < 1.5 * w[1], (wl, kernel, traffic / w[1])
+
+
+def test_only_experts_with_rows_count_as_weight_reads():
+    """An empty expert's weights are never read; its dW is still written."""
+    cfg = bench.workload("kimi-k2.7")
+    full = {n: bench.kernel_work(cfg, n, True)[1] for n in ("gemm2_down", "wgrad_down")}
+    cfg["E_active"] = cfg["E"] - 100
+    part = {n: bench.kernel_work(cfg, n, True)[1] for n in ("gemm2_down", "wgrad_down")}
+    w = 100 * cfg["d"] * cfg["m"] * bench.elem_bytes(cfg)
+    assert full["gemm2_down"] - part["gemm2_down"] == pytest.approx(w)
+    assert full["wgrad_down"] == part["wgrad_down"]
+    fwd = bench.layer_work(cfg, "fwd")[2]
+    cfg.pop("E_active")
+    assert bench.layer_work(cfg, "fwd")[2] - fwd == pytest.approx(3 * w)
 
 
 def test_clock_records_that_reject_a_number():
