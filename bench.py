@@ -681,12 +681,44 @@ def run_target(args, P):
         raise RuntimeError("device status after the target leg")
     ms = total_ms / args.steps
     summ = summarize(cfg, False, recs, args.steps, total_ms, P, 0.0)
+    ring = ring_leg(args, cfg, P, layer, x, logits, y, stream)
     return {"note": "MXFP8 forward of the largest workload; target: layer_roofline.frac >= 0.60",
             "value": round(cfg["T"] / (ms / 1e3), 1), "unit": "tokens/s", "ms_per_step": round(ms, 4),
             "steps": args.steps, "warmup": args.warmup, "config": workload_desc(cfg, False, layer),
             "layer_roofline": layer_roofline(cfg, "fwd", ms, P), "roofline": summ["roofline"],
             "kernels": summ["kernels"], "route_schedule_share": summ["route_schedule_share"],
-            "gpu_launches": summ["gpu_launches"], "clocks": clk}
+            "gpu_launches": summ["gpu_launches"], "clocks": clk, "ring": ring}
+
+
+def ring_leg(args, cfg, P, layer, x, logits, y_ref, stream, ring_rows=8192, gather_sms=8):
+    """The same forward through the persistent ring kernel: one cooperative
+    launch in which gather SMs copy the expert-sorted rows into a ring of
+    ring_rows rows that the other SMs' gate/up GEMM consumes, so the dispatched
+    rows are never materialised.  Timed after the materialised leg, on the same
+    weights and inputs; its output must equal that leg's bit for bit."""
+    import torch
+    import mixture_experts_layer_device_gb300 as pkg
+    c = layer.cfg
+    rc = pkg.MoeConfig(c.T, c.d, c.m, c.E, c.k, c.m_shared, c.dtype, c.flags, ring_rows, gather_sms)
+    ws = torch.empty(pkg.moe_workspace_bytes(rc), dtype=torch.uint8, device=x.device)
+    y = torch.empty_like(y_ref)
+
+    def step():
+        pkg.check(pkg.moe_forward(rc, x, logits, layer.W, y, None, ws, stream))
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    total_ms, _ = timed_region(stream, step, args.steps)
+    st = pkg.moe_get_status(ws)
+    if st != 0:
+        raise RuntimeError("device status %d after the ring leg" % st)
+    ms = total_ms / args.steps
+    return {"ms_per_step": round(ms, 4), "tokens_per_s": round(cfg["T"] / (ms / 1e3), 1),
+            "ring_rows": ring_rows, "gather_sms": gather_sms,
+            "workspace_gb": round(ws.numel() / 1e9, 3), "materialised_workspace_gb": round(layer.ws.numel() / 1e9, 3),
+            "layer_roofline_frac": layer_roofline(cfg, "fwd", ms, P)["frac"],
+            "bitwise_equal_to_materialised": bool(torch.equal(y.view(torch.int16), y_ref.view(torch.int16)))}
 
 
 def run_ours(args, cfg, passes):

@@ -106,7 +106,9 @@ def test_launches_per_traced_region():
 
 def _experts_with_rows(wl):
     """Experts the workload's routing gives rows to, from the oracle's top-k of
-    the seeded logits (the GPU's routing is bit-exact with it)."""
+    logits drawn on the CPU (the bench draws the same distribution on the GPU,
+    where the count comes out a few experts higher: 232 against 225 for
+    Kimi-K2.7); close enough for the bounds below."""
     import numpy as np
     import torch
     import moe_inputs as mi
