@@ -75,6 +75,10 @@ struct Cfg {
   static constexpr int SFA_COLS = 4 * SF_ATOMS;
   static constexpr int SF_COLS = SF_ATOMS * (4 + BN / 32);
   static constexpr int SF_COL0 = NUM_ACC * BN;
+  // The SwiGLU-backward epilogue's stash of accumulator chunks 1.. (one
+  // accumulator only): the last 64 (BN / 128 - 1) x 2 columns of TMEM.
+  static constexpr bool STASH = !NV && NUM_ACC == 1 && BN / 128 > 1;  // NVFP4 has no backward
+  static constexpr int STASH_COL = 512 - 2 * 64 * (BN / 128 - 1);
   static constexpr uint32_t TX_BYTES = STAGE_BYTES + SF_STAGE;
   static constexpr uint32_t IDESC = NV ? idesc_nvf4(128, BN) : (MX ? idesc_mxf8(128, BN) : idesc_bf16(128, BN));
   // epilogue staging: 2 KB pieces (32 rows x 64 B, 64-byte swizzle), 16 KB split
@@ -85,6 +89,7 @@ struct Cfg {
   static constexpr size_t SMEM = 1024 + static_cast<size_t>(STAGES) * (STAGE_BYTES + SF_STAGE) +
                                  STAGING_BYTES + NBAR * 8 + 16;
   static_assert(!MX || SF_COL0 + STAGES * SF_COLS <= 512, "TMEM columns");
+  static_assert(!STASH || SF_COL0 + (MX ? STAGES * SF_COLS : 0) <= STASH_COL, "TMEM columns of the stash");
   static_assert(NUM_ACC * BN <= 512, "TMEM columns");
   // dynamic + the kernel's static shared memory (the interleave tables)
   static_assert(SMEM + 8 * 1025 + 16 <= 232448, "shared memory");
@@ -610,8 +615,10 @@ __global__ void __launch_bounds__(64 + 32 * epi_warps<EPI, BN>(), 1)
       };
       float sc = 1.0f;  // NVFP4: the inverse of both operands' second-level scales
       if constexpr (NV) sc = 1.0f / ((g.a_gscale ? __ldg(g.a_gscale) : 1.0f) * __ldg(g.b_gscale + ti.e));
-      epilogue_tile_split<EPI, BN, DUMP, NV>(g, vO, vO2, vQ, st, tb, ti.nk, row0, grow, ti.out_col, lane, part,
-                                             true, release, sc);
+      constexpr bool STASH = EPI == EPI_SWIGLU_BWD && C::STASH;
+      const uint32_t ts = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(C::STASH_COL);
+      epilogue_tile_split<EPI, BN, DUMP, NV, STASH>(g, vO, vO2, vQ, st, tb, ti.nk, row0, grow, ti.out_col, lane,
+                                                    part, true, release, sc, ts);
       if (++acc == C::NUM_ACC) {
         acc = 0;
         aph ^= 1u;

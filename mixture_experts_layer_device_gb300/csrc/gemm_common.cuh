@@ -314,11 +314,11 @@ MOE_DEV void epilogue_tile(const GemmArgs &g, const OutView &vO, const OutView &
 // NV (NVFP4 operands): the accumulator is multiplied by `sc` (the inverse of
 // the operands' second-level scales) first, and the SwiGLU epilogue writes h
 // as NVFP4 (store and SwiGLU epilogues only).
-template <int EPI, int BN, bool DUMP = false, bool NV = false, typename Release>
+template <int EPI, int BN, bool DUMP = false, bool NV = false, bool STASH = false, typename Release>
 MOE_DEV void epilogue_tile_split(const GemmArgs &g, const OutView &vO, const OutView &vO2,
                                  const OutView &vQ, Stager &st, uint32_t tb, int nk, int row0,
                                  long grow, int out_col, int lane, int part, bool store,
-                                 Release release, float sc = 1.0f) {
+                                 Release release, float sc = 1.0f, uint32_t ts = 0) {
   if constexpr (EPI == EPI_STORE) {
     constexpr int NC = BN / 2;  // accumulator columns of this warp
     constexpr int NC32 = NC / 32;
@@ -391,17 +391,37 @@ MOE_DEV void epilogue_tile_split(const GemmArgs &g, const OutView &vO, const Out
     }
   } else if constexpr (EPI == EPI_SWIGLU_BWD) {
     // This warp's BN/2 dh columns, 64 at a time: each chunk is read from TMEM,
-    // then processed; TMEM is released once the last chunk has been read.
+    // then processed.  Without STASH, TMEM is released once the last chunk has
+    // been read.  With STASH (one accumulator), chunks 1.. are first copied into
+    // spare TMEM columns at ts (this warp's lane quarter; 64 (NCH - 1) columns
+    // per column half), so the accumulator is released after the reads instead
+    // of after chunk 0's processing, and the next tile's MMAs overlap it.
     constexpr int NCH = BN / 128;
+    const uint32_t stash = ts + static_cast<uint32_t>(part * 64 * (NCH - 1));
+    if constexpr (STASH) {
+#pragma unroll 1
+      for (int ch = 1; ch < NCH; ++ch) {
+        const int dc = part * (BN / 2) + 64 * ch;
+        uint32_t t[64];
+        tmem_ld32_async(tb + dc, t);
+        tmem_ld32_async(tb + dc + 32, t + 32);
+        tmem_ld_wait();
+        reg_fence<64>(t);
+        tmem_st32(stash + 64 * (ch - 1), t);
+        tmem_st32(stash + 64 * (ch - 1) + 32, t + 32);
+      }
+      tmem_st_wait();
+    }
 #pragma unroll 1
     for (int ch = 0; ch < NCH; ++ch) {
       const int dc = part * (BN / 2) + 64 * ch;  // accumulator column of this chunk
+      const uint32_t src = (STASH && ch > 0) ? stash + 64 * (ch - 1) : tb + dc;
       uint32_t hr[64];
-      tmem_ld32_async(tb + dc, hr);
-      tmem_ld32_async(tb + dc + 32, hr + 32);
+      tmem_ld32_async(src, hr);
+      tmem_ld32_async(src + 32, hr + 32);
       tmem_ld_wait();
       reg_fence<64>(hr);
-      if (ch == NCH - 1) release();
+      if (ch == (STASH ? 0 : NCH - 1)) release();
       if (!store) continue;
       const float *dh = reinterpret_cast<const float *>(hr);
       const int col = out_col + dc;
