@@ -311,8 +311,6 @@ __global__ void __launch_bounds__(192, 1)
     const OutView vO = out_view(g.out, g.ldo, g.out_rows, 2);
     const OutView vO2 = out_view(g.out2, g.ldo2, g.out_rows, 2);
     const OutView vQ = out_view(g.outq, g.ldq, g.out_rows, 1);
-    if (lane == 0) {
-    }
     int acc = 0;
     uint32_t aph = 0;
     for (int u = cluster_id; u < total; u += num_clusters) {
