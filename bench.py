@@ -47,7 +47,6 @@ NCU_TRAFFIC = {
     ("kimi-k2.7", "wgrad_down"): (819_456 + 4_397_618_944) + (1_653_164_800 + 6_752_859_904),
     ("kimi-k2.7", "gemm1_gate_up_swiglu"): 8_762_271_744 + 1_974_972_416,
     ("kimi-k2.7", "dgrad_gate_up"): 7_788_438_016 + 2_209_938_688,
-    ("kimi-k2.7", "dgrad_down_swiglu_bwd"): 6_789_948_160 + 1_518_551_552,
     ("kimi-k2.7", "gemm2_down"): 3_840_576_256 + 2_204_741_632,
     ("deepseek-v4-pro", "gemm1_gate_up_swiglu"): 23_420_308_992 + 679_740_928,
     ("deepseek-v4-pro", "gemm2_down"): 9_990_749_440 + 2_930_241_792,
@@ -460,6 +459,29 @@ def oracle_sample(cfg, passes, x_dev, logits_dev, dy_dev, n_tok):
                 need=need, masters=masters, shared=shared, passes=passes)
 
 
+def oracle_dw_sample(cfg, layer, x_dev, dy_dev, n=4, max_rows=2048):
+    """Host copies for the oracle's weight gradients of n seeded experts over all
+    their rows (experts with 1..max_rows rows, so the sample stays within
+    seconds): each expert's tokens, combine weights and masters, from the
+    layer's routing of the bench's own inputs."""
+    import numpy as np
+    import moe_inputs as mi
+    T, k, E = cfg["T"], cfg["k"], cfg["E"]
+    counts = layer.view(0, "counts", "i32", (E,)).cpu().numpy()
+    idx = layer.view(0, "idx", "i32", (T, k)).cpu().numpy().reshape(-1)
+    w = layer.view(0, "w", "f32", (T, k)).cpu().numpy().reshape(-1).astype(np.float64)
+    rows, masters = {}, {}
+    for e in mi.sample_experts(counts, cfg["seed"], n=n, max_rows=max_rows):
+        e = int(e)
+        slots = np.nonzero(idx == e)[0]
+        toks = slots // k
+        t_dev = __import__("torch").as_tensor(toks, device=x_dev.device)
+        rows[e] = (mi.to_f64(x_dev[t_dev]), mi.to_f64(dy_dev[t_dev]), w[slots])
+        gu, dn = mi.expert(cfg, e, device=x_dev.device)
+        masters[e] = (gu.float().cpu().numpy(), dn.float().cpu().numpy())
+    return dict(rows=rows, masters=masters, passes="fwdbwd", need=sorted(rows))
+
+
 def oracle_prepare(cfg, sample):
     """Weight preparation (S0) of the sample's experts by the oracle, in parallel
     (the masters themselves are not kept: with prepared operands the oracle
@@ -767,6 +789,7 @@ def run_ours(args, cfg, passes):
     if st != 0:
         raise RuntimeError("device status %d after warm-up" % st)
     cfg["E_active"] = experts_with_rows(layer, 0 if bwd else 1)
+    dw_sample = oracle_dw_sample(cfg, layer, x, dy) if (want_cpu and bwd) else None
 
     def timed(fn, K, trace=False):
         return timed_region(stream, fn, K, trace)
@@ -937,14 +960,15 @@ def run_ours(args, cfg, passes):
         "mxfp8_peak_probe": mxp,
     }
     if want_cpu:
-        out["cpu_baseline"] = cpu_baseline(cfg, passes, sample, sample256, n_tok)
+        out["cpu_baseline"] = cpu_baseline(cfg, passes, sample, sample256, n_tok, dw_sample)
     return out, P
 
 
-def cpu_baseline(cfg, passes, sample, sample256, n_tok):
+def cpu_baseline(cfg, passes, sample, sample256, n_tok, dw_sample=None):
     """The oracle as it stands on the host cores: the bounded n_tok-token step
     (the bench's metric, repeated to about 10 s) with BLAS on all cores and
-    again on one thread, and the 256-token seeded forward subset once."""
+    again on one thread, the 256-token seeded forward subset once, and (fwd+bwd)
+    the weight gradients of 4 seeded experts over all their rows once."""
     cores = os.cpu_count()
 
     def repeat(experts):
@@ -980,6 +1004,23 @@ def cpu_baseline(cfg, passes, sample, sample256, n_tok):
         res["fwd_256"] = {"value": round(256 / dt, 4), "unit": "tokens/s (forward)", "cores": cores,
                           "seconds": round(dt, 2), "s0_seconds": round(prep256, 2),
                           "sample": oracle_sample_desc(cfg, "fwd", 256, len(sample256["need"])) + "; run once"}
+    if dw_sample is not None and dw_sample["rows"]:
+        from oracle import moe as om
+        rows = dw_sample["rows"]
+        exw, prepw = oracle_prepare(cfg, dw_sample)
+        t0 = time.perf_counter()
+        for e, (X, dY, w) in rows.items():
+            W_gu, W_dn, ops = exw[e]
+            fw = om.expert_forward(X, W_gu, W_dn, cfg["fmt"], ops)
+            dO = om._rnd(cfg["fmt"])(w[:, None] * dY)
+            om.expert_backward(dO, X, fw["GU_saved"], fw["h_saved"], W_gu, W_dn, cfg["fmt"], ops)
+        dt = time.perf_counter() - t0
+        n_rows = int(sum(r[0].shape[0] for r in rows.values()))
+        res["dw_experts"] = {"value": round(n_rows / dt, 2), "unit": "expert rows/s (forward + backward with dW)",
+                             "cores": cores, "seconds": round(dt, 2), "s0_seconds": round(prepw, 2),
+                             "sample": "%d seeded experts (%s) over all their rows (%d rows; experts with 1..2048 "
+                                       "rows), float64 NumPy, run once"
+                                       % (len(rows), ", ".join(str(e) for e in rows), n_rows)}
     return res
 
 

@@ -179,3 +179,36 @@ def test_clock_sampler_against_a_fake_nvidia_smi(tmp_path, monkeypatch):
     assert rec["sm_mhz"] == 1980.0 and rec["sm_max_mhz"] == 2070.0
     assert rec["reasons"] == ["sw_power_cap"] and rec["samples"] >= 1
     assert not bench.clocks_rejected(rec)
+
+
+def test_dw_sample_takes_every_row_of_seeded_small_experts():
+    """The CPU baseline's weight-gradient leg: 4 seeded experts with 1..max_rows
+    rows, each with exactly the tokens and combine weights routed to it."""
+    import numpy as np
+    import torch
+
+    T, k, E = 64, 2, 8
+    rng = np.random.default_rng(5)
+    idx = np.stack([rng.choice(E, size=k, replace=False) for _ in range(T)]).astype(np.int32)
+    idx[:, 0] = np.where(np.arange(T) < 40, 0, idx[:, 0])    # expert 0 gets many rows
+    idx[:, 1] = np.where(idx[:, 1] == idx[:, 0], (idx[:, 0] + 1) % E, idx[:, 1])
+    w = rng.random((T, k)).astype(np.float32)
+    counts = np.bincount(idx.reshape(-1), minlength=E).astype(np.int32)
+
+    class FakeLayer:
+        def view(self, which, name, dtype, shape):
+            assert which == 0
+            return torch.as_tensor({"counts": counts, "idx": idx, "w": w}[name]).reshape(shape)
+
+    cfg = dict(T=T, d=64, m=32, E=E, k=k, m_shared=0, fmt="bf16", bias="none", seed=9, backward=True)
+    x = torch.randn(T, cfg["d"]).to(torch.bfloat16)
+    dy = torch.randn(T, cfg["d"]).to(torch.bfloat16)
+    s = bench.oracle_dw_sample(cfg, FakeLayer(), x, dy, n=4, max_rows=30)
+    assert len(s["rows"]) == 4 and 0 not in s["rows"]          # expert 0 (40+ rows) is over the cap
+    for e, (X, dY, we) in s["rows"].items():
+        slots = np.nonzero(idx.reshape(-1) == e)[0]
+        assert 1 <= slots.size <= 30 and X.shape == (slots.size, cfg["d"])
+        assert np.array_equal(X, x[slots // k].float().numpy().astype(np.float64))
+        assert np.array_equal(dY, dy[slots // k].float().numpy().astype(np.float64))
+        assert np.array_equal(we, w.reshape(-1)[slots].astype(np.float64))
+        assert s["masters"][e][0].shape == (2 * cfg["m"], cfg["d"])
