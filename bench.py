@@ -1005,23 +1005,31 @@ def cpu_baseline(cfg, passes, sample, sample256, n_tok, dw_sample=None):
                           "seconds": round(dt, 2), "s0_seconds": round(prep256, 2),
                           "sample": oracle_sample_desc(cfg, "fwd", 256, len(sample256["need"])) + "; run once"}
     if dw_sample is not None and dw_sample["rows"]:
-        from oracle import moe as om
-        rows = dw_sample["rows"]
-        exw, prepw = oracle_prepare(cfg, dw_sample)
-        t0 = time.perf_counter()
-        for e, (X, dY, w) in rows.items():
-            W_gu, W_dn, ops = exw[e]
-            fw = om.expert_forward(X, W_gu, W_dn, cfg["fmt"], ops)
-            dO = om._rnd(cfg["fmt"])(w[:, None] * dY)
-            om.expert_backward(dO, X, fw["GU_saved"], fw["h_saved"], W_gu, W_dn, cfg["fmt"], ops)
-        dt = time.perf_counter() - t0
-        n_rows = int(sum(r[0].shape[0] for r in rows.values()))
-        res["dw_experts"] = {"value": round(n_rows / dt, 2), "unit": "expert rows/s (forward + backward with dW)",
-                             "cores": cores, "seconds": round(dt, 2), "s0_seconds": round(prepw, 2),
-                             "sample": "%d seeded experts (%s) over all their rows (%d rows; experts with 1..2048 "
-                                       "rows), float64 NumPy, run once"
-                                       % (len(rows), ", ".join(str(e) for e in rows), n_rows)}
+        try:
+            res["dw_experts"] = oracle_dw_time(cfg, dw_sample, cores)
+        except Exception as exc:  # a reported baseline only: never lose the line over it
+            res["dw_experts"] = {"unavailable": "%s: %s" % (type(exc).__name__, str(exc)[:160])}
     return res
+
+
+def oracle_dw_time(cfg, dw_sample, cores):
+    """The oracle's expert forward + backward (with dW) over every row of the
+    sampled experts, once, after its own S0 for them."""
+    from oracle import moe as om
+    rows = dw_sample["rows"]
+    exw, prepw = oracle_prepare(cfg, dw_sample)
+    t0 = time.perf_counter()
+    for e, (X, dY, w) in rows.items():
+        W_gu, W_dn, ops = exw[e]
+        fw = om.expert_forward(X, W_gu, W_dn, cfg["fmt"], ops)
+        dO = om._rnd(cfg["fmt"])(w[:, None] * dY)
+        om.expert_backward(dO, X, fw["GU_saved"], fw["h_saved"], W_gu, W_dn, cfg["fmt"], ops)
+    dt = time.perf_counter() - t0
+    n_rows = int(sum(r[0].shape[0] for r in rows.values()))
+    return {"value": round(n_rows / dt, 2), "unit": "expert rows/s (forward + backward with dW)",
+            "cores": cores, "seconds": round(dt, 2), "s0_seconds": round(prepw, 2),
+            "sample": "%d seeded experts (%s) over all their rows (%d rows; experts with 1..2048 rows), "
+                      "float64 NumPy, run once" % (len(rows), ", ".join(str(e) for e in rows), n_rows)}
 
 
 def run_reference(args, cfg, passes):
