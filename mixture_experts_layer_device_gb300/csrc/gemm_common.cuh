@@ -79,14 +79,24 @@ struct Stager {
           make_uint4(w16[4 * j], w16[4 * j + 1], w16[4 * j + 2], w16[4 * j + 3]);
     }
     __syncwarp();
+    // Lane (j = lane % 4, rr = lane / 4) moves 16-byte chunk j of rows rr,
+    // rr + 8, rr + 16, rr + 24.  The swizzle term (row / 2) % 4 is the same for
+    // the four rows, so the shared-memory reads are one base plus 512 i, and
+    // the global rows one pointer plus 8 i rows.
     const int j = lane & 3;
-    uint8_t *colp = o.p + static_cast<long>(c0) * o.esz + j * 16;
+    const int rr = lane >> 2;
+    const uint8_t *src = buf + rr * 64 + ((j ^ ((rr >> 1) & 3)) * 16);
+    uint8_t *dst = o.p + static_cast<long>(c0) * o.esz + j * 16 + (static_cast<long>(row0) + rr) * o.ld;
+    const long step = 8 * o.ld;
+    if (static_cast<long>(row0) + 32 <= o.rows) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int r = 8 * i + (lane >> 2);
-      const uint4 v = *reinterpret_cast<const uint4 *>(buf + r * 64 + ((j ^ ((r >> 1) & 3)) * 16));
-      const long row = static_cast<long>(row0) + r;
-      if (row < o.rows) *reinterpret_cast<uint4 *>(colp + row * o.ld) = v;
+      for (int i = 0; i < 4; ++i)
+        *reinterpret_cast<uint4 *>(dst + i * step) = *reinterpret_cast<const uint4 *>(src + 512 * i);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        if (static_cast<long>(row0) + rr + 8 * i < o.rows)
+          *reinterpret_cast<uint4 *>(dst + i * step) = *reinterpret_cast<const uint4 *>(src + 512 * i);
     }
   }
   MOE_DEV void put_bf16(const OutView &o, const float *v32, int c0, int row0, int lane) {
@@ -111,12 +121,16 @@ struct Stager {
           make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
     }
     __syncwarp();
+    // Row r's chunk for this lane's column is (lane / 8) XOR ((r / 2) % 4): four
+    // per-lane bases, one per value of (r / 2) % 4, plus r * 64 (an immediate).
+    const uint8_t *base[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) base[c] = buf + (((lane >> 3) ^ c) * 16) + (lane & 7) * 2;
     float v[32];
     float am = 0.f;
 #pragma unroll
     for (int r = 0; r < 32; ++r) {
-      const uint16_t b = *reinterpret_cast<const uint16_t *>(
-          buf + r * 64 + (((lane >> 3) ^ ((r >> 1) & 3)) * 16) + (lane & 7) * 2);
+      const uint16_t b = *reinterpret_cast<const uint16_t *>(base[(r >> 1) & 3] + r * 64);
       v[r] = __uint_as_float(static_cast<uint32_t>(b) << 16);
       am = fmaxf(am, fabsf(v[r]));
     }
