@@ -24,6 +24,17 @@ namespace {
 // One warp per token.  Top-k by repeated warp argmax under the total order
 // (logit descending, index ascending); weights = softmax over the k chosen
 // logits, summed in slot order.
+
+// An unsigned key that orders like the fp32 value (a > b exactly when key(a) >
+// key(b)); -0 is first made +0, so equal values get equal keys.
+MOE_DEV uint32_t order_key(float v) {
+  const uint32_t u = __float_as_uint(v + 0.0f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+MOE_DEV float key_value(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
 template <int VPL>
 __global__ void __launch_bounds__(256) route_topk_kernel(const float *__restrict__ logits, int T,
                                                          int E, int k, int *__restrict__ idx,
@@ -53,15 +64,11 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float *__restrict
         be = e;
       }
     }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-      const int oe = __shfl_xor_sync(0xffffffffu, be, off);
-      if (ov > bv || (ov == bv && oe < be)) {
-        bv = ov;
-        be = oe;
-      }
-    }
+    // warp argmax: the largest key, then the smallest expert among the lanes holding it
+    const uint32_t kv = order_key(bv);
+    const uint32_t km = __reduce_max_sync(0xffffffffu, kv);
+    be = static_cast<int>(__reduce_min_sync(0xffffffffu, kv == km ? static_cast<uint32_t>(be) : 0xffffffffu));
+    bv = key_value(km);
     if ((be & 31) == lane) taken |= 1u << (be >> 5);
     if (lane == j) {
       my_e = be;
@@ -137,7 +144,21 @@ __global__ void __launch_bounds__(1024) sched_scan_kernel(int *__restrict__ hist
   const int e = threadIdx.x;
   int total = 0;
   if (e < E) {
-    for (int c = 0; c < nchunks; ++c) {
+    // 8 chunks' counts are loaded before any is replaced by its running
+    // prefix, so the loads overlap instead of forming one chain per expert.
+    constexpr int U = 8;
+    int c = 0;
+    for (; c + U <= nchunks; c += U) {
+      int v[U];
+#pragma unroll
+      for (int j = 0; j < U; ++j) v[j] = hist[static_cast<size_t>(c + j) * E + e];
+#pragma unroll
+      for (int j = 0; j < U; ++j) {
+        hist[static_cast<size_t>(c + j) * E + e] = total;
+        total += v[j];
+      }
+    }
+    for (; c < nchunks; ++c) {
       const size_t p = static_cast<size_t>(c) * E + e;
       const int v = hist[p];
       hist[p] = total;

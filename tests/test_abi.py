@@ -262,7 +262,12 @@ def test_product_path_never_reaches_the_oracle():
                 if isinstance(node, ast.Import) and any(a.name.split(".")[0] == "oracle" for a in node.names):
                     users.add(fn.name)
     assert users <= {"_prep_worker", "oracle_sample", "oracle_prepare", "oracle_step", "run_reference",
-                     "cpu_baseline"}, users
+                     "cpu_baseline", "oracle_dw_time"}, users
+    # the CPU baseline's helper is called from the CPU baseline only
+    callers = {fn.name for fn in ast.walk(tree) if isinstance(fn, ast.FunctionDef)
+               for node in ast.walk(fn) if isinstance(node, ast.Call)
+               and getattr(node.func, "id", None) == "oracle_dw_time"}
+    assert callers <= {"cpu_baseline"}, callers
     top = [n for n in tree.body if isinstance(n, (ast.Import, ast.ImportFrom))]
     assert not any("oracle" in ast.dump(n) for n in top)
 
