@@ -2,8 +2,9 @@
 oracle, in both expert formats: one token (most experts empty), every expert
 selected (k = E), every token on the same two experts (one expert spans
 several 128-row tiles, all others are empty: the wgrads write all-zero tiles),
-and ragged token counts.  Gradients are prefilled with NaN so that an element
-the backward never writes fails the comparison."""
+ragged token counts, and a thousand experts (a large grouped-GEMM schedule,
+most experts with zero to two rows).  Gradients are prefilled with NaN so
+that an element the backward never writes fails the comparison."""
 import numpy as np
 import pytest
 import torch
@@ -19,6 +20,7 @@ SHAPES = {
     "k-equals-E": dict(T=37, d=256, m=128, E=5, k=5),
     "all-on-two": dict(T=300, d=256, m=128, E=16, k=2, skew=True),
     "ragged": dict(T=129, d=512, m=256, E=12, k=3),
+    "many-experts": dict(T=200, d=256, m=128, E=1000, k=4),
 }
 
 
