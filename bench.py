@@ -43,12 +43,12 @@ NOMINAL = {"hbm_gbs": 7900.0, "bf16_tflops": 2250.0, "mx_tflops": 4500.0, "nv_tf
 NCU_TRAFFIC = {
     # full-size launches of the timed step, one-pass capture of dram__bytes_read.sum and
     # dram__bytes_write.sum; the gate/up wgrad is the empty experts' zero fill plus the GEMM
-    ("kimi-k2.7", "wgrad_gate_up"): (172_032 + 8_860_254_720) + (4_811_769_856 + 13_564_649_984),
-    ("kimi-k2.7", "wgrad_down"): (84_992 + 4_397_528_064) + (1_668_838_912 + 6_753_302_784),
-    ("kimi-k2.7", "gemm1_gate_up_swiglu"): 8_463_569_664 + 1_944_475_904,
-    ("kimi-k2.7", "dgrad_gate_up"): 7_734_252_544 + 2_209_944_832,
-    ("kimi-k2.7", "dgrad_down_swiglu_bwd"): 7_854_705_664 + 1_722_646_272,
-    ("kimi-k2.7", "gemm2_down"): 3_839_731_968 + 2_204_543_232,
+    ("kimi-k2.7", "wgrad_gate_up"): (129_536 + 8_860_143_616) + (4_777_004_032 + 13_564_823_552),
+    ("kimi-k2.7", "wgrad_down"): (103_168 + 4_397_457_920) + (1_658_128_640 + 6_752_918_272),
+    ("kimi-k2.7", "gemm1_gate_up_swiglu"): 8_806_697_984 + 1_949_560_832,
+    ("kimi-k2.7", "dgrad_gate_up"): 7_719_481_088 + 2_210_394_624,
+    ("kimi-k2.7", "dgrad_down_swiglu_bwd"): 6_870_545_920 + 1_586_176_256,
+    ("kimi-k2.7", "gemm2_down"): 3_839_812_864 + 2_203_856_128,
     ("deepseek-v4-pro", "gemm1_gate_up_swiglu"): 23_659_604_736 + 707_164_672,
     ("deepseek-v4-pro", "gemm2_down"): 9_965_006_592 + 2_929_535_232,
 }
