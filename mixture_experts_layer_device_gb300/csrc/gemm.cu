@@ -75,10 +75,11 @@ struct Cfg {
   static constexpr int SFA_COLS = 4 * SF_ATOMS;
   static constexpr int SF_COLS = SF_ATOMS * (4 + BN / 32);
   static constexpr int SF_COL0 = NUM_ACC * BN;
-  // The SwiGLU-backward epilogue's stash of accumulator chunks 1.. (one
-  // accumulator only): the last 64 (BN / 128 - 1) x 2 columns of TMEM.
+  // The SwiGLU-backward epilogue's stash (one accumulator only): every
+  // 32-column piece of the accumulator but each warp's first, the last
+  // 2 x 32 (BN / 64 - 1) columns of TMEM.
   static constexpr bool STASH = !NV && NUM_ACC == 1 && BN / 128 > 1;  // NVFP4 has no backward
-  static constexpr int STASH_COL = 512 - 2 * 64 * (BN / 128 - 1);
+  static constexpr int STASH_COL = 512 - 2 * 32 * (BN / 64 - 1);
   static constexpr uint32_t TX_BYTES = STAGE_BYTES + SF_STAGE;
   static constexpr uint32_t IDESC = NV ? idesc_nvf4(128, BN) : (MX ? idesc_mxf8(128, BN) : idesc_bf16(128, BN));
   // epilogue staging: 2 KB pieces (32 rows x 64 B, 64-byte swizzle), 16 KB split

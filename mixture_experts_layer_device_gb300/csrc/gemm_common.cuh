@@ -319,10 +319,60 @@ MOE_DEV void epilogue_tile(const GemmArgs &g, const OutView &vO, const OutView &
   }
 }
 
+// SwiGLU backward of 32 dh columns of this lane's row (from column col of
+// the tile's output): dG, dU from the saved bf16 G|U (read through aux),
+// rounded to bf16; stores the bf16 values (g.out) and the column-blocked codes
+// of dGU^T (g.outT), and returns the row-blocked MX codes of this block in
+// cg[0..8) / cu[0..8) with their scale bytes.
+MOE_DEV void swiglu_bwd32(const GemmArgs &g, const OutView &vO, Stager &st, const float *dh, int col, int row0,
+                          long grow, int lane, uint32_t *cg, uint32_t *cu, uint32_t &sg, uint32_t &su) {
+  float G[32], U[32];
+  load_bf16x32(g.aux, grow, g.ld_aux, col, G);
+  load_bf16x32(g.aux, grow, g.ld_aux, g.m_half + col, U);
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const float d = dh[i];
+    const float sgm = sigmoidf(G[i]);
+    const float dg = round_bf16(d * U[i] * sgm * (1.0f + G[i] * (1.0f - sgm)));
+    const float du = round_bf16(d * G[i] * sgm);
+    G[i] = dg;
+    U[i] = du;
+  }
+  if (g.out) {
+    st.put_bf16(vO, G, col, row0, lane);
+    st.put_bf16(vO, U, g.m_half + col, row0, lane);
+  }
+  // dG's codes first, then dU's, so that dG's values are dead while dU's
+  // column codes are made (fewer registers live at once).
+  if (g.outq) sg = mx_block_words(G, cg);
+  if (g.outT)  // the gate/up wgrad operand dGU^T, column-blocked, from the bf16 dG, dU
+    st.put_col_codes(G, g.outT, g.outT_sf, g.ldT, col, row0, lane);
+  if (g.outq) su = mx_block_words(U, cu);
+  if (g.outT) st.put_col_codes(U, g.outT, g.outT_sf, g.ldT, g.m_half + col, row0, lane);
+}
+
+// The row-blocked MX codes of 64 dG and 64 dU columns (two blocks each), with
+// their scale bytes, for the gate/up dgrad.
+MOE_DEV void swiglu_bwd_row_codes(const GemmArgs &g, const OutView &vQ, Stager &st, const uint32_t *cg,
+                                  const uint32_t *cu, const uint32_t *sg, const uint32_t *su, int col, int row0,
+                                  long grow, int lane) {
+  if (!g.outq) return;
+  st.put(vQ, cg, col, row0, lane);
+  st.put(vQ, cu, g.m_half + col, row0, lane);
+  *reinterpret_cast<uint16_t *>(g.outq_sf + sf_tiled_offset(grow, col / 32, g.ldq)) =
+      static_cast<uint16_t>(sg[0] | (sg[1] << 8));
+  *reinterpret_cast<uint16_t *>(g.outq_sf + sf_tiled_offset(grow, (g.m_half + col) / 32, g.ldq)) =
+      static_cast<uint16_t>(su[0] | (su[1] << 8));
+}
+
 // Epilogue shared by two warps per TMEM lane quarter: warp `part` (0 or 1)
 // drains half of the tile's columns.  For the store and SwiGLU epilogues the
 // accumulator is read in one round (two warps in parallel) and released before
 // any conversion or store; the SwiGLU backward reads its columns 64 at a time.
+// STASH (one accumulator; SwiGLU backward): each warp keeps its first 32
+// columns in registers, parks the rest in spare TMEM columns at ts, releases
+// the accumulator, and reads the parked columns back 32 at a time, so fewer
+// values are live at once (the 10-warp CTA has 168 registers per thread).
 // DUMP (SwiGLU, a separate instantiation so the normal kernel carries none of
 // its register pressure): also store the fp32 h to g.dump.
 // NV (NVFP4 operands): the accumulator is multiplied by `sc` (the inverse of
@@ -404,77 +454,74 @@ MOE_DEV void epilogue_tile_split(const GemmArgs &g, const OutView &vO, const Out
       }
     }
   } else if constexpr (EPI == EPI_SWIGLU_BWD) {
-    // This warp's BN/2 dh columns, 64 at a time: each chunk is read from TMEM,
-    // then processed.  Without STASH, TMEM is released once the last chunk has
-    // been read.  With STASH (one accumulator), chunks 1.. are first copied into
-    // spare TMEM columns at ts (this warp's lane quarter; 64 (NCH - 1) columns
-    // per column half), so the accumulator is released after the reads instead
-    // of after chunk 0's processing, and the next tile's MMAs overlap it.
+    // This warp's BN/2 dh columns, 64 at a time (two 32-column halves).
+    // Without STASH, each chunk is read from TMEM, then processed, and TMEM is
+    // released once the last chunk has been read.  With STASH (one
+    // accumulator), every 32-column piece but the first is copied into spare
+    // TMEM columns at ts (this warp's lane quarter; BN/2 - 32 columns per
+    // column half) and the accumulator is released, so the next tile's MMAs
+    // overlap the processing; each piece is then read back when it is used,
+    // which keeps 32 dh values in registers instead of 64.
     constexpr int NCH = BN / 128;
-    const uint32_t stash = ts + static_cast<uint32_t>(part * 64 * (NCH - 1));
     if constexpr (STASH) {
+      constexpr int NP = BN / 64;  // 32-column pieces of this warp
+      const uint32_t a0 = tb + static_cast<uint32_t>(part * (BN / 2));
+      const uint32_t stash = ts + static_cast<uint32_t>(part * 32 * (NP - 1));
+      uint32_t h0[32];
+      tmem_ld32_async(a0, h0);
 #pragma unroll 1
-      for (int ch = 1; ch < NCH; ++ch) {
-        const int dc = part * (BN / 2) + 64 * ch;
-        uint32_t t[64];
-        tmem_ld32_async(tb + dc, t);
-        tmem_ld32_async(tb + dc + 32, t + 32);
+      for (int p = 1; p < NP; ++p) {
+        uint32_t t[32];
+        tmem_ld32_async(a0 + 32 * p, t);
         tmem_ld_wait();
-        reg_fence<64>(t);
-        tmem_st32(stash + 64 * (ch - 1), t);
-        tmem_st32(stash + 64 * (ch - 1) + 32, t + 32);
+        reg_fence<32>(t);
+        tmem_st32(stash + 32 * (p - 1), t);
       }
-      tmem_st_wait();
-    }
-#pragma unroll 1
-    for (int ch = 0; ch < NCH; ++ch) {
-      const int dc = part * (BN / 2) + 64 * ch;  // accumulator column of this chunk
-      const uint32_t src = (STASH && ch > 0) ? stash + 64 * (ch - 1) : tb + dc;
-      uint32_t hr[64];
-      tmem_ld32_async(src, hr);
-      tmem_ld32_async(src + 32, hr + 32);
       tmem_ld_wait();
-      reg_fence<64>(hr);
-      if (ch == (STASH ? 0 : NCH - 1)) release();
-      if (!store) continue;
-      const float *dh = reinterpret_cast<const float *>(hr);
-      const int col = out_col + dc;
-      uint32_t cg[16], cu[16];  // MX codes of dG and dU (two blocks each)
-      uint32_t sg[2], su[2];
+      reg_fence<32>(h0);
+      tmem_st_wait();
+      release();
+      if (!store) return;
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        float G[32], U[32];
-        load_bf16x32(g.aux, grow, g.ld_aux, col + 32 * hh, G);
-        load_bf16x32(g.aux, grow, g.ld_aux, g.m_half + col + 32 * hh, U);
+      for (int ch = 0; ch < NCH; ++ch) {
+        const int col = out_col + part * (BN / 2) + 64 * ch;
+        uint32_t cg[16], cu[16];  // MX codes of dG and dU (two blocks each)
+        uint32_t sg[2], su[2];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float d = dh[32 * hh + i];
-          const float sgm = sigmoidf(G[i]);
-          const float dg = round_bf16(d * U[i] * sgm * (1.0f + G[i] * (1.0f - sgm)));
-          const float du = round_bf16(d * G[i] * sgm);
-          G[i] = dg;
-          U[i] = du;
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t hr[32];
+          if (ch == 0 && hh == 0) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) hr[i] = h0[i];
+          } else {
+            tmem_ld32_async(stash + 32 * (2 * ch + hh - 1), hr);
+            tmem_ld_wait();
+            reg_fence<32>(hr);
+          }
+          swiglu_bwd32(g, vO, st, reinterpret_cast<const float *>(hr), col + 32 * hh, row0, grow, lane,
+                       cg + 8 * hh, cu + 8 * hh, sg[hh], su[hh]);
         }
-        if (g.out) {
-          st.put_bf16(vO, G, col + 32 * hh, row0, lane);
-          st.put_bf16(vO, U, g.m_half + col + 32 * hh, row0, lane);
-        }
-        if (g.outT) {  // the gate/up wgrad operand dGU^T, column-blocked, from the bf16 dG, dU
-          st.put_col_codes(G, g.outT, g.outT_sf, g.ldT, col + 32 * hh, row0, lane);
-          st.put_col_codes(U, g.outT, g.outT_sf, g.ldT, g.m_half + col + 32 * hh, row0, lane);
-        }
-        if (g.outq) {
-          sg[hh] = mx_block_words(G, cg + 8 * hh);
-          su[hh] = mx_block_words(U, cu + 8 * hh);
-        }
+        swiglu_bwd_row_codes(g, vQ, st, cg, cu, sg, su, col, row0, grow, lane);
       }
-      if (g.outq) {
-        st.put(vQ, cg, col, row0, lane);
-        st.put(vQ, cu, g.m_half + col, row0, lane);
-        *reinterpret_cast<uint16_t *>(g.outq_sf + sf_tiled_offset(grow, col / 32, g.ldq)) =
-            static_cast<uint16_t>(sg[0] | (sg[1] << 8));
-        *reinterpret_cast<uint16_t *>(g.outq_sf + sf_tiled_offset(grow, (g.m_half + col) / 32, g.ldq)) =
-            static_cast<uint16_t>(su[0] | (su[1] << 8));
+    } else {
+#pragma unroll 1
+      for (int ch = 0; ch < NCH; ++ch) {
+        const int dc = part * (BN / 2) + 64 * ch;  // accumulator column of this chunk
+        uint32_t hr[64];
+        tmem_ld32_async(tb + dc, hr);
+        tmem_ld32_async(tb + dc + 32, hr + 32);
+        tmem_ld_wait();
+        reg_fence<64>(hr);
+        if (ch == NCH - 1) release();
+        if (!store) continue;
+        const int col = out_col + dc;
+        uint32_t cg[16], cu[16];
+        uint32_t sg[2], su[2];
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh)
+          swiglu_bwd32(g, vO, st, reinterpret_cast<const float *>(hr) + 32 * hh, col + 32 * hh, row0, grow, lane,
+                       cg + 8 * hh, cu + 8 * hh, sg[hh], su[hh]);
+        swiglu_bwd_row_codes(g, vQ, st, cg, cu, sg, su, col, row0, grow, lane);
       }
     }
   } else {  // EPI_SWIGLU: accumulator [0,128) = G, [128,256) = U; this warp: 64 h columns
