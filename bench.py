@@ -47,7 +47,6 @@ NCU_TRAFFIC = {
     ("kimi-k2.7", "wgrad_down"): (103_168 + 4_397_457_920) + (1_658_128_640 + 6_752_918_272),
     ("kimi-k2.7", "gemm1_gate_up_swiglu"): 8_806_697_984 + 1_949_560_832,
     ("kimi-k2.7", "dgrad_gate_up"): 7_719_481_088 + 2_210_394_624,
-    ("kimi-k2.7", "dgrad_down_swiglu_bwd"): 6_870_545_920 + 1_586_176_256,
     ("kimi-k2.7", "gemm2_down"): 3_839_812_864 + 2_203_856_128,
     ("deepseek-v4-pro", "gemm1_gate_up_swiglu"): 23_659_604_736 + 707_164_672,
     ("deepseek-v4-pro", "gemm2_down"): 9_965_006_592 + 2_929_535_232,
